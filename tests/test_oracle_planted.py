@@ -1,0 +1,85 @@
+"""Plant plausible mistakes in the oracle (CPU only) and check that the pins
+catch each of them.  Every plant is undone by monkeypatch after its test."""
+import numpy as np
+import pytest
+
+from oracle import ttt_ref as O
+import test_oracle_pins as P
+
+
+def _fails(fn, *a, **kw):
+    try:
+        fn(*a, **kw)
+    except AssertionError:
+        return True
+    return False
+
+
+def test_wrong_rope_backward_sign_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "rope_bwd", O.rope)
+    assert P.fd_check("tiny-ttt2", 0) > 1e-3
+
+
+def test_dropped_rmsnorm_backward_term_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "rmsnorm_bwd", lambda x, g, r, dy: r * (g * dy))
+    assert P.fd_check("tiny", 0) > 1e-3
+
+
+def test_stale_stash_in_backward_is_caught(monkeypatch):
+    """The backward reads an up-projection that differs from the forward's."""
+    orig = O.backward_chunk
+
+    def bad_backward(st, z, acts, valid, tgt, n_tgt):
+        for l in acts:
+            if l != "final":
+                acts[l] = dict(acts[l], up=acts[l]["up"] * 1.0001 + 1e-3)
+        return orig(st, z, acts, valid, tgt, n_tgt)
+
+    monkeypatch.setattr(O, "backward_chunk", bad_backward)
+    assert P.fd_check("tiny", 0) > 1e-4
+
+
+def test_wrong_kv_head_grouping_is_caught(monkeypatch):
+    """Query head i paired with KV head i % Hkv instead of i // (H/Hkv)."""
+    import math
+
+    def bad_attention(q, kw, vw, qpos, kpos, window, group):
+        head_kv = np.arange(q.shape[1]) % kw.shape[1]
+        kh, vh = kw[:, head_kv, :], vw[:, head_kv, :]
+        S = np.einsum("nhd,mhd->hnm", q, kh) / math.sqrt(q.shape[-1])
+        rel = qpos[:, None] - kpos[None, :]
+        S = np.where(((rel >= 0) & (rel < window))[None], S, -np.inf)
+        E = np.exp(S - S.max(-1, keepdims=True))
+        Pm = E / E.sum(-1, keepdims=True)
+        return np.einsum("hnm,mhd->nhd", Pm, vh), Pm
+
+    monkeypatch.setattr(O, "attention", bad_attention)
+    assert _fails(P.test_forward_matches_torch_library_restatement, "tiny-gqa")
+
+
+def test_window_off_by_one_is_caught(monkeypatch):
+    orig = O.attention
+    monkeypatch.setattr(O, "attention",
+                        lambda q, kw, vw, qp, kp, window, group: orig(q, kw, vw, qp, kp, window + 1, group))
+    assert _fails(P.test_attention_band_matches_sdpa_with_mask)
+
+
+def test_target_shift_is_caught(monkeypatch):
+    def bad_targets(tokens, s, e):
+        T = len(tokens)
+        t = np.arange(s, e)
+        valid = (t + 1) < T
+        return valid, np.where(valid, np.asarray(tokens)[t], 0)
+
+    monkeypatch.setattr(O, "chunk_targets", bad_targets)
+    assert _fails(P.test_lr0_chunked_equals_unchunked, "tiny")
+
+
+def test_update_sign_is_caught(monkeypatch):
+    orig = O.step_chunk
+
+    def bad_step(st, tokens, s, e, lr, update=True, want_grads=False):
+        return orig(st, tokens, s, e, -lr, update, want_grads)
+
+    monkeypatch.setattr(O, "step_chunk", bad_step)
+    assert _fails(P.test_loss_falls_on_repeated_context)
