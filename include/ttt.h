@@ -1,0 +1,146 @@
+/*
+ * ttt.h — C ABI of the TTT-E2E test-time inner loop on one B300 (sm_103a).
+ *
+ * The method ("End-to-End Test-Time Training for Long Context"): a
+ * decoder-only Transformer with sliding-window attention reads a long
+ * context in mini-batches ("chunks") of b tokens; on each chunk it runs the
+ * forward pass, takes the next-token cross-entropy loss, back-propagates
+ * into the MLPs of the last quarter of the blocks only, and takes one plain
+ * gradient step on them, so the next chunk is read by the updated weights
+ * (summary page, Method; podcast page, 6:36 and 7:08; NVIDIA blog, "Our
+ * method: compressing context into weights").  Keys and values of earlier
+ * chunks stay cached and are not differentiated.  The meta-learned outer
+ * loop is not part of this library.
+ *
+ * Conventions for every call:
+ *   - Return value: TTT_OK (0) or a negative TTT_ERR_* code.  Nothing aborts
+ *     and no C++ exception crosses this boundary.  ttt_last_error() returns
+ *     a NUL-terminated description of the last failure on that context
+ *     (owned by the context, valid until the next call on it).
+ *   - Matrices use the [out, in] row-major layout of a linear layer
+ *     (y = x W^T): wq [H*hd, d], wk/wv [Hkv*hd, d], wo [d, H*hd],
+ *     w_gate/w_up [d_ff, d], w_down [d, d_ff], tok_embed/lm_head [vocab, d].
+ *     Embeddings are untied.  Norm gains are [d].
+ *   - Pointers may be host memory or device memory of the current device;
+ *     the library tells them apart with cudaPointerGetAttributes and copies
+ *     host data itself.  The library never keeps a caller pointer after a
+ *     call returns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All device
+ *     work of a call is issued on it.
+ */
+#ifndef TTT_H_
+#define TTT_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  TTT_OK = 0,
+  TTT_ERR_INVALID = -1,   /* null pointer, bad enum, bad config value          */
+  TTT_ERR_SHAPE = -2,     /* sizes the kernels do not support                  */
+  TTT_ERR_OOM = -3,       /* device allocation failed                          */
+  TTT_ERR_CUDA = -4,      /* a CUDA runtime/driver call failed                 */
+  TTT_ERR_NONFINITE = -5, /* a chunk loss was NaN/Inf (chunk index in message) */
+  TTT_ERR_STATE = -6,     /* call not allowed in the context's current state   */
+  TTT_ERR_INTERNAL = -7   /* a device-side check or bounded wait failed        */
+};
+
+enum {
+  TTT_BF16 = 0,       /* bf16 storage, fp32 accumulation, tensor cores          */
+  TTT_FP32_CHECK = 1  /* fp32 everywhere, SIMT kernels (correctness mode)        */
+};
+
+/* Model and loop configuration.
+ *   n_layers L, d_model d, n_heads H, n_kv_heads Hkv (H % Hkv == 0),
+ *   head_dim hd (even), d_ff, vocab V, window W (query t sees keys j with
+ *   t-W < j <= t), chunk b (test-time mini-batch), n_ttt_layers (the MLPs
+ *   of blocks [L-n_ttt_layers, L) are the fast weights), precision
+ *   (TTT_BF16 | TTT_FP32_CHECK), lr (SGD step), rope_theta, norm_eps,
+ *   max_tokens (longest sequence ttt_prefill will be given; sizes the
+ *   device staging of host token arrays).                                   */
+typedef struct ttt_config {
+  int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, d_ff, vocab;
+  int32_t window, chunk, n_ttt_layers, precision;
+  float lr, rope_theta, norm_eps;
+  int64_t max_tokens;
+} ttt_config;
+
+/* Initial weights, fp32 values (host or device).  Per-layer fields are
+ * arrays of n_layers pointers (the arrays themselves live in host memory). */
+typedef struct ttt_weights {
+  const float* tok_embed;  /* [V, d] */
+  const float* final_norm; /* [d]    */
+  const float* lm_head;    /* [V, d] */
+  const float* const* attn_norm; /* [d]        */
+  const float* const* wq;        /* [H*hd, d]  */
+  const float* const* wk;        /* [Hkv*hd, d]*/
+  const float* const* wv;        /* [Hkv*hd, d]*/
+  const float* const* wo;        /* [d, H*hd]  */
+  const float* const* mlp_norm;  /* [d]        */
+  const float* const* w_gate;    /* [d_ff, d]  */
+  const float* const* w_up;      /* [d_ff, d]  */
+  const float* const* w_down;    /* [d, d_ff]  */
+} ttt_weights;
+
+typedef struct ttt_ctx ttt_ctx;
+
+/* Validate `cfg`, allocate all device state (weights in the working
+ * precision, fp32 masters of the fast weights, the key/value ring of
+ * W+b-1 positions per layer, per-chunk activations), copy and convert the
+ * weights (bf16 by round-to-nearest-even in TTT_BF16 mode), and return the
+ * context in *out.  The context is fresh: position 0, initial fast weights.
+ * Errors: INVALID (null args, bad enum), SHAPE (unsupported sizes), OOM,
+ * CUDA.  On error *out is NULL and nothing is leaked. */
+int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* stream, ttt_ctx** out);
+
+/* The test-time inner loop over tokens[0..T) (int32 ids in [0, V)).
+ * Chunk c covers positions [c*b, min(T,(c+1)*b)); the target of position t
+ * is tokens[t+1] when t+1 < T.  For each chunk: forward with the current
+ * weights, loss = mean over the chunk's targets of (logsumexp(z_t) -
+ * z_t[target]), backward into w_gate/w_up/w_down of the fast blocks with
+ * earlier keys/values held constant, then W <- W - lr * dW (fp32 master;
+ * the bf16 copy is re-rounded).  A chunk without targets reports loss 0 and
+ * makes no update.
+ *   chunk_losses: [ceil(T/b)] fp32, host or device.
+ * Requires a fresh (or reset) context and 1 <= T <= cfg.max_tokens;
+ * otherwise STATE / SHAPE.  Returns after the work has completed on
+ * `stream`.  A NaN/Inf chunk loss returns NONFINITE with the first such
+ * chunk index in ttt_last_error(); the context is then left as is.  After
+ * success the context holds the final fast weights and the ring at
+ * position T. */
+int ttt_prefill(ttt_ctx* ctx, const int32_t* tokens, int64_t T, float* chunk_losses,
+                void* stream);
+
+/* Forward only: logits of a continuation cont[0..n) placed at positions
+ * P..P+n-1, where P is the number of positions consumed so far, using the
+ * current fast weights and the cached keys/values.  1 <= n <= cfg.chunk.
+ *   logits: [n, V] fp32 row-major, host or device.
+ * The context's weights, position and visible cache are unchanged (ring
+ * slots beyond position P may be overwritten; they are outside every later
+ * query's window). */
+int ttt_logits(ttt_ctx* ctx, const int32_t* cont, int32_t n, float* logits, void* stream);
+
+/* Copy the current fp32 value of one fast weight:
+ *   block in [0, n_ttt_layers) (0 = layer L-n_ttt_layers),
+ *   which 0 = w_gate [d_ff, d], 1 = w_up [d_ff, d], 2 = w_down [d, d_ff],
+ *   dst host or device, in the [out, in] layout above. */
+int ttt_get_fast_weights(ttt_ctx* ctx, int32_t block, int32_t which, float* dst, void* stream);
+
+/* Restore the initial fast weights, empty the ring, set position 0.
+ * Synchronous. */
+int ttt_reset(ttt_ctx* ctx);
+
+/* Free everything owned by ctx (NULL is ignored). */
+void ttt_destroy(ttt_ctx* ctx);
+
+/* Description of the last error on ctx ("" if none).  With ctx == NULL:
+ * the last error of a failed ttt_create on this thread. */
+const char* ttt_last_error(const ttt_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TTT_H_ */

@@ -1,0 +1,179 @@
+// common.cuh — shared device helpers of the TTT kernels: element types,
+// the GEMM epilogue descriptor, and the epilogue arithmetic applied to each
+// pair of adjacent accumulator columns.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ttt {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------------------
+// element conversions (round to nearest even for bf16)
+// ---------------------------------------------------------------------------
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<bf16>(bf16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+template <typename T> __device__ __forceinline__ void store2(T* p, float a, float b);
+template <> __device__ __forceinline__ void store2<float>(float* p, float a, float b) {
+  *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+template <> __device__ __forceinline__ void store2<bf16>(bf16* p, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+}
+template <typename T> __device__ __forceinline__ float2 load2(const T* p);
+template <> __device__ __forceinline__ float2 load2<float>(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
+template <> __device__ __forceinline__ float2 load2<bf16>(const bf16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// ---------------------------------------------------------------------------
+// GEMM:  C[m, n] = sum_k A(m, k) * B(n, k)
+//   A(m,k) = a_mn ? A[k*lda + m] : A[m*lda + k]
+//   B(n,k) = b_mn ? B[k*ldb + n] : B[n*ldb + k]
+// The accumulator (fp32) goes through one of the epilogues below; every
+// epilogue works on column pairs (n even, n+1), so N must be even.
+// ---------------------------------------------------------------------------
+enum EpiKind : int {
+  EPI_STORE = 0,      // out[m, n] = acc                      (out fp32 or T)
+  EPI_RESID = 1,      // out[m, n] = resid[m, n] + acc        (fp32)
+  EPI_QKV = 2,        // RoPE on q/k pairs, q -> out, k/v -> key/value ring
+  EPI_SWIGLU = 3,     // (g, u) pair -> a = silu(g) u; optional stash of (g, u)
+  EPI_SWIGLU_BWD = 4, // da -> (dg, du) using the stashed (g, u)
+  EPI_SGD = 5,        // w32 -= lr * acc; w16 = rn(w32); w16lo = rn(w32 - w16)
+  EPI_CE_Z = 6,       // z slab (fp32) + pick the target logit
+  EPI_CE_ACC = 7,     // acc_out = acc_out * alpha[m] + acc * beta[m]
+};
+
+struct Epi {
+  int kind;
+  int out_f32;            // EPI_STORE: 1 = fp32 output, 0 = element type T
+  void* out;              // output matrix
+  int64_t ldo;
+  const float* resid;     // EPI_RESID
+  int64_t ldr;
+  // EPI_QKV
+  int n_q, n_kv, hd;      // heads of q, heads of k/v, head dim
+  int64_t pos0;           // absolute position of row 0
+  int ring;               // ring slots R
+  void* kring;            // [n_kv][R][hd]
+  void* vring;
+  const float2* rope_cs;  // [rows][hd/2] (cos, sin) of the rows' positions
+  // EPI_SWIGLU / EPI_SWIGLU_BWD
+  void* stash;            // (g, u) interleaved [rows][2*d_ff]
+  int64_t ld_stash;
+  // EPI_SGD
+  float* w32;
+  void* w16;              // may be null (fp32 mode: w32 is the weight)
+  void* w16lo;            // may be null: low half of the compensated pair
+  float lr;
+  // EPI_CE_Z
+  const int32_t* tgt;     // target id per row (-1: none)
+  float* ztgt;
+  int64_t col0;           // vocab index of column 0
+  // EPI_CE_ACC
+  const float* alpha;
+  const float* beta;
+  int first;              // 1: ignore the old content of out
+};
+
+// Apply the epilogue to columns (n, n+1) of row m.  T is the element type of
+// the activations (float in check mode, bf16 otherwise).
+template <typename T>
+__device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, float v1) {
+  switch (e.kind) {
+    case EPI_STORE: {
+      if (e.out_f32) store2<float>((float*)e.out + (int64_t)m * e.ldo + n, v0, v1);
+      else store2<T>((T*)e.out + (int64_t)m * e.ldo + n, v0, v1);
+    } break;
+    case EPI_RESID: {
+      float2 r = load2<float>(e.resid + (int64_t)m * e.ldr + n);
+      store2<float>((float*)e.out + (int64_t)m * e.ldo + n, r.x + v0, r.y + v1);
+    } break;
+    case EPI_QKV: {
+      const int hd = e.hd;
+      const int qcols = e.n_q * hd;
+      const int kcols = e.n_kv * hd;
+      if (n < qcols + kcols) {
+        const float2 cs = e.rope_cs[(int64_t)m * (hd >> 1) + ((n % hd) >> 1)];
+        const float a = v0 * cs.x - v1 * cs.y;
+        const float b = v1 * cs.x + v0 * cs.y;
+        if (n < qcols) {
+          store2<T>((T*)e.out + (int64_t)m * e.ldo + n, a, b);
+        } else {
+          const int c = n - qcols;
+          const int64_t slot = (e.pos0 + m) % e.ring;
+          store2<T>((T*)e.kring + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd), a, b);
+        }
+      } else {
+        const int c = n - qcols - kcols;
+        const int64_t slot = (e.pos0 + m) % e.ring;
+        store2<T>((T*)e.vring + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd), v0, v1);
+      }
+    } break;
+    case EPI_SWIGLU: {
+      const float a = v0 * sigmoidf_(v0) * v1;
+      ((T*)e.out)[(int64_t)m * e.ldo + (n >> 1)] = from_f<T>(a);
+      if (e.stash) store2<T>((T*)e.stash + (int64_t)m * e.ld_stash + n, v0, v1);
+    } break;
+    case EPI_SWIGLU_BWD: {
+      // columns n, n+1 are d_ff indices f, f+1; outputs go to 2f .. 2f+3
+      const T* st = (const T*)e.stash + (int64_t)m * e.ld_stash + 2 * n;
+      float2 gu0 = load2<T>(st), gu1 = load2<T>(st + 2);
+      float s0 = sigmoidf_(gu0.x), s1 = sigmoidf_(gu1.x);
+      float dg0 = v0 * gu0.y * s0 * (1.0f + gu0.x * (1.0f - s0));
+      float du0 = v0 * gu0.x * s0;
+      float dg1 = v1 * gu1.y * s1 * (1.0f + gu1.x * (1.0f - s1));
+      float du1 = v1 * gu1.x * s1;
+      T* o = (T*)e.out + (int64_t)m * e.ldo + 2 * n;
+      store2<T>(o, dg0, du0);
+      store2<T>(o + 2, dg1, du1);
+    } break;
+    case EPI_SGD: {
+      float* w = e.w32 + (int64_t)m * e.ldo + n;
+      float2 cur = load2<float>(w);
+      cur.x -= e.lr * v0;
+      cur.y -= e.lr * v1;
+      store2<float>(w, cur.x, cur.y);
+      if (e.w16) {
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(cur.x, cur.y);
+        *reinterpret_cast<__nv_bfloat162*>((bf16*)e.w16 + (int64_t)m * e.ldo + n) = hi;
+        if (e.w16lo) {
+          const float2 hf = __bfloat1622float2(hi);
+          store2<bf16>((bf16*)e.w16lo + (int64_t)m * e.ldo + n, cur.x - hf.x, cur.y - hf.y);
+        }
+      }
+    } break;
+    case EPI_CE_Z: {
+      store2<float>((float*)e.out + (int64_t)m * e.ldo + n, v0, v1);
+      const int64_t t = (int64_t)e.tgt[m] - e.col0;
+      if (t == n) e.ztgt[m] = v0;
+      else if (t == n + 1) e.ztgt[m] = v1;
+    } break;
+    case EPI_CE_ACC: {
+      float* o = (float*)e.out + (int64_t)m * e.ldo + n;
+      const float be = e.beta[m];
+      if (e.first) {
+        store2<float>(o, v0 * be, v1 * be);
+      } else {
+        const float al = e.alpha[m];
+        float2 c = load2<float>(o);
+        store2<float>(o, c.x * al + v0 * be, c.y * al + v1 * be);
+      }
+    } break;
+    default: break;
+  }
+}
+
+}  // namespace ttt

@@ -1,0 +1,820 @@
+// engine.cu — the inner loop behind the C ABI of ttt.h.
+//
+// One context owns, on one GPU:
+//   * the weights in the working type T (bf16, or fp32 in check mode), with
+//     q/k rows of every head reordered so that RoPE pairs (i, i+hd/2) become
+//     adjacent columns (2i, 2i+1) — attention only sees q.k products, which
+//     this shared reordering leaves unchanged — and gate/up rows interleaved
+//     (gate f -> row 2f, up f -> row 2f+1) so SwiGLU pairs are adjacent too;
+//   * fp32 masters of the fast weights (the MLPs of the last n_ttt_layers
+//     blocks) and a copy of their initial values for ttt_reset;
+//   * per layer a key/value ring of R >= W+b-1 slots (position p in slot
+//     p mod R), constant in the sequence length;
+//   * the activations of one chunk (all of them for the fast blocks, which
+//     the backward needs; one scratch set for the static blocks).
+// The residual stream, norm statistics, softmax statistics and all
+// gradients that cross kernels in fp32 stay fp32; matrices fed to GEMMs are
+// in T.
+#include <climits>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "../../include/ttt.h"
+#include "kernels.h"
+
+namespace ttt {
+
+static thread_local std::string g_create_error;
+
+// ---------------------------------------------------------------------------
+struct DeviceArena {
+  std::vector<void*> ptrs;
+  size_t total = 0;
+  cudaError_t alloc(void** p, size_t bytes) {
+    *p = nullptr;
+    if (bytes == 0) bytes = 16;
+    bytes = (bytes + 255) & ~size_t(255);
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e == cudaSuccess) {
+      ptrs.push_back(*p);
+      total += bytes;
+    }
+    return e;
+  }
+  ~DeviceArena() {
+    for (void* p : ptrs) cudaFree(p);
+  }
+};
+
+static bool is_device_ptr(const void* p) {
+  if (!p) return false;
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+struct Status {
+  int code = TTT_OK;
+  std::string msg;
+};
+
+#define CU_TRY(expr)                                                                         \
+  do {                                                                                       \
+    cudaError_t e_ = (expr);                                                                 \
+    if (e_ != cudaSuccess) {                                                                 \
+      err = std::string(#expr) + ": " + cudaGetErrorString(e_);                              \
+      return e_ == cudaErrorMemoryAllocation ? TTT_ERR_OOM : TTT_ERR_CUDA;                   \
+    }                                                                                        \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+struct EngineBase {
+  ttt_config cfg;
+  std::string err;
+  int R = 0, qkv_cols = 0, Vs = 0, num_sms = 148;
+  int64_t pos = 0;
+  bool used = false;
+  bool use_tc_gemm = false, use_tc_attn = false;
+  virtual ~EngineBase() {}
+  virtual int init(const ttt_weights* w, cudaStream_t st) = 0;
+  virtual int prefill(const int32_t* tok, int64_t T, float* losses, cudaStream_t st) = 0;
+  virtual int logits(const int32_t* cont, int n, float* out, cudaStream_t st) = 0;
+  virtual int get_fast(int block, int which, float* dst, cudaStream_t st) = 0;
+  virtual int reset(cudaStream_t st) = 0;
+};
+
+template <typename T>
+struct Engine : EngineBase {
+  static constexpr bool kBF16 = sizeof(T) == 2;
+  DeviceArena mem;
+
+  struct Layer {
+    float *g_attn = nullptr, *g_mlp = nullptr;
+    T *wqkv = nullptr, *wo = nullptr, *wgu = nullptr, *wd = nullptr;
+    float *wgu32 = nullptr, *wd32 = nullptr;            // fast layers: fp32 value
+    T *wgu_lo = nullptr, *wd_lo = nullptr;              // bf16 fast layers: w ~ hi + lo
+    float *wgu32_init = nullptr, *wd32_init = nullptr;  // for ttt_reset
+    T *kring = nullptr, *vring = nullptr;
+  };
+  struct Stash {
+    float* x = nullptr;  // layer input (fp32)
+    T* xn = nullptr;
+    float* r1 = nullptr;
+    T* q = nullptr;
+    T* o = nullptr;
+    float* lse = nullptr;
+    float* h = nullptr;
+    T* hn = nullptr;
+    float* r2 = nullptr;
+    T* gu = nullptr;
+    T* a = nullptr;
+  };
+  std::vector<Layer> layers;
+  std::vector<Stash> fstash;  // fast blocks
+  Stash sstash;               // static blocks (scratch)
+  T *E = nullptr, *Wlm = nullptr;
+  float* g_final = nullptr;
+  float* xlow[2] = {nullptr, nullptr};
+  std::vector<float*> xs;  // inputs of the fast blocks, then the final stream
+  int32_t *tgt = nullptr, *tok_stage = nullptr;
+  float2* cs = nullptr;
+  T* hf = nullptr;
+  float* rf = nullptr;
+  float *z_slab = nullptr, *m_run = nullptr, *l_run = nullptr, *alpha = nullptr, *beta = nullptr,
+        *ztgt = nullptr, *dh_acc = nullptr, *dhf = nullptr, *loss_row = nullptr;
+  T* p_slab = nullptr;
+  float *dy = nullptr, *dhn = nullptr, *dh = nullptr, *dxn = nullptr, *Dsum = nullptr;
+  T *dy_t = nullptr, *dgu = nullptr, *dh_t = nullptr, *dO = nullptr, *dqkv = nullptr;
+  float* losses_stage = nullptr;
+  float* logits_stage = nullptr;
+  int* dev_err = nullptr;  // [0] first non-finite chunk, [1] bad token, [2] kernel check
+  float* stage32 = nullptr;
+  size_t stage32_elems = 0;
+
+  template <typename U>
+  int A(U** p, size_t elems) {
+    cudaError_t e = mem.alloc((void**)p, elems * sizeof(U));
+    if (e != cudaSuccess) {
+      err = "cudaMalloc(" + std::to_string(elems * sizeof(U)) + " bytes): " + cudaGetErrorString(e);
+      cudaGetLastError();
+      return TTT_ERR_OOM;
+    }
+    return TTT_OK;
+  }
+#define A_TRY(p, n)            \
+  do {                         \
+    int rc_ = A(&(p), (n));    \
+    if (rc_) return rc_;       \
+  } while (0)
+
+  // copy an fp32 [rows, cols] tensor (host or device) into dst (type U) with
+  // the row mapping `mode` of launch_pack
+  template <typename U>
+  int upload(const float* src, int64_t rows, int64_t cols, int mode, U* dst, cudaStream_t st) {
+    if (!src) {
+      err = "null weight pointer";
+      return TTT_ERR_INVALID;
+    }
+    const float* s = src;
+    if (!is_device_ptr(src)) {
+      CU_TRY(cudaMemcpyAsync(stage32, src, rows * cols * sizeof(float), cudaMemcpyHostToDevice, st));
+      s = stage32;
+    }
+    launch_pack<U>(s, rows, cols, mode, cfg.head_dim, dst, st);
+    if (!is_device_ptr(src)) CU_TRY(cudaStreamSynchronize(st));  // stage reused next call
+    CU_TRY(cudaGetLastError());
+    return TTT_OK;
+  }
+
+  int init(const ttt_weights* w, cudaStream_t st) override {
+    const int L = cfg.n_layers, d = cfg.d_model, H = cfg.n_heads, Hkv = cfg.n_kv_heads,
+              hd = cfg.head_dim, ff = cfg.d_ff, V = cfg.vocab, b = cfg.chunk, Lt = cfg.n_ttt_layers;
+    const int64_t Hhd = (int64_t)H * hd;
+    int dev = 0;
+    CU_TRY(cudaGetDevice(&dev));
+    CU_TRY(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+    stage32_elems = std::max<int64_t>((int64_t)V * d, (int64_t)2 * ff * d);
+    A_TRY(stage32, stage32_elems);
+    A_TRY(E, (size_t)V * d);
+    A_TRY(Wlm, (size_t)V * d);
+    A_TRY(g_final, d);
+    int rc;
+    if ((rc = upload<T>(w->tok_embed, V, d, 0, E, st))) return rc;
+    if ((rc = upload<T>(w->lm_head, V, d, 0, Wlm, st))) return rc;
+    if ((rc = upload<float>(w->final_norm, 1, d, 0, g_final, st))) return rc;
+    layers.resize(L);
+    for (int l = 0; l < L; ++l) {
+      Layer& y = layers[l];
+      const bool fast = l >= L - Lt;
+      A_TRY(y.g_attn, d);
+      A_TRY(y.g_mlp, d);
+      A_TRY(y.wqkv, (size_t)qkv_cols * d);
+      A_TRY(y.wo, (size_t)d * Hhd);
+      A_TRY(y.wgu, (size_t)2 * ff * d);
+      A_TRY(y.wd, (size_t)d * ff);
+      A_TRY(y.kring, (size_t)Hkv * R * hd);
+      A_TRY(y.vring, (size_t)Hkv * R * hd);
+      CU_TRY(cudaMemsetAsync(y.kring, 0, sizeof(T) * (size_t)Hkv * R * hd, st));
+      CU_TRY(cudaMemsetAsync(y.vring, 0, sizeof(T) * (size_t)Hkv * R * hd, st));
+      if (!w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo || !w->mlp_norm || !w->w_gate ||
+          !w->w_up || !w->w_down) {
+        err = "null per-layer weight array";
+        return TTT_ERR_INVALID;
+      }
+      if ((rc = upload<float>(w->attn_norm[l], 1, d, 0, y.g_attn, st))) return rc;
+      if ((rc = upload<float>(w->mlp_norm[l], 1, d, 0, y.g_mlp, st))) return rc;
+      if ((rc = upload<T>(w->wq[l], Hhd, d, 1, y.wqkv, st))) return rc;
+      if ((rc = upload<T>(w->wk[l], (int64_t)Hkv * hd, d, 1, y.wqkv + Hhd * d, st))) return rc;
+      if ((rc = upload<T>(w->wv[l], (int64_t)Hkv * hd, d, 0, y.wqkv + (Hhd + (int64_t)Hkv * hd) * d, st)))
+        return rc;
+      if ((rc = upload<T>(w->wo[l], d, Hhd, 0, y.wo, st))) return rc;
+      if ((rc = upload<T>(w->w_gate[l], ff, d, 2, y.wgu, st))) return rc;
+      if ((rc = upload<T>(w->w_up[l], ff, d, 3, y.wgu, st))) return rc;
+      if ((rc = upload<T>(w->w_down[l], d, ff, 0, y.wd, st))) return rc;
+      if (fast) {
+        if (kBF16) {
+          A_TRY(y.wgu32, (size_t)2 * ff * d);
+          A_TRY(y.wd32, (size_t)d * ff);
+          if ((rc = upload<float>(w->w_gate[l], ff, d, 2, y.wgu32, st))) return rc;
+          if ((rc = upload<float>(w->w_up[l], ff, d, 3, y.wgu32, st))) return rc;
+          if ((rc = upload<float>(w->w_down[l], d, ff, 0, y.wd32, st))) return rc;
+          A_TRY(y.wgu_lo, (size_t)2 * ff * d);
+          A_TRY(y.wd_lo, (size_t)d * ff);
+          launch_split_bf16(y.wgu32, 2 * (int64_t)ff * d, (bf16*)y.wgu, (bf16*)y.wgu_lo, st);
+          launch_split_bf16(y.wd32, (int64_t)d * ff, (bf16*)y.wd, (bf16*)y.wd_lo, st);
+        } else {
+          y.wgu32 = (float*)y.wgu;
+          y.wd32 = (float*)y.wd;
+        }
+        A_TRY(y.wgu32_init, (size_t)2 * ff * d);
+        A_TRY(y.wd32_init, (size_t)d * ff);
+        CU_TRY(cudaMemcpyAsync(y.wgu32_init, y.wgu32, sizeof(float) * 2 * ff * (size_t)d,
+                               cudaMemcpyDeviceToDevice, st));
+        CU_TRY(cudaMemcpyAsync(y.wd32_init, y.wd32, sizeof(float) * (size_t)d * ff,
+                               cudaMemcpyDeviceToDevice, st));
+      }
+    }
+    // activations of one chunk
+    auto alloc_stash = [&](Stash& s, bool fast) -> int {
+      A_TRY(s.xn, (size_t)b * d);
+      A_TRY(s.r1, b);
+      A_TRY(s.q, (size_t)b * Hhd);
+      A_TRY(s.o, (size_t)b * Hhd);
+      A_TRY(s.lse, (size_t)H * b);
+      A_TRY(s.h, (size_t)b * d);
+      A_TRY(s.hn, (size_t)b * d);
+      A_TRY(s.r2, b);
+      A_TRY(s.a, (size_t)b * ff);
+      if (fast) A_TRY(s.gu, (size_t)b * 2 * ff);
+      return TTT_OK;
+    };
+    if ((rc = alloc_stash(sstash, false))) return rc;
+    fstash.resize(Lt);
+    xs.resize(Lt + 1);
+    for (int i = 0; i <= Lt; ++i) A_TRY(xs[i], (size_t)b * d);
+    for (int i = 0; i < Lt; ++i) {
+      if ((rc = alloc_stash(fstash[i], true))) return rc;
+      fstash[i].x = xs[i];
+    }
+    A_TRY(xlow[0], (size_t)b * d);
+    A_TRY(xlow[1], (size_t)b * d);
+    A_TRY(tgt, b);
+    A_TRY(tok_stage, (size_t)std::max<int64_t>(cfg.max_tokens, b));
+    A_TRY(cs, (size_t)b * (hd / 2));
+    A_TRY(hf, (size_t)b * d);
+    A_TRY(rf, b);
+    A_TRY(z_slab, (size_t)b * Vs);
+    A_TRY(p_slab, (size_t)b * Vs);
+    A_TRY(m_run, b);
+    A_TRY(l_run, b);
+    A_TRY(alpha, b);
+    A_TRY(beta, b);
+    A_TRY(ztgt, b);
+    A_TRY(dh_acc, (size_t)b * d);
+    A_TRY(dhf, (size_t)b * d);
+    A_TRY(loss_row, b);
+    A_TRY(dy, (size_t)b * d);
+    A_TRY(dy_t, (size_t)b * d);
+    A_TRY(dgu, (size_t)b * 2 * ff);
+    A_TRY(dhn, (size_t)b * d);
+    A_TRY(dh, (size_t)b * d);
+    A_TRY(dh_t, (size_t)b * d);
+    A_TRY(dO, (size_t)b * Hhd);
+    A_TRY(dqkv, (size_t)b * qkv_cols);
+    A_TRY(dxn, (size_t)b * d);
+    A_TRY(Dsum, (size_t)H * b);
+    A_TRY(losses_stage, (size_t)(cfg.max_tokens + b - 1) / b + 1);
+    A_TRY(dev_err, 4);
+    CU_TRY(cudaStreamSynchronize(st));
+    return TTT_OK;
+  }
+
+  // -------------------------------------------------------------------------
+  void gemm(int M, int N, int K, const T* A_, int64_t lda, int a_mn, const T* B_, int64_t ldb,
+            int b_mn, const Epi& e, cudaStream_t st, int* rc, const T* B2 = nullptr) {
+    GemmArgs<T> g{M, N, K, A_, lda, a_mn, B_, ldb, b_mn, e, B2};
+    if constexpr (kBF16) {
+      if (use_tc_gemm) {
+        int r = gemm_tc(g, num_sms, dev_err + 2, st);
+        if (r != 0 && *rc == TTT_OK) {
+          *rc = TTT_ERR_SHAPE;
+          err = "tensor-core GEMM rejected M=" + std::to_string(M) + " N=" + std::to_string(N) +
+                " K=" + std::to_string(K) + " (" + cudaGetErrorString((cudaError_t)r) + ")";
+        }
+        return;
+      }
+    }
+    gemm_simt<T>(g, st);
+  }
+  static Epi epi(int kind) {
+    Epi e;
+    memset(&e, 0, sizeof(e));
+    e.kind = kind;
+    return e;
+  }
+  AttnArgs attn_args(const Stash& S, const Layer& y, int64_t s, int n) {
+    AttnArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = S.q;
+    a.kring = y.kring;
+    a.vring = y.vring;
+    a.o = S.o;
+    a.lse = S.lse;
+    a.ld_lse = cfg.chunk;
+    a.n = n;
+    a.H = cfg.n_heads;
+    a.Hkv = cfg.n_kv_heads;
+    a.hd = cfg.head_dim;
+    a.W = cfg.window;
+    a.R = R;
+    a.pos0 = s;
+    return a;
+  }
+  void attn_fwd(const AttnArgs& a, cudaStream_t st, int* rc) {
+    if constexpr (kBF16) {
+      if (use_tc_attn) {
+        int r = attn_fwd_tc(a, st);
+        if (r != 0 && *rc == TTT_OK) {
+          *rc = TTT_ERR_SHAPE;
+          err = "tensor-core attention forward rejected the shape";
+        }
+        return;
+      }
+    }
+    attn_fwd_simt<T>(a, st);
+  }
+  void attn_bwd(const AttnArgs& a, cudaStream_t st, int* rc) {
+    if constexpr (kBF16) {
+      if (use_tc_attn) {
+        int r = attn_bwd_tc(a, st);
+        if (r != 0 && *rc == TTT_OK) {
+          *rc = TTT_ERR_SHAPE;
+          err = "tensor-core attention backward rejected the shape";
+        }
+        return;
+      }
+    }
+    attn_bwd_simt<T>(a, st);
+  }
+
+  // forward of positions [s, s+n) with the current weights; leaves the final
+  // normed hidden state in hf (T) and its statistics in rf.
+  void forward(const int32_t* tok_chunk, int64_t s, int n, cudaStream_t st, int* rc) {
+    const int L = cfg.n_layers, d = cfg.d_model, H = cfg.n_heads, hd = cfg.head_dim, ff = cfg.d_ff,
+              Lt = cfg.n_ttt_layers;
+    const int lo = L - Lt;
+    const int64_t Hhd = (int64_t)H * hd;
+    launch_rope_table(s, n, hd, cfg.rope_theta, cs, st);
+    float* x_in = lo == 0 ? xs[0] : xlow[0];
+    launch_embed<T>(tok_chunk, n, E, d, x_in, cfg.vocab, dev_err + 1, st);
+    for (int l = 0; l < L; ++l) {
+      const bool fast = l >= lo;
+      Stash& S = fast ? fstash[l - lo] : sstash;
+      Layer& y = layers[l];
+      float* x_out = (l + 1 >= lo) ? xs[l + 1 - lo] : xlow[(l + 1) & 1];
+      launch_rmsnorm_fwd<T>(x_in, y.g_attn, n, d, cfg.norm_eps, S.xn, S.r1, st);
+      Epi e = epi(EPI_QKV);
+      e.out = S.q;
+      e.ldo = Hhd;
+      e.n_q = H;
+      e.n_kv = cfg.n_kv_heads;
+      e.hd = hd;
+      e.pos0 = s;
+      e.ring = R;
+      e.kring = y.kring;
+      e.vring = y.vring;
+      e.rope_cs = cs;
+      gemm(n, qkv_cols, d, S.xn, d, 0, y.wqkv, d, 0, e, st, rc);
+      attn_fwd(attn_args(S, y, s, n), st, rc);
+      e = epi(EPI_RESID);
+      e.out = S.h;
+      e.ldo = d;
+      e.resid = x_in;
+      e.ldr = d;
+      gemm(n, d, (int)Hhd, S.o, Hhd, 0, y.wo, Hhd, 0, e, st, rc);
+      launch_rmsnorm_fwd<T>(S.h, y.g_mlp, n, d, cfg.norm_eps, S.hn, S.r2, st);
+      e = epi(EPI_SWIGLU);
+      e.out = S.a;
+      e.ldo = ff;
+      e.stash = fast ? S.gu : nullptr;
+      e.ld_stash = 2 * (int64_t)ff;
+      // fast weights in bf16 mode are read as the pair hi + lo, so updates
+      // below one bf16 ulp still reach the forward
+      gemm(n, 2 * ff, d, S.hn, d, 0, y.wgu, d, 0, e, st, rc, y.wgu_lo);
+      e = epi(EPI_RESID);
+      e.out = x_out;
+      e.ldo = d;
+      e.resid = S.h;
+      e.ldr = d;
+      gemm(n, d, ff, S.a, ff, 0, y.wd, ff, 0, e, st, rc, y.wd_lo);
+      x_in = x_out;
+    }
+    launch_rmsnorm_fwd<T>(x_in, g_final, n, d, cfg.norm_eps, hf, rf, st);
+  }
+
+  // streamed lm_head + cross-entropy: loss of chunk c into losses[c] and the
+  // gradient w.r.t. the final normed hidden state into dhf (fp32)
+  void cross_entropy(const int32_t* tok, int64_t n_tok, int64_t s, int n, int n_tgt, float* losses, int c,
+                     cudaStream_t st, int* rc) {
+    const int d = cfg.d_model, V = cfg.vocab;
+    launch_targets(tok, n_tok, s, n, tgt, V, dev_err + 1, st);
+    for (int v0 = 0; v0 < V; v0 += Vs) {
+      const int nv = std::min(Vs, V - v0);
+      const int first = v0 == 0;
+      Epi e = epi(EPI_CE_Z);
+      e.out = z_slab;
+      e.ldo = Vs;
+      e.tgt = tgt;
+      e.ztgt = ztgt;
+      e.col0 = v0;
+      gemm(n, nv, d, hf, d, 0, Wlm + (int64_t)v0 * d, d, 0, e, st, rc);
+      launch_ce_slab_stats<T>(z_slab, Vs, n, nv, p_slab, Vs, m_run, l_run, alpha, beta, first, st);
+      e = epi(EPI_CE_ACC);
+      e.out = dh_acc;
+      e.ldo = d;
+      e.alpha = alpha;
+      e.beta = beta;
+      e.first = first;
+      gemm(n, d, nv, p_slab, Vs, 0, Wlm + (int64_t)v0 * d, d, 1, e, st, rc);
+    }
+    const float inv = 1.0f / (float)n_tgt;
+    launch_ce_finalize<T>(n, m_run, l_run, ztgt, tgt, inv, dh_acc, Wlm, d, dhf, loss_row, st);
+    launch_loss_reduce(loss_row, n, inv, losses, c, dev_err, st);
+  }
+
+  // backward of the chunk loss into the fast MLPs, with the SGD step fused
+  // into the weight-gradient GEMMs.  Every read of a fast weight (da, dhn)
+  // happens before that weight's update in stream order.
+  void backward(int64_t s, int n, cudaStream_t st, int* rc) {
+    const int L = cfg.n_layers, d = cfg.d_model, H = cfg.n_heads, Hkv = cfg.n_kv_heads,
+              hd = cfg.head_dim, ff = cfg.d_ff, Lt = cfg.n_ttt_layers;
+    const int lo = L - Lt;
+    const int64_t Hhd = (int64_t)H * hd;
+    launch_rmsnorm_bwd<T>(xs[Lt], g_final, rf, dhf, nullptr, n, d, dy, dy_t, st);
+    for (int l = L - 1; l >= lo; --l) {
+      Stash& S = fstash[l - lo];
+      Layer& y = layers[l];
+      // da = dy Wd  ->  (dg, du) with the stashed (g, u)
+      Epi e = epi(EPI_SWIGLU_BWD);
+      e.out = dgu;
+      e.ldo = 2 * (int64_t)ff;
+      e.stash = S.gu;
+      e.ld_stash = 2 * (int64_t)ff;
+      gemm(n, ff, d, dy_t, d, 0, y.wd, ff, 1, e, st, rc);
+      if (l > lo) {
+        // dhn = [dg du] [Wg; Wu]
+        e = epi(EPI_STORE);
+        e.out_f32 = 1;
+        e.out = dhn;
+        e.ldo = d;
+        gemm(n, d, 2 * ff, dgu, 2 * (int64_t)ff, 0, y.wgu, d, 1, e, st, rc);
+      }
+      // Wd -= lr dy^T a ;  [Wg;Wu] -= lr [dg du]^T hn
+      e = epi(EPI_SGD);
+      e.w32 = y.wd32;
+      e.w16 = kBF16 ? (void*)y.wd : nullptr;
+      e.w16lo = y.wd_lo;
+      e.ldo = ff;
+      e.lr = cfg.lr;
+      gemm(d, ff, n, dy_t, d, 1, S.a, ff, 1, e, st, rc);
+      e.w32 = y.wgu32;
+      e.w16 = kBF16 ? (void*)y.wgu : nullptr;
+      e.w16lo = y.wgu_lo;
+      e.ldo = d;
+      gemm(2 * ff, d, n, dgu, 2 * (int64_t)ff, 1, S.hn, d, 1, e, st, rc);
+      if (l == lo) break;
+      // through the MLP norm and the residual
+      launch_rmsnorm_bwd<T>(S.h, y.g_mlp, S.r2, dhn, dy, n, d, dh, dh_t, st);
+      // dO = dh Wo
+      e = epi(EPI_STORE);
+      e.out = dO;
+      e.ldo = Hhd;
+      gemm(n, (int)Hhd, d, dh_t, d, 0, y.wo, Hhd, 1, e, st, rc);
+      AttnArgs a = attn_args(S, y, s, n);
+      a.dout = dO;
+      a.out = S.o;
+      a.Dsum = Dsum;
+      a.dqkv = dqkv;
+      attn_bwd(a, st, rc);
+      launch_rope_bwd<T>(dqkv, n, qkv_cols, H + Hkv, hd, cs, st);
+      // dxn = [dq dk dv] Wqkv
+      e = epi(EPI_STORE);
+      e.out_f32 = 1;
+      e.out = dxn;
+      e.ldo = d;
+      gemm(n, d, qkv_cols, dqkv, qkv_cols, 0, y.wqkv, d, 1, e, st, rc);
+      launch_rmsnorm_bwd<T>(S.x, y.g_attn, S.r1, dxn, dh, n, d, dy, dy_t, st);
+    }
+  }
+
+  int finish(cudaStream_t st, const char* what) {
+    CU_TRY(cudaGetLastError());
+    int h_err[3];
+    CU_TRY(cudaMemcpyAsync(h_err, dev_err, sizeof(h_err), cudaMemcpyDeviceToHost, st));
+    CU_TRY(cudaStreamSynchronize(st));
+    if (h_err[2] != 0) {
+      err = std::string(what) + ": a device-side check failed (code " + std::to_string(h_err[2]) + ")";
+      return TTT_ERR_INTERNAL;
+    }
+    if (h_err[1] != 0) {
+      err = std::string(what) + ": token id outside [0, vocab)";
+      return TTT_ERR_INVALID;
+    }
+    if (h_err[0] != INT_MAX) {
+      err = std::string(what) + ": non-finite loss at chunk " + std::to_string(h_err[0]);
+      return TTT_ERR_NONFINITE;
+    }
+    return TTT_OK;
+  }
+  int clear_err(cudaStream_t st) {
+    int h_err[4] = {INT_MAX, 0, 0, 0};
+    CU_TRY(cudaMemcpyAsync(dev_err, h_err, sizeof(h_err), cudaMemcpyHostToDevice, st));
+    return TTT_OK;
+  }
+
+  int prefill(const int32_t* tok, int64_t n_tok, float* losses, cudaStream_t st) override {
+    const int b = cfg.chunk;
+    if (used) {
+      err = "ttt_prefill needs a fresh or reset context";
+      return TTT_ERR_STATE;
+    }
+    if (n_tok < 1 || n_tok > cfg.max_tokens) {
+      err = "T must be in [1, max_tokens]";
+      return TTT_ERR_SHAPE;
+    }
+    if (!tok || !losses) {
+      err = "null tokens or losses";
+      return TTT_ERR_INVALID;
+    }
+    const int nC = (int)((n_tok + b - 1) / b);
+    const int32_t* tok_d = tok;
+    if (!is_device_ptr(tok)) {
+      CU_TRY(cudaMemcpyAsync(tok_stage, tok, sizeof(int32_t) * n_tok, cudaMemcpyHostToDevice, st));
+      tok_d = tok_stage;
+    }
+    const bool host_out = !is_device_ptr(losses);
+    float* loss_d = host_out ? losses_stage : losses;
+    int rc = clear_err(st);
+    if (rc) return rc;
+    used = true;
+    for (int c = 0; c < nC && rc == TTT_OK; ++c) {
+      const int64_t s = (int64_t)c * b;
+      const int n = (int)std::min<int64_t>(b, n_tok - s);
+      const int n_tgt = (int)std::min<int64_t>(n, n_tok - 1 - s);
+      forward(tok_d + s, s, n, st, &rc);
+      if (n_tgt <= 0) {
+        CU_TRY(cudaMemsetAsync(loss_d + c, 0, sizeof(float), st));
+        continue;
+      }
+      cross_entropy(tok_d, n_tok, s, n, n_tgt, loss_d, c, st, &rc);
+      backward(s, n, st, &rc);
+      CU_TRY(cudaPeekAtLastError());
+    }
+    if (rc) return rc;
+    pos = n_tok;
+    if (host_out)
+      CU_TRY(cudaMemcpyAsync(losses, loss_d, sizeof(float) * nC, cudaMemcpyDeviceToHost, st));
+    return finish(st, "ttt_prefill");
+  }
+
+  int logits(const int32_t* cont, int n, float* out, cudaStream_t st) override {
+    if (n < 1 || n > cfg.chunk) {
+      err = "n must be in [1, chunk]";
+      return TTT_ERR_SHAPE;
+    }
+    if (!cont || !out) {
+      err = "null continuation or logits";
+      return TTT_ERR_INVALID;
+    }
+    const int32_t* c_d = cont;
+    if (!is_device_ptr(cont)) {
+      CU_TRY(cudaMemcpyAsync(tok_stage, cont, sizeof(int32_t) * n, cudaMemcpyHostToDevice, st));
+      c_d = tok_stage;
+    }
+    const bool host_out = !is_device_ptr(out);
+    float* o = out;
+    if (host_out) {
+      if (!logits_stage) A_TRY(logits_stage, (size_t)cfg.chunk * cfg.vocab);
+      o = logits_stage;
+    }
+    int rc = clear_err(st);
+    if (rc) return rc;
+    forward(c_d, pos, n, st, &rc);
+    Epi e = epi(EPI_STORE);
+    e.out_f32 = 1;
+    e.out = o;
+    e.ldo = cfg.vocab;
+    gemm(n, cfg.vocab, cfg.d_model, hf, cfg.d_model, 0, Wlm, cfg.d_model, 0, e, st, &rc);
+    if (rc) return rc;
+    if (host_out)
+      CU_TRY(cudaMemcpyAsync(out, o, sizeof(float) * (size_t)n * cfg.vocab, cudaMemcpyDeviceToHost, st));
+    return finish(st, "ttt_logits");
+  }
+
+  int get_fast(int block, int which, float* dst, cudaStream_t st) override {
+    const int d = cfg.d_model, ff = cfg.d_ff;
+    if (block < 0 || block >= cfg.n_ttt_layers || which < 0 || which > 2 || !dst) {
+      err = "bad block/which/dst";
+      return TTT_ERR_INVALID;
+    }
+    Layer& y = layers[cfg.n_layers - cfg.n_ttt_layers + block];
+    if (which == 2) {
+      CU_TRY(cudaMemcpyAsync(dst, y.wd32, sizeof(float) * (size_t)d * ff, cudaMemcpyDefault, st));
+    } else {
+      CU_TRY(cudaMemcpy2DAsync(dst, sizeof(float) * d, y.wgu32 + (which == 1 ? d : 0),
+                               sizeof(float) * 2 * d, sizeof(float) * d, ff, cudaMemcpyDefault, st));
+    }
+    CU_TRY(cudaStreamSynchronize(st));
+    return TTT_OK;
+  }
+
+  int reset(cudaStream_t st) override {
+    const int L = cfg.n_layers, d = cfg.d_model, ff = cfg.d_ff, Hkv = cfg.n_kv_heads, hd = cfg.head_dim;
+    for (int l = 0; l < L; ++l) {
+      Layer& y = layers[l];
+      CU_TRY(cudaMemsetAsync(y.kring, 0, sizeof(T) * (size_t)Hkv * R * hd, st));
+      CU_TRY(cudaMemsetAsync(y.vring, 0, sizeof(T) * (size_t)Hkv * R * hd, st));
+      if (l >= L - cfg.n_ttt_layers) {
+        CU_TRY(cudaMemcpyAsync(y.wgu32, y.wgu32_init, sizeof(float) * 2 * ff * (size_t)d,
+                               cudaMemcpyDeviceToDevice, st));
+        CU_TRY(cudaMemcpyAsync(y.wd32, y.wd32_init, sizeof(float) * (size_t)d * ff,
+                               cudaMemcpyDeviceToDevice, st));
+        if (kBF16) {
+          launch_split_bf16(y.wgu32, 2 * (int64_t)ff * d, (bf16*)y.wgu, (bf16*)y.wgu_lo, st);
+          launch_split_bf16(y.wd32, (int64_t)d * ff, (bf16*)y.wd, (bf16*)y.wd_lo, st);
+        }
+      }
+    }
+    CU_TRY(cudaGetLastError());
+    CU_TRY(cudaStreamSynchronize(st));
+    pos = 0;
+    used = false;
+    return TTT_OK;
+  }
+};
+
+}  // namespace ttt
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+struct ttt_ctx {
+  std::unique_ptr<ttt::EngineBase> eng;
+};
+
+static int validate(const ttt_config* c, std::string& msg) {
+  if (c->precision != TTT_BF16 && c->precision != TTT_FP32_CHECK) {
+    msg = "precision must be TTT_BF16 or TTT_FP32_CHECK";
+    return TTT_ERR_INVALID;
+  }
+  if (c->n_layers < 1 || c->d_model < 2 || c->n_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 2 ||
+      c->d_ff < 2 || c->vocab < 2 || c->window < 1 || c->chunk < 1 || c->n_ttt_layers < 1 ||
+      c->max_tokens < 1) {
+    msg = "every size must be positive (n_ttt_layers >= 1)";
+    return TTT_ERR_INVALID;
+  }
+  if (c->n_ttt_layers > c->n_layers) {
+    msg = "n_ttt_layers > n_layers";
+    return TTT_ERR_INVALID;
+  }
+  if (c->n_heads % c->n_kv_heads) {
+    msg = "n_heads must be a multiple of n_kv_heads";
+    return TTT_ERR_SHAPE;
+  }
+  if ((c->head_dim & 1) || (c->d_model & 1) || (c->d_ff & 1) || (c->vocab & 1) || c->head_dim > 256) {
+    msg = "head_dim, d_model, d_ff and vocab must be even; head_dim <= 256";
+    return TTT_ERR_SHAPE;
+  }
+  if (!std::isfinite(c->lr)) {
+    msg = "lr is not finite";
+    return TTT_ERR_NONFINITE;
+  }
+  if (!(c->rope_theta > 0.f) || !std::isfinite(c->rope_theta) || !(c->norm_eps >= 0.f) ||
+      !std::isfinite(c->norm_eps)) {
+    msg = "rope_theta must be positive and norm_eps non-negative (both finite)";
+    return TTT_ERR_INVALID;
+  }
+  return TTT_OK;
+}
+
+extern "C" int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* stream, ttt_ctx** out) {
+  ttt::g_create_error.clear();
+  if (!out) {
+    ttt::g_create_error = "out is null";
+    return TTT_ERR_INVALID;
+  }
+  *out = nullptr;
+  if (!cfg || !w) {
+    ttt::g_create_error = "cfg or weights is null";
+    return TTT_ERR_INVALID;
+  }
+  std::string msg;
+  int rc = validate(cfg, msg);
+  if (rc) {
+    ttt::g_create_error = msg;
+    return rc;
+  }
+  std::unique_ptr<ttt::EngineBase> eng;
+  try {
+    if (cfg->precision == TTT_BF16) eng.reset(new ttt::Engine<ttt::bf16>());
+    else eng.reset(new ttt::Engine<float>());
+  } catch (...) {
+    ttt::g_create_error = "host allocation failed";
+    return TTT_ERR_OOM;
+  }
+  eng->cfg = *cfg;
+  const int need = cfg->window + cfg->chunk - 1;
+  eng->R = ((need + 127) / 128) * 128;
+  eng->qkv_cols = (cfg->n_heads + 2 * cfg->n_kv_heads) * cfg->head_dim;
+  eng->Vs = std::min(cfg->vocab, 8192);
+  const bool bf = cfg->precision == TTT_BF16;
+  const char* g = getenv("TTT_GEMM_IMPL");
+  const char* a = getenv("TTT_ATTN_IMPL");
+  eng->use_tc_gemm = bf && !(g && strcmp(g, "simt") == 0);
+  eng->use_tc_attn = bf && (a && strcmp(a, "tc") == 0);
+  if (eng->use_tc_gemm) {
+    int r = ttt::gemm_tc_init();
+    if (r) {
+      ttt::g_create_error = "tensor-core GEMM initialisation failed";
+      return TTT_ERR_CUDA;
+    }
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  try {
+    rc = eng->init(w, st);
+  } catch (...) {
+    rc = TTT_ERR_INTERNAL;
+    eng->err = "exception during initialisation";
+  }
+  if (rc) {
+    ttt::g_create_error = eng->err;
+    cudaStreamSynchronize(st);
+    return rc;
+  }
+  ttt_ctx* c = new (std::nothrow) ttt_ctx();
+  if (!c) {
+    ttt::g_create_error = "host allocation failed";
+    return TTT_ERR_OOM;
+  }
+  c->eng = std::move(eng);
+  *out = c;
+  return TTT_OK;
+}
+
+#define CTX_GUARD(ctx)                 \
+  if (!(ctx) || !(ctx)->eng) return TTT_ERR_INVALID;
+
+extern "C" int ttt_prefill(ttt_ctx* ctx, const int32_t* tokens, int64_t T, float* chunk_losses,
+                           void* stream) {
+  CTX_GUARD(ctx);
+  ctx->eng->err.clear();
+  try {
+    return ctx->eng->prefill(tokens, T, chunk_losses, (cudaStream_t)stream);
+  } catch (...) {
+    ctx->eng->err = "exception in ttt_prefill";
+    return TTT_ERR_INTERNAL;
+  }
+}
+
+extern "C" int ttt_logits(ttt_ctx* ctx, const int32_t* cont, int32_t n, float* logits, void* stream) {
+  CTX_GUARD(ctx);
+  ctx->eng->err.clear();
+  try {
+    return ctx->eng->logits(cont, n, logits, (cudaStream_t)stream);
+  } catch (...) {
+    ctx->eng->err = "exception in ttt_logits";
+    return TTT_ERR_INTERNAL;
+  }
+}
+
+extern "C" int ttt_get_fast_weights(ttt_ctx* ctx, int32_t block, int32_t which, float* dst, void* stream) {
+  CTX_GUARD(ctx);
+  ctx->eng->err.clear();
+  return ctx->eng->get_fast(block, which, dst, (cudaStream_t)stream);
+}
+
+extern "C" int ttt_reset(ttt_ctx* ctx) {
+  CTX_GUARD(ctx);
+  ctx->eng->err.clear();
+  return ctx->eng->reset((cudaStream_t)0);
+}
+
+extern "C" void ttt_destroy(ttt_ctx* ctx) {
+  if (!ctx) return;
+  cudaDeviceSynchronize();
+  delete ctx;
+}
+
+extern "C" const char* ttt_last_error(const ttt_ctx* ctx) {
+  if (!ctx || !ctx->eng) return ttt::g_create_error.c_str();
+  return ctx->eng->err.c_str();
+}

@@ -1,0 +1,328 @@
+// gemm_tc.cu — persistent, warp-specialised bf16 GEMM on the 5th-generation
+// tensor cores (tcgen05) with TMA-fed shared-memory pipelines and the fused
+// epilogues of common.cuh.
+//
+//   C[m, n] = sum_k A(m, k) B(n, k)     (fp32 accumulate in TMEM)
+//
+// Tile 128 x BN x 64 (BN = 128 or 256).  Per CTA (one per SM, persistent
+// over output tiles):
+//   warp 0     TMA producer: A and B tiles into a STAGES-deep ring of
+//              128-byte-swizzled shared-memory buffers (mbarrier full/empty);
+//   warp 1     allocates TMEM (two BN-column fp32 accumulators) and issues
+//              tcgen05.mma from one thread; tcgen05.commit frees smem stages
+//              and publishes finished accumulators;
+//   warps 2-5  epilogue: tcgen05.ld 32 columns at a time (each thread owns
+//              one output row), apply the epilogue, release the accumulator,
+//              so the next tile's MMAs overlap this tile's epilogue.
+// Either operand may be K-major (rows of K contiguous) or MN-major (K rows of
+// M/N contiguous); the TMA box orientation and the descriptor's major bit
+// follow.  All waits are bounded (see tc_common.cuh).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace ttt {
+
+namespace {
+
+constexpr int BM = 128, BK = 64;
+constexpr int A_BYTES = BM * BK * 2;
+
+template <int BN>
+struct Cfg {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int SMEM = 1024 /*align slack*/ + BAR_OFF + 256;
+};
+
+enum : int { ERR_WAIT_PRODUCER = 101, ERR_WAIT_MMA = 102, ERR_WAIT_EPI = 103, ERR_WAIT_DRAIN = 104 };
+
+template <int BN, int A_MN, int B_MN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                   const __grid_constant__ CUtensorMap mapB2, int dual, int M, int N, int K, Epi e, int* err) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = tc::smem_u32(smem);
+  uint64_t* bars = (uint64_t*)(smem + C::BAR_OFF);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain
+  const uint32_t full0 = tc::smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * C::STAGES;
+  const uint32_t tfull0 = empty0 + 8 * C::STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+  uint32_t* tmem_slot = (uint32_t*)(smem + C::BAR_OFF + 8 * (2 * C::STAGES + 5));
+  volatile int* abort = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+  const int ntiles = num_m * num_n;
+  const int nk = (K + BK - 1) / BK;
+  const int nk_total = dual ? 2 * nk : nk;  // dual: A B^T then A B2^T into one accumulator
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      tc::mbar_init(full0 + 8 * s, 1);
+      tc::mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(tfull0 + 8 * a, 1);
+      tc::mbar_init(tempty0 + 8 * a, 128);
+    }
+    tc::mbar_init(drain, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&mapA);
+    tc::prefetch_tmap(&mapB);
+    if (dual) tc::prefetch_tmap(&mapB2);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_parity[C::STAGES];
+      for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
+        for (int kb = 0; kb < nk_total; ++kb) {
+          if (!tc::mbar_wait(empty0 + 8 * stage, phase ^ 1, err, ERR_WAIT_PRODUCER, abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * stage;
+          const uint32_t a_s = sbase + stage * C::STAGE_BYTES;
+          const uint32_t b_s = a_s + A_BYTES;
+          const int k0 = (kb < nk ? kb : kb - nk) * BK;
+          const CUtensorMap* mb = kb < nk ? &mapB : &mapB2;
+          tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          if (A_MN) {
+            tc::tma_load_2d(a_s, &mapA, m0, k0, fb);
+            tc::tma_load_2d(a_s + 8192, &mapA, m0 + 64, k0, fb);
+          } else {
+            tc::tma_load_2d(a_s, &mapA, k0, m0, fb);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tc::tma_load_2d(b_s + 8192 * j, mb, n0 + 64 * j, k0, fb);
+          } else {
+            tc::tma_load_2d(b_s, mb, k0, n0, fb);
+          }
+          last_parity[stage] = (int)phase;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // let copies already issued land before the CTA exits
+        for (int s = 0; s < C::STAGES; ++s)
+          if (last_parity[s] >= 0) {
+            const long long t0 = clock64();
+            while (!tc::mbar_try_wait(full0 + 8 * s, (uint32_t)last_parity[s]) && clock64() - t0 < tc::kWaitClocks) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t idesc = tc::idesc_bf16(BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        if (!tc::mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, err, ERR_WAIT_MMA, abort)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * BN;
+        for (int kb = 0; kb < nk_total; ++kb) {
+          if (!tc::mbar_wait(full0 + 8 * stage, phase, err, ERR_WAIT_MMA, abort)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t a_s = sbase + stage * C::STAGE_BYTES;
+          const uint32_t b_s = a_s + A_BYTES;
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j) {
+            const uint64_t ad = A_MN ? tc::smem_desc_sw128(a_s + 2048 * j, 8192, 1024)
+                                     : tc::smem_desc_sw128(a_s + 32 * j, 16, 1024);
+            const uint64_t bd = B_MN ? tc::smem_desc_sw128(b_s + 2048 * j, 8192, 1024)
+                                     : tc::smem_desc_sw128(b_s + 32 * j, 16, 1024);
+            tc::mma_bf16(d_tmem, ad, bd, idesc, (kb | j) != 0);
+          }
+          issued = true;
+          tc::mma_commit(empty0 + 8 * stage);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(tfull0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if (!ok && issued) {
+        // drain MMAs in flight before TMEM is released
+        tc::mma_commit(drain);
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(drain, 0) && clock64() - t0 < tc::kWaitClocks) {
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      if (!tc::mbar_wait(tfull0 + 8 * acc, acc_phase, err, ERR_WAIT_EPI, abort)) break;
+      tc::tc_fence_after();
+      const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
+      const int row = m0 + quarter * 32 + lane;
+      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        if (n0 + c * 32 >= N) break;  // warp-uniform
+        float v[32];
+        tc::tmem_ld32(tbase + c * 32, v);
+        if (row < M) {
+#pragma unroll
+          for (int p = 0; p < 16; ++p) {
+            const int col = n0 + c * 32 + 2 * p;
+            if (col < N) epi_pair<bf16>(e, row, col, v[2 * p], v[2 * p + 1]);
+          }
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(tempty0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+int g_init_rc = 0;
+
+int make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld_elems,
+             uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld_elems * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+}
+
+template <int BN, int A_MN, int B_MN>
+int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st) {
+  using C = Cfg<BN>;
+  CUtensorMap ma, mb, mb2;
+  int rc;
+  if (A_MN) rc = make_map(&ma, g.A, g.M, g.K, g.lda, 64, 64);
+  else rc = make_map(&ma, g.A, g.K, g.M, g.lda, 64, BM);
+  if (rc) return rc;
+  if (B_MN) rc = make_map(&mb, g.B, g.N, g.K, g.ldb, 64, 64);
+  else rc = make_map(&mb, g.B, g.K, g.N, g.ldb, 64, BN);
+  if (rc) return rc;
+  if (g.B2) {
+    if (B_MN) rc = make_map(&mb2, g.B2, g.N, g.K, g.ldb, 64, 64);
+    else rc = make_map(&mb2, g.B2, g.K, g.N, g.ldb, 64, BN);
+    if (rc) return rc;
+  } else {
+    mb2 = mb;
+  }
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  const int ntiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const int grid = ntiles < num_sms ? ntiles : num_sms;
+  gemm_tc_kernel<BN, A_MN, B_MN><<<grid, 192, C::SMEM, st>>>(ma, mb, mb2, g.B2 ? 1 : 0, g.M, g.N, g.K, g.e, err);
+  return (int)cudaPeekAtLastError();
+}
+
+template <int BN>
+int dispatch_major(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st) {
+  if (g.a_mn) {
+    return g.b_mn ? launch<BN, 1, 1>(g, num_sms, err, st) : launch<BN, 1, 0>(g, num_sms, err, st);
+  }
+  return g.b_mn ? launch<BN, 0, 1>(g, num_sms, err, st) : launch<BN, 0, 0>(g, num_sms, err, st);
+}
+
+}  // namespace
+
+int gemm_tc_init() {
+  std::call_once(g_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+      g_init_rc = (int)cudaErrorNotSupported;
+      return;
+    }
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  });
+  return g_init_rc;
+}
+
+int gemm_tc(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st) {
+  if (g.M <= 0 || g.N <= 0) return 0;
+  if (!g_encode) return (int)cudaErrorNotSupported;
+  // TMA: 16-byte aligned base and row pitch
+  if (((uintptr_t)g.A & 15) || ((uintptr_t)g.B & 15) || ((uintptr_t)g.B2 & 15) || (g.lda & 7) ||
+      (g.ldb & 7) || g.K <= 0)
+    return (int)cudaErrorNotSupported;
+  const int tiles256 = ((g.M + BM - 1) / BM) * ((g.N + 255) / 256);
+  if (g.N > 128 && tiles256 >= num_sms) return dispatch_major<256>(g, num_sms, err, st);
+  return dispatch_major<128>(g, num_sms, err, st);
+}
+
+}  // namespace ttt

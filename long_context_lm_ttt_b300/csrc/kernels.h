@@ -1,0 +1,91 @@
+// kernels.h — host-side launchers of every kernel of the inner loop.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace ttt {
+
+template <typename T>
+struct GemmArgs {
+  int M, N, K;
+  const T* A;
+  int64_t lda;
+  int a_mn;
+  const T* B;
+  int64_t ldb;
+  int b_mn;
+  Epi e;
+  const T* B2;  // optional second B (same layout): C = A B^T + A B2^T
+};
+
+// SIMT fp32-accumulate GEMM (check mode; reference for the tensor-core one)
+template <typename T> void gemm_simt(const GemmArgs<T>& g, cudaStream_t st);
+
+// tcgen05 / TMA GEMM (bf16 in, fp32 accumulate).  Returns a cudaError_t
+// (cudaErrorNotSupported when the shape cannot be described by TMA).
+int gemm_tc(const GemmArgs<bf16>& g, int num_sms, int* dev_err, cudaStream_t st);
+int gemm_tc_init();
+
+// --- element-wise / row kernels (kernels.cu) -------------------------------
+template <typename T>
+void launch_embed(const int32_t* tok, int n, const T* E, int d, float* x, int V, int* err_tok,
+                  cudaStream_t st);
+template <typename T>
+void launch_rmsnorm_fwd(const float* x, const float* g, int n, int d, float eps, T* out, float* r,
+                        cudaStream_t st);
+// out = resid + rmsnorm_bwd(x, g, r, dy); also out_t = (T)out when out_t != null
+template <typename T>
+void launch_rmsnorm_bwd(const float* x, const float* g, const float* r, const float* dy,
+                        const float* resid, int n, int d, float* out, T* out_t, cudaStream_t st);
+void launch_rope_table(int64_t pos0, int n, int hd, float theta, float2* cs, cudaStream_t st);
+template <typename T>
+void launch_rope_bwd(T* dqkv, int n, int ld, int n_rot_heads, int hd, const float2* cs,
+                     cudaStream_t st);
+void launch_targets(const int32_t* tok, int64_t T, int64_t pos0, int n, int32_t* tgt, int V,
+                    int* err_tok, cudaStream_t st);
+template <typename T>
+void launch_ce_slab_stats(const float* z, int64_t ldz, int n, int nv, T* p, int64_t ldp,
+                          float* m_run, float* l_run, float* alpha, float* beta, int first,
+                          cudaStream_t st);
+template <typename T>
+void launch_ce_finalize(int n, const float* m_run, const float* l_run, const float* ztgt,
+                        const int32_t* tgt, float inv_ntgt, const float* dh_acc, const T* Wlm,
+                        int d, float* dhf, float* loss_row, cudaStream_t st);
+void launch_loss_reduce(const float* loss_row, int n, float inv_ntgt, float* out, int chunk,
+                        int* err_chunk, cudaStream_t st);
+// pack an fp32 [rows, cols] matrix into T with a row permutation:
+// dst[(row_map(r)) * cols + c] = src[r * cols + c]
+//   mode 0: identity, 1: rope pair interleave within heads of size hd
+//   (i < hd/2 -> 2i, else 2(i-hd/2)+1), 2: interleave into even rows
+//   (r -> 2r), 3: interleave into odd rows (r -> 2r+1)
+template <typename T>
+void launch_pack(const float* src, int64_t rows, int64_t cols, int mode, int hd, T* dst,
+                 cudaStream_t st);
+void launch_f32_to_bf16(const float* src, int64_t n, bf16* dst, cudaStream_t st);
+// hi = rn(w), lo = rn(w - hi): a bf16 pair whose sum carries ~16 mantissa bits
+void launch_split_bf16(const float* w, int64_t n, bf16* hi, bf16* lo, cudaStream_t st);
+
+// --- attention (attn_simt.cu / attn_mma.cu) --------------------------------
+struct AttnArgs {
+  const void* q;      // [n, H*hd] (pair-interleaved RoPE layout)
+  const void* kring;  // [Hkv][R][hd]
+  const void* vring;
+  void* o;            // [n, H*hd]
+  float* lse;         // [H][ld_lse]
+  int ld_lse;
+  int n, H, Hkv, hd, W, R;
+  int64_t pos0;
+  // backward
+  const void* dout;   // [n, H*hd]
+  const void* out;    // forward output o
+  float* Dsum;        // [H][ld_lse]
+  void* dqkv;         // [n, (H+2Hkv)*hd]: dq | dk | dv
+};
+template <typename T> void attn_fwd_simt(const AttnArgs& a, cudaStream_t st);
+template <typename T> void attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
+int attn_fwd_tc(const AttnArgs& a, cudaStream_t st);
+int attn_bwd_tc(const AttnArgs& a, cudaStream_t st);
+
+}  // namespace ttt

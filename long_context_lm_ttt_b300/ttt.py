@@ -1,0 +1,265 @@
+"""Python binding of the C ABI in include/ttt.h (argument marshalling only).
+
+The functions below carry the C names and forward to libttt.so; every step
+of the inner loop runs in the library's CUDA kernels.  Arrays may be numpy
+arrays (host memory) or torch CUDA tensors (device memory); the library
+tells the two apart.  If libttt.so is missing the import fails loudly:
+there is no other implementation behind these names.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_float, c_int32, c_int64, c_void_p
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libttt.so")
+
+TTT_OK = 0
+TTT_ERR_INVALID = -1
+TTT_ERR_SHAPE = -2
+TTT_ERR_OOM = -3
+TTT_ERR_CUDA = -4
+TTT_ERR_NONFINITE = -5
+TTT_ERR_STATE = -6
+TTT_ERR_INTERNAL = -7
+ERR_NAMES = {0: "OK", -1: "INVALID", -2: "SHAPE", -3: "OOM", -4: "CUDA", -5: "NONFINITE",
+             -6: "STATE", -7: "INTERNAL"}
+
+TTT_BF16 = 0
+TTT_FP32_CHECK = 1
+
+EXPORTS = ("ttt_create", "ttt_prefill", "ttt_logits", "ttt_get_fast_weights", "ttt_reset",
+           "ttt_destroy", "ttt_last_error")
+
+
+class ttt_config(ctypes.Structure):
+    _fields_ = [("n_layers", c_int32), ("d_model", c_int32), ("n_heads", c_int32),
+                ("n_kv_heads", c_int32), ("head_dim", c_int32), ("d_ff", c_int32),
+                ("vocab", c_int32), ("window", c_int32), ("chunk", c_int32),
+                ("n_ttt_layers", c_int32), ("precision", c_int32), ("lr", c_float),
+                ("rope_theta", c_float), ("norm_eps", c_float), ("max_tokens", c_int64)]
+
+
+class ttt_weights(ctypes.Structure):
+    _fields_ = [("tok_embed", c_void_p), ("final_norm", c_void_p), ("lm_head", c_void_p)] + [
+        (name, POINTER(c_void_p)) for name in
+        ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down")]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libttt.so (raises OSError if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise OSError(f"{path} not found: build it with `python -m long_context_lm_ttt_b300.build`")
+    lib = ctypes.CDLL(path)
+    lib.ttt_create.argtypes = [POINTER(ttt_config), POINTER(ttt_weights), c_void_p, POINTER(c_void_p)]
+    lib.ttt_create.restype = c_int32
+    lib.ttt_prefill.argtypes = [c_void_p, c_void_p, c_int64, c_void_p, c_void_p]
+    lib.ttt_prefill.restype = c_int32
+    lib.ttt_logits.argtypes = [c_void_p, c_void_p, c_int32, c_void_p, c_void_p]
+    lib.ttt_logits.restype = c_int32
+    lib.ttt_get_fast_weights.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p]
+    lib.ttt_get_fast_weights.restype = c_int32
+    lib.ttt_reset.argtypes = [c_void_p]
+    lib.ttt_reset.restype = c_int32
+    lib.ttt_destroy.argtypes = [c_void_p]
+    lib.ttt_destroy.restype = None
+    lib.ttt_last_error.argtypes = [c_void_p]
+    lib.ttt_last_error.restype = c_char_p
+    lib.ttt_kernel_gemm.argtypes = [c_int32, c_int32, c_int32, c_void_p, c_int64, c_int32, c_void_p,
+                                    c_int64, c_int32, c_void_p, c_void_p, c_int64, c_int32, c_void_p]
+    lib.ttt_kernel_gemm.restype = c_int32
+    lib.ttt_kernel_error.argtypes = []
+    lib.ttt_kernel_error.restype = c_int32
+    _lib = lib
+    return lib
+
+
+class TTTError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERR_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def _ptr(a) -> int:
+    """Address of a numpy array (host) or torch tensor (device or host)."""
+    if a is None:
+        return 0
+    if isinstance(a, np.ndarray):
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("arrays must be C-contiguous")
+        return a.ctypes.data
+    if hasattr(a, "data_ptr"):
+        if not a.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        return a.data_ptr()
+    raise TypeError(type(a))
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return 0
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+# ---------------------------------------------------------------------------
+# the C calls, same names
+# ---------------------------------------------------------------------------
+def ttt_last_error(ctx=None) -> str:
+    m = load().ttt_last_error(ctx)
+    return m.decode() if m else ""
+
+
+def _check(rc: int, ctx=None):
+    if rc != TTT_OK:
+        raise TTTError(rc, ttt_last_error(ctx))
+
+
+def make_config(shape, precision: int = TTT_BF16, max_tokens: Optional[int] = None,
+                lr: Optional[float] = None) -> ttt_config:
+    """ttt_config from any object with the ModelShape field names."""
+    return ttt_config(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads, shape.head_dim,
+                      shape.d_ff, shape.vocab, shape.window, shape.chunk, shape.n_ttt_layers, precision,
+                      shape.lr if lr is None else lr, shape.rope_theta, shape.norm_eps,
+                      max_tokens if max_tokens is not None else shape.seq_len)
+
+
+def make_weights(w: dict):
+    """ttt_weights from a dict of fp32 arrays (numpy host or torch device);
+    returns (struct, keepalive)."""
+    keep = []
+    layers = w["layers"]
+
+    def arr(name):
+        a = (c_void_p * len(layers))(*[_ptr(lw[name]) for lw in layers])
+        keep.append(a)
+        return ctypes.cast(a, POINTER(c_void_p))
+
+    for lw in layers:
+        for v in lw.values():
+            if isinstance(v, np.ndarray) and v.dtype != np.float32:
+                raise TypeError("weights must be float32")
+    s = ttt_weights(_ptr(w["tok_embed"]), _ptr(w["final_norm"]), _ptr(w["lm_head"]),
+                    arr("attn_norm"), arr("wq"), arr("wk"), arr("wv"), arr("wo"), arr("mlp_norm"),
+                    arr("w_gate"), arr("w_up"), arr("w_down"))
+    return s, keep
+
+
+def ttt_create(cfg: ttt_config, weights: ttt_weights, stream=None) -> c_void_p:
+    ctx = c_void_p()
+    _check(load().ttt_create(ctypes.byref(cfg), ctypes.byref(weights), _stream(stream), ctypes.byref(ctx)))
+    return ctx
+
+
+def ttt_prefill(ctx, tokens, T: int, chunk_losses, stream=None) -> int:
+    rc = load().ttt_prefill(ctx, _ptr(tokens), int(T), _ptr(chunk_losses), _stream(stream))
+    _check(rc, ctx)
+    return rc
+
+
+def ttt_logits(ctx, cont, n: int, logits, stream=None) -> int:
+    rc = load().ttt_logits(ctx, _ptr(cont), int(n), _ptr(logits), _stream(stream))
+    _check(rc, ctx)
+    return rc
+
+
+def ttt_get_fast_weights(ctx, block: int, which: int, dst, stream=None) -> int:
+    rc = load().ttt_get_fast_weights(ctx, int(block), int(which), _ptr(dst), _stream(stream))
+    _check(rc, ctx)
+    return rc
+
+
+def ttt_reset(ctx) -> int:
+    rc = load().ttt_reset(ctx)
+    _check(rc, ctx)
+    return rc
+
+
+def ttt_destroy(ctx) -> None:
+    if ctx:
+        load().ttt_destroy(ctx)
+
+
+# kernel-level entry points (include/ttt_kernels.h)
+GEMM_TC, GEMM_SIMT_BF16, GEMM_SIMT_F32 = 0, 1, 2
+
+
+def ttt_kernel_gemm(M, N, K, A, lda, a_mn, B, ldb, b_mn, B2, C, ldc, impl, stream=None) -> int:
+    rc = load().ttt_kernel_gemm(int(M), int(N), int(K), _ptr(A), int(lda), int(a_mn), _ptr(B), int(ldb),
+                                int(b_mn), _ptr(B2), _ptr(C), int(ldc), int(impl), _stream(stream))
+    _check(rc)
+    return rc
+
+
+def ttt_kernel_error() -> int:
+    return int(load().ttt_kernel_error())
+
+
+# ---------------------------------------------------------------------------
+# a small object wrapper around one context
+# ---------------------------------------------------------------------------
+class TTT:
+    """One test-time-training context on the current CUDA device."""
+
+    def __init__(self, shape, weights: dict, precision: int = TTT_BF16,
+                 max_tokens: Optional[int] = None, lr: Optional[float] = None, stream=None):
+        self.shape = shape
+        self.cfg = make_config(shape, precision, max_tokens, lr)
+        ws, keep = make_weights(weights)
+        self.ctx = ttt_create(self.cfg, ws, stream)
+        del keep
+
+    def n_chunks(self, T: int) -> int:
+        return -(-T // self.cfg.chunk)
+
+    def prefill(self, tokens, chunk_losses=None, stream=None):
+        """Run the inner loop; returns the chunk losses (numpy for host
+        tokens, else the given / a new float32 CUDA tensor)."""
+        T = len(tokens)
+        if chunk_losses is None:
+            if isinstance(tokens, np.ndarray):
+                chunk_losses = np.zeros(self.n_chunks(T), np.float32)
+            else:
+                import torch
+                chunk_losses = torch.zeros(self.n_chunks(T), dtype=torch.float32, device=tokens.device)
+        ttt_prefill(self.ctx, tokens, T, chunk_losses, stream)
+        return chunk_losses
+
+    def logits(self, cont, out=None, stream=None):
+        n = len(cont)
+        if out is None:
+            out = np.zeros((n, self.cfg.vocab), np.float32)
+        ttt_logits(self.ctx, cont, n, out, stream)
+        return out
+
+    def fast_weights(self, block: int) -> dict:
+        d, ff = self.cfg.d_model, self.cfg.d_ff
+        out = {}
+        for which, name, shp in ((0, "w_gate", (ff, d)), (1, "w_up", (ff, d)), (2, "w_down", (d, ff))):
+            a = np.zeros(shp, np.float32)
+            ttt_get_fast_weights(self.ctx, block, which, a)
+            out[name] = a
+        return out
+
+    def reset(self):
+        ttt_reset(self.ctx)
+
+    def close(self):
+        if self.ctx:
+            ttt_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

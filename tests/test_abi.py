@@ -1,0 +1,81 @@
+"""The C-ABI library without a GPU: it loads, exports every call that
+include/ttt.h declares, the ctypes mirrors match the C structs, and argument
+checks that run before any device work return their error codes."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from long_context_lm_ttt_b300 import inputs
+from long_context_lm_ttt_b300 import ttt as T
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^\s*(?:int|void|const char\*)\s+(ttt_\w+)\s*\(", src, re.M))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(T.LIB_PATH):
+        from long_context_lm_ttt_b300 import build
+        build.build()
+    return T.load()
+
+
+def test_exports_every_declared_call(lib):
+    declared = _declared()
+    assert set(T.EXPORTS) <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_struct_layout():
+    assert ctypes.sizeof(T.ttt_config) == 11 * 4 + 3 * 4 + 8
+    assert T.ttt_config.max_tokens.offset == 56
+    assert ctypes.sizeof(T.ttt_weights) == 12 * ctypes.sizeof(ctypes.c_void_p)
+
+
+def _cfg(**kw):
+    c = T.make_config(inputs.shape("tiny"), T.TTT_FP32_CHECK)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(precision=7), T.TTT_ERR_INVALID),
+    (dict(n_layers=0), T.TTT_ERR_INVALID),
+    (dict(n_ttt_layers=3), T.TTT_ERR_INVALID),
+    (dict(n_kv_heads=3), T.TTT_ERR_SHAPE),
+    (dict(head_dim=31), T.TTT_ERR_SHAPE),
+    (dict(lr=float("nan")), T.TTT_ERR_NONFINITE),
+    (dict(lr=float("inf")), T.TTT_ERR_NONFINITE),
+    (dict(max_tokens=0), T.TTT_ERR_INVALID),
+])
+def test_create_rejects_bad_config(lib, kw, code):
+    ws = T.ttt_weights()
+    ctx = ctypes.c_void_p()
+    rc = lib.ttt_create(ctypes.byref(_cfg(**kw)), ctypes.byref(ws), None, ctypes.byref(ctx))
+    assert rc == code
+    assert not ctx.value
+    assert T.ttt_last_error(None) != ""
+
+
+def test_null_arguments(lib):
+    ctx = ctypes.c_void_p()
+    assert lib.ttt_create(None, None, None, ctypes.byref(ctx)) == T.TTT_ERR_INVALID
+    assert lib.ttt_create(ctypes.byref(_cfg()), None, None, None) == T.TTT_ERR_INVALID
+    assert lib.ttt_prefill(None, None, 0, None, None) == T.TTT_ERR_INVALID
+    assert lib.ttt_logits(None, None, 1, None, None) == T.TTT_ERR_INVALID
+    assert lib.ttt_get_fast_weights(None, 0, 0, None, None) == T.TTT_ERR_INVALID
+    assert lib.ttt_reset(None) == T.TTT_ERR_INVALID
+    lib.ttt_destroy(None)

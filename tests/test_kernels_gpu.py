@@ -1,0 +1,90 @@
+"""Unit tests of single CUDA kernels through the kernel-level C entry points
+(include/ttt_kernels.h), against float64 products computed on the CPU."""
+import numpy as np
+import pytest
+
+from long_context_lm_ttt_b300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _env():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from long_context_lm_ttt_b300 import ttt as T
+    T.load()
+    return torch, T
+
+
+def _operand(rng, rows, cols, mn, bf16=True):
+    """Logical [rows (M or N), cols (K)] operand and its storage."""
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    if bf16:
+        x = inputs.round_bf16(x)
+    store = np.ascontiguousarray(x.T) if mn else x      # mn: stored [K, rows]
+    return x.astype(np.float64), store
+
+
+SHAPES = [(128, 128, 64), (256, 384, 192), (100, 200, 96), (32, 128, 32), (130, 258, 70),
+          (1024, 3072, 1024), (512, 512, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("impl", [0, 1])
+def test_gemm_bf16(M, N, K, a_mn, b_mn, impl):
+    torch, T = _env()
+    if impl == 1 and M * N * K > 2 ** 28:
+        pytest.skip("SIMT reference only on the small shapes")
+    rng = np.random.default_rng(M * 7 + N * 3 + K + 11 * a_mn + 5 * b_mn)
+    a, a_st = _operand(rng, M, K, a_mn)
+    b, b_st = _operand(rng, N, K, b_mn)
+    ref = a @ b.T
+    dA = torch.from_numpy(a_st).to(torch.bfloat16).cuda()
+    dB = torch.from_numpy(b_st).to(torch.bfloat16).cuda()
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    lda = M if a_mn else K
+    ldb = N if b_mn else K
+    if impl == 0 and (lda % 8 or ldb % 8):
+        pytest.skip("TMA needs 16-byte row pitch")
+    T.ttt_kernel_gemm(M, N, K, dA, lda, a_mn, dB, ldb, b_mn, None, C, N, impl)
+    torch.cuda.synchronize()
+    assert T.ttt_kernel_error() == 0
+    got = C.cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err          # fp32 accumulation of exact bf16 products
+
+
+@pytest.mark.parametrize("impl", [0, 1])
+@pytest.mark.parametrize("b_mn", [0, 1])
+def test_gemm_dual_b(impl, b_mn):
+    """C = A B^T + A B2^T (the hi + lo fast-weight pair)."""
+    torch, T = _env()
+    M, N, K = 200, 384, 320
+    rng = np.random.default_rng(3)
+    a, a_st = _operand(rng, M, K, 0)
+    b, b_st = _operand(rng, N, K, b_mn)
+    b2, b2_st = _operand(rng, N, K, b_mn)
+    ref = a @ b.T + a @ b2.T
+    cu = lambda x: torch.from_numpy(x).to(torch.bfloat16).cuda()
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    T.ttt_kernel_gemm(M, N, K, cu(a_st), K, 0, cu(b_st), N if b_mn else K, b_mn, cu(b2_st), C, N, impl)
+    torch.cuda.synchronize()
+    assert T.ttt_kernel_error() == 0
+    err = np.abs(C.cpu().numpy() - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err
+
+
+def test_gemm_fp32_simt():
+    torch, T = _env()
+    M, N, K = 70, 130, 50
+    rng = np.random.default_rng(4)
+    a = rng.standard_normal((M, K)).astype(np.float32)
+    b = rng.standard_normal((K, N)).astype(np.float32)      # MN-major B
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    T.ttt_kernel_gemm(M, N, K, torch.from_numpy(a).cuda(), K, 0, torch.from_numpy(b).cuda(), N, 1, None,
+                      C, N, 2)
+    torch.cuda.synchronize()
+    ref = a.astype(np.float64) @ b.astype(np.float64)
+    assert np.abs(C.cpu().numpy() - ref).max() / np.abs(ref).max() < 1e-5
