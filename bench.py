@@ -1,0 +1,365 @@
+#!/usr/bin/env python3
+"""Throughput of the TTT-E2E test-time inner loop (prefill) on one B300.
+
+A step is one full pass of the inner loop over one synthetic sequence: reset
+the context (initial fast weights, empty key/value ring), then ttt_prefill over
+T tokens, i.e. for every chunk of b tokens the forward pass, the next-token
+cross-entropy, the backward into the fast MLPs and their SGD step.  The
+default workload is the 3B-class model at T = 131072 (window 8192, chunk 1024,
+the MLPs of the last 7 of 28 blocks are fast), with seeded N(0, 0.02) weights
+rounded to bf16 and Zipf(1.1) token ids.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is tokens/s over all ranks with the
+inputs already resident on the device; `e2e` repeats the measurement through
+the same C call with host (pinned) token and loss buffers, so the copies are
+inside the timed region.  With N > 1 (torchrun) every rank runs its own
+sequence (independent replicas: the chunk loop of one sequence is a strict
+dependency chain and there is nothing to exchange).
+
+`--impl reference` times the plain CPU oracle on the host cores on a bounded
+sample of the same workload (the only other implementation of this method).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from long_context_lm_ttt_b300 import inputs  # noqa: E402
+
+METRIC = "TTT-E2E prefill tokens/s at 3B, 128K ctx on 1 B300; % of dense BF16 peak"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="3b", choices=sorted(inputs.SHAPES))
+    ap.add_argument("--T", type=int, default=None, help="sequence length (default: the config's)")
+    ap.add_argument("--lr", type=float, default=None, help="override the SGD step (0: plain SWA forward)")
+    ap.add_argument("--cpu-tokens", type=int, default=None,
+                    help="tokens the oracle is timed on (default: one chunk, 256 at 3B)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile", choices=["timed", "off"], default="timed",
+                    help="per-launch CUDA events over the timed region (roofline), or none")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    rows.append((float(p[1]), float(p[2]), float(p[3]), p[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        pmax = max(r[2] for r in rows)
+        load = [r for r in rows if r[2] >= 0.5 * pmax] or rows
+        reasons = sorted({self.REASONS[i] for r in load for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": pmax}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+def workload(args, rank=0):
+    s = inputs.shape(args.config)
+    if args.T is not None:
+        s = s.replace(seq_len=args.T)
+    if args.lr is not None:
+        s = s.replace(lr=args.lr)
+    tok = inputs.make_tokens(s, seed=1 + rank)
+    return s, tok
+
+
+def workload_name(s):
+    return (f"{s.name} TTT-E2E prefill: L={s.n_layers} d={s.d_model} H={s.n_heads}/{s.n_kv_heads}x{s.head_dim} "
+            f"ff={s.d_ff} V={s.vocab} W={s.window} b={s.chunk} T={s.seq_len} fast={s.n_ttt_layers} lr={s.lr}")
+
+
+def cpu_baseline(s, w, tok, n_tokens):
+    """The oracle as it stands, timed on the host cores over the first
+    n_tokens positions (a prefix of the first chunk, or whole chunks)."""
+    from oracle import ttt_ref as O
+    try:
+        import psutil
+        avail = psutil.virtual_memory().available
+    except Exception:
+        avail = 1 << 62
+    dtype = np.float64 if avail > 3.2 * 8 * inputs.n_params(s) else np.float32
+    cfg = O.OracleConfig.from_mapping(s.as_dict())
+    t0 = time.perf_counter()
+    O.prefill(cfg, w, tok[:n_tokens], dtype=dtype)
+    dt = time.perf_counter() - t0
+    n_ch = -(-n_tokens // s.chunk)
+    return {"value": n_tokens / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"first {n_tokens} tokens of the sequence ({n_ch} chunk(s) of the {s.name} workload, "
+                      f"same weights and ids), {np.dtype(dtype).name} numpy, {dt:.1f} s"}
+
+
+def default_cpu_tokens(s):
+    return 256 if s.d_model >= 3072 else (s.chunk if s.d_model >= 1536 else min(s.seq_len, 4 * s.chunk))
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    """--impl reference: the CPU oracle, each step a bounded sample."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    s, tok = workload(args)
+    w = inputs.make_weights(s)
+    n = args.cpu_tokens or default_cpu_tokens(s)
+    times = []
+    base = None
+    for i in range(args.warmup + args.steps):
+        b = cpu_baseline(s, w, tok, n)
+        if i >= args.warmup:
+            times.append(n / b["value"])
+            base = b
+    total = sum(times)
+    v = n * args.steps / total
+    base["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_name(s), "global_batch": 1,
+                                            "seq_len": s.seq_len, "sample_tokens": n},
+            "cpu_baseline": base,
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def roofline(prof, peaks, peak_src):
+    dom = max(prof.items(), key=lambda kv: kv[1]["ms"])
+    name, st = dom
+    if st["launches"] == 0 or st["ms"] <= 0:
+        return None, dom
+    sec = st["ms"] / 1e3
+    if st["flops"] > 0:
+        ach = st["flops"] / sec / 1e12
+        pk = peaks["bf16_tflops_sustained"]
+        r = {"bound": "tensor", "achieved": ach, "peak": pk, "unit": "TFLOP/s", "frac": ach / pk}
+    else:
+        ach = st["bytes"] / sec / 1e9
+        pk = peaks["hbm_gbs"]
+        r = {"bound": "hbm", "achieved": ach, "peak": pk, "unit": "GB/s", "frac": ach / pk}
+    r.update({"traffic": None, "kernel": name, "launches": st["launches"],
+              "avg_launch_ms": st["ms"] / st["launches"],
+              "peak_source": f"{peak_src} ({'sustained bf16' if r['bound'] == 'tensor' else 'copy'})"})
+    return r, dom
+
+
+def run_ours(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from long_context_lm_ttt_b300 import ttt as TT
+    TT.load()
+    peaks, peak_src = load_peaks()
+
+    s, tok = workload(args, rank)
+    T = s.seq_len
+    nC = s.n_chunks
+    t_setup = time.perf_counter()
+    w = inputs.make_weights(s)
+    m = TT.TTT(s, w, TT.TTT_BF16, max_tokens=T)
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if not want_cpu:
+        del w
+    t_setup = time.perf_counter() - t_setup
+
+    tok_d = torch.from_numpy(tok).cuda()
+    loss_d = torch.zeros(nC, dtype=torch.float32, device="cuda")
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def step(tk, ls):
+        m.reset()
+        m.prefill(tk, ls)
+
+    for _ in range(args.warmup):
+        step(tok_d, loss_d)
+    losses = loss_d.cpu().numpy()
+    if not np.all(np.isfinite(losses)):
+        raise SystemExit(f"non-finite chunk losses: {losses}")
+
+    uuid = str(torch.cuda.get_device_properties(local).uuid)
+    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    if args.profile == "timed":
+        m.profile(True)
+    barrier()
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(args.steps):
+        step(tok_d, loss_d)
+    ev1.record()
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    prof = m.profile_read() if args.profile == "timed" else None
+    m.profile(False)
+    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    value = world * T * args.steps / (ms_max / 1e3)
+
+    # end to end through the same call with host buffers (pinned)
+    e2e = None
+    if not args.no_e2e:
+        tok_h = torch.from_numpy(tok).pin_memory()
+        loss_h = torch.zeros(nC, dtype=torch.float32).pin_memory()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step(tok_h, loss_h)
+        barrier()
+        dt = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device="cuda")
+        if dist is not None:
+            dist.all_reduce(dt, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * T * args.steps / float(dt.item()), "unit": UNIT,
+               "h2d_bytes_per_step": int(tok_h.numel() * 4), "d2h_bytes_per_step": int(loss_h.numel() * 4)}
+
+    fl = inputs.flops_per_sequence(s)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_name(s), "global_batch": world, "seq_len": T,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (every chunk streams all weights, 6+ GB at 3B)"},
+        "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"), "reasons": clk.get("reasons")},
+        "e2e": e2e,
+        "model_tflops": fl["total"] * world * args.steps / (ms_max / 1e3) / 1e12,
+        "frac_of_peak": {"burst": fl["total"] * world * args.steps / (ms_max / 1e3) / 1e12 / peaks["bf16_tflops"],
+                         "sustained": fl["total"] * world * args.steps / (ms_max / 1e3) / 1e12
+                         / peaks["bf16_tflops_sustained"], "peaks": peak_src},
+        "setup_s": t_setup,
+    }
+    if prof is not None:
+        rl, _ = roofline(prof, peaks, peak_src)
+        line["roofline"] = rl
+        line["gpu_launches"] = int(sum(v["launches"] for v in prof.values()))
+        tot = sum(v["ms"] for v in prof.values()) or 1.0
+        line["kernels"] = {k: {"launches": v["launches"], "ms_per_step": v["ms"] / args.steps,
+                               "share": v["ms"] / tot,
+                               "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["ms"] > 0 and v["flops"] else None,
+                               "gbs": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["ms"] > 0 else None}
+                           for k, v in prof.items() if v["launches"]}
+    if want_cpu:
+        n = args.cpu_tokens or default_cpu_tokens(s)
+        line["cpu_baseline"] = cpu_baseline(s, w, tok, n)
+    m.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -133,6 +133,39 @@ int ttt_get_fast_weights(ttt_ctx* ctx, int32_t block, int32_t which, float* dst,
  * Synchronous. */
 int ttt_reset(ttt_ctx* ctx);
 
+/* Per-launch timing of the kernels of the loop, by kernel class.  With
+ * profiling on, every kernel launch of ttt_prefill / ttt_logits is
+ * bracketed by two CUDA events on the call's stream; the pairs are resolved
+ * when the call synchronises and summed per class:
+ *   "gemm_fwd"      projections of the forward (q/k/v + RoPE + ring write,
+ *                   output + residual, gate/up + SwiGLU, down + residual)
+ *   "gemm_lm_head"  the streamed lm_head products of the cross-entropy
+ *   "gemm_bwd_dx"   input-gradient products of the backward
+ *   "gemm_dw_sgd"   weight-gradient products with the fused SGD step
+ *   "attn_fwd"      sliding-window attention forward
+ *   "attn_bwd"      chunk-local attention backward
+ *   "rowwise"       embedding, norms, softmax statistics, RoPE backward
+ * `flops` counts 2 per multiply-add of the operation as defined (attention:
+ * unmasked query/key pairs only; no recomputation, no padding), `bytes`
+ * the operands read once and results written once.  The events add a few
+ * microseconds per launch on the host; device time is unaffected apart
+ * from the gaps they leave between kernels. */
+typedef struct ttt_kernel_stat {
+  char name[24];
+  int64_t launches;
+  double ms;    /* summed event-to-event device time */
+  double flops; /* algorithmic FLOPs of those launches */
+  double bytes; /* algorithmic bytes of those launches */
+} ttt_kernel_stat;
+
+/* Switch per-launch timing on (on != 0) or off; clears the counters. */
+int ttt_profile(ttt_ctx* ctx, int32_t on);
+
+/* Copy up to `cap` class records (in the order listed above) into out and
+ * set *n_out to the number of classes.  Counters accumulate over calls
+ * until ttt_profile() is called again. */
+int ttt_profile_read(ttt_ctx* ctx, ttt_kernel_stat* out, int32_t cap, int32_t* n_out);
+
 /* Free everything owned by ctx (NULL is ignored). */
 void ttt_destroy(ttt_ctx* ctx);
 

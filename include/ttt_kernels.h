@@ -32,6 +32,32 @@ int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda,
                     const void* B, int64_t ldb, int32_t b_mn, const void* B2, float* C, int64_t ldc,
                     int32_t impl, void* stream);
 
+/* Sliding-window causal attention of one chunk, the attention core of the
+ * decoder block (query t sees keys j with t - W < j <= t; grouped KV heads:
+ * query head h reads KV head h / (H/Hkv)).  All matrices bf16, device memory:
+ *   q     [n, H*hd]        queries of chunk positions pos0 .. pos0+n-1
+ *   kring [Hkv, R, hd]     keys by ring slot (position p in slot p mod R)
+ *   vring [Hkv, R, hd]     values, same layout
+ *   o     [n, H*hd]        output (forward) / forward output (backward)
+ *   lse   [H, ld_lse]      fp32 log-sum-exp per (head, row): written by
+ *                          the forward, read by the backward
+ *   dout  [n, H*hd]        gradient of o (backward)
+ *   dqkv  [n, (H+2Hkv)*hd] backward output: dq | dk | dv; dk and dv are the
+ *                          gradients of the chunk's own keys and values
+ *                          (earlier positions are constants), summed over
+ *                          the query heads of each KV head
+ *   dsum  [H, ld_lse]      fp32 scratch of the backward (rowsum(dO * O))
+ * R must cover W + n - 1 positions.  impl 0: tcgen05 tensor cores
+ * (64 <= hd <= 128, hd % 16 == 0, R % 128 == 0, 16-byte aligned bases,
+ * else TTT_ERR_SHAPE); impl 1: SIMT fp32 arithmetic. */
+int ttt_kernel_attn_fwd(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R,
+                        int64_t pos0, const void* q, const void* kring, const void* vring, void* o, float* lse,
+                        int32_t ld_lse, void* stream);
+int ttt_kernel_attn_bwd(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R,
+                        int64_t pos0, const void* q, const void* kring, const void* vring, const void* o,
+                        const float* lse, int32_t ld_lse, const void* dout, float* dsum, void* dqkv,
+                        void* stream);
+
 /* Error word of the tensor-core kernels launched through this header since
  * the last call (0 = none; otherwise the code of a bounded wait that gave
  * up).  Synchronises the device. */

@@ -1,8 +1,1235 @@
-// attn_tc.cu — tensor-core sliding-window attention (placeholder until the
-// tensor-core kernels land): reports "not supported".
+// attn_tc.cu — sliding-window causal attention on the 5th-generation tensor
+// cores (tcgen05), forward and chunk-local backward, bf16 in / fp32 math.
+//
+// Geometry shared by every kernel here:
+//   * a query tile is 128 consecutive rows of the chunk (one TMEM lane per
+//     row); a key block is BN = 64 consecutive absolute positions starting
+//     at a multiple of 64, so its ring slots (p mod R, R a multiple of 128)
+//     are contiguous and one TMA box fetches it;
+//   * query t (absolute) sees keys j with t - W < j <= t; key blocks that
+//     straddle either edge are masked element-wise, interior blocks are not;
+//   * head_dim hd <= 128 is split into 64-wide "atoms" of 128 bytes, the
+//     unit of the 128-byte swizzle shared by TMA and the MMA descriptors.
+//     With hd = 96 the second atom's upper half is zero (key/value maps end
+//     at hd) or ignored (q/o/dO rows: the MMA reads hd/16 K-steps only).
+//
+// Forward, one CTA per (query tile, head), 6 warps:
+//   warp 0    TMA producer: Q once, then K and V blocks into a 2-stage ring;
+//   warp 1    TMEM owner and MMA issuer: S_i = Q K_i^T into one of two
+//             64-column TMEM buffers, then O += P_i V_i (O in TMEM);
+//   warps 2-5 softmax, one query row per thread: read S_i, mask, online
+//             max with lazy rescaling of O (only when the running max grows
+//             by more than 2^8), write P_i (bf16) into shared memory in the
+//             swizzled K-major layout the MMA reads, and at the end scale O
+//             by 1/l and store it with the row's log-sum-exp.
+// S_{i+1} is issued before P_i V_i so the tensor core works on the next
+// scores while the softmax warps work on the current ones.  Two CTAs fit on
+// one SM (112 KB shared memory, 256 TMEM columns each).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace ttt {
-int attn_fwd_tc(const AttnArgs&, cudaStream_t) { return (int)cudaErrorNotSupported; }
-int attn_bwd_tc(const AttnArgs&, cudaStream_t) { return (int)cudaErrorNotSupported; }
+namespace {
+
+constexpr int BM = 128;   // query rows per tile
+constexpr int BN = 64;    // keys per block
+constexpr int STAGES = 2; // key/value ring depth
+
+enum : int {
+  ERR_A_PROD = 201,
+  ERR_A_MMA = 202,
+  ERR_A_SOFT = 203,
+};
+
+// shared-memory map of the forward kernel for NA head-dim atoms
+template <int NA>
+struct FwdSmem {
+  static constexpr int Q_BYTES = NA * BM * 128;
+  static constexpr int KV_BYTES = NA * BN * 128;
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + Q_BYTES;
+  static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
+  static constexpr int P_OFF = V_OFF + STAGES * KV_BYTES;
+  static constexpr int BAR_OFF = P_OFF + P_BYTES;
+  static constexpr int SMEM = BAR_OFF + 256;
+};
+
+struct FwdParams {
+  int n, H, Hkv, hd, W, R;
+  long long pos0;
+  float scale_log2;  // log2(e) / sqrt(hd)
+  bf16* o;
+  int64_t ldo;
+  float* lse;
+  int ld_lse;
+  int* err;
+};
+
+// first key block and block count of the query tile starting at row r0
+__device__ __forceinline__ void tile_blocks(const FwdParams& p, int r0, long long* kb0, int* nb) {
+  const long long t_lo = p.pos0 + r0;
+  const long long t_hi = p.pos0 + min(r0 + BM, p.n) - 1;
+  long long k_lo = t_lo - p.W + 1;
+  if (k_lo < 0) k_lo = 0;
+  *kb0 = k_lo / BN;
+  *nb = (int)(t_hi / BN - *kb0 + 1);
+}
+
+// every lane waits on the barrier; the warp agrees on the outcome so that
+// warp-collective tcgen05 instructions are reached by all lanes or none
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err, int code,
+                                          volatile int* abort) {
+  const bool ok = tc::mbar_wait(bar, parity, err, code, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// one row of 64 bf16 values into a 128-byte-swizzled K-major tile
+__device__ __forceinline__ void store_row_sw128(uint32_t tile, int row, const float (&p)[64]) {
+  const uint32_t base = tile + row * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t addr = base + ((c ^ (row & 7)) << 4);
+    st_shared_v4(addr, pack_bf16(p[8 * c + 0], p[8 * c + 1]), pack_bf16(p[8 * c + 2], p[8 * c + 3]),
+                 pack_bf16(p[8 * c + 4], p[8 * c + 5]), pack_bf16(p[8 * c + 6], p[8 * c + 7]));
+  }
+}
+
+template <int NA>
+__global__ void __launch_bounds__(192, 2)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                       const __grid_constant__ CUtensorMap mapV, FwdParams p) {
+  using SM = FwdSmem<NA>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t bar0 = sbase + SM::BAR_OFF;
+  // barriers (8 bytes each)
+  const uint32_t q_full = bar0;
+  const uint32_t k_full = bar0 + 8;          // [2]
+  const uint32_t v_full = bar0 + 24;         // [2]
+  const uint32_t kv_empty = bar0 + 40;       // [2]
+  const uint32_t s_full = bar0 + 56;         // [2]
+  const uint32_t s_empty = bar0 + 72;        // [2]
+  const uint32_t p_full = bar0 + 88;
+  const uint32_t o_done = bar0 + 96;
+  uint32_t* tmem_slot = (uint32_t*)(smem + SM::BAR_OFF + 128);
+  volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 132);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x, h = blockIdx.y;
+  const int r0 = qt * BM;
+  const int kvh = h / (p.H / p.Hkv);
+  long long kb0;
+  int nb;
+  tile_blocks(p, r0, &kb0, &nb);
+  const int ksteps = p.hd / 16;
+  const int nO = (p.hd + 15) & ~15;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(k_full + 8 * s, 1);
+      tc::mbar_init(v_full + 8 * s, 1);
+      tc::mbar_init(kv_empty + 8 * s, 1);
+      tc::mbar_init(s_full + 8 * s, 1);
+      tc::mbar_init(s_empty + 8 * s, 128);
+    }
+    tc::mbar_init(p_full, 128);
+    tc::mbar_init(o_done, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&mapQ);
+    tc::prefetch_tmap(&mapK);
+    tc::prefetch_tmap(&mapV);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem;          // two 64-column score buffers
+  const uint32_t tO = tmem + 128;    // output accumulator (nO columns)
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      bool ok = true;
+      int issued = 0;
+      tc::mbar_arrive_expect_tx(q_full, SM::Q_BYTES);
+      for (int a = 0; a < NA; ++a)
+        tc::tma_load_2d(sbase + SM::Q_OFF + a * BM * 128, &mapQ, h * p.hd + 64 * a, r0, q_full);
+      for (int i = 0; i < nb && ok; ++i) {
+        const int st = i & 1;
+        if (!tc::mbar_wait(kv_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
+          ok = false;
+          break;
+        }
+        const long long kpos = (kb0 + i) * BN;
+        const int row = kvh * p.R + (int)(kpos % p.R);
+        tc::mbar_arrive_expect_tx(k_full + 8 * st, SM::KV_BYTES);
+        for (int a = 0; a < NA; ++a)
+          tc::tma_load_2d(sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN * 128, &mapK, 64 * a, row,
+                          k_full + 8 * st);
+        tc::mbar_arrive_expect_tx(v_full + 8 * st, SM::KV_BYTES);
+        for (int a = 0; a < NA; ++a)
+          tc::tma_load_2d(sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN * 128, &mapV, 64 * a, row,
+                          v_full + 8 * st);
+        issued = i + 1;
+      }
+      // let copies in flight land before the CTA can exit
+      const long long t0 = clock64();
+      while (!tc::mbar_try_wait(q_full, 0) && clock64() - t0 < tc::kWaitClocks) {
+      }
+      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
+        const int st = i & 1;
+        const uint32_t par = (i >> 1) & 1;
+        const long long t1 = clock64();
+        while (!(tc::mbar_try_wait(k_full + 8 * st, par) && tc::mbar_try_wait(v_full + 8 * st, par)) &&
+               clock64() - t1 < tc::kWaitClocks) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      const uint32_t idS = tc::idesc_bf16(BM, BN, 0, 0);
+      const uint32_t idO = tc::idesc_bf16(BM, nO, 0, 1);
+      bool ok = tc::mbar_wait(q_full, 0, p.err, ERR_A_MMA, abort);
+      bool issued = false;
+      for (int i = 0; i <= nb && ok; ++i) {
+        if (i < nb) {
+          const int st = i & 1;
+          const uint32_t par = (i >> 1) & 1;
+          if (!tc::mbar_wait(k_full + 8 * st, par, p.err, ERR_A_MMA, abort) ||
+              !tc::mbar_wait(s_empty + 8 * st, par ^ 1, p.err, ERR_A_MMA, abort)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t kb = sbase + SM::K_OFF + st * SM::KV_BYTES;
+          for (int j = 0; j < ksteps; ++j) {
+            const int a = j >> 2;
+            const uint64_t ad = tc::smem_desc_sw128(sbase + SM::Q_OFF + a * BM * 128 + 32 * (j & 3), 16, 1024);
+            const uint64_t bd = tc::smem_desc_sw128(kb + a * BN * 128 + 32 * (j & 3), 16, 1024);
+            tc::mma_bf16(tS + st * BN, ad, bd, idS, j > 0);
+          }
+          issued = true;
+          tc::mma_commit(s_full + 8 * st);
+        }
+        if (i >= 1) {
+          const int k = i - 1;
+          const int st = k & 1;
+          if (!tc::mbar_wait(v_full + 8 * st, (k >> 1) & 1, p.err, ERR_A_MMA, abort) ||
+              !tc::mbar_wait(p_full, k & 1, p.err, ERR_A_MMA, abort)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t vb = sbase + SM::V_OFF + st * SM::KV_BYTES;
+#pragma unroll
+          for (int j = 0; j < BN / 16; ++j) {
+            const uint64_t ad = tc::smem_desc_sw128(sbase + SM::P_OFF + 32 * j, 16, 1024);
+            const uint64_t bd = tc::smem_desc_sw128(vb + 2048 * j, BN * 128, 1024);
+            tc::mma_bf16(tO, ad, bd, idO, (k > 0 || j > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(o_done);
+          tc::mma_commit(kv_empty + 8 * st);
+        }
+      }
+      if (!ok && issued) {
+        // drain MMAs in flight before TMEM is released
+        const uint32_t drain = bar0 + 104;
+        tc::mbar_init(drain, 1);
+        tc::fence_mbar_init();
+        tc::mma_commit(drain);
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(drain, 0) && clock64() - t0 < tc::kWaitClocks) {
+        }
+      }
+    }
+  } else {
+    // ---------------- softmax (warps 2..5) ----------------
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;           // TMEM lane / tile row
+    const long long t = p.pos0 + r0 + row;         // absolute position
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const float NEG_INF = -INFINITY;
+    float m_run = NEG_INF, l_run = 0.f;
+    bool ok = true;
+    for (int i = 0; i < nb; ++i) {
+      const int st = i & 1;
+      if (!warp_wait(s_full + 8 * st, (i >> 1) & 1, p.err, ERR_A_SOFT, abort)) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      float s[64];
+      {
+        float (&s0)[32] = *reinterpret_cast<float(*)[32]>(&s[0]);
+        float (&s1)[32] = *reinterpret_cast<float(*)[32]>(&s[32]);
+        tc::tmem_ld32(tS + st * BN + lane_off, s0);
+        tc::tmem_ld32(tS + st * BN + 32 + lane_off, s1);
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(s_empty + 8 * st);
+      // valid columns c: t - W < kpos + c <= t
+      const long long kpos = (kb0 + i) * BN;
+      const long long lo = t - p.W + 1 - kpos, hi = t - kpos;
+      float mb = NEG_INF;
+      if (lo <= 0 && hi >= BN - 1) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          s[c] *= p.scale_log2;
+          mb = fmaxf(mb, s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          s[c] = (c >= lo && c <= hi) ? s[c] * p.scale_log2 : NEG_INF;
+          mb = fmaxf(mb, s[c]);
+        }
+      }
+      // lazy rescaling: the reference max only moves when it must
+      const bool grow = mb > m_run + 8.0f;
+      const float m_new = grow ? mb : m_run;
+      const float alpha = (grow && m_run != NEG_INF) ? exp2f(m_run - m_new) : 1.0f;
+      const float m_use = m_new == NEG_INF ? 0.f : m_new;
+      float ls = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        s[c] = exp2f(s[c] - m_use);
+        ls += s[c];
+      }
+      l_run = l_run * alpha + ls;
+      m_run = m_new;
+      // P V of the previous block must be done: it reads the P buffer and
+      // accumulates into the O that may need rescaling
+      if (i > 0) {
+        if (!warp_wait(o_done, (i - 1) & 1, p.err, ERR_A_SOFT, abort)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+          for (int c0 = 0; c0 < nO; c0 += 32) {
+            float v[32];
+            tc::tmem_ld32(tO + c0 + lane_off, v);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] *= alpha;
+            tmem_st32(tO + c0 + lane_off, v);
+          }
+        }
+      }
+      store_row_sw128(sbase + SM::P_OFF, row, s);
+      fence_proxy_async_smem();
+      tc::tc_fence_before();
+      tc::mbar_arrive(p_full);
+    }
+    // ---------------- epilogue ----------------
+    if (ok && warp_wait(o_done, (nb - 1) & 1, p.err, ERR_A_SOFT, abort)) {
+      tc::tc_fence_after();
+      const int grow_ = r0 + row;
+      const float il = 1.0f / l_run;
+      for (int c0 = 0; c0 < nO; c0 += 32) {
+        float v[32];
+        tc::tmem_ld32(tO + c0 + lane_off, v);
+        if (grow_ < p.n) {
+          bf16* dst = p.o + (int64_t)grow_ * p.ldo + (int64_t)h * p.hd + c0;
+#pragma unroll
+          for (int k = 0; k < 32; k += 8) {
+            if (c0 + k < p.hd) {
+              uint4 u;
+              u.x = pack_bf16(v[k] * il, v[k + 1] * il);
+              u.y = pack_bf16(v[k + 2] * il, v[k + 3] * il);
+              u.z = pack_bf16(v[k + 4] * il, v[k + 5] * il);
+              u.w = pack_bf16(v[k + 6] * il, v[k + 7] * il);
+              *reinterpret_cast<uint4*>(dst + k) = u;
+            }
+          }
+        }
+      }
+      if (grow_ < p.n) p.lse[(int64_t)h * p.ld_lse + grow_] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 256);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// backward
+//
+//   D[t]   = sum_d dO[t,d] O[t,d]                          (attn_bwd_prep)
+//   P      = exp(q.k / sqrt(hd) - lse[t])   (masked to the band)
+//   dS     = P (dO.v - D[t]) / sqrt(hd)
+//   dq[t]  = sum_j dS[t,j] k_j        over the whole window  (dq kernel)
+//   dk[j]  = sum_t dS[t,j] q_t,  dv[j] = sum_t P[t,j] dO_t
+//            for the chunk's own keys only                   (dkv kernel)
+// The dq kernel may split a tile's key range into `parts` (more CTAs than
+// SMs for short chunks); partial sums go to fp32 scratch and a reduction
+// adds them in a fixed order, so results are deterministic.  The dkv kernel
+// works per query head; a second reduction sums the heads of each KV group.
+// ---------------------------------------------------------------------------
+struct BwdParams {
+  int n, H, Hkv, hd, W, R;
+  long long pos0;
+  float scale_log2;  // log2(e) / sqrt(hd)
+  float scale;       // 1 / sqrt(hd)
+  const float* lse;  // [H][ld_lse]
+  const float* dsum; // [H][ld_lse]
+  int ld_lse;
+  int parts;
+  bf16* dqkv;
+  int64_t ldg;
+  float* ws;
+  int* err;
+};
+
+__device__ __forceinline__ void store_row_sw128_pk(uint32_t tile, int row, const uint32_t (&pk)[32]) {
+  const uint32_t base = tile + row * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    st_shared_v4(base + ((c ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+}
+
+template <int NA>
+struct DqSmem {
+  static constexpr int Q_BYTES = NA * BM * 128;
+  static constexpr int KV_BYTES = NA * BN * 128;
+  static constexpr int DS_BYTES = BM * BN * 2;
+  static constexpr int Q_OFF = 0;
+  static constexpr int DO_OFF = Q_OFF + Q_BYTES;
+  static constexpr int K_OFF = DO_OFF + Q_BYTES;
+  static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
+  static constexpr int DS_OFF = V_OFF + STAGES * KV_BYTES;
+  static constexpr int BAR_OFF = DS_OFF + 2 * DS_BYTES;
+  static constexpr int SMEM = BAR_OFF + 256;
+};
+
+__device__ __forceinline__ void bwd_tile_blocks(const BwdParams& p, int r0, long long* kb0, int* nb) {
+  const long long t_lo = p.pos0 + r0;
+  const long long t_hi = p.pos0 + min(r0 + BM, p.n) - 1;
+  long long k_lo = t_lo - p.W + 1;
+  if (k_lo < 0) k_lo = 0;
+  *kb0 = k_lo / BN;
+  *nb = (int)(t_hi / BN - *kb0 + 1);
+}
+
+template <int NA>
+__global__ void __launch_bounds__(192, 1)
+    attn_dq_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
+                      const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                      BwdParams p) {
+  using SM = DqSmem<NA>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t bar0 = sbase + SM::BAR_OFF;
+  const uint32_t q_full = bar0;
+  const uint32_t k_full = bar0 + 8;      // [2]
+  const uint32_t v_full = bar0 + 24;     // [2]
+  const uint32_t kv_empty = bar0 + 40;   // [2]
+  const uint32_t s_full = bar0 + 56;     // [2]
+  const uint32_t s_empty = bar0 + 72;    // [2]
+  const uint32_t ds_full = bar0 + 88;    // [2]
+  const uint32_t ds_empty = bar0 + 104;  // [2]
+  const uint32_t dq_done = bar0 + 120;
+  const uint32_t drain = bar0 + 128;
+  uint32_t* tmem_slot = (uint32_t*)(smem + SM::BAR_OFF + 192);
+  volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 196);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x, h = blockIdx.y, part = blockIdx.z;
+  const int r0 = qt * BM;
+  const int kvh = h / (p.H / p.Hkv);
+  long long kb0;
+  int nb_all;
+  bwd_tile_blocks(p, r0, &kb0, &nb_all);
+  const int b_lo = (int)((long long)part * nb_all / p.parts);
+  const int b_hi = (int)((long long)(part + 1) * nb_all / p.parts);
+  const int nb = b_hi - b_lo;
+  kb0 += b_lo;
+  const int ksteps = p.hd / 16;
+  const int nO = (p.hd + 15) & ~15;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(k_full + 8 * s, 1);
+      tc::mbar_init(v_full + 8 * s, 1);
+      tc::mbar_init(kv_empty + 8 * s, 1);
+      tc::mbar_init(s_full + 8 * s, 1);
+      tc::mbar_init(s_empty + 8 * s, 128);
+      tc::mbar_init(ds_full + 8 * s, 128);
+      tc::mbar_init(ds_empty + 8 * s, 1);
+    }
+    tc::mbar_init(dq_done, 1);
+    tc::mbar_init(drain, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&mapQ);
+    tc::prefetch_tmap(&mapDO);
+    tc::prefetch_tmap(&mapK);
+    tc::prefetch_tmap(&mapV);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256;
+
+  if (warp == 0) {
+    if (lane == 0 && nb > 0) {
+      bool ok = true;
+      int issued = 0;
+      tc::mbar_arrive_expect_tx(q_full, 2 * SM::Q_BYTES);
+      for (int a = 0; a < NA; ++a) {
+        tc::tma_load_2d(sbase + SM::Q_OFF + a * BM * 128, &mapQ, h * p.hd + 64 * a, r0, q_full);
+        tc::tma_load_2d(sbase + SM::DO_OFF + a * BM * 128, &mapDO, h * p.hd + 64 * a, r0, q_full);
+      }
+      for (int i = 0; i < nb && ok; ++i) {
+        const int st = i & 1;
+        if (!tc::mbar_wait(kv_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
+          ok = false;
+          break;
+        }
+        const long long kpos = (kb0 + i) * BN;
+        const int row = kvh * p.R + (int)(kpos % p.R);
+        tc::mbar_arrive_expect_tx(k_full + 8 * st, SM::KV_BYTES);
+        for (int a = 0; a < NA; ++a)
+          tc::tma_load_2d(sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN * 128, &mapK, 64 * a, row,
+                          k_full + 8 * st);
+        tc::mbar_arrive_expect_tx(v_full + 8 * st, SM::KV_BYTES);
+        for (int a = 0; a < NA; ++a)
+          tc::tma_load_2d(sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN * 128, &mapV, 64 * a, row,
+                          v_full + 8 * st);
+        issued = i + 1;
+      }
+      const long long t0 = clock64();
+      while (!tc::mbar_try_wait(q_full, 0) && clock64() - t0 < tc::kWaitClocks) {
+      }
+      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
+        const int st = i & 1;
+        const uint32_t par = (i >> 1) & 1;
+        const long long t1 = clock64();
+        while (!(tc::mbar_try_wait(k_full + 8 * st, par) && tc::mbar_try_wait(v_full + 8 * st, par)) &&
+               clock64() - t1 < tc::kWaitClocks) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && nb > 0) {
+      const uint32_t idS = tc::idesc_bf16(BM, BN, 0, 0);
+      const uint32_t idQ = tc::idesc_bf16(BM, nO, 0, 1);
+      bool ok = tc::mbar_wait(q_full, 0, p.err, ERR_A_MMA, abort);
+      bool issued = false;
+      for (int i = 0; i <= nb && ok; ++i) {
+        if (i < nb) {
+          const int st = i & 1;
+          const uint32_t par = (i >> 1) & 1;
+          if (!tc::mbar_wait(k_full + 8 * st, par, p.err, ERR_A_MMA, abort) ||
+              !tc::mbar_wait(v_full + 8 * st, par, p.err, ERR_A_MMA, abort) ||
+              !tc::mbar_wait(s_empty + 8 * st, par ^ 1, p.err, ERR_A_MMA, abort)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t kb = sbase + SM::K_OFF + st * SM::KV_BYTES;
+          const uint32_t vb = sbase + SM::V_OFF + st * SM::KV_BYTES;
+          for (int j = 0; j < ksteps; ++j) {
+            const int a = j >> 2;
+            const uint32_t ao = a * BM * 128 + 32 * (j & 3);
+            const uint32_t bo = a * BN * 128 + 32 * (j & 3);
+            tc::mma_bf16(tS + st * BN, tc::smem_desc_sw128(sbase + SM::Q_OFF + ao, 16, 1024),
+                         tc::smem_desc_sw128(kb + bo, 16, 1024), idS, j > 0);
+            tc::mma_bf16(tP + st * BN, tc::smem_desc_sw128(sbase + SM::DO_OFF + ao, 16, 1024),
+                         tc::smem_desc_sw128(vb + bo, 16, 1024), idS, j > 0);
+          }
+          issued = true;
+          tc::mma_commit(s_full + 8 * st);
+        }
+        if (i >= 1) {
+          const int k = i - 1;
+          const int st = k & 1;
+          if (!tc::mbar_wait(ds_full + 8 * st, (k >> 1) & 1, p.err, ERR_A_MMA, abort)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t kb = sbase + SM::K_OFF + st * SM::KV_BYTES;
+#pragma unroll
+          for (int j = 0; j < BN / 16; ++j)
+            tc::mma_bf16(tQ, tc::smem_desc_sw128(sbase + SM::DS_OFF + st * SM::DS_BYTES + 32 * j, 16, 1024),
+                         tc::smem_desc_sw128(kb + 2048 * j, BN * 128, 1024), idQ, (k > 0 || j > 0) ? 1u : 0u);
+          tc::mma_commit(ds_empty + 8 * st);
+          tc::mma_commit(kv_empty + 8 * st);
+        }
+      }
+      if (ok) tc::mma_commit(dq_done);
+      if (!ok && issued) {
+        tc::mma_commit(drain);
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(drain, 0) && clock64() - t0 < tc::kWaitClocks) {
+        }
+      }
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int grow_ = r0 + row;
+    const long long t = p.pos0 + grow_;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const bool rvalid = grow_ < p.n;
+    const float lse2 = rvalid ? p.lse[(int64_t)h * p.ld_lse + grow_] * 1.4426950408889634f : 0.f;
+    const float Dt = rvalid ? p.dsum[(int64_t)h * p.ld_lse + grow_] : 0.f;
+    bool ok = true;
+    for (int i = 0; i < nb; ++i) {
+      const int st = i & 1;
+      const uint32_t par = (i >> 1) & 1;
+      if (!warp_wait(s_full + 8 * st, par, p.err, ERR_A_SOFT, abort)) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      const long long kpos = (kb0 + i) * BN;
+      const long long lo = t - p.W + 1 - kpos, hi = t - kpos;
+      uint32_t pk[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float sv[32], dp[32];
+        tc::tmem_ld32(tS + st * BN + 32 * half + lane_off, sv);
+        tc::tmem_ld32(tP + st * BN + 32 * half + lane_off, dp);
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const int cc = 32 * half + c;
+          const float p0 = (cc >= lo && cc <= hi) ? exp2f(sv[c] * p.scale_log2 - lse2) : 0.f;
+          const float p1 = (cc + 1 >= lo && cc + 1 <= hi) ? exp2f(sv[c + 1] * p.scale_log2 - lse2) : 0.f;
+          pk[16 * half + c / 2] = pack_bf16(p0 * (dp[c] - Dt) * p.scale, p1 * (dp[c + 1] - Dt) * p.scale);
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(s_empty + 8 * st);
+      if (!warp_wait(ds_empty + 8 * st, par ^ 1, p.err, ERR_A_SOFT, abort)) {
+        ok = false;
+        break;
+      }
+      store_row_sw128_pk(sbase + SM::DS_OFF + st * SM::DS_BYTES, row, pk);
+      fence_proxy_async_smem();
+      tc::tc_fence_before();
+      tc::mbar_arrive(ds_full + 8 * st);
+    }
+    if (ok && nb > 0 && !warp_wait(dq_done, 0, p.err, ERR_A_SOFT, abort)) ok = false;
+    if (ok) {
+      tc::tc_fence_after();
+      for (int c0 = 0; c0 < nO; c0 += 32) {
+        float v[32];
+        if (nb > 0) {
+          tc::tmem_ld32(tQ + c0 + lane_off, v);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = 0.f;
+        }
+        if (!rvalid) continue;
+        if (p.parts == 1) {
+          bf16* dst = p.dqkv + (int64_t)grow_ * p.ldg + (int64_t)h * p.hd + c0;
+#pragma unroll
+          for (int k = 0; k < 32; k += 8)
+            if (c0 + k < p.hd) {
+              uint4 u;
+              u.x = pack_bf16(v[k], v[k + 1]);
+              u.y = pack_bf16(v[k + 2], v[k + 3]);
+              u.z = pack_bf16(v[k + 4], v[k + 5]);
+              u.w = pack_bf16(v[k + 6], v[k + 7]);
+              *reinterpret_cast<uint4*>(dst + k) = u;
+            }
+        } else {
+          float* dst = p.ws + ((int64_t)part * p.n + grow_) * ((int64_t)p.H * p.hd) + (int64_t)h * p.hd + c0;
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            if (c0 + k < p.hd) *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// --- dk / dv of the chunk's own keys, one CTA per (key tile, query head) ---
+template <int NA>
+struct DkvSmem {
+  static constexpr int T_BYTES = NA * BM * 128;  // 128 key rows
+  static constexpr int B_BYTES = NA * BN * 128;  // 64 query rows
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + T_BYTES;
+  static constexpr int Q_OFF = V_OFF + T_BYTES;
+  static constexpr int DO_OFF = Q_OFF + STAGES * B_BYTES;
+  static constexpr int PT_OFF = DO_OFF + STAGES * B_BYTES;
+  static constexpr int DS_OFF = PT_OFF + 2 * P_BYTES;
+  static constexpr int BAR_OFF = DS_OFF + 2 * P_BYTES;
+  static constexpr int SMEM = BAR_OFF + 256;
+};
+
+template <int NA>
+__global__ void __launch_bounds__(192, 1)
+    attn_dkv_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
+                       const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                       BwdParams p) {
+  using SM = DkvSmem<NA>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t bar0 = sbase + SM::BAR_OFF;
+  const uint32_t kv_full = bar0;
+  const uint32_t q_full = bar0 + 8;      // [2]
+  const uint32_t q_empty = bar0 + 24;    // [2]
+  const uint32_t s_full = bar0 + 40;     // [2]
+  const uint32_t s_empty = bar0 + 56;    // [2]
+  const uint32_t pd_full = bar0 + 72;    // [2]
+  const uint32_t pd_empty = bar0 + 88;   // [2]
+  const uint32_t acc_done = bar0 + 104;
+  const uint32_t drain = bar0 + 112;
+  uint32_t* tmem_slot = (uint32_t*)(smem + SM::BAR_OFF + 192);
+  volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 196);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x, kt = blockIdx.y;
+  const int j0 = kt * BM;                       // first key row (chunk-local)
+  const int kvh = h / (p.H / p.Hkv);
+  const int j_last = min(j0 + BM, p.n) - 1;
+  const int t_last = min(p.n - 1, j_last + p.W - 1);
+  const int qb0 = j0 / BN;
+  const int nb = t_last / BN - qb0 + 1;
+  const int ksteps = p.hd / 16;
+  const int nO = (p.hd + 15) & ~15;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(q_full + 8 * s, 1);
+      tc::mbar_init(q_empty + 8 * s, 1);
+      tc::mbar_init(s_full + 8 * s, 1);
+      tc::mbar_init(s_empty + 8 * s, 128);
+      tc::mbar_init(pd_full + 8 * s, 128);
+      tc::mbar_init(pd_empty + 8 * s, 1);
+    }
+    tc::mbar_init(acc_done, 1);
+    tc::mbar_init(drain, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&mapQ);
+    tc::prefetch_tmap(&mapDO);
+    tc::prefetch_tmap(&mapK);
+    tc::prefetch_tmap(&mapV);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tP = tmem + 128, tK = tmem + 256, tV = tmem + 384;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      int issued = 0;
+      // the tile's keys and values: two 64-row boxes per atom (chunk starts
+      // are multiples of 64, so each box is contiguous in the ring)
+      tc::mbar_arrive_expect_tx(kv_full, 2 * SM::T_BYTES);
+      for (int m = 0; m < 2; ++m) {
+        const int row = kvh * p.R + (int)((p.pos0 + j0 + 64 * m) % p.R);
+        for (int a = 0; a < NA; ++a) {
+          tc::tma_load_2d(sbase + SM::K_OFF + a * BM * 128 + m * 64 * 128, &mapK, 64 * a, row, kv_full);
+          tc::tma_load_2d(sbase + SM::V_OFF + a * BM * 128 + m * 64 * 128, &mapV, 64 * a, row, kv_full);
+        }
+      }
+      for (int i = 0; i < nb && ok; ++i) {
+        const int st = i & 1;
+        if (!tc::mbar_wait(q_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
+          ok = false;
+          break;
+        }
+        const int t0 = (qb0 + i) * BN;
+        tc::mbar_arrive_expect_tx(q_full + 8 * st, 2 * SM::B_BYTES);
+        for (int a = 0; a < NA; ++a) {
+          tc::tma_load_2d(sbase + SM::Q_OFF + st * SM::B_BYTES + a * BN * 128, &mapQ, h * p.hd + 64 * a, t0,
+                          q_full + 8 * st);
+          tc::tma_load_2d(sbase + SM::DO_OFF + st * SM::B_BYTES + a * BN * 128, &mapDO, h * p.hd + 64 * a, t0,
+                          q_full + 8 * st);
+        }
+        issued = i + 1;
+      }
+      const long long t0 = clock64();
+      while (!tc::mbar_try_wait(kv_full, 0) && clock64() - t0 < tc::kWaitClocks) {
+      }
+      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
+        const long long t1 = clock64();
+        while (!tc::mbar_try_wait(q_full + 8 * (i & 1), (i >> 1) & 1) && clock64() - t1 < tc::kWaitClocks) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idS = tc::idesc_bf16(BM, BN, 0, 0);
+      const uint32_t idA = tc::idesc_bf16(BM, nO, 0, 1);
+      bool ok = tc::mbar_wait(kv_full, 0, p.err, ERR_A_MMA, abort);
+      bool issued = false;
+      for (int i = 0; i <= nb && ok; ++i) {
+        if (i < nb) {
+          const int st = i & 1;
+          const uint32_t par = (i >> 1) & 1;
+          if (!tc::mbar_wait(q_full + 8 * st, par, p.err, ERR_A_MMA, abort) ||
+              !tc::mbar_wait(s_empty + 8 * st, par ^ 1, p.err, ERR_A_MMA, abort)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t qb = sbase + SM::Q_OFF + st * SM::B_BYTES;
+          const uint32_t ob = sbase + SM::DO_OFF + st * SM::B_BYTES;
+          for (int j = 0; j < ksteps; ++j) {
+            const int a = j >> 2;
+            const uint32_t ao = a * BM * 128 + 32 * (j & 3);
+            const uint32_t bo = a * BN * 128 + 32 * (j & 3);
+            tc::mma_bf16(tS + st * BN, tc::smem_desc_sw128(sbase + SM::K_OFF + ao, 16, 1024),
+                         tc::smem_desc_sw128(qb + bo, 16, 1024), idS, j > 0);
+            tc::mma_bf16(tP + st * BN, tc::smem_desc_sw128(sbase + SM::V_OFF + ao, 16, 1024),
+                         tc::smem_desc_sw128(ob + bo, 16, 1024), idS, j > 0);
+          }
+          issued = true;
+          tc::mma_commit(s_full + 8 * st);
+        }
+        if (i >= 1) {
+          const int k = i - 1;
+          const int st = k & 1;
+          if (!tc::mbar_wait(pd_full + 8 * st, (k >> 1) & 1, p.err, ERR_A_MMA, abort)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t qb = sbase + SM::Q_OFF + st * SM::B_BYTES;
+          const uint32_t ob = sbase + SM::DO_OFF + st * SM::B_BYTES;
+#pragma unroll
+          for (int j = 0; j < BN / 16; ++j) {
+            const uint32_t acc = (k > 0 || j > 0) ? 1u : 0u;
+            tc::mma_bf16(tV, tc::smem_desc_sw128(sbase + SM::PT_OFF + st * SM::P_BYTES + 32 * j, 16, 1024),
+                         tc::smem_desc_sw128(ob + 2048 * j, BN * 128, 1024), idA, acc);
+            tc::mma_bf16(tK, tc::smem_desc_sw128(sbase + SM::DS_OFF + st * SM::P_BYTES + 32 * j, 16, 1024),
+                         tc::smem_desc_sw128(qb + 2048 * j, BN * 128, 1024), idA, acc);
+          }
+          tc::mma_commit(pd_empty + 8 * st);
+          tc::mma_commit(q_empty + 8 * st);
+        }
+      }
+      if (ok) tc::mma_commit(acc_done);
+      if (!ok && issued) {
+        tc::mma_commit(drain);
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(drain, 0) && clock64() - t0 < tc::kWaitClocks) {
+        }
+      }
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int j = j0 + row;                  // chunk-local key index
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const float* lse_h = p.lse + (int64_t)h * p.ld_lse;
+    const float* d_h = p.dsum + (int64_t)h * p.ld_lse;
+    bool ok = true;
+    for (int i = 0; i < nb; ++i) {
+      const int st = i & 1;
+      const uint32_t par = (i >> 1) & 1;
+      if (!warp_wait(s_full + 8 * st, par, p.err, ERR_A_SOFT, abort)) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      const int t0 = (qb0 + i) * BN;
+      uint32_t pp[32], pd[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float sv[32], dp[32];
+        tc::tmem_ld32(tS + st * BN + 32 * half + lane_off, sv);
+        tc::tmem_ld32(tP + st * BN + 32 * half + lane_off, dp);
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int t = t0 + 32 * half + c + e;
+            const int rel = t - j;
+            const bool valid = t < p.n && j < p.n && rel >= 0 && rel < p.W;
+            const float l2 = valid ? lse_h[t] * 1.4426950408889634f : 0.f;
+            const float Dt = valid ? d_h[t] : 0.f;
+            pv[e] = valid ? exp2f(sv[c + e] * p.scale_log2 - l2) : 0.f;
+            dv[e] = pv[e] * (dp[c + e] - Dt) * p.scale;
+          }
+          pp[16 * half + c / 2] = pack_bf16(pv[0], pv[1]);
+          pd[16 * half + c / 2] = pack_bf16(dv[0], dv[1]);
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(s_empty + 8 * st);
+      if (!warp_wait(pd_empty + 8 * st, par ^ 1, p.err, ERR_A_SOFT, abort)) {
+        ok = false;
+        break;
+      }
+      store_row_sw128_pk(sbase + SM::PT_OFF + st * SM::P_BYTES, row, pp);
+      store_row_sw128_pk(sbase + SM::DS_OFF + st * SM::P_BYTES, row, pd);
+      fence_proxy_async_smem();
+      tc::tc_fence_before();
+      tc::mbar_arrive(pd_full + 8 * st);
+    }
+    if (ok && warp_wait(acc_done, 0, p.err, ERR_A_SOFT, abort)) {
+      tc::tc_fence_after();
+      // per-head partials: ws[0][h][j][:] = dk, ws[1][h][j][:] = dv
+      const int64_t plane = (int64_t)p.H * p.n * p.hd;
+      for (int c0 = 0; c0 < nO; c0 += 32) {
+        float vk[32], vv[32];
+        tc::tmem_ld32(tK + c0 + lane_off, vk);
+        tc::tmem_ld32(tV + c0 + lane_off, vv);
+        if (j < p.n) {
+          float* dk = p.ws + ((int64_t)h * p.n + j) * p.hd + c0;
+          float* dv = dk + plane;
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            if (c0 + k < p.hd) {
+              *reinterpret_cast<float4*>(dk + k) = make_float4(vk[k], vk[k + 1], vk[k + 2], vk[k + 3]);
+              *reinterpret_cast<float4*>(dv + k) = make_float4(vv[k], vv[k + 1], vv[k + 2], vv[k + 3]);
+            }
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// D[h][r] = sum_d dO[r, h*hd + d] * O[r, h*hd + d]; one warp per (r, h)
+__global__ void attn_bwd_prep_tc_kernel(const bf16* __restrict__ dO, const bf16* __restrict__ O, int n, int H,
+                                        int hd, float* __restrict__ dsum, int ld) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (w >= n * H) return;
+  const int r = w / H, h = w % H;
+  const int64_t off = (int64_t)r * H * hd + (int64_t)h * hd;
+  float s = 0.f;
+  for (int d = 2 * lane; d < hd; d += 64) {
+    const float2 a = load2<bf16>(dO + off + d);
+    const float2 b = load2<bf16>(O + off + d);
+    s = fmaf(a.x, b.x, fmaf(a.y, b.y, s));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) dsum[(int64_t)h * ld + r] = s;
+}
+
+// dq = sum over parts (fixed order) -> bf16 columns [0, H*hd) of dqkv
+__global__ void attn_dq_reduce_kernel(const float* __restrict__ ws, int parts, int n, int cols,
+                                      bf16* __restrict__ dqkv, int64_t ldg) {
+  const int64_t total = (int64_t)n * cols / 4;
+  const int64_t plane = (int64_t)n * cols;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = 4 * i;
+    float4 acc = *reinterpret_cast<const float4*>(ws + e);
+    for (int q = 1; q < parts; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(ws + q * plane + e);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int64_t r = e / cols, c = e % cols;
+    bf16* d = dqkv + r * ldg + c;
+    *reinterpret_cast<uint2*>(d) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  }
+}
+
+// dk, dv of KV head g = sum over its query heads (fixed order) -> bf16
+__global__ void attn_dkv_reduce_kernel(const float* __restrict__ ws, int n, int H, int Hkv, int hd,
+                                       bf16* __restrict__ dqkv, int64_t ldg) {
+  const int group = H / Hkv;
+  const int64_t total = (int64_t)2 * n * Hkv * hd / 4;
+  const int64_t plane = (int64_t)H * n * hd;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    int64_t e = 4 * i;
+    const int which = (int)(e / ((int64_t)n * Hkv * hd));   // 0 dk, 1 dv
+    e -= (int64_t)which * n * Hkv * hd;
+    const int r = (int)(e / ((int64_t)Hkv * hd));
+    const int g = (int)((e / hd) % Hkv);
+    const int d = (int)(e % hd);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < group; ++k) {
+      const int h = g * group + k;
+      const float4 v = *reinterpret_cast<const float4*>(ws + which * plane + ((int64_t)h * n + r) * hd + d);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    bf16* dst = dqkv + (int64_t)r * ldg + (int64_t)(H + which * Hkv + g) * hd + d;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  }
+}
+
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
+std::once_flag g_enc_once;
+
+bool encoder() {
+  std::call_once(g_enc_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  });
+  return g_enc != nullptr;
+}
+
+// bf16 2-D map: inner extent `inner` (elements, contiguous), `outer` rows of
+// pitch `ld` elements, box {64, box_rows}, 128-byte swizzle, zero fill
+int map2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+}
+
+template <int NA>
+int launch_fwd(const AttnArgs& a, int* err, cudaStream_t st) {
+  using SM = FwdSmem<NA>;
+  CUtensorMap mq, mk, mv;
+  const uint64_t ldq = (uint64_t)a.H * a.hd;
+  int rc = map2d(&mq, a.q, ldq, a.n, ldq, BM);
+  if (!rc) rc = map2d(&mk, a.kring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
+  if (!rc) rc = map2d(&mv, a.vring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
+  if (rc) return rc;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SM::SMEM);
+    if (e != cudaSuccess) return (int)e;
+    attr = true;
+  }
+  FwdParams p;
+  p.n = a.n;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.hd = a.hd;
+  p.W = a.W;
+  p.R = a.R;
+  p.pos0 = a.pos0;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)a.hd);
+  p.o = (bf16*)a.o;
+  p.ldo = (int64_t)a.H * a.hd;
+  p.lse = a.lse;
+  p.ld_lse = a.ld_lse;
+  p.err = err;
+  dim3 grid((a.n + BM - 1) / BM, a.H);
+  attn_fwd_tc_kernel<NA><<<grid, 192, SM::SMEM, st>>>(mq, mk, mv, p);
+  return (int)cudaPeekAtLastError();
+}
+
+}  // namespace
+
+bool attn_tc_supported(const AttnArgs& a) {
+  return a.hd >= 64 && a.hd <= 128 && a.hd % 16 == 0 && a.R % 128 == 0 && a.H % a.Hkv == 0 &&
+         ((uintptr_t)a.q & 15) == 0 && ((uintptr_t)a.kring & 15) == 0 && ((uintptr_t)a.vring & 15) == 0 &&
+         ((uintptr_t)a.o & 15) == 0;
+}
+
+int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st) {
+  if (a.n <= 0) return 0;
+  if (!encoder() || !attn_tc_supported(a)) return (int)cudaErrorNotSupported;
+  return a.hd <= 64 ? launch_fwd<1>(a, err, st) : launch_fwd<2>(a, err, st);
+}
+
+// key-range parts of the dq kernel: enough CTAs to fill the SMs in whole
+// waves, never more parts than the smallest tile has key blocks
+static int dq_parts(const AttnArgs& a, int num_sms) {
+  const int ntiles = (a.n + BM - 1) / BM;
+  long long kb0 = (a.pos0 - a.W + 1 > 0 ? a.pos0 - a.W + 1 : 0) / BN;
+  int nb_min = INT32_MAX;
+  for (int t = 0; t < ntiles; ++t) {
+    const long long t_lo = a.pos0 + (long long)t * BM;
+    const long long t_hi = a.pos0 + std::min(t * BM + BM, a.n) - 1;
+    long long k_lo = t_lo - a.W + 1;
+    if (k_lo < 0) k_lo = 0;
+    kb0 = k_lo / BN;
+    nb_min = std::min<int>(nb_min, (int)(t_hi / BN - kb0 + 1));
+  }
+  const int units = ntiles * a.H;
+  int best = 1;
+  double best_cost = 1e30;
+  for (int P = 1; P <= 4 && P <= nb_min; ++P) {
+    const double waves = std::ceil((double)units * P / num_sms);
+    const double cost = waves / P * (1.0 + 0.02 * (P - 1));
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = P;
+    }
+  }
+  return best;
+}
+
+int64_t attn_bwd_tc_ws_elems(int n, int H, int hd, int num_sms) {
+  (void)num_sms;
+  const int64_t plane = (int64_t)n * H * hd;
+  return std::max<int64_t>(4 * plane, 2 * plane);
+}
+
+template <int NA>
+int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
+  using DQ = DqSmem<NA>;
+  using DKV = DkvSmem<NA>;
+  CUtensorMap mq, mdo, mk, mv, mq64, mdo64;
+  const uint64_t ldq = (uint64_t)a.H * a.hd;
+  int rc = map2d(&mq, a.q, ldq, a.n, ldq, BM);
+  if (!rc) rc = map2d(&mdo, a.dout, ldq, a.n, ldq, BM);
+  if (!rc) rc = map2d(&mq64, a.q, ldq, a.n, ldq, BN);
+  if (!rc) rc = map2d(&mdo64, a.dout, ldq, a.n, ldq, BN);
+  if (!rc) rc = map2d(&mk, a.kring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
+  if (!rc) rc = map2d(&mv, a.vring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
+  if (rc) return rc;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_dq_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DQ::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_dkv_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize, DKV::SMEM);
+    if (e != cudaSuccess) return (int)e;
+    attr = true;
+  }
+  BwdParams p;
+  p.n = a.n;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.hd = a.hd;
+  p.W = a.W;
+  p.R = a.R;
+  p.pos0 = a.pos0;
+  p.scale = 1.0f / sqrtf((float)a.hd);
+  p.scale_log2 = 1.4426950408889634f * p.scale;
+  p.lse = a.lse;
+  p.dsum = a.Dsum;
+  p.ld_lse = a.ld_lse;
+  p.dqkv = (bf16*)a.dqkv;
+  p.ldg = (int64_t)(a.H + 2 * a.Hkv) * a.hd;
+  p.ws = a.ws;
+  p.err = err;
+  {
+    const int warps = a.n * a.H;
+    attn_bwd_prep_tc_kernel<<<(warps + 7) / 8, 256, 0, st>>>((const bf16*)a.dout, (const bf16*)a.out, a.n, a.H,
+                                                             a.hd, a.Dsum, a.ld_lse);
+  }
+  p.parts = dq_parts(a, num_sms);
+  const int64_t plane = (int64_t)a.n * a.H * a.hd;
+  if (p.parts > 1 && (int64_t)p.parts * plane > a.ws_elems) p.parts = 1;
+  attn_dq_tc_kernel<NA><<<dim3((a.n + BM - 1) / BM, a.H, p.parts), 192, DQ::SMEM, st>>>(mq, mdo, mk, mv, p);
+  if (p.parts > 1) {
+    const int cols = a.H * a.hd;
+    const int64_t quads = plane / 4;
+    const int grid = (int)std::min<int64_t>((quads + 255) / 256, (int64_t)num_sms * 8);
+    attn_dq_reduce_kernel<<<grid, 256, 0, st>>>(a.ws, p.parts, a.n, cols, p.dqkv, p.ldg);
+  }
+  // dk / dv (after the dq reduction, which may use the same scratch)
+  attn_dkv_tc_kernel<NA><<<dim3(a.H, (a.n + BM - 1) / BM), 192, DKV::SMEM, st>>>(mq64, mdo64, mk, mv, p);
+  {
+    const int64_t quads = (int64_t)2 * a.n * a.Hkv * a.hd / 4;
+    const int grid = (int)std::min<int64_t>((quads + 255) / 256, (int64_t)num_sms * 8);
+    attn_dkv_reduce_kernel<<<grid, 256, 0, st>>>(a.ws, a.n, a.H, a.Hkv, a.hd, p.dqkv, p.ldg);
+  }
+  return (int)cudaPeekAtLastError();
+}
+
+bool attn_bwd_tc_supported(const AttnArgs& a) {
+  return attn_tc_supported(a) && a.pos0 % BN == 0 && ((uintptr_t)a.dout & 15) == 0 &&
+         ((uintptr_t)a.dqkv & 15) == 0 && a.ws != nullptr &&
+         a.ws_elems >= attn_bwd_tc_ws_elems(a.n, a.H, a.hd, 0) / 2;
+}
+
+int attn_bwd_tc(const AttnArgs& a, int* err, cudaStream_t st) {
+  if (a.n <= 0) return 0;
+  if (!encoder() || !attn_bwd_tc_supported(a)) return (int)cudaErrorNotSupported;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return a.hd <= 64 ? launch_bwd<1>(a, err, st, sms) : launch_bwd<2>(a, err, st, sms);
+}
+
 }  // namespace ttt

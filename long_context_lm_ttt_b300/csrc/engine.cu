@@ -83,13 +83,79 @@ struct EngineBase {
   int R = 0, qkv_cols = 0, Vs = 0, num_sms = 148;
   int64_t pos = 0;
   bool used = false;
-  bool use_tc_gemm = false, use_tc_attn = false;
-  virtual ~EngineBase() {}
+  bool use_tc_gemm = false, use_tc_attn = false, use_tc_attn_bwd = false;
   virtual int init(const ttt_weights* w, cudaStream_t st) = 0;
   virtual int prefill(const int32_t* tok, int64_t T, float* losses, cudaStream_t st) = 0;
   virtual int logits(const int32_t* cont, int n, float* out, cudaStream_t st) = 0;
   virtual int get_fast(int block, int which, float* dst, cudaStream_t st) = 0;
   virtual int reset(cudaStream_t st) = 0;
+
+  // --- optional per-launch timing (ttt_profile) ---------------------------
+  // Each profiled launch is bracketed by two events on its own stream; the
+  // events are resolved after the call's final synchronisation.
+  enum ProfCls { P_GEMM_FWD, P_GEMM_LMHEAD, P_GEMM_BWD, P_GEMM_SGD, P_ATTN_FWD, P_ATTN_BWD, P_ROW, P_N };
+  struct ProfRec {
+    int cls, nk;
+    cudaEvent_t a, b;
+    double flops, bytes;
+  };
+  bool prof_on = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_next = 0;
+  std::vector<ProfRec> prof_recs;
+  ttt_kernel_stat prof_stat[P_N];
+  static const char* prof_name(int c) {
+    static const char* n[P_N] = {"gemm_fwd", "gemm_lm_head", "gemm_bwd_dx", "gemm_dw_sgd",
+                                 "attn_fwd", "attn_bwd", "rowwise"};
+    return n[c];
+  }
+  void prof_clear() {
+    memset(prof_stat, 0, sizeof(prof_stat));
+    for (int c = 0; c < P_N; ++c) snprintf(prof_stat[c].name, sizeof(prof_stat[c].name), "%s", prof_name(c));
+    prof_recs.clear();
+    ev_next = 0;
+  }
+  cudaEvent_t prof_event() {
+    if (ev_next == ev_pool.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      ev_pool.push_back(e);
+    }
+    return ev_pool[ev_next++];
+  }
+  // nk: kernels the launch function issues
+  template <typename F>
+  void prof(int cls, double flops, double bytes, cudaStream_t st, F&& launch, int nk = 1) {
+    if (!prof_on) {
+      launch();
+      return;
+    }
+    cudaEvent_t a = prof_event(), b = prof_event();
+    if (a) cudaEventRecord(a, st);
+    launch();
+    if (b) cudaEventRecord(b, st);
+    if (a && b) prof_recs.push_back({cls, nk, a, b, flops, bytes});
+  }
+  // after a synchronisation: fold the recorded pairs into prof_stat
+  void prof_collect() {
+    for (const ProfRec& r : prof_recs) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
+      ttt_kernel_stat& k = prof_stat[r.cls];
+      k.launches += r.nk;
+      k.ms += ms;
+      k.flops += r.flops;
+      k.bytes += r.bytes;
+    }
+    prof_recs.clear();
+    ev_next = 0;
+  }
+  virtual ~EngineBase() {
+    for (cudaEvent_t e : ev_pool) cudaEventDestroy(e);
+  }
 };
 
 template <typename T>
@@ -139,6 +205,8 @@ struct Engine : EngineBase {
   int* dev_err = nullptr;  // [0] first non-finite chunk, [1] bad token, [2] kernel check
   float* stage32 = nullptr;
   size_t stage32_elems = 0;
+  float* attn_ws = nullptr;  // scratch of the tensor-core attention backward
+  int64_t attn_ws_elems = 0;
 
   template <typename U>
   int A(U** p, size_t elems) {
@@ -292,6 +360,10 @@ struct Engine : EngineBase {
     A_TRY(dqkv, (size_t)b * qkv_cols);
     A_TRY(dxn, (size_t)b * d);
     A_TRY(Dsum, (size_t)H * b);
+    if (kBF16 && use_tc_attn_bwd) {
+      attn_ws_elems = attn_bwd_tc_ws_elems(b, H, hd, num_sms);
+      A_TRY(attn_ws, (size_t)attn_ws_elems);
+    }
     A_TRY(losses_stage, (size_t)(cfg.max_tokens + b - 1) / b + 1);
     A_TRY(dev_err, 4);
     CU_TRY(cudaStreamSynchronize(st));
@@ -302,18 +374,46 @@ struct Engine : EngineBase {
   void gemm(int M, int N, int K, const T* A_, int64_t lda, int a_mn, const T* B_, int64_t ldb,
             int b_mn, const Epi& e, cudaStream_t st, int* rc, const T* B2 = nullptr) {
     GemmArgs<T> g{M, N, K, A_, lda, a_mn, B_, ldb, b_mn, e, B2};
-    if constexpr (kBF16) {
-      if (use_tc_gemm) {
-        int r = gemm_tc(g, num_sms, dev_err + 2, st);
-        if (r != 0 && *rc == TTT_OK) {
-          *rc = TTT_ERR_SHAPE;
-          err = "tensor-core GEMM rejected M=" + std::to_string(M) + " N=" + std::to_string(N) +
-                " K=" + std::to_string(K) + " (" + cudaGetErrorString((cudaError_t)r) + ")";
-        }
-        return;
-      }
+    int cls = P_GEMM_FWD;
+    double out_b = (double)M * N * (e.kind == EPI_STORE && !e.out_f32 ? sizeof(T) : 4);
+    switch (e.kind) {
+      case EPI_RESID: out_b *= 2; break;                              // residual read + write
+      case EPI_CE_Z: case EPI_CE_ACC: cls = P_GEMM_LMHEAD; out_b *= 2; break;
+      case EPI_SWIGLU_BWD: cls = P_GEMM_BWD; out_b = (double)M * N * 4 * sizeof(T); break;
+      case EPI_STORE: cls = P_GEMM_BWD; break;
+      case EPI_SGD: cls = P_GEMM_SGD; out_b = (double)M * N * (8 + 2 * sizeof(T)); break;
+      case EPI_SWIGLU: out_b = (double)M * N * sizeof(T) * (e.stash ? 1.5 : 0.5); break;
+      default: break;
     }
-    gemm_simt<T>(g, st);
+    const double flops = 2.0 * M * N * K;
+    const double bytes = (double)sizeof(T) * ((double)M * K + (double)N * K) + out_b;
+    prof(cls, flops, bytes, st, [&] {
+      if constexpr (kBF16) {
+        if (use_tc_gemm) {
+          int r = gemm_tc(g, num_sms, dev_err + 2, st);
+          if (r != 0 && *rc == TTT_OK) {
+            *rc = TTT_ERR_SHAPE;
+            err = "tensor-core GEMM rejected M=" + std::to_string(M) + " N=" + std::to_string(N) +
+                  " K=" + std::to_string(K) + " (" + cudaGetErrorString((cudaError_t)r) + ")";
+          }
+          return;
+        }
+      }
+      gemm_simt<T>(g, st);
+    });
+  }
+  // algorithmic attention work of a chunk of n queries starting at pos0:
+  // unmasked (query, key) pairs and the pairs whose key is in the chunk
+  void attn_pairs(int64_t pos0, int n, double* pairs, double* local) const {
+    const int64_t W = cfg.window;
+    double p = 0, q = 0;
+    for (int r = 0; r < n; ++r) {
+      const int64_t t = pos0 + r;
+      p += (double)std::min<int64_t>(t + 1, W);
+      q += (double)std::min<int64_t>(r + 1, W);
+    }
+    *pairs = p;
+    *local = q;
   }
   static Epi epi(int kind) {
     Epi e;
@@ -340,30 +440,49 @@ struct Engine : EngineBase {
     return a;
   }
   void attn_fwd(const AttnArgs& a, cudaStream_t st, int* rc) {
-    if constexpr (kBF16) {
-      if (use_tc_attn) {
-        int r = attn_fwd_tc(a, st);
-        if (r != 0 && *rc == TTT_OK) {
-          *rc = TTT_ERR_SHAPE;
-          err = "tensor-core attention forward rejected the shape";
+    double P, Pl;
+    attn_pairs(a.pos0, a.n, &P, &Pl);
+    const double hdH = (double)a.H * a.hd;
+    const double kv = (double)std::min<int64_t>(a.pos0 + a.n, (int64_t)a.W + a.n - 1) * a.Hkv * a.hd;
+    const double bytes = sizeof(T) * (2.0 * a.n * hdH + 2.0 * kv) + 4.0 * a.n * a.H;
+    prof(P_ATTN_FWD, 4.0 * hdH * P, bytes, st, [&] {
+      if constexpr (kBF16) {
+        if (use_tc_attn && attn_tc_supported(a)) {
+          int r = attn_fwd_tc(a, dev_err + 2, st);
+          if (r != 0 && *rc == TTT_OK) {
+            *rc = TTT_ERR_SHAPE;
+            err = "tensor-core attention forward rejected the shape";
+          }
+          return;
         }
-        return;
       }
-    }
-    attn_fwd_simt<T>(a, st);
+      attn_fwd_simt<T>(a, st);
+    });
   }
   void attn_bwd(const AttnArgs& a, cudaStream_t st, int* rc) {
-    if constexpr (kBF16) {
-      if (use_tc_attn) {
-        int r = attn_bwd_tc(a, st);
-        if (r != 0 && *rc == TTT_OK) {
-          *rc = TTT_ERR_SHAPE;
-          err = "tensor-core attention backward rejected the shape";
+    double P, Pl;
+    attn_pairs(a.pos0, a.n, &P, &Pl);
+    const double hdH = (double)a.H * a.hd;
+    const double kv = (double)std::min<int64_t>(a.pos0 + a.n, (int64_t)a.W + a.n - 1) * a.Hkv * a.hd;
+    const double bytes = sizeof(T) * (4.0 * a.n * hdH + 2.0 * kv + (double)a.n * qkv_cols) + 8.0 * a.n * a.H;
+    prof(P_ATTN_BWD, 6.0 * hdH * P + 4.0 * hdH * Pl, bytes, st, [&] {
+      if constexpr (kBF16) {
+        if (use_tc_attn_bwd && attn_bwd_tc_supported(a)) {
+          int r = attn_bwd_tc(a, dev_err + 2, st);
+          if (r != 0 && *rc == TTT_OK) {
+            *rc = TTT_ERR_SHAPE;
+            err = "tensor-core attention backward rejected the shape";
+          }
+          return;
         }
-        return;
       }
-    }
-    attn_bwd_simt<T>(a, st);
+      attn_bwd_simt<T>(a, st);
+    }, use_tc_attn_bwd && attn_bwd_tc_supported(a) ? 5 : 3);
+  }
+  // row-wise kernels: bytes moved, no tensor work
+  template <typename F>
+  void row(double bytes, cudaStream_t st, F&& launch) {
+    prof(P_ROW, 0.0, bytes, st, launch);
   }
 
   // forward of positions [s, s+n) with the current weights; leaves the final
@@ -373,15 +492,15 @@ struct Engine : EngineBase {
               Lt = cfg.n_ttt_layers;
     const int lo = L - Lt;
     const int64_t Hhd = (int64_t)H * hd;
-    launch_rope_table(s, n, hd, cfg.rope_theta, cs, st);
+    row((double)n * hd * 4, st, [&] { launch_rope_table(s, n, hd, cfg.rope_theta, cs, st); });
     float* x_in = lo == 0 ? xs[0] : xlow[0];
-    launch_embed<T>(tok_chunk, n, E, d, x_in, cfg.vocab, dev_err + 1, st);
+    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_embed<T>(tok_chunk, n, E, d, x_in, cfg.vocab, dev_err + 1, st); });
     for (int l = 0; l < L; ++l) {
       const bool fast = l >= lo;
       Stash& S = fast ? fstash[l - lo] : sstash;
       Layer& y = layers[l];
       float* x_out = (l + 1 >= lo) ? xs[l + 1 - lo] : xlow[(l + 1) & 1];
-      launch_rmsnorm_fwd<T>(x_in, y.g_attn, n, d, cfg.norm_eps, S.xn, S.r1, st);
+      row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(x_in, y.g_attn, n, d, cfg.norm_eps, S.xn, S.r1, st); });
       Epi e = epi(EPI_QKV);
       e.out = S.q;
       e.ldo = Hhd;
@@ -401,7 +520,7 @@ struct Engine : EngineBase {
       e.resid = x_in;
       e.ldr = d;
       gemm(n, d, (int)Hhd, S.o, Hhd, 0, y.wo, Hhd, 0, e, st, rc);
-      launch_rmsnorm_fwd<T>(S.h, y.g_mlp, n, d, cfg.norm_eps, S.hn, S.r2, st);
+      row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(S.h, y.g_mlp, n, d, cfg.norm_eps, S.hn, S.r2, st); });
       e = epi(EPI_SWIGLU);
       e.out = S.a;
       e.ldo = ff;
@@ -418,7 +537,7 @@ struct Engine : EngineBase {
       gemm(n, d, ff, S.a, ff, 0, y.wd, ff, 0, e, st, rc, y.wd_lo);
       x_in = x_out;
     }
-    launch_rmsnorm_fwd<T>(x_in, g_final, n, d, cfg.norm_eps, hf, rf, st);
+    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(x_in, g_final, n, d, cfg.norm_eps, hf, rf, st); });
   }
 
   // streamed lm_head + cross-entropy: loss of chunk c into losses[c] and the
@@ -426,7 +545,7 @@ struct Engine : EngineBase {
   void cross_entropy(const int32_t* tok, int64_t n_tok, int64_t s, int n, int n_tgt, float* losses, int c,
                      cudaStream_t st, int* rc) {
     const int d = cfg.d_model, V = cfg.vocab;
-    launch_targets(tok, n_tok, s, n, tgt, V, dev_err + 1, st);
+    row((double)n * 8, st, [&] { launch_targets(tok, n_tok, s, n, tgt, V, dev_err + 1, st); });
     for (int v0 = 0; v0 < V; v0 += Vs) {
       const int nv = std::min(Vs, V - v0);
       const int first = v0 == 0;
@@ -437,7 +556,7 @@ struct Engine : EngineBase {
       e.ztgt = ztgt;
       e.col0 = v0;
       gemm(n, nv, d, hf, d, 0, Wlm + (int64_t)v0 * d, d, 0, e, st, rc);
-      launch_ce_slab_stats<T>(z_slab, Vs, n, nv, p_slab, Vs, m_run, l_run, alpha, beta, first, st);
+      row((double)n * nv * (4 + sizeof(T)), st, [&] { launch_ce_slab_stats<T>(z_slab, Vs, n, nv, p_slab, Vs, m_run, l_run, alpha, beta, first, st); });
       e = epi(EPI_CE_ACC);
       e.out = dh_acc;
       e.ldo = d;
@@ -447,8 +566,8 @@ struct Engine : EngineBase {
       gemm(n, d, nv, p_slab, Vs, 0, Wlm + (int64_t)v0 * d, d, 1, e, st, rc);
     }
     const float inv = 1.0f / (float)n_tgt;
-    launch_ce_finalize<T>(n, m_run, l_run, ztgt, tgt, inv, dh_acc, Wlm, d, dhf, loss_row, st);
-    launch_loss_reduce(loss_row, n, inv, losses, c, dev_err, st);
+    row((double)n * d * (8 + sizeof(T)), st, [&] { launch_ce_finalize<T>(n, m_run, l_run, ztgt, tgt, inv, dh_acc, Wlm, d, dhf, loss_row, st); });
+    row((double)n * 4, st, [&] { launch_loss_reduce(loss_row, n, inv, losses, c, dev_err, st); });
   }
 
   // backward of the chunk loss into the fast MLPs, with the SGD step fused
@@ -459,7 +578,7 @@ struct Engine : EngineBase {
               hd = cfg.head_dim, ff = cfg.d_ff, Lt = cfg.n_ttt_layers;
     const int lo = L - Lt;
     const int64_t Hhd = (int64_t)H * hd;
-    launch_rmsnorm_bwd<T>(xs[Lt], g_final, rf, dhf, nullptr, n, d, dy, dy_t, st);
+    row((double)n * d * (12 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(xs[Lt], g_final, rf, dhf, nullptr, n, d, dy, dy_t, st); });
     for (int l = L - 1; l >= lo; --l) {
       Stash& S = fstash[l - lo];
       Layer& y = layers[l];
@@ -493,7 +612,7 @@ struct Engine : EngineBase {
       gemm(2 * ff, d, n, dgu, 2 * (int64_t)ff, 1, S.hn, d, 1, e, st, rc);
       if (l == lo) break;
       // through the MLP norm and the residual
-      launch_rmsnorm_bwd<T>(S.h, y.g_mlp, S.r2, dhn, dy, n, d, dh, dh_t, st);
+      row((double)n * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.h, y.g_mlp, S.r2, dhn, dy, n, d, dh, dh_t, st); });
       // dO = dh Wo
       e = epi(EPI_STORE);
       e.out = dO;
@@ -504,15 +623,17 @@ struct Engine : EngineBase {
       a.out = S.o;
       a.Dsum = Dsum;
       a.dqkv = dqkv;
+      a.ws = attn_ws;
+      a.ws_elems = attn_ws_elems;
       attn_bwd(a, st, rc);
-      launch_rope_bwd<T>(dqkv, n, qkv_cols, H + Hkv, hd, cs, st);
+      row((double)n * (H + Hkv) * hd * 2 * sizeof(T), st, [&] { launch_rope_bwd<T>(dqkv, n, qkv_cols, H + Hkv, hd, cs, st); });
       // dxn = [dq dk dv] Wqkv
       e = epi(EPI_STORE);
       e.out_f32 = 1;
       e.out = dxn;
       e.ldo = d;
       gemm(n, d, qkv_cols, dqkv, qkv_cols, 0, y.wqkv, d, 1, e, st, rc);
-      launch_rmsnorm_bwd<T>(S.x, y.g_attn, S.r1, dxn, dh, n, d, dy, dy_t, st);
+      row((double)n * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.x, y.g_attn, S.r1, dxn, dh, n, d, dy, dy_t, st); });
     }
   }
 
@@ -521,6 +642,7 @@ struct Engine : EngineBase {
     int h_err[3];
     CU_TRY(cudaMemcpyAsync(h_err, dev_err, sizeof(h_err), cudaMemcpyDeviceToHost, st));
     CU_TRY(cudaStreamSynchronize(st));
+    if (prof_on) prof_collect();
     if (h_err[2] != 0) {
       err = std::string(what) + ": a device-side check failed (code " + std::to_string(h_err[2]) + ")";
       return TTT_ERR_INTERNAL;
@@ -732,6 +854,7 @@ extern "C" int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* str
     return TTT_ERR_OOM;
   }
   eng->cfg = *cfg;
+  eng->prof_clear();
   const int need = cfg->window + cfg->chunk - 1;
   eng->R = ((need + 127) / 128) * 128;
   eng->qkv_cols = (cfg->n_heads + 2 * cfg->n_kv_heads) * cfg->head_dim;
@@ -740,7 +863,10 @@ extern "C" int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* str
   const char* g = getenv("TTT_GEMM_IMPL");
   const char* a = getenv("TTT_ATTN_IMPL");
   eng->use_tc_gemm = bf && !(g && strcmp(g, "simt") == 0);
+  // TTT_ATTN_IMPL=tc puts attention on the tensor-core kernels for every
+  // shape they support; otherwise the SIMT kernels run
   eng->use_tc_attn = bf && (a && strcmp(a, "tc") == 0);
+  eng->use_tc_attn_bwd = eng->use_tc_attn;
   if (eng->use_tc_gemm) {
     int r = ttt::gemm_tc_init();
     if (r) {
@@ -800,6 +926,26 @@ extern "C" int ttt_get_fast_weights(ttt_ctx* ctx, int32_t block, int32_t which, 
   CTX_GUARD(ctx);
   ctx->eng->err.clear();
   return ctx->eng->get_fast(block, which, dst, (cudaStream_t)stream);
+}
+
+extern "C" int ttt_profile(ttt_ctx* ctx, int32_t on) {
+  CTX_GUARD(ctx);
+  ctx->eng->err.clear();
+  ctx->eng->prof_clear();
+  ctx->eng->prof_on = on != 0;
+  return TTT_OK;
+}
+
+extern "C" int ttt_profile_read(ttt_ctx* ctx, ttt_kernel_stat* out, int32_t cap, int32_t* n_out) {
+  CTX_GUARD(ctx);
+  if (!n_out || (cap > 0 && !out) || cap < 0) {
+    ctx->eng->err = "bad output arguments";
+    return TTT_ERR_INVALID;
+  }
+  const int n = std::min<int>(cap, ttt::EngineBase::P_N);
+  for (int i = 0; i < n; ++i) out[i] = ctx->eng->prof_stat[i];
+  *n_out = ttt::EngineBase::P_N;
+  return TTT_OK;
 }
 
 extern "C" int ttt_reset(ttt_ctx* ctx) {

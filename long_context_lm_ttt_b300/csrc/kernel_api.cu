@@ -48,6 +48,91 @@ extern "C" int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, i
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
 }
 
+static int attn_check(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R) {
+  if (impl != 0 && impl != 1) return TTT_ERR_INVALID;
+  if (n < 0 || H < 1 || Hkv < 1 || H % Hkv || hd < 2 || (hd & 1) || hd > 256 || W < 1 || R < 1)
+    return TTT_ERR_INVALID;
+  if ((int64_t)R < (int64_t)W + n - 1) return TTT_ERR_SHAPE;
+  return 0;
+}
+
+static ttt::AttnArgs attn_args(int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R, int64_t pos0,
+                               const void* q, const void* kring, const void* vring, void* o, float* lse,
+                               int32_t ld_lse) {
+  ttt::AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.kring = kring;
+  a.vring = vring;
+  a.o = o;
+  a.lse = lse;
+  a.ld_lse = ld_lse;
+  a.n = n;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.hd = hd;
+  a.W = W;
+  a.R = R;
+  a.pos0 = pos0;
+  return a;
+}
+
+extern "C" int ttt_kernel_attn_fwd(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W,
+                                   int32_t R, int64_t pos0, const void* q, const void* kring, const void* vring,
+                                   void* o, float* lse, int32_t ld_lse, void* stream) {
+  int rc = attn_check(impl, n, H, Hkv, hd, W, R);
+  if (rc) return rc;
+  if (!q || !kring || !vring || !o || !lse || ld_lse < n) return TTT_ERR_INVALID;
+  if (ensure_err()) return TTT_ERR_OOM;
+  ttt::AttnArgs a = attn_args(n, H, Hkv, hd, W, R, pos0, q, kring, vring, o, lse, ld_lse);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (impl == 0) {
+    if (!ttt::attn_tc_supported(a)) return TTT_ERR_SHAPE;
+    rc = ttt::attn_fwd_tc(a, g_err, st);
+    return rc ? TTT_ERR_CUDA : 0;
+  }
+  ttt::attn_fwd_simt<ttt::bf16>(a, st);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
+}
+
+extern "C" int ttt_kernel_attn_bwd(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W,
+                                   int32_t R, int64_t pos0, const void* q, const void* kring, const void* vring,
+                                   const void* o, const float* lse, int32_t ld_lse, const void* dout, float* dsum,
+                                   void* dqkv, void* stream) {
+  int rc = attn_check(impl, n, H, Hkv, hd, W, R);
+  if (rc) return rc;
+  if (!q || !kring || !vring || !o || !lse || !dout || !dsum || !dqkv || ld_lse < n) return TTT_ERR_INVALID;
+  if (ensure_err()) return TTT_ERR_OOM;
+  ttt::AttnArgs a = attn_args(n, H, Hkv, hd, W, R, pos0, q, kring, vring, nullptr, const_cast<float*>(lse),
+                              ld_lse);
+  a.out = o;
+  a.dout = dout;
+  a.Dsum = dsum;
+  a.dqkv = dqkv;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (impl == 0) {
+    // scratch for this entry point: grown on demand, kept for later calls
+    static float* ws = nullptr;
+    static int64_t ws_elems = 0;
+    const int64_t need = ttt::attn_bwd_tc_ws_elems(n, H, hd, 0);
+    if (need > ws_elems) {
+      if (ws) cudaFree(ws);
+      ws = nullptr;
+      ws_elems = 0;
+      if (cudaMalloc(&ws, need * sizeof(float)) != cudaSuccess) return TTT_ERR_OOM;
+      ws_elems = need;
+    }
+    a.ws = ws;
+    a.ws_elems = ws_elems;
+    if (!ttt::attn_bwd_tc_supported(a)) return TTT_ERR_SHAPE;
+    rc = ttt::attn_bwd_tc(a, g_err, st);
+    if (rc == (int)cudaErrorNotSupported) return TTT_ERR_SHAPE;
+    return rc ? TTT_ERR_CUDA : 0;
+  }
+  ttt::attn_bwd_simt<ttt::bf16>(a, st);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
+}
+
 extern "C" int ttt_kernel_error(void) {
   if (ensure_err()) return TTT_ERR_OOM;
   if (cudaDeviceSynchronize() != cudaSuccess) return TTT_ERR_CUDA;

@@ -82,10 +82,22 @@ struct AttnArgs {
   const void* out;    // forward output o
   float* Dsum;        // [H][ld_lse]
   void* dqkv;         // [n, (H+2Hkv)*hd]: dq | dk | dv
+  float* ws;          // fp32 scratch of the tensor-core backward
+  int64_t ws_elems;   //   (attn_bwd_tc_ws_elems() of the shape)
 };
 template <typename T> void attn_fwd_simt(const AttnArgs& a, cudaStream_t st);
 template <typename T> void attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
-int attn_fwd_tc(const AttnArgs& a, cudaStream_t st);
-int attn_bwd_tc(const AttnArgs& a, cudaStream_t st);
+// tcgen05 kernels (bf16); attn_tc_supported() tells whether the shape and
+// alignment fit them (64 <= hd <= 128, hd % 16 == 0, R % 128 == 0).  They
+// return a cudaError_t; device-side bounded waits that give up write a code
+// into *err.
+bool attn_tc_supported(const AttnArgs& a);
+int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st);
+int attn_bwd_tc(const AttnArgs& a, int* err, cudaStream_t st);
+// the backward additionally needs chunk starts at multiples of 64 and scratch
+bool attn_bwd_tc_supported(const AttnArgs& a);
+// fp32 elements of scratch attn_bwd_tc needs for a chunk of n rows with the
+// given heads (an upper bound over all chunk positions)
+int64_t attn_bwd_tc_ws_elems(int n, int H, int hd, int num_sms);
 
 }  // namespace ttt

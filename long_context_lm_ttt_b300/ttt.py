@@ -33,7 +33,7 @@ TTT_BF16 = 0
 TTT_FP32_CHECK = 1
 
 EXPORTS = ("ttt_create", "ttt_prefill", "ttt_logits", "ttt_get_fast_weights", "ttt_reset",
-           "ttt_destroy", "ttt_last_error")
+           "ttt_destroy", "ttt_last_error", "ttt_profile", "ttt_profile_read")
 
 
 class ttt_config(ctypes.Structure):
@@ -48,6 +48,11 @@ class ttt_weights(ctypes.Structure):
     _fields_ = [("tok_embed", c_void_p), ("final_norm", c_void_p), ("lm_head", c_void_p)] + [
         (name, POINTER(c_void_p)) for name in
         ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down")]
+
+
+class ttt_kernel_stat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 24), ("launches", c_int64), ("ms", ctypes.c_double),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
 
 
 _lib = None
@@ -75,9 +80,21 @@ def load(path: str = LIB_PATH):
     lib.ttt_destroy.restype = None
     lib.ttt_last_error.argtypes = [c_void_p]
     lib.ttt_last_error.restype = c_char_p
+    lib.ttt_profile.argtypes = [c_void_p, c_int32]
+    lib.ttt_profile.restype = c_int32
+    lib.ttt_profile_read.argtypes = [c_void_p, POINTER(ttt_kernel_stat), c_int32, POINTER(c_int32)]
+    lib.ttt_profile_read.restype = c_int32
     lib.ttt_kernel_gemm.argtypes = [c_int32, c_int32, c_int32, c_void_p, c_int64, c_int32, c_void_p,
                                     c_int64, c_int32, c_void_p, c_void_p, c_int64, c_int32, c_void_p]
     lib.ttt_kernel_gemm.restype = c_int32
+    i32 = c_int32
+    lib.ttt_kernel_attn_fwd.argtypes = [i32, i32, i32, i32, i32, i32, i32, c_int64, c_void_p, c_void_p,
+                                        c_void_p, c_void_p, c_void_p, i32, c_void_p]
+    lib.ttt_kernel_attn_fwd.restype = c_int32
+    lib.ttt_kernel_attn_bwd.argtypes = [i32, i32, i32, i32, i32, i32, i32, c_int64, c_void_p, c_void_p,
+                                        c_void_p, c_void_p, c_void_p, i32, c_void_p, c_void_p, c_void_p,
+                                        c_void_p]
+    lib.ttt_kernel_attn_bwd.restype = c_int32
     lib.ttt_kernel_error.argtypes = []
     lib.ttt_kernel_error.restype = c_int32
     _lib = lib
@@ -184,6 +201,22 @@ def ttt_reset(ctx) -> int:
     return rc
 
 
+def ttt_profile(ctx, on: bool) -> int:
+    rc = load().ttt_profile(ctx, 1 if on else 0)
+    _check(rc, ctx)
+    return rc
+
+
+def ttt_profile_read(ctx) -> dict:
+    """{class name: dict(launches, ms, flops, bytes)} of the profiled launches."""
+    buf = (ttt_kernel_stat * 16)()
+    n = c_int32()
+    _check(load().ttt_profile_read(ctx, buf, 16, ctypes.byref(n)), ctx)
+    return {buf[i].name.decode(): dict(launches=int(buf[i].launches), ms=float(buf[i].ms),
+                                       flops=float(buf[i].flops), bytes=float(buf[i].bytes))
+            for i in range(min(n.value, 16))}
+
+
 def ttt_destroy(ctx) -> None:
     if ctx:
         load().ttt_destroy(ctx)
@@ -252,6 +285,12 @@ class TTT:
 
     def reset(self):
         ttt_reset(self.ctx)
+
+    def profile(self, on: bool = True):
+        ttt_profile(self.ctx, on)
+
+    def profile_read(self) -> dict:
+        return ttt_profile_read(self.ctx)
 
     def close(self):
         if self.ctx:

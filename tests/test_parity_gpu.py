@@ -154,3 +154,12 @@ def test_bf16_parity_760m_shape_2_layers():
     w = inputs.make_weights(s)
     tok = inputs.make_tokens(s, 2500)
     compare(s, w, tok, "bf16")
+
+
+def test_bf16_parity_tc_attention_small():
+    """Head dim 64 and chunks of 128 put the attention forward and backward
+    on the tensor-core kernels at a size the oracle runs in seconds; a
+    ragged last chunk and a window shorter than the sequence."""
+    s = inputs.shape("tiny-gqa", n_heads=4, n_kv_heads=2, head_dim=64, d_model=256, d_ff=512, chunk=128,
+                     window=200, seq_len=700, bf16=True)
+    compare(s, inputs.make_weights(s), inputs.make_tokens(s, 700), "bf16")
