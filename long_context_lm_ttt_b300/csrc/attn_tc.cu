@@ -62,7 +62,9 @@ struct FwdSmem {
   static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
   static constexpr int P_OFF = V_OFF + STAGES * KV_BYTES;
   static constexpr int BAR_OFF = P_OFF + P_BYTES;
-  static constexpr int SMEM = BAR_OFF + 256;
+  // at least 80 KB so that no more than two CTAs (2 x 256 TMEM columns)
+  // share an SM
+  static constexpr int SMEM = BAR_OFF + 256 > 80 * 1024 ? BAR_OFF + 256 : 80 * 1024;
 };
 
 struct FwdParams {
@@ -455,7 +457,8 @@ struct DqSmem {
   static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
   static constexpr int DS_OFF = V_OFF + STAGES * KV_BYTES;
   static constexpr int BAR_OFF = DS_OFF + 2 * DS_BYTES;
-  static constexpr int SMEM = BAR_OFF + 256;
+  // at least 120 KB: one CTA (512 TMEM columns) per SM
+  static constexpr int SMEM = BAR_OFF + 256 > 120 * 1024 ? BAR_OFF + 256 : 120 * 1024;
 };
 
 __device__ __forceinline__ void bwd_tile_blocks(const BwdParams& p, int r0, long long* kb0, int* nb) {
@@ -729,7 +732,7 @@ struct DkvSmem {
   static constexpr int PT_OFF = DO_OFF + STAGES * B_BYTES;
   static constexpr int DS_OFF = PT_OFF + 2 * P_BYTES;
   static constexpr int BAR_OFF = DS_OFF + 2 * P_BYTES;
-  static constexpr int SMEM = BAR_OFF + 256;
+  static constexpr int SMEM = BAR_OFF + 256 > 120 * 1024 ? BAR_OFF + 256 : 120 * 1024;
 };
 
 template <int NA>

@@ -8,10 +8,18 @@
 //     (gate f -> row 2f, up f -> row 2f+1) so SwiGLU pairs are adjacent too;
 //   * fp32 masters of the fast weights (the MLPs of the last n_ttt_layers
 //     blocks) and a copy of their initial values for ttt_reset;
-//   * per layer a key/value ring of R >= W+b-1 slots (position p in slot
-//     p mod R), constant in the sequence length;
-//   * the activations of one chunk (all of them for the fast blocks, which
-//     the backward needs; one scratch set for the static blocks).
+//   * per layer a key/value ring (position p in slot p mod R_l), constant in
+//     the sequence length: R >= W+b-1 slots for the fast blocks, R_s >=
+//     W+S-1 for the static ones;
+//   * the activations of one chunk for the fast blocks (the backward needs
+//     them all) and one scratch set of S rows for the static blocks.
+//
+// The static blocks [0, L-n_ttt_layers) never change, so their outputs do
+// not depend on any test-time update: ttt_prefill runs them over
+// super-chunks of S tokens (a multiple of b) with large-M GEMMs, then runs
+// the chunk loop (fast blocks forward, cross-entropy, backward, SGD) over
+// the chunks of that super-chunk.  Every value is the one the chunk-by-chunk
+// order produces; only the batching of the frozen part differs.
 // The residual stream, norm statistics, softmax statistics and all
 // gradients that cross kernels in fp32 stay fp32; matrices fed to GEMMs are
 // in T.
@@ -80,7 +88,7 @@ struct Status {
 struct EngineBase {
   ttt_config cfg;
   std::string err;
-  int R = 0, qkv_cols = 0, Vs = 0, num_sms = 148;
+  int R = 0, R_s = 0, S_bulk = 0, qkv_cols = 0, Vs = 0, num_sms = 148;
   int64_t pos = 0;
   bool used = false;
   bool use_tc_gemm = false, use_tc_attn = false, use_tc_attn_bwd = false;
@@ -170,6 +178,7 @@ struct Engine : EngineBase {
     T *wgu_lo = nullptr, *wd_lo = nullptr;              // bf16 fast layers: w ~ hi + lo
     float *wgu32_init = nullptr, *wd32_init = nullptr;  // for ttt_reset
     T *kring = nullptr, *vring = nullptr;
+    int R = 0;  // ring slots
   };
   struct Stash {
     float* x = nullptr;  // layer input (fp32)
@@ -183,10 +192,16 @@ struct Engine : EngineBase {
     float* r2 = nullptr;
     T* gu = nullptr;
     T* a = nullptr;
+    int ld_lse = 0;
   };
   std::vector<Layer> layers;
   std::vector<Stash> fstash;  // fast blocks
-  Stash sstash;               // static blocks (scratch)
+  Stash sstash;               // static blocks, one chunk (ttt_logits)
+  Stash bstash;               // static blocks, one super-chunk (ttt_prefill)
+  float* bx[2] = {nullptr, nullptr};  // residual stream of the bulk pass
+  float* x_lo = nullptr;      // input of the first fast block, S rows
+  float2* cs_bulk = nullptr;  // RoPE table of the super-chunk
+  const float2* cs_cur = nullptr;  // RoPE table of the chunk being processed
   T *E = nullptr, *Wlm = nullptr;
   float* g_final = nullptr;
   float* xlow[2] = {nullptr, nullptr};
@@ -269,10 +284,11 @@ struct Engine : EngineBase {
       A_TRY(y.wo, (size_t)d * Hhd);
       A_TRY(y.wgu, (size_t)2 * ff * d);
       A_TRY(y.wd, (size_t)d * ff);
-      A_TRY(y.kring, (size_t)Hkv * R * hd);
-      A_TRY(y.vring, (size_t)Hkv * R * hd);
-      CU_TRY(cudaMemsetAsync(y.kring, 0, sizeof(T) * (size_t)Hkv * R * hd, st));
-      CU_TRY(cudaMemsetAsync(y.vring, 0, sizeof(T) * (size_t)Hkv * R * hd, st));
+      y.R = fast ? R : R_s;
+      A_TRY(y.kring, (size_t)Hkv * y.R * hd);
+      A_TRY(y.vring, (size_t)Hkv * y.R * hd);
+      CU_TRY(cudaMemsetAsync(y.kring, 0, sizeof(T) * (size_t)Hkv * y.R * hd, st));
+      CU_TRY(cudaMemsetAsync(y.vring, 0, sizeof(T) * (size_t)Hkv * y.R * hd, st));
       if (!w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo || !w->mlp_norm || !w->w_gate ||
           !w->w_up || !w->w_down) {
         err = "null per-layer weight array";
@@ -312,25 +328,33 @@ struct Engine : EngineBase {
       }
     }
     // activations of one chunk
-    auto alloc_stash = [&](Stash& s, bool fast) -> int {
-      A_TRY(s.xn, (size_t)b * d);
-      A_TRY(s.r1, b);
-      A_TRY(s.q, (size_t)b * Hhd);
-      A_TRY(s.o, (size_t)b * Hhd);
-      A_TRY(s.lse, (size_t)H * b);
-      A_TRY(s.h, (size_t)b * d);
-      A_TRY(s.hn, (size_t)b * d);
-      A_TRY(s.r2, b);
-      A_TRY(s.a, (size_t)b * ff);
-      if (fast) A_TRY(s.gu, (size_t)b * 2 * ff);
+    auto alloc_stash = [&](Stash& s, bool fast, int rows) -> int {
+      A_TRY(s.xn, (size_t)rows * d);
+      A_TRY(s.r1, rows);
+      A_TRY(s.q, (size_t)rows * Hhd);
+      A_TRY(s.o, (size_t)rows * Hhd);
+      A_TRY(s.lse, (size_t)H * rows);
+      A_TRY(s.h, (size_t)rows * d);
+      A_TRY(s.hn, (size_t)rows * d);
+      A_TRY(s.r2, rows);
+      A_TRY(s.a, (size_t)rows * ff);
+      if (fast) A_TRY(s.gu, (size_t)rows * 2 * ff);
+      s.ld_lse = rows;
       return TTT_OK;
     };
-    if ((rc = alloc_stash(sstash, false))) return rc;
+    if ((rc = alloc_stash(sstash, false, b))) return rc;
+    if (L - Lt > 0) {
+      if ((rc = alloc_stash(bstash, false, S_bulk))) return rc;
+      A_TRY(bx[0], (size_t)S_bulk * d);
+      A_TRY(bx[1], (size_t)S_bulk * d);
+    }
+    A_TRY(x_lo, (size_t)S_bulk * d);
+    A_TRY(cs_bulk, (size_t)S_bulk * (hd / 2));
     fstash.resize(Lt);
     xs.resize(Lt + 1);
     for (int i = 0; i <= Lt; ++i) A_TRY(xs[i], (size_t)b * d);
     for (int i = 0; i < Lt; ++i) {
-      if ((rc = alloc_stash(fstash[i], true))) return rc;
+      if ((rc = alloc_stash(fstash[i], true, b))) return rc;
       fstash[i].x = xs[i];
     }
     A_TRY(xlow[0], (size_t)b * d);
@@ -429,13 +453,13 @@ struct Engine : EngineBase {
     a.vring = y.vring;
     a.o = S.o;
     a.lse = S.lse;
-    a.ld_lse = cfg.chunk;
+    a.ld_lse = S.ld_lse;
     a.n = n;
     a.H = cfg.n_heads;
     a.Hkv = cfg.n_kv_heads;
     a.hd = cfg.head_dim;
     a.W = cfg.window;
-    a.R = R;
+    a.R = y.R;
     a.pos0 = s;
     return a;
   }
@@ -485,59 +509,94 @@ struct Engine : EngineBase {
     prof(P_ROW, 0.0, bytes, st, launch);
   }
 
-  // forward of positions [s, s+n) with the current weights; leaves the final
-  // normed hidden state in hf (T) and its statistics in rf.
-  void forward(const int32_t* tok_chunk, int64_t s, int n, cudaStream_t st, int* rc) {
-    const int L = cfg.n_layers, d = cfg.d_model, H = cfg.n_heads, hd = cfg.head_dim, ff = cfg.d_ff,
-              Lt = cfg.n_ttt_layers;
-    const int lo = L - Lt;
+  // one decoder block over rows [0, n) at positions s..s+n-1 (RoPE table
+  // cs_), from x_in to x_out, keeping its intermediates in S
+  void block_fwd(int l, Stash& S, const float* x_in, float* x_out, const float2* cs_, int64_t s, int n,
+                 cudaStream_t st, int* rc) {
+    const int d = cfg.d_model, H = cfg.n_heads, hd = cfg.head_dim, ff = cfg.d_ff;
+    const bool fast = l >= cfg.n_layers - cfg.n_ttt_layers;
     const int64_t Hhd = (int64_t)H * hd;
-    row((double)n * hd * 4, st, [&] { launch_rope_table(s, n, hd, cfg.rope_theta, cs, st); });
-    float* x_in = lo == 0 ? xs[0] : xlow[0];
-    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_embed<T>(tok_chunk, n, E, d, x_in, cfg.vocab, dev_err + 1, st); });
-    for (int l = 0; l < L; ++l) {
-      const bool fast = l >= lo;
-      Stash& S = fast ? fstash[l - lo] : sstash;
-      Layer& y = layers[l];
-      float* x_out = (l + 1 >= lo) ? xs[l + 1 - lo] : xlow[(l + 1) & 1];
-      row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(x_in, y.g_attn, n, d, cfg.norm_eps, S.xn, S.r1, st); });
-      Epi e = epi(EPI_QKV);
-      e.out = S.q;
-      e.ldo = Hhd;
-      e.n_q = H;
-      e.n_kv = cfg.n_kv_heads;
-      e.hd = hd;
-      e.pos0 = s;
-      e.ring = R;
-      e.kring = y.kring;
-      e.vring = y.vring;
-      e.rope_cs = cs;
-      gemm(n, qkv_cols, d, S.xn, d, 0, y.wqkv, d, 0, e, st, rc);
-      attn_fwd(attn_args(S, y, s, n), st, rc);
-      e = epi(EPI_RESID);
-      e.out = S.h;
-      e.ldo = d;
-      e.resid = x_in;
-      e.ldr = d;
-      gemm(n, d, (int)Hhd, S.o, Hhd, 0, y.wo, Hhd, 0, e, st, rc);
-      row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(S.h, y.g_mlp, n, d, cfg.norm_eps, S.hn, S.r2, st); });
-      e = epi(EPI_SWIGLU);
-      e.out = S.a;
-      e.ldo = ff;
-      e.stash = fast ? S.gu : nullptr;
-      e.ld_stash = 2 * (int64_t)ff;
-      // fast weights in bf16 mode are read as the pair hi + lo, so updates
-      // below one bf16 ulp still reach the forward
-      gemm(n, 2 * ff, d, S.hn, d, 0, y.wgu, d, 0, e, st, rc, y.wgu_lo);
-      e = epi(EPI_RESID);
-      e.out = x_out;
-      e.ldo = d;
-      e.resid = S.h;
-      e.ldr = d;
-      gemm(n, d, ff, S.a, ff, 0, y.wd, ff, 0, e, st, rc, y.wd_lo);
-      x_in = x_out;
+    Layer& y = layers[l];
+    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(x_in, y.g_attn, n, d, cfg.norm_eps, S.xn, S.r1, st); });
+    Epi e = epi(EPI_QKV);
+    e.out = S.q;
+    e.ldo = Hhd;
+    e.n_q = H;
+    e.n_kv = cfg.n_kv_heads;
+    e.hd = hd;
+    e.pos0 = s;
+    e.ring = y.R;
+    e.kring = y.kring;
+    e.vring = y.vring;
+    e.rope_cs = cs_;
+    gemm(n, qkv_cols, d, S.xn, d, 0, y.wqkv, d, 0, e, st, rc);
+    attn_fwd(attn_args(S, y, s, n), st, rc);
+    e = epi(EPI_RESID);
+    e.out = S.h;
+    e.ldo = d;
+    e.resid = x_in;
+    e.ldr = d;
+    gemm(n, d, (int)Hhd, S.o, Hhd, 0, y.wo, Hhd, 0, e, st, rc);
+    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(S.h, y.g_mlp, n, d, cfg.norm_eps, S.hn, S.r2, st); });
+    e = epi(EPI_SWIGLU);
+    e.out = S.a;
+    e.ldo = ff;
+    e.stash = fast ? S.gu : nullptr;
+    e.ld_stash = 2 * (int64_t)ff;
+    // fast weights in bf16 mode are read as the pair hi + lo, so updates
+    // below one bf16 ulp still reach the forward
+    gemm(n, 2 * ff, d, S.hn, d, 0, y.wgu, d, 0, e, st, rc, y.wgu_lo);
+    e = epi(EPI_RESID);
+    e.out = x_out;
+    e.ldo = d;
+    e.resid = S.h;
+    e.ldr = d;
+    gemm(n, d, ff, S.a, ff, 0, y.wd, ff, 0, e, st, rc, y.wd_lo);
+  }
+
+  // static blocks over a super-chunk [s0, s0+n): embedding, blocks
+  // [0, L-n_ttt_layers); leaves the input of the first fast block in x_lo
+  // and the super-chunk's RoPE table in cs_bulk
+  void static_fwd(const int32_t* tok, int64_t s0, int n, cudaStream_t st, int* rc) {
+    const int d = cfg.d_model, hd = cfg.head_dim, lo = cfg.n_layers - cfg.n_ttt_layers;
+    row((double)n * hd * 4, st, [&] { launch_rope_table(s0, n, hd, cfg.rope_theta, cs_bulk, st); });
+    float* x = lo == 0 ? x_lo : bx[0];
+    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_embed<T>(tok, n, E, d, x, cfg.vocab, dev_err + 1, st); });
+    for (int l = 0; l < lo; ++l) {
+      float* x_out = l + 1 == lo ? x_lo : bx[(l + 1) & 1];
+      block_fwd(l, bstash, x, x_out, cs_bulk, s0, n, st, rc);
+      x = x_out;
     }
-    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(x_in, g_final, n, d, cfg.norm_eps, hf, rf, st); });
+  }
+
+  // fast blocks of positions [s, s+n) from x_in (the output of the static
+  // blocks), then the final norm: leaves the normed hidden state in hf and
+  // its statistics in rf
+  void fast_fwd(const float* x_in, const float2* cs_, int64_t s, int n, cudaStream_t st, int* rc) {
+    const int L = cfg.n_layers, d = cfg.d_model, Lt = cfg.n_ttt_layers, lo = L - Lt;
+    cs_cur = cs_;
+    fstash[0].x = const_cast<float*>(x_in);
+    const float* x = x_in;
+    for (int l = lo; l < L; ++l) {
+      float* x_out = xs[l + 1 - lo];
+      block_fwd(l, fstash[l - lo], x, x_out, cs_, s, n, st, rc);
+      x = x_out;
+    }
+    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(x, g_final, n, d, cfg.norm_eps, hf, rf, st); });
+  }
+
+  // every block for a span of at most b positions (ttt_logits)
+  void forward_all(const int32_t* tok, int64_t s, int n, cudaStream_t st, int* rc) {
+    const int d = cfg.d_model, hd = cfg.head_dim, lo = cfg.n_layers - cfg.n_ttt_layers;
+    row((double)n * hd * 4, st, [&] { launch_rope_table(s, n, hd, cfg.rope_theta, cs, st); });
+    float* x = xlow[0];
+    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_embed<T>(tok, n, E, d, x, cfg.vocab, dev_err + 1, st); });
+    for (int l = 0; l < lo; ++l) {
+      float* x_out = xlow[(l + 1) & 1];
+      block_fwd(l, sstash, x, x_out, cs, s, n, st, rc);
+      x = x_out;
+    }
+    fast_fwd(x, cs, s, n, st, rc);
   }
 
   // streamed lm_head + cross-entropy: loss of chunk c into losses[c] and the
@@ -626,7 +685,7 @@ struct Engine : EngineBase {
       a.ws = attn_ws;
       a.ws_elems = attn_ws_elems;
       attn_bwd(a, st, rc);
-      row((double)n * (H + Hkv) * hd * 2 * sizeof(T), st, [&] { launch_rope_bwd<T>(dqkv, n, qkv_cols, H + Hkv, hd, cs, st); });
+      row((double)n * (H + Hkv) * hd * 2 * sizeof(T), st, [&] { launch_rope_bwd<T>(dqkv, n, qkv_cols, H + Hkv, hd, cs_cur, st); });
       // dxn = [dq dk dv] Wqkv
       e = epi(EPI_STORE);
       e.out_f32 = 1;
@@ -688,18 +747,23 @@ struct Engine : EngineBase {
     int rc = clear_err(st);
     if (rc) return rc;
     used = true;
-    for (int c = 0; c < nC && rc == TTT_OK; ++c) {
-      const int64_t s = (int64_t)c * b;
-      const int n = (int)std::min<int64_t>(b, n_tok - s);
-      const int n_tgt = (int)std::min<int64_t>(n, n_tok - 1 - s);
-      forward(tok_d + s, s, n, st, &rc);
-      if (n_tgt <= 0) {
-        CU_TRY(cudaMemsetAsync(loss_d + c, 0, sizeof(float), st));
-        continue;
+    const int d = cfg.d_model, hd = cfg.head_dim;
+    for (int64_t s0 = 0; s0 < n_tok && rc == TTT_OK; s0 += S_bulk) {
+      const int sn = (int)std::min<int64_t>(S_bulk, n_tok - s0);
+      static_fwd(tok_d + s0, s0, sn, st, &rc);
+      for (int64_t s = s0; s < s0 + sn && rc == TTT_OK; s += b) {
+        const int c = (int)(s / b);
+        const int n = (int)std::min<int64_t>(b, n_tok - s);
+        const int n_tgt = (int)std::min<int64_t>(n, n_tok - 1 - s);
+        fast_fwd(x_lo + (s - s0) * d, cs_bulk + (s - s0) * (hd / 2), s, n, st, &rc);
+        if (n_tgt <= 0) {
+          CU_TRY(cudaMemsetAsync(loss_d + c, 0, sizeof(float), st));
+          continue;
+        }
+        cross_entropy(tok_d, n_tok, s, n, n_tgt, loss_d, c, st, &rc);
+        backward(s, n, st, &rc);
+        CU_TRY(cudaPeekAtLastError());
       }
-      cross_entropy(tok_d, n_tok, s, n, n_tgt, loss_d, c, st, &rc);
-      backward(s, n, st, &rc);
-      CU_TRY(cudaPeekAtLastError());
     }
     if (rc) return rc;
     pos = n_tok;
@@ -730,7 +794,7 @@ struct Engine : EngineBase {
     }
     int rc = clear_err(st);
     if (rc) return rc;
-    forward(c_d, pos, n, st, &rc);
+    forward_all(c_d, pos, n, st, &rc);
     Epi e = epi(EPI_STORE);
     e.out_f32 = 1;
     e.out = o;
@@ -763,21 +827,23 @@ struct Engine : EngineBase {
     const int L = cfg.n_layers, d = cfg.d_model, ff = cfg.d_ff, Hkv = cfg.n_kv_heads, hd = cfg.head_dim;
     for (int l = 0; l < L; ++l) {
       Layer& y = layers[l];
-      CU_TRY(cudaMemsetAsync(y.kring, 0, sizeof(T) * (size_t)Hkv * R * hd, st));
-      CU_TRY(cudaMemsetAsync(y.vring, 0, sizeof(T) * (size_t)Hkv * R * hd, st));
+      CU_TRY(cudaMemsetAsync(y.kring, 0, sizeof(T) * (size_t)Hkv * y.R * hd, st));
+      CU_TRY(cudaMemsetAsync(y.vring, 0, sizeof(T) * (size_t)Hkv * y.R * hd, st));
       if (l >= L - cfg.n_ttt_layers) {
         CU_TRY(cudaMemcpyAsync(y.wgu32, y.wgu32_init, sizeof(float) * 2 * ff * (size_t)d,
                                cudaMemcpyDeviceToDevice, st));
         CU_TRY(cudaMemcpyAsync(y.wd32, y.wd32_init, sizeof(float) * (size_t)d * ff,
                                cudaMemcpyDeviceToDevice, st));
         if (kBF16) {
-          launch_split_bf16(y.wgu32, 2 * (int64_t)ff * d, (bf16*)y.wgu, (bf16*)y.wgu_lo, st);
-          launch_split_bf16(y.wd32, (int64_t)d * ff, (bf16*)y.wd, (bf16*)y.wd_lo, st);
+          const double nb = 2.0 * ff * d;
+          row(nb * 8, st, [&] { launch_split_bf16(y.wgu32, 2 * (int64_t)ff * d, (bf16*)y.wgu, (bf16*)y.wgu_lo, st); });
+          row(nb * 4, st, [&] { launch_split_bf16(y.wd32, (int64_t)d * ff, (bf16*)y.wd, (bf16*)y.wd_lo, st); });
         }
       }
     }
     CU_TRY(cudaGetLastError());
     CU_TRY(cudaStreamSynchronize(st));
+    if (prof_on) prof_collect();
     pos = 0;
     used = false;
     return TTT_OK;
@@ -857,15 +923,25 @@ extern "C" int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* str
   eng->prof_clear();
   const int need = cfg->window + cfg->chunk - 1;
   eng->R = ((need + 127) / 128) * 128;
+  // super-chunk of the bulk static pass: a multiple of b, about 16K tokens,
+  // never more than the longest sequence needs
+  {
+    const int64_t b = cfg->chunk;
+    const int64_t want = std::max<int64_t>(b, (16384 / b) * b);
+    const int64_t cap = ((cfg->max_tokens + b - 1) / b) * b;
+    eng->S_bulk = (int)std::min(want, cap);
+    const int64_t need_s = (int64_t)cfg->window + eng->S_bulk - 1;
+    eng->R_s = (int)(((need_s + 127) / 128) * 128);
+  }
   eng->qkv_cols = (cfg->n_heads + 2 * cfg->n_kv_heads) * cfg->head_dim;
   eng->Vs = std::min(cfg->vocab, 8192);
   const bool bf = cfg->precision == TTT_BF16;
   const char* g = getenv("TTT_GEMM_IMPL");
   const char* a = getenv("TTT_ATTN_IMPL");
   eng->use_tc_gemm = bf && !(g && strcmp(g, "simt") == 0);
-  // TTT_ATTN_IMPL=tc puts attention on the tensor-core kernels for every
-  // shape they support; otherwise the SIMT kernels run
-  eng->use_tc_attn = bf && (a && strcmp(a, "tc") == 0);
+  // attention runs on the tensor-core kernels for every shape they support;
+  // TTT_ATTN_IMPL=simt keeps it on the SIMT kernels (a GPU-side cross-check)
+  eng->use_tc_attn = bf && !(a && strcmp(a, "simt") == 0);
   eng->use_tc_attn_bwd = eng->use_tc_attn;
   if (eng->use_tc_gemm) {
     int r = ttt::gemm_tc_init();
