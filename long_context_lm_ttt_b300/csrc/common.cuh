@@ -86,6 +86,9 @@ struct Epi {
   const float* alpha;
   const float* beta;
   int first;              // 1: ignore the old content of out
+  // set by the tensor-core launcher: every pointer and row pitch the
+  // epilogue touches allows 16-byte vector access (epi_row32 below)
+  int vec;
 };
 
 // Apply the epilogue to columns (n, n+1) of row m.  T is the element type of
@@ -170,6 +173,208 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, f
         const float al = e.alpha[m];
         float2 c = load2<float>(o);
         store2<float>(o, c.x * al + v0 * be, c.y * al + v1 * be);
+      }
+    } break;
+    default: break;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Row-chunk form of the epilogues for the tensor-core GEMM: one thread owns
+// one output row and applies the epilogue to 32 consecutive accumulator
+// columns [col0, col0+32) at once, with 16-byte loads and stores.  The
+// operand the epilogue reads besides the accumulator (its "source": the
+// residual, the fp32 master weight, the running dh, the (g, u) stash, or
+// the RoPE (cos, sin) pairs) is exactly 128 bytes per row chunk; it is
+// fetched by epi_src_load ahead of use so the load latency overlaps the
+// previous chunk.  Requires e.vec, col0 + 32 <= N and, for EPI_QKV,
+// hd % 32 == 0 (a chunk never straddles two heads); otherwise the caller
+// falls back to epi_pair.  bf16 activations only.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ldg16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ void stg16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+__device__ __forceinline__ uint32_t bf2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unbf2(uint32_t u) {
+  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
+  return __bfloat1622float2(h);
+}
+
+__device__ __forceinline__ bool epi_has_src(const Epi& e) {
+  switch (e.kind) {
+    case EPI_RESID:
+    case EPI_SGD:
+    case EPI_SWIGLU_BWD:
+      return true;
+    case EPI_CE_ACC:
+      return !e.first;
+    case EPI_QKV:
+      return true;
+    default:
+      return false;
+  }
+}
+
+__device__ __forceinline__ void epi_src_load(const Epi& e, int m, int col0, uint4 (&src)[8]) {
+  const uint8_t* p = nullptr;
+  switch (e.kind) {
+    case EPI_RESID: p = (const uint8_t*)(e.resid + (int64_t)m * e.ldr + col0); break;
+    case EPI_SGD: p = (const uint8_t*)(e.w32 + (int64_t)m * e.ldo + col0); break;
+    case EPI_CE_ACC: p = (const uint8_t*)((const float*)e.out + (int64_t)m * e.ldo + col0); break;
+    case EPI_SWIGLU_BWD: p = (const uint8_t*)((const bf16*)e.stash + (int64_t)m * e.ld_stash + 2 * col0); break;
+    case EPI_QKV: {
+      const int hd = e.hd;
+      if (col0 >= (e.n_q + e.n_kv) * hd) return;  // values: no rotation
+      p = (const uint8_t*)(e.rope_cs + (int64_t)m * (hd >> 1) + ((col0 % hd) >> 1));
+    } break;
+    default: return;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) src[i] = ldg16(p + 16 * i);
+}
+
+__device__ __forceinline__ void epi_row32(const Epi& e, int m, int col0, const float (&v)[32],
+                                          const uint4 (&src)[8]) {
+  const float* sf = reinterpret_cast<const float*>(src);      // 32 fp32 sources
+  const uint32_t* su = reinterpret_cast<const uint32_t*>(src);
+  switch (e.kind) {
+    case EPI_STORE: {
+      if (e.out_f32) {
+        float* o = (float*)e.out + (int64_t)m * e.ldo + col0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          stg16(o + 4 * i, make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                                      __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])));
+      } else {
+        bf16* o = (bf16*)e.out + (int64_t)m * e.ldo + col0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          stg16(o + 8 * i, make_uint4(bf2(v[8 * i], v[8 * i + 1]), bf2(v[8 * i + 2], v[8 * i + 3]),
+                                      bf2(v[8 * i + 4], v[8 * i + 5]), bf2(v[8 * i + 6], v[8 * i + 7])));
+      }
+    } break;
+    case EPI_RESID: {
+      float* o = (float*)e.out + (int64_t)m * e.ldo + col0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        stg16(o + 4 * i, make_uint4(__float_as_uint(sf[4 * i] + v[4 * i]), __float_as_uint(sf[4 * i + 1] + v[4 * i + 1]),
+                                    __float_as_uint(sf[4 * i + 2] + v[4 * i + 2]),
+                                    __float_as_uint(sf[4 * i + 3] + v[4 * i + 3])));
+    } break;
+    case EPI_QKV: {
+      const int hd = e.hd;
+      const int qcols = e.n_q * hd, kcols = e.n_kv * hd;
+      float r[32];
+      if (col0 < qcols + kcols) {
+        const float2* cs = reinterpret_cast<const float2*>(src);
+#pragma unroll
+        for (int p = 0; p < 16; ++p) {
+          r[2 * p] = v[2 * p] * cs[p].x - v[2 * p + 1] * cs[p].y;
+          r[2 * p + 1] = v[2 * p + 1] * cs[p].x + v[2 * p] * cs[p].y;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = v[k];
+      }
+      bf16* o;
+      if (col0 < qcols) {
+        o = (bf16*)e.out + (int64_t)m * e.ldo + col0;
+      } else {
+        const bool is_k = col0 < qcols + kcols;
+        const int c = col0 - (is_k ? qcols : qcols + kcols);
+        const int64_t slot = (e.pos0 + m) % e.ring;
+        o = (bf16*)(is_k ? e.kring : e.vring) + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        stg16(o + 8 * i, make_uint4(bf2(r[8 * i], r[8 * i + 1]), bf2(r[8 * i + 2], r[8 * i + 3]),
+                                    bf2(r[8 * i + 4], r[8 * i + 5]), bf2(r[8 * i + 6], r[8 * i + 7])));
+    } break;
+    case EPI_SWIGLU: {
+      float a[16];
+#pragma unroll
+      for (int p = 0; p < 16; ++p) a[p] = v[2 * p] * sigmoidf_(v[2 * p]) * v[2 * p + 1];
+      bf16* o = (bf16*)e.out + (int64_t)m * e.ldo + (col0 >> 1);
+      stg16(o, make_uint4(bf2(a[0], a[1]), bf2(a[2], a[3]), bf2(a[4], a[5]), bf2(a[6], a[7])));
+      stg16(o + 8, make_uint4(bf2(a[8], a[9]), bf2(a[10], a[11]), bf2(a[12], a[13]), bf2(a[14], a[15])));
+      if (e.stash) {
+        bf16* st = (bf16*)e.stash + (int64_t)m * e.ld_stash + col0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          stg16(st + 8 * i, make_uint4(bf2(v[8 * i], v[8 * i + 1]), bf2(v[8 * i + 2], v[8 * i + 3]),
+                                       bf2(v[8 * i + 4], v[8 * i + 5]), bf2(v[8 * i + 6], v[8 * i + 7])));
+      }
+    } break;
+    case EPI_SWIGLU_BWD: {
+      // columns are d_ff indices f; the stash holds (g, u) at 2f, 2f+1 and
+      // the outputs (dg, du) go to the same places of out
+      uint32_t r[32];
+#pragma unroll
+      for (int f = 0; f < 32; ++f) {
+        const float2 gu = unbf2(su[f]);
+        const float sg = sigmoidf_(gu.x);
+        const float dg = v[f] * gu.y * sg * (1.0f + gu.x * (1.0f - sg));
+        const float du = v[f] * gu.x * sg;
+        r[f] = bf2(dg, du);
+      }
+      bf16* o = (bf16*)e.out + (int64_t)m * e.ldo + 2 * col0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) stg16(o + 8 * i, make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]));
+    } break;
+    case EPI_SGD: {
+      float w[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) w[k] = sf[k] - e.lr * v[k];
+      float* wp = e.w32 + (int64_t)m * e.ldo + col0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        stg16(wp + 4 * i, make_uint4(__float_as_uint(w[4 * i]), __float_as_uint(w[4 * i + 1]),
+                                     __float_as_uint(w[4 * i + 2]), __float_as_uint(w[4 * i + 3])));
+      if (e.w16) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int p = 0; p < 16; ++p) {
+          hi[p] = bf2(w[2 * p], w[2 * p + 1]);
+          const float2 hf = unbf2(hi[p]);
+          lo[p] = bf2(w[2 * p] - hf.x, w[2 * p + 1] - hf.y);
+        }
+        bf16* hp = (bf16*)e.w16 + (int64_t)m * e.ldo + col0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) stg16(hp + 8 * i, make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]));
+        if (e.w16lo) {
+          bf16* lp = (bf16*)e.w16lo + (int64_t)m * e.ldo + col0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            stg16(lp + 8 * i, make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]));
+        }
+      }
+    } break;
+    case EPI_CE_Z: {
+      float* o = (float*)e.out + (int64_t)m * e.ldo + col0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        stg16(o + 4 * i, make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                                    __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])));
+      const int64_t t = (int64_t)e.tgt[m] - e.col0 - col0;
+      if (t >= 0 && t < 32) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (k == t) e.ztgt[m] = v[k];
+      }
+    } break;
+    case EPI_CE_ACC: {
+      float* o = (float*)e.out + (int64_t)m * e.ldo + col0;
+      const float be = e.beta[m];
+      const float al = e.first ? 0.f : e.alpha[m];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) r[k] = e.first ? v[4 * i + k] * be : sf[4 * i + k] * al + v[4 * i + k] * be;
+        stg16(o + 4 * i, make_uint4(__float_as_uint(r[0]), __float_as_uint(r[1]), __float_as_uint(r[2]),
+                                    __float_as_uint(r[3])));
       }
     } break;
     default: break;

@@ -203,27 +203,44 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
+    // Thread i of a warp owns TMEM lane (tile row) i and applies the
+    // epilogue to its row 32 columns at a time (epi_row32: 16-byte loads and
+    // stores).  The source operand of the next chunk is loaded before the
+    // current chunk is processed, the first chunk's before the accumulator
+    // is waited for, so global-load latency overlaps useful work.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const bool has_src = epi_has_src(e);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      if (!tc::mbar_wait(tfull0 + 8 * acc, acc_phase, err, ERR_WAIT_EPI, abort)) break;
-      tc::tc_fence_after();
       const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
       const int row = m0 + quarter * 32 + lane;
+      const int nch = min(BN, N - n0 + 31) / 32;  // chunks with columns < N
+      auto vec_chunk = [&](int c) { return e.vec && n0 + 32 * c + 32 <= N; };
+      uint4 src[8];
+      if (has_src && row < M && vec_chunk(0)) epi_src_load(e, row, n0, src);
+      if (!tc::mbar_wait(tfull0 + 8 * acc, acc_phase, err, ERR_WAIT_EPI, abort)) break;
+      tc::tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        if (n0 + c * 32 >= N) break;  // warp-uniform
+      for (int c = 0; c < nch; ++c) {
         float v[32];
         tc::tmem_ld32(tbase + c * 32, v);
+        uint4 nxt[8];
+        if (has_src && row < M && c + 1 < nch && vec_chunk(c + 1)) epi_src_load(e, row, n0 + 32 * (c + 1), nxt);
         if (row < M) {
+          if (vec_chunk(c)) {
+            epi_row32(e, row, n0 + 32 * c, v, src);
+          } else {
 #pragma unroll
-          for (int p = 0; p < 16; ++p) {
-            const int col = n0 + c * 32 + 2 * p;
-            if (col < N) epi_pair<bf16>(e, row, col, v[2 * p], v[2 * p + 1]);
+            for (int p = 0; p < 16; ++p) {
+              const int col = n0 + c * 32 + 2 * p;
+              if (col < N) epi_pair<bf16>(e, row, col, v[2 * p], v[2 * p + 1]);
+            }
           }
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) src[i] = nxt[i];
       }
       tc::tc_fence_before();
       tc::mbar_arrive(tempty0 + 8 * acc);
@@ -313,7 +330,29 @@ int gemm_tc_init() {
   return g_init_rc;
 }
 
-int gemm_tc(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st) {
+// may the epilogue of g use 16-byte vector accesses (epi_row32)?
+static bool a16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+static bool epi_vec_ok(const Epi& e) {
+  const int64_t o4 = e.ldo * 4, o2 = e.ldo * 2;
+  switch (e.kind) {
+    case EPI_STORE: return a16(e.out) && ((e.out_f32 ? o4 : o2) % 16 == 0);
+    case EPI_RESID: return a16(e.out) && a16(e.resid) && o4 % 16 == 0 && (e.ldr * 4) % 16 == 0;
+    case EPI_QKV:
+      return e.hd % 32 == 0 && a16(e.out) && a16(e.kring) && a16(e.vring) && a16(e.rope_cs) && o2 % 16 == 0;
+    case EPI_SWIGLU:
+      return a16(e.out) && o2 % 16 == 0 && (!e.stash || (a16(e.stash) && (e.ld_stash * 2) % 16 == 0));
+    case EPI_SWIGLU_BWD: return a16(e.out) && a16(e.stash) && o2 % 16 == 0 && (e.ld_stash * 2) % 16 == 0;
+    case EPI_SGD:
+      return a16(e.w32) && o4 % 16 == 0 && (!e.w16 || a16(e.w16)) && (!e.w16lo || a16(e.w16lo));
+    case EPI_CE_Z:
+    case EPI_CE_ACC: return a16(e.out) && o4 % 16 == 0;
+    default: return false;
+  }
+}
+
+int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st) {
+  GemmArgs<bf16> g = g_in;
+  g.e.vec = epi_vec_ok(g.e) ? 1 : 0;
   if (g.M <= 0 || g.N <= 0) return 0;
   if (!g_encode) return (int)cudaErrorNotSupported;
   // TMA: 16-byte aligned base and row pitch
