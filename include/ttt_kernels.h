@@ -58,6 +58,28 @@ int ttt_kernel_attn_bwd(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t
                         const float* lse, int32_t ld_lse, const void* dout, float* dsum, void* dqkv,
                         void* stream);
 
+/* The tensor-core attention backward of ttt_kernel_attn_bwd (impl 0), same
+ * arguments and results, but it allocates nothing.  The pages have no
+ * counterpart: this entry point exists for callers that must not call
+ * cudaMalloc, such as code running under a CUDA graph capture in the global
+ * capture mode, code whose device memory belongs to a caching allocator or a
+ * fixed budget, and real-time callers that plan all memory up front.
+ *
+ * Its fp32 scratch is a fixed 32 MiB device array inside the library, held
+ * by every GPU on which this call runs until the process exits.  The
+ * backward needs 2 * n * H * hd floats of it: larger shapes return
+ * TTT_ERR_SHAPE before any device work.  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  All
+ * calls share the array and it keeps the previous call's contents (nothing
+ * in it has to start at zero); calls that overlap on the GPU race on it, so
+ * issue them on one stream.  A device-side bounded wait that gives up (not
+ * expected) leaves dqkv incomplete; it is not reported here. */
+int ttt_kernel_attn_bwd_noalloc(int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R,
+                                int64_t pos0, const void* q, const void* kring, const void* vring, const void* o,
+                                const float* lse, int32_t ld_lse, const void* dout, float* dsum, void* dqkv,
+                                void* stream);
+
 /* Error word of the tensor-core kernels launched through this header since
  * the last call (0 = none; otherwise the code of a bounded wait that gave
  * up).  Synchronises the device. */
