@@ -49,7 +49,10 @@ int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda,
  *   dsum  [H, ld_lse]      fp32 scratch of the backward (rowsum(dO * O))
  * R must cover W + n - 1 positions.  impl 0: tcgen05 tensor cores
  * (64 <= hd <= 128, hd % 16 == 0, R % 128 == 0, 16-byte aligned bases,
- * else TTT_ERR_SHAPE); impl 1: SIMT fp32 arithmetic. */
+ * else TTT_ERR_SHAPE), kernel variant chosen by size; impl 1: SIMT fp32
+ * arithmetic.  Forward only: impl 2 forces the tensor-core kernel with one
+ * 128-row query tile per CTA, impl 3 the one with two tiles per CTA and P
+ * kept in tensor memory. */
 int ttt_kernel_attn_fwd(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R,
                         int64_t pos0, const void* q, const void* kring, const void* vring, void* o, float* lse,
                         int32_t ld_lse, void* stream);

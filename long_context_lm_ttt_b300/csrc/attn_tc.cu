@@ -411,6 +411,346 @@ __global__ void __launch_bounds__(192, 2)
 }
 
 // ---------------------------------------------------------------------------
+// Forward for long spans: two query tiles per CTA, P kept in TMEM.
+//
+// One CTA (1 per SM, all 512 TMEM columns) takes 256 query rows of one head
+// as two 128-row tiles t = 0, 1 and walks 128-key blocks:
+//   S_t = Q_t K_j^T             (tcgen05, A and B in shared memory)
+//   P_t = exp(S_t - m)          (softmax warpgroup t; P written back to
+//                                TMEM over the first 64 columns of S_t, two
+//                                bf16 per 32-bit column)
+//   O_t += P_t V_j              (tcgen05 with A read from TMEM)
+// The MMA warp alternates the tiles (after P_0 V_j it issues S_0 of the next
+// block, then waits for P_1, ...) so the tensor core computes one tile's
+// products while the other tile's softmax runs, and P never passes through
+// shared memory.  Because MMAs of one thread complete in issue order, the
+// completion of S_t(j) also means P_t(j-1) V has completed: the softmax may
+// then overwrite P_t and rescale O_t without further waiting.
+// ---------------------------------------------------------------------------
+constexpr int BN2 = 128;  // keys per block
+
+template <int NA>
+struct Fwd2Smem {
+  static constexpr int Q_BYTES = NA * BM * 128;    // one 128-row tile
+  static constexpr int KV_BYTES = NA * BN2 * 128;  // one 128-key block
+  static constexpr int Q_OFF = 0;                  // two tiles
+  static constexpr int K_OFF = 2 * Q_BYTES;
+  static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
+  static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
+  // at least 120 KB: one CTA (512 TMEM columns) per SM
+  static constexpr int SMEM = BAR_OFF + 256 > 120 * 1024 ? BAR_OFF + 256 : 120 * 1024;
+};
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulate
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// key-block range of query tile t of the pair starting at row r0 (nb = 0:
+// the tile has no rows)
+__device__ __forceinline__ void tile2_range(const FwdParams& p, int r0, int t, long long* kb_lo, long long* kb_hi) {
+  const int rs = r0 + BM * t;
+  if (rs >= p.n) {
+    *kb_lo = 1;
+    *kb_hi = 0;
+    return;
+  }
+  const long long t_lo = p.pos0 + rs;
+  const long long t_hi = p.pos0 + min(rs + BM, p.n) - 1;
+  long long k_lo = t_lo - p.W + 1;
+  if (k_lo < 0) k_lo = 0;
+  *kb_lo = k_lo / BN2;
+  *kb_hi = t_hi / BN2;
+}
+
+template <int NA>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd2_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                        const __grid_constant__ CUtensorMap mapV, FwdParams p) {
+  using SM = Fwd2Smem<NA>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t bar0 = sbase + SM::BAR_OFF;
+  const uint32_t q_full = bar0;
+  const uint32_t k_full = bar0 + 8;     // [2] stages
+  const uint32_t v_full = bar0 + 24;    // [2]
+  const uint32_t kv_empty = bar0 + 40;  // [2]
+  const uint32_t s_full = bar0 + 56;    // [2] tiles
+  const uint32_t p_full = bar0 + 72;    // [2] tiles
+  const uint32_t o_done = bar0 + 88;    // [2] tiles
+  const uint32_t drain = bar0 + 104;
+  uint32_t* tmem_slot = (uint32_t*)(smem + SM::BAR_OFF + 192);
+  volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 196);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = blockIdx.x * 2 * BM, h = blockIdx.y;
+  const int kvh = h / (p.H / p.Hkv);
+  long long lo_t[2], hi_t[2];
+  tile2_range(p, r0, 0, &lo_t[0], &hi_t[0]);
+  tile2_range(p, r0, 1, &lo_t[1], &hi_t[1]);
+  const long long kb_lo = lo_t[0];
+  const long long kb_hi = hi_t[1] >= lo_t[1] ? max(hi_t[0], hi_t[1]) : hi_t[0];
+  const int nbl = (int)(kb_hi - kb_lo + 1);
+  auto part = [&](int t, long long j) { return j >= lo_t[t] && j <= hi_t[t]; };
+  const int ksteps = p.hd / 16;
+  const int nO = (p.hd + 15) & ~15;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(k_full + 8 * s, 1);
+      tc::mbar_init(v_full + 8 * s, 1);
+      tc::mbar_init(kv_empty + 8 * s, 1);
+      tc::mbar_init(s_full + 8 * s, 1);
+      tc::mbar_init(p_full + 8 * s, 128);
+      tc::mbar_init(o_done + 8 * s, 1);
+    }
+    tc::mbar_init(drain, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&mapQ);
+    tc::prefetch_tmap(&mapK);
+    tc::prefetch_tmap(&mapV);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // columns: S/P of tile 0 | S/P of tile 1 | O of tile 0 | O of tile 1
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      int issued = 0;
+      tc::mbar_arrive_expect_tx(q_full, 2 * SM::Q_BYTES);
+      for (int t = 0; t < 2; ++t)
+        for (int a = 0; a < NA; ++a)
+          tc::tma_load_2d(sbase + SM::Q_OFF + t * SM::Q_BYTES + a * BM * 128, &mapQ, h * p.hd + 64 * a, r0 + BM * t,
+                          q_full);
+      for (int i = 0; i < nbl && ok; ++i) {
+        const int st = i & 1;
+        if (!tc::mbar_wait(kv_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
+          ok = false;
+          break;
+        }
+        const long long kpos = (kb_lo + i) * BN2;
+        const int row = kvh * p.R + (int)(kpos % p.R);
+        tc::mbar_arrive_expect_tx(k_full + 8 * st, SM::KV_BYTES);
+        for (int a = 0; a < NA; ++a)
+          tc::tma_load_2d(sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN2 * 128, &mapK, 64 * a, row,
+                          k_full + 8 * st);
+        tc::mbar_arrive_expect_tx(v_full + 8 * st, SM::KV_BYTES);
+        for (int a = 0; a < NA; ++a)
+          tc::tma_load_2d(sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN2 * 128, &mapV, 64 * a, row,
+                          v_full + 8 * st);
+        issued = i + 1;
+      }
+      const long long t0 = clock64();
+      while (!tc::mbar_try_wait(q_full, 0) && clock64() - t0 < tc::kWaitClocks) {
+      }
+      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
+        const int st = i & 1;
+        const uint32_t par = (i >> 1) & 1;
+        const long long t1 = clock64();
+        while (!(tc::mbar_try_wait(k_full + 8 * st, par) && tc::mbar_try_wait(v_full + 8 * st, par)) &&
+               clock64() - t1 < tc::kWaitClocks) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idS = tc::idesc_bf16(BM, BN2, 0, 0);
+      const uint32_t idO = tc::idesc_bf16(BM, nO, 0, 1);
+      bool ok = tc::mbar_wait(q_full, 0, p.err, ERR_A_MMA, abort);
+      bool issued = false;
+      int cnt[2] = {0, 0};
+      // S_t of block i (K of stage i & 1 must have landed)
+      auto issue_s = [&](int t, int i) -> bool {
+        const int st = i & 1;
+        if (!tc::mbar_wait(k_full + 8 * st, (i >> 1) & 1, p.err, ERR_A_MMA, abort)) return false;
+        tc::tc_fence_after();
+        const uint32_t kb = sbase + SM::K_OFF + st * SM::KV_BYTES;
+        const uint32_t qb = sbase + SM::Q_OFF + t * SM::Q_BYTES;
+        for (int j = 0; j < ksteps; ++j) {
+          const int a = j >> 2;
+          tc::mma_bf16(tmem + 128 * t, tc::smem_desc_sw128(qb + a * BM * 128 + 32 * (j & 3), 16, 1024),
+                       tc::smem_desc_sw128(kb + a * BN2 * 128 + 32 * (j & 3), 16, 1024), idS, j > 0);
+        }
+        tc::mma_commit(s_full + 8 * t);
+        issued = true;
+        return true;
+      };
+      for (int t = 0; t < 2 && ok; ++t)
+        if (nbl > 0 && part(t, kb_lo)) ok = issue_s(t, 0);
+      for (int i = 0; i < nbl && ok; ++i) {
+        const long long j = kb_lo + i;
+        const int st = i & 1;
+        if (!tc::mbar_wait(v_full + 8 * st, (i >> 1) & 1, p.err, ERR_A_MMA, abort)) {
+          ok = false;
+          break;
+        }
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (part(t, j)) {
+            if (!tc::mbar_wait(p_full + 8 * t, cnt[t] & 1, p.err, ERR_A_MMA, abort)) {
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t vb = sbase + SM::V_OFF + st * SM::KV_BYTES;
+#pragma unroll
+            for (int k = 0; k < BN2 / 16; ++k)
+              mma_bf16_ts(tmem + 256 + 128 * t, tmem + 128 * t + 8 * k,
+                          tc::smem_desc_sw128(vb + 2048 * k, BN2 * 128, 1024), idO, (cnt[t] > 0 || k > 0) ? 1u : 0u);
+            tc::mma_commit(o_done + 8 * t);
+            ++cnt[t];
+          }
+          if (i + 1 < nbl && part(t, j + 1)) ok = issue_s(t, i + 1);
+        }
+        if (ok) tc::mma_commit(kv_empty + 8 * st);
+      }
+      if (!ok && issued) {
+        tc::mma_commit(drain);
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(drain, 0) && clock64() - t0 < tc::kWaitClocks) {
+        }
+      }
+    }
+  } else {
+    // ---------------- softmax warpgroups (warps 2-5: tile 0, 6-9: tile 1)
+    const int t = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int grow_ = r0 + BM * t + row;
+    const long long pos = p.pos0 + grow_;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + 128 * t + lane_off;
+    const uint32_t tO = tmem + 256 + 128 * t + lane_off;
+    const float NEG_INF = -INFINITY;
+    float m_run = NEG_INF, l_run = 0.f;
+    bool ok = true;
+    int cnt = 0;
+    for (long long j = lo_t[t]; j <= hi_t[t]; ++j, ++cnt) {
+      if (!warp_wait(s_full + 8 * t, cnt & 1, p.err, ERR_A_SOFT, abort)) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      // pass 1: block maximum (scores stay in TMEM; 32 live registers)
+      const long long kpos = j * BN2;
+      const long long lo = pos - p.W + 1 - kpos, hi = pos - kpos;
+      const bool full = lo <= 0 && hi >= BN2 - 1;
+      float mb = NEG_INF;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::tmem_ld32(tS + 32 * c, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int col = 32 * c + k;
+          if (full || (col >= lo && col <= hi)) mb = fmaxf(mb, v[k] * p.scale_log2);
+        }
+      }
+      const bool grow = mb > m_run + 8.0f;
+      const float m_new = grow ? mb : m_run;
+      const float alpha = (grow && m_run != NEG_INF) ? exp2f(m_run - m_new) : 1.0f;
+      const float m_use = m_new == NEG_INF ? 0.f : m_new;
+      // P_t(j-1) V has completed (it was issued before S_t(j)): O_t is
+      // stable and P_t may be overwritten
+      if (cnt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        for (int c0 = 0; c0 < nO; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(tO + c0, v);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] *= alpha;
+          tmem_st32(tO + c0, v);
+        }
+      }
+      // pass 2: exponentials, packed two per column over the columns of S
+      // already read (P columns [16c, 16c+16) come from S columns
+      // [32c, 32c+32))
+      float ls = 0.f;
+#pragma unroll 1
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int c = 2 * c2 + h2;
+          float v[32];
+          tc::tmem_ld32(tS + 32 * c, v);
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const int col = 32 * c + k;
+            const float p0 = (full || (col >= lo && col <= hi)) ? exp2f(v[k] * p.scale_log2 - m_use) : 0.f;
+            const float p1 = (full || (col + 1 >= lo && col + 1 <= hi)) ? exp2f(v[k + 1] * p.scale_log2 - m_use) : 0.f;
+            ls += p0 + p1;
+            pk[16 * h2 + k / 2] = pack_bf16(p0, p1);
+          }
+        }
+        tmem_st32u(tS + 32 * c2, pk);
+      }
+      l_run = l_run * alpha + ls;
+      m_run = m_new;
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc::tc_fence_before();
+      tc::mbar_arrive(p_full + 8 * t);
+    }
+    if (ok && cnt > 0 && warp_wait(o_done + 8 * t, (cnt - 1) & 1, p.err, ERR_A_SOFT, abort)) {
+      tc::tc_fence_after();
+      const float il = 1.0f / l_run;
+      for (int c0 = 0; c0 < nO; c0 += 32) {
+        float v[32];
+        tc::tmem_ld32(tO + c0, v);
+        if (grow_ < p.n) {
+          bf16* dst = p.o + (int64_t)grow_ * p.ldo + (int64_t)h * p.hd + c0;
+#pragma unroll
+          for (int k = 0; k < 32; k += 8) {
+            if (c0 + k < p.hd) {
+              uint4 u;
+              u.x = pack_bf16(v[k] * il, v[k + 1] * il);
+              u.y = pack_bf16(v[k + 2] * il, v[k + 3] * il);
+              u.z = pack_bf16(v[k + 4] * il, v[k + 5] * il);
+              u.w = pack_bf16(v[k + 6] * il, v[k + 7] * il);
+              *reinterpret_cast<uint4*>(dst + k) = u;
+            }
+          }
+        }
+      }
+      if (grow_ < p.n) p.lse[(int64_t)h * p.ld_lse + grow_] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // backward
 //
 //   D[t]   = sum_d dO[t,d] O[t,d]                          (attn_bwd_prep)
@@ -1108,6 +1448,41 @@ int launch_fwd(const AttnArgs& a, int* err, cudaStream_t st) {
   return (int)cudaPeekAtLastError();
 }
 
+template <int NA>
+int launch_fwd2(const AttnArgs& a, int* err, cudaStream_t st) {
+  using SM = Fwd2Smem<NA>;
+  CUtensorMap mq, mk, mv;
+  const uint64_t ldq = (uint64_t)a.H * a.hd;
+  int rc = map2d(&mq, a.q, ldq, a.n, ldq, BM);
+  if (!rc) rc = map2d(&mk, a.kring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN2);
+  if (!rc) rc = map2d(&mv, a.vring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN2);
+  if (rc) return rc;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd2_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SM::SMEM);
+    if (e != cudaSuccess) return (int)e;
+    attr = true;
+  }
+  FwdParams p;
+  p.n = a.n;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.hd = a.hd;
+  p.W = a.W;
+  p.R = a.R;
+  p.pos0 = a.pos0;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)a.hd);
+  p.o = (bf16*)a.o;
+  p.ldo = (int64_t)a.H * a.hd;
+  p.lse = a.lse;
+  p.ld_lse = a.ld_lse;
+  p.err = err;
+  dim3 grid((a.n + 2 * BM - 1) / (2 * BM), a.H);
+  attn_fwd2_tc_kernel<NA><<<grid, 320, SM::SMEM, st>>>(mq, mk, mv, p);
+  return (int)cudaPeekAtLastError();
+}
+
 }  // namespace
 
 bool attn_tc_supported(const AttnArgs& a) {
@@ -1116,9 +1491,12 @@ bool attn_tc_supported(const AttnArgs& a) {
          ((uintptr_t)a.o & 15) == 0;
 }
 
-int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st) {
+int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st, int variant) {
   if (a.n <= 0) return 0;
   if (!encoder() || !attn_tc_supported(a)) return (int)cudaErrorNotSupported;
+  // the one-tile kernel is the default: the two-tile one measured slower
+  if (variant == 0) variant = 1;
+  if (variant == 2) return a.hd <= 64 ? launch_fwd2<1>(a, err, st) : launch_fwd2<2>(a, err, st);
   return a.hd <= 64 ? launch_fwd<1>(a, err, st) : launch_fwd<2>(a, err, st);
 }
 

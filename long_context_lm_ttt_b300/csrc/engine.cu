@@ -134,6 +134,11 @@ struct EngineBase {
   // nk: kernels the launch function issues
   template <typename F>
   void prof(int cls, double flops, double bytes, cudaStream_t st, F&& launch, int nk = 1) {
+    prof(cls, flops, bytes, st, launch, [nk] { return nk; });
+  }
+  // nk(): kernels the launch issued, asked after it ran
+  template <typename F, typename G>
+  void prof(int cls, double flops, double bytes, cudaStream_t st, F&& launch, G&& nk) {
     if (!prof_on) {
       launch();
       return;
@@ -142,7 +147,7 @@ struct EngineBase {
     if (a) cudaEventRecord(a, st);
     launch();
     if (b) cudaEventRecord(b, st);
-    if (a && b) prof_recs.push_back({cls, nk, a, b, flops, bytes});
+    if (a && b) prof_recs.push_back({cls, nk(), a, b, flops, bytes});
   }
   // after a synchronisation: fold the recorded pairs into prof_stat
   void prof_collect() {
@@ -222,6 +227,8 @@ struct Engine : EngineBase {
   size_t stage32_elems = 0;
   float* attn_ws = nullptr;  // scratch of the tensor-core attention backward
   int64_t attn_ws_elems = 0;
+  float* gemm_ws = nullptr;  // split-K partial sums of the tensor-core GEMMs
+  int64_t gemm_ws_elems = 0;
 
   template <typename U>
   int A(U** p, size_t elems) {
@@ -265,6 +272,23 @@ struct Engine : EngineBase {
     int dev = 0;
     CU_TRY(cudaGetDevice(&dev));
     CU_TRY(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+    {
+      // vocabulary slab of the streamed cross-entropy: a whole number of
+      // 256-column tiles such that the slab's logits GEMM over b rows fills
+      // whole waves of SMs, about 16-24K columns
+      auto gcd = [](int a, int c) {
+        while (c) {
+          const int t = a % c;
+          a = c;
+          c = t;
+        }
+        return a;
+      };
+      const int num_m = (b + 127) / 128;
+      const int per = num_sms / gcd(num_sms, num_m);  // n-tiles per whole number of waves
+      const int k = std::max(1, 20480 / (per * 256));
+      Vs = (int)std::min<int64_t>(V, (int64_t)per * k * 256);
+    }
     stage32_elems = std::max<int64_t>((int64_t)V * d, (int64_t)2 * ff * d);
     A_TRY(stage32, stage32_elems);
     A_TRY(E, (size_t)V * d);
@@ -384,6 +408,10 @@ struct Engine : EngineBase {
     A_TRY(dqkv, (size_t)b * qkv_cols);
     A_TRY(dxn, (size_t)b * d);
     A_TRY(Dsum, (size_t)H * b);
+    if (kBF16 && use_tc_gemm) {
+      gemm_ws_elems = (int64_t)4 * b * std::max<int64_t>(std::max<int64_t>(d, qkv_cols), Hhd);
+      A_TRY(gemm_ws, (size_t)gemm_ws_elems);
+    }
     if (kBF16 && use_tc_attn_bwd) {
       attn_ws_elems = attn_bwd_tc_ws_elems(b, H, hd, num_sms);
       A_TRY(attn_ws, (size_t)attn_ws_elems);
@@ -397,7 +425,7 @@ struct Engine : EngineBase {
   // -------------------------------------------------------------------------
   void gemm(int M, int N, int K, const T* A_, int64_t lda, int a_mn, const T* B_, int64_t ldb,
             int b_mn, const Epi& e, cudaStream_t st, int* rc, const T* B2 = nullptr) {
-    GemmArgs<T> g{M, N, K, A_, lda, a_mn, B_, ldb, b_mn, e, B2};
+    GemmArgs<T> g{M, N, K, A_, lda, a_mn, B_, ldb, b_mn, e, B2, gemm_ws, gemm_ws_elems};
     int cls = P_GEMM_FWD;
     double out_b = (double)M * N * (e.kind == EPI_STORE && !e.out_f32 ? sizeof(T) : 4);
     switch (e.kind) {
@@ -411,10 +439,11 @@ struct Engine : EngineBase {
     }
     const double flops = 2.0 * M * N * K;
     const double bytes = (double)sizeof(T) * ((double)M * K + (double)N * K) + out_b;
+    int nk = 1;
     prof(cls, flops, bytes, st, [&] {
       if constexpr (kBF16) {
         if (use_tc_gemm) {
-          int r = gemm_tc(g, num_sms, dev_err + 2, st);
+          int r = gemm_tc(g, num_sms, dev_err + 2, st, &nk);
           if (r != 0 && *rc == TTT_OK) {
             *rc = TTT_ERR_SHAPE;
             err = "tensor-core GEMM rejected M=" + std::to_string(M) + " N=" + std::to_string(N) +
@@ -424,7 +453,7 @@ struct Engine : EngineBase {
         }
       }
       gemm_simt<T>(g, st);
-    });
+    }, [&] { return nk; });
   }
   // algorithmic attention work of a chunk of n queries starting at pos0:
   // unmasked (query, key) pairs and the pairs whose key is in the chunk
@@ -934,7 +963,7 @@ extern "C" int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* str
     eng->R_s = (int)(((need_s + 127) / 128) * 128);
   }
   eng->qkv_cols = (cfg->n_heads + 2 * cfg->n_kv_heads) * cfg->head_dim;
-  eng->Vs = std::min(cfg->vocab, 8192);
+  eng->Vs = 0;  // set in init(), once the SM count is known
   const bool bf = cfg->precision == TTT_BF16;
   const char* g = getenv("TTT_GEMM_IMPL");
   const char* a = getenv("TTT_ATTN_IMPL");

@@ -20,6 +20,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
@@ -33,23 +35,29 @@ namespace {
 constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 
-template <int BN>
+// SRC = 1: the epilogue's fp32 source tile (the master weights of the SGD
+// epilogue) is brought into shared memory by TMA at the start of each tile,
+// double-buffered, so its load overlaps the tile's main loop.
+template <int BN, int SRC = 0>
 struct Cfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int STAGES = SRC ? 3 : (BN == 256 ? 4 : 6);
   static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int SRC_OFF = STAGES * STAGE_BYTES;
+  static constexpr int SRC_BYTES = SRC ? BM * BN * 4 : 0;  // one fp32 tile
+  static constexpr int BAR_OFF = SRC_OFF + 2 * SRC_BYTES;
   static constexpr int SMEM = 1024 /*align slack*/ + BAR_OFF + 256;
 };
 
 enum : int { ERR_WAIT_PRODUCER = 101, ERR_WAIT_MMA = 102, ERR_WAIT_EPI = 103, ERR_WAIT_DRAIN = 104 };
 
-template <int BN, int A_MN, int B_MN>
+template <int BN, int A_MN, int B_MN, int SRC = 0>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                   const __grid_constant__ CUtensorMap mapB2, int dual, int M, int N, int K, Epi e, int* err) {
-  using C = Cfg<BN>;
+                   const __grid_constant__ CUtensorMap mapB2, const __grid_constant__ CUtensorMap mapS, int dual,
+                   int M, int N, int K, Epi e, int* err, int splits, float* ws) {
+  using C = Cfg<BN, SRC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = tc::smem_u32(smem);
@@ -60,7 +68,9 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tfull0 = empty0 + 8 * C::STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
-  uint32_t* tmem_slot = (uint32_t*)(smem + C::BAR_OFF + 8 * (2 * C::STAGES + 5));
+  const uint32_t src_full0 = drain + 8;       // [2] (SRC only)
+  const uint32_t src_empty0 = src_full0 + 16;  // [2]
+  uint32_t* tmem_slot = (uint32_t*)(smem + C::BAR_OFF + 8 * (2 * C::STAGES + 9));
   volatile int* abort = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -68,6 +78,9 @@ __global__ void __launch_bounds__(192, 1)
   const int ntiles = num_m * num_n;
   const int nk = (K + BK - 1) / BK;
   const int nk_total = dual ? 2 * nk : nk;  // dual: A B^T then A B2^T into one accumulator
+  // work units: (split, tile); split s covers k-blocks [kb_lo(s), kb_lo(s+1))
+  const int nunits = ntiles * splits;
+  auto kb_lo = [&](int sp) { return (int)((long long)sp * nk_total / splits); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -79,6 +92,10 @@ __global__ void __launch_bounds__(192, 1)
       tc::mbar_init(tempty0 + 8 * a, 128);
     }
     tc::mbar_init(drain, 1);
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(src_full0 + 8 * a, 1);
+      tc::mbar_init(src_empty0 + 8 * a, 128);
+    }
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -86,6 +103,7 @@ __global__ void __launch_bounds__(192, 1)
     tc::prefetch_tmap(&mapA);
     tc::prefetch_tmap(&mapB);
     if (dual) tc::prefetch_tmap(&mapB2);
+    if (SRC) tc::prefetch_tmap(&mapS);
   }
   if (warp == 1) {
     tc::tmem_alloc(tc::smem_u32(tmem_slot), C::TMEM_COLS);
@@ -104,9 +122,23 @@ __global__ void __launch_bounds__(192, 1)
       int last_parity[C::STAGES];
       for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      int lu = 0;  // this CTA's unit counter
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++lu) {
+        const int t = u % ntiles, sp = u / ntiles;
         const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
-        for (int kb = 0; kb < nk_total; ++kb) {
+        if (SRC) {
+          const int sb = lu & 1;
+          if (!tc::mbar_wait(src_empty0 + 8 * sb, ((lu >> 1) & 1) ^ 1, err, ERR_WAIT_PRODUCER, abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sf = src_full0 + 8 * sb;
+          tc::mbar_arrive_expect_tx(sf, C::SRC_BYTES);
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c)
+            tc::tma_load_2d(sbase + C::SRC_OFF + sb * C::SRC_BYTES + c * BM * 128, &mapS, n0 + 32 * c, m0, sf);
+        }
+        for (int kb = kb_lo(sp); kb < kb_lo(sp + 1); ++kb) {
           if (!tc::mbar_wait(empty0 + 8 * stage, phase ^ 1, err, ERR_WAIT_PRODUCER, abort)) {
             ok = false;
             break;
@@ -156,14 +188,16 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int sp = u / ntiles;
+        const int kb_first = kb_lo(sp);
         if (!tc::mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, err, ERR_WAIT_MMA, abort)) {
           ok = false;
           break;
         }
         tc::tc_fence_after();
         const uint32_t d_tmem = tmem + acc * BN;
-        for (int kb = 0; kb < nk_total; ++kb) {
+        for (int kb = kb_first; kb < kb_lo(sp + 1); ++kb) {
           if (!tc::mbar_wait(full0 + 8 * stage, phase, err, ERR_WAIT_MMA, abort)) {
             ok = false;
             break;
@@ -177,7 +211,7 @@ __global__ void __launch_bounds__(192, 1)
                                      : tc::smem_desc_sw128(a_s + 32 * j, 16, 1024);
             const uint64_t bd = B_MN ? tc::smem_desc_sw128(b_s + 2048 * j, 8192, 1024)
                                      : tc::smem_desc_sw128(b_s + 32 * j, 16, 1024);
-            tc::mma_bf16(d_tmem, ad, bd, idesc, (kb | j) != 0);
+            tc::mma_bf16(d_tmem, ad, bd, idesc, (kb != kb_first || j != 0) ? 1u : 0u);
           }
           issued = true;
           tc::mma_commit(empty0 + 8 * stage);
@@ -208,19 +242,27 @@ __global__ void __launch_bounds__(192, 1)
     // stores).  The source operand of the next chunk is loaded before the
     // current chunk is processed, the first chunk's before the accumulator
     // is waited for, so global-load latency overlaps useful work.
+    // With split K the epilogue only stores the fp32 partial sum of its
+    // split into ws[split][M][N]; splitk_reduce_kernel applies the epilogue.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
-    const bool has_src = epi_has_src(e);
+    const bool partial = splits > 1;
+    const bool has_src = !SRC && !partial && epi_has_src(e);
+    const int trow = quarter * 32 + lane;  // row within the tile
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    int lu = 0;
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++lu) {
+      const int t = u % ntiles, sp = u / ntiles;
       const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
-      const int row = m0 + quarter * 32 + lane;
+      const int row = m0 + trow;
       const int nch = min(BN, N - n0 + 31) / 32;  // chunks with columns < N
       auto vec_chunk = [&](int c) { return e.vec && n0 + 32 * c + 32 <= N; };
       uint4 src[8];
       if (has_src && row < M && vec_chunk(0)) epi_src_load(e, row, n0, src);
       if (!tc::mbar_wait(tfull0 + 8 * acc, acc_phase, err, ERR_WAIT_EPI, abort)) break;
       tc::tc_fence_after();
+      const uint32_t stile = sbase + C::SRC_OFF + (lu & 1) * C::SRC_BYTES;
+      if (SRC && !tc::mbar_wait(src_full0 + 8 * (lu & 1), (lu >> 1) & 1, err, ERR_WAIT_EPI, abort)) break;
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN;
 #pragma unroll 1
       for (int c = 0; c < nch; ++c) {
@@ -228,7 +270,31 @@ __global__ void __launch_bounds__(192, 1)
         tc::tmem_ld32(tbase + c * 32, v);
         uint4 nxt[8];
         if (has_src && row < M && c + 1 < nch && vec_chunk(c + 1)) epi_src_load(e, row, n0 + 32 * (c + 1), nxt);
-        if (row < M) {
+        if (SRC) {
+          // this row's 128 bytes of source chunk c (128-byte swizzle)
+          const uint32_t rb = stile + c * BM * 128 + trow * 128;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t a0, a1, a2, a3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                         : "r"(rb + ((i ^ (trow & 7)) << 4)));
+            src[i] = make_uint4(a0, a1, a2, a3);
+          }
+        }
+        if (row < M && partial) {
+          float* wp = ws + ((int64_t)sp * M + row) * N + n0 + 32 * c;
+          if (vec_chunk(c) && (N & 3) == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              stg16(wp + 4 * i, make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                                           __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (n0 + 32 * c + k < N) wp[k] = v[k];
+          }
+        } else if (row < M) {
           if (vec_chunk(c)) {
             epi_row32(e, row, n0 + 32 * c, v, src);
           } else {
@@ -239,11 +305,14 @@ __global__ void __launch_bounds__(192, 1)
             }
           }
         }
+        if (!SRC) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) src[i] = nxt[i];
+          for (int i = 0; i < 8; ++i) src[i] = nxt[i];
+        }
       }
       tc::tc_fence_before();
       tc::mbar_arrive(tempty0 + 8 * acc);
+      if (SRC) tc::mbar_arrive(src_empty0 + 8 * (lu & 1));
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
@@ -255,6 +324,46 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Sum of the split-K partials (fixed order) through the epilogue; one thread
+// per (row, 32-column chunk), consecutive threads on consecutive chunks.
+__global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, int M, int N, Epi e) {
+  const int nch = (N + 31) / 32;
+  const int64_t total = (int64_t)M * nch;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int row = (int)(i / nch), col0 = (int)(i % nch) * 32;
+    const bool vec = e.vec && col0 + 32 <= N && (N & 3) == 0;
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = 0.f;
+    for (int sp = 0; sp < splits; ++sp) {
+      const float* p = ws + ((int64_t)sp * M + row) * N + col0;
+      if (vec) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 x = *reinterpret_cast<const float4*>(p + 4 * q);
+          v[4 * q] += x.x;
+          v[4 * q + 1] += x.y;
+          v[4 * q + 2] += x.z;
+          v[4 * q + 3] += x.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (col0 + k < N) v[k] += p[k];
+      }
+    }
+    if (vec) {
+      uint4 src[8];
+      if (epi_has_src(e)) epi_src_load(e, row, col0, src);
+      epi_row32(e, row, col0, v, src);
+    } else {
+#pragma unroll
+      for (int p = 0; p < 16; ++p)
+        if (col0 + 2 * p < N) epi_pair<bf16>(e, row, col0 + 2 * p, v[2 * p], v[2 * p + 1]);
+    }
   }
 }
 
@@ -275,10 +384,22 @@ int make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, 
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
-template <int BN, int A_MN, int B_MN>
-int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st) {
-  using C = Cfg<BN>;
-  CUtensorMap ma, mb, mb2;
+// fp32 [rows, cols] tile map with 128-byte swizzle: box {32 columns, 128 rows}
+int make_map_f32(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld_elems) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld_elems * 4};
+  cuuint32_t box[2] = {32, (cuuint32_t)BM};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+}
+
+template <int BN, int A_MN, int B_MN, int SRC = 0>
+int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int splits) {
+  using C = Cfg<BN, SRC>;
+  CUtensorMap ma, mb, mb2, ms;
   int rc;
   if (A_MN) rc = make_map(&ma, g.A, g.M, g.K, g.lda, 64, 64);
   else rc = make_map(&ma, g.A, g.K, g.M, g.lda, 64, BM);
@@ -293,25 +414,72 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st) {
   } else {
     mb2 = mb;
   }
+  if (SRC) {
+    rc = make_map_f32(&ms, g.e.w32, g.N, g.M, g.e.ldo);
+    if (rc) return rc;
+  } else {
+    ms = mb;
+  }
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, SRC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
   const int ntiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
-  const int grid = ntiles < num_sms ? ntiles : num_sms;
-  gemm_tc_kernel<BN, A_MN, B_MN><<<grid, 192, C::SMEM, st>>>(ma, mb, mb2, g.B2 ? 1 : 0, g.M, g.N, g.K, g.e, err);
+  const int nunits = ntiles * splits;
+  const int grid = nunits < num_sms ? nunits : num_sms;
+  gemm_tc_kernel<BN, A_MN, B_MN, SRC><<<grid, 192, C::SMEM, st>>>(ma, mb, mb2, ms, g.B2 ? 1 : 0, g.M, g.N, g.K,
+                                                                   g.e, err, splits, g.ws);
+  if (splits > 1) {
+    const int64_t items = (int64_t)g.M * ((g.N + 31) / 32);
+    const int rgrid = (int)std::min<int64_t>((items + 127) / 128, (int64_t)num_sms * 16);
+    splitk_reduce_kernel<<<rgrid, 128, 0, st>>>(g.ws, splits, g.M, g.N, g.e);
+  }
   return (int)cudaPeekAtLastError();
 }
 
 template <int BN>
-int dispatch_major(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st) {
+int dispatch_major(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int splits) {
   if (g.a_mn) {
-    return g.b_mn ? launch<BN, 1, 1>(g, num_sms, err, st) : launch<BN, 1, 0>(g, num_sms, err, st);
+    return g.b_mn ? launch<BN, 1, 1>(g, num_sms, err, st, splits) : launch<BN, 1, 0>(g, num_sms, err, st, splits);
   }
-  return g.b_mn ? launch<BN, 0, 1>(g, num_sms, err, st) : launch<BN, 0, 0>(g, num_sms, err, st);
+  return g.b_mn ? launch<BN, 0, 1>(g, num_sms, err, st, splits) : launch<BN, 0, 0>(g, num_sms, err, st, splits);
+}
+
+// Tile width and K split by a simple time model: a k-block of a 128 x BN
+// tile costs BN units (BN = 128 tiles a little more per column: they are
+// closer to the shared-memory bandwidth limit), tiles run in waves of
+// num_sms, and a split adds a reduction pass over splits x M x N fp32.
+struct Plan {
+  int bn, splits;
+};
+static Plan plan_gemm(const GemmArgs<bf16>& g, int num_sms) {
+  const int nk = (g.K + BK - 1) / BK;
+  const int nkt = g.B2 ? 2 * nk : nk;
+  const int num_m = (g.M + BM - 1) / BM;
+  // cost unit: one k-block of a 128 x 256 tile (~0.27 us at full rate)
+  const double kb_us = 0.27;
+  Plan best{128, 1};
+  double best_cost = 1e300;
+  for (int bn : {128, 256}) {
+    if (bn == 256 && g.N <= 128) continue;
+    const int tiles = num_m * ((g.N + bn - 1) / bn);
+    const double kb_cost = (bn == 256 ? 1.0 : 0.58) * kb_us;
+    for (int sp = 1; sp <= 4; ++sp) {
+      if (sp > 1 && (!g.ws || nkt / sp < 8 || (int64_t)sp * g.M * g.N > g.ws_elems)) break;
+      const double waves = std::ceil((double)tiles * sp / num_sms);
+      const int kb_unit = (nkt + sp - 1) / sp;
+      double cost = waves * kb_unit * kb_cost;
+      if (sp > 1) cost += 3.0 + (double)sp * g.M * g.N * 8.0 / 8e6;  // launch + L2-resident traffic (us)
+      if (cost < best_cost * 0.97) {
+        best_cost = cost;
+        best = {bn, sp};
+      }
+    }
+  }
+  return best;
 }
 
 }  // namespace
@@ -350,8 +518,9 @@ static bool epi_vec_ok(const Epi& e) {
   }
 }
 
-int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st) {
+int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st, int* kernels) {
   GemmArgs<bf16> g = g_in;
+  if (kernels) *kernels = 1;
   g.e.vec = epi_vec_ok(g.e) ? 1 : 0;
   if (g.M <= 0 || g.N <= 0) return 0;
   if (!g_encode) return (int)cudaErrorNotSupported;
@@ -359,9 +528,17 @@ int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st) 
   if (((uintptr_t)g.A & 15) || ((uintptr_t)g.B & 15) || ((uintptr_t)g.B2 & 15) || (g.lda & 7) ||
       (g.ldb & 7) || g.K <= 0)
     return (int)cudaErrorNotSupported;
-  const int tiles256 = ((g.M + BM - 1) / BM) * ((g.N + 255) / 256);
-  if (g.N > 128 && tiles256 >= num_sms) return dispatch_major<256>(g, num_sms, err, st);
-  return dispatch_major<128>(g, num_sms, err, st);
+  // the SGD epilogue (weight-gradient GEMM, both operands MN-major) reads
+  // the fp32 masters through the TMA-fed shared-memory tile
+  if (g.e.kind == EPI_SGD && g.e.vec && g.a_mn && g.b_mn && !g.B2 && (g.N % 32) == 0) {
+    if (kernels) *kernels = 1;
+    return launch<128, 1, 1, 1>(g, num_sms, err, st, 1);
+  }
+  const Plan pl = plan_gemm(g, num_sms);
+  if (pl.splits > 1 && (((uintptr_t)g.ws & 15) != 0)) return (int)cudaErrorNotSupported;
+  if (kernels) *kernels = pl.splits > 1 ? 2 : 1;
+  if (pl.bn == 256) return dispatch_major<256>(g, num_sms, err, st, pl.splits);
+  return dispatch_major<128>(g, num_sms, err, st, pl.splits);
 }
 
 }  // namespace ttt

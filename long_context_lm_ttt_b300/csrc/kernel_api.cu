@@ -28,7 +28,7 @@ extern "C" int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, i
   e.ldo = ldc;
   if (impl == 0 || impl == 1) {
     ttt::GemmArgs<ttt::bf16> g{M, N, K, (const ttt::bf16*)A, lda, a_mn, (const ttt::bf16*)B, ldb, b_mn, e,
-                               (const ttt::bf16*)B2};
+                               (const ttt::bf16*)B2, nullptr, 0};
     if (impl == 0) {
       if (ttt::gemm_tc_init()) return TTT_ERR_CUDA;
       int dev = 0, sms = 148;
@@ -48,8 +48,9 @@ extern "C" int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, i
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
 }
 
-static int attn_check(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R) {
-  if (impl != 0 && impl != 1) return TTT_ERR_INVALID;
+static int attn_check(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R,
+                      int32_t max_impl = 1) {
+  if (impl < 0 || impl > max_impl) return TTT_ERR_INVALID;
   if (n < 0 || H < 1 || Hkv < 1 || H % Hkv || hd < 2 || (hd & 1) || hd > 256 || W < 1 || R < 1)
     return TTT_ERR_INVALID;
   if ((int64_t)R < (int64_t)W + n - 1) return TTT_ERR_SHAPE;
@@ -80,15 +81,15 @@ static ttt::AttnArgs attn_args(int32_t n, int32_t H, int32_t Hkv, int32_t hd, in
 extern "C" int ttt_kernel_attn_fwd(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W,
                                    int32_t R, int64_t pos0, const void* q, const void* kring, const void* vring,
                                    void* o, float* lse, int32_t ld_lse, void* stream) {
-  int rc = attn_check(impl, n, H, Hkv, hd, W, R);
+  int rc = attn_check(impl, n, H, Hkv, hd, W, R, 3);
   if (rc) return rc;
   if (!q || !kring || !vring || !o || !lse || ld_lse < n) return TTT_ERR_INVALID;
   if (ensure_err()) return TTT_ERR_OOM;
   ttt::AttnArgs a = attn_args(n, H, Hkv, hd, W, R, pos0, q, kring, vring, o, lse, ld_lse);
   cudaStream_t st = (cudaStream_t)stream;
-  if (impl == 0) {
+  if (impl == 0 || impl == 2 || impl == 3) {
     if (!ttt::attn_tc_supported(a)) return TTT_ERR_SHAPE;
-    rc = ttt::attn_fwd_tc(a, g_err, st);
+    rc = ttt::attn_fwd_tc(a, g_err, st, impl == 0 ? 0 : (impl == 2 ? 1 : 2));
     return rc ? TTT_ERR_CUDA : 0;
   }
   ttt::attn_fwd_simt<ttt::bf16>(a, st);

@@ -18,6 +18,10 @@ struct GemmArgs {
   int b_mn;
   Epi e;
   const T* B2;  // optional second B (same layout): C = A B^T + A B2^T
+  // optional fp32 scratch: lets the tensor-core GEMM split K across CTAs
+  // (partial sums here, then a fixed-order reduction applies the epilogue)
+  float* ws = nullptr;
+  int64_t ws_elems = 0;
 };
 
 // SIMT fp32-accumulate GEMM (check mode; reference for the tensor-core one)
@@ -25,7 +29,9 @@ template <typename T> void gemm_simt(const GemmArgs<T>& g, cudaStream_t st);
 
 // tcgen05 / TMA GEMM (bf16 in, fp32 accumulate).  Returns a cudaError_t
 // (cudaErrorNotSupported when the shape cannot be described by TMA).
-int gemm_tc(const GemmArgs<bf16>& g, int num_sms, int* dev_err, cudaStream_t st);
+// *kernels (optional) receives the number of kernels launched (2 with a
+// split-K reduction).
+int gemm_tc(const GemmArgs<bf16>& g, int num_sms, int* dev_err, cudaStream_t st, int* kernels = nullptr);
 int gemm_tc_init();
 
 // --- element-wise / row kernels (kernels.cu) -------------------------------
@@ -92,7 +98,9 @@ template <typename T> void attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
 // return a cudaError_t; device-side bounded waits that give up write a code
 // into *err.
 bool attn_tc_supported(const AttnArgs& a);
-int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st);
+// variant 0: choose by size; 1: one 128-row tile per CTA (two CTAs per
+// SM); 2: two tiles per CTA with P kept in tensor memory
+int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st, int variant = 0);
 int attn_bwd_tc(const AttnArgs& a, int* err, cudaStream_t st);
 // the backward additionally needs chunk starts at multiples of 64 and scratch
 bool attn_bwd_tc_supported(const AttnArgs& a);

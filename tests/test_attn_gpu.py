@@ -84,8 +84,10 @@ FWD_CASES = [
 
 
 @pytest.mark.parametrize("case", FWD_CASES)
-@pytest.mark.parametrize("impl", [0, 1])
+@pytest.mark.parametrize("impl", [0, 1, 2, 3])
 def test_attn_fwd(case, impl):
+    """impl 0: tensor cores (variant by size), 1: SIMT, 2: tensor cores with
+    one query tile per CTA, 3: two tiles per CTA with P in tensor memory."""
     torch, T = _env()
     n, H, Hkv, hd, W, pos0, R = case
     q, kr, vr = make_case(n, H, Hkv, hd, W, pos0, R, seed=n + hd)
@@ -97,14 +99,15 @@ def test_attn_fwd(case, impl):
     assert err_l < 2e-3, err_l
 
 
-def test_attn_fwd_3b_shape_sampled():
+@pytest.mark.parametrize("impl", [2, 3])
+def test_attn_fwd_3b_shape_sampled(impl):
     """3B head layout (24 q / 8 KV heads x 128) over a full 1024-row chunk
     deep in the sequence (window 8192 of a 9216-slot ring); sampled rows."""
     torch, T = _env()
     n, H, Hkv, hd, W, R = 1024, 24, 8, 128, 8192, 9216
     pos0 = 40 * 1024
     q, kr, vr = make_case(n, H, Hkv, hd, W, pos0, R, seed=7)
-    o, lse = run_fwd(T, torch, 0, q, kr, vr, n, H, Hkv, hd, W, pos0)
+    o, lse = run_fwd(T, torch, impl, q, kr, vr, n, H, Hkv, hd, W, pos0)
     rows = [0, 1, 127, 128, 500, 777, 1023]
     ro, rl = ref_forward(q, kr, vr, n, H, Hkv, hd, W, pos0, rows=rows)
     err_o = max(np.abs(o[r, h * hd:(h + 1) * hd] - v).max() for (r, h), v in ro.items())
@@ -114,7 +117,8 @@ def test_attn_fwd_3b_shape_sampled():
     assert np.isfinite(o).all()
 
 
-def test_attn_fwd_large_scores():
+@pytest.mark.parametrize("impl", [2, 3])
+def test_attn_fwd_large_scores(impl):
     """Scores spread over a wide range exercise the lazy rescaling of the
     output accumulator (the running max grows by more than 2^8)."""
     torch, T = _env()
@@ -123,7 +127,7 @@ def test_attn_fwd_large_scores():
     # make later keys dominate so that the max keeps growing along the row
     ramp = np.linspace(0.2, 3.0, R, dtype=np.float32)[None, :, None]
     kr = inputs.round_bf16(kr * ramp)
-    o, lse = run_fwd(T, torch, 0, q, kr, vr, n, H, Hkv, hd, W, pos0)
+    o, lse = run_fwd(T, torch, impl, q, kr, vr, n, H, Hkv, hd, W, pos0)
     ro, rl = ref_forward(q, kr, vr, n, H, Hkv, hd, W, pos0)
     err_o = max(np.abs(o[r, h * hd:(h + 1) * hd] - v).max() for (r, h), v in ro.items())
     err_l = max(abs(lse[h, r] - v) / max(1.0, abs(v)) for (r, h), v in rl.items())
