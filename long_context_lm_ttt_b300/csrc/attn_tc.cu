@@ -437,9 +437,41 @@ struct Fwd2Smem {
   static constexpr int K_OFF = 2 * Q_BYTES;
   static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
+  // row-max exchange [tile][parity][half][128] and row-sum exchange
+  // [tile][half][128] between the two warps that share a TMEM lane quarter
+  static constexpr int XMAX_OFF = BAR_OFF + 256;
+  static constexpr int XL_OFF = XMAX_OFF + 2 * 2 * 2 * 128 * 4;
+  static constexpr int END = XL_OFF + 2 * 2 * 128 * 4;
   // at least 120 KB: one CTA (512 TMEM columns) per SM
-  static constexpr int SMEM = BAR_OFF + 256 > 120 * 1024 ? BAR_OFF + 256 : 120 * 1024;
+  static constexpr int SMEM = END > 120 * 1024 ? END : 120 * 1024;
 };
+
+// 32 lanes x 32 columns, no wait (the caller waits once for several loads)
+__device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 lanes x 16 columns store (no wait)
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulate
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -482,7 +514,7 @@ __device__ __forceinline__ void tile2_range(const FwdParams& p, int r0, int t, l
 }
 
 template <int NA>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(576, 1)
     attn_fwd2_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                         const __grid_constant__ CUtensorMap mapV, FwdParams p) {
   using SM = Fwd2Smem<NA>;
@@ -497,6 +529,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t p_full = bar0 + 72;    // [2] tiles
   const uint32_t o_done = bar0 + 88;    // [2] tiles
   const uint32_t drain = bar0 + 104;
+  const uint32_t xbar = bar0 + 112;     // [2 tiles][4 quarters]: half-warp exchange
   uint32_t* tmem_slot = (uint32_t*)(smem + SM::BAR_OFF + 192);
   volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 196);
 
@@ -520,10 +553,11 @@ __global__ void __launch_bounds__(320, 1)
       tc::mbar_init(v_full + 8 * s, 1);
       tc::mbar_init(kv_empty + 8 * s, 1);
       tc::mbar_init(s_full + 8 * s, 1);
-      tc::mbar_init(p_full + 8 * s, 128);
+      tc::mbar_init(p_full + 8 * s, 256);
       tc::mbar_init(o_done + 8 * s, 1);
     }
     tc::mbar_init(drain, 1);
+    for (int x = 0; x < 8; ++x) tc::mbar_init(xbar + 8 * x, 64);
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -604,8 +638,9 @@ __global__ void __launch_bounds__(320, 1)
         issued = true;
         return true;
       };
-      for (int t = 0; t < 2 && ok; ++t)
-        if (nbl > 0 && part(t, kb_lo)) ok = issue_s(t, 0);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (ok && nbl > 0 && part(t, kb_lo)) ok = issue_s(t, 0);
       for (int i = 0; i < nbl && ok; ++i) {
         const long long j = kb_lo + i;
         const int st = i & 1;
@@ -613,7 +648,9 @@ __global__ void __launch_bounds__(320, 1)
           ok = false;
           break;
         }
-        for (int t = 0; t < 2 && ok; ++t) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
           if (part(t, j)) {
             if (!tc::mbar_wait(p_full + 8 * t, cnt[t] & 1, p.err, ERR_A_MMA, abort)) {
               ok = false;
@@ -640,8 +677,15 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
   } else {
-    // ---------------- softmax warpgroups (warps 2-5: tile 0, 6-9: tile 1)
-    const int t = (warp - 2) >> 2;
+    // ---------------- softmax: warps 2-9 tile 0, warps 10-17 tile 1 ------
+    // Two warps share each TMEM lane quarter of a tile; warp half hf takes
+    // keys [64 hf, 64 hf + 64) of every block and output columns
+    // [64 hf, 64 hf + 64).  The block's row maximum is combined through
+    // shared memory (double-buffered by block parity) and an mbarrier of the
+    // 64 threads of the pair, whose waits are bounded like every other wait
+    // here; each half keeps its own partial row sum.
+    const int t = (warp - 2) >> 3;
+    const int hf = ((warp - 2) >> 2) & 1;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int grow_ = r0 + BM * t + row;
@@ -649,39 +693,77 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tS = tmem + 128 * t + lane_off;
     const uint32_t tO = tmem + 256 + 128 * t + lane_off;
+    float* xmax = (float*)(smem + SM::XMAX_OFF) + t * (2 * 2 * 128);
+    float* xl = (float*)(smem + SM::XL_OFF) + t * (2 * 128);
+    const uint32_t xb = xbar + 8 * (4 * t + quarter);
     const float NEG_INF = -INFINITY;
     float m_run = NEG_INF, l_run = 0.f;
     bool ok = true;
     int cnt = 0;
-    for (long long j = lo_t[t]; j <= hi_t[t]; ++j, ++cnt) {
+    int xph = 0;  // completed phases of this pair's exchange barrier
+    long long my_lo, my_hi;
+    tile2_range(p, r0, t, &my_lo, &my_hi);
+    for (long long j = my_lo; j <= my_hi; ++j, ++cnt) {
       if (!warp_wait(s_full + 8 * t, cnt & 1, p.err, ERR_A_SOFT, abort)) {
         ok = false;
         break;
       }
       tc::tc_fence_after();
-      // pass 1: block maximum (scores stay in TMEM; 32 live registers)
+      float sv[64];
+      tmem_ld32_nw(tS + 64 * hf, *reinterpret_cast<float(*)[32]>(&sv[0]));
+      tmem_ld32_nw(tS + 64 * hf + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+      tmem_wait_ld();
       const long long kpos = j * BN2;
-      const long long lo = pos - p.W + 1 - kpos, hi = pos - kpos;
-      const bool full = lo <= 0 && hi >= BN2 - 1;
+      const long long lo_l = pos - p.W + 1 - kpos - 64 * hf, hi_l = pos - kpos - 64 * hf;
+      const int lo = (int)(lo_l < -1 ? -1 : (lo_l > 64 ? 64 : lo_l));
+      const int hi = (int)(hi_l < -1 ? -1 : (hi_l > 64 ? 64 : hi_l));
       float mb = NEG_INF;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tc::tmem_ld32(tS + 32 * c, v);
+      if (lo <= 0 && hi >= 63) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int col = 32 * c + k;
-          if (full || (col >= lo && col <= hi)) mb = fmaxf(mb, v[k] * p.scale_log2);
+        for (int c = 0; c < 64; ++c) {
+          sv[c] *= p.scale_log2;
+          mb = fmaxf(mb, sv[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          sv[c] = (c >= lo && c <= hi) ? sv[c] * p.scale_log2 : NEG_INF;
+          mb = fmaxf(mb, sv[c]);
         }
       }
+      float* xm = xmax + (cnt & 1) * (2 * 128);
+      xm[hf * 128 + row] = mb;
+      tc::mbar_arrive(xb);
+      if (!warp_wait(xb, xph & 1, p.err, ERR_A_SOFT, abort)) {
+        ok = false;
+        break;
+      }
+      ++xph;
+      mb = fmaxf(xm[row], xm[128 + row]);
       const bool grow = mb > m_run + 8.0f;
       const float m_new = grow ? mb : m_run;
       const float alpha = (grow && m_run != NEG_INF) ? exp2f(m_run - m_new) : 1.0f;
       const float m_use = m_new == NEG_INF ? 0.f : m_new;
       // P_t(j-1) V has completed (it was issued before S_t(j)): O_t is
-      // stable and P_t may be overwritten
+      // stable and P_t may be overwritten.  Keys [64 hf, 64 hf + 64) go to
+      // packed columns [32 hf, 32 hf + 32); the other half's columns of S
+      // were read before the exchange above.
+      float ls = 0.f;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float p0 = exp2f(sv[32 * q + 2 * c] - m_use), p1 = exp2f(sv[32 * q + 2 * c + 1] - m_use);
+          ls += p0 + p1;
+          pk[c] = pack_bf16(p0, p1);
+        }
+        tmem_st16u(tS + 32 * hf + 16 * q, pk);
+      }
+      l_run = l_run * alpha + ls;
+      m_run = m_new;
       if (cnt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        for (int c0 = 0; c0 < nO; c0 += 32) {
+        for (int c0 = 64 * hf; c0 < nO && c0 < 64 * hf + 64; c0 += 32) {
           float v[32];
           tc::tmem_ld32(tO + c0, v);
 #pragma unroll
@@ -689,39 +771,22 @@ __global__ void __launch_bounds__(320, 1)
           tmem_st32(tO + c0, v);
         }
       }
-      // pass 2: exponentials, packed two per column over the columns of S
-      // already read (P columns [16c, 16c+16) come from S columns
-      // [32c, 32c+32))
-      float ls = 0.f;
-#pragma unroll 1
-      for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int c = 2 * c2 + h2;
-          float v[32];
-          tc::tmem_ld32(tS + 32 * c, v);
-#pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            const int col = 32 * c + k;
-            const float p0 = (full || (col >= lo && col <= hi)) ? exp2f(v[k] * p.scale_log2 - m_use) : 0.f;
-            const float p1 = (full || (col + 1 >= lo && col + 1 <= hi)) ? exp2f(v[k + 1] * p.scale_log2 - m_use) : 0.f;
-            ls += p0 + p1;
-            pk[16 * h2 + k / 2] = pack_bf16(p0, p1);
-          }
-        }
-        tmem_st32u(tS + 32 * c2, pk);
-      }
-      l_run = l_run * alpha + ls;
-      m_run = m_new;
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc::tc_fence_before();
       tc::mbar_arrive(p_full + 8 * t);
     }
+    // row sum = both halves' partial sums
+    float l_tot = 0.f;
+    if (ok) {
+      xl[hf * 128 + row] = l_run;
+      tc::mbar_arrive(xb);
+      ok = warp_wait(xb, xph & 1, p.err, ERR_A_SOFT, abort);
+      l_tot = xl[row] + xl[128 + row];
+    }
     if (ok && cnt > 0 && warp_wait(o_done + 8 * t, (cnt - 1) & 1, p.err, ERR_A_SOFT, abort)) {
       tc::tc_fence_after();
-      const float il = 1.0f / l_run;
-      for (int c0 = 0; c0 < nO; c0 += 32) {
+      const float il = 1.0f / l_tot;
+      for (int c0 = 64 * hf; c0 < nO && c0 < 64 * hf + 64; c0 += 32) {
         float v[32];
         tc::tmem_ld32(tO + c0, v);
         if (grow_ < p.n) {
@@ -739,7 +804,8 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
       }
-      if (grow_ < p.n) p.lse[(int64_t)h * p.ld_lse + grow_] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+      if (hf == 0 && grow_ < p.n)
+        p.lse[(int64_t)h * p.ld_lse + grow_] = (m_run + log2f(l_tot)) * 0.69314718055994531f;
     }
   }
   tc::tc_fence_before();
@@ -811,7 +877,7 @@ __device__ __forceinline__ void bwd_tile_blocks(const BwdParams& p, int r0, long
 }
 
 template <int NA>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_dq_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
                       const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                       BwdParams p) {
@@ -853,8 +919,8 @@ __global__ void __launch_bounds__(192, 1)
       tc::mbar_init(v_full + 8 * s, 1);
       tc::mbar_init(kv_empty + 8 * s, 1);
       tc::mbar_init(s_full + 8 * s, 1);
-      tc::mbar_init(s_empty + 8 * s, 128);
-      tc::mbar_init(ds_full + 8 * s, 128);
+      tc::mbar_init(s_empty + 8 * s, 256);
+      tc::mbar_init(ds_full + 8 * s, 256);
       tc::mbar_init(ds_empty + 8 * s, 1);
     }
     tc::mbar_init(dq_done, 1);
@@ -974,7 +1040,10 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
+    // eight compute warps: two per TMEM lane quarter, each taking one half
+    // (32 columns) of the block's keys and of dq's head dimension
     const int quarter = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const int grow_ = r0 + row;
     const long long t = p.pos0 + grow_;
@@ -993,18 +1062,17 @@ __global__ void __launch_bounds__(192, 1)
       tc::tc_fence_after();
       const long long kpos = (kb0 + i) * BN;
       const long long lo = t - p.W + 1 - kpos, hi = t - kpos;
-      uint32_t pk[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      uint32_t pk[16];
+      {
         float sv[32], dp[32];
-        tc::tmem_ld32(tS + st * BN + 32 * half + lane_off, sv);
-        tc::tmem_ld32(tP + st * BN + 32 * half + lane_off, dp);
+        tc::tmem_ld32(tS + st * BN + 32 * hf + lane_off, sv);
+        tc::tmem_ld32(tP + st * BN + 32 * hf + lane_off, dp);
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const int cc = 32 * half + c;
+          const int cc = 32 * hf + c;
           const float p0 = (cc >= lo && cc <= hi) ? exp2f(sv[c] * p.scale_log2 - lse2) : 0.f;
           const float p1 = (cc + 1 >= lo && cc + 1 <= hi) ? exp2f(sv[c + 1] * p.scale_log2 - lse2) : 0.f;
-          pk[16 * half + c / 2] = pack_bf16(p0 * (dp[c] - Dt) * p.scale, p1 * (dp[c + 1] - Dt) * p.scale);
+          pk[c / 2] = pack_bf16(p0 * (dp[c] - Dt) * p.scale, p1 * (dp[c + 1] - Dt) * p.scale);
         }
       }
       tc::tc_fence_before();
@@ -1013,7 +1081,12 @@ __global__ void __launch_bounds__(192, 1)
         ok = false;
         break;
       }
-      store_row_sw128_pk(sbase + SM::DS_OFF + st * SM::DS_BYTES, row, pk);
+      {
+        const uint32_t base = sbase + SM::DS_OFF + st * SM::DS_BYTES + row * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          st_shared_v4(base + (((4 * hf + c) ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
       fence_proxy_async_smem();
       tc::tc_fence_before();
       tc::mbar_arrive(ds_full + 8 * st);
@@ -1021,7 +1094,7 @@ __global__ void __launch_bounds__(192, 1)
     if (ok && nb > 0 && !warp_wait(dq_done, 0, p.err, ERR_A_SOFT, abort)) ok = false;
     if (ok) {
       tc::tc_fence_after();
-      for (int c0 = 0; c0 < nO; c0 += 32) {
+      for (int c0 = 32 * hf; c0 < nO; c0 += 64) {
         float v[32];
         if (nb > 0) {
           tc::tmem_ld32(tQ + c0 + lane_off, v);
@@ -1076,7 +1149,7 @@ struct DkvSmem {
 };
 
 template <int NA>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_dkv_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
                        const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                        BwdParams p) {
@@ -1113,8 +1186,8 @@ __global__ void __launch_bounds__(192, 1)
       tc::mbar_init(q_full + 8 * s, 1);
       tc::mbar_init(q_empty + 8 * s, 1);
       tc::mbar_init(s_full + 8 * s, 1);
-      tc::mbar_init(s_empty + 8 * s, 128);
-      tc::mbar_init(pd_full + 8 * s, 128);
+      tc::mbar_init(s_empty + 8 * s, 256);
+      tc::mbar_init(pd_full + 8 * s, 256);
       tc::mbar_init(pd_empty + 8 * s, 1);
     }
     tc::mbar_init(acc_done, 1);
@@ -1238,7 +1311,10 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
+    // eight compute warps: two per TMEM lane quarter, each taking one half
+    // (32 query columns) of the block and of dk / dv's head dimension
     const int quarter = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const int j = j0 + row;                  // chunk-local key index
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -1253,19 +1329,18 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc::tc_fence_after();
-      const int t0 = (qb0 + i) * BN;
-      uint32_t pp[32], pd[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      const int t0 = (qb0 + i) * BN + 32 * hf;
+      uint32_t pp[16], pd[16];
+      {
         float sv[32], dp[32];
-        tc::tmem_ld32(tS + st * BN + 32 * half + lane_off, sv);
-        tc::tmem_ld32(tP + st * BN + 32 * half + lane_off, dp);
+        tc::tmem_ld32(tS + st * BN + 32 * hf + lane_off, sv);
+        tc::tmem_ld32(tP + st * BN + 32 * hf + lane_off, dp);
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float pv[2], dv[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int t = t0 + 32 * half + c + e;
+            const int t = t0 + c + e;
             const int rel = t - j;
             const bool valid = t < p.n && j < p.n && rel >= 0 && rel < p.W;
             const float l2 = valid ? lse_h[t] * 1.4426950408889634f : 0.f;
@@ -1273,8 +1348,8 @@ __global__ void __launch_bounds__(192, 1)
             pv[e] = valid ? exp2f(sv[c + e] * p.scale_log2 - l2) : 0.f;
             dv[e] = pv[e] * (dp[c + e] - Dt) * p.scale;
           }
-          pp[16 * half + c / 2] = pack_bf16(pv[0], pv[1]);
-          pd[16 * half + c / 2] = pack_bf16(dv[0], dv[1]);
+          pp[c / 2] = pack_bf16(pv[0], pv[1]);
+          pd[c / 2] = pack_bf16(dv[0], dv[1]);
         }
       }
       tc::tc_fence_before();
@@ -1283,8 +1358,16 @@ __global__ void __launch_bounds__(192, 1)
         ok = false;
         break;
       }
-      store_row_sw128_pk(sbase + SM::PT_OFF + st * SM::P_BYTES, row, pp);
-      store_row_sw128_pk(sbase + SM::DS_OFF + st * SM::P_BYTES, row, pd);
+      {
+        const uint32_t bp = sbase + SM::PT_OFF + st * SM::P_BYTES + row * 128;
+        const uint32_t bd = sbase + SM::DS_OFF + st * SM::P_BYTES + row * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t off = ((4 * hf + c) ^ (row & 7)) << 4;
+          st_shared_v4(bp + off, pp[4 * c], pp[4 * c + 1], pp[4 * c + 2], pp[4 * c + 3]);
+          st_shared_v4(bd + off, pd[4 * c], pd[4 * c + 1], pd[4 * c + 2], pd[4 * c + 3]);
+        }
+      }
       fence_proxy_async_smem();
       tc::tc_fence_before();
       tc::mbar_arrive(pd_full + 8 * st);
@@ -1293,18 +1376,18 @@ __global__ void __launch_bounds__(192, 1)
       tc::tc_fence_after();
       // per-head partials: ws[0][h][j][:] = dk, ws[1][h][j][:] = dv
       const int64_t plane = (int64_t)p.H * p.n * p.hd;
-      for (int c0 = 0; c0 < nO; c0 += 32) {
+      for (int c0 = 32 * hf; c0 < nO; c0 += 64) {
         float vk[32], vv[32];
         tc::tmem_ld32(tK + c0 + lane_off, vk);
         tc::tmem_ld32(tV + c0 + lane_off, vv);
         if (j < p.n) {
-          float* dk = p.ws + ((int64_t)h * p.n + j) * p.hd + c0;
-          float* dv = dk + plane;
+          float* dkp = p.ws + ((int64_t)h * p.n + j) * p.hd + c0;
+          float* dvp = dkp + plane;
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
             if (c0 + k < p.hd) {
-              *reinterpret_cast<float4*>(dk + k) = make_float4(vk[k], vk[k + 1], vk[k + 2], vk[k + 3]);
-              *reinterpret_cast<float4*>(dv + k) = make_float4(vv[k], vv[k + 1], vv[k + 2], vv[k + 3]);
+              *reinterpret_cast<float4*>(dkp + k) = make_float4(vk[k], vk[k + 1], vk[k + 2], vk[k + 3]);
+              *reinterpret_cast<float4*>(dvp + k) = make_float4(vv[k], vv[k + 1], vv[k + 2], vv[k + 3]);
             }
         }
       }
@@ -1479,7 +1562,7 @@ int launch_fwd2(const AttnArgs& a, int* err, cudaStream_t st) {
   p.ld_lse = a.ld_lse;
   p.err = err;
   dim3 grid((a.n + 2 * BM - 1) / (2 * BM), a.H);
-  attn_fwd2_tc_kernel<NA><<<grid, 320, SM::SMEM, st>>>(mq, mk, mv, p);
+  attn_fwd2_tc_kernel<NA><<<grid, 576, SM::SMEM, st>>>(mq, mk, mv, p);
   return (int)cudaPeekAtLastError();
 }
 
@@ -1494,8 +1577,9 @@ bool attn_tc_supported(const AttnArgs& a) {
 int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st, int variant) {
   if (a.n <= 0) return 0;
   if (!encoder() || !attn_tc_supported(a)) return (int)cudaErrorNotSupported;
-  // the one-tile kernel is the default: the two-tile one measured slower
-  if (variant == 0) variant = 1;
+  // the two-tile kernel measured faster at every size tried (1K and 16K
+  // rows, head dims 64 and 128)
+  if (variant == 0) variant = 2;
   if (variant == 2) return a.hd <= 64 ? launch_fwd2<1>(a, err, st) : launch_fwd2<2>(a, err, st);
   return a.hd <= 64 ? launch_fwd<1>(a, err, st) : launch_fwd<2>(a, err, st);
 }
@@ -1581,7 +1665,7 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
   p.parts = dq_parts(a, num_sms);
   const int64_t plane = (int64_t)a.n * a.H * a.hd;
   if (p.parts > 1 && (int64_t)p.parts * plane > a.ws_elems) p.parts = 1;
-  attn_dq_tc_kernel<NA><<<dim3((a.n + BM - 1) / BM, a.H, p.parts), 192, DQ::SMEM, st>>>(mq, mdo, mk, mv, p);
+  attn_dq_tc_kernel<NA><<<dim3((a.n + BM - 1) / BM, a.H, p.parts), 320, DQ::SMEM, st>>>(mq, mdo, mk, mv, p);
   if (p.parts > 1) {
     const int cols = a.H * a.hd;
     const int64_t quads = plane / 4;
@@ -1589,7 +1673,7 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
     attn_dq_reduce_kernel<<<grid, 256, 0, st>>>(a.ws, p.parts, a.n, cols, p.dqkv, p.ldg);
   }
   // dk / dv (after the dq reduction, which may use the same scratch)
-  attn_dkv_tc_kernel<NA><<<dim3(a.H, (a.n + BM - 1) / BM), 192, DKV::SMEM, st>>>(mq64, mdo64, mk, mv, p);
+  attn_dkv_tc_kernel<NA><<<dim3(a.H, (a.n + BM - 1) / BM), 320, DKV::SMEM, st>>>(mq64, mdo64, mk, mv, p);
   {
     const int64_t quads = (int64_t)2 * a.n * a.Hkv * a.hd / 4;
     const int grid = (int)std::min<int64_t>((quads + 255) / 256, (int64_t)num_sms * 8);
