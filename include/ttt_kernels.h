@@ -32,6 +32,17 @@ int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda,
                     const void* B, int64_t ldb, int32_t b_mn, const void* B2, float* C, int64_t ldc,
                     int32_t impl, void* stream);
 
+/* Weight-gradient product with the fused SGD step of the inner loop (the
+ * update of one fast weight, one plain gradient step per chunk):
+ *   w32[m, n] -= lr * sum_k A(m, k) B(n, k)
+ *   w16[m, n]  = rn_bf16(w32[m, n]);  w16lo[m, n] = rn_bf16(w32 - w16)
+ * A(m, k), B(n, k) as in ttt_kernel_gemm (bf16); w32 fp32 and w16 / w16lo
+ * bf16, all [M, N] row-major with row pitch ldw (w16 / w16lo may be NULL).
+ * impl 0: tcgen05 tensor cores; impl 1: SIMT. */
+int ttt_kernel_gemm_sgd(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn, const void* B,
+                        int64_t ldb, int32_t b_mn, float* w32, void* w16, void* w16lo, int64_t ldw, float lr,
+                        int32_t impl, void* stream);
+
 /* Sliding-window causal attention of one chunk, the attention core of the
  * decoder block (query t sees keys j with t - W < j <= t; grouped KV heads:
  * query head h reads KV head h / (H/Hkv)).  All matrices bf16, device memory:

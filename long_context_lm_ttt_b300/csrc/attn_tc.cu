@@ -1132,6 +1132,298 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
+// --- dq, two query tiles per CTA, dS kept in TMEM ---------------------------
+// As attn_dq_tc_kernel, but a CTA takes 256 query rows (two 128-row tiles)
+// of one head over 64-key blocks, and dS is written back into TMEM (two bf16
+// per 32-bit column) where the dQ product reads it as its A operand:
+//   TMEM per tile t: S [256t, +64) | dP [256t+64, +64) | dQ [256t+128, +128)
+// Each of the 16 compute warps (two per lane quarter and tile) handles 32
+// keys of a block and writes its packed dS over score columns it has read
+// itself (keys 32hf.. -> columns 32hf.., 16 wide), so no warp overwrites
+// scores another warp still has to read; the dQ MMA takes its four K = 16
+// slices from columns {0, 8, 32, 40}.  The MMA warp ping-pongs the tiles.
+template <int NA>
+struct Dq2Smem {
+  static constexpr int Q_BYTES = NA * BM * 128;   // one 128-row tile
+  static constexpr int KV_BYTES = NA * BN * 128;  // one 64-key block
+  static constexpr int Q_OFF = 0;                 // Q0, Q1
+  static constexpr int DO_OFF = 2 * Q_BYTES;      // dO0, dO1
+  static constexpr int K_OFF = 4 * Q_BYTES;
+  static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
+  static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
+  static constexpr int SMEM = BAR_OFF + 256 > 120 * 1024 ? BAR_OFF + 256 : 120 * 1024;
+};
+
+// key-block range of query tile t of the pair at r0 for the dq kernel
+__device__ __forceinline__ void dq2_range(const BwdParams& p, int r0, int t, long long* lo, long long* hi) {
+  const int rs = r0 + BM * t;
+  if (rs >= p.n) {
+    *lo = 1;
+    *hi = 0;
+    return;
+  }
+  const long long t_lo = p.pos0 + rs;
+  const long long t_hi = p.pos0 + min(rs + BM, p.n) - 1;
+  long long k_lo = t_lo - p.W + 1;
+  if (k_lo < 0) k_lo = 0;
+  *lo = k_lo / BN;
+  *hi = t_hi / BN;
+}
+
+template <int NA>
+__global__ void __launch_bounds__(576, 1)
+    attn_dq2_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
+                       const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                       BwdParams p) {
+  using SM = Dq2Smem<NA>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t bar0 = sbase + SM::BAR_OFF;
+  const uint32_t q_full = bar0;
+  const uint32_t k_full = bar0 + 8;      // [2] stages
+  const uint32_t v_full = bar0 + 24;     // [2]
+  const uint32_t kv_empty = bar0 + 40;   // [2]
+  const uint32_t s_full = bar0 + 56;     // [2] tiles
+  const uint32_t ds_full = bar0 + 72;    // [2] tiles
+  const uint32_t dq_done = bar0 + 88;
+  const uint32_t drain = bar0 + 96;
+  uint32_t* tmem_slot = (uint32_t*)(smem + SM::BAR_OFF + 192);
+  volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 196);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = blockIdx.x * 2 * BM, h = blockIdx.y, part = blockIdx.z;
+  const int kvh = h / (p.H / p.Hkv);
+  long long lo_t[2], hi_t[2];
+  dq2_range(p, r0, 0, &lo_t[0], &hi_t[0]);
+  dq2_range(p, r0, 1, &lo_t[1], &hi_t[1]);
+  const long long u_lo = lo_t[0];
+  const long long u_hi = hi_t[1] >= lo_t[1] ? max(hi_t[0], hi_t[1]) : hi_t[0];
+  const long long nb_all = u_hi - u_lo + 1;
+  const long long jb = u_lo + part * nb_all / p.parts;         // this part's blocks
+  const int nb = (int)(u_lo + (part + 1) * nb_all / p.parts - jb);
+  auto part_of = [&](int t, long long j) { return j >= lo_t[t] && j <= hi_t[t]; };
+  const int ksteps = p.hd / 16;
+  const int nO = (p.hd + 15) & ~15;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(k_full + 8 * s, 1);
+      tc::mbar_init(v_full + 8 * s, 1);
+      tc::mbar_init(kv_empty + 8 * s, 1);
+      tc::mbar_init(s_full + 8 * s, 1);
+      tc::mbar_init(ds_full + 8 * s, 256);
+    }
+    tc::mbar_init(dq_done, 1);
+    tc::mbar_init(drain, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&mapQ);
+    tc::prefetch_tmap(&mapDO);
+    tc::prefetch_tmap(&mapK);
+    tc::prefetch_tmap(&mapV);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0 && nb > 0) {
+      bool ok = true;
+      int issued = 0;
+      tc::mbar_arrive_expect_tx(q_full, 4 * SM::Q_BYTES);
+      for (int t = 0; t < 2; ++t)
+        for (int a = 0; a < NA; ++a) {
+          tc::tma_load_2d(sbase + SM::Q_OFF + t * SM::Q_BYTES + a * BM * 128, &mapQ, h * p.hd + 64 * a,
+                          r0 + BM * t, q_full);
+          tc::tma_load_2d(sbase + SM::DO_OFF + t * SM::Q_BYTES + a * BM * 128, &mapDO, h * p.hd + 64 * a,
+                          r0 + BM * t, q_full);
+        }
+      for (int i = 0; i < nb && ok; ++i) {
+        const int st = i & 1;
+        if (!tc::mbar_wait(kv_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
+          ok = false;
+          break;
+        }
+        const long long kpos = (jb + i) * BN;
+        const int row = kvh * p.R + (int)(kpos % p.R);
+        tc::mbar_arrive_expect_tx(k_full + 8 * st, SM::KV_BYTES);
+        for (int a = 0; a < NA; ++a)
+          tc::tma_load_2d(sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN * 128, &mapK, 64 * a, row,
+                          k_full + 8 * st);
+        tc::mbar_arrive_expect_tx(v_full + 8 * st, SM::KV_BYTES);
+        for (int a = 0; a < NA; ++a)
+          tc::tma_load_2d(sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN * 128, &mapV, 64 * a, row,
+                          v_full + 8 * st);
+        issued = i + 1;
+      }
+      const long long t0 = clock64();
+      while (!tc::mbar_try_wait(q_full, 0) && clock64() - t0 < tc::kWaitClocks) {
+      }
+      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
+        const int st = i & 1;
+        const uint32_t par = (i >> 1) & 1;
+        const long long t1 = clock64();
+        while (!(tc::mbar_try_wait(k_full + 8 * st, par) && tc::mbar_try_wait(v_full + 8 * st, par)) &&
+               clock64() - t1 < tc::kWaitClocks) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && nb > 0) {
+      const uint32_t idS = tc::idesc_bf16(BM, BN, 0, 0);
+      const uint32_t idQ = tc::idesc_bf16(BM, nO, 0, 1);
+      bool ok = tc::mbar_wait(q_full, 0, p.err, ERR_A_MMA, abort);
+      bool issued = false;
+      int cnt[2] = {0, 0};
+      auto issue_sdp = [&](int t, int i) -> bool {
+        const int st = i & 1;
+        if (!tc::mbar_wait(k_full + 8 * st, (i >> 1) & 1, p.err, ERR_A_MMA, abort) ||
+            !tc::mbar_wait(v_full + 8 * st, (i >> 1) & 1, p.err, ERR_A_MMA, abort))
+          return false;
+        tc::tc_fence_after();
+        const uint32_t kb = sbase + SM::K_OFF + st * SM::KV_BYTES;
+        const uint32_t vb = sbase + SM::V_OFF + st * SM::KV_BYTES;
+        for (int j = 0; j < ksteps; ++j) {
+          const int a = j >> 2;
+          const uint32_t ao = a * BM * 128 + 32 * (j & 3);
+          const uint32_t bo = a * BN * 128 + 32 * (j & 3);
+          tc::mma_bf16(tmem + 256 * t, tc::smem_desc_sw128(sbase + SM::Q_OFF + t * SM::Q_BYTES + ao, 16, 1024),
+                       tc::smem_desc_sw128(kb + bo, 16, 1024), idS, j > 0);
+          tc::mma_bf16(tmem + 256 * t + 64,
+                       tc::smem_desc_sw128(sbase + SM::DO_OFF + t * SM::Q_BYTES + ao, 16, 1024),
+                       tc::smem_desc_sw128(vb + bo, 16, 1024), idS, j > 0);
+        }
+        tc::mma_commit(s_full + 8 * t);
+        issued = true;
+        return true;
+      };
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (ok && part_of(t, jb)) ok = issue_sdp(t, 0);
+      for (int i = 0; i < nb && ok; ++i) {
+        const long long j = jb + i;
+        const int st = i & 1;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
+          if (part_of(t, j)) {
+            if (!tc::mbar_wait(ds_full + 8 * t, cnt[t] & 1, p.err, ERR_A_MMA, abort)) {
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t kb = sbase + SM::K_OFF + st * SM::KV_BYTES;
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k)
+              mma_bf16_ts(tmem + 256 * t + 128, tmem + 256 * t + (k < 2 ? 8 * k : 32 + 8 * (k - 2)),
+                          tc::smem_desc_sw128(kb + 2048 * k, BN * 128, 1024), idQ, (cnt[t] > 0 || k > 0) ? 1u : 0u);
+            ++cnt[t];
+          }
+          if (i + 1 < nb && part_of(t, j + 1)) ok = issue_sdp(t, i + 1);
+        }
+        if (ok) tc::mma_commit(kv_empty + 8 * st);
+      }
+      if (ok) tc::mma_commit(dq_done);
+      if (!ok && issued) {
+        tc::mma_commit(drain);
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(drain, 0) && clock64() - t0 < tc::kWaitClocks) {
+        }
+      }
+    }
+  } else {
+    const int t = (warp - 2) >> 3;
+    const int hf = ((warp - 2) >> 2) & 1;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int grow_ = r0 + BM * t + row;
+    const long long pos = p.pos0 + grow_;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tT = tmem + 256 * t + lane_off;
+    const bool rvalid = grow_ < p.n;
+    const float lse2 = rvalid ? p.lse[(int64_t)h * p.ld_lse + grow_] * 1.4426950408889634f : 0.f;
+    const float Dt = rvalid ? p.dsum[(int64_t)h * p.ld_lse + grow_] : 0.f;
+    long long my_lo, my_hi;
+    dq2_range(p, r0, t, &my_lo, &my_hi);
+    const long long j_beg = max(my_lo, jb), j_end = min(my_hi, jb + nb - 1);
+    bool ok = true;
+    int cnt = 0;
+    for (long long j = j_beg; j <= j_end; ++j, ++cnt) {
+      if (!warp_wait(s_full + 8 * t, cnt & 1, p.err, ERR_A_SOFT, abort)) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      float sv[32], dp[32];
+      tmem_ld32_nw(tT + 32 * hf, sv);
+      tmem_ld32_nw(tT + 64 + 32 * hf, dp);
+      tmem_wait_ld();
+      const long long kpos = j * BN + 32 * hf;
+      const long long lo_l = pos - p.W + 1 - kpos, hi_l = pos - kpos;
+      const int lo = (int)(lo_l < -1 ? -1 : (lo_l > 32 ? 32 : lo_l));
+      const int hi = (int)(hi_l < -1 ? -1 : (hi_l > 32 ? 32 : hi_l));
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        const float p0 = (c >= lo && c <= hi) ? exp2f(sv[c] * p.scale_log2 - lse2) : 0.f;
+        const float p1 = (c + 1 >= lo && c + 1 <= hi) ? exp2f(sv[c + 1] * p.scale_log2 - lse2) : 0.f;
+        pk[c / 2] = pack_bf16(p0 * (dp[c] - Dt) * p.scale, p1 * (dp[c + 1] - Dt) * p.scale);
+      }
+      tmem_st16u(tT + 32 * hf, pk);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc::tc_fence_before();
+      tc::mbar_arrive(ds_full + 8 * t);
+    }
+    const bool have = cnt > 0;
+    if (ok && have && !warp_wait(dq_done, 0, p.err, ERR_A_SOFT, abort)) ok = false;
+    if (ok && (have || p.parts > 1)) {
+      tc::tc_fence_after();
+      for (int c0 = 64 * hf; c0 < nO && c0 < 64 * hf + 64; c0 += 32) {
+        float v[32];
+        if (have) {
+          tc::tmem_ld32(tT + 128 + c0, v);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = 0.f;
+        }
+        if (!rvalid) continue;
+        if (p.parts == 1) {
+          bf16* dst = p.dqkv + (int64_t)grow_ * p.ldg + (int64_t)h * p.hd + c0;
+#pragma unroll
+          for (int k = 0; k < 32; k += 8)
+            if (c0 + k < p.hd) {
+              uint4 u;
+              u.x = pack_bf16(v[k], v[k + 1]);
+              u.y = pack_bf16(v[k + 2], v[k + 3]);
+              u.z = pack_bf16(v[k + 4], v[k + 5]);
+              u.w = pack_bf16(v[k + 6], v[k + 7]);
+              *reinterpret_cast<uint4*>(dst + k) = u;
+            }
+        } else {
+          float* dst = p.ws + ((int64_t)part * p.n + grow_) * ((int64_t)p.H * p.hd) + (int64_t)h * p.hd + c0;
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            if (c0 + k < p.hd) *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
 // --- dk / dv of the chunk's own keys, one CTA per (key tile, query head) ---
 template <int NA>
 struct DkvSmem {
@@ -1586,13 +1878,14 @@ int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st, int variant) {
 
 // key-range parts of the dq kernel: enough CTAs to fill the SMs in whole
 // waves, never more parts than the smallest tile has key blocks
-static int dq_parts(const AttnArgs& a, int num_sms) {
-  const int ntiles = (a.n + BM - 1) / BM;
+// rows per dq CTA: 2 * BM (two-tile kernel) or BM
+static int dq_parts(const AttnArgs& a, int num_sms, int rows_per_cta = BM) {
+  const int ntiles = (a.n + rows_per_cta - 1) / rows_per_cta;
   long long kb0 = (a.pos0 - a.W + 1 > 0 ? a.pos0 - a.W + 1 : 0) / BN;
   int nb_min = INT32_MAX;
   for (int t = 0; t < ntiles; ++t) {
-    const long long t_lo = a.pos0 + (long long)t * BM;
-    const long long t_hi = a.pos0 + std::min(t * BM + BM, a.n) - 1;
+    const long long t_lo = a.pos0 + (long long)t * rows_per_cta;
+    const long long t_hi = a.pos0 + std::min(t * rows_per_cta + rows_per_cta, a.n) - 1;
     long long k_lo = t_lo - a.W + 1;
     if (k_lo < 0) k_lo = 0;
     kb0 = k_lo / BN;
@@ -1620,7 +1913,7 @@ int64_t attn_bwd_tc_ws_elems(int n, int H, int hd, int num_sms) {
 
 template <int NA>
 int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
-  using DQ = DqSmem<NA>;
+  using DQ = Dq2Smem<NA>;
   using DKV = DkvSmem<NA>;
   CUtensorMap mq, mdo, mk, mv, mq64, mdo64;
   const uint64_t ldq = (uint64_t)a.H * a.hd;
@@ -1633,7 +1926,7 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
   if (rc) return rc;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_dq_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_dq2_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DQ::SMEM);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_dkv_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize, DKV::SMEM);
@@ -1662,10 +1955,11 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
     attn_bwd_prep_tc_kernel<<<(warps + 7) / 8, 256, 0, st>>>((const bf16*)a.dout, (const bf16*)a.out, a.n, a.H,
                                                              a.hd, a.Dsum, a.ld_lse);
   }
-  p.parts = dq_parts(a, num_sms);
+  p.parts = dq_parts(a, num_sms, 2 * BM);
   const int64_t plane = (int64_t)a.n * a.H * a.hd;
   if (p.parts > 1 && (int64_t)p.parts * plane > a.ws_elems) p.parts = 1;
-  attn_dq_tc_kernel<NA><<<dim3((a.n + BM - 1) / BM, a.H, p.parts), 320, DQ::SMEM, st>>>(mq, mdo, mk, mv, p);
+  attn_dq2_tc_kernel<NA><<<dim3((a.n + 2 * BM - 1) / (2 * BM), a.H, p.parts), 576, DQ::SMEM, st>>>(mq, mdo, mk, mv,
+                                                                                                  p);
   if (p.parts > 1) {
     const int cols = a.H * a.hd;
     const int64_t quads = plane / 4;

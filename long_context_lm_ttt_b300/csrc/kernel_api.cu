@@ -48,6 +48,36 @@ extern "C" int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, i
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
 }
 
+extern "C" int ttt_kernel_gemm_sgd(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn,
+                                   const void* B, int64_t ldb, int32_t b_mn, float* w32, void* w16, void* w16lo,
+                                   int64_t ldw, float lr, int32_t impl, void* stream) {
+  if (!A || !B || !w32 || M < 0 || N < 0 || K < 1 || (N & 1) || (ldw & 1) || ldw < N) return TTT_ERR_INVALID;
+  if (impl != 0 && impl != 1) return TTT_ERR_INVALID;
+  if (ensure_err()) return TTT_ERR_OOM;
+  cudaStream_t st = (cudaStream_t)stream;
+  ttt::Epi e;
+  memset(&e, 0, sizeof(e));
+  e.kind = ttt::EPI_SGD;
+  e.w32 = w32;
+  e.w16 = w16;
+  e.w16lo = w16lo;
+  e.ldo = ldw;
+  e.lr = lr;
+  ttt::GemmArgs<ttt::bf16> g{M, N, K, (const ttt::bf16*)A, lda, a_mn, (const ttt::bf16*)B, ldb, b_mn, e,
+                             nullptr, nullptr, 0};
+  if (impl == 0) {
+    if (ttt::gemm_tc_init()) return TTT_ERR_CUDA;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int rc = ttt::gemm_tc(g, sms, g_err, st);
+    if (rc == (int)cudaErrorNotSupported || rc == (int)cudaErrorInvalidValue) return TTT_ERR_SHAPE;
+    return rc ? TTT_ERR_CUDA : 0;
+  }
+  ttt::gemm_simt<ttt::bf16>(g, st);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
+}
+
 static int attn_check(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R,
                       int32_t max_impl = 1) {
   if (impl < 0 || impl > max_impl) return TTT_ERR_INVALID;

@@ -2,6 +2,7 @@
 points (include/ttt_kernels.h), for profiling one kernel in isolation.
 
     python -m long_context_lm_ttt_b300.microbench gemm --M 1024 --N 16384 --K 3072
+    python -m long_context_lm_ttt_b300.microbench gemm-sgd --M 3072 --N 8192 --K 1024
     python -m long_context_lm_ttt_b300.microbench attn-fwd --n 1024 --H 24 --Hkv 8 --hd 128 --W 8192
     python -m long_context_lm_ttt_b300.microbench attn-bwd --n 1024 --H 24 --Hkv 8 --hd 128 --W 8192
 
@@ -49,6 +50,25 @@ def gemm(args):
     assert T.ttt_kernel_error() == 0
     return {"kernel": "gemm", "M": M, "N": N, "K": K, "a_mn": args.a_mn, "b_mn": args.b_mn, "ms": ms,
             "tflops": 2.0 * M * N * K / (ms / 1e3) / 1e12}
+
+
+def gemm_sgd(args):
+    g = torch.Generator(device="cuda").manual_seed(0)
+    M, N, K = args.M, args.N, args.K
+    A = torch.randn((K, M), device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn((K, N), device="cuda", generator=g).to(torch.bfloat16)
+    w32 = torch.randn((M, N), device="cuda", generator=g) * 0.02
+    hi = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
+    lo = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
+
+    def run():
+        T.ttt_kernel_gemm_sgd(M, N, K, A, M, 1, B, N, 1, w32, hi, lo, N, 1e-6, args.impl)
+
+    ms = _events(run, args.warmup, args.iters)
+    assert T.ttt_kernel_error() == 0
+    nbytes = 12.0 * M * N + 2.0 * K * (M + N)
+    return {"kernel": "gemm_sgd", "M": M, "N": N, "K": K, "ms": ms,
+            "tflops": 2.0 * M * N * K / (ms / 1e3) / 1e12, "gbs": nbytes / (ms / 1e3) / 1e9}
 
 
 def _attn_inputs(args):
@@ -111,6 +131,10 @@ def main():
     g.add_argument("--K", type=int, default=3072)
     g.add_argument("--a-mn", type=int, default=0)
     g.add_argument("--b-mn", type=int, default=0)
+    gs = sub.add_parser("gemm-sgd")
+    gs.add_argument("--M", type=int, default=3072)
+    gs.add_argument("--N", type=int, default=8192)
+    gs.add_argument("--K", type=int, default=1024)
     for name in ("attn-fwd", "attn-bwd"):
         a = sub.add_parser(name)
         a.add_argument("--n", type=int, default=1024)
@@ -126,7 +150,7 @@ def main():
     args = ap.parse_args()
     torch.cuda.set_device(0)
     T.load()
-    out = {"gemm": gemm, "attn-fwd": attn_fwd, "attn-bwd": attn_bwd}[args.what](args)
+    out = {"gemm": gemm, "gemm-sgd": gemm_sgd, "attn-fwd": attn_fwd, "attn-bwd": attn_bwd}[args.what](args)
     print(json.dumps(out), flush=True)
 
 

@@ -88,6 +88,9 @@ def load(path: str = LIB_PATH):
                                     c_int64, c_int32, c_void_p, c_void_p, c_int64, c_int32, c_void_p]
     lib.ttt_kernel_gemm.restype = c_int32
     i32 = c_int32
+    lib.ttt_kernel_gemm_sgd.argtypes = [i32, i32, i32, c_void_p, c_int64, i32, c_void_p, c_int64, i32, c_void_p,
+                                        c_void_p, c_void_p, c_int64, c_float, i32, c_void_p]
+    lib.ttt_kernel_gemm_sgd.restype = c_int32
     lib.ttt_kernel_attn_fwd.argtypes = [i32, i32, i32, i32, i32, i32, i32, c_int64, c_void_p, c_void_p,
                                         c_void_p, c_void_p, c_void_p, i32, c_void_p]
     lib.ttt_kernel_attn_fwd.restype = c_int32
@@ -229,6 +232,14 @@ GEMM_TC, GEMM_SIMT_BF16, GEMM_SIMT_F32 = 0, 1, 2
 def ttt_kernel_gemm(M, N, K, A, lda, a_mn, B, ldb, b_mn, B2, C, ldc, impl, stream=None) -> int:
     rc = load().ttt_kernel_gemm(int(M), int(N), int(K), _ptr(A), int(lda), int(a_mn), _ptr(B), int(ldb),
                                 int(b_mn), _ptr(B2), _ptr(C), int(ldc), int(impl), _stream(stream))
+    _check(rc)
+    return rc
+
+
+def ttt_kernel_gemm_sgd(M, N, K, A, lda, a_mn, B, ldb, b_mn, w32, w16, w16lo, ldw, lr, impl, stream=None) -> int:
+    rc = load().ttt_kernel_gemm_sgd(int(M), int(N), int(K), _ptr(A), int(lda), int(a_mn), _ptr(B), int(ldb),
+                                    int(b_mn), _ptr(w32), _ptr(w16), _ptr(w16lo), int(ldw), float(lr), int(impl),
+                                    _stream(stream))
     _check(rc)
     return rc
 

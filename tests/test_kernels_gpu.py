@@ -88,3 +88,33 @@ def test_gemm_fp32_simt():
     torch.cuda.synchronize()
     ref = a.astype(np.float64) @ b.astype(np.float64)
     assert np.abs(C.cpu().numpy() - ref).max() / np.abs(ref).max() < 1e-5
+
+
+@pytest.mark.parametrize("M,N,K", [(3072, 8192, 1024), (16384, 3072, 1024), (200, 96, 40), (256, 384, 512)])
+@pytest.mark.parametrize("impl", [0, 1])
+def test_gemm_sgd(M, N, K, impl):
+    """Weight gradient + fused SGD step: w32 -= lr A^T B (both operands stored
+    [K, M] / [K, N], as the chunk's activations are), then the bf16 pair
+    hi = rn(w32), lo = rn(w32 - hi)."""
+    torch, T = _env()
+    if impl == 1 and M * N * K > 2 ** 30:
+        pytest.skip("SIMT reference only on the small shapes")
+    rng = np.random.default_rng(M + N + K + impl)
+    a, a_st = _operand(rng, M, K, 1)
+    b, b_st = _operand(rng, N, K, 1)
+    w0 = (rng.standard_normal((M, N)) * 0.02).astype(np.float32)
+    lr = 1e-3
+    cu = lambda x: torch.from_numpy(x).to(torch.bfloat16).cuda()
+    w32 = torch.from_numpy(w0).cuda()
+    hi = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    lo = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    T.ttt_kernel_gemm_sgd(M, N, K, cu(a_st), M, 1, cu(b_st), N, 1, w32, hi, lo, N, lr, impl)
+    torch.cuda.synchronize()
+    assert T.ttt_kernel_error() == 0
+    ref = w0.astype(np.float64) - lr * (a @ b.T)
+    got = w32.cpu().numpy().astype(np.float64)
+    upd = np.abs(lr * (a @ b.T)).max()
+    assert np.abs(got - ref).max() <= 1e-5 * upd + 2e-9, np.abs(got - ref).max()
+    g32 = w32.cpu()
+    assert torch.equal(hi.cpu(), g32.to(torch.bfloat16))
+    assert torch.equal(lo.cpu(), (g32 - g32.to(torch.bfloat16).float()).to(torch.bfloat16))
