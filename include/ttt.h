@@ -137,7 +137,7 @@ int ttt_reset(ttt_ctx* ctx);
  * profiling on, every kernel launch of ttt_prefill / ttt_logits is
  * bracketed by two CUDA events on the call's stream; the pairs are resolved
  * when the call synchronises and summed per class:
- *   "gemm_fwd"      projections of the forward (q/k/v + RoPE + ring write,
+ *   "gemm_fwd"      projections of the chunk loop's forward (q/k/v + RoPE + ring write,
  *                   output + residual, gate/up + SwiGLU, down + residual)
  *   "gemm_lm_head"  the streamed lm_head products of the cross-entropy
  *   "gemm_bwd_dx"   input-gradient products of the backward
@@ -145,6 +145,9 @@ int ttt_reset(ttt_ctx* ctx);
  *   "attn_fwd"      sliding-window attention forward
  *   "attn_bwd"      chunk-local attention backward
  *   "rowwise"       embedding, norms, softmax statistics, RoPE backward
+ *   "gemm_fwd_bulk" forward projections of the frozen blocks, run over
+ *                   spans longer than a chunk (ttt_prefill)
+ *   "attn_fwd_bulk" their sliding-window attention forward
  * `flops` counts 2 per multiply-add of the operation as defined (attention:
  * unmasked query/key pairs only; no recomputation, no padding), `bytes`
  * the operands read once and results written once.  The events add a few

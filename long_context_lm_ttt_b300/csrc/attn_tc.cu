@@ -463,6 +463,51 @@ __device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 2^x for x <= 0 (the softmax exponent after the row maximum is subtracted):
+// the MUFU instruction, subnormal results flushed to zero
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// (a0, a1) * b + c for two lanes of fp32 in one packed instruction
+__device__ __forceinline__ void fma2(float a0, float a1, float b, float c, float& d0, float& d1) {
+  asm("{\n.reg .b64 ra, rb, rc, rd;\n"
+      "mov.b64 ra, {%2, %3};\n"
+      "mov.b64 rb, {%4, %4};\n"
+      "mov.b64 rc, {%5, %5};\n"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n"
+      "mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// (a0, a1) * (b0, b1)
+__device__ __forceinline__ void mul2(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+  asm("{\n.reg .b64 ra, rb, rd;\n"
+      "mov.b64 ra, {%2, %3};\n"
+      "mov.b64 rb, {%4, %5};\n"
+      "mul.rn.f32x2 rd, ra, rb;\n"
+      "mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// (a0, a1) + (b0, b1)
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n.reg .b64 ra, rb, rd;\n"
+      "mov.b64 ra, {%0, %1};\n"
+      "mov.b64 rb, {%2, %3};\n"
+      "add.rn.f32x2 rd, ra, rb;\n"
+      "mov.b64 {%0, %1}, rd;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
 // 32 lanes x 16 columns store (no wait)
 __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
@@ -717,20 +762,15 @@ __global__ void __launch_bounds__(576, 1)
       const long long lo_l = pos - p.W + 1 - kpos - 64 * hf, hi_l = pos - kpos - 64 * hf;
       const int lo = (int)(lo_l < -1 ? -1 : (lo_l > 64 ? 64 : lo_l));
       const int hi = (int)(hi_l < -1 ? -1 : (hi_l > 64 ? 64 : hi_l));
-      float mb = NEG_INF;
-      if (lo <= 0 && hi >= 63) {
+      // maximum of the raw scores (the scale is positive); masked -> -inf
+      if (!(lo <= 0 && hi >= 63)) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          sv[c] *= p.scale_log2;
-          mb = fmaxf(mb, sv[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          sv[c] = (c >= lo && c <= hi) ? sv[c] * p.scale_log2 : NEG_INF;
-          mb = fmaxf(mb, sv[c]);
-        }
+        for (int c = 0; c < 64; ++c) sv[c] = (c >= lo && c <= hi) ? sv[c] : NEG_INF;
       }
+      float mb = NEG_INF;
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) mb = max3f(mb, sv[c], sv[c + 1]);
+      mb *= p.scale_log2;
       float* xm = xmax + (cnt & 1) * (2 * 128);
       xm[hf * 128 + row] = mb;
       tc::mbar_arrive(xb);
@@ -748,18 +788,23 @@ __global__ void __launch_bounds__(576, 1)
       // stable and P_t may be overwritten.  Keys [64 hf, 64 hf + 64) go to
       // packed columns [32 hf, 32 hf + 32); the other half's columns of S
       // were read before the exchange above.
-      float ls = 0.f;
+      // p = 2^(s * scale - m): one packed FMA per two scores, one MUFU each
+      float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float p0 = exp2f(sv[32 * q + 2 * c] - m_use), p1 = exp2f(sv[32 * q + 2 * c + 1] - m_use);
-          ls += p0 + p1;
+          float x0, x1;
+          fma2(sv[32 * q + 2 * c], sv[32 * q + 2 * c + 1], p.scale_log2, -m_use, x0, x1);
+          const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+          ls0 += p0;
+          ls1 += p1;
           pk[c] = pack_bf16(p0, p1);
         }
         tmem_st16u(tS + 32 * hf + 16 * q, pk);
       }
+      const float ls = ls0 + ls1;
       l_run = l_run * alpha + ls;
       m_run = m_new;
       if (cnt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
@@ -1370,12 +1415,18 @@ __global__ void __launch_bounds__(576, 1)
       const long long lo_l = pos - p.W + 1 - kpos, hi_l = pos - kpos;
       const int lo = (int)(lo_l < -1 ? -1 : (lo_l > 32 ? 32 : lo_l));
       const int hi = (int)(hi_l < -1 ? -1 : (hi_l > 32 ? 32 : hi_l));
+      // dS = P (dP - D) / sqrt(hd) = P * (dP * scale - D * scale)
+      const float nDs = -Dt * p.scale;
       uint32_t pk[16];
 #pragma unroll
       for (int c = 0; c < 32; c += 2) {
-        const float p0 = (c >= lo && c <= hi) ? exp2f(sv[c] * p.scale_log2 - lse2) : 0.f;
-        const float p1 = (c + 1 >= lo && c + 1 <= hi) ? exp2f(sv[c + 1] * p.scale_log2 - lse2) : 0.f;
-        pk[c / 2] = pack_bf16(p0 * (dp[c] - Dt) * p.scale, p1 * (dp[c + 1] - Dt) * p.scale);
+        float x0, x1, y0, y1, d0, d1;
+        fma2(sv[c], sv[c + 1], p.scale_log2, -lse2, x0, x1);
+        const float p0 = (c >= lo && c <= hi) ? ex2_ftz(x0) : 0.f;
+        const float p1 = (c + 1 >= lo && c + 1 <= hi) ? ex2_ftz(x1) : 0.f;
+        fma2(dp[c], dp[c + 1], p.scale, nDs, y0, y1);
+        mul2(p0, p1, y0, y1, d0, d1);
+        pk[c / 2] = pack_bf16(d0, d1);
       }
       tmem_st16u(tT + 32 * hf, pk);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -1637,8 +1688,8 @@ __global__ void __launch_bounds__(320, 1)
             const bool valid = t < p.n && j < p.n && rel >= 0 && rel < p.W;
             const float l2 = valid ? lse_h[t] * 1.4426950408889634f : 0.f;
             const float Dt = valid ? d_h[t] : 0.f;
-            pv[e] = valid ? exp2f(sv[c + e] * p.scale_log2 - l2) : 0.f;
-            dv[e] = pv[e] * (dp[c + e] - Dt) * p.scale;
+            pv[e] = valid ? ex2_ftz(fmaf(sv[c + e], p.scale_log2, -l2)) : 0.f;
+            dv[e] = pv[e] * fmaf(dp[c + e], p.scale, -Dt * p.scale);
           }
           pp[c / 2] = pack_bf16(pv[0], pv[1]);
           pd[c / 2] = pack_bf16(dv[0], dv[1]);

@@ -101,7 +101,10 @@ struct EngineBase {
   // --- optional per-launch timing (ttt_profile) ---------------------------
   // Each profiled launch is bracketed by two events on its own stream; the
   // events are resolved after the call's final synchronisation.
-  enum ProfCls { P_GEMM_FWD, P_GEMM_LMHEAD, P_GEMM_BWD, P_GEMM_SGD, P_ATTN_FWD, P_ATTN_BWD, P_ROW, P_N };
+  enum ProfCls {
+    P_GEMM_FWD, P_GEMM_LMHEAD, P_GEMM_BWD, P_GEMM_SGD, P_ATTN_FWD, P_ATTN_BWD, P_ROW,
+    P_GEMM_FWD_BULK, P_ATTN_FWD_BULK, P_N
+  };
   struct ProfRec {
     int cls, nk;
     cudaEvent_t a, b;
@@ -113,8 +116,8 @@ struct EngineBase {
   std::vector<ProfRec> prof_recs;
   ttt_kernel_stat prof_stat[P_N];
   static const char* prof_name(int c) {
-    static const char* n[P_N] = {"gemm_fwd", "gemm_lm_head", "gemm_bwd_dx", "gemm_dw_sgd",
-                                 "attn_fwd", "attn_bwd", "rowwise"};
+    static const char* n[P_N] = {"gemm_fwd", "gemm_lm_head", "gemm_bwd_dx", "gemm_dw_sgd", "attn_fwd",
+                                 "attn_bwd", "rowwise", "gemm_fwd_bulk", "attn_fwd_bulk"};
     return n[c];
   }
   void prof_clear() {
@@ -437,6 +440,9 @@ struct Engine : EngineBase {
       case EPI_SWIGLU: out_b = (double)M * N * sizeof(T) * (e.stash ? 1.5 : 0.5); break;
       default: break;
     }
+    // the forward products of the frozen blocks' bulk pass (more rows than a
+    // chunk) form their own class
+    if (cls == P_GEMM_FWD && M > cfg.chunk) cls = P_GEMM_FWD_BULK;
     const double flops = 2.0 * M * N * K;
     const double bytes = (double)sizeof(T) * ((double)M * K + (double)N * K) + out_b;
     int nk = 1;
@@ -498,7 +504,7 @@ struct Engine : EngineBase {
     const double hdH = (double)a.H * a.hd;
     const double kv = (double)std::min<int64_t>(a.pos0 + a.n, (int64_t)a.W + a.n - 1) * a.Hkv * a.hd;
     const double bytes = sizeof(T) * (2.0 * a.n * hdH + 2.0 * kv) + 4.0 * a.n * a.H;
-    prof(P_ATTN_FWD, 4.0 * hdH * P, bytes, st, [&] {
+    prof(a.n > cfg.chunk ? P_ATTN_FWD_BULK : P_ATTN_FWD, 4.0 * hdH * P, bytes, st, [&] {
       if constexpr (kBF16) {
         if (use_tc_attn && attn_tc_supported(a)) {
           int r = attn_fwd_tc(a, dev_err + 2, st);
