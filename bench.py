@@ -54,8 +54,12 @@ def parse_args():
     ap.add_argument("--config", default="3b", choices=sorted(inputs.SHAPES))
     ap.add_argument("--T", type=int, default=None, help="sequence length (default: the config's)")
     ap.add_argument("--lr", type=float, default=None, help="override the SGD step (0: plain SWA forward)")
+    ap.add_argument("--window", type=int, default=None,
+                    help="override the attention window (>= T: full attention)")
+    ap.add_argument("--fast-layers", type=int, default=None,
+                    help="override the number of fast blocks (0: no test-time training, forward only)")
     ap.add_argument("--cpu-tokens", type=int, default=None,
-                    help="tokens the oracle is timed on (default: one chunk, 256 at 3B)")
+                    help="tokens the oracle is timed on (default: one chunk; 128 at 3B)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile", choices=["timed", "off"], default="timed",
@@ -148,6 +152,10 @@ def workload(args, rank=0):
         s = s.replace(seq_len=args.T)
     if args.lr is not None:
         s = s.replace(lr=args.lr)
+    if args.window is not None:
+        s = s.replace(window=args.window)
+    if args.fast_layers is not None:
+        s = s.replace(n_ttt_layers=args.fast_layers)
     tok = inputs.make_tokens(s, seed=1 + rank)
     return s, tok
 
@@ -178,7 +186,7 @@ def cpu_baseline(s, w, tok, n_tokens):
 
 
 def default_cpu_tokens(s):
-    return 256 if s.d_model >= 3072 else (s.chunk if s.d_model >= 1536 else min(s.seq_len, 4 * s.chunk))
+    return 128 if s.d_model >= 3072 else (s.chunk if s.d_model >= 1536 else min(s.seq_len, 4 * s.chunk))
 
 
 # ---------------------------------------------------------------------------
@@ -209,6 +217,18 @@ def run_reference(args):
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def job_rate(local_ms: float, world: int, tokens_per_rank: int, steps: int, dist=None, device=None):
+    """Whole-job throughput of independent replicas: every rank processed
+    `steps` sequences of `tokens_per_rank` tokens; the job took as long as
+    its slowest rank.  Returns (max_ms over ranks, tokens/s of the job)."""
+    import torch
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    if dist is not None and world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, world * tokens_per_rank * steps / (ms_max / 1e3)
 
 
 def roofline(prof, peaks, peak_src):
@@ -294,11 +314,7 @@ def run_ours(args):
     ms = ev0.elapsed_time(ev1)
     prof = m.profile_read() if args.profile == "timed" else None
     m.profile(False)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    value = world * T * args.steps / (ms_max / 1e3)
+    ms_max, value = job_rate(ms, world, T, args.steps, dist, device="cuda")
 
     # end to end through the same call with host buffers (pinned)
     e2e = None
@@ -310,10 +326,8 @@ def run_ours(args):
         for _ in range(args.steps):
             step(tok_h, loss_h)
         barrier()
-        dt = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device="cuda")
-        if dist is not None:
-            dist.all_reduce(dt, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * T * args.steps / float(dt.item()), "unit": UNIT,
+        _, e2e_value = job_rate(1e3 * (time.perf_counter() - t0), world, T, args.steps, dist, device="cuda")
+        e2e = {"value": e2e_value, "unit": UNIT,
                "h2d_bytes_per_step": int(tok_h.numel() * 4), "d2h_bytes_per_step": int(loss_h.numel() * 4)}
 
     fl = inputs.flops_per_sequence(s)

@@ -57,7 +57,9 @@ enum {
  *   n_layers L, d_model d, n_heads H, n_kv_heads Hkv (H % Hkv == 0),
  *   head_dim hd (even), d_ff, vocab V, window W (query t sees keys j with
  *   t-W < j <= t), chunk b (test-time mini-batch), n_ttt_layers (the MLPs
- *   of blocks [L-n_ttt_layers, L) are the fast weights), precision
+ *   of blocks [L-n_ttt_layers, L) are the fast weights; 0: no test-time
+ *   training, ttt_prefill only scores the chunks of a frozen model, e.g. a
+ *   full-attention Transformer with window >= T), precision
  *   (TTT_BF16 | TTT_FP32_CHECK), lr (SGD step), rope_theta, norm_eps,
  *   max_tokens (longest sequence ttt_prefill will be given; sizes the
  *   device staging of host token arrays).                                   */

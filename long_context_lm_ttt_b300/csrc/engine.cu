@@ -610,7 +610,7 @@ struct Engine : EngineBase {
   void fast_fwd(const float* x_in, const float2* cs_, int64_t s, int n, cudaStream_t st, int* rc) {
     const int L = cfg.n_layers, d = cfg.d_model, Lt = cfg.n_ttt_layers, lo = L - Lt;
     cs_cur = cs_;
-    fstash[0].x = const_cast<float*>(x_in);
+    if (Lt > 0) fstash[0].x = const_cast<float*>(x_in);
     const float* x = x_in;
     for (int l = lo; l < L; ++l) {
       float* x_out = xs[l + 1 - lo];
@@ -636,8 +636,9 @@ struct Engine : EngineBase {
 
   // streamed lm_head + cross-entropy: loss of chunk c into losses[c] and the
   // gradient w.r.t. the final normed hidden state into dhf (fp32)
+  // need_grad = false (no fast blocks): the loss only, no d hidden
   void cross_entropy(const int32_t* tok, int64_t n_tok, int64_t s, int n, int n_tgt, float* losses, int c,
-                     cudaStream_t st, int* rc) {
+                     cudaStream_t st, int* rc, bool need_grad = true) {
     const int d = cfg.d_model, V = cfg.vocab;
     row((double)n * 8, st, [&] { launch_targets(tok, n_tok, s, n, tgt, V, dev_err + 1, st); });
     for (int v0 = 0; v0 < V; v0 += Vs) {
@@ -651,6 +652,7 @@ struct Engine : EngineBase {
       e.col0 = v0;
       gemm(n, nv, d, hf, d, 0, Wlm + (int64_t)v0 * d, d, 0, e, st, rc);
       row((double)n * nv * (4 + sizeof(T)), st, [&] { launch_ce_slab_stats<T>(z_slab, Vs, n, nv, p_slab, Vs, m_run, l_run, alpha, beta, first, st); });
+      if (!need_grad) continue;
       e = epi(EPI_CE_ACC);
       e.out = dh_acc;
       e.ldo = d;
@@ -660,7 +662,9 @@ struct Engine : EngineBase {
       gemm(n, d, nv, p_slab, Vs, 0, Wlm + (int64_t)v0 * d, d, 1, e, st, rc);
     }
     const float inv = 1.0f / (float)n_tgt;
-    row((double)n * d * (8 + sizeof(T)), st, [&] { launch_ce_finalize<T>(n, m_run, l_run, ztgt, tgt, inv, dh_acc, Wlm, d, dhf, loss_row, st); });
+    row((double)n * d * (8 + sizeof(T)), st, [&] {
+      launch_ce_finalize<T>(n, m_run, l_run, ztgt, tgt, inv, need_grad ? dh_acc : nullptr, Wlm, d, dhf, loss_row, st);
+    });
     row((double)n * 4, st, [&] { launch_loss_reduce(loss_row, n, inv, losses, c, dev_err, st); });
   }
 
@@ -795,8 +799,9 @@ struct Engine : EngineBase {
           CU_TRY(cudaMemsetAsync(loss_d + c, 0, sizeof(float), st));
           continue;
         }
-        cross_entropy(tok_d, n_tok, s, n, n_tgt, loss_d, c, st, &rc);
-        backward(s, n, st, &rc);
+        // without fast blocks the chunk loop only scores the chunk
+        cross_entropy(tok_d, n_tok, s, n, n_tgt, loss_d, c, st, &rc, cfg.n_ttt_layers > 0);
+        if (cfg.n_ttt_layers > 0) backward(s, n, st, &rc);
         CU_TRY(cudaPeekAtLastError());
       }
     }
@@ -900,9 +905,9 @@ static int validate(const ttt_config* c, std::string& msg) {
     return TTT_ERR_INVALID;
   }
   if (c->n_layers < 1 || c->d_model < 2 || c->n_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 2 ||
-      c->d_ff < 2 || c->vocab < 2 || c->window < 1 || c->chunk < 1 || c->n_ttt_layers < 1 ||
+      c->d_ff < 2 || c->vocab < 2 || c->window < 1 || c->chunk < 1 || c->n_ttt_layers < 0 ||
       c->max_tokens < 1) {
-    msg = "every size must be positive (n_ttt_layers >= 1)";
+    msg = "every size must be positive (n_ttt_layers >= 0)";
     return TTT_ERR_INVALID;
   }
   if (c->n_ttt_layers > c->n_layers) {

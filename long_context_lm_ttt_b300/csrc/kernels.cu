@@ -4,6 +4,7 @@
 // statistics of the streamed cross-entropy, its finalisation, the
 // deterministic chunk-loss reduction, and weight packing.
 #include <math.h>
+#include <stdint.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -186,8 +187,9 @@ __global__ void ce_finalize_kernel(const float* m_run, const float* l_run, const
   const float l = l_run[r];
   const float il = 1.0f / l;
   const T* wy = Wlm + (int64_t)y * d;
-  for (int c = threadIdx.x; c < d; c += blockDim.x)
-    dhf[o + c] = (dh_acc[o + c] * il - to_f<T>(wy[c])) * inv_ntgt;
+  if (dh_acc)
+    for (int c = threadIdx.x; c < d; c += blockDim.x)
+      dhf[o + c] = (dh_acc[o + c] * il - to_f<T>(wy[c])) * inv_ntgt;
   if (threadIdx.x == 0) loss_row[r] = m_run[r] + logf(l) - ztgt[r];
 }
 
@@ -243,6 +245,148 @@ __global__ void split_bf16_kernel(const float* __restrict__ w, int64_t n, bf16* 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Vectorised row kernels for the bf16 path: 16-byte loads, the row held in
+// registers (one read of each input), VPT float4 per thread.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint2 pack4_bf16(float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  return make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(256) rmsnorm_fwd_vec_kernel(const float* __restrict__ x, const float* __restrict__ g,
+                                                              int d, float eps, bf16* __restrict__ out,
+                                                              float* __restrict__ rr) {
+  __shared__ float sh[32];
+  const int r = blockIdx.x;
+  const float4* xr = reinterpret_cast<const float4*>(x + (int64_t)r * d);
+  const float4* gr = reinterpret_cast<const float4*>(g);
+  const int nq = d >> 2;
+  float4 v[VPT];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int q = threadIdx.x + 256 * i;
+    v[i] = q < nq ? xr[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+    s = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, fmaf(v[i].w, v[i].w, s))));
+  }
+  s = block_reduce(s, AddOp(), sh);
+  const float rinv = 1.0f / sqrtf(s / (float)d + eps);
+  uint2* o = reinterpret_cast<uint2*>(out + (int64_t)r * d);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int q = threadIdx.x + 256 * i;
+    if (q < nq) {
+      const float4 gg = gr[q];
+      o[q] = pack4_bf16(make_float4(gg.x * v[i].x * rinv, gg.y * v[i].y * rinv, gg.z * v[i].z * rinv,
+                                    gg.w * v[i].w * rinv));
+    }
+  }
+  if (threadIdx.x == 0) rr[r] = rinv;
+}
+
+// out = resid + r (g dy) - r^3 x mean(x g dy); out_t = bf16(out)
+template <int VPT>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_vec_kernel(const float* __restrict__ x, const float* __restrict__ g,
+                                                              const float* __restrict__ rr, const float* __restrict__ dy,
+                                                              const float* __restrict__ resid, int d,
+                                                              float* __restrict__ out, bf16* __restrict__ out_t) {
+  __shared__ float sh[32];
+  const int r = blockIdx.x;
+  const int64_t o = (int64_t)r * d;
+  const float4* xr = reinterpret_cast<const float4*>(x + o);
+  const float4* dr = reinterpret_cast<const float4*>(dy + o);
+  const float4* gr = reinterpret_cast<const float4*>(g);
+  const int nq = d >> 2;
+  float4 xv[VPT], gd[VPT];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int q = threadIdx.x + 256 * i;
+    if (q < nq) {
+      xv[i] = xr[q];
+      const float4 gg = gr[q], dd = dr[q];
+      gd[i] = make_float4(gg.x * dd.x, gg.y * dd.y, gg.z * dd.z, gg.w * dd.w);
+    } else {
+      xv[i] = gd[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    s = fmaf(xv[i].x, gd[i].x, fmaf(xv[i].y, gd[i].y, fmaf(xv[i].z, gd[i].z, fmaf(xv[i].w, gd[i].w, s))));
+  }
+  s = block_reduce(s, AddOp(), sh) / (float)d;
+  const float ri = rr[r];
+  const float c3 = ri * ri * ri * s;
+  float4* outr = reinterpret_cast<float4*>(out + o);
+  const float4* rs = reinterpret_cast<const float4*>(resid ? resid + o : nullptr);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int q = threadIdx.x + 256 * i;
+    if (q < nq) {
+      float4 v = make_float4(ri * gd[i].x - c3 * xv[i].x, ri * gd[i].y - c3 * xv[i].y, ri * gd[i].z - c3 * xv[i].z,
+                             ri * gd[i].w - c3 * xv[i].w);
+      if (rs) {
+        const float4 t = rs[q];
+        v.x += t.x;
+        v.y += t.y;
+        v.z += t.z;
+        v.w += t.w;
+      }
+      outr[q] = v;
+      if (out_t) reinterpret_cast<uint2*>(out_t + o)[q] = pack4_bf16(v);
+    }
+  }
+}
+
+// Streamed softmax statistics of one vocabulary slab: max, sum of exp, and
+// P = exp(z - max) in bf16.  1024 threads per row, float4 loads; the second
+// pass re-reads the slab, which is resident in L2.
+__global__ void __launch_bounds__(1024) ce_slab_stats_vec_kernel(const float* __restrict__ z, int64_t ldz, int nv,
+                                                                 bf16* __restrict__ p, int64_t ldp, float* m_run,
+                                                                 float* l_run, float* alpha, float* beta, int first) {
+  __shared__ float sh[32];
+  const int r = blockIdx.x;
+  const float4* zr = reinterpret_cast<const float4*>(z + (int64_t)r * ldz);
+  uint2* pr = reinterpret_cast<uint2*>(p + (int64_t)r * ldp);
+  const int nq = nv >> 2;
+  float m = -INFINITY;
+  for (int q = threadIdx.x; q < nq; q += blockDim.x) {
+    const float4 v = zr[q];
+    m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+  }
+  m = block_reduce(m, MaxOp(), sh);
+  const float L2E = 1.4426950408889634f;
+  const float nm = -m * L2E;
+  float l = 0.f;
+  for (int q = threadIdx.x; q < nq; q += blockDim.x) {
+    const float4 v = zr[q];
+    // exp(z - m) = 2^(z log2(e) - m log2(e))
+    float4 e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.x) : "f"(fmaf(v.x, L2E, nm)));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(fmaf(v.y, L2E, nm)));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.z) : "f"(fmaf(v.z, L2E, nm)));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.w) : "f"(fmaf(v.w, L2E, nm)));
+    l += (e.x + e.y) + (e.z + e.w);
+    pr[q] = pack4_bf16(e);
+  }
+  l = block_reduce(l, AddOp(), sh);
+  if (threadIdx.x == 0) {
+    if (first) {
+      m_run[r] = m;
+      l_run[r] = l;
+      alpha[r] = 0.f;
+      beta[r] = 1.f;
+    } else {
+      const float mo = m_run[r];
+      const float mn = fmaxf(mo, m);
+      const float a = expf(mo - mn), b = expf(m - mn);
+      l_run[r] = l_run[r] * a + l * b;
+      m_run[r] = mn;
+      alpha[r] = a;
+      beta[r] = b;
+    }
+  }
+}
+
 inline int grid_for(int64_t total, int threads) {
   int64_t g = (total + threads - 1) / threads;
   return (int)(g > 148 * 32 ? 148 * 32 : (g < 1 ? 1 : g));
@@ -255,15 +399,39 @@ void launch_embed(const int32_t* tok, int n, const T* E, int d, float* x, int V,
                   cudaStream_t st) {
   if (n > 0) embed_kernel<T><<<n, RB, 0, st>>>(tok, d, E, x, V, err_tok);
 }
+static inline bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
 template <typename T>
 void launch_rmsnorm_fwd(const float* x, const float* g, int n, int d, float eps, T* out, float* r,
                         cudaStream_t st) {
-  if (n > 0) rmsnorm_fwd_kernel<T><<<n, RB, 0, st>>>(x, g, d, eps, out, r);
+  if (n <= 0) return;
+  if constexpr (sizeof(T) == 2) {
+    if (d % 4 == 0 && d <= 4 * 256 * 4 && al16(x) && al16(g) && ((uintptr_t)out & 7) == 0) {
+      const int vpt = (d / 4 + 255) / 256;
+      if (vpt <= 1) rmsnorm_fwd_vec_kernel<1><<<n, 256, 0, st>>>(x, g, d, eps, (bf16*)out, r);
+      else if (vpt <= 2) rmsnorm_fwd_vec_kernel<2><<<n, 256, 0, st>>>(x, g, d, eps, (bf16*)out, r);
+      else if (vpt <= 3) rmsnorm_fwd_vec_kernel<3><<<n, 256, 0, st>>>(x, g, d, eps, (bf16*)out, r);
+      else rmsnorm_fwd_vec_kernel<4><<<n, 256, 0, st>>>(x, g, d, eps, (bf16*)out, r);
+      return;
+    }
+  }
+  rmsnorm_fwd_kernel<T><<<n, RB, 0, st>>>(x, g, d, eps, out, r);
 }
 template <typename T>
 void launch_rmsnorm_bwd(const float* x, const float* g, const float* r, const float* dy,
                         const float* resid, int n, int d, float* out, T* out_t, cudaStream_t st) {
-  if (n > 0) rmsnorm_bwd_kernel<T><<<n, RB, 0, st>>>(x, g, r, dy, resid, d, out, out_t);
+  if (n <= 0) return;
+  if constexpr (sizeof(T) == 2) {
+    if (d % 4 == 0 && d <= 3 * 256 * 4 && al16(x) && al16(g) && al16(dy) && al16(out) &&
+        (!resid || al16(resid)) && ((uintptr_t)out_t & 7) == 0) {
+      const int vpt = (d / 4 + 255) / 256;
+      if (vpt <= 1) rmsnorm_bwd_vec_kernel<1><<<n, 256, 0, st>>>(x, g, r, dy, resid, d, out, (bf16*)out_t);
+      else if (vpt <= 2) rmsnorm_bwd_vec_kernel<2><<<n, 256, 0, st>>>(x, g, r, dy, resid, d, out, (bf16*)out_t);
+      else rmsnorm_bwd_vec_kernel<3><<<n, 256, 0, st>>>(x, g, r, dy, resid, d, out, (bf16*)out_t);
+      return;
+    }
+  }
+  rmsnorm_bwd_kernel<T><<<n, RB, 0, st>>>(x, g, r, dy, resid, d, out, out_t);
 }
 void launch_rope_table(int64_t pos0, int n, int hd, float theta, float2* cs, cudaStream_t st) {
   const int total = n * (hd / 2);
@@ -281,7 +449,14 @@ void launch_targets(const int32_t* tok, int64_t T, int64_t pos0, int n, int32_t*
 template <typename T>
 void launch_ce_slab_stats(const float* z, int64_t ldz, int n, int nv, T* p, int64_t ldp, float* m_run,
                           float* l_run, float* alpha, float* beta, int first, cudaStream_t st) {
-  if (n > 0) ce_slab_stats_kernel<T><<<n, RB, 0, st>>>(z, ldz, nv, p, ldp, m_run, l_run, alpha, beta, first);
+  if (n <= 0) return;
+  if constexpr (sizeof(T) == 2) {
+    if (nv % 4 == 0 && ldz % 4 == 0 && ldp % 4 == 0 && al16(z) && ((uintptr_t)p & 7) == 0) {
+      ce_slab_stats_vec_kernel<<<n, 1024, 0, st>>>(z, ldz, nv, (bf16*)p, ldp, m_run, l_run, alpha, beta, first);
+      return;
+    }
+  }
+  ce_slab_stats_kernel<T><<<n, RB, 0, st>>>(z, ldz, nv, p, ldp, m_run, l_run, alpha, beta, first);
 }
 template <typename T>
 void launch_ce_finalize(int n, const float* m_run, const float* l_run, const float* ztgt,

@@ -223,6 +223,8 @@ def flops_per_sequence(s: ModelShape, T: Optional[int] = None) -> Dict[str, floa
         tt = np.arange(n, dtype=np.float64)
         P_local += float(np.minimum(tt + 1, W).sum())
     fwd = 2.0 * (n_attn + n_mlp) * L * T + 2.0 * d * V * T + 4.0 * L * H * hd * P
+    if Lt == 0:  # no fast blocks: the chunks are only scored
+        return {"fwd": fwd, "bwd": 0.0, "total": fwd}
     bwd = (2.0 * d * V * T                                    # d hidden from lm_head
            + 2.0 * Lt * n_mlp * T                             # MLP weight grads
            + 2.0 * (Lt - 1) * (n_mlp + n_attn) * T            # dX through upper fast blocks

@@ -55,6 +55,7 @@ def _cfg(**kw):
     (dict(precision=7), T.TTT_ERR_INVALID),
     (dict(n_layers=0), T.TTT_ERR_INVALID),
     (dict(n_ttt_layers=3), T.TTT_ERR_INVALID),
+    (dict(n_ttt_layers=-1), T.TTT_ERR_INVALID),
     (dict(n_kv_heads=3), T.TTT_ERR_SHAPE),
     (dict(head_dim=31), T.TTT_ERR_SHAPE),
     (dict(lr=float("nan")), T.TTT_ERR_NONFINITE),

@@ -378,3 +378,18 @@ def test_oracle_regression_lock():
     for name, ref in g["losses"].items():
         s, cfg, w, tok = _setup(name)
         np.testing.assert_allclose(O.prefill(cfg, w, tok)["losses"], ref, rtol=1e-12)
+
+
+def test_no_fast_blocks_is_a_frozen_model():
+    """n_ttt_layers = 0: nothing is trained at test time, so the chunk losses
+    are the chunk means of one un-chunked forward, for any lr."""
+    s = inputs.shape("tiny-ttt2", n_ttt_layers=0, lr=0.5)
+    w = inputs.make_weights(s)
+    tok = inputs.make_tokens(s)
+    cfg = O.OracleConfig.from_mapping(s.as_dict())
+    r = O.prefill(cfg, w, tok)
+    full = O.full_forward_losses(cfg, w, tok)
+    b, T = s.chunk, len(tok)
+    ref = np.array([full[c * b:min(T - 1, (c + 1) * b)].mean() for c in range(-(-T // b))])
+    np.testing.assert_allclose(r["losses"], ref, rtol=1e-12, atol=1e-12)
+    assert r["fast"] == []

@@ -163,3 +163,21 @@ def test_bf16_parity_tc_attention_small():
     s = inputs.shape("tiny-gqa", n_heads=4, n_kv_heads=2, head_dim=64, d_model=256, d_ff=512, chunk=128,
                      window=200, seq_len=700, bf16=True)
     compare(s, inputs.make_weights(s), inputs.make_tokens(s, 700), "bf16")
+
+
+
+@pytest.mark.parametrize("precision", ["fp32", "bf16"])
+def test_full_attention_without_test_time_training(precision):
+    """n_ttt_layers = 0 with a window covering the whole sequence: a plain
+    full-attention Transformer scoring its chunks (the baseline the pages
+    compare against), against the un-chunked oracle forward."""
+    s = inputs.shape("tiny-gqa", n_ttt_layers=0, window=4096, seq_len=200, bf16=precision == "bf16")
+    w = inputs.make_weights(s)
+    tok = inputs.make_tokens(s)
+    g, fast = run_gpu(s, w, tok, precision)
+    assert fast == []
+    cfg = O.OracleConfig.from_mapping(s.as_dict())
+    full = O.full_forward_losses(cfg, w, tok)
+    b, T = s.chunk, len(tok)
+    ref = np.array([full[c * b:min(T - 1, (c + 1) * b)].mean() for c in range(-(-T // b))])
+    np.testing.assert_allclose(g, ref, rtol=TOL[precision])
