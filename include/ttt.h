@@ -112,7 +112,9 @@ int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* stream, ttt_ct
  * `stream`.  A NaN/Inf chunk loss returns NONFINITE with the first such
  * chunk index in ttt_last_error(); the context is then left as is.  After
  * success the context holds the final fast weights and the ring at
- * position T. */
+ * position T.  Internally the call forks two streams from `stream`: one
+ * runs the frozen blocks' bulk pass a super-chunk ahead, the other the
+ * chunk loop; both join back into `stream` before the call returns. */
 int ttt_prefill(ttt_ctx* ctx, const int32_t* tokens, int64_t T, float* chunk_losses,
                 void* stream);
 
@@ -152,9 +154,11 @@ int ttt_reset(ttt_ctx* ctx);
  *   "attn_fwd_bulk" their sliding-window attention forward
  * `flops` counts 2 per multiply-add of the operation as defined (attention:
  * unmasked query/key pairs only; no recomputation, no padding), `bytes`
- * the operands read once and results written once.  The events add a few
- * microseconds per launch on the host; device time is unaffected apart
- * from the gaps they leave between kernels. */
+ * the operands read once and results written once.  While profiling is
+ * on, ttt_prefill runs its bulk pass and chunk loop on the call's stream
+ * alone (no overlap), so that each event pair times one kernel by itself.
+ * The events add a few microseconds per launch on the host; device time is
+ * unaffected apart from the gaps they leave between kernels. */
 typedef struct ttt_kernel_stat {
   char name[24];
   int64_t launches;

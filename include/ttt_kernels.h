@@ -94,6 +94,14 @@ int ttt_kernel_attn_bwd_noalloc(int32_t n, int32_t H, int32_t Hkv, int32_t hd, i
                                 const float* lse, int32_t ld_lse, const void* dout, float* dsum, void* dqkv,
                                 void* stream);
 
+/* Self-test of the bounded device-side waits every tensor-core kernel uses:
+ * launches one CTA whose thread waits on an mbarrier that nothing
+ * completes, with a budget of `clocks` SM clocks (1 .. 2e9).  The wait
+ * gives up, records its code in the kernel error word and the kernel
+ * returns, so the context stays usable.  Returns 0 if the launch went
+ * through; read the code with ttt_kernel_error(). */
+int ttt_kernel_wait_selftest(int64_t clocks, void* stream);
+
 /* Error word of the tensor-core kernels launched through this header since
  * the last call (0 = none; otherwise the code of a bounded wait that gave
  * up).  Synchronises the device. */

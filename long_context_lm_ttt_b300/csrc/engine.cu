@@ -178,6 +178,13 @@ template <typename T>
 struct Engine : EngineBase {
   static constexpr bool kBF16 = sizeof(T) == 2;
   DeviceArena mem;
+  ~Engine() override {
+    cudaDeviceSynchronize();
+    for (cudaEvent_t e : {ev_fork, ev_a[0], ev_a[1], ev_b[0], ev_b[1], ev_join_a, ev_join_b})
+      if (e) cudaEventDestroy(e);
+    if (sa) cudaStreamDestroy(sa);
+    if (sb) cudaStreamDestroy(sb);
+  }
 
   struct Layer {
     float *g_attn = nullptr, *g_mlp = nullptr;
@@ -207,8 +214,17 @@ struct Engine : EngineBase {
   Stash sstash;               // static blocks, one chunk (ttt_logits)
   Stash bstash;               // static blocks, one super-chunk (ttt_prefill)
   float* bx[2] = {nullptr, nullptr};  // residual stream of the bulk pass
-  float* x_lo = nullptr;      // input of the first fast block, S rows
-  float2* cs_bulk = nullptr;  // RoPE table of the super-chunk
+  // Double-buffered by super-chunk parity: the bulk pass over super-chunk
+  // k+1 (low-priority stream sa) runs while the chunk loop consumes
+  // super-chunk k (high-priority stream sb).
+  float* x_lo_buf[2] = {nullptr, nullptr};      // input of the first fast block, S rows
+  float2* cs_bulk_buf[2] = {nullptr, nullptr};  // RoPE table of the super-chunk
+  float* x_lo = nullptr;                        // buffers of the span being processed
+  float2* cs_bulk = nullptr;
+  cudaStream_t sa = nullptr, sb = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_a[2] = {nullptr, nullptr}, ev_b[2] = {nullptr, nullptr},
+              ev_join_a = nullptr, ev_join_b = nullptr;
+  int grid_cap = 0;  // CTA cap of tensor-core GEMMs (0: one per SM, persistent)
   const float2* cs_cur = nullptr;  // RoPE table of the chunk being processed
   T *E = nullptr, *Wlm = nullptr;
   float* g_final = nullptr;
@@ -375,8 +391,20 @@ struct Engine : EngineBase {
       A_TRY(bx[0], (size_t)S_bulk * d);
       A_TRY(bx[1], (size_t)S_bulk * d);
     }
-    A_TRY(x_lo, (size_t)S_bulk * d);
-    A_TRY(cs_bulk, (size_t)S_bulk * (hd / 2));
+    for (int k = 0; k < 2; ++k) {
+      A_TRY(x_lo_buf[k], (size_t)S_bulk * d);
+      A_TRY(cs_bulk_buf[k], (size_t)S_bulk * (hd / 2));
+    }
+    x_lo = x_lo_buf[0];
+    cs_bulk = cs_bulk_buf[0];
+    {
+      int lo_pri = 0, hi_pri = 0;
+      CU_TRY(cudaDeviceGetStreamPriorityRange(&lo_pri, &hi_pri));
+      CU_TRY(cudaStreamCreateWithPriority(&sa, cudaStreamNonBlocking, lo_pri));
+      CU_TRY(cudaStreamCreateWithPriority(&sb, cudaStreamNonBlocking, hi_pri));
+      for (cudaEvent_t* e : {&ev_fork, &ev_a[0], &ev_a[1], &ev_b[0], &ev_b[1], &ev_join_a, &ev_join_b})
+        CU_TRY(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+    }
     fstash.resize(Lt);
     xs.resize(Lt + 1);
     for (int i = 0; i <= Lt; ++i) A_TRY(xs[i], (size_t)b * d);
@@ -428,7 +456,10 @@ struct Engine : EngineBase {
   // -------------------------------------------------------------------------
   void gemm(int M, int N, int K, const T* A_, int64_t lda, int a_mn, const T* B_, int64_t ldb,
             int b_mn, const Epi& e, cudaStream_t st, int* rc, const T* B2 = nullptr) {
-    GemmArgs<T> g{M, N, K, A_, lda, a_mn, B_, ldb, b_mn, e, B2, gemm_ws, gemm_ws_elems};
+    // the split-K scratch belongs to the chunk loop; the bulk pass (grid_cap
+    // set, other stream) never splits
+    GemmArgs<T> g{M, N, K, A_, lda, a_mn, B_, ldb, b_mn, e, B2, grid_cap ? nullptr : gemm_ws,
+                  grid_cap ? 0 : gemm_ws_elems, grid_cap};
     int cls = P_GEMM_FWD;
     double out_b = (double)M * N * (e.kind == EPI_STORE && !e.out_f32 ? sizeof(T) : 4);
     switch (e.kind) {
@@ -592,16 +623,23 @@ struct Engine : EngineBase {
   // static blocks over a super-chunk [s0, s0+n): embedding, blocks
   // [0, L-n_ttt_layers); leaves the input of the first fast block in x_lo
   // and the super-chunk's RoPE table in cs_bulk
-  void static_fwd(const int32_t* tok, int64_t s0, int n, cudaStream_t st, int* rc) {
+  // (buffers x_lo_buf[buf], cs_bulk_buf[buf]).  Its GEMMs launch one CTA per
+  // tile instead of one persistent CTA per SM, so that SMs free up often
+  // for the chunk loop running concurrently on the other stream.
+  void static_fwd(const int32_t* tok, int64_t s0, int n, int buf, cudaStream_t st, int* rc) {
     const int d = cfg.d_model, hd = cfg.head_dim, lo = cfg.n_layers - cfg.n_ttt_layers;
-    row((double)n * hd * 4, st, [&] { launch_rope_table(s0, n, hd, cfg.rope_theta, cs_bulk, st); });
-    float* x = lo == 0 ? x_lo : bx[0];
+    float2* cs_ = cs_bulk_buf[buf];
+    float* xl = x_lo_buf[buf];
+    row((double)n * hd * 4, st, [&] { launch_rope_table(s0, n, hd, cfg.rope_theta, cs_, st); });
+    float* x = lo == 0 ? xl : bx[0];
     row((double)n * d * (4 + sizeof(T)), st, [&] { launch_embed<T>(tok, n, E, d, x, cfg.vocab, dev_err + 1, st); });
+    grid_cap = INT_MAX;
     for (int l = 0; l < lo; ++l) {
-      float* x_out = l + 1 == lo ? x_lo : bx[(l + 1) & 1];
-      block_fwd(l, bstash, x, x_out, cs_bulk, s0, n, st, rc);
+      float* x_out = l + 1 == lo ? xl : bx[(l + 1) & 1];
+      block_fwd(l, bstash, x, x_out, cs_, s0, n, st, rc);
       x = x_out;
     }
+    grid_cap = 0;
   }
 
   // fast blocks of positions [s, s+n) from x_in (the output of the static
@@ -787,25 +825,56 @@ struct Engine : EngineBase {
     if (rc) return rc;
     used = true;
     const int d = cfg.d_model, hd = cfg.head_dim;
-    for (int64_t s0 = 0; s0 < n_tok && rc == TTT_OK; s0 += S_bulk) {
+    // Two internal streams fork from `st`: s_bulk runs the bulk pass of the
+    // frozen blocks one super-chunk ahead, s_loop the chunk loop.  Events order
+    // the hand-offs: the chunk loop of super-chunk k waits for its bulk pass
+    // (ev_a); the bulk pass of super-chunk k+2 reuses buffer k & 1 and waits
+    // for the chunk loop of k (ev_b).  Both join back into `st`.  With
+    // profiling on, both roles run on `st` itself, in the same order.
+    cudaStream_t s_bulk = prof_on ? st : sa, s_loop = prof_on ? st : sb;
+    CU_TRY(cudaEventRecord(ev_fork, st));
+    CU_TRY(cudaStreamWaitEvent(s_bulk, ev_fork, 0));
+    CU_TRY(cudaStreamWaitEvent(s_loop, ev_fork, 0));
+    const int nS = (int)((n_tok + S_bulk - 1) / S_bulk);
+    auto bulk = [&](int k) {
+      const int64_t s0 = (int64_t)k * S_bulk;
       const int sn = (int)std::min<int64_t>(S_bulk, n_tok - s0);
-      static_fwd(tok_d + s0, s0, sn, st, &rc);
+      if (k >= 2) cudaStreamWaitEvent(s_bulk, ev_b[k & 1], 0);
+      static_fwd(tok_d + s0, s0, sn, k & 1, s_bulk, &rc);
+      cudaEventRecord(ev_a[k & 1], s_bulk);
+    };
+    bulk(0);
+    for (int k = 0; k < nS && rc == TTT_OK; ++k) {
+      if (k + 1 < nS) bulk(k + 1);
+      const int64_t s0 = (int64_t)k * S_bulk;
+      const int sn = (int)std::min<int64_t>(S_bulk, n_tok - s0);
+      CU_TRY(cudaStreamWaitEvent(s_loop, ev_a[k & 1], 0));
+      x_lo = x_lo_buf[k & 1];
+      cs_bulk = cs_bulk_buf[k & 1];
       for (int64_t s = s0; s < s0 + sn && rc == TTT_OK; s += b) {
         const int c = (int)(s / b);
         const int n = (int)std::min<int64_t>(b, n_tok - s);
         const int n_tgt = (int)std::min<int64_t>(n, n_tok - 1 - s);
-        fast_fwd(x_lo + (s - s0) * d, cs_bulk + (s - s0) * (hd / 2), s, n, st, &rc);
+        fast_fwd(x_lo + (s - s0) * d, cs_bulk + (s - s0) * (hd / 2), s, n, s_loop, &rc);
         if (n_tgt <= 0) {
-          CU_TRY(cudaMemsetAsync(loss_d + c, 0, sizeof(float), st));
+          CU_TRY(cudaMemsetAsync(loss_d + c, 0, sizeof(float), s_loop));
           continue;
         }
         // without fast blocks the chunk loop only scores the chunk
-        cross_entropy(tok_d, n_tok, s, n, n_tgt, loss_d, c, st, &rc, cfg.n_ttt_layers > 0);
-        if (cfg.n_ttt_layers > 0) backward(s, n, st, &rc);
+        cross_entropy(tok_d, n_tok, s, n, n_tgt, loss_d, c, s_loop, &rc, cfg.n_ttt_layers > 0);
+        if (cfg.n_ttt_layers > 0) backward(s, n, s_loop, &rc);
         CU_TRY(cudaPeekAtLastError());
       }
+      CU_TRY(cudaEventRecord(ev_b[k & 1], s_loop));
     }
-    if (rc) return rc;
+    CU_TRY(cudaEventRecord(ev_join_a, s_bulk));
+    CU_TRY(cudaEventRecord(ev_join_b, s_loop));
+    CU_TRY(cudaStreamWaitEvent(st, ev_join_a, 0));
+    CU_TRY(cudaStreamWaitEvent(st, ev_join_b, 0));
+    if (rc) {
+      cudaStreamSynchronize(st);
+      return rc;
+    }
     pos = n_tok;
     if (host_out)
       CU_TRY(cudaMemcpyAsync(losses, loss_d, sizeof(float) * nC, cudaMemcpyDeviceToHost, st));

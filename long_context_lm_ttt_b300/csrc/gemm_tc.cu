@@ -52,6 +52,21 @@ struct Cfg {
 
 enum : int { ERR_WAIT_PRODUCER = 101, ERR_WAIT_MMA = 102, ERR_WAIT_EPI = 103, ERR_WAIT_DRAIN = 104 };
 
+// Tile t -> (row tile, column tile) in groups of GROUP_M row tiles: inside a
+// group the row index runs fastest, then the column index.  The tiles in
+// flight at once (one per SM) then share GROUP_M row strips of A and a few
+// column strips of B, which stay in L2, instead of streaming all of A once
+// per column tile.
+constexpr int GROUP_M = 16;
+__device__ __forceinline__ void tile_mn(int t, int num_m, int num_n, int* mt, int* nt) {
+  const int per_group = GROUP_M * num_n;
+  const int g = t / per_group, r = t % per_group;
+  const int first = g * GROUP_M;
+  const int gm = min(num_m - first, GROUP_M);
+  *mt = first + r % gm;
+  *nt = r / gm;
+}
+
 template <int BN, int A_MN, int B_MN, int SRC = 0>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
@@ -125,7 +140,9 @@ __global__ void __launch_bounds__(192, 1)
       int lu = 0;  // this CTA's unit counter
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++lu) {
         const int t = u % ntiles, sp = u / ntiles;
-        const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
+        int mt_, nt_;
+        tile_mn(t, num_m, num_n, &mt_, &nt_);
+        const int m0 = mt_ * BM, n0 = nt_ * BN;
         if (SRC) {
           const int sb = lu & 1;
           if (!tc::mbar_wait(src_empty0 + 8 * sb, ((lu >> 1) & 1) ^ 1, err, ERR_WAIT_PRODUCER, abort)) {
@@ -253,7 +270,9 @@ __global__ void __launch_bounds__(192, 1)
     int lu = 0;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++lu) {
       const int t = u % ntiles, sp = u / ntiles;
-      const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
+      int mt_, nt_;
+        tile_mn(t, num_m, num_n, &mt_, &nt_);
+        const int m0 = mt_ * BM, n0 = nt_ * BN;
       const int row = m0 + trow;
       const int nch = min(BN, N - n0 + 31) / 32;  // chunks with columns < N
       auto vec_chunk = [&](int c) { return e.vec && n0 + 32 * c + 32 <= N; };
@@ -429,7 +448,8 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
   }
   const int ntiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const int nunits = ntiles * splits;
-  const int grid = nunits < num_sms ? nunits : num_sms;
+  const int cap = g.grid_cap > 0 ? g.grid_cap : num_sms;
+  const int grid = nunits < cap ? nunits : cap;
   gemm_tc_kernel<BN, A_MN, B_MN, SRC><<<grid, 192, C::SMEM, st>>>(ma, mb, mb2, ms, g.B2 ? 1 : 0, g.M, g.N, g.K,
                                                                    g.e, err, splits, g.ws);
   if (splits > 1) {

@@ -164,6 +164,39 @@ extern "C" int ttt_kernel_attn_bwd(int32_t impl, int32_t n, int32_t H, int32_t H
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
 }
 
+namespace {
+// one thread waits on an mbarrier expecting one arrival that never comes
+__global__ void wait_selftest_kernel(long long budget, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(&bar);
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(a) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a)
+        : "memory");
+    if (ok) return;
+    if (clock64() - t0 > budget) {
+      atomicCAS(err, 0, 199);
+      return;
+    }
+  }
+}
+}  // namespace
+
+extern "C" int ttt_kernel_wait_selftest(int64_t clocks, void* stream) {
+  if (clocks < 1 || clocks > 2000000000LL) return TTT_ERR_INVALID;
+  if (ensure_err()) return TTT_ERR_OOM;
+  wait_selftest_kernel<<<1, 1, 0, (cudaStream_t)stream>>>((long long)clocks, g_err);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
+}
+
 extern "C" int ttt_kernel_error(void) {
   if (ensure_err()) return TTT_ERR_OOM;
   if (cudaDeviceSynchronize() != cudaSuccess) return TTT_ERR_CUDA;

@@ -22,6 +22,9 @@ struct GemmArgs {
   // (partial sums here, then a fixed-order reduction applies the epilogue)
   float* ws = nullptr;
   int64_t ws_elems = 0;
+  // tensor-core GEMM CTAs: 0 = one persistent CTA per SM; otherwise at most
+  // this many (a large value gives one CTA per tile)
+  int grid_cap = 0;
 };
 
 // SIMT fp32-accumulate GEMM (check mode; reference for the tensor-core one)

@@ -98,6 +98,8 @@ def load(path: str = LIB_PATH):
                                         c_void_p, c_void_p, c_void_p, i32, c_void_p, c_void_p, c_void_p,
                                         c_void_p]
     lib.ttt_kernel_attn_bwd.restype = c_int32
+    lib.ttt_kernel_wait_selftest.argtypes = [c_int64, c_void_p]
+    lib.ttt_kernel_wait_selftest.restype = c_int32
     lib.ttt_kernel_error.argtypes = []
     lib.ttt_kernel_error.restype = c_int32
     _lib = lib
