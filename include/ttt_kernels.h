@@ -25,7 +25,9 @@ extern "C" {
  *   B(n, k) = b_mn ? B[k*ldb + n] : B[n*ldb + k]   (B2 alike)
  * C is fp32 row-major with row pitch ldc (N and ldc even).
  *   impl 0: tcgen05 tensor cores, A/B/B2 bf16 (lda, ldb multiples of 8,
- *           16-byte aligned bases);
+ *           16-byte aligned bases), tile shape chosen by the planner;
+ *   impl 3: as 0 with 128-row tiles on single CTAs;
+ *   impl 4: as 0 with 256-row tiles on CTA pairs (cta_group::2);
  *   impl 1: SIMT, A/B/B2 bf16;   impl 2: SIMT, A/B/B2 fp32.
  * Accumulation is fp32 in every case. */
 int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn,
@@ -38,7 +40,8 @@ int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda,
  *   w16[m, n]  = rn_bf16(w32[m, n]);  w16lo[m, n] = rn_bf16(w32 - w16)
  * A(m, k), B(n, k) as in ttt_kernel_gemm (bf16); w32 fp32 and w16 / w16lo
  * bf16, all [M, N] row-major with row pitch ldw (w16 / w16lo may be NULL).
- * impl 0: tcgen05 tensor cores; impl 1: SIMT. */
+ * impl 0: tcgen05 tensor cores; impl 2: tensor cores on single CTAs;
+ * impl 3: tensor cores on CTA pairs (cta_group::2); impl 1: SIMT. */
 int ttt_kernel_gemm_sgd(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn, const void* B,
                         int64_t ldb, int32_t b_mn, float* w32, void* w16, void* w16lo, int64_t ldw, float lr,
                         int32_t impl, void* stream);

@@ -38,16 +38,30 @@ constexpr int A_BYTES = BM * BK * 2;
 // SRC = 1: the epilogue's fp32 source tile (the master weights of the SGD
 // epilogue) is brought into shared memory by TMA at the start of each tile,
 // double-buffered, so its load overlaps the tile's main loop.
-template <int BN, int SRC = 0>
+//
+// PAIR = 1: a cluster of two CTAs (on the two SMs of a TPC) computes a
+// 256 x BN tile with tcgen05 MMAs of M = 256 (cta_group::2).  CTA r of the
+// pair holds rows [128 r, 128 r + 128) of the A tile and columns
+// [r BN/2, (r + 1) BN/2) of the B tile, and its TMEM receives rows
+// [128 r, 128 r + 128) of the accumulator.  Each SM thus loads half of the
+// B tile of a one-CTA 128 x BN tile, so a stage is smaller and the ring
+// deeper in the same shared memory.
+constexpr int kSmemMax = 232448;  // per-CTA opt-in limit
+template <int BN, int SRC = 0, int PAIR = 0>
 struct Cfg {
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int BNL = PAIR ? BN / 2 : BN;  // B rows this CTA loads
+  static constexpr int TM = PAIR ? 2 * BM : BM;   // rows of a work tile
+  static constexpr int B_BYTES = BNL * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = SRC ? 3 : (BN == 256 ? 4 : 6);
+  static constexpr int SRC_BYTES = SRC ? BM * BN * 4 : 0;  // one fp32 tile
+  static constexpr int PAIR_STAGES = (kSmemMax - 2048 - 2 * SRC_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = !PAIR ? (SRC ? 3 : (BN == 256 ? 4 : 6)) : (PAIR_STAGES > 8 ? 8 : PAIR_STAGES);
   static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
   static constexpr int SRC_OFF = STAGES * STAGE_BYTES;
-  static constexpr int SRC_BYTES = SRC ? BM * BN * 4 : 0;  // one fp32 tile
   static constexpr int BAR_OFF = SRC_OFF + 2 * SRC_BYTES;
   static constexpr int SMEM = 1024 /*align slack*/ + BAR_OFF + 256;
+  static_assert(SMEM <= kSmemMax, "shared memory");
+  static_assert(8 * (2 * STAGES + 9) + 8 <= 256, "barrier area");
 };
 
 enum : int { ERR_WAIT_PRODUCER = 101, ERR_WAIT_MMA = 102, ERR_WAIT_EPI = 103, ERR_WAIT_DRAIN = 104 };
@@ -67,12 +81,12 @@ __device__ __forceinline__ void tile_mn(int t, int num_m, int num_n, int* mt, in
   *nt = r / gm;
 }
 
-template <int BN, int A_MN, int B_MN, int SRC = 0>
+template <int BN, int A_MN, int B_MN, int SRC = 0, int PAIR = 0>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapB2, const __grid_constant__ CUtensorMap mapS, int dual,
                    int M, int N, int K, Epi e, int* err, int splits, float* ws) {
-  using C = Cfg<BN, SRC>;
+  using C = Cfg<BN, SRC, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = tc::smem_u32(smem);
@@ -89,7 +103,11 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+  // work units go to CTAs, or with PAIR to CTA pairs (clusters of two)
+  const int rank = PAIR ? (int)tc::cluster_rank() : 0;
+  const int unit0 = PAIR ? (int)tc::cluster_id() : (int)blockIdx.x;
+  const int ustride = PAIR ? (int)tc::cluster_count() : (int)gridDim.x;
+  const int num_m = (M + C::TM - 1) / C::TM, num_n = (N + BN - 1) / BN;
   const int ntiles = num_m * num_n;
   const int nk = (K + BK - 1) / BK;
   const int nk_total = dual ? 2 * nk : nk;  // dual: A B^T then A B2^T into one accumulator
@@ -104,7 +122,8 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull0 + 8 * a, 1);
-      tc::mbar_init(tempty0 + 8 * a, 128);
+      // PAIR: one arrival per epilogue warp of both CTAs, on the first CTA's
+      tc::mbar_init(tempty0 + 8 * a, PAIR ? 8 : 128);
     }
     tc::mbar_init(drain, 1);
     for (int a = 0; a < 2; ++a) {
@@ -121,11 +140,19 @@ __global__ void __launch_bounds__(192, 1)
     if (SRC) tc::prefetch_tmap(&mapS);
   }
   if (warp == 1) {
-    tc::tmem_alloc(tc::smem_u32(tmem_slot), C::TMEM_COLS);
-    tc::tmem_relinquish();
+    if (PAIR) {
+      tc::tmem_alloc_pair(tc::smem_u32(tmem_slot), C::TMEM_COLS);
+      tc::tmem_relinquish_pair();
+    } else {
+      tc::tmem_alloc(tc::smem_u32(tmem_slot), C::TMEM_COLS);
+      tc::tmem_relinquish();
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
+  // PAIR: the peer's barriers must be initialised before the first remote
+  // arrival or copy completion
+  if (PAIR) tc::cluster_sync();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -138,11 +165,12 @@ __global__ void __launch_bounds__(192, 1)
       for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
       bool ok = true;
       int lu = 0;  // this CTA's unit counter
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++lu) {
+      for (int u = unit0; u < nunits && ok; u += ustride, ++lu) {
         const int t = u % ntiles, sp = u / ntiles;
         int mt_, nt_;
         tile_mn(t, num_m, num_n, &mt_, &nt_);
-        const int m0 = mt_ * BM, n0 = nt_ * BN;
+        // this CTA's rows of the tile and the B columns it loads
+        const int m0 = mt_ * C::TM + rank * BM, n0 = nt_ * BN, nb0 = n0 + rank * C::BNL;
         if (SRC) {
           const int sb = lu & 1;
           if (!tc::mbar_wait(src_empty0 + 8 * sb, ((lu >> 1) & 1) ^ 1, err, ERR_WAIT_PRODUCER, abort)) {
@@ -165,18 +193,37 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t b_s = a_s + A_BYTES;
           const int k0 = (kb < nk ? kb : kb - nk) * BK;
           const CUtensorMap* mb = kb < nk ? &mapB : &mapB2;
-          tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          if (A_MN) {
-            tc::tma_load_2d(a_s, &mapA, m0, k0, fb);
-            tc::tma_load_2d(a_s + 8192, &mapA, m0 + 64, k0, fb);
-          } else {
-            tc::tma_load_2d(a_s, &mapA, k0, m0, fb);
-          }
-          if (B_MN) {
+          if (PAIR) {
+            // both halves of the stage complete on the first CTA's barrier,
+            // which expects the bytes of both
+            const uint32_t fbc = tc::mapa(fb, 0);
+            if (rank == 0) tc::mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
+            if (A_MN) {
+              tc::tma_load_2d_pair(a_s, &mapA, m0, k0, fbc);
+              tc::tma_load_2d_pair(a_s + 8192, &mapA, m0 + 64, k0, fbc);
+            } else {
+              tc::tma_load_2d_pair(a_s, &mapA, k0, m0, fbc);
+            }
+            if (B_MN) {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tc::tma_load_2d(b_s + 8192 * j, mb, n0 + 64 * j, k0, fb);
+              for (int j = 0; j < C::BNL / 64; ++j) tc::tma_load_2d_pair(b_s + 8192 * j, mb, nb0 + 64 * j, k0, fbc);
+            } else {
+              tc::tma_load_2d_pair(b_s, mb, k0, nb0, fbc);
+            }
           } else {
-            tc::tma_load_2d(b_s, mb, k0, n0, fb);
+            tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+            if (A_MN) {
+              tc::tma_load_2d(a_s, &mapA, m0, k0, fb);
+              tc::tma_load_2d(a_s + 8192, &mapA, m0 + 64, k0, fb);
+            } else {
+              tc::tma_load_2d(a_s, &mapA, k0, m0, fb);
+            }
+            if (B_MN) {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j) tc::tma_load_2d(b_s + 8192 * j, mb, n0 + 64 * j, k0, fb);
+            } else {
+              tc::tma_load_2d(b_s, mb, k0, n0, fb);
+            }
           }
           last_parity[stage] = (int)phase;
           if (++stage == C::STAGES) {
@@ -186,26 +233,45 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       if (!ok) {
-        // let copies already issued land before the CTA exits
-        for (int s = 0; s < C::STAGES; ++s)
-          if (last_parity[s] >= 0) {
-            const long long t0 = clock64();
-            while (!tc::mbar_try_wait(full0 + 8 * s, (uint32_t)last_parity[s]) && clock64() - t0 < tc::kWaitClocks) {
-            }
+        // let copies already issued land before the CTA exits (PAIR: the
+        // second CTA's copies complete on the first CTA's barriers, which
+        // it cannot poll, so it waits a fixed while instead)
+        if (PAIR && rank != 0) {
+          const long long t0 = clock64();
+          while (clock64() - t0 < 4000000) {
           }
+        } else {
+          for (int s = 0; s < C::STAGES; ++s)
+            if (last_parity[s] >= 0) {
+              const long long t0 = clock64();
+              while (!tc::mbar_try_wait(full0 + 8 * s, (uint32_t)last_parity[s]) &&
+                     clock64() - t0 < tc::kWaitClocks) {
+              }
+            }
+        }
+      } else if (PAIR) {
+        // the MMA issuer's releases of this CTA's stages arrive from the
+        // other SM: wait for the last release of every stage before exit
+        for (int i = 0; i < C::STAGES && ok; ++i) {
+          ok = tc::mbar_wait(empty0 + 8 * stage, phase ^ 1, err, ERR_WAIT_PRODUCER, abort);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      constexpr uint32_t idesc = tc::idesc_bf16(BM, BN, A_MN, B_MN);
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (PAIR: the first CTA's, for both) ----------------
+      constexpr uint32_t idesc = tc::idesc_bf16(C::TM, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      for (int u = unit0; u < nunits && ok; u += ustride) {
         const int sp = u / ntiles;
         const int kb_first = kb_lo(sp);
         if (!tc::mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, err, ERR_WAIT_MMA, abort)) {
@@ -228,17 +294,26 @@ __global__ void __launch_bounds__(192, 1)
                                      : tc::smem_desc_sw128(a_s + 32 * j, 16, 1024);
             const uint64_t bd = B_MN ? tc::smem_desc_sw128(b_s + 2048 * j, 8192, 1024)
                                      : tc::smem_desc_sw128(b_s + 32 * j, 16, 1024);
-            tc::mma_bf16(d_tmem, ad, bd, idesc, (kb != kb_first || j != 0) ? 1u : 0u);
+            if (PAIR)
+              tc::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb != kb_first || j != 0) ? 1u : 0u);
+            else
+              tc::mma_bf16(d_tmem, ad, bd, idesc, (kb != kb_first || j != 0) ? 1u : 0u);
           }
           issued = true;
-          tc::mma_commit(empty0 + 8 * stage);
+          if (PAIR)
+            tc::mma_commit_pair(empty0 + 8 * stage, 3);
+          else
+            tc::mma_commit(empty0 + 8 * stage);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        tc::mma_commit(tfull0 + 8 * acc);
+        if (PAIR)
+          tc::mma_commit_pair(tfull0 + 8 * acc, 3);
+        else
+          tc::mma_commit(tfull0 + 8 * acc);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
@@ -246,7 +321,10 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (!ok && issued) {
         // drain MMAs in flight before TMEM is released
-        tc::mma_commit(drain);
+        if (PAIR)
+          tc::mma_commit_pair(drain, 1);
+        else
+          tc::mma_commit(drain);
         const long long t0 = clock64();
         while (!tc::mbar_try_wait(drain, 0) && clock64() - t0 < tc::kWaitClocks) {
         }
@@ -268,11 +346,11 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int lu = 0;
-    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++lu) {
+    for (int u = unit0; u < nunits; u += ustride, ++lu) {
       const int t = u % ntiles, sp = u / ntiles;
       int mt_, nt_;
-        tile_mn(t, num_m, num_n, &mt_, &nt_);
-        const int m0 = mt_ * BM, n0 = nt_ * BN;
+      tile_mn(t, num_m, num_n, &mt_, &nt_);
+      const int m0 = mt_ * C::TM + rank * BM, n0 = nt_ * BN;
       const int row = m0 + trow;
       const int nch = min(BN, N - n0 + 31) / 32;  // chunks with columns < N
       auto vec_chunk = [&](int c) { return e.vec && n0 + 32 * c + 32 <= N; };
@@ -330,7 +408,12 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       tc::tc_fence_before();
-      tc::mbar_arrive(tempty0 + 8 * acc);
+      if (PAIR) {
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_cluster(tc::mapa(tempty0 + 8 * acc, 0));
+      } else {
+        tc::mbar_arrive(tempty0 + 8 * acc);
+      }
       if (SRC) tc::mbar_arrive(src_empty0 + 8 * (lu & 1));
       if (++acc == 2) {
         acc = 0;
@@ -340,9 +423,15 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
+  // PAIR: neither CTA leaves (or frees TMEM) while the other may still
+  // touch its barriers or write its accumulator
+  if (PAIR) tc::cluster_sync();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+    if (PAIR)
+      tc::tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    else
+      tc::tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -415,20 +504,20 @@ int make_map_f32(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
-template <int BN, int A_MN, int B_MN, int SRC = 0>
+template <int BN, int A_MN, int B_MN, int SRC = 0, int PAIR = 0>
 int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int splits) {
-  using C = Cfg<BN, SRC>;
+  using C = Cfg<BN, SRC, PAIR>;
   CUtensorMap ma, mb, mb2, ms;
   int rc;
   if (A_MN) rc = make_map(&ma, g.A, g.M, g.K, g.lda, 64, 64);
   else rc = make_map(&ma, g.A, g.K, g.M, g.lda, 64, BM);
   if (rc) return rc;
   if (B_MN) rc = make_map(&mb, g.B, g.N, g.K, g.ldb, 64, 64);
-  else rc = make_map(&mb, g.B, g.K, g.N, g.ldb, 64, BN);
+  else rc = make_map(&mb, g.B, g.K, g.N, g.ldb, 64, C::BNL);
   if (rc) return rc;
   if (g.B2) {
     if (B_MN) rc = make_map(&mb2, g.B2, g.N, g.K, g.ldb, 64, 64);
-    else rc = make_map(&mb2, g.B2, g.K, g.N, g.ldb, 64, BN);
+    else rc = make_map(&mb2, g.B2, g.K, g.N, g.ldb, 64, C::BNL);
     if (rc) return rc;
   } else {
     mb2 = mb;
@@ -439,19 +528,48 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
   } else {
     ms = mb;
   }
+  auto kern = gemm_tc_kernel<BN, A_MN, B_MN, SRC, PAIR>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, SRC>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
-  const int ntiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const int ntiles = ((g.M + C::TM - 1) / C::TM) * ((g.N + BN - 1) / BN);
   const int nunits = ntiles * splits;
   const int cap = g.grid_cap > 0 ? g.grid_cap : num_sms;
-  const int grid = nunits < cap ? nunits : cap;
-  gemm_tc_kernel<BN, A_MN, B_MN, SRC><<<grid, 192, C::SMEM, st>>>(ma, mb, mb2, ms, g.B2 ? 1 : 0, g.M, g.N, g.K,
-                                                                   g.e, err, splits, g.ws);
+  if (PAIR) {
+    // one unit per cluster of two CTAs, at most as many clusters as fit at once
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    static int resident = 0;  // per instantiation
+    if (!resident) {
+      cfg.gridDim = dim3(2 * (num_sms / 2));
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = num_sms / 2;
+      }
+      resident = n;
+    }
+    const int pairs = std::max(1, std::min(cap / 2, resident));
+    cfg.gridDim = dim3(2 * (nunits < pairs ? nunits : pairs));
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, ma, mb, mb2, ms, g.B2 ? 1 : 0, g.M, g.N, g.K, g.e, err,
+                                              splits, g.ws);
+    if (le != cudaSuccess) return (int)le;
+  } else {
+    const int grid = nunits < cap ? nunits : cap;
+    kern<<<grid, 192, C::SMEM, st>>>(ma, mb, mb2, ms, g.B2 ? 1 : 0, g.M, g.N, g.K, g.e, err, splits, g.ws);
+  }
   if (splits > 1) {
     const int64_t items = (int64_t)g.M * ((g.N + 31) / 32);
     const int rgrid = (int)std::min<int64_t>((items + 127) / 128, (int64_t)num_sms * 16);
@@ -460,42 +578,51 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
   return (int)cudaPeekAtLastError();
 }
 
-template <int BN>
+template <int BN, int PAIR>
 int dispatch_major(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int splits) {
   if (g.a_mn) {
-    return g.b_mn ? launch<BN, 1, 1>(g, num_sms, err, st, splits) : launch<BN, 1, 0>(g, num_sms, err, st, splits);
+    return g.b_mn ? launch<BN, 1, 1, 0, PAIR>(g, num_sms, err, st, splits)
+                  : launch<BN, 1, 0, 0, PAIR>(g, num_sms, err, st, splits);
   }
-  return g.b_mn ? launch<BN, 0, 1>(g, num_sms, err, st, splits) : launch<BN, 0, 0>(g, num_sms, err, st, splits);
+  return g.b_mn ? launch<BN, 0, 1, 0, PAIR>(g, num_sms, err, st, splits)
+                : launch<BN, 0, 0, 0, PAIR>(g, num_sms, err, st, splits);
 }
 
-// Tile width and K split by a simple time model: a k-block of a 128 x BN
+// Tile shape and K split by a simple time model: a k-block of a 128 x BN
 // tile costs BN units (BN = 128 tiles a little more per column: they are
 // closer to the shared-memory bandwidth limit), tiles run in waves of
-// num_sms, and a split adds a reduction pass over splits x M x N fp32.
+// num_sms, and a split adds a reduction pass over splits x M x N fp32.  A
+// CTA pair runs a 256 x BN tile in the time a single CTA runs 128 x BN, in
+// waves of num_sms / 2, and loads half as much B per SM (kPairGain).
 struct Plan {
-  int bn, splits;
+  int bn, splits, pair;
 };
+constexpr double kPairGain = 0.88;
 static Plan plan_gemm(const GemmArgs<bf16>& g, int num_sms) {
   const int nk = (g.K + BK - 1) / BK;
   const int nkt = g.B2 ? 2 * nk : nk;
-  const int num_m = (g.M + BM - 1) / BM;
   // cost unit: one k-block of a 128 x 256 tile (~0.27 us at full rate)
   const double kb_us = 0.27;
-  Plan best{128, 1};
+  Plan best{128, 1, 0};
   double best_cost = 1e300;
-  for (int bn : {128, 256}) {
-    if (bn == 256 && g.N <= 128) continue;
-    const int tiles = num_m * ((g.N + bn - 1) / bn);
-    const double kb_cost = (bn == 256 ? 1.0 : 0.58) * kb_us;
-    for (int sp = 1; sp <= 4; ++sp) {
-      if (sp > 1 && (!g.ws || nkt / sp < 8 || (int64_t)sp * g.M * g.N > g.ws_elems)) break;
-      const double waves = std::ceil((double)tiles * sp / num_sms);
-      const int kb_unit = (nkt + sp - 1) / sp;
-      double cost = waves * kb_unit * kb_cost;
-      if (sp > 1) cost += 3.0 + (double)sp * g.M * g.N * 8.0 / 8e6;  // launch + L2-resident traffic (us)
-      if (cost < best_cost * 0.97) {
-        best_cost = cost;
-        best = {bn, sp};
+  for (int pair = 0; pair <= 1; ++pair) {
+    if (g.pair >= 0 ? pair != g.pair : (pair && g.M <= BM)) continue;
+    const int slots = pair ? num_sms / 2 : num_sms;
+    const int num_m = (g.M + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
+    for (int bn : {128, 256}) {
+      if (bn == 256 && g.N <= 128) continue;
+      const int tiles = num_m * ((g.N + bn - 1) / bn);
+      const double kb_cost = (bn == 256 ? 1.0 : 0.58) * (pair ? kPairGain : 1.0) * kb_us;
+      for (int sp = 1; sp <= 4; ++sp) {
+        if (sp > 1 && (!g.ws || nkt / sp < 8 || (int64_t)sp * g.M * g.N > g.ws_elems)) break;
+        const double waves = std::ceil((double)tiles * sp / slots);
+        const int kb_unit = (nkt + sp - 1) / sp;
+        double cost = waves * kb_unit * kb_cost;
+        if (sp > 1) cost += 3.0 + (double)sp * g.M * g.N * 8.0 / 8e6;  // launch + L2-resident traffic (us)
+        if (cost < best_cost * 0.97) {
+          best_cost = cost;
+          best = {bn, sp, pair};
+        }
       }
     }
   }
@@ -552,13 +679,17 @@ int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st, 
   // the fp32 masters through the TMA-fed shared-memory tile
   if (g.e.kind == EPI_SGD && g.e.vec && g.a_mn && g.b_mn && !g.B2 && (g.N % 32) == 0) {
     if (kernels) *kernels = 1;
-    return launch<128, 1, 1, 1>(g, num_sms, err, st, 1);
+    const bool pair = g.pair >= 0 ? g.pair == 1 : g.M > BM;
+    return pair ? launch<128, 1, 1, 1, 1>(g, num_sms, err, st, 1) : launch<128, 1, 1, 1, 0>(g, num_sms, err, st, 1);
   }
   const Plan pl = plan_gemm(g, num_sms);
   if (pl.splits > 1 && (((uintptr_t)g.ws & 15) != 0)) return (int)cudaErrorNotSupported;
   if (kernels) *kernels = pl.splits > 1 ? 2 : 1;
-  if (pl.bn == 256) return dispatch_major<256>(g, num_sms, err, st, pl.splits);
-  return dispatch_major<128>(g, num_sms, err, st, pl.splits);
+  if (pl.pair)
+    return pl.bn == 256 ? dispatch_major<256, 1>(g, num_sms, err, st, pl.splits)
+                        : dispatch_major<128, 1>(g, num_sms, err, st, pl.splits);
+  return pl.bn == 256 ? dispatch_major<256, 0>(g, num_sms, err, st, pl.splits)
+                      : dispatch_major<128, 0>(g, num_sms, err, st, pl.splits);
 }
 
 }  // namespace ttt

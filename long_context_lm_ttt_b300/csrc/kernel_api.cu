@@ -26,10 +26,11 @@ extern "C" int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, i
   e.out_f32 = 1;
   e.out = C;
   e.ldo = ldc;
-  if (impl == 0 || impl == 1) {
+  if (impl == 0 || impl == 1 || impl == 3 || impl == 4) {
     ttt::GemmArgs<ttt::bf16> g{M, N, K, (const ttt::bf16*)A, lda, a_mn, (const ttt::bf16*)B, ldb, b_mn, e,
                                (const ttt::bf16*)B2, nullptr, 0};
-    if (impl == 0) {
+    if (impl != 1) {
+      g.pair = impl == 3 ? 0 : (impl == 4 ? 1 : -1);
       if (ttt::gemm_tc_init()) return TTT_ERR_CUDA;
       int dev = 0, sms = 148;
       cudaGetDevice(&dev);
@@ -52,7 +53,7 @@ extern "C" int ttt_kernel_gemm_sgd(int32_t M, int32_t N, int32_t K, const void* 
                                    const void* B, int64_t ldb, int32_t b_mn, float* w32, void* w16, void* w16lo,
                                    int64_t ldw, float lr, int32_t impl, void* stream) {
   if (!A || !B || !w32 || M < 0 || N < 0 || K < 1 || (N & 1) || (ldw & 1) || ldw < N) return TTT_ERR_INVALID;
-  if (impl != 0 && impl != 1) return TTT_ERR_INVALID;
+  if (impl < 0 || impl > 3) return TTT_ERR_INVALID;
   if (ensure_err()) return TTT_ERR_OOM;
   cudaStream_t st = (cudaStream_t)stream;
   ttt::Epi e;
@@ -65,7 +66,8 @@ extern "C" int ttt_kernel_gemm_sgd(int32_t M, int32_t N, int32_t K, const void* 
   e.lr = lr;
   ttt::GemmArgs<ttt::bf16> g{M, N, K, (const ttt::bf16*)A, lda, a_mn, (const ttt::bf16*)B, ldb, b_mn, e,
                              nullptr, nullptr, 0};
-  if (impl == 0) {
+  if (impl != 1) {
+    g.pair = impl == 2 ? 0 : (impl == 3 ? 1 : -1);
     if (ttt::gemm_tc_init()) return TTT_ERR_CUDA;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);

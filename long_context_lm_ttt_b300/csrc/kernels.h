@@ -25,6 +25,9 @@ struct GemmArgs {
   // tensor-core GEMM CTAs: 0 = one persistent CTA per SM; otherwise at most
   // this many (a large value gives one CTA per tile)
   int grid_cap = 0;
+  // tensor-core GEMM tiles: -1 = chosen by the planner, 0 = 128-row tiles on
+  // one CTA, 1 = 256-row tiles on a CTA pair (cta_group::2)
+  int pair = -1;
 };
 
 // SIMT fp32-accumulate GEMM (check mode; reference for the tensor-core one)

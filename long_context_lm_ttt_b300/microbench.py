@@ -144,7 +144,9 @@ def main():
         a.add_argument("--W", type=int, default=8192)
         a.add_argument("--pos0", type=int, default=40960)
     for p in sub.choices.values():
-        p.add_argument("--impl", type=int, default=0, help="0 tensor cores, 1 SIMT")
+        p.add_argument("--impl", type=int, default=0,
+                       help="as the C entry point's impl: 0 tensor cores, 1 SIMT; gemm 3/4 and gemm-sgd 2/3 "
+                            "force single-CTA / CTA-pair tiles")
         p.add_argument("--warmup", type=int, default=3)
         p.add_argument("--iters", type=int, default=10)
     args = ap.parse_args()

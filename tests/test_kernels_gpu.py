@@ -27,12 +27,16 @@ def _operand(rng, rows, cols, mn, bf16=True):
 
 
 SHAPES = [(128, 128, 64), (256, 384, 192), (100, 200, 96), (32, 128, 32), (130, 258, 70),
-          (1024, 3072, 1024), (512, 512, 4096)]
+          (1024, 3072, 1024), (512, 512, 4096), (520, 640, 200), (300, 136, 1000)]
+
+# impl 0: tensor cores, planner's choice; 3: 128-row tiles on one CTA;
+# 4: 256-row tiles on a CTA pair (also for M < 256: the second CTA's rows
+# are all out of range); 1: SIMT
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
-@pytest.mark.parametrize("impl", [0, 1])
+@pytest.mark.parametrize("impl", [0, 1, 3, 4])
 def test_gemm_bf16(M, N, K, a_mn, b_mn, impl):
     torch, T = _env()
     if impl == 1 and M * N * K > 2 ** 28:
@@ -46,7 +50,7 @@ def test_gemm_bf16(M, N, K, a_mn, b_mn, impl):
     C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     lda = M if a_mn else K
     ldb = N if b_mn else K
-    if impl == 0 and (lda % 8 or ldb % 8):
+    if impl != 1 and (lda % 8 or ldb % 8):
         pytest.skip("TMA needs 16-byte row pitch")
     T.ttt_kernel_gemm(M, N, K, dA, lda, a_mn, dB, ldb, b_mn, None, C, N, impl)
     torch.cuda.synchronize()
@@ -56,7 +60,7 @@ def test_gemm_bf16(M, N, K, a_mn, b_mn, impl):
     assert err < 1e-5, err          # fp32 accumulation of exact bf16 products
 
 
-@pytest.mark.parametrize("impl", [0, 1])
+@pytest.mark.parametrize("impl", [0, 1, 3, 4])
 @pytest.mark.parametrize("b_mn", [0, 1])
 def test_gemm_dual_b(impl, b_mn):
     """C = A B^T + A B2^T (the hi + lo fast-weight pair)."""
@@ -90,12 +94,14 @@ def test_gemm_fp32_simt():
     assert np.abs(C.cpu().numpy() - ref).max() / np.abs(ref).max() < 1e-5
 
 
-@pytest.mark.parametrize("M,N,K", [(3072, 8192, 1024), (16384, 3072, 1024), (200, 96, 40), (256, 384, 512)])
-@pytest.mark.parametrize("impl", [0, 1])
+@pytest.mark.parametrize("M,N,K", [(3072, 8192, 1024), (16384, 3072, 1024), (200, 96, 40), (256, 384, 512),
+                                   (392, 160, 72)])
+@pytest.mark.parametrize("impl", [0, 1, 2, 3])
 def test_gemm_sgd(M, N, K, impl):
     """Weight gradient + fused SGD step: w32 -= lr A^T B (both operands stored
     [K, M] / [K, N], as the chunk's activations are), then the bf16 pair
-    hi = rn(w32), lo = rn(w32 - hi)."""
+    hi = rn(w32), lo = rn(w32 - hi).  impl 0 tensor cores (planner), 2 one
+    CTA per tile, 3 CTA pairs, 1 SIMT."""
     torch, T = _env()
     if impl == 1 and M * N * K > 2 ** 30:
         pytest.skip("SIMT reference only on the small shapes")
