@@ -35,9 +35,12 @@ namespace {
 constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 
-// SRC = 1: the epilogue's fp32 source tile (the master weights of the SGD
-// epilogue) is brought into shared memory by TMA at the start of each tile,
-// double-buffered, so its load overlaps the tile's main loop.
+// SRC = 1 (the SGD epilogue): the tile's fp32 master weights are brought
+// into shared memory by TMA at the start of each tile, so the load overlaps
+// the tile's main loop.  The epilogue updates them in place and writes the
+// bf16 pair (hi, lo) into a staging tile; each epilogue warp then sends its
+// 32 rows of all three back with TMA stores, so every global write is a
+// whole 128-byte line.
 //
 // PAIR = 1: a cluster of two CTAs (on the two SMs of a TPC) computes a
 // 256 x BN tile with tcgen05 MMAs of M = 256 (cta_group::2).  CTA r of the
@@ -53,12 +56,19 @@ struct Cfg {
   static constexpr int TM = PAIR ? 2 * BM : BM;   // rows of a work tile
   static constexpr int B_BYTES = BNL * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int SRC_BYTES = SRC ? BM * BN * 4 : 0;  // one fp32 tile
-  static constexpr int PAIR_STAGES = (kSmemMax - 2048 - 2 * SRC_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = !PAIR ? (SRC ? 3 : (BN == 256 ? 4 : 6)) : (PAIR_STAGES > 8 ? 8 : PAIR_STAGES);
+  // SRC: the master tile moves through two slots of 64 columns (one slice
+  // each, 32 KB fp32); the bf16 pair of the slice being stored is staged in
+  // one 64-column slot of hi and one of lo (16 KB each)
+  static constexpr int SLICES = BN / 64;
+  static constexpr int SLOT_BYTES = BM * 64 * 4;
+  static constexpr int SRC_BYTES = SRC ? 2 * SLOT_BYTES : 0;
+  static constexpr int HL_BYTES = SRC ? 2 * BM * 128 : 0;
+  static constexpr int FIT_STAGES = (kSmemMax - 2048 - SRC_BYTES - HL_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = (PAIR || SRC) ? (FIT_STAGES > 8 ? 8 : FIT_STAGES) : (BN == 256 ? 4 : 6);
   static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
   static constexpr int SRC_OFF = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = SRC_OFF + 2 * SRC_BYTES;
+  static constexpr int HL_OFF = SRC_OFF + SRC_BYTES;
+  static constexpr int BAR_OFF = HL_OFF + HL_BYTES;
   static constexpr int SMEM = 1024 /*align slack*/ + BAR_OFF + 256;
   static_assert(SMEM <= kSmemMax, "shared memory");
   static_assert(8 * (2 * STAGES + 9) + 8 <= 256, "barrier area");
@@ -84,8 +94,10 @@ __device__ __forceinline__ void tile_mn(int t, int num_m, int num_n, int* mt, in
 template <int BN, int A_MN, int B_MN, int SRC = 0, int PAIR = 0>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                   const __grid_constant__ CUtensorMap mapB2, const __grid_constant__ CUtensorMap mapS, int dual,
-                   int M, int N, int K, Epi e, int* err, int splits, float* ws) {
+                   const __grid_constant__ CUtensorMap mapB2, const __grid_constant__ CUtensorMap mapS,
+                   const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapH,
+                   const __grid_constant__ CUtensorMap mapL, int dual, int M, int N, int K, Epi e, int* err,
+                   int splits, float* ws) {
   using C = Cfg<BN, SRC, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -97,8 +109,8 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tfull0 = empty0 + 8 * C::STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
-  const uint32_t src_full0 = drain + 8;       // [2] (SRC only)
-  const uint32_t src_empty0 = src_full0 + 16;  // [2]
+  const uint32_t src_full = drain + 8;        // [2] halves of the master tile (SRC only)
+  const uint32_t src_empty = src_full + 16;   // [2]
   uint32_t* tmem_slot = (uint32_t*)(smem + C::BAR_OFF + 8 * (2 * C::STAGES + 9));
   volatile int* abort = (volatile int*)(tmem_slot + 1);
 
@@ -126,9 +138,9 @@ __global__ void __launch_bounds__(192, 1)
       tc::mbar_init(tempty0 + 8 * a, PAIR ? 8 : 128);
     }
     tc::mbar_init(drain, 1);
-    for (int a = 0; a < 2; ++a) {
-      tc::mbar_init(src_full0 + 8 * a, 1);
-      tc::mbar_init(src_empty0 + 8 * a, 128);
+    for (int j = 0; j < 2; ++j) {
+      tc::mbar_init(src_full + 8 * j, 1);
+      tc::mbar_init(src_empty + 8 * j, 4);  // one arrival per epilogue warp
     }
     *abort = 0;
     tc::fence_mbar_init();
@@ -137,7 +149,12 @@ __global__ void __launch_bounds__(192, 1)
     tc::prefetch_tmap(&mapA);
     tc::prefetch_tmap(&mapB);
     if (dual) tc::prefetch_tmap(&mapB2);
-    if (SRC) tc::prefetch_tmap(&mapS);
+    if (SRC) {
+      tc::prefetch_tmap(&mapS);
+      tc::prefetch_tmap(&mapW);
+      tc::prefetch_tmap(&mapH);
+      tc::prefetch_tmap(&mapL);
+    }
   }
   if (warp == 1) {
     if (PAIR) {
@@ -164,6 +181,46 @@ __global__ void __launch_bounds__(192, 1)
       int last_parity[C::STAGES];
       for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
       bool ok = true;
+      // SRC: the 64-column slices of the master tiles of this CTA's units go,
+      // in order, into the two slots as soon as the epilogue has stored a
+      // slot's previous slice.  The producer issues them whenever it finds
+      // a slot free, also while it waits for a pipeline stage, and waits
+      // for slots only once every k-block has been issued, so the main loop
+      // never waits for them.  gs counts slices issued.
+      const int src_total = SRC && unit0 < nunits ? ((nunits - 1 - unit0) / ustride + 1) * C::SLICES : 0;
+      int gs = 0;
+      auto issue_src = [&] {
+        const int u = unit0 + (gs / C::SLICES) * ustride, sl = gs % C::SLICES;
+        int sm_, sn_;
+        tile_mn(u % ntiles, num_m, num_n, &sm_, &sn_);
+        const uint32_t sf = src_full + 8 * (gs & 1);
+        tc::mbar_arrive_expect_tx(sf, C::SLOT_BYTES);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          tc::tma_load_2d(sbase + C::SRC_OFF + (gs & 1) * C::SLOT_BYTES + j * BM * 128, &mapS,
+                          sn_ * BN + 64 * sl + 32 * j, sm_ * C::TM + rank * BM, sf);
+        ++gs;
+      };
+      auto slot_bar = [&] { return src_empty + 8 * (gs & 1); };
+      auto slot_par = [&] { return (uint32_t)(((gs >> 1) & 1) ^ 1); };
+      auto pump = [&] {
+        while (gs < src_total && tc::mbar_try_wait(slot_bar(), slot_par())) issue_src();
+      };
+      // wait for a free pipeline stage (SRC: issuing slices meanwhile)
+      auto wait_stage = [&](uint32_t bar, uint32_t par) -> bool {
+        if (!SRC) return tc::mbar_wait(bar, par, err, ERR_WAIT_PRODUCER, abort);
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(bar, par)) {
+          pump();
+          if (*abort) return false;
+          if (clock64() - t0 > tc::kWaitClocks) {
+            atomicCAS(err, 0, ERR_WAIT_PRODUCER);
+            *abort = 1;
+            return false;
+          }
+        }
+        return true;
+      };
       int lu = 0;  // this CTA's unit counter
       for (int u = unit0; u < nunits && ok; u += ustride, ++lu) {
         const int t = u % ntiles, sp = u / ntiles;
@@ -171,20 +228,9 @@ __global__ void __launch_bounds__(192, 1)
         tile_mn(t, num_m, num_n, &mt_, &nt_);
         // this CTA's rows of the tile and the B columns it loads
         const int m0 = mt_ * C::TM + rank * BM, n0 = nt_ * BN, nb0 = n0 + rank * C::BNL;
-        if (SRC) {
-          const int sb = lu & 1;
-          if (!tc::mbar_wait(src_empty0 + 8 * sb, ((lu >> 1) & 1) ^ 1, err, ERR_WAIT_PRODUCER, abort)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sf = src_full0 + 8 * sb;
-          tc::mbar_arrive_expect_tx(sf, C::SRC_BYTES);
-#pragma unroll
-          for (int c = 0; c < BN / 32; ++c)
-            tc::tma_load_2d(sbase + C::SRC_OFF + sb * C::SRC_BYTES + c * BM * 128, &mapS, n0 + 32 * c, m0, sf);
-        }
         for (int kb = kb_lo(sp); kb < kb_lo(sp + 1); ++kb) {
-          if (!tc::mbar_wait(empty0 + 8 * stage, phase ^ 1, err, ERR_WAIT_PRODUCER, abort)) {
+          if (SRC) pump();
+          if (!wait_stage(empty0 + 8 * stage, phase ^ 1)) {
             ok = false;
             break;
           }
@@ -232,6 +278,13 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
+      while (ok && gs < src_total) {
+        if (!tc::mbar_wait(slot_bar(), slot_par(), err, ERR_WAIT_PRODUCER, abort)) {
+          ok = false;
+          break;
+        }
+        issue_src();
+      }
       if (!ok) {
         // let copies already issued land before the CTA exits (PAIR: the
         // second CTA's copies complete on the first CTA's barriers, which
@@ -248,6 +301,13 @@ __global__ void __launch_bounds__(192, 1)
                      clock64() - t0 < tc::kWaitClocks) {
               }
             }
+        }
+        // and the last master-tile slice of each slot
+        for (int k = gs > 2 ? gs - 2 : 0; k < gs; ++k) {
+          const long long t0 = clock64();
+          while (!tc::mbar_try_wait(src_full + 8 * (k & 1), (uint32_t)((k >> 1) & 1)) &&
+                 clock64() - t0 < tc::kWaitClocks) {
+          }
         }
       } else if (PAIR) {
         // the MMA issuer's releases of this CTA's stages arrive from the
@@ -346,6 +406,7 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int lu = 0;
+    int gs = 0;  // SRC: master-tile slices consumed
     for (int u = unit0; u < nunits; u += ustride, ++lu) {
       const int t = u % ntiles, sp = u / ntiles;
       int mt_, nt_;
@@ -358,68 +419,132 @@ __global__ void __launch_bounds__(192, 1)
       if (has_src && row < M && vec_chunk(0)) epi_src_load(e, row, n0, src);
       if (!tc::mbar_wait(tfull0 + 8 * acc, acc_phase, err, ERR_WAIT_EPI, abort)) break;
       tc::tc_fence_after();
-      const uint32_t stile = sbase + C::SRC_OFF + (lu & 1) * C::SRC_BYTES;
-      if (SRC && !tc::mbar_wait(src_full0 + 8 * (lu & 1), (lu >> 1) & 1, err, ERR_WAIT_EPI, abort)) break;
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-#pragma unroll 1
-      for (int c = 0; c < nch; ++c) {
-        float v[32];
-        tc::tmem_ld32(tbase + c * 32, v);
-        uint4 nxt[8];
-        if (has_src && row < M && c + 1 < nch && vec_chunk(c + 1)) epi_src_load(e, row, n0 + 32 * (c + 1), nxt);
-        if (SRC) {
-          // this row's 128 bytes of source chunk c (128-byte swizzle)
-          const uint32_t rb = stile + c * BM * 128 + trow * 128;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint32_t a0, a1, a2, a3;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                         : "r"(rb + ((i ^ (trow & 7)) << 4)));
-            src[i] = make_uint4(a0, a1, a2, a3);
-          }
+      // release the accumulator once this warp's TMEM reads are done
+      auto release_acc = [&] {
+        tc::tc_fence_before();
+        if (PAIR) {
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive_cluster(tc::mapa(tempty0 + 8 * acc, 0));
+        } else {
+          tc::mbar_arrive(tempty0 + 8 * acc);
         }
-        if (row < M && partial) {
-          float* wp = ws + ((int64_t)sp * M + row) * N + n0 + 32 * c;
-          if (vec_chunk(c) && (N & 3) == 0) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              stg16(wp + 4 * i, make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
-                                           __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])));
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-              if (n0 + 32 * c + k < N) wp[k] = v[k];
+      };
+      if (SRC) {
+        // One 64-column slice at a time: w -= lr * acc on this row's bytes
+        // of the slice's slot of the master tile (128-byte swizzle), in
+        // place; hi = rn(w) and lo = rn(w - hi) into the staging slots
+        // ([128 rows][128 B] each); then this warp's 32 rows of the slice go
+        // out by TMA (boxes past the last row or column are not issued), and
+        // the slots are released once the stores have read them.
+        bool failed = false;
+#pragma unroll 1
+        for (int sl = 0; sl < C::SLICES; ++sl, ++gs) {
+          const uint32_t slot = sbase + C::SRC_OFF + (gs & 1) * C::SLOT_BYTES;
+          if (!tc::mbar_wait(src_full + 8 * (gs & 1), (gs >> 1) & 1, err, ERR_WAIT_EPI, abort)) {
+            failed = true;
+            break;
           }
-        } else if (row < M) {
-          if (vec_chunk(c)) {
-            epi_row32(e, row, n0 + 32 * c, v, src);
-          } else {
+#pragma unroll 1
+          for (int j = 0; j < 2; ++j) {
+            const int c = 2 * sl + j;
+            if (n0 + 32 * c >= N) continue;
+            float v[32];
+            tc::tmem_ld32(tbase + c * 32, v);
+            const uint32_t rb = slot + j * BM * 128 + trow * 128;
+            uint32_t hl[16], ll[16];
 #pragma unroll
-            for (int p = 0; p < 16; ++p) {
-              const int col = n0 + c * 32 + 2 * p;
-              if (col < N) epi_pair<bf16>(e, row, col, v[2 * p], v[2 * p + 1]);
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t ad = rb + ((i ^ (trow & 7)) << 4);
+              float w0, w1, w2, w3;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(w0), "=f"(w1), "=f"(w2), "=f"(w3)
+                           : "r"(ad));
+              w0 -= e.lr * v[4 * i];
+              w1 -= e.lr * v[4 * i + 1];
+              w2 -= e.lr * v[4 * i + 2];
+              w3 -= e.lr * v[4 * i + 3];
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ad), "f"(w0), "f"(w1), "f"(w2), "f"(w3)
+                           : "memory");
+              hl[2 * i] = bf2(w0, w1);
+              hl[2 * i + 1] = bf2(w2, w3);
+              const float2 h01 = unbf2(hl[2 * i]), h23 = unbf2(hl[2 * i + 1]);
+              ll[2 * i] = bf2(w0 - h01.x, w1 - h01.y);
+              ll[2 * i + 1] = bf2(w2 - h23.x, w3 - h23.y);
+            }
+            const uint32_t hb = sbase + C::HL_OFF + trow * 128;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t off = (((4 * j + i) ^ (trow & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(hb + off), "r"(hl[4 * i]),
+                           "r"(hl[4 * i + 1]), "r"(hl[4 * i + 2]), "r"(hl[4 * i + 3])
+                           : "memory");
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(hb + BM * 128 + off), "r"(ll[4 * i]),
+                           "r"(ll[4 * i + 1]), "r"(ll[4 * i + 2]), "r"(ll[4 * i + 3])
+                           : "memory");
             }
           }
+          if (sl == C::SLICES - 1) release_acc();
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int r = m0 + quarter * 32, c0 = n0 + 64 * sl;
+            if (r < M && c0 < N) {
+              for (int j = 0; j < 2; ++j)
+                if (c0 + 32 * j < N) tc::tma_store_2d(&mapW, c0 + 32 * j, r, slot + j * BM * 128 + quarter * 4096);
+              const uint32_t hb = sbase + C::HL_OFF + quarter * 4096;
+              tc::tma_store_2d(&mapH, c0, r, hb);
+              tc::tma_store_2d(&mapL, c0, r, hb + BM * 128);
+            }
+            tc::bulk_commit();
+            tc::bulk_wait_read();
+            tc::mbar_arrive(src_empty + 8 * (gs & 1));
+          }
+          __syncwarp();
         }
-        if (!SRC) {
+        if (failed) break;
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+          float v[32];
+          tc::tmem_ld32(tbase + c * 32, v);
+          uint4 nxt[8];
+          if (has_src && row < M && c + 1 < nch && vec_chunk(c + 1)) epi_src_load(e, row, n0 + 32 * (c + 1), nxt);
+          if (row < M && partial) {
+            float* wp = ws + ((int64_t)sp * M + row) * N + n0 + 32 * c;
+            if (vec_chunk(c) && (N & 3) == 0) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                stg16(wp + 4 * i, make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                                             __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])));
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                if (n0 + 32 * c + k < N) wp[k] = v[k];
+            }
+          } else if (row < M) {
+            if (vec_chunk(c)) {
+              epi_row32(e, row, n0 + 32 * c, v, src);
+            } else {
+#pragma unroll
+              for (int p = 0; p < 16; ++p) {
+                const int col = n0 + c * 32 + 2 * p;
+                if (col < N) epi_pair<bf16>(e, row, col, v[2 * p], v[2 * p + 1]);
+              }
+            }
+          }
 #pragma unroll
           for (int i = 0; i < 8; ++i) src[i] = nxt[i];
         }
+        release_acc();
       }
-      tc::tc_fence_before();
-      if (PAIR) {
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive_cluster(tc::mapa(tempty0 + 8 * acc, 0));
-      } else {
-        tc::mbar_arrive(tempty0 + 8 * acc);
-      }
-      if (SRC) tc::mbar_arrive(src_empty0 + 8 * (lu & 1));
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
       }
     }
+    // global writes of the last stores complete before the CTA exits
+    if (SRC && lane == 0) tc::bulk_wait_all();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -492,11 +617,12 @@ int make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, 
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
-// fp32 [rows, cols] tile map with 128-byte swizzle: box {32 columns, 128 rows}
-int make_map_f32(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld_elems) {
+// fp32 [rows, cols] tile map with 128-byte swizzle: box {32 columns, box_rows}
+int make_map_f32(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld_elems,
+                 uint32_t box_rows) {
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {ld_elems * 4};
-  cuuint32_t box[2] = {32, (cuuint32_t)BM};
+  cuuint32_t box[2] = {32, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -507,7 +633,7 @@ int make_map_f32(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows
 template <int BN, int A_MN, int B_MN, int SRC = 0, int PAIR = 0>
 int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int splits) {
   using C = Cfg<BN, SRC, PAIR>;
-  CUtensorMap ma, mb, mb2, ms;
+  CUtensorMap ma, mb, mb2, ms, mw, mh, ml;
   int rc;
   if (A_MN) rc = make_map(&ma, g.A, g.M, g.K, g.lda, 64, 64);
   else rc = make_map(&ma, g.A, g.K, g.M, g.lda, 64, BM);
@@ -523,10 +649,14 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
     mb2 = mb;
   }
   if (SRC) {
-    rc = make_map_f32(&ms, g.e.w32, g.N, g.M, g.e.ldo);
+    // master tile in (128 rows), master / hi / lo out (32-row slab per warp)
+    rc = make_map_f32(&ms, g.e.w32, g.N, g.M, g.e.ldo, BM);
+    if (!rc) rc = make_map_f32(&mw, g.e.w32, g.N, g.M, g.e.ldo, 32);
+    if (!rc) rc = make_map(&mh, g.e.w16, g.N, g.M, g.e.ldo, 64, 32);
+    if (!rc) rc = make_map(&ml, g.e.w16lo, g.N, g.M, g.e.ldo, 64, 32);
     if (rc) return rc;
   } else {
-    ms = mb;
+    ms = mw = mh = ml = mb;
   }
   auto kern = gemm_tc_kernel<BN, A_MN, B_MN, SRC, PAIR>;
   static bool attr_set = false;  // per instantiation
@@ -563,12 +693,13 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
     }
     const int pairs = std::max(1, std::min(cap / 2, resident));
     cfg.gridDim = dim3(2 * (nunits < pairs ? nunits : pairs));
-    const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, ma, mb, mb2, ms, g.B2 ? 1 : 0, g.M, g.N, g.K, g.e, err,
-                                              splits, g.ws);
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, ma, mb, mb2, ms, mw, mh, ml, g.B2 ? 1 : 0, g.M, g.N, g.K,
+                                              g.e, err, splits, g.ws);
     if (le != cudaSuccess) return (int)le;
   } else {
     const int grid = nunits < cap ? nunits : cap;
-    kern<<<grid, 192, C::SMEM, st>>>(ma, mb, mb2, ms, g.B2 ? 1 : 0, g.M, g.N, g.K, g.e, err, splits, g.ws);
+    kern<<<grid, 192, C::SMEM, st>>>(ma, mb, mb2, ms, mw, mh, ml, g.B2 ? 1 : 0, g.M, g.N, g.K, g.e, err, splits,
+                                     g.ws);
   }
   if (splits > 1) {
     const int64_t items = (int64_t)g.M * ((g.N + 31) / 32);
@@ -675,12 +806,14 @@ int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st, 
   if (((uintptr_t)g.A & 15) || ((uintptr_t)g.B & 15) || ((uintptr_t)g.B2 & 15) || (g.lda & 7) ||
       (g.ldb & 7) || g.K <= 0)
     return (int)cudaErrorNotSupported;
-  // the SGD epilogue (weight-gradient GEMM, both operands MN-major) reads
-  // the fp32 masters through the TMA-fed shared-memory tile
-  if (g.e.kind == EPI_SGD && g.e.vec && g.a_mn && g.b_mn && !g.B2 && (g.N % 32) == 0) {
+  // the SGD epilogue (weight-gradient GEMM, both operands MN-major, the
+  // bf16 pair wanted) updates the fp32 masters in a TMA-fed shared-memory
+  // tile and stores all three outputs by TMA
+  if (g.e.kind == EPI_SGD && g.e.vec && g.a_mn && g.b_mn && !g.B2 && (g.N % 32) == 0 && g.e.w16 && g.e.w16lo &&
+      (g.e.ldo % 8) == 0 && a16(g.e.w16) && a16(g.e.w16lo)) {
     if (kernels) *kernels = 1;
     const bool pair = g.pair >= 0 ? g.pair == 1 : g.M > BM;
-    return pair ? launch<128, 1, 1, 1, 1>(g, num_sms, err, st, 1) : launch<128, 1, 1, 1, 0>(g, num_sms, err, st, 1);
+    return pair ? launch<256, 1, 1, 1, 1>(g, num_sms, err, st, 1) : launch<128, 1, 1, 1, 0>(g, num_sms, err, st, 1);
   }
   const Plan pl = plan_gemm(g, num_sms);
   if (pl.splits > 1 && (((uintptr_t)g.ws & 15) != 0)) return (int)cudaErrorNotSupported;
