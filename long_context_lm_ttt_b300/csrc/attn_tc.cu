@@ -569,7 +569,8 @@ __global__ void __launch_bounds__(576, 1)
   const uint32_t q_full = bar0;
   const uint32_t k_full = bar0 + 8;     // [2] stages
   const uint32_t v_full = bar0 + 24;    // [2]
-  const uint32_t kv_empty = bar0 + 40;  // [2]
+  const uint32_t k_empty = bar0 + 40;   // [2] stages: K of the stage consumed
+  const uint32_t v_empty = bar0 + 200;  // [2] stages: V of the stage consumed
   const uint32_t s_full = bar0 + 56;    // [2] tiles
   const uint32_t p_full = bar0 + 72;    // [2] tiles
   const uint32_t o_done = bar0 + 88;    // [2] tiles
@@ -596,7 +597,8 @@ __global__ void __launch_bounds__(576, 1)
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(k_full + 8 * s, 1);
       tc::mbar_init(v_full + 8 * s, 1);
-      tc::mbar_init(kv_empty + 8 * s, 1);
+      tc::mbar_init(k_empty + 8 * s, 1);
+      tc::mbar_init(v_empty + 8 * s, 1);
       tc::mbar_init(s_full + 8 * s, 1);
       tc::mbar_init(p_full + 8 * s, 256);
       tc::mbar_init(o_done + 8 * s, 1);
@@ -632,7 +634,10 @@ __global__ void __launch_bounds__(576, 1)
                           q_full);
       for (int i = 0; i < nbl && ok; ++i) {
         const int st = i & 1;
-        if (!tc::mbar_wait(kv_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
+        // K and V of a stage are released separately: K once both tiles'
+        // scores of its block are done, V once both P.V products are, so
+        // the next K lands a block earlier than with one shared release
+        if (!tc::mbar_wait(k_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
           ok = false;
           break;
         }
@@ -642,6 +647,10 @@ __global__ void __launch_bounds__(576, 1)
         for (int a = 0; a < NA; ++a)
           tc::tma_load_2d(sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN2 * 128, &mapK, 64 * a, row,
                           k_full + 8 * st);
+        if (!tc::mbar_wait(v_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
+          ok = false;
+          break;
+        }
         tc::mbar_arrive_expect_tx(v_full + 8 * st, SM::KV_BYTES);
         for (int a = 0; a < NA; ++a)
           tc::tma_load_2d(sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN2 * 128, &mapV, 64 * a, row,
@@ -686,6 +695,7 @@ __global__ void __launch_bounds__(576, 1)
 #pragma unroll
       for (int t = 0; t < 2; ++t)
         if (ok && nbl > 0 && part(t, kb_lo)) ok = issue_s(t, 0);
+      if (ok && nbl > 0) tc::mma_commit(k_empty);
       for (int i = 0; i < nbl && ok; ++i) {
         const long long j = kb_lo + i;
         const int st = i & 1;
@@ -710,9 +720,10 @@ __global__ void __launch_bounds__(576, 1)
             tc::mma_commit(o_done + 8 * t);
             ++cnt[t];
           }
-          if (i + 1 < nbl && part(t, j + 1)) ok = issue_s(t, i + 1);
+          if (t == 1 && ok) tc::mma_commit(v_empty + 8 * st);
+          if (ok && i + 1 < nbl && part(t, j + 1)) ok = issue_s(t, i + 1);
         }
-        if (ok) tc::mma_commit(kv_empty + 8 * st);
+        if (ok && i + 1 < nbl) tc::mma_commit(k_empty + 8 * ((i + 1) & 1));
       }
       if (!ok && issued) {
         tc::mma_commit(drain);
