@@ -20,6 +20,11 @@ dependency chain and there is nothing to exchange).
 
 `--impl reference` times the plain CPU oracle on the host cores on a bounded
 sample of the same workload (the only other implementation of this method).
+
+`--mode decode` measures decode-time test-time training instead: after an
+untimed prefill of `--context` tokens, ttt_decode generates `--decode-tokens`
+tokens greedily (one position per step, a test-time step on every completed
+chunk); a step of the benchmark is one such decode call.
 """
 from __future__ import annotations
 
@@ -62,6 +67,11 @@ def parse_args():
                     help="tokens the oracle is timed on (default: one chunk; 128 at 3B)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--mode", choices=["prefill", "decode"], default="prefill")
+    ap.add_argument("--context", type=int, default=None,
+                    help="decode: tokens prefilled before decoding (default 8 chunks)")
+    ap.add_argument("--decode-tokens", type=int, default=None,
+                    help="decode: tokens generated per step (default one chunk)")
     ap.add_argument("--profile", choices=["timed", "off"], default="timed",
                     help="per-launch CUDA events over a second, profiled pass of the timed steps (roofline), or none")
     return ap.parse_args()
@@ -383,10 +393,104 @@ def run_ours(args):
     return 0
 
 
+def decode_bytes_per_token(s, ctx: int) -> float:
+    """HBM bytes one decode step must read: every weight once (the fast
+    MLPs as the bf16 pair), the window's keys and values in every layer,
+    and one embedding row."""
+    d, ff, H, Hkv, hd, L, Lt = s.d_model, s.d_ff, s.n_heads, s.n_kv_heads, s.head_dim, s.n_layers, s.n_ttt_layers
+    attn = d * (H + 2 * Hkv) * hd + H * hd * d
+    mlp = 3 * d * ff
+    w = 2.0 * (L * attn + (L - Lt) * mlp + 2 * Lt * mlp + s.vocab * d + d)
+    kv = 2.0 * 2 * L * min(ctx, s.window) * Hkv * hd
+    return w + kv
+
+
+def run_decode(args):
+    """--mode decode: tokens/s of one sequence generating greedily with a
+    test-time step on every completed chunk."""
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    torch.cuda.set_device(0)
+    from long_context_lm_ttt_b300 import ttt as TT
+    TT.load()
+    peaks, peak_src = load_peaks()
+    s, tok = workload(args)
+    b = s.chunk
+    ctx = args.context if args.context is not None else 8 * b
+    nd = args.decode_tokens or b
+    if ctx % b:
+        raise SystemExit("--context must be a multiple of the chunk length")
+    w = inputs.make_weights(s)
+    tok = inputs.make_tokens(s.replace(seq_len=ctx + 1), seed=1)
+    m = TT.TTT(s, w, TT.TTT_BF16, max_tokens=ctx + nd + 1)
+    del w
+    tok_d = torch.from_numpy(tok).cuda()
+    out_d = torch.zeros(nd + 1, dtype=torch.int32, device="cuda")
+    loss_d = torch.zeros(nd // b + 1, dtype=torch.float32, device="cuda")
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+
+    def step(host=False):
+        m.reset()
+        m.prefill(tok_d[:ctx])
+        torch.cuda.synchronize()
+        if host:
+            t0 = time.perf_counter()
+            o, l = m.decode(tok[ctx:ctx + 1], nd)
+            return 1e3 * (time.perf_counter() - t0), o
+        ev0.record()
+        m.decode(tok_d[ctx:ctx + 1], nd, out_d, loss_d)
+        ev1.record()
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1), None
+
+    for _ in range(args.warmup):
+        step()
+    uuid = str(torch.cuda.get_device_properties(0).uuid)
+    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    clocks.start()
+    ms = [step()[0] for _ in range(args.steps)]
+    clk = clocks.stop()
+    dec_ms = sum(ms)
+    value = nd * args.steps / (dec_ms / 1e3)
+    if not np.all(np.isfinite(loss_d.cpu().numpy()[: nd // b])):
+        raise SystemExit("non-finite decode chunk loss")
+    e2e_ms = sum(step(host=True)[0] for _ in range(args.steps))
+    per_tok = dec_ms / args.steps / nd
+    bytes_tok = decode_bytes_per_token(s, ctx + nd // 2)
+    ach = bytes_tok / (per_tok / 1e3) / 1e9
+    line = {
+        "metric": "TTT-E2E decode-time test-time training, tokens/s of one sequence (greedy, "
+                  "one test-time step per chunk of generated tokens)",
+        "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dec_ms / args.steps, "ms_per_token": per_tok, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_name(s) + f" decode: context {ctx}, {nd} generated tokens",
+                   "global_batch": 1, "context": ctx, "decode_tokens": nd,
+                   "l2": "every step streams all weights (7+ GB at 3B), larger than L2"},
+        "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"), "reasons": clk.get("reasons")},
+        "e2e": {"value": nd * args.steps / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": 4,
+                "d2h_bytes_per_step": 4 * (nd + 1) + 4 * (nd // b + 1)},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "whole decode step (weights + window keys/values per token; the chunk "
+                               "steps' time is included, their bytes are not)",
+                     "peak_source": f"{peak_src} (copy)"},
+    }
+    m.close()
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode == "decode":
+        return run_decode(args)
     return run_ours(args)
 
 

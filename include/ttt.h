@@ -118,6 +118,36 @@ int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* stream, ttt_ct
 int ttt_prefill(ttt_ctx* ctx, const int32_t* tokens, int64_t T, float* chunk_losses,
                 void* stream);
 
+/* Decode-time test-time training: generation one token per step, with the
+ * same test-time step as ttt_prefill's chunk loop once every b positions
+ * (the latency per token stays constant in the context length: summary
+ * page, Key claims; podcast 5:55).  Step i (position pos + i, where pos is
+ * the context's position) runs the token through every block with the
+ * current weights, writing its keys and values to the ring, and forms the
+ * next input: tokens[i + 1] while given, else the greedy prediction (the
+ * index of the largest logit, the smallest index on ties).  When position
+ * p completes a chunk [p + 1 - b, p + 1), the chunk is trained on as in
+ * ttt_prefill: its fast blocks are recomputed over the chunk, the loss is
+ * the mean over its b positions of (logsumexp(z_t) - z_t[token t+1]), where
+ * the target of the chunk's last position is that step's next input, and
+ * one SGD step updates the fast weights.  Teacher-forced decode of
+ * tokens[0..n_steps] therefore trains exactly like ttt_prefill over those
+ * n_steps + 1 tokens, chunk for chunk.
+ *   tokens:       [n_given] int32 (host or device), 1 <= n_given <= n_steps + 1;
+ *                 tokens[0] is the input at position pos.
+ *   tokens_out:   [n_steps + 1] int32 (host or device): the input token of
+ *                 every step, then the next input after the last step.
+ *   chunk_losses: losses of the chunks completed by this call, in order
+ *                 (at most (n_steps + b - 1) / b + 1 of them).
+ * A chunk left incomplete carries over to the next ttt_decode call.  The
+ * first decode on a context must start at a chunk boundary (pos a multiple
+ * of b: a fresh or reset context, or after ttt_prefill of a multiple of b
+ * tokens), else STATE; pos + n_steps <= max_tokens, else SHAPE.  A non-finite
+ * chunk loss returns NONFINITE with its index within this call.  Returns
+ * after the work has completed on `stream`; pos advances by n_steps. */
+int ttt_decode(ttt_ctx* ctx, const int32_t* tokens, int64_t n_given, int64_t n_steps, int32_t* tokens_out,
+               float* chunk_losses, void* stream);
+
 /* Forward only: logits of a continuation cont[0..n) placed at positions
  * P..P+n-1, where P is the number of positions consumed so far, using the
  * current fast weights and the cached keys/values.  1 <= n <= cfg.chunk.

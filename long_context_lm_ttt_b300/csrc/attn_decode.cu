@@ -1,0 +1,180 @@
+// attn_decode.cu — sliding-window attention of ONE query position (a decode
+// step), split over the key range so that the whole GPU streams the window.
+//
+//   o_h = sum_j softmax_j(q_h . k_j / sqrt(hd)) v_j,   j in [max(0, t-W+1), t]
+//
+// attn_decode_part_kernel: one CTA per (KV head, key slice).  Its four warps
+// take every fourth key of the slice; the G = H / Hkv query heads of the KV
+// group share each key and value row read.  Lane i holds hd / 32 consecutive
+// dimensions.  Each warp keeps an online softmax per query head (running
+// max, sum, unnormalised output); the CTA folds its warps together and
+// writes (max, sum, output) of the slice.
+// attn_decode_combine_kernel: one CTA per query head folds the slices and
+// writes o (row 0) and the log-sum-exp.
+// Scores use log2 units (q.k * log2(e) / sqrt(hd)) and exp2f throughout.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ttt {
+
+namespace {
+
+constexpr int kDecWarps = 4;
+constexpr int kMaxGroup = 8;  // query heads per KV head
+constexpr int kMaxEpl = 8;    // dimensions per lane (hd <= 256)
+
+template <typename T, int EPL>
+__global__ void __launch_bounds__(kDecWarps * 32)
+    attn_decode_part_kernel(const T* __restrict__ q, const T* __restrict__ kring, const T* __restrict__ vring,
+                            int H, int Hkv, int W, int R, int64_t pos, int splits, float scale_log2,
+                            float* __restrict__ part) {
+  constexpr int hd = EPL * 32;
+  const int kvh = blockIdx.x, sp = blockIdx.y;
+  const int G = H / Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t j_lo = pos - W + 1 > 0 ? pos - W + 1 : 0;
+  const int64_t cnt = pos - j_lo + 1;
+  const int64_t s0 = j_lo + cnt * sp / splits, s1 = j_lo + cnt * (sp + 1) / splits;
+
+  float qv[kMaxGroup][EPL];
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+      qv[g][e] = g < G ? to_f<T>(q[(int64_t)(kvh * G + g) * hd + lane * EPL + e]) : 0.f;
+  float m[kMaxGroup], l[kMaxGroup], acc[kMaxGroup][EPL];
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
+  }
+  for (int64_t j = s0 + warp; j < s1; j += kDecWarps) {
+    const int64_t row = (int64_t)kvh * R + j % R;
+    float kv[EPL], vv[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      kv[e] = to_f<T>(kring[row * hd + lane * EPL + e]);
+      vv[e] = to_f<T>(vring[row * hd + lane * EPL + e]);
+    }
+#pragma unroll
+    for (int g = 0; g < kMaxGroup; ++g) {
+      if (g >= G) break;
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) s = fmaf(qv[g][e], kv[e], s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      s *= scale_log2;
+      const float mn = fmaxf(m[g], s);
+      const float alpha = exp2f(m[g] - mn);  // 0 while m is -inf
+      const float p = exp2f(s - mn);
+      l[g] = l[g] * alpha + p;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(acc[g][e], alpha, p * vv[e]);
+      m[g] = mn;
+    }
+  }
+  // fold the four warps: per (query head, dimension)
+  __shared__ float sm[kDecWarps][kMaxGroup], sl[kDecWarps][kMaxGroup];
+  __shared__ float sa[kDecWarps][kMaxGroup][hd];
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g) {
+    if (g >= G) break;
+    if (lane == 0) {
+      sm[warp][g] = m[g];
+      sl[warp][g] = l[g];
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) sa[warp][g][lane * EPL + e] = acc[g][e];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * (hd + 2); idx += blockDim.x) {
+    const int g = idx / (hd + 2), e = idx % (hd + 2);
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm[w][g]);
+    float v = 0.f;
+    if (e == hd) {
+      v = M;
+    } else if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float f = exp2f(sm[w][g] - M);
+        v += f * (e == hd + 1 ? sl[w][g] : sa[w][g][e]);
+      }
+    }
+    part[((int64_t)(kvh * G + g) * splits + sp) * (hd + 2) + e] = v;
+  }
+}
+
+template <typename T>
+__global__ void attn_decode_combine_kernel(const float* __restrict__ part, int hd, int splits, T* __restrict__ o,
+                                           float* __restrict__ lse, int ld_lse) {
+  const int h = blockIdx.x;
+  const float* ph = part + (int64_t)h * splits * (hd + 2);
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, ph[(int64_t)s * (hd + 2) + hd]);
+  float L = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float ms = ph[(int64_t)s * (hd + 2) + hd];
+    if (ms != -INFINITY) L += exp2f(ms - M) * ph[(int64_t)s * (hd + 2) + hd + 1];
+  }
+  const float inv = L > 0.f ? 1.0f / L : 0.f;
+  for (int e = threadIdx.x; e < hd; e += blockDim.x) {
+    float a = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      const float ms = ph[(int64_t)s * (hd + 2) + hd];
+      if (ms != -INFINITY) a += exp2f(ms - M) * ph[(int64_t)s * (hd + 2) + e];
+    }
+    o[(int64_t)h * hd + e] = from_f<T>(a * inv);
+  }
+  if (threadIdx.x == 0 && lse) lse[(int64_t)h * ld_lse] = (M + log2f(L)) * 0.69314718055994531f;
+}
+
+template <typename T, int EPL>
+void launch_part(const AttnArgs& a, int splits, float* part, cudaStream_t st) {
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.hd);
+  attn_decode_part_kernel<T, EPL><<<dim3(a.Hkv, splits), kDecWarps * 32, 0, st>>>(
+      (const T*)a.q, (const T*)a.kring, (const T*)a.vring, a.H, a.Hkv, a.W, a.R, a.pos0, splits, scale_log2, part);
+}
+
+}  // namespace
+
+bool attn_decode_supported(const AttnArgs& a) {
+  return a.n == 1 && a.hd % 32 == 0 && a.hd / 32 <= kMaxEpl && a.H % a.Hkv == 0 && a.H / a.Hkv <= kMaxGroup;
+}
+
+int attn_decode_splits(const AttnArgs& a, int num_sms) {
+  const int64_t keys = std::min<int64_t>(a.pos0 + 1, a.W);
+  // two CTAs per SM over the KV heads, at least 32 keys per slice
+  int s = (2 * num_sms + a.Hkv - 1) / a.Hkv;
+  const int64_t by_keys = (keys + 31) / 32;
+  if (s > by_keys) s = (int)by_keys;
+  return s < 1 ? 1 : (s > kMaxDecodeSplits ? kMaxDecodeSplits : s);
+}
+
+template <typename T>
+void attn_decode(const AttnArgs& a, int splits, float* part, cudaStream_t st) {
+  switch (a.hd / 32) {
+    case 1: launch_part<T, 1>(a, splits, part, st); break;
+    case 2: launch_part<T, 2>(a, splits, part, st); break;
+    case 3: launch_part<T, 3>(a, splits, part, st); break;
+    case 4: launch_part<T, 4>(a, splits, part, st); break;
+    case 5: launch_part<T, 5>(a, splits, part, st); break;
+    case 6: launch_part<T, 6>(a, splits, part, st); break;
+    case 7: launch_part<T, 7>(a, splits, part, st); break;
+    default: launch_part<T, 8>(a, splits, part, st); break;
+  }
+  attn_decode_combine_kernel<T><<<a.H, a.hd, 0, st>>>(part, a.hd, splits, (T*)a.o, a.lse, a.ld_lse);
+}
+
+template void attn_decode<bf16>(const AttnArgs&, int, float*, cudaStream_t);
+template void attn_decode<float>(const AttnArgs&, int, float*, cudaStream_t);
+
+}  // namespace ttt

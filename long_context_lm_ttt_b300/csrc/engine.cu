@@ -95,6 +95,10 @@ struct EngineBase {
   virtual int init(const ttt_weights* w, cudaStream_t st) = 0;
   virtual int prefill(const int32_t* tok, int64_t T, float* losses, cudaStream_t st) = 0;
   virtual int logits(const int32_t* cont, int n, float* out, cudaStream_t st) = 0;
+  virtual int decode(const int32_t* tokens, int64_t n_given, int64_t n_steps, int32_t* tokens_out, float* losses,
+                     cudaStream_t st) = 0;
+  // decode state: rows of the current chunk already decoded
+  int dec_fill = 0;
   virtual int get_fast(int block, int which, float* dst, cudaStream_t st) = 0;
   virtual int reset(cudaStream_t st) = 0;
 
@@ -241,6 +245,15 @@ struct Engine : EngineBase {
   T *dy_t = nullptr, *dgu = nullptr, *dh_t = nullptr, *dO = nullptr, *dqkv = nullptr;
   float* losses_stage = nullptr;
   float* logits_stage = nullptr;
+  // decode (allocated on first use): the fast blocks' input rows of the
+  // current chunk, its tokens (b + 1: the last is the next input), one row
+  // of logits and the tokens of one call
+  float* xdec = nullptr;
+  int32_t* dtok = nullptr;
+  float* dec_z = nullptr;
+  int32_t* dec_out = nullptr;
+  float* dec_part = nullptr;  // one-query attention slices (set while decoding)
+  float* dec_buf = nullptr;
   int* dev_err = nullptr;  // [0] first non-finite chunk, [1] bad token, [2] kernel check
   float* stage32 = nullptr;
   size_t stage32_elems = 0;
@@ -536,6 +549,11 @@ struct Engine : EngineBase {
     const double kv = (double)std::min<int64_t>(a.pos0 + a.n, (int64_t)a.W + a.n - 1) * a.Hkv * a.hd;
     const double bytes = sizeof(T) * (2.0 * a.n * hdH + 2.0 * kv) + 4.0 * a.n * a.H;
     prof(a.n > cfg.chunk ? P_ATTN_FWD_BULK : P_ATTN_FWD, 4.0 * hdH * P, bytes, st, [&] {
+      // a decode step: one query, the window split over the whole GPU
+      if (dec_part && a.n == 1 && attn_decode_supported(a)) {
+        attn_decode<T>(a, attn_decode_splits(a, num_sms), dec_part, st);
+        return;
+      }
       if constexpr (kBF16) {
         if (use_tc_attn && attn_tc_supported(a)) {
           int r = attn_fwd_tc(a, dev_err + 2, st);
@@ -881,6 +899,97 @@ struct Engine : EngineBase {
     return finish(st, "ttt_prefill");
   }
 
+  // Decode-time test-time training: one token per step through every block
+  // with the current weights, then the greedy next token; when a chunk of b
+  // positions is complete, the same test-time step as the prefill's chunk
+  // loop (fast blocks recomputed over the chunk, loss, backward, SGD).
+  int decode(const int32_t* tokens, int64_t n_given, int64_t n_steps, int32_t* tokens_out, float* losses,
+             cudaStream_t st) override {
+    const int b = cfg.chunk, d = cfg.d_model, hd = cfg.head_dim, V = cfg.vocab;
+    const int lo = cfg.n_layers - cfg.n_ttt_layers;
+    if (!tokens || !tokens_out || !losses) {
+      err = "null tokens, tokens_out or chunk_losses";
+      return TTT_ERR_INVALID;
+    }
+    if (n_steps < 1 || n_given < 1 || n_given > n_steps + 1) {
+      err = "need 1 <= n_given <= n_steps + 1";
+      return TTT_ERR_INVALID;
+    }
+    if (pos + n_steps > cfg.max_tokens || n_given > std::max<int64_t>(cfg.max_tokens, b)) {
+      err = "decode past max_tokens";
+      return TTT_ERR_SHAPE;
+    }
+    if (dec_fill == 0 && pos % b != 0) {
+      err = "decode starts at a chunk boundary (a prefill of a multiple of the chunk length)";
+      return TTT_ERR_STATE;
+    }
+    if (!xdec) {
+      A_TRY(xdec, (size_t)b * d);
+      A_TRY(dtok, (size_t)b + 1);
+      A_TRY(dec_z, (size_t)V);
+      A_TRY(dec_out, (size_t)cfg.max_tokens + 1);
+      A_TRY(dec_buf, (size_t)cfg.n_heads * kMaxDecodeSplits * (hd + 2));
+    }
+    const int32_t* given = tokens;
+    if (!is_device_ptr(tokens)) {
+      CU_TRY(cudaMemcpyAsync(tok_stage, tokens, sizeof(int32_t) * n_given, cudaMemcpyHostToDevice, st));
+      given = tok_stage;
+    }
+    const bool host_tok = !is_device_ptr(tokens_out), host_loss = !is_device_ptr(losses);
+    int32_t* tok_d = host_tok ? dec_out : tokens_out;
+    float* loss_d = host_loss ? losses_stage : losses;
+    int rc = clear_err(st);
+    if (rc) return rc;
+    used = true;
+    int done = 0;  // chunks completed by this call
+    for (int64_t i = 0; i < n_steps && rc == TTT_OK; ++i) {
+      const int64_t p = pos;
+      const int r = dec_fill;
+      if (i < n_given) CU_TRY(cudaMemcpyAsync(dtok + r, given + i, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+      dec_part = dec_buf;
+      forward_all(dtok + r, p, 1, st, &rc);
+      dec_part = nullptr;
+      // input row of the first fast block (the embedding if there is none)
+      CU_TRY(cudaMemcpyAsync(xdec + (int64_t)r * d, xlow[lo & 1], sizeof(float) * d, cudaMemcpyDeviceToDevice, st));
+      if (i + 1 < n_given) {
+        CU_TRY(cudaMemcpyAsync(dtok + r + 1, given + i + 1, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+      } else {
+        Epi e = epi(EPI_STORE);
+        e.out_f32 = 1;
+        e.out = dec_z;
+        e.ldo = V;
+        gemm(1, V, d, hf, d, 0, Wlm, d, 0, e, st, &rc);
+        row((double)V * 4, st, [&] { launch_argmax(dec_z, V, dtok + r + 1, st); });
+      }
+      CU_TRY(cudaMemcpyAsync(tok_d + i, dtok + r, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+      pos = p + 1;
+      dec_fill = r + 1;
+      if (dec_fill == b) {
+        // chunk [s, s + b) complete; its targets are dtok[1..b]
+        const int64_t s = p + 1 - b;
+        row((double)b * hd * 4, st, [&] { launch_rope_table(s, b, hd, cfg.rope_theta, cs, st); });
+        fast_fwd(xdec, cs, s, b, st, &rc);
+        cross_entropy(dtok, b + 1, 0, b, b, loss_d, done, st, &rc, cfg.n_ttt_layers > 0);
+        if (cfg.n_ttt_layers > 0) backward(s, b, st, &rc);
+        CU_TRY(cudaMemcpyAsync(dtok, dtok + b, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+        dec_fill = 0;
+        ++done;
+      }
+      CU_TRY(cudaPeekAtLastError());
+    }
+    if (rc) {
+      cudaStreamSynchronize(st);
+      return rc;
+    }
+    // the prediction after the last step (the next input)
+    CU_TRY(cudaMemcpyAsync(tok_d + n_steps, dtok + dec_fill, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    if (host_tok)
+      CU_TRY(cudaMemcpyAsync(tokens_out, tok_d, sizeof(int32_t) * (n_steps + 1), cudaMemcpyDeviceToHost, st));
+    if (host_loss && done > 0)
+      CU_TRY(cudaMemcpyAsync(losses, loss_d, sizeof(float) * done, cudaMemcpyDeviceToHost, st));
+    return finish(st, "ttt_decode");
+  }
+
   int logits(const int32_t* cont, int n, float* out, cudaStream_t st) override {
     if (n < 1 || n > cfg.chunk) {
       err = "n must be in [1, chunk]";
@@ -955,6 +1064,7 @@ struct Engine : EngineBase {
     if (prof_on) prof_collect();
     pos = 0;
     used = false;
+    dec_fill = 0;
     return TTT_OK;
   }
 };
@@ -1092,6 +1202,18 @@ extern "C" int ttt_prefill(ttt_ctx* ctx, const int32_t* tokens, int64_t T, float
     return ctx->eng->prefill(tokens, T, chunk_losses, (cudaStream_t)stream);
   } catch (...) {
     ctx->eng->err = "exception in ttt_prefill";
+    return TTT_ERR_INTERNAL;
+  }
+}
+
+extern "C" int ttt_decode(ttt_ctx* ctx, const int32_t* tokens, int64_t n_given, int64_t n_steps, int32_t* tokens_out,
+                          float* chunk_losses, void* stream) {
+  CTX_GUARD(ctx);
+  ctx->eng->err.clear();
+  try {
+    return ctx->eng->decode(tokens, n_given, n_steps, tokens_out, chunk_losses, (cudaStream_t)stream);
+  } catch (...) {
+    ctx->eng->err = "exception in ttt_decode";
     return TTT_ERR_INTERNAL;
   }
 }

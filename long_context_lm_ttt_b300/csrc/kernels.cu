@@ -206,6 +206,53 @@ __global__ void loss_reduce_kernel(const float* loss_row, int n, float inv_ntgt,
   }
 }
 
+// greedy next token: the index of the largest logit (the smallest such
+// index on ties; NaN logits never win)
+__global__ void argmax_kernel(const float* __restrict__ z, int V, int32_t* out) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  float best = -INFINITY;
+  int bi = V;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    const float v = z[i];
+    if (v > best) {
+      best = v;
+      bi = i;
+    }
+  }
+  // warp, then block: the larger value wins, the smaller index on equal ones
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > best || (ov == best && oi < bi)) {
+      best = ov;
+      bi = oi;
+    }
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    sv[w] = best;
+    si[w] = bi;
+  }
+  __syncthreads();
+  if (w == 0) {
+    const int nw = blockDim.x >> 5;
+    best = l < nw ? sv[l] : -INFINITY;
+    bi = l < nw ? si[l] : V;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > best || (ov == best && oi < bi)) {
+        best = ov;
+        bi = oi;
+      }
+    }
+    if (l == 0) *out = bi < V ? bi : 0;
+  }
+}
+
 __device__ __forceinline__ int64_t map_row(int64_t r, int mode, int hd) {
   switch (mode) {
     case 1: {
@@ -464,6 +511,9 @@ void launch_ce_finalize(int n, const float* m_run, const float* l_run, const flo
                         float* dhf, float* loss_row, cudaStream_t st) {
   if (n > 0)
     ce_finalize_kernel<T><<<n, RB, 0, st>>>(m_run, l_run, ztgt, tgt, inv_ntgt, dh_acc, Wlm, d, dhf, loss_row);
+}
+void launch_argmax(const float* z, int V, int32_t* out, cudaStream_t st) {
+  argmax_kernel<<<1, 1024, 0, st>>>(z, V, out);
 }
 void launch_loss_reduce(const float* loss_row, int n, float inv_ntgt, float* out, int chunk, int* err_chunk,
                         cudaStream_t st) {

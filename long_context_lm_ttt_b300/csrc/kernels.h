@@ -57,6 +57,8 @@ void launch_rope_bwd(T* dqkv, int n, int ld, int n_rot_heads, int hd, const floa
                      cudaStream_t st);
 void launch_targets(const int32_t* tok, int64_t T, int64_t pos0, int n, int32_t* tgt, int V,
                     int* err_tok, cudaStream_t st);
+// out[0] = the index of the largest of z[0..V) (smallest index on ties)
+void launch_argmax(const float* z, int V, int32_t* out, cudaStream_t st);
 template <typename T>
 void launch_ce_slab_stats(const float* z, int64_t ldz, int n, int nv, T* p, int64_t ldp,
                           float* m_run, float* l_run, float* alpha, float* beta, int first,
@@ -98,6 +100,14 @@ struct AttnArgs {
   int64_t ws_elems;   //   (attn_bwd_tc_ws_elems() of the shape)
 };
 template <typename T> void attn_fwd_simt(const AttnArgs& a, cudaStream_t st);
+// one query position (n == 1, a decode step): key range split into `splits`
+// slices (at most kMaxDecodeSplits) folded through fp32 scratch `part` of
+// H * splits * (hd + 2) values; hd a multiple of 32 up to 256, at most 8
+// query heads per KV head
+constexpr int kMaxDecodeSplits = 64;
+bool attn_decode_supported(const AttnArgs& a);
+int attn_decode_splits(const AttnArgs& a, int num_sms);
+template <typename T> void attn_decode(const AttnArgs& a, int splits, float* part, cudaStream_t st);
 template <typename T> void attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
 // tcgen05 kernels (bf16); attn_tc_supported() tells whether the shape and
 // alignment fit them (64 <= hd <= 128, hd % 16 == 0, R % 128 == 0).  They

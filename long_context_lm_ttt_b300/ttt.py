@@ -32,7 +32,7 @@ ERR_NAMES = {0: "OK", -1: "INVALID", -2: "SHAPE", -3: "OOM", -4: "CUDA", -5: "NO
 TTT_BF16 = 0
 TTT_FP32_CHECK = 1
 
-EXPORTS = ("ttt_create", "ttt_prefill", "ttt_logits", "ttt_get_fast_weights", "ttt_reset",
+EXPORTS = ("ttt_create", "ttt_prefill", "ttt_decode", "ttt_logits", "ttt_get_fast_weights", "ttt_reset",
            "ttt_destroy", "ttt_last_error", "ttt_profile", "ttt_profile_read")
 
 
@@ -70,6 +70,8 @@ def load(path: str = LIB_PATH):
     lib.ttt_create.restype = c_int32
     lib.ttt_prefill.argtypes = [c_void_p, c_void_p, c_int64, c_void_p, c_void_p]
     lib.ttt_prefill.restype = c_int32
+    lib.ttt_decode.argtypes = [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p]
+    lib.ttt_decode.restype = c_int32
     lib.ttt_logits.argtypes = [c_void_p, c_void_p, c_int32, c_void_p, c_void_p]
     lib.ttt_logits.restype = c_int32
     lib.ttt_get_fast_weights.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p]
@@ -188,6 +190,13 @@ def ttt_prefill(ctx, tokens, T: int, chunk_losses, stream=None) -> int:
     return rc
 
 
+def ttt_decode(ctx, tokens, n_given: int, n_steps: int, tokens_out, chunk_losses, stream=None) -> int:
+    rc = load().ttt_decode(ctx, _ptr(tokens), int(n_given), int(n_steps), _ptr(tokens_out), _ptr(chunk_losses),
+                           _stream(stream))
+    _check(rc, ctx)
+    return rc
+
+
 def ttt_logits(ctx, cont, n: int, logits, stream=None) -> int:
     rc = load().ttt_logits(ctx, _ptr(cont), int(n), _ptr(logits), _stream(stream))
     _check(rc, ctx)
@@ -279,6 +288,27 @@ class TTT:
                 chunk_losses = torch.zeros(self.n_chunks(T), dtype=torch.float32, device=tokens.device)
         ttt_prefill(self.ctx, tokens, T, chunk_losses, stream)
         return chunk_losses
+
+    def decode(self, tokens, n_steps: int, tokens_out=None, chunk_losses=None, stream=None):
+        """Decode-time test-time training for n_steps positions, inputs
+        given by ``tokens`` while they last, then greedy.  Returns
+        (tokens_out [n_steps + 1], chunk losses of the chunks completed);
+        numpy for host tokens, else CUDA tensors on the tokens' device."""
+        n_given = len(tokens)
+        n_loss = n_steps // self.cfg.chunk + 1
+        if tokens_out is None or chunk_losses is None:
+            if isinstance(tokens, np.ndarray):
+                tokens_out = np.zeros(n_steps + 1, np.int32) if tokens_out is None else tokens_out
+                chunk_losses = np.zeros(n_loss, np.float32) if chunk_losses is None else chunk_losses
+            else:
+                import torch
+                dev = tokens.device
+                if tokens_out is None:
+                    tokens_out = torch.zeros(n_steps + 1, dtype=torch.int32, device=dev)
+                if chunk_losses is None:
+                    chunk_losses = torch.zeros(n_loss, dtype=torch.float32, device=dev)
+        ttt_decode(self.ctx, tokens, n_given, n_steps, tokens_out, chunk_losses, stream)
+        return tokens_out, chunk_losses
 
     def logits(self, cont, out=None, stream=None):
         n = len(cont)

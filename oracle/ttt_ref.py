@@ -360,6 +360,63 @@ def prefill(cfg: OracleConfig, weights: dict, tokens, lr: Optional[float] = None
     return out
 
 
+def decode(cfg: OracleConfig, weights: dict, tokens, n_steps: int, lr: Optional[float] = None,
+           dtype=np.float64, state: Optional[OracleState] = None):
+    """Decode-time test-time training: generation one position at a time,
+    training on every completed chunk.  It starts at position 0, or at
+    ``state.pos`` (a chunk boundary) of a state left by ``prefill``.
+
+    The pages state that the method's latency per token stays constant in
+    the context length, like a recurrent model (summary page, Key claims;
+    podcast page, 5:55): generation keeps the same inner loop, one gradient
+    step per chunk of the tokens read.  Readings taken here:
+      * step i reads input token x_i at position i with the current weights
+        (its keys and values enter the cache) and gives the logits z_i;
+      * the next input is tokens[i + 1] while given, else the greedy choice
+        argmax z_i (the first index on ties);
+      * when position p completes a chunk [p + 1 - b, p + 1), that chunk is
+        trained on exactly as in the prefill (``step_chunk``): its targets
+        are the inputs that followed each position, the last one being the
+        input chosen at step p.
+    So teacher-forced decoding of tokens[0..n_steps] trains like ``prefill``
+    over those n_steps + 1 tokens, chunk for chunk.
+
+    Returns dict(tokens=[n_steps + 1] (the inputs, then the next input after
+    the last step), logits=[n_steps, V] (z_i before any update of the chunk
+    holding i), losses=[completed chunks], fast=final fast weights).
+    """
+    lr = cfg.lr if lr is None else lr
+    tokens = np.asarray(tokens)
+    n_given = len(tokens)
+    assert 1 <= n_given <= n_steps + 1
+    b = cfg.chunk
+    if state is None:
+        st = OracleState(cfg, weights, max_positions=n_steps + 1, dtype=dtype)
+    else:
+        st = state
+        assert st.pos % b == 0
+        grow = st.pos + n_steps + 1 - st.kcache[0].shape[0]
+        if grow > 0:
+            for l in range(cfg.n_layers):
+                st.kcache[l] = np.concatenate([st.kcache[l], np.zeros((grow,) + st.kcache[l].shape[1:], st.dtype)])
+                st.vcache[l] = np.concatenate([st.vcache[l], np.zeros((grow,) + st.vcache[l].shape[1:], st.dtype)])
+    p0 = st.pos
+    seq = np.zeros(p0 + n_steps + 1, np.int64)  # inputs by absolute position
+    seq[p0] = tokens[0]
+    logits, losses = [], []
+    for i in range(n_steps):
+        p = p0 + i
+        z, _ = forward_span(st, seq[p:p + 1], p, write_cache=True)
+        logits.append(z[0])
+        seq[p + 1] = tokens[i + 1] if i + 1 < n_given else int(np.argmax(z[0]))
+        st.pos = p + 1
+        if (p + 1) % b == 0:
+            loss, _ = step_chunk(st, seq[:p + 2], p + 1 - b, p + 1, lr)
+            losses.append(loss)
+    return {"tokens": seq[p0:], "logits": np.array(logits), "losses": np.array(losses, dtype=np.float64),
+            "fast": st.fast_weights()}
+
+
 def logits_after(st: OracleState, cont) -> np.ndarray:
     """Logits of a continuation at positions pos..pos+n-1 with the current
     weights and cache; the state is left unchanged."""

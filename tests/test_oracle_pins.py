@@ -393,3 +393,48 @@ def test_no_fast_blocks_is_a_frozen_model():
     ref = np.array([full[c * b:min(T - 1, (c + 1) * b)].mean() for c in range(-(-T // b))])
     np.testing.assert_allclose(r["losses"], ref, rtol=1e-12, atol=1e-12)
     assert r["fast"] == []
+
+
+# ---------------------------------------------------------------------------
+# decode-time test-time training
+# ---------------------------------------------------------------------------
+def test_teacher_forced_decode_trains_like_prefill():
+    """Reading tokens one position at a time and training on each completed
+    chunk gives the prefill's chunk losses and final fast weights over the
+    same tokens (the prefill's extra last chunk has no target)."""
+    s, cfg, w, tok = _setup("tiny-ttt2")
+    b = s.chunk
+    N = 3 * b
+    d = O.decode(cfg, w, tok[:N + 1], N)
+    r = O.prefill(cfg, w, tok[:N + 1])
+    assert len(d["losses"]) == 3 and len(r["losses"]) == 4 and r["losses"][3] == 0.0
+    np.testing.assert_allclose(d["losses"], r["losses"][:3], rtol=1e-11, atol=0)
+    for a, c in zip(d["fast"], r["fast"]):
+        for k in O.FAST:
+            np.testing.assert_allclose(a[k], c[k], rtol=0, atol=1e-11 * np.abs(c[k]).max())
+    assert np.array_equal(d["tokens"], tok[:N + 1])
+
+
+def test_decode_step_logits_equal_one_unchunked_forward_at_lr0():
+    """With lr = 0 nothing changes the weights, so the logits of every step
+    equal the logits of one forward over the whole sequence."""
+    s, cfg, w, tok = _setup("tiny-gqa", lr=0.0)
+    N = 2 * s.chunk + 9
+    d = O.decode(cfg, w, tok[:N + 1], N)
+    st = O.OracleState(cfg, w, max_positions=N)
+    z, _ = O.forward_span(st, tok[:N], 0)
+    np.testing.assert_allclose(d["logits"], z, rtol=0, atol=1e-10 * np.abs(z).max())
+
+
+def test_greedy_decode_picks_argmax_and_replays():
+    """Greedy steps take the largest logit; feeding the generated tokens back
+    as given inputs reproduces the run exactly."""
+    s, cfg, w, tok = _setup("tiny-ttt2")
+    N = 2 * s.chunk + 10
+    g = O.decode(cfg, w, tok[:5], N)
+    for i in range(4, N):
+        assert g["tokens"][i + 1] == int(np.argmax(g["logits"][i]))
+    assert np.array_equal(g["tokens"][:5], tok[:5])
+    t = O.decode(cfg, w, g["tokens"], N)
+    assert np.array_equal(t["tokens"], g["tokens"])
+    np.testing.assert_array_equal(t["losses"], g["losses"])
