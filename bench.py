@@ -459,6 +459,21 @@ def run_decode(args):
     if not np.all(np.isfinite(loss_d.cpu().numpy()[: nd // b])):
         raise SystemExit("non-finite decode chunk loss")
     e2e_ms = sum(step(host=True)[0] for _ in range(args.steps))
+    # one more decode call with per-launch events (classes as in the
+    # prefill profile; the test-time step of the completed chunk included)
+    kernels = None
+    if args.profile == "timed":
+        m.reset()
+        m.prefill(tok_d[:ctx])
+        torch.cuda.synchronize()
+        m.profile(True)
+        m.decode(tok_d[ctx:ctx + 1], nd, out_d, loss_d)
+        prof = m.profile_read()
+        m.profile(False)
+        tot = sum(v["ms"] for v in prof.values()) or 1.0
+        kernels = {k: {"launches": v["launches"], "ms_per_token": v["ms"] / nd, "share": v["ms"] / tot,
+                       "gbs": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["ms"] > 0 else None}
+                   for k, v in prof.items() if v["launches"]}
     per_tok = dec_ms / args.steps / nd
     bytes_tok = decode_bytes_per_token(s, ctx + nd // 2)
     ach = bytes_tok / (per_tok / 1e3) / 1e9
@@ -480,6 +495,9 @@ def run_decode(args):
                                "steps' time is included, their bytes are not)",
                      "peak_source": f"{peak_src} (copy)"},
     }
+    if kernels is not None:
+        line["kernels"] = kernels
+        line["gpu_launches_per_token"] = sum(v["launches"] for v in kernels.values()) / nd
     m.close()
     print(json.dumps(line), flush=True)
     return 0

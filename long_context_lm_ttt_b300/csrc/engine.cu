@@ -254,6 +254,7 @@ struct Engine : EngineBase {
   int32_t* dec_out = nullptr;
   float* dec_part = nullptr;  // one-query attention slices (set while decoding)
   float* dec_buf = nullptr;
+  int gemm_cls = -1;          // profile class of the next GEMMs, if set
   int* dev_err = nullptr;  // [0] first non-finite chunk, [1] bad token, [2] kernel check
   float* stage32 = nullptr;
   size_t stage32_elems = 0;
@@ -487,6 +488,7 @@ struct Engine : EngineBase {
     // the forward products of the frozen blocks' bulk pass (more rows than a
     // chunk) form their own class
     if (cls == P_GEMM_FWD && M > cfg.chunk) cls = P_GEMM_FWD_BULK;
+    if (gemm_cls >= 0) cls = gemm_cls;
     const double flops = 2.0 * M * N * K;
     const double bytes = (double)sizeof(T) * ((double)M * K + (double)N * K) + out_b;
     int nk = 1;
@@ -958,7 +960,9 @@ struct Engine : EngineBase {
         e.out_f32 = 1;
         e.out = dec_z;
         e.ldo = V;
+        gemm_cls = P_GEMM_LMHEAD;
         gemm(1, V, d, hf, d, 0, Wlm, d, 0, e, st, &rc);
+        gemm_cls = -1;
         row((double)V * 4, st, [&] { launch_argmax(dec_z, V, dtok + r + 1, st); });
       }
       CU_TRY(cudaMemcpyAsync(tok_d + i, dtok + r, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));

@@ -600,6 +600,51 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
   }
 }
 
+// One-row product (M = 1, a decode step): C[0, n] = x . B[n] (+ x . B2[n]).
+// The work is streaming B from HBM once, so it runs on SIMT cores rather
+// than on 128-row tensor-core tiles: one warp per two adjacent output
+// columns, 16-byte loads along K, a warp reduction, then the epilogue of
+// the column pair (the same epi_pair as the GEMM's ragged-column path).
+__device__ __forceinline__ float dot8(uint4 a, uint4 b) {
+  const uint32_t ua[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 fa = unbf2(ua[i]), fb = unbf2(ub[i]);
+    s = fmaf(fa.x, fb.x, s);
+    s = fmaf(fa.y, fb.y, s);
+  }
+  return s;
+}
+
+template <bool DUAL>
+__global__ void __launch_bounds__(256) gemv_row_kernel(const bf16* __restrict__ x, const bf16* __restrict__ B,
+                                                       const bf16* __restrict__ B2, int N, int K, int64_t ldb,
+                                                       Epi e) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = 2 * (blockIdx.x * 8 + warp);
+  if (n >= N) return;
+  const bf16* b0 = B + (int64_t)n * ldb;
+  const bf16* b1 = b0 + ldb;
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
+  for (int k = lane * 8; k < K; k += 256) {
+    const uint4 xv = *reinterpret_cast<const uint4*>(x + k);
+    a0 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(b0 + k)));
+    a1 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(b1 + k)));
+    if (DUAL) {
+      a0 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(B2 + (int64_t)n * ldb + k)));
+      a1 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(B2 + (int64_t)(n + 1) * ldb + k)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+    a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+  }
+  if (lane == 0) epi_pair<bf16>(e, 0, n, a0, a1);
+}
+
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
@@ -801,6 +846,16 @@ int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st, 
   if (kernels) *kernels = 1;
   g.e.vec = epi_vec_ok(g.e) ? 1 : 0;
   if (g.M <= 0 || g.N <= 0) return 0;
+  // one row, K-major operands, 16-byte aligned rows: stream B once
+  if (g.M == 1 && !g.a_mn && !g.b_mn && (g.N & 1) == 0 && (g.K & 7) == 0 && (g.ldb & 7) == 0 && a16(g.A) &&
+      a16(g.B) && (!g.B2 || a16(g.B2))) {
+    const int blocks = (g.N / 2 + 7) / 8;
+    if (g.B2)
+      gemv_row_kernel<true><<<blocks, 256, 0, st>>>(g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e);
+    else
+      gemv_row_kernel<false><<<blocks, 256, 0, st>>>(g.A, g.B, nullptr, g.N, g.K, g.ldb, g.e);
+    return (int)cudaPeekAtLastError();
+  }
   if (!g_encode) return (int)cudaErrorNotSupported;
   // TMA: 16-byte aligned base and row pitch
   if (((uintptr_t)g.A & 15) || ((uintptr_t)g.B & 15) || ((uintptr_t)g.B2 & 15) || (g.lda & 7) ||

@@ -27,7 +27,8 @@ def _operand(rng, rows, cols, mn, bf16=True):
 
 
 SHAPES = [(128, 128, 64), (256, 384, 192), (100, 200, 96), (32, 128, 32), (130, 258, 70),
-          (1024, 3072, 1024), (512, 512, 4096), (520, 640, 200), (300, 136, 1000)]
+          (1024, 3072, 1024), (512, 512, 4096), (520, 640, 200), (300, 136, 1000),
+          (1, 256, 200), (1, 3072, 3072)]
 
 # impl 0: tensor cores, planner's choice; 3: 128-row tiles on one CTA;
 # 4: 256-row tiles on a CTA pair (also for M < 256: the second CTA's rows
@@ -62,10 +63,12 @@ def test_gemm_bf16(M, N, K, a_mn, b_mn, impl):
 
 @pytest.mark.parametrize("impl", [0, 1, 3, 4])
 @pytest.mark.parametrize("b_mn", [0, 1])
-def test_gemm_dual_b(impl, b_mn):
-    """C = A B^T + A B2^T (the hi + lo fast-weight pair)."""
+@pytest.mark.parametrize("M", [200, 1])
+def test_gemm_dual_b(impl, b_mn, M):
+    """C = A B^T + A B2^T (the hi + lo fast-weight pair); M = 1 is the
+    one-row product of a decode step."""
     torch, T = _env()
-    M, N, K = 200, 384, 320
+    N, K = 384, 320
     rng = np.random.default_rng(3)
     a, a_st = _operand(rng, M, K, 0)
     b, b_st = _operand(rng, N, K, b_mn)
