@@ -4,10 +4,13 @@
 //   o_h = sum_j softmax_j(q_h . k_j / sqrt(hd)) v_j,   j in [max(0, t-W+1), t]
 //
 // attn_decode_part_kernel: one CTA per (KV head, key slice).  Its four warps
-// take every fourth key of the slice; the G = H / Hkv query heads of the KV
-// group share each key and value row read.  Lane i holds hd / 32 consecutive
-// dimensions.  Each warp keeps an online softmax per query head (running
-// max, sum, unnormalised output); the CTA folds its warps together and
+// take every fourth tile of 32 keys of the slice; the G = H / Hkv query
+// heads of the KV group share each key and value row read.  For the scores
+// lane j reads key j of the tile (its whole row, 16 bytes at a time), so a
+// warp has 32 rows in flight; for P.V lane i holds hd / 32 consecutive
+// output dimensions and the probabilities come by shuffle.  Each warp keeps
+// an online softmax per query head (running max, sum, unnormalised
+// output), updated once per tile; the CTA folds its warps together and
 // writes (max, sum, output) of the slice.
 // attn_decode_combine_kernel: one CTA per query head folds the slices and
 // writes o (row 0) and the log-sum-exp.
@@ -40,12 +43,12 @@ __global__ void __launch_bounds__(kDecWarps * 32)
   const int64_t cnt = pos - j_lo + 1;
   const int64_t s0 = j_lo + cnt * sp / splits, s1 = j_lo + cnt * (sp + 1) / splits;
 
-  float qv[kMaxGroup][EPL];
-#pragma unroll
-  for (int g = 0; g < kMaxGroup; ++g)
-#pragma unroll
-    for (int e = 0; e < EPL; ++e)
-      qv[g][e] = g < G ? to_f<T>(q[(int64_t)(kvh * G + g) * hd + lane * EPL + e]) : 0.f;
+  // the group's query rows, scaled into log2 units, shared by every lane
+  __shared__ float sq[kMaxGroup][hd];
+  for (int i = threadIdx.x; i < G * hd; i += blockDim.x)
+    sq[i / hd][i % hd] = to_f<T>(q[(int64_t)kvh * G * hd + i]) * scale_log2;
+  __syncthreads();
+
   float m[kMaxGroup], l[kMaxGroup], acc[kMaxGroup][EPL];
 #pragma unroll
   for (int g = 0; g < kMaxGroup; ++g) {
@@ -54,30 +57,76 @@ __global__ void __launch_bounds__(kDecWarps * 32)
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
   }
-  for (int64_t j = s0 + warp; j < s1; j += kDecWarps) {
-    const int64_t row = (int64_t)kvh * R + j % R;
-    float kv[EPL], vv[EPL];
+  // tiles of 32 keys: lane j scores key kb + j over the whole head
+  // dimension, then the lanes own EPL output dimensions for P.V
+  for (int64_t kb = s0 + 32 * warp; kb < s1; kb += 32 * kDecWarps) {
+    const int64_t k = kb + lane;
+    const bool valid = k < s1;
+    float sc[kMaxGroup];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      kv[e] = to_f<T>(kring[row * hd + lane * EPL + e]);
-      vv[e] = to_f<T>(vring[row * hd + lane * EPL + e]);
+    for (int g = 0; g < kMaxGroup; ++g) sc[g] = 0.f;
+    if (valid) {
+      const T* kr = kring + ((int64_t)kvh * R + k % R) * hd;
+#pragma unroll
+      for (int c = 0; c < hd; c += 16 / (int)sizeof(T)) {
+        float kv[16 / sizeof(T)];
+        if constexpr (sizeof(T) == 2) {
+          const uint4 u = *reinterpret_cast<const uint4*>(kr + c);
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float2 f = unbf2(w4[t]);
+            kv[2 * t] = f.x;
+            kv[2 * t + 1] = f.y;
+          }
+        } else {
+          const float4 f = *reinterpret_cast<const float4*>(kr + c);
+          kv[0] = f.x;
+          kv[1] = f.y;
+          kv[2] = f.z;
+          kv[3] = f.w;
+        }
+#pragma unroll
+        for (int g = 0; g < kMaxGroup; ++g) {
+          if (g >= G) break;
+#pragma unroll
+          for (int t = 0; t < (int)(16 / sizeof(T)); ++t) sc[g] = fmaf(sq[g][c + t], kv[t], sc[g]);
+        }
+      }
     }
+    float p[kMaxGroup];
 #pragma unroll
     for (int g = 0; g < kMaxGroup; ++g) {
       if (g >= G) break;
-      float s = 0.f;
+      const float s = valid ? sc[g] : -INFINITY;
+      float mt = s;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) s = fmaf(qv[g][e], kv[e], s);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      s *= scale_log2;
-      const float mn = fmaxf(m[g], s);
+      for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+      const float mn = fmaxf(m[g], mt);
       const float alpha = exp2f(m[g] - mn);  // 0 while m is -inf
-      const float p = exp2f(s - mn);
-      l[g] = l[g] * alpha + p;
+      p[g] = exp2f(s - mn);
+      float ps = p[g];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(acc[g][e], alpha, p * vv[e]);
+      for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      l[g] = l[g] * alpha + ps;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[g][e] *= alpha;
       m[g] = mn;
+    }
+    const int nk = s1 - kb < 32 ? (int)(s1 - kb) : 32;
+#pragma unroll 4
+    for (int jj = 0; jj < nk; ++jj) {
+      const T* vr = vring + ((int64_t)kvh * R + (kb + jj) % R) * hd + lane * EPL;
+      float vv[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) vv[e] = to_f<T>(vr[e]);
+#pragma unroll
+      for (int g = 0; g < kMaxGroup; ++g) {
+        if (g >= G) break;
+        const float pj = __shfl_sync(0xffffffffu, p[g], jj);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pj, vv[e], acc[g][e]);
+      }
     }
   }
   // fold the four warps: per (query head, dimension)

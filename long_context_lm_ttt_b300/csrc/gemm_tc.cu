@@ -617,24 +617,33 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b) {
   return s;
 }
 
-template <bool DUAL>
+// KS warps share one column pair, each over a K range of its own, and their
+// sums are added in a fixed order (KS > 1 when there are too few column
+// pairs to give every SM several blocks).
+template <bool DUAL, int KS>
 __global__ void __launch_bounds__(256) gemv_row_kernel(const bf16* __restrict__ x, const bf16* __restrict__ B,
                                                        const bf16* __restrict__ B2, int N, int K, int64_t ldb,
                                                        Epi e) {
+  constexpr int RP = 8 / KS;  // column pairs per block
+  __shared__ float red[8][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = 2 * (blockIdx.x * 8 + warp);
-  if (n >= N) return;
-  const bf16* b0 = B + (int64_t)n * ldb;
-  const bf16* b1 = b0 + ldb;
+  const int rp = warp / KS, ks = warp % KS;
+  const int n = 2 * (blockIdx.x * RP + rp);
+  const int kchunk = ((K / 8 + KS - 1) / KS) * 8;
+  const int k0 = ks * kchunk, k1 = min(K, k0 + kchunk);
   float a0 = 0.f, a1 = 0.f;
+  if (n < N) {
+    const bf16* b0 = B + (int64_t)n * ldb;
+    const bf16* b1 = b0 + ldb;
 #pragma unroll 4
-  for (int k = lane * 8; k < K; k += 256) {
-    const uint4 xv = *reinterpret_cast<const uint4*>(x + k);
-    a0 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(b0 + k)));
-    a1 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(b1 + k)));
-    if (DUAL) {
-      a0 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(B2 + (int64_t)n * ldb + k)));
-      a1 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(B2 + (int64_t)(n + 1) * ldb + k)));
+    for (int k = k0 + lane * 8; k < k1; k += 256) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(x + k);
+      a0 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(b0 + k)));
+      a1 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(b1 + k)));
+      if (DUAL) {
+        a0 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(B2 + (int64_t)n * ldb + k)));
+        a1 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(B2 + (int64_t)(n + 1) * ldb + k)));
+      }
     }
   }
 #pragma unroll
@@ -642,7 +651,40 @@ __global__ void __launch_bounds__(256) gemv_row_kernel(const bf16* __restrict__ 
     a0 += __shfl_xor_sync(0xffffffffu, a0, o);
     a1 += __shfl_xor_sync(0xffffffffu, a1, o);
   }
-  if (lane == 0) epi_pair<bf16>(e, 0, n, a0, a1);
+  if (KS == 1) {
+    if (lane == 0 && n < N) epi_pair<bf16>(e, 0, n, a0, a1);
+    return;
+  }
+  if (lane == 0) {
+    red[warp][0] = a0;
+    red[warp][1] = a1;
+  }
+  __syncthreads();
+  if (ks == 0 && lane == 0 && n < N) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int t = 0; t < KS; ++t) {
+      s0 += red[warp + t][0];
+      s1 += red[warp + t][1];
+    }
+    epi_pair<bf16>(e, 0, n, s0, s1);
+  }
+}
+
+template <bool DUAL>
+void launch_gemv(const GemmArgs<bf16>& g, int num_sms, cudaStream_t st) {
+  // enough blocks for about four per SM
+  const int64_t want = 4ll * num_sms;
+  int ks = 1;
+  while (ks < 8 && (int64_t)(g.N / 2) * ks / 8 < want) ks *= 2;
+  const int rp = 8 / ks;
+  const int blocks = (g.N / 2 + rp - 1) / rp;
+  switch (ks) {
+    case 1: gemv_row_kernel<DUAL, 1><<<blocks, 256, 0, st>>>(g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
+    case 2: gemv_row_kernel<DUAL, 2><<<blocks, 256, 0, st>>>(g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
+    case 4: gemv_row_kernel<DUAL, 4><<<blocks, 256, 0, st>>>(g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
+    default: gemv_row_kernel<DUAL, 8><<<blocks, 256, 0, st>>>(g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -849,11 +891,10 @@ int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st, 
   // one row, K-major operands, 16-byte aligned rows: stream B once
   if (g.M == 1 && !g.a_mn && !g.b_mn && (g.N & 1) == 0 && (g.K & 7) == 0 && (g.ldb & 7) == 0 && a16(g.A) &&
       a16(g.B) && (!g.B2 || a16(g.B2))) {
-    const int blocks = (g.N / 2 + 7) / 8;
     if (g.B2)
-      gemv_row_kernel<true><<<blocks, 256, 0, st>>>(g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e);
+      launch_gemv<true>(g, num_sms, st);
     else
-      gemv_row_kernel<false><<<blocks, 256, 0, st>>>(g.A, g.B, nullptr, g.N, g.K, g.ldb, g.e);
+      launch_gemv<false>(g, num_sms, st);
     return (int)cudaPeekAtLastError();
   }
   if (!g_encode) return (int)cudaErrorNotSupported;
