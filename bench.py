@@ -67,6 +67,8 @@ def parse_args():
                     help="tokens the oracle is timed on (default: one chunk; 128 at 3B)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--dual-mlp", action="store_true",
+                    help="fast blocks carry a static second MLP after the fast one")
     ap.add_argument("--mode", choices=["prefill", "decode"], default="prefill")
     ap.add_argument("--context", type=int, default=None,
                     help="decode: tokens prefilled before decoding (default 8 chunks)")
@@ -166,13 +168,16 @@ def workload(args, rank=0):
         s = s.replace(window=args.window)
     if args.fast_layers is not None:
         s = s.replace(n_ttt_layers=args.fast_layers)
+    if args.dual_mlp:
+        s = s.replace(dual_mlp=True)
     tok = inputs.make_tokens(s, seed=1 + rank)
     return s, tok
 
 
 def workload_name(s):
     return (f"{s.name} TTT-E2E prefill: L={s.n_layers} d={s.d_model} H={s.n_heads}/{s.n_kv_heads}x{s.head_dim} "
-            f"ff={s.d_ff} V={s.vocab} W={s.window} b={s.chunk} T={s.seq_len} fast={s.n_ttt_layers} lr={s.lr}")
+            f"ff={s.d_ff} V={s.vocab} W={s.window} b={s.chunk} T={s.seq_len} fast={s.n_ttt_layers} lr={s.lr}"
+            + (" dual-MLP fast blocks" if s.dual_mlp else ""))
 
 
 def cpu_baseline(s, w, tok, n_tokens):

@@ -62,12 +62,16 @@ enum {
  *   full-attention Transformer with window >= T), precision
  *   (TTT_BF16 | TTT_FP32_CHECK), lr (SGD step), rope_theta, norm_eps,
  *   max_tokens (longest sequence ttt_prefill will be given; sizes the
- *   device staging of host token arrays).                                   */
+ *   device staging of host token arrays), dual_mlp (0 or 1: each fast block
+ *   carries a second, static SwiGLU MLP after its fast one, with its own
+ *   pre-norm and residual: y = h2 + MLP2(n(h2)), h2 = h + MLP_fast(n(h));
+ *   podcast page, 7:08).                                                    */
 typedef struct ttt_config {
   int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, d_ff, vocab;
   int32_t window, chunk, n_ttt_layers, precision;
   float lr, rope_theta, norm_eps;
   int64_t max_tokens;
+  int32_t dual_mlp;
 } ttt_config;
 
 /* Initial weights, fp32 values (host or device).  Per-layer fields are
@@ -85,6 +89,13 @@ typedef struct ttt_weights {
   const float* const* w_gate;    /* [d_ff, d]  */
   const float* const* w_up;      /* [d_ff, d]  */
   const float* const* w_down;    /* [d, d_ff]  */
+  /* dual_mlp only: the static second MLP of each fast block (entries of
+   * other blocks are ignored and may be NULL; the arrays may be NULL when
+   * dual_mlp is 0) */
+  const float* const* mlp2_norm; /* [d]        */
+  const float* const* w_gate2;   /* [d_ff, d]  */
+  const float* const* w_up2;     /* [d_ff, d]  */
+  const float* const* w_down2;   /* [d, d_ff]  */
 } ttt_weights;
 
 typedef struct ttt_ctx ttt_ctx;

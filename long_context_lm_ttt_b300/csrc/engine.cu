@@ -198,6 +198,9 @@ struct Engine : EngineBase {
     float *wgu32_init = nullptr, *wd32_init = nullptr;  // for ttt_reset
     T *kring = nullptr, *vring = nullptr;
     int R = 0;  // ring slots
+    // dual_mlp, fast blocks: the static second MLP (after the fast one)
+    float* g_mlp2 = nullptr;
+    T *wgu2 = nullptr, *wd2 = nullptr;
   };
   struct Stash {
     float* x = nullptr;  // layer input (fp32)
@@ -212,6 +215,11 @@ struct Engine : EngineBase {
     T* gu = nullptr;
     T* a = nullptr;
     int ld_lse = 0;
+    // dual_mlp, fast blocks: input and norm statistics of the static second
+    // MLP and its (gate, up) pairs
+    float* h2 = nullptr;
+    float* r3 = nullptr;
+    T* gu2 = nullptr;
   };
   std::vector<Layer> layers;
   std::vector<Stash> fstash;  // fast blocks
@@ -243,6 +251,10 @@ struct Engine : EngineBase {
   T* p_slab = nullptr;
   float *dy = nullptr, *dhn = nullptr, *dh = nullptr, *dxn = nullptr, *Dsum = nullptr;
   T *dy_t = nullptr, *dgu = nullptr, *dh_t = nullptr, *dO = nullptr, *dqkv = nullptr;
+  // dual_mlp: the static MLP's normed input and activation (forward
+  // temporaries) and the gradient at its input (backward)
+  T *hn2 = nullptr, *a2 = nullptr, *dy2_t = nullptr;
+  float* dy2 = nullptr;
   float* losses_stage = nullptr;
   float* logits_stage = nullptr;
   // decode (allocated on first use): the fast blocks' input rows of the
@@ -382,6 +394,19 @@ struct Engine : EngineBase {
                                cudaMemcpyDeviceToDevice, st));
         CU_TRY(cudaMemcpyAsync(y.wd32_init, y.wd32, sizeof(float) * (size_t)d * ff,
                                cudaMemcpyDeviceToDevice, st));
+        if (cfg.dual_mlp) {
+          if (!w->mlp2_norm || !w->w_gate2 || !w->w_up2 || !w->w_down2) {
+            err = "dual_mlp needs mlp2_norm, w_gate2, w_up2 and w_down2";
+            return TTT_ERR_INVALID;
+          }
+          A_TRY(y.g_mlp2, d);
+          A_TRY(y.wgu2, (size_t)2 * ff * d);
+          A_TRY(y.wd2, (size_t)d * ff);
+          if ((rc = upload<float>(w->mlp2_norm[l], 1, d, 0, y.g_mlp2, st))) return rc;
+          if ((rc = upload<T>(w->w_gate2[l], ff, d, 2, y.wgu2, st))) return rc;
+          if ((rc = upload<T>(w->w_up2[l], ff, d, 3, y.wgu2, st))) return rc;
+          if ((rc = upload<T>(w->w_down2[l], d, ff, 0, y.wd2, st))) return rc;
+        }
       }
     }
     // activations of one chunk
@@ -396,6 +421,11 @@ struct Engine : EngineBase {
       A_TRY(s.r2, rows);
       A_TRY(s.a, (size_t)rows * ff);
       if (fast) A_TRY(s.gu, (size_t)rows * 2 * ff);
+      if (fast && cfg.dual_mlp) {
+        A_TRY(s.h2, (size_t)rows * d);
+        A_TRY(s.r3, rows);
+        A_TRY(s.gu2, (size_t)rows * 2 * ff);
+      }
       s.ld_lse = rows;
       return TTT_OK;
     };
@@ -453,6 +483,12 @@ struct Engine : EngineBase {
     A_TRY(dqkv, (size_t)b * qkv_cols);
     A_TRY(dxn, (size_t)b * d);
     A_TRY(Dsum, (size_t)H * b);
+    if (cfg.dual_mlp && Lt > 0) {
+      A_TRY(hn2, (size_t)b * d);
+      A_TRY(a2, (size_t)b * ff);
+      A_TRY(dy2, (size_t)b * d);
+      A_TRY(dy2_t, (size_t)b * d);
+    }
     if (kBF16 && use_tc_gemm) {
       gemm_ws_elems = (int64_t)4 * b * std::max<int64_t>(std::max<int64_t>(d, qkv_cols), Hhd);
       A_TRY(gemm_ws, (size_t)gemm_ws_elems);
@@ -632,12 +668,29 @@ struct Engine : EngineBase {
     // fast weights in bf16 mode are read as the pair hi + lo, so updates
     // below one bf16 ulp still reach the forward
     gemm(n, 2 * ff, d, S.hn, d, 0, y.wgu, d, 0, e, st, rc, y.wgu_lo);
+    const bool dual = fast && cfg.dual_mlp;
     e = epi(EPI_RESID);
-    e.out = x_out;
+    e.out = dual ? S.h2 : x_out;
     e.ldo = d;
     e.resid = S.h;
     e.ldr = d;
     gemm(n, d, ff, S.a, ff, 0, y.wd, ff, 0, e, st, rc, y.wd_lo);
+    if (dual) {
+      // the static second MLP: x_out = h2 + Wd2 (silu(Wg2 n(h2)) * Wu2 n(h2))
+      row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(S.h2, y.g_mlp2, n, d, cfg.norm_eps, hn2, S.r3, st); });
+      e = epi(EPI_SWIGLU);
+      e.out = a2;
+      e.ldo = ff;
+      e.stash = S.gu2;
+      e.ld_stash = 2 * (int64_t)ff;
+      gemm(n, 2 * ff, d, hn2, d, 0, y.wgu2, d, 0, e, st, rc);
+      e = epi(EPI_RESID);
+      e.out = x_out;
+      e.ldo = d;
+      e.resid = S.h2;
+      e.ldr = d;
+      gemm(n, d, ff, a2, ff, 0, y.wd2, ff, 0, e, st, rc);
+    }
   }
 
   // static blocks over a super-chunk [s0, s0+n): embedding, blocks
@@ -738,13 +791,33 @@ struct Engine : EngineBase {
     for (int l = L - 1; l >= lo; --l) {
       Stash& S = fstash[l - lo];
       Layer& y = layers[l];
+      // gradient at the fast MLP's output: dy, or with dual_mlp the one at
+      // the static second MLP's input h2 = dy + n'(h2)^T ([dg2 du2] [Wg2; Wu2])
+      float* gy = dy;
+      T* gy_t = dy_t;
+      if (cfg.dual_mlp) {
+        Epi e2 = epi(EPI_SWIGLU_BWD);
+        e2.out = dgu;
+        e2.ldo = 2 * (int64_t)ff;
+        e2.stash = S.gu2;
+        e2.ld_stash = 2 * (int64_t)ff;
+        gemm(n, ff, d, dy_t, d, 0, y.wd2, ff, 1, e2, st, rc);
+        e2 = epi(EPI_STORE);
+        e2.out_f32 = 1;
+        e2.out = dhn;
+        e2.ldo = d;
+        gemm(n, d, 2 * ff, dgu, 2 * (int64_t)ff, 0, y.wgu2, d, 1, e2, st, rc);
+        row((double)n * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.h2, y.g_mlp2, S.r3, dhn, dy, n, d, dy2, dy2_t, st); });
+        gy = dy2;
+        gy_t = dy2_t;
+      }
       // da = dy Wd  ->  (dg, du) with the stashed (g, u)
       Epi e = epi(EPI_SWIGLU_BWD);
       e.out = dgu;
       e.ldo = 2 * (int64_t)ff;
       e.stash = S.gu;
       e.ld_stash = 2 * (int64_t)ff;
-      gemm(n, ff, d, dy_t, d, 0, y.wd, ff, 1, e, st, rc);
+      gemm(n, ff, d, gy_t, d, 0, y.wd, ff, 1, e, st, rc);
       if (l > lo) {
         // dhn = [dg du] [Wg; Wu]
         e = epi(EPI_STORE);
@@ -760,7 +833,7 @@ struct Engine : EngineBase {
       e.w16lo = y.wd_lo;
       e.ldo = ff;
       e.lr = cfg.lr;
-      gemm(d, ff, n, dy_t, d, 1, S.a, ff, 1, e, st, rc);
+      gemm(d, ff, n, gy_t, d, 1, S.a, ff, 1, e, st, rc);
       e.w32 = y.wgu32;
       e.w16 = kBF16 ? (void*)y.wgu : nullptr;
       e.w16lo = y.wgu_lo;
@@ -768,7 +841,7 @@ struct Engine : EngineBase {
       gemm(2 * ff, d, n, dgu, 2 * (int64_t)ff, 1, S.hn, d, 1, e, st, rc);
       if (l == lo) break;
       // through the MLP norm and the residual
-      row((double)n * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.h, y.g_mlp, S.r2, dhn, dy, n, d, dh, dh_t, st); });
+      row((double)n * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.h, y.g_mlp, S.r2, dhn, gy, n, d, dh, dh_t, st); });
       // dO = dh Wo
       e = epi(EPI_STORE);
       e.out = dO;
@@ -1095,6 +1168,10 @@ static int validate(const ttt_config* c, std::string& msg) {
   }
   if (c->n_ttt_layers > c->n_layers) {
     msg = "n_ttt_layers > n_layers";
+    return TTT_ERR_INVALID;
+  }
+  if (c->dual_mlp != 0 && c->dual_mlp != 1) {
+    msg = "dual_mlp must be 0 or 1";
     return TTT_ERR_INVALID;
   }
   if (c->n_heads % c->n_kv_heads) {

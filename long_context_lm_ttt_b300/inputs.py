@@ -14,7 +14,8 @@ weights in the MLPs of the last quarter of the blocks (the podcast page, the
 Recipe:
   * weights: tensor number k in the fixed order
       tok_embed, then per block (attn_norm, wq, wk, wv, wo, mlp_norm,
-      w_gate, w_up, w_down), then final_norm, lm_head
+      w_gate, w_up, w_down), then final_norm, lm_head, then (dual-MLP
+      shapes only) per fast block (mlp2_norm, w_gate2, w_up2, w_down2)
     is default_rng([seed, k]).standard_normal(shape, float32) * 0.02;
     norm gains are ones (they still take their index k).  With
     ``bf16=True`` every value is rounded to the nearest bfloat16
@@ -55,6 +56,9 @@ class ModelShape:
     tokens: str = "zipf"          # "uniform" | "zipf"
     rope_theta: float = 10000.0
     norm_eps: float = 1e-6
+    # fast blocks carry a second, static MLP after the fast one (podcast
+    # page, 7:08)
+    dual_mlp: bool = False
 
     def replace(self, **kw) -> "ModelShape":
         return dataclasses.replace(self, **kw)
@@ -98,6 +102,8 @@ def shape(name: str, **overrides) -> ModelShape:
 # weights
 # --------------------------------------------------------------------------
 LAYER_TENSORS = ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down")
+# the static second MLP of a fast block (dual-MLP shapes)
+LAYER2_TENSORS = ("mlp2_norm", "w_gate2", "w_up2", "w_down2")
 
 
 def _layer_shapes(s: ModelShape) -> Dict[str, tuple]:
@@ -143,6 +149,13 @@ def weight_plan(s: ModelShape) -> List[tuple]:
             k += 1
     plan.append((k, ("final_norm",), (s.d_model,), True))
     plan.append((k + 1, ("lm_head",), (s.vocab, s.d_model), False))
+    k += 2
+    if s.dual_mlp:
+        for l in range(s.n_layers - s.n_ttt_layers, s.n_layers):
+            for name in LAYER2_TENSORS:
+                plan.append((k, ("layers", l, name), ls[name[:-1] if name != "mlp2_norm" else "mlp_norm"],
+                             name.endswith("norm")))
+                k += 1
     return plan
 
 
@@ -223,6 +236,8 @@ def flops_per_sequence(s: ModelShape, T: Optional[int] = None) -> Dict[str, floa
         tt = np.arange(n, dtype=np.float64)
         P_local += float(np.minimum(tt + 1, W).sum())
     fwd = 2.0 * (n_attn + n_mlp) * L * T + 2.0 * d * V * T + 4.0 * L * H * hd * P
+    if s.dual_mlp:
+        fwd += 2.0 * n_mlp * Lt * T
     if Lt == 0:  # no fast blocks: the chunks are only scored
         return {"fwd": fwd, "bwd": 0.0, "total": fwd}
     bwd = (2.0 * d * V * T                                    # d hidden from lm_head
@@ -231,4 +246,6 @@ def flops_per_sequence(s: ModelShape, T: Optional[int] = None) -> Dict[str, floa
            + (Lt - 1) * (6.0 * H * hd * P + 4.0 * H * hd * P_local))
     # the lowest fast block still needs dX of its down projection (da = dy Wd)
     bwd += 2.0 * d * ff * T
+    if s.dual_mlp:  # dX through every static second MLP
+        bwd += 2.0 * Lt * n_mlp * T
     return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}

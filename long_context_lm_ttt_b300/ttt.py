@@ -41,13 +41,15 @@ class ttt_config(ctypes.Structure):
                 ("n_kv_heads", c_int32), ("head_dim", c_int32), ("d_ff", c_int32),
                 ("vocab", c_int32), ("window", c_int32), ("chunk", c_int32),
                 ("n_ttt_layers", c_int32), ("precision", c_int32), ("lr", c_float),
-                ("rope_theta", c_float), ("norm_eps", c_float), ("max_tokens", c_int64)]
+                ("rope_theta", c_float), ("norm_eps", c_float), ("max_tokens", c_int64),
+                ("dual_mlp", c_int32)]
 
 
 class ttt_weights(ctypes.Structure):
     _fields_ = [("tok_embed", c_void_p), ("final_norm", c_void_p), ("lm_head", c_void_p)] + [
         (name, POINTER(c_void_p)) for name in
-        ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down")]
+        ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down",
+         "mlp2_norm", "w_gate2", "w_up2", "w_down2")]
 
 
 class ttt_kernel_stat(ctypes.Structure):
@@ -154,7 +156,8 @@ def make_config(shape, precision: int = TTT_BF16, max_tokens: Optional[int] = No
     return ttt_config(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads, shape.head_dim,
                       shape.d_ff, shape.vocab, shape.window, shape.chunk, shape.n_ttt_layers, precision,
                       shape.lr if lr is None else lr, shape.rope_theta, shape.norm_eps,
-                      max_tokens if max_tokens is not None else shape.seq_len)
+                      max_tokens if max_tokens is not None else shape.seq_len,
+                      1 if getattr(shape, "dual_mlp", False) else 0)
 
 
 def make_weights(w: dict):
@@ -164,7 +167,7 @@ def make_weights(w: dict):
     layers = w["layers"]
 
     def arr(name):
-        a = (c_void_p * len(layers))(*[_ptr(lw[name]) for lw in layers])
+        a = (c_void_p * len(layers))(*[_ptr(lw.get(name)) for lw in layers])
         keep.append(a)
         return ctypes.cast(a, POINTER(c_void_p))
 
@@ -174,7 +177,8 @@ def make_weights(w: dict):
                 raise TypeError("weights must be float32")
     s = ttt_weights(_ptr(w["tok_embed"]), _ptr(w["final_norm"]), _ptr(w["lm_head"]),
                     arr("attn_norm"), arr("wq"), arr("wk"), arr("wv"), arr("wo"), arr("mlp_norm"),
-                    arr("w_gate"), arr("w_up"), arr("w_down"))
+                    arr("w_gate"), arr("w_up"), arr("w_down"),
+                    arr("mlp2_norm"), arr("w_gate2"), arr("w_up2"), arr("w_down2"))
     return s, keep
 
 

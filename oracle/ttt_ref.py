@@ -64,6 +64,7 @@ class OracleConfig:
     lr: float
     rope_theta: float = 10000.0
     norm_eps: float = 1e-6
+    dual_mlp: bool = False
 
     @classmethod
     def from_mapping(cls, m) -> "OracleConfig":
@@ -219,6 +220,16 @@ def forward_span(st: OracleState, tok_span, s, write_cache=True, keep=None):
         if l in keep:
             acts[l] = dict(x=x, xn=xn, r1=r1, qr=qr, kw=kw, vw=vw, P=P, o=of, h=h, hn=hn,
                            r2=r2, gp=gp, up=up, a=a, v=v)
+        if cfg.dual_mlp and l >= cfg.n_layers - cfg.n_ttt_layers:
+            # the fast block's static second MLP, after the fast one, with
+            # its own pre-norm and residual
+            h2 = y
+            hn2, r3 = rmsnorm(h2, lw["mlp2_norm"], cfg.norm_eps)
+            gp2 = hn2 @ lw["w_gate2"].T
+            up2 = hn2 @ lw["w_up2"].T
+            y = h2 + (silu(gp2) * up2) @ lw["w_down2"].T
+            if l in keep:
+                acts[l].update(h2=h2, r3=r3, gp2=gp2, up2=up2)
         x = y
     hf, rf = rmsnorm(x, st.final_norm, cfg.norm_eps)
     z = hf @ st.lm_head.T
@@ -269,6 +280,15 @@ def backward_chunk(st: OracleState, z, acts, valid, tgt, n_tgt):
     n_cached = s - lo                       # keys before the chunk: constants
     for l in range(L - 1, L - Lt - 1, -1):
         lw, A = st.layers[l], acts[l]
+        if cfg.dual_mlp:
+            # y = h2 + a2 Wd2^T with a2 = silu(n(h2) Wg2^T) * (n(h2) Wu2^T):
+            # the static MLP's input gradient, then dy is the one at h2
+            da2 = dy @ lw["w_down2"]
+            sg2 = sigmoid(A["gp2"])
+            dgp2 = da2 * A["up2"] * (sg2 * (1.0 + A["gp2"] * (1.0 - sg2)))
+            dup2 = da2 * A["gp2"] * sg2
+            dhn2 = dgp2 @ lw["w_gate2"] + dup2 @ lw["w_up2"]
+            dy = dy + rmsnorm_bwd(A["h2"], lw["mlp2_norm"], A["r3"], dhn2)
         # y = h + a Wd^T
         da = dy @ lw["w_down"]
         g_down = dy.T @ A["a"]

@@ -39,9 +39,12 @@ def test_exports_every_declared_call(lib):
 
 
 def test_struct_layout():
-    assert ctypes.sizeof(T.ttt_config) == 11 * 4 + 3 * 4 + 8
+    # 11 int32, 3 float, int64 max_tokens, int32 dual_mlp (+ 4 bytes of tail
+    # padding to the int64 alignment), as the C declaration lays them out
+    assert ctypes.sizeof(T.ttt_config) == 11 * 4 + 3 * 4 + 8 + 8
     assert T.ttt_config.max_tokens.offset == 56
-    assert ctypes.sizeof(T.ttt_weights) == 12 * ctypes.sizeof(ctypes.c_void_p)
+    assert T.ttt_config.dual_mlp.offset == 64
+    assert ctypes.sizeof(T.ttt_weights) == 16 * ctypes.sizeof(ctypes.c_void_p)
 
 
 def _cfg(**kw):
@@ -56,6 +59,7 @@ def _cfg(**kw):
     (dict(n_layers=0), T.TTT_ERR_INVALID),
     (dict(n_ttt_layers=3), T.TTT_ERR_INVALID),
     (dict(n_ttt_layers=-1), T.TTT_ERR_INVALID),
+    (dict(dual_mlp=2), T.TTT_ERR_INVALID),
     (dict(n_kv_heads=3), T.TTT_ERR_SHAPE),
     (dict(head_dim=31), T.TTT_ERR_SHAPE),
     (dict(lr=float("nan")), T.TTT_ERR_NONFINITE),

@@ -215,3 +215,20 @@ def test_decode_errors():
         assert e.value.code == -1  # INVALID: token id out of range
     finally:
         m.close()
+
+
+@pytest.mark.parametrize("precision", ["fp32", "bf16"])
+def test_teacher_forced_decode_dual_mlp(precision):
+    """Decode-time test-time training with the static second MLP."""
+    s = inputs.shape("tiny-ttt2", dual_mlp=True, bf16=precision == "bf16")
+    w, tok = inputs.make_weights(s), inputs.make_tokens(s)
+    N = 2 * s.chunk
+    T, m = _model(s, w, precision, N + 1)
+    try:
+        out, losses = m.decode(np.ascontiguousarray(tok[:N + 1], np.int32), N)
+        fast = [m.fast_weights(i) for i in range(s.n_ttt_layers)]
+    finally:
+        m.close()
+    cfg = O.OracleConfig.from_mapping(s.as_dict())
+    r = O.decode(cfg, w, tok[:N + 1], N)
+    _check_losses_weights(losses[:2], fast, r, TOL[precision])

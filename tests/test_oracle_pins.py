@@ -148,23 +148,28 @@ def _torch_forward_losses(s, w, tok, fast=None):
         hn = F.rms_norm(h, (s.d_model,), lwt["mlp_norm"], eps=s.norm_eps)
         x = h + F.linear(F.silu(F.linear(hn, lwt["w_gate"])) * F.linear(hn, lwt["w_up"]),
                          lwt["w_down"])
+        if s.dual_mlp and l >= s.n_layers - s.n_ttt_layers:
+            hn2 = F.rms_norm(x, (s.d_model,), lwt["mlp2_norm"], eps=s.norm_eps)
+            x = x + F.linear(F.silu(F.linear(hn2, lwt["w_gate2"])) * F.linear(hn2, lwt["w_up2"]),
+                             lwt["w_down2"])
     z = F.linear(F.rms_norm(x, (s.d_model,), t(w["final_norm"]), eps=s.norm_eps),
                  t(w["lm_head"]))
     return F.cross_entropy(z[:-1], torch.as_tensor(tok[1:], dtype=torch.long), reduction="none")
 
 
-@pytest.mark.parametrize("name", ["tiny", "tiny-gqa"])
-def test_forward_matches_torch_library_restatement(name):
-    s, cfg, w, tok = _setup(name)
+@pytest.mark.parametrize("name,dual", [("tiny", False), ("tiny-gqa", False), ("tiny-gqa", True)])
+def test_forward_matches_torch_library_restatement(name, dual):
+    s, cfg, w, tok = _setup(name, dual_mlp=dual)
     ours = O.full_forward_losses(cfg, w, tok)
     ref = _torch_forward_losses(s, w, tok).numpy()
     np.testing.assert_allclose(ours, ref, rtol=1e-10, atol=1e-11)
 
 
-@pytest.mark.parametrize("name", ["tiny", "tiny-ttt2", "tiny-gqa"])
-def test_lr0_chunked_equals_unchunked(name):
+@pytest.mark.parametrize("name,dual", [("tiny", False), ("tiny-ttt2", False), ("tiny-gqa", False),
+                                       ("tiny-ttt2", True)])
+def test_lr0_chunked_equals_unchunked(name, dual):
     """With lr=0 the chunk losses are those of one plain SWA forward."""
-    s, cfg, w, tok = _setup(name)
+    s, cfg, w, tok = _setup(name, dual_mlp=dual)
     r0 = O.prefill(cfg, w, tok, lr=0.0)
     full = O.full_forward_losses(cfg, w, tok)
     T, b = len(tok), s.chunk
@@ -230,10 +235,18 @@ def test_gradients_central_differences(name, c):
     assert fd_check(name, c) < 1e-6
 
 
-def test_gradients_match_torch_autograd():
+@pytest.mark.parametrize("name,c", [("tiny-ttt2", 0), ("tiny-gqa", 2)])
+def test_gradients_central_differences_dual_mlp(name, c):
+    """Fast blocks with a static second MLP after the fast one: the fast
+    weights' gradients pass through the static MLP's input gradient."""
+    assert fd_check(name, c, dual_mlp=True) < 1e-6
+
+
+@pytest.mark.parametrize("dual", [False, True])
+def test_gradients_match_torch_autograd(dual):
     """One chunk's fast-weight gradients against torch.autograd (fp64) on the
     library restatement (first chunk: no cache involved)."""
-    s, cfg, w, tok = _setup("tiny-gqa")
+    s, cfg, w, tok = _setup("tiny-gqa", dual_mlp=dual)
     b = s.chunk
     tok1 = tok[:b + 1]                      # chunk 0 plus its last target
     st = O.OracleState(cfg, w, max_positions=b + 1)

@@ -54,7 +54,7 @@ def test_wrong_kv_head_grouping_is_caught(monkeypatch):
         return np.einsum("hnm,mhd->nhd", Pm, vh), Pm
 
     monkeypatch.setattr(O, "attention", bad_attention)
-    assert _fails(P.test_forward_matches_torch_library_restatement, "tiny-gqa")
+    assert _fails(P.test_forward_matches_torch_library_restatement, "tiny-gqa", False)
 
 
 def test_window_off_by_one_is_caught(monkeypatch):
@@ -72,7 +72,7 @@ def test_target_shift_is_caught(monkeypatch):
         return valid, np.where(valid, np.asarray(tokens)[t], 0)
 
     monkeypatch.setattr(O, "chunk_targets", bad_targets)
-    assert _fails(P.test_lr0_chunked_equals_unchunked, "tiny")
+    assert _fails(P.test_lr0_chunked_equals_unchunked, "tiny", False)
 
 
 def test_update_sign_is_caught(monkeypatch):
@@ -83,3 +83,18 @@ def test_update_sign_is_caught(monkeypatch):
 
     monkeypatch.setattr(O, "step_chunk", bad_step)
     assert _fails(P.test_loss_falls_on_repeated_context)
+
+
+def test_skipped_static_mlp_backward_is_caught(monkeypatch):
+    """With a static second MLP, the backward treats it as the identity
+    (passes dy straight to the fast MLP)."""
+    orig = O.backward_chunk
+
+    def bad_backward(st, z, acts, valid, tgt, n_tgt):
+        import copy
+        st2 = copy.copy(st)
+        st2.cfg = O.dataclasses.replace(st.cfg, dual_mlp=False)
+        return orig(st2, z, acts, valid, tgt, n_tgt)
+
+    monkeypatch.setattr(O, "backward_chunk", bad_backward)
+    assert P.fd_check("tiny-ttt2", 0, dual_mlp=True) > 1e-3

@@ -181,3 +181,40 @@ def test_full_attention_without_test_time_training(precision):
     b, T = s.chunk, len(tok)
     ref = np.array([full[c * b:min(T - 1, (c + 1) * b)].mean() for c in range(-(-T // b))])
     np.testing.assert_allclose(g, ref, rtol=TOL[precision])
+
+
+# ---------------------------------------------------------------------------
+# fast blocks with a static second MLP (dual_mlp)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["tiny-ttt2", "tiny-gqa"])
+def test_fp32_parity_dual_mlp(name):
+    s = inputs.shape(name, dual_mlp=True)
+    compare(s, inputs.make_weights(s), inputs.make_tokens(s), "fp32", check_delta=1e-4)
+
+
+@pytest.mark.parametrize("name", ["tiny-ttt2", "tiny-gqa"])
+def test_bf16_parity_dual_mlp(name):
+    s = inputs.shape(name, dual_mlp=True, bf16=True)
+    compare(s, inputs.make_weights(s), inputs.make_tokens(s), "bf16")
+
+
+def test_bf16_parity_dual_mlp_tc_attention():
+    """Tensor-core attention shapes (head dim 64, chunks of 128) with the
+    static second MLP in both fast blocks."""
+    s = inputs.shape("tiny-gqa", n_heads=4, n_kv_heads=2, head_dim=64, d_model=256, d_ff=512, chunk=128,
+                     window=200, seq_len=520, bf16=True, dual_mlp=True)
+    compare(s, inputs.make_weights(s), inputs.make_tokens(s, 520), "bf16")
+
+
+def test_fp32_dual_mlp_lr0_is_plain_forward():
+    """lr = 0: the dual-MLP model scores its chunks like one un-chunked
+    forward of the same model."""
+    s = inputs.shape("tiny-ttt2", dual_mlp=True)
+    w = inputs.make_weights(s)
+    tok = inputs.make_tokens(s)
+    g, _ = run_gpu(s, w, tok, "fp32", lr=0.0)
+    cfg = O.OracleConfig.from_mapping(s.as_dict())
+    full = O.full_forward_losses(cfg, w, tok)
+    b, T = s.chunk, len(tok)
+    ref = np.array([full[c * b:min(T - 1, (c + 1) * b)].mean() for c in range(-(-T // b))])
+    np.testing.assert_allclose(g, ref, rtol=1e-4)
