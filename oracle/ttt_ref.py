@@ -1,4 +1,4 @@
-"""CPU oracle for the TTT-E2E test-time inner loop (prefill).
+"""CPU oracle for the TTT-E2E test-time inner loop (prefill and decode).
 
 TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports, links or runs
 this module; only the tests, the smoke check and the CPU-baseline leg of the
@@ -34,7 +34,12 @@ notes):
   * one SGD step per chunk, W <- W - lr * dL/dW, applied after all gradients
     of the chunk are formed; keys and values of earlier chunks are constants
     (cached, detached), so gradients reach only the current chunk's own
-    queries, keys and values.
+    queries, keys and values;
+  * optionally (``dual_mlp``) each updated block keeps a static second MLP
+    (podcast page, 7:08), placed after its fast MLP with its own pre-norm
+    and residual; it is never updated, and gradients pass through it;
+  * decoding (``decode``) keeps the same loop, one chunk step per b
+    positions read, as stated in its docstring.
 
 Everything runs in float64 (``dtype`` may be lowered for timing only).
 """
