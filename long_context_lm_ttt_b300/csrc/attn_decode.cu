@@ -162,24 +162,46 @@ __global__ void __launch_bounds__(kDecWarps * 32)
   }
 }
 
+// One CTA per query head: warp 0 reduces the slices' maxima and sums (two
+// slices per lane), leaving each slice's weight exp2(m_s - M) in shared
+// memory; then every thread sums its output dimensions over the slices with
+// independent loads.
 template <typename T>
 __global__ void attn_decode_combine_kernel(const float* __restrict__ part, int hd, int splits, T* __restrict__ o,
                                            float* __restrict__ lse, int ld_lse) {
+  __shared__ float wsh[kMaxDecodeSplits];
+  __shared__ float sML[2];
   const int h = blockIdx.x;
-  const float* ph = part + (int64_t)h * splits * (hd + 2);
-  float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, ph[(int64_t)s * (hd + 2) + hd]);
-  float L = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const float ms = ph[(int64_t)s * (hd + 2) + hd];
-    if (ms != -INFINITY) L += exp2f(ms - M) * ph[(int64_t)s * (hd + 2) + hd + 1];
+  const int64_t st = hd + 2;
+  const float* ph = part + (int64_t)h * splits * st;
+  if (threadIdx.x < 32) {
+    const int l = threadIdx.x;
+    const float m0 = l < splits ? ph[l * st + hd] : -INFINITY;
+    const float m1 = l + 32 < splits ? ph[(l + 32) * st + hd] : -INFINITY;
+    float M = fmaxf(m0, m1);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
+    const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+    float L = (w0 > 0.f ? w0 * ph[l * st + hd + 1] : 0.f) + (w1 > 0.f ? w1 * ph[(l + 32) * st + hd + 1] : 0.f);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (l < splits) wsh[l] = w0;
+    if (l + 32 < splits) wsh[l + 32] = w1;
+    if (l == 0) {
+      sML[0] = M;
+      sML[1] = L;
+    }
   }
+  __syncthreads();
+  const float M = sML[0], L = sML[1];
   const float inv = L > 0.f ? 1.0f / L : 0.f;
   for (int e = threadIdx.x; e < hd; e += blockDim.x) {
     float a = 0.f;
-    for (int s = 0; s < splits; ++s) {
-      const float ms = ph[(int64_t)s * (hd + 2) + hd];
-      if (ms != -INFINITY) a += exp2f(ms - M) * ph[(int64_t)s * (hd + 2) + e];
+#pragma unroll 8
+    for (int s2 = 0; s2 < splits; ++s2) {
+      const float w = wsh[s2];
+      if (w > 0.f) a = fmaf(w, ph[s2 * st + e], a);
     }
     o[(int64_t)h * hd + e] = from_f<T>(a * inv);
   }
