@@ -25,8 +25,10 @@
  *     the library tells them apart with cudaPointerGetAttributes and copies
  *     host data itself.  The library never keeps a caller pointer after a
  *     call returns.
- *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All device
- *     work of a call is issued on it.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  The device
+ *     work of a call starts after the work already queued on `stream` and
+ *     finishes before anything queued on it later (ttt_prefill forks two
+ *     internal streams from `stream` and joins them back into it).
  */
 #ifndef TTT_H_
 #define TTT_H_
