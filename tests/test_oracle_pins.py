@@ -451,3 +451,27 @@ def test_greedy_decode_picks_argmax_and_replays():
     t = O.decode(cfg, w, g["tokens"], N)
     assert np.array_equal(t["tokens"], g["tokens"])
     np.testing.assert_array_equal(t["losses"], g["losses"])
+
+
+def test_teacher_forced_decode_trains_like_prefill_dual_mlp():
+    s, cfg, w, tok = _setup("tiny-gqa", dual_mlp=True)
+    N = 2 * s.chunk
+    d = O.decode(cfg, w, tok[:N + 1], N)
+    r = O.prefill(cfg, w, tok[:N + 1])
+    np.testing.assert_allclose(d["losses"], r["losses"][:2], rtol=1e-11, atol=0)
+    for a, c in zip(d["fast"], r["fast"]):
+        for k in O.FAST:
+            np.testing.assert_allclose(a[k], c[k], rtol=0, atol=1e-11 * np.abs(c[k]).max())
+
+
+def test_decode_without_fast_blocks_scores_a_frozen_model():
+    """n_ttt_layers = 0: decoding only scores; its chunk losses are the
+    chunk means of one un-chunked forward."""
+    s, cfg, w, tok = _setup("tiny-ttt2", n_ttt_layers=0)
+    b = s.chunk
+    N = 3 * b
+    d = O.decode(cfg, w, tok[:N + 1], N)
+    full = O.full_forward_losses(cfg, w, tok[:N + 1])
+    ref = np.array([full[c * b:(c + 1) * b].mean() for c in range(3)])
+    np.testing.assert_allclose(d["losses"], ref, rtol=1e-12, atol=1e-12)
+    assert d["fast"] == []
