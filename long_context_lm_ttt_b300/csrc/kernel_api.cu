@@ -113,12 +113,31 @@ static ttt::AttnArgs attn_args(int32_t n, int32_t H, int32_t Hkv, int32_t hd, in
 extern "C" int ttt_kernel_attn_fwd(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W,
                                    int32_t R, int64_t pos0, const void* q, const void* kring, const void* vring,
                                    void* o, float* lse, int32_t ld_lse, void* stream) {
-  int rc = attn_check(impl, n, H, Hkv, hd, W, R, 3);
+  int rc = attn_check(impl, n, H, Hkv, hd, W, R, 4);
   if (rc) return rc;
   if (!q || !kring || !vring || !o || !lse || ld_lse < n) return TTT_ERR_INVALID;
   if (ensure_err()) return TTT_ERR_OOM;
   ttt::AttnArgs a = attn_args(n, H, Hkv, hd, W, R, pos0, q, kring, vring, o, lse, ld_lse);
   cudaStream_t st = (cudaStream_t)stream;
+  if (impl == 4) {
+    // one query position (a decode step): the key range split over the GPU
+    if (!ttt::attn_decode_supported(a)) return TTT_ERR_SHAPE;
+    static float* part = nullptr;  // slice scratch, kept for the process
+    static size_t part_elems = 0;
+    const size_t need = (size_t)H * ttt::kMaxDecodeSplits * (hd + 2);
+    if (part_elems < need) {
+      if (part) cudaFree(part);
+      part = nullptr;
+      part_elems = 0;
+      if (cudaMalloc(&part, need * sizeof(float)) != cudaSuccess) return TTT_ERR_OOM;
+      part_elems = need;
+    }
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    ttt::attn_decode<ttt::bf16>(a, ttt::attn_decode_splits(a, sms), part, st);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
+  }
   if (impl == 0 || impl == 2 || impl == 3) {
     if (!ttt::attn_tc_supported(a)) return TTT_ERR_SHAPE;
     rc = ttt::attn_fwd_tc(a, g_err, st, impl == 0 ? 0 : (impl == 2 ? 1 : 2));

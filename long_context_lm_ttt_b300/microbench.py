@@ -5,6 +5,8 @@ points (include/ttt_kernels.h), for profiling one kernel in isolation.
     python -m long_context_lm_ttt_b300.microbench gemm-sgd --M 3072 --N 8192 --K 1024
     python -m long_context_lm_ttt_b300.microbench attn-fwd --n 1024 --H 24 --Hkv 8 --hd 128 --W 8192
     python -m long_context_lm_ttt_b300.microbench attn-bwd --n 1024 --H 24 --Hkv 8 --hd 128 --W 8192
+    python -m long_context_lm_ttt_b300.microbench attn-fwd --n 1 --impl 4 --pos0 9000   # a decode step
+    python -m long_context_lm_ttt_b300.microbench gemm --M 1 --N 16384 --K 3072          # a one-row product
 
 Inputs are seeded random bf16 tensors on cuda:0.  Prints one JSON line with
 the mean time of `--iters` launches (CUDA events, after `--warmup`) and the

@@ -99,6 +99,31 @@ def test_attn_fwd(case, impl):
     assert err_l < 2e-3, err_l
 
 
+DECODE_CASES = [
+    # H, Hkv, hd, W, pos0, R: one query position
+    (24, 8, 128, 8192, 40 * 1024 + 17, 9216),  # 3B heads deep in the sequence, ring wraps
+    (24, 8, 128, 8192, 5, 9216),               # fewer keys than one slice
+    (4, 4, 32, 64, 300, 128),                  # hd 32, one query head per KV head
+    (6, 2, 96, 300, 1024, 640),                # hd 96, GQA 3
+    (16, 2, 64, 1000, 999, 1024),              # GQA 8, window covers everything
+]
+
+
+@pytest.mark.parametrize("case", DECODE_CASES)
+def test_attn_fwd_one_query(case):
+    """impl 4: the decode step's one-query kernel (key range split over
+    CTAs, slices folded) against the restatement."""
+    torch, T = _env()
+    H, Hkv, hd, W, pos0, R = case
+    q, kr, vr = make_case(1, H, Hkv, hd, W, pos0, R, seed=hd + H)
+    o, lse = run_fwd(T, torch, 4, q, kr, vr, 1, H, Hkv, hd, W, pos0)
+    ro, rl = ref_forward(q, kr, vr, 1, H, Hkv, hd, W, pos0)
+    err_o = max(np.abs(o[r, h * hd:(h + 1) * hd] - v).max() for (r, h), v in ro.items())
+    err_l = max(abs(lse[h, r] - v) for (r, h), v in rl.items())
+    assert err_o < 2e-2, err_o
+    assert err_l < 2e-3, err_l
+
+
 @pytest.mark.parametrize("impl", [2, 3])
 def test_attn_fwd_3b_shape_sampled(impl):
     """3B head layout (24 q / 8 KV heads x 128) over a full 1024-row chunk
