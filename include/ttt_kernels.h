@@ -68,7 +68,8 @@ int ttt_kernel_gemm_sgd(int32_t M, int32_t N, int32_t K, const void* A, int64_t 
  * 128-row query tile per CTA, impl 3 the one with two tiles per CTA and P
  * kept in tensor memory, impl 4 the one-query kernel of a decode step
  * (n == 1, hd a multiple of 32, at most 8 query heads per KV head; its
- * slice scratch is allocated on first use and kept). */
+ * slice scratch is allocated per device on first use and kept, so calls on
+ * one device must not overlap). */
 int ttt_kernel_attn_fwd(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R,
                         int64_t pos0, const void* q, const void* kring, const void* vring, void* o, float* lse,
                         int32_t ld_lse, void* stream);

@@ -122,19 +122,22 @@ extern "C" int ttt_kernel_attn_fwd(int32_t impl, int32_t n, int32_t H, int32_t H
   if (impl == 4) {
     // one query position (a decode step): the key range split over the GPU
     if (!ttt::attn_decode_supported(a)) return TTT_ERR_SHAPE;
-    static float* part = nullptr;  // slice scratch, kept for the process
-    static size_t part_elems = 0;
-    const size_t need = (size_t)H * ttt::kMaxDecodeSplits * (hd + 2);
-    if (part_elems < need) {
-      if (part) cudaFree(part);
-      part = nullptr;
-      part_elems = 0;
-      if (cudaMalloc(&part, need * sizeof(float)) != cudaSuccess) return TTT_ERR_OOM;
-      part_elems = need;
-    }
+    // slice scratch per device, grown as needed and kept for the process
+    constexpr int kDevs = 64;
+    static float* part_of[kDevs] = {};
+    static size_t elems_of[kDevs] = {};
     int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return TTT_ERR_CUDA;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t need = (size_t)H * ttt::kMaxDecodeSplits * (hd + 2);
+    if (elems_of[dev] < need) {
+      if (part_of[dev]) cudaFree(part_of[dev]);
+      part_of[dev] = nullptr;
+      elems_of[dev] = 0;
+      if (cudaMalloc(&part_of[dev], need * sizeof(float)) != cudaSuccess) return TTT_ERR_OOM;
+      elems_of[dev] = need;
+    }
+    float* part = part_of[dev];
     ttt::attn_decode<ttt::bf16>(a, ttt::attn_decode_splits(a, sms), part, st);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
   }
