@@ -131,6 +131,19 @@ int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* stream, ttt_ct
 int ttt_prefill(ttt_ctx* ctx, const int32_t* tokens, int64_t T, float* chunk_losses,
                 void* stream);
 
+/* Several sequences in one call: ttt_prefill on each of n_ctx distinct
+ * contexts, every context with its own fast weights and ring (scope row
+ * "batched sequences").  The contexts run concurrently: the calling thread
+ * drives the first and one host thread each of the others, each on
+ * streams[i] (streams may be NULL: every context then uses the legacy
+ * default stream, which orders them one after another).  Arguments are
+ * arrays of n_ctx entries with the meaning of ttt_prefill's.  Each
+ * context's result and ttt_last_error are as if ttt_prefill had been called
+ * on it alone; the return value is the first non-OK code in index order.
+ * Two entries naming the same context are INVALID. */
+int ttt_prefill_batch(ttt_ctx* const* ctxs, int32_t n_ctx, const int32_t* const* tokens, const int64_t* T,
+                      float* const* chunk_losses, void* const* streams);
+
 /* Decode-time test-time training: generation one token per step, with the
  * same test-time step as ttt_prefill's chunk loop once every b positions
  * (the latency per token stays constant in the context length: summary

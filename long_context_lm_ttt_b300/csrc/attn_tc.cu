@@ -26,6 +26,8 @@
 // scores while the softmax warps work on the current ones.  Two CTAs fit on
 // one SM (112 KB shared memory, 256 TMEM columns each).
 #include <cuda.h>
+
+#include <atomic>
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -1859,7 +1861,7 @@ int launch_fwd(const AttnArgs& a, int* err, cudaStream_t st) {
   if (!rc) rc = map2d(&mk, a.kring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
   if (!rc) rc = map2d(&mv, a.vring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
   if (rc) return rc;
-  static bool attr = false;
+  static std::atomic<bool> attr{false};
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SM::SMEM);
@@ -1894,7 +1896,7 @@ int launch_fwd2(const AttnArgs& a, int* err, cudaStream_t st) {
   if (!rc) rc = map2d(&mk, a.kring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN2);
   if (!rc) rc = map2d(&mv, a.vring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN2);
   if (rc) return rc;
-  static bool attr = false;
+  static std::atomic<bool> attr{false};
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd2_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SM::SMEM);
@@ -1986,7 +1988,7 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
   if (!rc) rc = map2d(&mk, a.kring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
   if (!rc) rc = map2d(&mv, a.vring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
   if (rc) return rc;
-  static bool attr = false;
+  static std::atomic<bool> attr{false};
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attn_dq2_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DQ::SMEM);

@@ -30,6 +30,7 @@
 #include <cstring>
 #include <memory>
 #include <string>
+#include <thread>
 #include <vector>
 
 #include "../../include/ttt.h"
@@ -1285,6 +1286,50 @@ extern "C" int ttt_prefill(ttt_ctx* ctx, const int32_t* tokens, int64_t T, float
     ctx->eng->err = "exception in ttt_prefill";
     return TTT_ERR_INTERNAL;
   }
+}
+
+extern "C" int ttt_prefill_batch(ttt_ctx* const* ctxs, int32_t n_ctx, const int32_t* const* tokens,
+                                 const int64_t* T, float* const* chunk_losses, void* const* streams) {
+  if (!ctxs || !tokens || !T || !chunk_losses || n_ctx < 1) return TTT_ERR_INVALID;
+  for (int i = 0; i < n_ctx; ++i) {
+    if (!ctxs[i] || !ctxs[i]->eng) return TTT_ERR_INVALID;
+    for (int j = 0; j < i; ++j)
+      if (ctxs[j] == ctxs[i]) return TTT_ERR_INVALID;  // one sequence per context
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TTT_ERR_CUDA;
+  std::vector<int> rc(n_ctx, TTT_OK);
+  auto run = [&](int i) {
+    ttt::EngineBase* e = ctxs[i]->eng.get();
+    e->err.clear();
+    try {
+      rc[i] = e->prefill(tokens[i], T[i], chunk_losses[i], streams ? (cudaStream_t)streams[i] : nullptr);
+    } catch (...) {
+      e->err = "exception in ttt_prefill_batch";
+      rc[i] = TTT_ERR_INTERNAL;
+    }
+  };
+  // one host thread per further sequence, so that every context issues its
+  // work while the others run; the calling thread takes the first
+  std::vector<std::thread> th;
+  try {
+    for (int i = 1; i < n_ctx; ++i)
+      th.emplace_back([&, i] {
+        if (cudaSetDevice(dev) != cudaSuccess) {
+          rc[i] = TTT_ERR_CUDA;
+          return;
+        }
+        run(i);
+      });
+  } catch (...) {
+    // no more threads: the remaining sequences run on this thread
+    for (size_t i = th.size() + 1; i < (size_t)n_ctx; ++i) run((int)i);
+  }
+  run(0);
+  for (std::thread& t : th) t.join();
+  for (int i = 0; i < n_ctx; ++i)
+    if (rc[i] != TTT_OK) return rc[i];
+  return TTT_OK;
 }
 
 extern "C" int ttt_decode(ttt_ctx* ctx, const int32_t* tokens, int64_t n_given, int64_t n_steps, int32_t* tokens_out,

@@ -18,6 +18,8 @@
 // M/N contiguous); the TMA box orientation and the descriptor's major bit
 // follow.  All waits are bounded (see tc_common.cuh).
 #include <cuda.h>
+
+#include <atomic>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -746,7 +748,7 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
     ms = mw = mh = ml = mb;
   }
   auto kern = gemm_tc_kernel<BN, A_MN, B_MN, SRC, PAIR>;
-  static bool attr_set = false;  // per instantiation
+  static std::atomic<bool> attr_set{false};  // per instantiation
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return (int)e;
@@ -768,7 +770,7 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    static int resident = 0;  // per instantiation
+    static std::atomic<int> resident{0};  // per instantiation
     if (!resident) {
       cfg.gridDim = dim3(2 * (num_sms / 2));
       int n = 0;
@@ -778,7 +780,7 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
       }
       resident = n;
     }
-    const int pairs = std::max(1, std::min(cap / 2, resident));
+    const int pairs = std::max(1, std::min(cap / 2, resident.load()));
     cfg.gridDim = dim3(2 * (nunits < pairs ? nunits : pairs));
     const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, ma, mb, mb2, ms, mw, mh, ml, g.B2 ? 1 : 0, g.M, g.N, g.K,
                                               g.e, err, splits, g.ws);

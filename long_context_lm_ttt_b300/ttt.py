@@ -32,8 +32,8 @@ ERR_NAMES = {0: "OK", -1: "INVALID", -2: "SHAPE", -3: "OOM", -4: "CUDA", -5: "NO
 TTT_BF16 = 0
 TTT_FP32_CHECK = 1
 
-EXPORTS = ("ttt_create", "ttt_prefill", "ttt_decode", "ttt_logits", "ttt_get_fast_weights", "ttt_reset",
-           "ttt_destroy", "ttt_last_error", "ttt_profile", "ttt_profile_read")
+EXPORTS = ("ttt_create", "ttt_prefill", "ttt_prefill_batch", "ttt_decode", "ttt_logits", "ttt_get_fast_weights",
+           "ttt_reset", "ttt_destroy", "ttt_last_error", "ttt_profile", "ttt_profile_read")
 
 
 class ttt_config(ctypes.Structure):
@@ -72,6 +72,9 @@ def load(path: str = LIB_PATH):
     lib.ttt_create.restype = c_int32
     lib.ttt_prefill.argtypes = [c_void_p, c_void_p, c_int64, c_void_p, c_void_p]
     lib.ttt_prefill.restype = c_int32
+    lib.ttt_prefill_batch.argtypes = [POINTER(c_void_p), c_int32, POINTER(c_void_p), POINTER(c_int64),
+                                      POINTER(c_void_p), POINTER(c_void_p)]
+    lib.ttt_prefill_batch.restype = c_int32
     lib.ttt_decode.argtypes = [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p]
     lib.ttt_decode.restype = c_int32
     lib.ttt_logits.argtypes = [c_void_p, c_void_p, c_int32, c_void_p, c_void_p]
@@ -191,6 +194,22 @@ def ttt_create(cfg: ttt_config, weights: ttt_weights, stream=None) -> c_void_p:
 def ttt_prefill(ctx, tokens, T: int, chunk_losses, stream=None) -> int:
     rc = load().ttt_prefill(ctx, _ptr(tokens), int(T), _ptr(chunk_losses), _stream(stream))
     _check(rc, ctx)
+    return rc
+
+
+def ttt_prefill_batch(ctxs, tokens, T, chunk_losses, streams=None) -> int:
+    """ttt_prefill on several contexts at once (lists of equal length)."""
+    n = len(ctxs)
+    arr = lambda vals: (c_void_p * n)(*vals)
+    c_ctx = arr([c.value if isinstance(c, c_void_p) else c for c in ctxs])
+    c_tok = arr([_ptr(t) for t in tokens])
+    c_T = (c_int64 * n)(*[int(t) for t in T])
+    c_loss = arr([_ptr(l) for l in chunk_losses])
+    c_st = arr([_stream(s) for s in streams]) if streams is not None else None
+    rc = load().ttt_prefill_batch(c_ctx, n, c_tok, c_T, c_loss, c_st)
+    if rc != 0:
+        bad = next((c for c in ctxs if load().ttt_last_error(c)), ctxs[0])
+        _check(rc, bad)
     return rc
 
 
