@@ -69,7 +69,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dual-mlp", action="store_true",
                     help="fast blocks carry a static second MLP after the fast one")
-    ap.add_argument("--mode", choices=["prefill", "decode"], default="prefill")
+    ap.add_argument("--mode", choices=["prefill", "decode", "batch"], default="prefill")
+    ap.add_argument("--sequences", type=int, default=2,
+                    help="batch: sequences per ttt_prefill_batch call (one context each)")
     ap.add_argument("--context", type=int, default=None,
                     help="decode: tokens prefilled before decoding (default 8 chunks)")
     ap.add_argument("--decode-tokens", type=int, default=None,
@@ -508,12 +510,69 @@ def run_decode(args):
     return 0
 
 
+def run_batch(args):
+    """--mode batch: tokens/s of ttt_prefill_batch over --sequences
+    contexts (independent sequences, own fast weights), each on its own
+    stream; a step resets every context and prefills all of them."""
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    torch.cuda.set_device(0)
+    from long_context_lm_ttt_b300 import ttt as TT
+    TT.load()
+    B = args.sequences
+    s, _ = workload(args)
+    T = s.seq_len
+    w = inputs.make_weights(s)
+    models = [TT.TTT(s, w, TT.TTT_BF16, max_tokens=T) for _ in range(B)]
+    del w
+    toks = [torch.from_numpy(inputs.make_tokens(s, seed=1 + i)).cuda() for i in range(B)]
+    losses = [torch.zeros(s.n_chunks, dtype=torch.float32, device="cuda") for _ in range(B)]
+    streams = [torch.cuda.Stream() for _ in range(B)]
+
+    def step():
+        for m in models:
+            m.reset()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        TT.ttt_prefill_batch([m.ctx for m in models], toks, [T] * B, losses, streams)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        step()
+    uuid = str(torch.cuda.get_device_properties(0).uuid)
+    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    clocks.start()
+    sec = sum(step() for _ in range(args.steps))
+    clk = clocks.stop()
+    value = B * T * args.steps / sec
+    fl = inputs.flops_per_sequence(s)
+    line = {
+        "metric": f"TTT-E2E prefill tokens/s, {B} sequences per call (concurrent contexts)",
+        "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_name(s) + f", {B} sequences", "global_batch": B, "seq_len": T},
+        "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"), "reasons": clk.get("reasons")},
+        "model_tflops": fl["total"] * B * args.steps / sec / 1e12,
+        "timing": "host wall clock around each ttt_prefill_batch call (it returns after the work has completed)",
+    }
+    for m in models:
+        m.close()
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.mode == "decode":
         return run_decode(args)
+    if args.mode == "batch":
+        return run_batch(args)
     return run_ours(args)
 
 
