@@ -84,3 +84,13 @@ def test_null_arguments(lib):
     assert lib.ttt_get_fast_weights(None, 0, 0, None, None) == T.TTT_ERR_INVALID
     assert lib.ttt_reset(None) == T.TTT_ERR_INVALID
     lib.ttt_destroy(None)
+
+
+def test_prefill_batch_rejects_null_contexts(lib):
+    """The batch entry checks every context before any device work."""
+    toks = [np.zeros(8, np.int32), np.zeros(8, np.int32)]
+    losses = [np.zeros(1, np.float32), np.zeros(1, np.float32)]
+    with pytest.raises(T.TTTError) as e:
+        T.ttt_prefill_batch([ctypes.c_void_p(), ctypes.c_void_p()], toks, [8, 8], losses)
+    assert e.value.code == T.TTT_ERR_INVALID
+    assert lib.ttt_prefill_batch(None, 2, None, None, None, None) == T.TTT_ERR_INVALID
