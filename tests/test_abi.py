@@ -81,6 +81,7 @@ def test_null_arguments(lib):
     assert lib.ttt_create(ctypes.byref(_cfg()), None, None, None) == T.TTT_ERR_INVALID
     assert lib.ttt_prefill(None, None, 0, None, None) == T.TTT_ERR_INVALID
     assert lib.ttt_logits(None, None, 1, None, None) == T.TTT_ERR_INVALID
+    assert lib.ttt_decode(None, None, 1, 1, None, None, None) == T.TTT_ERR_INVALID
     assert lib.ttt_get_fast_weights(None, 0, 0, None, None) == T.TTT_ERR_INVALID
     assert lib.ttt_reset(None) == T.TTT_ERR_INVALID
     lib.ttt_destroy(None)
