@@ -171,14 +171,15 @@ def attention(q, kw, vw, qpos, kpos, window, group):
     head_kv = np.arange(q.shape[1]) // group
     kh = kw[:, head_kv, :]                     # [m, H, hd]
     vh = vw[:, head_kv, :]
-    S = np.einsum("nhd,mhd->hnm", q, kh) / math.sqrt(hd)
+    # per head: S_h = q_h k_h^T / sqrt(hd), as batched matrix products
+    S = np.matmul(q.transpose(1, 0, 2), kh.transpose(1, 2, 0)) / math.sqrt(hd)   # [H, n, m]
     rel = qpos[:, None] - kpos[None, :]
     allowed = (rel >= 0) & (rel < window)
     S = np.where(allowed[None], S, -np.inf)
     m = np.max(S, axis=-1, keepdims=True)
     E = np.exp(S - m)
     P = E / np.sum(E, axis=-1, keepdims=True)
-    o = np.einsum("hnm,mhd->nhd", P, vh)
+    o = np.matmul(P, vh.transpose(1, 0, 2)).transpose(1, 0, 2)                    # [n, H, hd]
     return o, P
 
 
@@ -313,14 +314,17 @@ def backward_chunk(st: OracleState, z, acts, valid, tgt, n_tgt):
         head_kv = np.arange(H) // group
         kh = A["kw"][:, head_kv, :]
         vh = A["vw"][:, head_kv, :]
-        dP = np.einsum("nhd,mhd->hnm", do, vh)
+        # per head h (batched matrix products over the head axis):
+        # dP_h = do_h v_h^T, dq_h = dS_h k_h, and for the chunk's own keys
+        # dk_h = dS_h^T q_h, dv_h = P_h^T do_h
+        dP = np.matmul(do.transpose(1, 0, 2), vh.transpose(1, 2, 0))               # [H, n, m]
         o = A["o"].reshape(n, H, hd)
-        Dt = np.einsum("nhd,nhd->hn", do, o)[..., None]
+        Dt = np.sum(do * o, axis=-1).T[..., None]                                  # [H, n, 1]
         dS = P * (dP - Dt) / math.sqrt(hd)
-        dq = np.einsum("hnm,mhd->nhd", dS, kh)
+        dq = np.matmul(dS, kh.transpose(1, 0, 2)).transpose(1, 0, 2)               # [n, H, hd]
         # keys / values of the chunk itself: the last n columns of the window
-        dk_h = np.einsum("hnm,nhd->mhd", dS[:, :, n_cached:], A["qr"])
-        dv_h = np.einsum("hnm,nhd->mhd", P[:, :, n_cached:], do)
+        dk_h = np.matmul(dS[:, :, n_cached:].transpose(0, 2, 1), A["qr"].transpose(1, 0, 2)).transpose(1, 0, 2)
+        dv_h = np.matmul(P[:, :, n_cached:].transpose(0, 2, 1), do.transpose(1, 0, 2)).transpose(1, 0, 2)
         dk = dk_h.reshape(n, Hkv, group, hd).sum(axis=2)
         dv = dv_h.reshape(n, Hkv, group, hd).sum(axis=2)
         dq = rope_bwd(dq, ang).reshape(n, H * hd)
