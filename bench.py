@@ -64,11 +64,16 @@ def parse_args():
     ap.add_argument("--fast-layers", type=int, default=None,
                     help="override the number of fast blocks (0: no test-time training, forward only)")
     ap.add_argument("--cpu-tokens", type=int, default=None,
-                    help="tokens the oracle is timed on (default: one chunk; 128 at 3B)")
+                    help="tokens the oracle is timed on (default: one chunk from 760M up, four below; "
+                         "--impl reference: 128 at 3B)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dual-mlp", action="store_true",
                     help="fast blocks carry a static second MLP after the fast one")
+    ap.add_argument("--fast-bf16-single", action="store_true",
+                    help="the forward reads the fast weights as one bf16 copy (default: the bf16 pair hi + lo)")
+    ap.add_argument("--bulk-tokens", type=int, default=0,
+                    help="tokens per super-chunk of the frozen blocks' bulk pass (0: automatic)")
     ap.add_argument("--mode", choices=["prefill", "decode", "batch"], default="prefill")
     ap.add_argument("--sequences", type=int, default=2,
                     help="batch: sequences per ttt_prefill_batch call (one context each)")
@@ -176,15 +181,25 @@ def workload(args, rank=0):
     return s, tok
 
 
-def workload_name(s):
+def workload_name(s, args=None):
+    single = bool(args is not None and getattr(args, "fast_bf16_single", False))
     return (f"{s.name} TTT-E2E prefill: L={s.n_layers} d={s.d_model} H={s.n_heads}/{s.n_kv_heads}x{s.head_dim} "
             f"ff={s.d_ff} V={s.vocab} W={s.window} b={s.chunk} T={s.seq_len} fast={s.n_ttt_layers} lr={s.lr}"
-            + (" dual-MLP fast blocks" if s.dual_mlp else ""))
+            + (" dual-MLP fast blocks" if s.dual_mlp else "")
+            + (", fast weights fp32 master read as one bf16 copy" if single
+               else ", fast weights fp32 master read as a bf16 hi+lo pair"))
+
+
+def make_model(TT, s, w, args, max_tokens):
+    return TT.TTT(s, w, TT.TTT_BF16, max_tokens=max_tokens, bulk_tokens=args.bulk_tokens,
+                  fast_bf16_single=args.fast_bf16_single)
 
 
 def cpu_baseline(s, w, tok, n_tokens):
     """The oracle as it stands, timed on the host cores over the first
-    n_tokens positions (a prefix of the first chunk, or whole chunks)."""
+    n_tokens positions (a prefix of the first chunk, or whole chunks).  Its
+    state (an fp64 copy of every weight) is built before the timer starts;
+    the timed region is the oracle's own chunk steps, in prefill's order."""
     from oracle import ttt_ref as O
     try:
         import psutil
@@ -193,17 +208,33 @@ def cpu_baseline(s, w, tok, n_tokens):
         avail = 1 << 62
     dtype = np.float64 if avail > 3.2 * 8 * inputs.n_params(s) else np.float32
     cfg = O.OracleConfig.from_mapping(s.as_dict())
+    sample = np.asarray(tok[:n_tokens])
+    bounds = O.chunk_bounds(n_tokens, s.chunk)
     t0 = time.perf_counter()
-    O.prefill(cfg, w, tok[:n_tokens], dtype=dtype)
+    st = O.OracleState(cfg, w, max_positions=bounds[-1][1], dtype=dtype)
+    setup = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    for a, b in bounds:
+        O.step_chunk(st, sample, a, b, cfg.lr)
     dt = time.perf_counter() - t0
-    n_ch = -(-n_tokens // s.chunk)
+    del st
     return {"value": n_tokens / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": f"first {n_tokens} tokens of the sequence ({n_ch} chunk(s) of the {s.name} workload, "
-                      f"same weights and ids), {np.dtype(dtype).name} numpy, {dt:.1f} s"}
+            "sample": f"first {n_tokens} tokens of the sequence ({len(bounds)} chunk(s) of the {s.name} workload, "
+                      f"same weights and ids), {np.dtype(dtype).name} numpy, {dt:.1f} s of chunk steps; the "
+                      f"oracle's state set-up ({setup:.1f} s, a {np.dtype(dtype).name} copy of every weight) "
+                      f"is outside the timed region"}
 
 
 def default_cpu_tokens(s):
-    return 128 if s.d_model >= 3072 else (s.chunk if s.d_model >= 1536 else min(s.seq_len, 4 * s.chunk))
+    # one whole chunk from the 760M class up (the 3B chunk is 1024 tokens),
+    # four chunks below
+    return s.chunk if s.d_model >= 1536 else min(s.seq_len, 4 * s.chunk)
+
+
+def reference_tokens(s):
+    # --impl reference repeats the sample warmup + steps times: a shorter
+    # prefix of the first chunk at the largest shapes keeps the run to minutes
+    return 128 if s.d_model >= 3072 else default_cpu_tokens(s)
 
 
 # ---------------------------------------------------------------------------
@@ -214,7 +245,7 @@ def run_reference(args):
         return 0
     s, tok = workload(args)
     w = inputs.make_weights(s)
-    n = args.cpu_tokens or default_cpu_tokens(s)
+    n = args.cpu_tokens or reference_tokens(s)
     times = []
     base = None
     for i in range(args.warmup + args.steps):
@@ -228,7 +259,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": workload_name(s), "global_batch": 1,
+            "data": "synthetic", "config": {"workload": workload_name(s, args), "global_batch": 1,
                                             "seq_len": s.seq_len, "sample_tokens": n},
             "cpu_baseline": base,
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -289,7 +320,7 @@ def run_ours(args):
     nC = s.n_chunks
     t_setup = time.perf_counter()
     w = inputs.make_weights(s)
-    m = TT.TTT(s, w, TT.TTT_BF16, max_tokens=T)
+    m = make_model(TT, s, w, args, T)
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     if not want_cpu:
         del w
@@ -364,7 +395,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(s), "global_batch": world, "seq_len": T,
+        "config": {"workload": workload_name(s, args), "global_batch": world, "seq_len": T,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (every chunk streams all weights, 6+ GB at 3B)"},
         "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"), "reasons": clk.get("reasons")},
@@ -432,7 +463,7 @@ def run_decode(args):
         raise SystemExit("--context must be a multiple of the chunk length")
     w = inputs.make_weights(s)
     tok = inputs.make_tokens(s.replace(seq_len=ctx + 1), seed=1)
-    m = TT.TTT(s, w, TT.TTT_BF16, max_tokens=ctx + nd + 1)
+    m = make_model(TT, s, w, args, ctx + nd + 1)
     del w
     tok_d = torch.from_numpy(tok).cuda()
     out_d = torch.zeros(nd + 1, dtype=torch.int32, device="cuda")
@@ -490,7 +521,7 @@ def run_decode(args):
         "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dec_ms / args.steps, "ms_per_token": per_tok, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(s) + f" decode: context {ctx}, {nd} generated tokens",
+        "config": {"workload": workload_name(s, args) + f" decode: context {ctx}, {nd} generated tokens",
                    "global_batch": 1, "context": ctx, "decode_tokens": nd,
                    "l2": "every step streams all weights (7+ GB at 3B), larger than L2"},
         "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"), "reasons": clk.get("reasons")},
@@ -526,7 +557,7 @@ def run_batch(args):
     s, _ = workload(args)
     T = s.seq_len
     w = inputs.make_weights(s)
-    models = [TT.TTT(s, w, TT.TTT_BF16, max_tokens=T) for _ in range(B)]
+    models = [make_model(TT, s, w, args, T) for _ in range(B)]
     del w
     toks = [torch.from_numpy(inputs.make_tokens(s, seed=1 + i)).cuda() for i in range(B)]
     losses = [torch.zeros(s.n_chunks, dtype=torch.float32, device="cuda") for _ in range(B)]
@@ -554,7 +585,7 @@ def run_batch(args):
         "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(s) + f", {B} sequences", "global_batch": B, "seq_len": T},
+        "config": {"workload": workload_name(s, args) + f", {B} sequences", "global_batch": B, "seq_len": T},
         "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"), "reasons": clk.get("reasons")},
         "model_tflops": fl["total"] * B * args.steps / sec / 1e12,
         "timing": "host wall clock around each ttt_prefill_batch call (it returns after the work has completed)",

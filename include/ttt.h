@@ -67,13 +67,26 @@ enum {
  *   device staging of host token arrays), dual_mlp (0 or 1: each fast block
  *   carries a second, static SwiGLU MLP after its fast one, with its own
  *   pre-norm and residual: y = h2 + MLP2(n(h2)), h2 = h + MLP_fast(n(h));
- *   podcast page, 7:08).                                                    */
+ *   podcast page, 7:08), bulk_tokens (>= 0: tokens per super-chunk of the
+ *   frozen blocks' bulk pass in ttt_prefill, rounded down to a multiple of
+ *   chunk and at least one chunk; 0 picks about 16K tokens.  It changes how
+ *   the work is batched, never what is computed), fast_bf16_single (0 or
+ *   1, TTT_BF16 only: how the forward reads a fast weight w, whose value is
+ *   an fp32 master updated in place.  0: as the bf16 pair hi = rn(w),
+ *   lo = rn(w - hi), read as hi + lo, which carries about 16 significant
+ *   bits, so every update reaches the forward.  1: one bf16 copy rn(w),
+ *   re-rounded after every update, at half the tensor work of the fast
+ *   MLPs' forward products; an update smaller than half a bf16 step of w
+ *   leaves that copy unchanged, so at small lr the forward does not see
+ *   the test-time training until updates accumulate past that step).       */
 typedef struct ttt_config {
   int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, d_ff, vocab;
   int32_t window, chunk, n_ttt_layers, precision;
   float lr, rope_theta, norm_eps;
   int64_t max_tokens;
   int32_t dual_mlp;
+  int32_t bulk_tokens;
+  int32_t fast_bf16_single;
 } ttt_config;
 
 /* Initial weights, fp32 values (host or device).  Per-layer fields are
@@ -117,7 +130,7 @@ int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* stream, ttt_ct
  * weights, loss = mean over the chunk's targets of (logsumexp(z_t) -
  * z_t[target]), backward into w_gate/w_up/w_down of the fast blocks with
  * earlier keys/values held constant, then W <- W - lr * dW (fp32 master;
- * the bf16 copy is re-rounded).  A chunk without targets reports loss 0 and
+ * its bf16 pair, or the single bf16 copy, is re-rounded).  A chunk without targets reports loss 0 and
  * makes no update.
  *   chunk_losses: [ceil(T/b)] fp32, host or device.
  * Requires a fresh (or reset) context and 1 <= T <= cfg.max_tokens;

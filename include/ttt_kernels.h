@@ -67,9 +67,10 @@ int ttt_kernel_gemm_sgd(int32_t M, int32_t N, int32_t K, const void* A, int64_t 
  * arithmetic.  Forward only: impl 2 forces the tensor-core kernel with one
  * 128-row query tile per CTA, impl 3 the one with two tiles per CTA and P
  * kept in tensor memory, impl 4 the one-query kernel of a decode step
- * (n == 1, hd a multiple of 32, at most 8 query heads per KV head; its
- * slice scratch is allocated per device on first use and kept, so calls on
- * one device must not overlap). */
+ * (n == 1, hd a multiple of 32, at most 8 query heads per KV head, q,
+ * kring, vring and o 16-byte aligned, else TTT_ERR_SHAPE before any device
+ * work; its slice scratch is allocated per device on first use and kept, so
+ * calls on one device must not overlap). */
 int ttt_kernel_attn_fwd(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R,
                         int64_t pos0, const void* q, const void* kring, const void* vring, void* o, float* lse,
                         int32_t ld_lse, void* stream);
@@ -81,20 +82,24 @@ int ttt_kernel_attn_bwd(int32_t impl, int32_t n, int32_t H, int32_t Hkv, int32_t
 /* The tensor-core attention backward of ttt_kernel_attn_bwd (impl 0), same
  * arguments and results, but it allocates nothing.  The pages have no
  * counterpart: this entry point exists for callers that must not call
- * cudaMalloc, such as code running under a CUDA graph capture in the global
- * capture mode, code whose device memory belongs to a caching allocator or a
- * fixed budget, and real-time callers that plan all memory up front.
+ * cudaMalloc, such as code whose device memory belongs to a caching
+ * allocator or a fixed budget (an allocation outside it can fail once that
+ * allocator holds the free memory, and escapes its accounting), and
+ * real-time callers that plan all memory up front.
  *
- * Its fp32 scratch is a fixed 32 MiB device array inside the library, held
- * by every GPU on which this call runs until the process exits.  The
- * backward needs 2 * n * H * hd floats of it: larger shapes return
- * TTT_ERR_SHAPE before any device work.  The first call on each device
- * looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  All
+ * Its fp32 scratch is a fixed 32 MiB device array inside the library.  Every
+ * device context that loads this library's module may reserve it, until the
+ * process exits: with lazy module loading (the CUDA default) from the first
+ * use of the library on that device, with eager loading when the context is
+ * created.  The backward needs 2 * n * H * hd floats of it: larger shapes
+ * return TTT_ERR_SHAPE before any device work.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  All
  * calls share the array and it keeps the previous call's contents (nothing
  * in it has to start at zero); calls that overlap on the GPU race on it, so
  * issue them on one stream.  A device-side bounded wait that gives up (not
- * expected) leaves dqkv incomplete; it is not reported here. */
+ * expected) leaves dqkv incomplete and records its code, which the next
+ * ttt_kernel_error() returns. */
 int ttt_kernel_attn_bwd_noalloc(int32_t n, int32_t H, int32_t Hkv, int32_t hd, int32_t W, int32_t R,
                                 int64_t pos0, const void* q, const void* kring, const void* vring, const void* o,
                                 const float* lse, int32_t ld_lse, const void* dout, float* dsum, void* dqkv,
@@ -108,9 +113,10 @@ int ttt_kernel_attn_bwd_noalloc(int32_t n, int32_t H, int32_t Hkv, int32_t hd, i
  * through; read the code with ttt_kernel_error(). */
 int ttt_kernel_wait_selftest(int64_t clocks, void* stream);
 
-/* Error word of the tensor-core kernels launched through this header since
- * the last call (0 = none; otherwise the code of a bounded wait that gave
- * up).  Synchronises the device. */
+/* Error word of the tensor-core kernels launched through this header on the
+ * current device since the last call, ttt_kernel_attn_bwd_noalloc included
+ * (0 = none; otherwise the code of a bounded wait that gave up).  Reading
+ * clears it.  Synchronises the device. */
 int ttt_kernel_error(void);
 
 #ifdef __cplusplus

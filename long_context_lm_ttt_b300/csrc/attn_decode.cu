@@ -218,7 +218,11 @@ void launch_part(const AttnArgs& a, int splits, float* part, cudaStream_t st) {
 }  // namespace
 
 bool attn_decode_supported(const AttnArgs& a) {
-  return a.n == 1 && a.hd % 32 == 0 && a.hd / 32 <= kMaxEpl && a.H % a.Hkv == 0 && a.H / a.Hkv <= kMaxGroup;
+  // the kernels read query, key and value rows with 16-byte vector loads
+  const bool aligned =
+      (((uintptr_t)a.q | (uintptr_t)a.kring | (uintptr_t)a.vring | (uintptr_t)a.o) & 15) == 0;
+  return a.n == 1 && a.hd % 32 == 0 && a.hd / 32 <= kMaxEpl && a.H % a.Hkv == 0 && a.H / a.Hkv <= kMaxGroup &&
+         aligned;
 }
 
 int attn_decode_splits(const AttnArgs& a, int num_sms) {

@@ -1200,6 +1200,11 @@ __global__ void __launch_bounds__(320, 1)
 // itself (keys 32hf.. -> columns 32hf.., 16 wide), so no warp overwrites
 // scores another warp still has to read; the dQ MMA takes its four K = 16
 // slices from columns {0, 8, 32, 40}.  The MMA warp ping-pongs the tiles.
+// Keys and values move through separate rings of DQ_STAGES blocks: a value
+// block is released once both tiles' dP products of it are issued, a key
+// block once both dQ products are, so the loads run two blocks ahead of the
+// products that need them.
+constexpr int DQ_STAGES = 3;
 template <int NA>
 struct Dq2Smem {
   static constexpr int Q_BYTES = NA * BM * 128;   // one 128-row tile
@@ -1207,9 +1212,11 @@ struct Dq2Smem {
   static constexpr int Q_OFF = 0;                 // Q0, Q1
   static constexpr int DO_OFF = 2 * Q_BYTES;      // dO0, dO1
   static constexpr int K_OFF = 4 * Q_BYTES;
-  static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
-  static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
+  static constexpr int V_OFF = K_OFF + DQ_STAGES * KV_BYTES;
+  static constexpr int BAR_OFF = V_OFF + DQ_STAGES * KV_BYTES;
   static constexpr int SMEM = BAR_OFF + 256 > 120 * 1024 ? BAR_OFF + 256 : 120 * 1024;
+  static_assert(SMEM <= 232448, "shared memory");
+  static_assert(8 + 32 * DQ_STAGES + 48 <= 192, "barrier area");
 };
 
 // key-block range of query tile t of the pair at r0 for the dq kernel
@@ -1236,17 +1243,22 @@ __global__ void __launch_bounds__(576, 1)
   using SM = Dq2Smem<NA>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = tc::smem_u32(smem);
+  constexpr int NS = DQ_STAGES;
   const uint32_t bar0 = sbase + SM::BAR_OFF;
   const uint32_t q_full = bar0;
-  const uint32_t k_full = bar0 + 8;      // [2] stages
-  const uint32_t v_full = bar0 + 24;     // [2]
-  const uint32_t kv_empty = bar0 + 40;   // [2]
-  const uint32_t s_full = bar0 + 56;     // [2] tiles
-  const uint32_t ds_full = bar0 + 72;    // [2] tiles
-  const uint32_t dq_done = bar0 + 88;
-  const uint32_t drain = bar0 + 96;
+  const uint32_t k_full = bar0 + 8;             // [NS] stages
+  const uint32_t v_full = k_full + 8 * NS;      // [NS]
+  const uint32_t k_empty = v_full + 8 * NS;     // [NS]
+  const uint32_t v_empty = k_empty + 8 * NS;    // [NS]
+  const uint32_t s_full = v_empty + 8 * NS;     // [2] tiles
+  const uint32_t ds_full = s_full + 16;         // [2] tiles
+  const uint32_t dq_done = ds_full + 16;
+  const uint32_t drain = dq_done + 8;
   uint32_t* tmem_slot = (uint32_t*)(smem + SM::BAR_OFF + 192);
   volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 196);
+  // stage and phase parity of the i-th block of the rings
+  auto stage_of = [](int i) { return i % NS; };
+  auto phase_of = [](int i) { return (uint32_t)((i / NS) & 1); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.x * 2 * BM, h = blockIdx.y, part = blockIdx.z;
@@ -1265,12 +1277,15 @@ __global__ void __launch_bounds__(576, 1)
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NS; ++s) {
       tc::mbar_init(k_full + 8 * s, 1);
       tc::mbar_init(v_full + 8 * s, 1);
-      tc::mbar_init(kv_empty + 8 * s, 1);
-      tc::mbar_init(s_full + 8 * s, 1);
-      tc::mbar_init(ds_full + 8 * s, 256);
+      tc::mbar_init(k_empty + 8 * s, 1);
+      tc::mbar_init(v_empty + 8 * s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      tc::mbar_init(s_full + 8 * t, 1);
+      tc::mbar_init(ds_full + 8 * t, 256);
     }
     tc::mbar_init(dq_done, 1);
     tc::mbar_init(drain, 1);
@@ -1295,7 +1310,7 @@ __global__ void __launch_bounds__(576, 1)
   if (warp == 0) {
     if (lane == 0 && nb > 0) {
       bool ok = true;
-      int issued = 0;
+      int issued_k = 0, issued_v = 0;
       tc::mbar_arrive_expect_tx(q_full, 4 * SM::Q_BYTES);
       for (int t = 0; t < 2; ++t)
         for (int a = 0; a < NA; ++a) {
@@ -1305,32 +1320,41 @@ __global__ void __launch_bounds__(576, 1)
                           r0 + BM * t, q_full);
         }
       for (int i = 0; i < nb && ok; ++i) {
-        const int st = i & 1;
-        if (!tc::mbar_wait(kv_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
+        const int st = stage_of(i);
+        const long long kpos = (jb + i) * BN;
+        const int row = kvh * p.R + (int)(kpos % p.R);
+        if (!tc::mbar_wait(k_empty + 8 * st, phase_of(i) ^ 1, p.err, ERR_A_PROD, abort)) {
           ok = false;
           break;
         }
-        const long long kpos = (jb + i) * BN;
-        const int row = kvh * p.R + (int)(kpos % p.R);
         tc::mbar_arrive_expect_tx(k_full + 8 * st, SM::KV_BYTES);
         for (int a = 0; a < NA; ++a)
           tc::tma_load_2d(sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN * 128, &mapK, 64 * a, row,
                           k_full + 8 * st);
+        issued_k = i + 1;
+        if (!tc::mbar_wait(v_empty + 8 * st, phase_of(i) ^ 1, p.err, ERR_A_PROD, abort)) {
+          ok = false;
+          break;
+        }
         tc::mbar_arrive_expect_tx(v_full + 8 * st, SM::KV_BYTES);
         for (int a = 0; a < NA; ++a)
           tc::tma_load_2d(sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN * 128, &mapV, 64 * a, row,
                           v_full + 8 * st);
-        issued = i + 1;
+        issued_v = i + 1;
       }
+      // the CTA must not exit with copies into its shared memory in flight
+      // (bounded: a failed role has already set the error word)
       const long long t0 = clock64();
       while (!tc::mbar_try_wait(q_full, 0) && clock64() - t0 < tc::kWaitClocks) {
       }
-      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
-        const int st = i & 1;
-        const uint32_t par = (i >> 1) & 1;
+      for (int i = (issued_k > NS ? issued_k - NS : 0); i < issued_k; ++i) {
         const long long t1 = clock64();
-        while (!(tc::mbar_try_wait(k_full + 8 * st, par) && tc::mbar_try_wait(v_full + 8 * st, par)) &&
-               clock64() - t1 < tc::kWaitClocks) {
+        while (!tc::mbar_try_wait(k_full + 8 * stage_of(i), phase_of(i)) && clock64() - t1 < tc::kWaitClocks) {
+        }
+      }
+      for (int i = (issued_v > NS ? issued_v - NS : 0); i < issued_v; ++i) {
+        const long long t1 = clock64();
+        while (!tc::mbar_try_wait(v_full + 8 * stage_of(i), phase_of(i)) && clock64() - t1 < tc::kWaitClocks) {
         }
       }
     }
@@ -1342,9 +1366,9 @@ __global__ void __launch_bounds__(576, 1)
       bool issued = false;
       int cnt[2] = {0, 0};
       auto issue_sdp = [&](int t, int i) -> bool {
-        const int st = i & 1;
-        if (!tc::mbar_wait(k_full + 8 * st, (i >> 1) & 1, p.err, ERR_A_MMA, abort) ||
-            !tc::mbar_wait(v_full + 8 * st, (i >> 1) & 1, p.err, ERR_A_MMA, abort))
+        const int st = stage_of(i);
+        if (!tc::mbar_wait(k_full + 8 * st, phase_of(i), p.err, ERR_A_MMA, abort) ||
+            !tc::mbar_wait(v_full + 8 * st, phase_of(i), p.err, ERR_A_MMA, abort))
           return false;
         tc::tc_fence_after();
         const uint32_t kb = sbase + SM::K_OFF + st * SM::KV_BYTES;
@@ -1363,12 +1387,17 @@ __global__ void __launch_bounds__(576, 1)
         issued = true;
         return true;
       };
+      // Issue order per block i: dQ(0, i), S/dP(0, i+1), [release K(i)],
+      // dQ(1, i), S/dP(1, i+1), [release V(i+1)].  Every block of the part
+      // is used by at least one tile, so each ring slot is released exactly
+      // once per use.
 #pragma unroll
       for (int t = 0; t < 2; ++t)
         if (ok && part_of(t, jb)) ok = issue_sdp(t, 0);
+      if (ok) tc::mma_commit(v_empty + 8 * stage_of(0));
       for (int i = 0; i < nb && ok; ++i) {
         const long long j = jb + i;
-        const int st = i & 1;
+        const int st = stage_of(i);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
@@ -1385,9 +1414,13 @@ __global__ void __launch_bounds__(576, 1)
                           tc::smem_desc_sw128(kb + 2048 * k, BN * 128, 1024), idQ, (cnt[t] > 0 || k > 0) ? 1u : 0u);
             ++cnt[t];
           }
+          // both dQ products of block i are issued: its key slot frees
+          // when they complete
+          if (t == 1) tc::mma_commit(k_empty + 8 * st);
           if (i + 1 < nb && part_of(t, j + 1)) ok = issue_sdp(t, i + 1);
         }
-        if (ok) tc::mma_commit(kv_empty + 8 * st);
+        // both dP products of block i + 1 are issued: its value slot frees
+        if (ok && i + 1 < nb) tc::mma_commit(v_empty + 8 * stage_of(i + 1));
       }
       if (ok) tc::mma_commit(dq_done);
       if (!ok && issued) {
@@ -1861,12 +1894,10 @@ int launch_fwd(const AttnArgs& a, int* err, cudaStream_t st) {
   if (!rc) rc = map2d(&mk, a.kring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
   if (!rc) rc = map2d(&mv, a.vring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
   if (rc) return rc;
-  static std::atomic<bool> attr{false};
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SM::SMEM);
+  static std::atomic<uint64_t> attr{0};
+  {
+    cudaError_t e = raise_smem_limit(attr, attn_fwd_tc_kernel<NA>, SM::SMEM);
     if (e != cudaSuccess) return (int)e;
-    attr = true;
   }
   FwdParams p;
   p.n = a.n;
@@ -1896,12 +1927,10 @@ int launch_fwd2(const AttnArgs& a, int* err, cudaStream_t st) {
   if (!rc) rc = map2d(&mk, a.kring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN2);
   if (!rc) rc = map2d(&mv, a.vring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN2);
   if (rc) return rc;
-  static std::atomic<bool> attr{false};
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd2_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SM::SMEM);
+  static std::atomic<uint64_t> attr{0};
+  {
+    cudaError_t e = raise_smem_limit(attr, attn_fwd2_tc_kernel<NA>, SM::SMEM);
     if (e != cudaSuccess) return (int)e;
-    attr = true;
   }
   FwdParams p;
   p.n = a.n;
@@ -1988,14 +2017,11 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
   if (!rc) rc = map2d(&mk, a.kring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
   if (!rc) rc = map2d(&mv, a.vring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
   if (rc) return rc;
-  static std::atomic<bool> attr{false};
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_dq2_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DQ::SMEM);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_dkv_tc_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize, DKV::SMEM);
+  static std::atomic<uint64_t> attr_dq{0}, attr_dkv{0};
+  {
+    cudaError_t e = raise_smem_limit(attr_dq, attn_dq2_tc_kernel<NA>, DQ::SMEM);
+    if (e == cudaSuccess) e = raise_smem_limit(attr_dkv, attn_dkv_tc_kernel<NA>, DKV::SMEM);
     if (e != cudaSuccess) return (int)e;
-    attr = true;
   }
   BwdParams p;
   p.n = a.n;

@@ -195,7 +195,7 @@ struct Engine : EngineBase {
     float *g_attn = nullptr, *g_mlp = nullptr;
     T *wqkv = nullptr, *wo = nullptr, *wgu = nullptr, *wd = nullptr;
     float *wgu32 = nullptr, *wd32 = nullptr;            // fast layers: fp32 value
-    T *wgu_lo = nullptr, *wd_lo = nullptr;              // bf16 fast layers: w ~ hi + lo
+    T *wgu_lo = nullptr, *wd_lo = nullptr;              // bf16: w ~ hi + lo (null: hi alone)
     float *wgu32_init = nullptr, *wd32_init = nullptr;  // for ttt_reset
     T *kring = nullptr, *vring = nullptr;
     int R = 0;  // ring slots
@@ -381,8 +381,10 @@ struct Engine : EngineBase {
           if ((rc = upload<float>(w->w_gate[l], ff, d, 2, y.wgu32, st))) return rc;
           if ((rc = upload<float>(w->w_up[l], ff, d, 3, y.wgu32, st))) return rc;
           if ((rc = upload<float>(w->w_down[l], d, ff, 0, y.wd32, st))) return rc;
-          A_TRY(y.wgu_lo, (size_t)2 * ff * d);
-          A_TRY(y.wd_lo, (size_t)d * ff);
+          if (!cfg.fast_bf16_single) {
+            A_TRY(y.wgu_lo, (size_t)2 * ff * d);
+            A_TRY(y.wd_lo, (size_t)d * ff);
+          }
           launch_split_bf16(y.wgu32, 2 * (int64_t)ff * d, (bf16*)y.wgu, (bf16*)y.wgu_lo, st);
           launch_split_bf16(y.wd32, (int64_t)d * ff, (bf16*)y.wd, (bf16*)y.wd_lo, st);
         } else {
@@ -518,7 +520,7 @@ struct Engine : EngineBase {
       case EPI_CE_Z: case EPI_CE_ACC: cls = P_GEMM_LMHEAD; out_b *= 2; break;
       case EPI_SWIGLU_BWD: cls = P_GEMM_BWD; out_b = (double)M * N * 4 * sizeof(T); break;
       case EPI_STORE: cls = P_GEMM_BWD; break;
-      case EPI_SGD: cls = P_GEMM_SGD; out_b = (double)M * N * (8 + 2 * sizeof(T)); break;
+      case EPI_SGD: cls = P_GEMM_SGD; out_b = (double)M * N * (8 + (e.w16lo ? 2 : 1) * sizeof(T)); break;
       case EPI_SWIGLU: out_b = (double)M * N * sizeof(T) * (e.stash ? 1.5 : 0.5); break;
       default: break;
     }
@@ -666,8 +668,9 @@ struct Engine : EngineBase {
     e.ldo = ff;
     e.stash = fast ? S.gu : nullptr;
     e.ld_stash = 2 * (int64_t)ff;
-    // fast weights in bf16 mode are read as the pair hi + lo, so updates
-    // below one bf16 ulp still reach the forward
+    // fast weights in bf16 mode: the pair hi + lo of the master, so updates
+    // below one bf16 ulp still reach the forward, or with fast_bf16_single
+    // the bf16 copy alone (the low halves are null then)
     gemm(n, 2 * ff, d, S.hn, d, 0, y.wgu, d, 0, e, st, rc, y.wgu_lo);
     const bool dual = fast && cfg.dual_mlp;
     e = epi(EPI_RESID);
@@ -1175,6 +1178,14 @@ static int validate(const ttt_config* c, std::string& msg) {
     msg = "dual_mlp must be 0 or 1";
     return TTT_ERR_INVALID;
   }
+  if (c->bulk_tokens < 0) {
+    msg = "bulk_tokens must be >= 0 (0: automatic)";
+    return TTT_ERR_INVALID;
+  }
+  if (c->fast_bf16_single != 0 && c->fast_bf16_single != 1) {
+    msg = "fast_bf16_single must be 0 or 1";
+    return TTT_ERR_INVALID;
+  }
   if (c->n_heads % c->n_kv_heads) {
     msg = "n_heads must be a multiple of n_kv_heads";
     return TTT_ERR_SHAPE;
@@ -1224,11 +1235,13 @@ extern "C" int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* str
   eng->prof_clear();
   const int need = cfg->window + cfg->chunk - 1;
   eng->R = ((need + 127) / 128) * 128;
-  // super-chunk of the bulk static pass: a multiple of b, about 16K tokens,
-  // never more than the longest sequence needs
+  // super-chunk of the bulk static pass: a multiple of b, about 16K tokens
+  // unless the configuration names another length, never more than the
+  // longest sequence needs
   {
     const int64_t b = cfg->chunk;
-    const int64_t want = std::max<int64_t>(b, (16384 / b) * b);
+    const int64_t asked = cfg->bulk_tokens > 0 ? cfg->bulk_tokens : 16384;
+    const int64_t want = std::max<int64_t>(b, (asked / b) * b);
     const int64_t cap = ((cfg->max_tokens + b - 1) / b) * b;
     eng->S_bulk = (int)std::min(want, cap);
     const int64_t need_s = (int64_t)cfg->window + eng->S_bulk - 1;

@@ -5,12 +5,29 @@
 #include "../../include/ttt_kernels.h"
 #include "kernels.h"
 
+namespace ttt {
+// code of a bounded wait of ttt_kernel_attn_bwd_noalloc that gave up on the
+// current device, cleared by the read (noalloc.cu)
+int noalloc_take_wait_error();
+}  // namespace ttt
+
 namespace {
-int* g_err = nullptr;  // device error word shared by kernel-level launches
+constexpr int kDevs = 64;
+// device error word shared by the kernel-level launches, one per device;
+// g_err names the current device's word after ensure_err()
+int* g_err_of[kDevs] = {};
+int* g_err = nullptr;
 int ensure_err() {
-  if (g_err) return 0;
-  if (cudaMalloc(&g_err, sizeof(int)) != cudaSuccess) return TTT_ERR_OOM;
-  return cudaMemset(g_err, 0, sizeof(int)) == cudaSuccess ? 0 : TTT_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return TTT_ERR_CUDA;
+  if (!g_err_of[dev]) {
+    int* p = nullptr;
+    if (cudaMalloc(&p, sizeof(int)) != cudaSuccess) return TTT_ERR_OOM;
+    if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return TTT_ERR_CUDA;
+    g_err_of[dev] = p;
+  }
+  g_err = g_err_of[dev];
+  return 0;
 }
 }  // namespace
 
@@ -18,7 +35,7 @@ extern "C" int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, i
                                const void* B, int64_t ldb, int32_t b_mn, const void* B2, float* C,
                                int64_t ldc, int32_t impl, void* stream) {
   if (!A || !B || !C || M < 0 || N < 0 || K < 1 || (N & 1) || (ldc & 1)) return TTT_ERR_INVALID;
-  if (ensure_err()) return TTT_ERR_OOM;
+  if (int r = ensure_err()) return r;
   cudaStream_t st = (cudaStream_t)stream;
   ttt::Epi e;
   memset(&e, 0, sizeof(e));
@@ -54,7 +71,7 @@ extern "C" int ttt_kernel_gemm_sgd(int32_t M, int32_t N, int32_t K, const void* 
                                    int64_t ldw, float lr, int32_t impl, void* stream) {
   if (!A || !B || !w32 || M < 0 || N < 0 || K < 1 || (N & 1) || (ldw & 1) || ldw < N) return TTT_ERR_INVALID;
   if (impl < 0 || impl > 3) return TTT_ERR_INVALID;
-  if (ensure_err()) return TTT_ERR_OOM;
+  if (int r = ensure_err()) return r;
   cudaStream_t st = (cudaStream_t)stream;
   ttt::Epi e;
   memset(&e, 0, sizeof(e));
@@ -116,14 +133,14 @@ extern "C" int ttt_kernel_attn_fwd(int32_t impl, int32_t n, int32_t H, int32_t H
   int rc = attn_check(impl, n, H, Hkv, hd, W, R, 4);
   if (rc) return rc;
   if (!q || !kring || !vring || !o || !lse || ld_lse < n) return TTT_ERR_INVALID;
-  if (ensure_err()) return TTT_ERR_OOM;
   ttt::AttnArgs a = attn_args(n, H, Hkv, hd, W, R, pos0, q, kring, vring, o, lse, ld_lse);
+  // shape and alignment of the one-query kernel, checked before any device work
+  if (impl == 4 && !ttt::attn_decode_supported(a)) return TTT_ERR_SHAPE;
+  if (int r = ensure_err()) return r;
   cudaStream_t st = (cudaStream_t)stream;
   if (impl == 4) {
     // one query position (a decode step): the key range split over the GPU
-    if (!ttt::attn_decode_supported(a)) return TTT_ERR_SHAPE;
     // slice scratch per device, grown as needed and kept for the process
-    constexpr int kDevs = 64;
     static float* part_of[kDevs] = {};
     static size_t elems_of[kDevs] = {};
     int dev = 0, sms = 148;
@@ -157,7 +174,7 @@ extern "C" int ttt_kernel_attn_bwd(int32_t impl, int32_t n, int32_t H, int32_t H
   int rc = attn_check(impl, n, H, Hkv, hd, W, R);
   if (rc) return rc;
   if (!q || !kring || !vring || !o || !lse || !dout || !dsum || !dqkv || ld_lse < n) return TTT_ERR_INVALID;
-  if (ensure_err()) return TTT_ERR_OOM;
+  if (int r = ensure_err()) return r;
   ttt::AttnArgs a = attn_args(n, H, Hkv, hd, W, R, pos0, q, kring, vring, nullptr, const_cast<float*>(lse),
                               ld_lse);
   a.out = o;
@@ -166,19 +183,22 @@ extern "C" int ttt_kernel_attn_bwd(int32_t impl, int32_t n, int32_t H, int32_t H
   a.dqkv = dqkv;
   cudaStream_t st = (cudaStream_t)stream;
   if (impl == 0) {
-    // scratch for this entry point: grown on demand, kept for later calls
-    static float* ws = nullptr;
-    static int64_t ws_elems = 0;
+    // scratch for this entry point, per device: grown on demand, kept for
+    // later calls (calls on one device must not overlap)
+    static float* ws_of[kDevs] = {};
+    static int64_t elems_of[kDevs] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return TTT_ERR_CUDA;
     const int64_t need = ttt::attn_bwd_tc_ws_elems(n, H, hd, 0);
-    if (need > ws_elems) {
-      if (ws) cudaFree(ws);
-      ws = nullptr;
-      ws_elems = 0;
-      if (cudaMalloc(&ws, need * sizeof(float)) != cudaSuccess) return TTT_ERR_OOM;
-      ws_elems = need;
+    if (need > elems_of[dev]) {
+      if (ws_of[dev]) cudaFree(ws_of[dev]);
+      ws_of[dev] = nullptr;
+      elems_of[dev] = 0;
+      if (cudaMalloc(&ws_of[dev], need * sizeof(float)) != cudaSuccess) return TTT_ERR_OOM;
+      elems_of[dev] = need;
     }
-    a.ws = ws;
-    a.ws_elems = ws_elems;
+    a.ws = ws_of[dev];
+    a.ws_elems = elems_of[dev];
     if (!ttt::attn_bwd_tc_supported(a)) return TTT_ERR_SHAPE;
     rc = ttt::attn_bwd_tc(a, g_err, st);
     if (rc == (int)cudaErrorNotSupported) return TTT_ERR_SHAPE;
@@ -216,16 +236,17 @@ __global__ void wait_selftest_kernel(long long budget, int* err) {
 
 extern "C" int ttt_kernel_wait_selftest(int64_t clocks, void* stream) {
   if (clocks < 1 || clocks > 2000000000LL) return TTT_ERR_INVALID;
-  if (ensure_err()) return TTT_ERR_OOM;
+  if (int r = ensure_err()) return r;
   wait_selftest_kernel<<<1, 1, 0, (cudaStream_t)stream>>>((long long)clocks, g_err);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
 }
 
 extern "C" int ttt_kernel_error(void) {
-  if (ensure_err()) return TTT_ERR_OOM;
+  if (int r = ensure_err()) return r;
   if (cudaDeviceSynchronize() != cudaSuccess) return TTT_ERR_CUDA;
   int h = 0;
-  cudaMemcpy(&h, g_err, sizeof(int), cudaMemcpyDeviceToHost);
-  cudaMemset(g_err, 0, sizeof(int));
-  return h;
+  if (cudaMemcpy(&h, g_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TTT_ERR_CUDA;
+  if (cudaMemset(g_err, 0, sizeof(int)) != cudaSuccess) return TTT_ERR_CUDA;
+  const int h2 = ttt::noalloc_take_wait_error();
+  return h != 0 ? h : h2;
 }

@@ -288,7 +288,7 @@ __global__ void split_bf16_kernel(const float* __restrict__ w, int64_t n, bf16* 
        i += (int64_t)gridDim.x * blockDim.x) {
     const bf16 h = __float2bfloat16_rn(w[i]);
     hi[i] = h;
-    lo[i] = __float2bfloat16_rn(w[i] - __bfloat162float(h));
+    if (lo) lo[i] = __float2bfloat16_rn(w[i] - __bfloat162float(h));
   }
 }
 

@@ -3,9 +3,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace ttt {
+
+// cudaFuncSetAttribute acts on the current device only.  `done` remembers
+// the devices (bit d for device d < 64) on which `kern`'s dynamic shared
+// memory limit is already raised to `bytes`; devices beyond 64 are set on
+// every call.
+template <typename K>
+inline cudaError_t raise_smem_limit(std::atomic<uint64_t>& done, K kern, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0;
+  if (bit && (done.load() & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit);
+  return e;
+}
 
 template <typename T>
 struct GemmArgs {
@@ -78,7 +96,8 @@ template <typename T>
 void launch_pack(const float* src, int64_t rows, int64_t cols, int mode, int hd, T* dst,
                  cudaStream_t st);
 void launch_f32_to_bf16(const float* src, int64_t n, bf16* dst, cudaStream_t st);
-// hi = rn(w), lo = rn(w - hi): a bf16 pair whose sum carries ~16 mantissa bits
+// hi = rn(w), lo = rn(w - hi): a bf16 pair whose sum carries ~16 mantissa
+// bits (lo may be null: hi alone)
 void launch_split_bf16(const float* w, int64_t n, bf16* hi, bf16* lo, cudaStream_t st);
 
 // --- attention (attn_simt.cu / attn_mma.cu) --------------------------------

@@ -2,24 +2,25 @@
 // with its scratch in a fixed device array instead of memory from
 // cudaMalloc, for callers that must not allocate.
 //
-// Who cannot allocate: code that runs while a CUDA graph is being captured
-// in the global capture mode (cudaMalloc is an unsafe call there and fails
-// the capture), code whose device memory is owned by a framework's caching
-// allocator or a fixed budget (a cudaMalloc outside it can fail once that
-// allocator holds the free memory, and escapes its accounting), and
-// real-time callers that plan every byte before they start.
+// Who cannot allocate: code whose device memory is owned by a framework's
+// caching allocator or by a fixed budget (a cudaMalloc outside it can fail
+// once that allocator holds the free memory, and escapes its accounting),
+// and real-time callers that plan every byte before they start and may not
+// block in the driver's allocator in the middle of a step.
 //
 // The scratch is a file-scope __device__ array of kMaxScratchFloats fp32
-// values (32 MiB).  Every GPU on which this entry point runs holds it until
-// the process exits.  Host code cannot use the array's name as a device
-// address (in host code it names a host-side stand-in), so the first call
-// on each device looks up the real address with cudaGetSymbolAddress, with
-// that device current, and caches it; that first call should therefore come
-// before any stream capture.  All calls share the array and it keeps the
-// last call's contents: nothing in it needs to start at zero (every value
-// the reductions read was written earlier in the same call), and calls that
-// overlap on the GPU (different streams, or different host threads) race on
-// it.
+// values (32 MiB).  A device context that loads this module reserves it
+// until the process exits: with lazy module loading (the CUDA default) that
+// happens at the first use of the module on the device, with eager loading
+// (CUDA_MODULE_LOADING=EAGER) when the context is created.  Host code cannot
+// use the array's name as a device address (in host code it names a
+// host-side stand-in), so the first call on each device looks up the real
+// address with cudaGetSymbolAddress, with that device current, and caches
+// it; that first call should therefore come before any stream capture.  All
+// calls share the array and it keeps the last call's contents: nothing in it
+// needs to start at zero (every value the reductions read was written
+// earlier in the same call), and calls that overlap on the GPU (different
+// streams, or different host threads) race on it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -34,7 +35,8 @@ constexpr int64_t kMaxScratchFloats = 8ll << 20;  // 32 MiB of fp32
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_scratch[kMaxScratchFloats];
-// code of a bounded device-side wait that gave up (kept for inspection)
+// code of a bounded device-side wait that gave up; read and cleared by
+// ttt_kernel_error()
 static __device__ int g_wait_error;
 
 std::mutex g_mu;
@@ -99,3 +101,22 @@ extern "C" int ttt_kernel_attn_bwd_noalloc(int32_t n, int32_t H, int32_t Hkv, in
   if (rc == (int)cudaErrorNotSupported) return TTT_ERR_SHAPE;
   return rc ? TTT_ERR_CUDA : TTT_OK;
 }
+
+namespace ttt {
+// The wait code of the device that is current, read and cleared with plain
+// copies (nothing allocated).  0 when the entry point never ran on it.
+int noalloc_take_wait_error() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int* e = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    e = g_err_ptr[dev];
+  }
+  if (!e) return 0;
+  int h = 0;
+  if (cudaMemcpy(&h, e, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TTT_ERR_CUDA;
+  if (h != 0 && cudaMemset(e, 0, sizeof(int)) != cudaSuccess) return TTT_ERR_CUDA;
+  return h;
+}
+}  // namespace ttt

@@ -42,7 +42,7 @@ class ttt_config(ctypes.Structure):
                 ("vocab", c_int32), ("window", c_int32), ("chunk", c_int32),
                 ("n_ttt_layers", c_int32), ("precision", c_int32), ("lr", c_float),
                 ("rope_theta", c_float), ("norm_eps", c_float), ("max_tokens", c_int64),
-                ("dual_mlp", c_int32)]
+                ("dual_mlp", c_int32), ("bulk_tokens", c_int32), ("fast_bf16_single", c_int32)]
 
 
 class ttt_weights(ctypes.Structure):
@@ -154,13 +154,14 @@ def _check(rc: int, ctx=None):
 
 
 def make_config(shape, precision: int = TTT_BF16, max_tokens: Optional[int] = None,
-                lr: Optional[float] = None) -> ttt_config:
+                lr: Optional[float] = None, bulk_tokens: int = 0, fast_bf16_single: bool = False) -> ttt_config:
     """ttt_config from any object with the ModelShape field names."""
     return ttt_config(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads, shape.head_dim,
                       shape.d_ff, shape.vocab, shape.window, shape.chunk, shape.n_ttt_layers, precision,
                       shape.lr if lr is None else lr, shape.rope_theta, shape.norm_eps,
                       max_tokens if max_tokens is not None else shape.seq_len,
-                      1 if getattr(shape, "dual_mlp", False) else 0)
+                      1 if getattr(shape, "dual_mlp", False) else 0, int(bulk_tokens),
+                      1 if fast_bf16_single else 0)
 
 
 def make_weights(w: dict):
@@ -289,9 +290,10 @@ class TTT:
     """One test-time-training context on the current CUDA device."""
 
     def __init__(self, shape, weights: dict, precision: int = TTT_BF16,
-                 max_tokens: Optional[int] = None, lr: Optional[float] = None, stream=None):
+                 max_tokens: Optional[int] = None, lr: Optional[float] = None, stream=None,
+                 bulk_tokens: int = 0, fast_bf16_single: bool = False):
         self.shape = shape
-        self.cfg = make_config(shape, precision, max_tokens, lr)
+        self.cfg = make_config(shape, precision, max_tokens, lr, bulk_tokens, fast_bf16_single)
         ws, keep = make_weights(weights)
         self.ctx = ttt_create(self.cfg, ws, stream)
         del keep

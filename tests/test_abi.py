@@ -39,11 +39,14 @@ def test_exports_every_declared_call(lib):
 
 
 def test_struct_layout():
-    # 11 int32, 3 float, int64 max_tokens, int32 dual_mlp (+ 4 bytes of tail
-    # padding to the int64 alignment), as the C declaration lays them out
-    assert ctypes.sizeof(T.ttt_config) == 11 * 4 + 3 * 4 + 8 + 8
+    # 11 int32, 3 float, int64 max_tokens, int32 dual_mlp, bulk_tokens and
+    # fast_bf16_single (+ 4 bytes of tail padding to the int64 alignment), as the
+    # C declaration lays them out
+    assert ctypes.sizeof(T.ttt_config) == 11 * 4 + 3 * 4 + 8 + 3 * 4 + 4
     assert T.ttt_config.max_tokens.offset == 56
     assert T.ttt_config.dual_mlp.offset == 64
+    assert T.ttt_config.bulk_tokens.offset == 68
+    assert T.ttt_config.fast_bf16_single.offset == 72
     assert ctypes.sizeof(T.ttt_weights) == 16 * ctypes.sizeof(ctypes.c_void_p)
 
 
@@ -60,6 +63,8 @@ def _cfg(**kw):
     (dict(n_ttt_layers=3), T.TTT_ERR_INVALID),
     (dict(n_ttt_layers=-1), T.TTT_ERR_INVALID),
     (dict(dual_mlp=2), T.TTT_ERR_INVALID),
+    (dict(bulk_tokens=-1), T.TTT_ERR_INVALID),
+    (dict(fast_bf16_single=2), T.TTT_ERR_INVALID),
     (dict(n_kv_heads=3), T.TTT_ERR_SHAPE),
     (dict(head_dim=31), T.TTT_ERR_SHAPE),
     (dict(lr=float("nan")), T.TTT_ERR_NONFINITE),
@@ -95,3 +100,23 @@ def test_prefill_batch_rejects_null_contexts(lib):
         T.ttt_prefill_batch([ctypes.c_void_p(), ctypes.c_void_p()], toks, [8, 8], losses)
     assert e.value.code == T.TTT_ERR_INVALID
     assert lib.ttt_prefill_batch(None, 2, None, None, None, None) == T.TTT_ERR_INVALID
+
+
+@pytest.mark.parametrize("offset", [0, 2, 8])
+def test_decode_attention_rejects_misaligned_rows(lib, offset):
+    """The one-query attention kernel (impl 4) reads rows with 16-byte loads:
+    a key, value, query or output pointer off a 16-byte boundary returns
+    TTT_ERR_SHAPE before any device work.  The addresses are never
+    dereferenced (an aligned set is rejected for its head count instead)."""
+    base = 0x10000
+    H, Hkv, hd, W = 4, 2, 64, 64
+    R = 128
+    args = [base, base + 0x1000, base + 0x2000, base + 0x3000]
+    for i in range(4):
+        a = list(args)
+        a[i] += offset
+        # 9 query heads per KV head exceed the kernel's limit: even the
+        # aligned case stops at the shape check, so nothing reaches a GPU
+        Hq = Hkv * 9 if offset == 0 else H
+        rc = lib.ttt_kernel_attn_fwd(4, 1, Hq, Hkv, hd, W, R, 5, a[0], a[1], a[2], a[3], base + 0x4000, 1, None)
+        assert rc == T.TTT_ERR_SHAPE, (i, offset, rc)

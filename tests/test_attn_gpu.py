@@ -272,3 +272,79 @@ def test_attn_bwd_deterministic():
     assert T.ttt_kernel_error() == 0
     assert torch.equal(outs[0], outs[1])
     assert torch.isfinite(outs[0].float()).all()
+
+
+def ref_backward_heads(q, kr, vr, dout, n, H, Hkv, hd, W, pos0, kv_heads):
+    """The backward restated with whole-chunk matrix products for the query
+    heads of the given KV heads: {('dq', h): [n, hd], ('dk', kv): [n, hd],
+    ('dv', kv): [n, hd]} (dk, dv of the chunk's own keys, summed over the
+    KV head's query heads)."""
+    R = kr.shape[1]
+    g = H // Hkv
+    js = np.arange(max(0, pos0 - W + 1), pos0 + n)
+    slots = js % R
+    t = pos0 + np.arange(n)
+    rel = t[:, None] - js[None, :]
+    allowed = (rel >= 0) & (rel < W)
+    own = js >= pos0
+    out = {}
+    for kv in kv_heads:
+        K = kr[kv, slots].astype(np.float64)
+        V = vr[kv, slots].astype(np.float64)
+        dk = np.zeros((n, hd))
+        dv = np.zeros((n, hd))
+        for h in range(kv * g, (kv + 1) * g):
+            Q = q[:, h * hd:(h + 1) * hd].astype(np.float64)
+            dO = dout[:, h * hd:(h + 1) * hd].astype(np.float64)
+            S = np.where(allowed, Q @ K.T / math.sqrt(hd), -np.inf)
+            P = np.exp(S - S.max(axis=1, keepdims=True))
+            P /= P.sum(axis=1, keepdims=True)
+            O = P @ V
+            dS = P * (dO @ V.T - (dO * O).sum(axis=1, keepdims=True)) / math.sqrt(hd)
+            out[("dq", h)] = dS @ K
+            dk += dS[:, own].T @ Q
+            dv += P[:, own].T @ dO
+        out[("dk", kv)] = dk
+        out[("dv", kv)] = dv
+    return out
+
+
+@pytest.mark.parametrize("pos0", [40 * 1024, 1024])
+def test_attn_bwd_3b_shape_heads(pos0):
+    """The backward at the 3B chunk shape (1024 rows, 24 q / 8 KV heads x
+    128, window 8192 in a 9216-slot ring) as the inner loop runs it: deep in
+    the sequence the dq kernel splits the window's key blocks into parts
+    summed in a fixed order; near the start the window is still short.
+    Every row of two KV groups (KV heads 0 and 7 with their 6 query heads)
+    against the restatement in float64."""
+    torch, T = _env()
+    n, H, Hkv, hd, W, R = 1024, 24, 8, 128, 8192, 9216
+    q, kr, vr = make_case(n, H, Hkv, hd, W, pos0, R, seed=5 + pos0 % 7)
+    rng = np.random.default_rng(pos0)
+    dout = inputs.round_bf16(rng.standard_normal((n, H * hd)).astype(np.float32))
+    cu = lambda a: torch.from_numpy(a).to(torch.bfloat16).cuda()
+    dq_, dk_, dv_, do_ = cu(q), cu(kr), cu(vr), cu(dout)
+    lib = T.load()
+    o = torch.zeros((n, H * hd), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((H, n), dtype=torch.float32, device="cuda")
+    assert lib.ttt_kernel_attn_fwd(0, n, H, Hkv, hd, W, R, pos0, dq_.data_ptr(), dk_.data_ptr(), dv_.data_ptr(),
+                                   o.data_ptr(), lse.data_ptr(), n, None) == 0
+    dsum = torch.zeros((H, n), dtype=torch.float32, device="cuda")
+    g = torch.full((n, (H + 2 * Hkv) * hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert lib.ttt_kernel_attn_bwd(0, n, H, Hkv, hd, W, R, pos0, dq_.data_ptr(), dk_.data_ptr(), dv_.data_ptr(),
+                                   o.data_ptr(), lse.data_ptr(), n, do_.data_ptr(), dsum.data_ptr(), g.data_ptr(),
+                                   None) == 0
+    torch.cuda.synchronize()
+    assert T.ttt_kernel_error() == 0
+    got = g.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    ref = ref_backward_heads(q, kr, vr, dout, n, H, Hkv, hd, W, pos0, kv_heads=(0, Hkv - 1))
+    for (name, h), b in ref.items():
+        if name == "dq":
+            a = got[:, h * hd:(h + 1) * hd]
+        elif name == "dk":
+            a = got[:, (H + h) * hd:(H + h + 1) * hd]
+        else:
+            a = got[:, (H + Hkv + h) * hd:(H + Hkv + h + 1) * hd]
+        err = np.abs(a - b).max() / max(np.abs(b).max(), 1e-6)
+        assert err < 2e-2, (name, h, err)
