@@ -63,10 +63,13 @@ int ttt_kernel_gemm_sgd(int32_t M, int32_t N, int32_t K, const void* A, int64_t 
  *   dsum  [H, ld_lse]      fp32 scratch of the backward (rowsum(dO * O))
  * R must cover W + n - 1 positions.  impl 0: tcgen05 tensor cores
  * (64 <= hd <= 128, hd % 16 == 0, R % 128 == 0, 16-byte aligned bases,
- * else TTT_ERR_SHAPE), kernel variant chosen by size; impl 1: SIMT fp32
+ * else TTT_ERR_SHAPE), kernel variant chosen by size (the forward may split
+ * each query tile pair's key range into parts merged by a second kernel,
+ * through fp32 scratch allocated per device on first use and kept, so
+ * forward calls on one device must not overlap); impl 1: SIMT fp32
  * arithmetic.  Forward only: impl 2 forces the tensor-core kernel with one
  * 128-row query tile per CTA, impl 3 the one with two tiles per CTA and P
- * kept in tensor memory, impl 4 the one-query kernel of a decode step
+ * kept in tensor memory (never split), impl 4 the one-query kernel of a decode step
  * (n == 1, hd a multiple of 32, at most 8 query heads per KV head, q,
  * kring, vring and o 16-byte aligned, else TTT_ERR_SHAPE before any device
  * work; its slice scratch is allocated per device on first use and kept, so

@@ -78,6 +78,13 @@ struct FwdParams {
   float* lse;
   int ld_lse;
   int* err;
+  // two-tile kernel with the key range split into parts (parts > 1): part
+  // z leaves its unnormalised output in ws[z][row][H*hd] and its row
+  // statistics (max in log2 units, sum) in ws_ml[z][h][row][2]; a combine
+  // kernel merges the parts
+  int parts;
+  float* ws;
+  float* ws_ml;
 };
 
 // first key block and block count of the query tile starting at row r0
@@ -582,14 +589,17 @@ __global__ void __launch_bounds__(576, 1)
   volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 196);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = blockIdx.x * 2 * BM, h = blockIdx.y;
+  const int r0 = blockIdx.x * 2 * BM, h = blockIdx.y, zpart = blockIdx.z;
   const int kvh = h / (p.H / p.Hkv);
   long long lo_t[2], hi_t[2];
   tile2_range(p, r0, 0, &lo_t[0], &hi_t[0]);
   tile2_range(p, r0, 1, &lo_t[1], &hi_t[1]);
-  const long long kb_lo = lo_t[0];
-  const long long kb_hi = hi_t[1] >= lo_t[1] ? max(hi_t[0], hi_t[1]) : hi_t[0];
-  const int nbl = (int)(kb_hi - kb_lo + 1);
+  // the pair's key blocks, and this part's share of them
+  const long long u_lo = lo_t[0];
+  const long long u_hi = hi_t[1] >= lo_t[1] ? max(hi_t[0], hi_t[1]) : hi_t[0];
+  const long long nb_all = u_hi - u_lo + 1;
+  const long long kb_lo = u_lo + zpart * nb_all / p.parts;
+  const int nbl = (int)(u_lo + (zpart + 1) * nb_all / p.parts - kb_lo);
   auto part = [&](int t, long long j) { return j >= lo_t[t] && j <= hi_t[t]; };
   const int ksteps = p.hd / 16;
   const int nO = (p.hd + 15) & ~15;
@@ -626,7 +636,7 @@ __global__ void __launch_bounds__(576, 1)
   // columns: S/P of tile 0 | S/P of tile 1 | O of tile 0 | O of tile 1
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && nbl > 0) {
       bool ok = true;
       int issued = 0;
       tc::mbar_arrive_expect_tx(q_full, 2 * SM::Q_BYTES);
@@ -672,7 +682,7 @@ __global__ void __launch_bounds__(576, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && nbl > 0) {
       const uint32_t idS = tc::idesc_bf16(BM, BN2, 0, 0);
       const uint32_t idO = tc::idesc_bf16(BM, nO, 0, 1);
       bool ok = tc::mbar_wait(q_full, 0, p.err, ERR_A_MMA, abort);
@@ -761,6 +771,8 @@ __global__ void __launch_bounds__(576, 1)
     int xph = 0;  // completed phases of this pair's exchange barrier
     long long my_lo, my_hi;
     tile2_range(p, r0, t, &my_lo, &my_hi);
+    my_lo = max(my_lo, kb_lo);
+    my_hi = min(my_hi, kb_lo + nbl - 1);
     for (long long j = my_lo; j <= my_hi; ++j, ++cnt) {
       if (!warp_wait(s_full + 8 * t, cnt & 1, p.err, ERR_A_SOFT, abort)) {
         ok = false;
@@ -841,7 +853,35 @@ __global__ void __launch_bounds__(576, 1)
       ok = warp_wait(xb, xph & 1, p.err, ERR_A_SOFT, abort);
       l_tot = xl[row] + xl[128 + row];
     }
-    if (ok && cnt > 0 && warp_wait(o_done + 8 * t, (cnt - 1) & 1, p.err, ERR_A_SOFT, abort)) {
+    if (ok && p.parts > 1) {
+      // this part's share: the unnormalised output (zero if the tile saw no
+      // key block here) and (max, sum) of the row, merged by the combine
+      // kernel
+      const bool have = cnt > 0 && warp_wait(o_done + 8 * t, (cnt - 1) & 1, p.err, ERR_A_SOFT, abort);
+      if (cnt > 0 && !have) ok = false;
+      if (ok) {
+        tc::tc_fence_after();
+        const int64_t ldw = (int64_t)p.H * p.hd;
+        for (int c0 = 64 * hf; c0 < nO && c0 < 64 * hf + 64; c0 += 32) {
+          float v[32];
+          if (have) {
+            tc::tmem_ld32(tO + c0, v);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = 0.f;
+          }
+          if (grow_ < p.n) {
+            float* dst = p.ws + ((int64_t)zpart * p.n + grow_) * ldw + (int64_t)h * p.hd + c0;
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+              if (c0 + k < p.hd) *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+          }
+        }
+        if (hf == 0 && grow_ < p.n)
+          *reinterpret_cast<float2*>(p.ws_ml + (((int64_t)zpart * p.H + h) * p.n + grow_) * 2) =
+              make_float2(have ? m_run : NEG_INF, have ? l_tot : 0.f);
+      }
+    } else if (ok && cnt > 0 && warp_wait(o_done + 8 * t, (cnt - 1) & 1, p.err, ERR_A_SOFT, abort)) {
       tc::tc_fence_after();
       const float il = 1.0f / l_tot;
       for (int c0 = 64 * hf; c0 < nO && c0 < 64 * hf + 64; c0 += 32) {
@@ -1790,6 +1830,48 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
+// Merge the key-range parts of the split forward, in part order: with
+// M = max_z m_z and L = sum_z 2^(m_z - M) l_z,
+//   o = sum_z 2^(m_z - M) O_z / L,   lse = (M + log2 L) ln 2.
+// One warp per (row, head); each lane takes hd / 32 columns.
+__global__ void attn_fwd_combine_kernel(const float* __restrict__ ws, const float* __restrict__ ws_ml, int parts,
+                                        int n, int H, int hd, bf16* __restrict__ o, int64_t ldo,
+                                        float* __restrict__ lse, int ld_lse) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (w >= n * H) return;
+  const int r = w / H, h = w % H;
+  auto ml_of = [&](int z) {
+    return *reinterpret_cast<const float2*>(ws_ml + (((int64_t)z * H + h) * n + r) * 2);
+  };
+  float M = -INFINITY;
+  for (int z = 0; z < parts; ++z) M = fmaxf(M, ml_of(z).x);
+  const float Mu = M == -INFINITY ? 0.f : M;
+  float L = 0.f;
+  for (int z = 0; z < parts; ++z) {
+    const float2 ml = ml_of(z);
+    L += (ml.x == -INFINITY ? 0.f : exp2f(ml.x - Mu)) * ml.y;
+  }
+  const float il = L > 0.f ? 1.0f / L : 0.f;
+  const int64_t ldw = (int64_t)H * hd;
+  for (int c = 4 * lane; c < hd; c += 128) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (int z = 0; z < parts; ++z) {
+      const float mz = ml_of(z).x;
+      const float sc = mz == -INFINITY ? 0.f : exp2f(mz - Mu);
+      const float4 v = *reinterpret_cast<const float4*>(ws + ((int64_t)z * n + r) * ldw + (int64_t)h * hd + c);
+      a0 = fmaf(sc, v.x, a0);
+      a1 = fmaf(sc, v.y, a1);
+      a2 = fmaf(sc, v.z, a2);
+      a3 = fmaf(sc, v.w, a3);
+    }
+    uint2 u;
+    u.x = pack_bf16(a0 * il, a1 * il);
+    u.y = pack_bf16(a2 * il, a3 * il);
+    *reinterpret_cast<uint2*>(o + (int64_t)r * ldo + (int64_t)h * hd + c) = u;
+  }
+  if (lane == 0) lse[(int64_t)h * ld_lse + r] = (M + log2f(L)) * 0.69314718055994531f;
+}
+
 // D[h][r] = sum_d dO[r, h*hd + d] * O[r, h*hd + d]; one warp per (r, h)
 __global__ void attn_bwd_prep_tc_kernel(const bf16* __restrict__ dO, const bf16* __restrict__ O, int n, int H,
                                         int hd, float* __restrict__ dsum, int ld) {
@@ -1885,6 +1967,33 @@ int map2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint6
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
+// Key-range parts of a kernel whose CTA takes rows_per_cta query rows of a
+// head over blocks of bn keys: enough CTAs to fill the SMs in whole waves,
+// never more parts than the smallest tile has key blocks, at most max_parts.
+static int split_parts(const AttnArgs& a, int num_sms, int rows_per_cta, int bn, int max_parts) {
+  const int ntiles = (a.n + rows_per_cta - 1) / rows_per_cta;
+  int nb_min = INT32_MAX;
+  for (int t = 0; t < ntiles; ++t) {
+    const long long t_lo = a.pos0 + (long long)t * rows_per_cta;
+    const long long t_hi = a.pos0 + std::min(t * rows_per_cta + rows_per_cta, a.n) - 1;
+    long long k_lo = t_lo - a.W + 1;
+    if (k_lo < 0) k_lo = 0;
+    nb_min = std::min<int>(nb_min, (int)(t_hi / bn - k_lo / bn + 1));
+  }
+  const int units = ntiles * a.H;
+  int best = 1;
+  double best_cost = 1e30;
+  for (int P = 1; P <= max_parts && P <= nb_min; ++P) {
+    const double waves = std::ceil((double)units * P / num_sms);
+    const double cost = waves / P * (1.0 + 0.02 * (P - 1));
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = P;
+    }
+  }
+  return best;
+}
+
 template <int NA>
 int launch_fwd(const AttnArgs& a, int* err, cudaStream_t st) {
   using SM = FwdSmem<NA>;
@@ -1913,13 +2022,15 @@ int launch_fwd(const AttnArgs& a, int* err, cudaStream_t st) {
   p.lse = a.lse;
   p.ld_lse = a.ld_lse;
   p.err = err;
+  p.parts = 1;
+  p.ws = p.ws_ml = nullptr;
   dim3 grid((a.n + BM - 1) / BM, a.H);
   attn_fwd_tc_kernel<NA><<<grid, 192, SM::SMEM, st>>>(mq, mk, mv, p);
   return (int)cudaPeekAtLastError();
 }
 
 template <int NA>
-int launch_fwd2(const AttnArgs& a, int* err, cudaStream_t st) {
+int launch_fwd2(const AttnArgs& a, int* err, cudaStream_t st, int* kernels) {
   using SM = Fwd2Smem<NA>;
   CUtensorMap mq, mk, mv;
   const uint64_t ldq = (uint64_t)a.H * a.hd;
@@ -1946,8 +2057,31 @@ int launch_fwd2(const AttnArgs& a, int* err, cudaStream_t st) {
   p.lse = a.lse;
   p.ld_lse = a.ld_lse;
   p.err = err;
-  dim3 grid((a.n + 2 * BM - 1) / (2 * BM), a.H);
+  // with scratch, split the key range when the tile pairs alone leave SMs
+  // idle (a chunk of 1024 rows has 4 pairs per head)
+  p.parts = 1;
+  p.ws = p.ws_ml = nullptr;
+  if (a.ws) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t plane = (int64_t)a.n * a.H * a.hd, ml = (int64_t)2 * a.n * a.H;
+    int parts = split_parts(a, sms, 2 * BM, BN2, 3);
+    while (parts > 1 && (int64_t)parts * (plane + ml) > a.ws_elems) --parts;
+    if (parts > 1) {
+      p.parts = parts;
+      p.ws = a.ws;
+      p.ws_ml = a.ws + (int64_t)parts * plane;
+    }
+  }
+  dim3 grid((a.n + 2 * BM - 1) / (2 * BM), a.H, p.parts);
   attn_fwd2_tc_kernel<NA><<<grid, 576, SM::SMEM, st>>>(mq, mk, mv, p);
+  if (kernels) *kernels = p.parts > 1 ? 2 : 1;
+  if (p.parts > 1) {
+    const int64_t warps = (int64_t)a.n * a.H;
+    attn_fwd_combine_kernel<<<(int)((warps + 7) / 8), 256, 0, st>>>(p.ws, p.ws_ml, p.parts, a.n, a.H, a.hd, p.o,
+                                                                      p.ldo, a.lse, a.ld_lse);
+  }
   return (int)cudaPeekAtLastError();
 }
 
@@ -1959,43 +2093,15 @@ bool attn_tc_supported(const AttnArgs& a) {
          ((uintptr_t)a.o & 15) == 0;
 }
 
-int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st, int variant) {
+int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st, int variant, int* kernels) {
+  if (kernels) *kernels = 1;
   if (a.n <= 0) return 0;
   if (!encoder() || !attn_tc_supported(a)) return (int)cudaErrorNotSupported;
   // the two-tile kernel measured faster at every size tried (1K and 16K
   // rows, head dims 64 and 128)
   if (variant == 0) variant = 2;
-  if (variant == 2) return a.hd <= 64 ? launch_fwd2<1>(a, err, st) : launch_fwd2<2>(a, err, st);
+  if (variant == 2) return a.hd <= 64 ? launch_fwd2<1>(a, err, st, kernels) : launch_fwd2<2>(a, err, st, kernels);
   return a.hd <= 64 ? launch_fwd<1>(a, err, st) : launch_fwd<2>(a, err, st);
-}
-
-// key-range parts of the dq kernel: enough CTAs to fill the SMs in whole
-// waves, never more parts than the smallest tile has key blocks
-// rows per dq CTA: 2 * BM (two-tile kernel) or BM
-static int dq_parts(const AttnArgs& a, int num_sms, int rows_per_cta = BM) {
-  const int ntiles = (a.n + rows_per_cta - 1) / rows_per_cta;
-  long long kb0 = (a.pos0 - a.W + 1 > 0 ? a.pos0 - a.W + 1 : 0) / BN;
-  int nb_min = INT32_MAX;
-  for (int t = 0; t < ntiles; ++t) {
-    const long long t_lo = a.pos0 + (long long)t * rows_per_cta;
-    const long long t_hi = a.pos0 + std::min(t * rows_per_cta + rows_per_cta, a.n) - 1;
-    long long k_lo = t_lo - a.W + 1;
-    if (k_lo < 0) k_lo = 0;
-    kb0 = k_lo / BN;
-    nb_min = std::min<int>(nb_min, (int)(t_hi / BN - kb0 + 1));
-  }
-  const int units = ntiles * a.H;
-  int best = 1;
-  double best_cost = 1e30;
-  for (int P = 1; P <= 4 && P <= nb_min; ++P) {
-    const double waves = std::ceil((double)units * P / num_sms);
-    const double cost = waves / P * (1.0 + 0.02 * (P - 1));
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = P;
-    }
-  }
-  return best;
 }
 
 int64_t attn_bwd_tc_ws_elems(int n, int H, int hd, int num_sms) {
@@ -2045,7 +2151,7 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
     attn_bwd_prep_tc_kernel<<<(warps + 7) / 8, 256, 0, st>>>((const bf16*)a.dout, (const bf16*)a.out, a.n, a.H,
                                                              a.hd, a.Dsum, a.ld_lse);
   }
-  p.parts = dq_parts(a, num_sms, 2 * BM);
+  p.parts = split_parts(a, num_sms, 2 * BM, BN, 4);
   const int64_t plane = (int64_t)a.n * a.H * a.hd;
   if (p.parts > 1 && (int64_t)p.parts * plane > a.ws_elems) p.parts = 1;
   attn_dq2_tc_kernel<NA><<<dim3((a.n + 2 * BM - 1) / (2 * BM), a.H, p.parts), 576, DQ::SMEM, st>>>(mq, mdo, mk, mv,

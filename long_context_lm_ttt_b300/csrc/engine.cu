@@ -589,6 +589,7 @@ struct Engine : EngineBase {
     const double hdH = (double)a.H * a.hd;
     const double kv = (double)std::min<int64_t>(a.pos0 + a.n, (int64_t)a.W + a.n - 1) * a.Hkv * a.hd;
     const double bytes = sizeof(T) * (2.0 * a.n * hdH + 2.0 * kv) + 4.0 * a.n * a.H;
+    int nk = 1;
     prof(a.n > cfg.chunk ? P_ATTN_FWD_BULK : P_ATTN_FWD, 4.0 * hdH * P, bytes, st, [&] {
       // a decode step: one query, the window split over the whole GPU
       if (dec_part && a.n == 1 && attn_decode_supported(a)) {
@@ -597,7 +598,15 @@ struct Engine : EngineBase {
       }
       if constexpr (kBF16) {
         if (use_tc_attn && attn_tc_supported(a)) {
-          int r = attn_fwd_tc(a, dev_err + 2, st);
+          // the chunk loop's forward may split key ranges through the
+          // attention scratch; the bulk pass (grid_cap set, other stream)
+          // never touches it
+          AttnArgs as = a;
+          if (!grid_cap && attn_ws) {
+            as.ws = attn_ws;
+            as.ws_elems = attn_ws_elems;
+          }
+          int r = attn_fwd_tc(as, dev_err + 2, st, 0, &nk);
           if (r != 0 && *rc == TTT_OK) {
             *rc = TTT_ERR_SHAPE;
             err = "tensor-core attention forward rejected the shape";
@@ -606,7 +615,7 @@ struct Engine : EngineBase {
         }
       }
       attn_fwd_simt<T>(a, st);
-    });
+    }, [&] { return nk; });
   }
   void attn_bwd(const AttnArgs& a, cudaStream_t st, int* rc) {
     double P, Pl;

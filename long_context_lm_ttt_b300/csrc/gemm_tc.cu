@@ -40,9 +40,10 @@ constexpr int A_BYTES = BM * BK * 2;
 // SRC = 1 (the SGD epilogue): the tile's fp32 master weights are brought
 // into shared memory by TMA at the start of each tile, so the load overlaps
 // the tile's main loop.  The epilogue updates them in place and writes the
-// bf16 pair (hi, lo) into a staging tile; each epilogue warp then sends its
-// 32 rows of all three back with TMA stores, so every global write is a
-// whole 128-byte line.
+// bf16 copy hi = rn(w) (and, when a low half is wanted, lo = rn(w - hi))
+// into a staging tile; each epilogue warp then sends its 32 rows of the
+// outputs back with TMA stores, so every global write is a whole 128-byte
+// line.
 //
 // PAIR = 1: a cluster of two CTAs (on the two SMs of a TPC) computes a
 // 256 x BN tile with tcgen05 MMAs of M = 256 (cta_group::2).  CTA r of the
@@ -66,13 +67,19 @@ struct Cfg {
   static constexpr int SRC_BYTES = SRC ? 2 * SLOT_BYTES : 0;
   static constexpr int HL_BYTES = SRC ? 2 * BM * 128 : 0;
   static constexpr int FIT_STAGES = (kSmemMax - 2048 - SRC_BYTES - HL_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = (PAIR || SRC) ? (FIT_STAGES > 8 ? 8 : FIT_STAGES) : (BN == 256 ? 4 : 6);
+  static constexpr int STAGES =
+      (PAIR || SRC) ? (FIT_STAGES > 8 ? 8 : FIT_STAGES) : (BN == 256 ? 4 : (BN == 192 ? 5 : 6));
   static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+  // columns allocated: a power of two, at least 32
+  static constexpr int TMEM_ALLOC = TMEM_COLS <= 32 ? 32 : TMEM_COLS <= 64 ? 64 : TMEM_COLS <= 128 ? 128
+                                    : TMEM_COLS <= 256 ? 256 : 512;
   static constexpr int SRC_OFF = STAGES * STAGE_BYTES;
   static constexpr int HL_OFF = SRC_OFF + SRC_BYTES;
   static constexpr int BAR_OFF = HL_OFF + HL_BYTES;
   static constexpr int SMEM = 1024 /*align slack*/ + BAR_OFF + 256;
   static_assert(SMEM <= kSmemMax, "shared memory");
+  static_assert(TMEM_COLS <= 512, "tensor memory");
+  static_assert(BN % 32 == 0 && BNL % 8 == 0, "tile width");
   static_assert(8 * (2 * STAGES + 9) + 8 <= 256, "barrier area");
 };
 
@@ -101,6 +108,8 @@ __global__ void __launch_bounds__(192, 1)
                    const __grid_constant__ CUtensorMap mapL, int dual, int M, int N, int K, Epi e, int* err,
                    int splits, float* ws) {
   using C = Cfg<BN, SRC, PAIR>;
+  // an MN-major B tile arrives in 64-column boxes
+  static_assert(!B_MN || C::BNL % 64 == 0, "MN-major B needs whole 64-column boxes");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = tc::smem_u32(smem);
@@ -160,10 +169,10 @@ __global__ void __launch_bounds__(192, 1)
   }
   if (warp == 1) {
     if (PAIR) {
-      tc::tmem_alloc_pair(tc::smem_u32(tmem_slot), C::TMEM_COLS);
+      tc::tmem_alloc_pair(tc::smem_u32(tmem_slot), C::TMEM_ALLOC);
       tc::tmem_relinquish_pair();
     } else {
-      tc::tmem_alloc(tc::smem_u32(tmem_slot), C::TMEM_COLS);
+      tc::tmem_alloc(tc::smem_u32(tmem_slot), C::TMEM_ALLOC);
       tc::tmem_relinquish();
     }
   }
@@ -496,7 +505,7 @@ __global__ void __launch_bounds__(192, 1)
                 if (c0 + 32 * j < N) tc::tma_store_2d(&mapW, c0 + 32 * j, r, slot + j * BM * 128 + quarter * 4096);
               const uint32_t hb = sbase + C::HL_OFF + quarter * 4096;
               tc::tma_store_2d(&mapH, c0, r, hb);
-              tc::tma_store_2d(&mapL, c0, r, hb + BM * 128);
+              if (e.w16lo) tc::tma_store_2d(&mapL, c0, r, hb + BM * 128);
             }
             tc::bulk_commit();
             tc::bulk_wait_read();
@@ -556,9 +565,9 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) {
     tc::tc_fence_after();
     if (PAIR)
-      tc::tmem_dealloc_pair(tmem, C::TMEM_COLS);
+      tc::tmem_dealloc_pair(tmem, C::TMEM_ALLOC);
     else
-      tc::tmem_dealloc(tmem, C::TMEM_COLS);
+      tc::tmem_dealloc(tmem, C::TMEM_ALLOC);
   }
 }
 
@@ -742,17 +751,20 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
     rc = make_map_f32(&ms, g.e.w32, g.N, g.M, g.e.ldo, BM);
     if (!rc) rc = make_map_f32(&mw, g.e.w32, g.N, g.M, g.e.ldo, 32);
     if (!rc) rc = make_map(&mh, g.e.w16, g.N, g.M, g.e.ldo, 64, 32);
-    if (!rc) rc = make_map(&ml, g.e.w16lo, g.N, g.M, g.e.ldo, 64, 32);
+    // no low half: the epilogue stores only w32 and w16
+    if (!rc) {
+      if (g.e.w16lo) rc = make_map(&ml, g.e.w16lo, g.N, g.M, g.e.ldo, 64, 32);
+      else ml = mh;
+    }
     if (rc) return rc;
   } else {
     ms = mw = mh = ml = mb;
   }
   auto kern = gemm_tc_kernel<BN, A_MN, B_MN, SRC, PAIR>;
-  static std::atomic<bool> attr_set{false};  // per instantiation
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static std::atomic<uint64_t> attr_set{0};  // per instantiation, per device
+  {
+    cudaError_t e = raise_smem_limit(attr_set, kern, C::SMEM);
     if (e != cudaSuccess) return (int)e;
-    attr_set = true;
   }
   const int ntiles = ((g.M + C::TM - 1) / C::TM) * ((g.N + BN - 1) / BN);
   const int nunits = ntiles * splits;
@@ -807,13 +819,24 @@ int dispatch_major(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t 
   return g.b_mn ? launch<BN, 0, 1, 0, PAIR>(g, num_sms, err, st, splits)
                 : launch<BN, 0, 0, 0, PAIR>(g, num_sms, err, st, splits);
 }
+// 192-column tiles on CTA pairs: each CTA loads 96 rows of B, which only a
+// K-major B provides in one box (the planner never picks it otherwise)
+int dispatch_192_pair(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int splits) {
+  if (g.b_mn) return (int)cudaErrorNotSupported;
+  return g.a_mn ? launch<192, 1, 0, 0, 1>(g, num_sms, err, st, splits)
+                : launch<192, 0, 0, 0, 1>(g, num_sms, err, st, splits);
+}
 
 // Tile shape and K split by a simple time model: a k-block of a 128 x BN
-// tile costs BN units (BN = 128 tiles a little more per column: they are
+// tile costs BN units (narrower tiles a little more per column: they are
 // closer to the shared-memory bandwidth limit), tiles run in waves of
 // num_sms, and a split adds a reduction pass over splits x M x N fp32.  A
 // CTA pair runs a 256 x BN tile in the time a single CTA runs 128 x BN, in
 // waves of num_sms / 2, and loads half as much B per SM (kPairGain).
+// BN = 192 exists for outputs 3072 wide at M = 1024 (the chunk's o-proj,
+// down-proj and most input-gradient products): 16 column tiles make 64 pair
+// tiles (or 128 single ones), 86% of one wave, where 256-wide tiles leave
+// 35% of the SMs idle.
 struct Plan {
   int bn, splits, pair;
 };
@@ -829,10 +852,14 @@ static Plan plan_gemm(const GemmArgs<bf16>& g, int num_sms) {
     if (g.pair >= 0 ? pair != g.pair : (pair && g.M <= BM)) continue;
     const int slots = pair ? num_sms / 2 : num_sms;
     const int num_m = (g.M + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
-    for (int bn : {128, 256}) {
-      if (bn == 256 && g.N <= 128) continue;
+    // on near-ties (3%) the earlier candidate stays: 192-wide tiles cost a
+    // little more per column, so they come last and win only where they
+    // fill a wave clearly better
+    for (int bn : {128, 256, 192}) {
+      if (bn > 128 && g.N <= 128) continue;
+      if (bn == 192 && pair && g.b_mn) continue;  // see dispatch_192_pair
       const int tiles = num_m * ((g.N + bn - 1) / bn);
-      const double kb_cost = (bn == 256 ? 1.0 : 0.58) * (pair ? kPairGain : 1.0) * kb_us;
+      const double kb_cost = (bn == 256 ? 1.0 : (bn == 192 ? 0.79 : 0.58)) * (pair ? kPairGain : 1.0) * kb_us;
       for (int sp = 1; sp <= 4; ++sp) {
         if (sp > 1 && (!g.ws || nkt / sp < 8 || (int64_t)sp * g.M * g.N > g.ws_elems)) break;
         const double waves = std::ceil((double)tiles * sp / slots);
@@ -904,11 +931,11 @@ int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st, 
   if (((uintptr_t)g.A & 15) || ((uintptr_t)g.B & 15) || ((uintptr_t)g.B2 & 15) || (g.lda & 7) ||
       (g.ldb & 7) || g.K <= 0)
     return (int)cudaErrorNotSupported;
-  // the SGD epilogue (weight-gradient GEMM, both operands MN-major, the
-  // bf16 pair wanted) updates the fp32 masters in a TMA-fed shared-memory
-  // tile and stores all three outputs by TMA
-  if (g.e.kind == EPI_SGD && g.e.vec && g.a_mn && g.b_mn && !g.B2 && (g.N % 32) == 0 && g.e.w16 && g.e.w16lo &&
-      (g.e.ldo % 8) == 0 && a16(g.e.w16) && a16(g.e.w16lo)) {
+  // the SGD epilogue (weight-gradient GEMM, both operands MN-major, a bf16
+  // copy wanted, with or without its low half) updates the fp32 masters in
+  // a TMA-fed shared-memory tile and stores the outputs by TMA
+  if (g.e.kind == EPI_SGD && g.e.vec && g.a_mn && g.b_mn && !g.B2 && (g.N % 32) == 0 && g.e.w16 &&
+      (g.e.ldo % 8) == 0 && a16(g.e.w16) && (!g.e.w16lo || a16(g.e.w16lo))) {
     if (kernels) *kernels = 1;
     const bool pair = g.pair >= 0 ? g.pair == 1 : g.M > BM;
     return pair ? launch<256, 1, 1, 1, 1>(g, num_sms, err, st, 1) : launch<128, 1, 1, 1, 0>(g, num_sms, err, st, 1);
@@ -916,9 +943,12 @@ int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st, 
   const Plan pl = plan_gemm(g, num_sms);
   if (pl.splits > 1 && (((uintptr_t)g.ws & 15) != 0)) return (int)cudaErrorNotSupported;
   if (kernels) *kernels = pl.splits > 1 ? 2 : 1;
-  if (pl.pair)
+  if (pl.pair) {
+    if (pl.bn == 192) return dispatch_192_pair(g, num_sms, err, st, pl.splits);
     return pl.bn == 256 ? dispatch_major<256, 1>(g, num_sms, err, st, pl.splits)
                         : dispatch_major<128, 1>(g, num_sms, err, st, pl.splits);
+  }
+  if (pl.bn == 192) return dispatch_major<192, 0>(g, num_sms, err, st, pl.splits);
   return pl.bn == 256 ? dispatch_major<256, 0>(g, num_sms, err, st, pl.splits)
                       : dispatch_major<128, 0>(g, num_sms, err, st, pl.splits);
 }

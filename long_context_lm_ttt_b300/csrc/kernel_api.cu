@@ -160,6 +160,24 @@ extern "C" int ttt_kernel_attn_fwd(int32_t impl, int32_t n, int32_t H, int32_t H
   }
   if (impl == 0 || impl == 2 || impl == 3) {
     if (!ttt::attn_tc_supported(a)) return TTT_ERR_SHAPE;
+    if (impl == 0) {
+      // scratch that lets the kernel split key ranges, per device: grown on
+      // demand, kept for later calls (calls on one device must not overlap)
+      static float* ws_of[kDevs] = {};
+      static int64_t elems_of[kDevs] = {};
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return TTT_ERR_CUDA;
+      const int64_t need = (int64_t)3 * ((int64_t)n * H * hd + (int64_t)2 * n * H);
+      if (need > elems_of[dev]) {
+        if (ws_of[dev]) cudaFree(ws_of[dev]);
+        ws_of[dev] = nullptr;
+        elems_of[dev] = 0;
+        if (cudaMalloc(&ws_of[dev], need * sizeof(float)) != cudaSuccess) return TTT_ERR_OOM;
+        elems_of[dev] = need;
+      }
+      a.ws = ws_of[dev];
+      a.ws_elems = elems_of[dev];
+    }
     rc = ttt::attn_fwd_tc(a, g_err, st, impl == 0 ? 0 : (impl == 2 ? 1 : 2));
     return rc ? TTT_ERR_CUDA : 0;
   }

@@ -134,8 +134,11 @@ template <typename T> void attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
 // into *err.
 bool attn_tc_supported(const AttnArgs& a);
 // variant 0: choose by size; 1: one 128-row tile per CTA (two CTAs per
-// SM); 2: two tiles per CTA with P kept in tensor memory
-int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st, int variant = 0);
+// SM); 2: two tiles per CTA with P kept in tensor memory.  With scratch
+// (a.ws, at least 3 x (n H hd + 2 n H) floats) variant 2 may split each
+// tile pair's key range into parts merged by a second kernel.  *kernels
+// (optional) receives the number of kernels launched.
+int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st, int variant = 0, int* kernels = nullptr);
 int attn_bwd_tc(const AttnArgs& a, int* err, cudaStream_t st);
 // the backward additionally needs chunk starts at multiples of 64 and scratch
 bool attn_bwd_tc_supported(const AttnArgs& a);

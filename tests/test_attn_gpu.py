@@ -124,10 +124,11 @@ def test_attn_fwd_one_query(case):
     assert err_l < 2e-3, err_l
 
 
-@pytest.mark.parametrize("impl", [2, 3])
+@pytest.mark.parametrize("impl", [0, 2, 3])
 def test_attn_fwd_3b_shape_sampled(impl):
     """3B head layout (24 q / 8 KV heads x 128) over a full 1024-row chunk
-    deep in the sequence (window 8192 of a 9216-slot ring); sampled rows."""
+    deep in the sequence (window 8192 of a 9216-slot ring); sampled rows.
+    impl 0 splits each tile pair's key range into parts there."""
     torch, T = _env()
     n, H, Hkv, hd, W, R = 1024, 24, 8, 128, 8192, 9216
     pos0 = 40 * 1024

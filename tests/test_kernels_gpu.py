@@ -28,7 +28,10 @@ def _operand(rng, rows, cols, mn, bf16=True):
 
 SHAPES = [(128, 128, 64), (256, 384, 192), (100, 200, 96), (32, 128, 32), (130, 258, 70),
           (1024, 3072, 1024), (512, 512, 4096), (520, 640, 200), (300, 136, 1000),
-          (1, 256, 200), (1, 3072, 3072)]
+          (1, 256, 200), (1, 3072, 3072),
+          # 192-wide tiles with ragged edges (planner: pairs for a K-major B,
+          # single CTAs otherwise)
+          (1000, 3000, 200)]
 
 # impl 0: tensor cores, planner's choice; 3: 128-row tiles on one CTA;
 # 4: 256-row tiles on a CTA pair (also for M < 256: the second CTA's rows
@@ -127,3 +130,28 @@ def test_gemm_sgd(M, N, K, impl):
     g32 = w32.cpu()
     assert torch.equal(hi.cpu(), g32.to(torch.bfloat16))
     assert torch.equal(lo.cpu(), (g32 - g32.to(torch.bfloat16).float()).to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("impl", [0, 2, 3])
+def test_gemm_sgd_without_low_half(impl):
+    """The SGD step with one bf16 copy (no low half), the forward read the
+    inner loop uses by default: w32 as above, w16 = rn(w32) exactly."""
+    torch, T = _env()
+    M, N, K = 3072, 8192, 1024
+    rng = np.random.default_rng(17 + impl)
+    a, a_st = _operand(rng, M, K, 1)
+    b, b_st = _operand(rng, N, K, 1)
+    w0 = (rng.standard_normal((M, N)) * 0.02).astype(np.float32)
+    lr = 1e-3
+    cu = lambda x: torch.from_numpy(x).to(torch.bfloat16).cuda()
+    w32 = torch.from_numpy(w0).cuda()
+    hi = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    T.ttt_kernel_gemm_sgd(M, N, K, cu(a_st), M, 1, cu(b_st), N, 1, w32, hi, None, N, lr, impl)
+    torch.cuda.synchronize()
+    assert T.ttt_kernel_error() == 0
+    ref = w0.astype(np.float64) - lr * (a @ b.T)
+    got = w32.cpu().numpy().astype(np.float64)
+    upd = np.abs(lr * (a @ b.T)).max()
+    assert np.abs(got - ref).max() <= 1e-5 * upd + 2e-9, np.abs(got - ref).max()
+    assert torch.equal(hi.cpu(), w32.cpu().to(torch.bfloat16))
+
