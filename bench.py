@@ -49,6 +49,38 @@ METRIC = "TTT-E2E prefill tokens/s at 3B, 128K ctx on 1 B300; % of dense BF16 pe
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
+# kernel class, from one ncu capture of that class at the bench's shapes.  It
+# is reported only while the sources the kernels are built from still hash to
+# the value recorded with the capture; after any change it reads null until
+# the capture is taken again.
+TRAFFIC = {
+    "gemm_fwd_bulk": {"bytes_per_launch": 643.9e6 + 186.1e6, "sha16": "f45d99e0799ca6c7",
+                      "sources": ("gemm_tc.cu", "common.cuh", "tc_common.cuh"),
+                      "capture": "profiles/gemm_bulk_traffic_3b_T16384.md"},
+}
+
+
+def _sources_sha16(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "long_context_lm_ttt_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(kernel: str):
+    t = TRAFFIC.get(kernel)
+    if t is None:
+        return None, None
+    try:
+        if _sources_sha16(t["sources"]) != t["sha16"]:
+            return None, f"{t['capture']} (stale: the kernel sources changed since the capture)"
+    except OSError:
+        return None, None
+    return t["bytes_per_launch"], t["capture"]
+
 
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -293,9 +325,13 @@ def roofline(prof, peaks, peak_src):
         ach = st["bytes"] / sec / 1e9
         pk = peaks["hbm_gbs"]
         r = {"bound": "hbm", "achieved": ach, "peak": pk, "unit": "GB/s", "frac": ach / pk}
-    r.update({"traffic": None, "kernel": name, "launches": st["launches"],
+    traffic, src = traffic_of(name)
+    r.update({"traffic": traffic, "kernel": name, "launches": st["launches"],
               "avg_launch_ms": st["ms"] / st["launches"],
+              "algorithmic_bytes_per_launch": st["bytes"] / st["launches"],
               "peak_source": f"{peak_src} ({'sustained bf16' if r['bound'] == 'tensor' else 'copy'})"})
+    if src:
+        r["traffic_source"] = src
     return r, dom
 
 

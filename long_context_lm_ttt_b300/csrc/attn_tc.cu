@@ -97,6 +97,14 @@ __device__ __forceinline__ void tile_blocks(const FwdParams& p, int r0, long lon
   *nb = (int)(t_hi / BN - *kb0 + 1);
 }
 
+// One arrival per warp on a hand-off barrier: every lane has finished (and
+// fenced) its own shared/tensor-memory writes; the warp synchronises and
+// lane 0 arrives, so the barrier counts warps rather than threads.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) tc::mbar_arrive(bar);
+}
+
 // every lane waits on the barrier; the warp agrees on the outcome so that
 // warp-collective tcgen05 instructions are reached by all lanes or none
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err, int code,
@@ -507,16 +515,6 @@ __device__ __forceinline__ void mul2(float a0, float a1, float b0, float b1, flo
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
-// (a0, a1) + (b0, b1)
-__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
-  asm("{\n.reg .b64 ra, rb, rd;\n"
-      "mov.b64 ra, {%0, %1};\n"
-      "mov.b64 rb, {%2, %3};\n"
-      "add.rn.f32x2 rd, ra, rb;\n"
-      "mov.b64 {%0, %1}, rd;\n}"
-      : "+f"(a0), "+f"(a1)
-      : "f"(b0), "f"(b1));
-}
 // 32 lanes x 16 columns store (no wait)
 __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
@@ -535,18 +533,6 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "setp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
 
@@ -612,11 +598,11 @@ __global__ void __launch_bounds__(576, 1)
       tc::mbar_init(k_empty + 8 * s, 1);
       tc::mbar_init(v_empty + 8 * s, 1);
       tc::mbar_init(s_full + 8 * s, 1);
-      tc::mbar_init(p_full + 8 * s, 256);
+      tc::mbar_init(p_full + 8 * s, 8);  // one arrival per softmax warp of the tile
       tc::mbar_init(o_done + 8 * s, 1);
     }
     tc::mbar_init(drain, 1);
-    for (int x = 0; x < 8; ++x) tc::mbar_init(xbar + 8 * x, 64);
+    for (int x = 0; x < 8; ++x) tc::mbar_init(xbar + 8 * x, 2);  // the two warps of a lane quarter
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -798,7 +784,7 @@ __global__ void __launch_bounds__(576, 1)
       mb *= p.scale_log2;
       float* xm = xmax + (cnt & 1) * (2 * 128);
       xm[hf * 128 + row] = mb;
-      tc::mbar_arrive(xb);
+      warp_arrive(xb);
       if (!warp_wait(xb, xph & 1, p.err, ERR_A_SOFT, abort)) {
         ok = false;
         break;
@@ -843,13 +829,13 @@ __global__ void __launch_bounds__(576, 1)
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc::tc_fence_before();
-      tc::mbar_arrive(p_full + 8 * t);
+      warp_arrive(p_full + 8 * t);
     }
     // row sum = both halves' partial sums
     float l_tot = 0.f;
     if (ok) {
       xl[hf * 128 + row] = l_run;
-      tc::mbar_arrive(xb);
+      warp_arrive(xb);
       ok = warp_wait(xb, xph & 1, p.err, ERR_A_SOFT, abort);
       l_tot = xl[row] + xl[128 + row];
     }
@@ -943,296 +929,10 @@ struct BwdParams {
   int* err;
 };
 
-__device__ __forceinline__ void store_row_sw128_pk(uint32_t tile, int row, const uint32_t (&pk)[32]) {
-  const uint32_t base = tile + row * 128;
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    st_shared_v4(base + ((c ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-}
-
-template <int NA>
-struct DqSmem {
-  static constexpr int Q_BYTES = NA * BM * 128;
-  static constexpr int KV_BYTES = NA * BN * 128;
-  static constexpr int DS_BYTES = BM * BN * 2;
-  static constexpr int Q_OFF = 0;
-  static constexpr int DO_OFF = Q_OFF + Q_BYTES;
-  static constexpr int K_OFF = DO_OFF + Q_BYTES;
-  static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
-  static constexpr int DS_OFF = V_OFF + STAGES * KV_BYTES;
-  static constexpr int BAR_OFF = DS_OFF + 2 * DS_BYTES;
-  // at least 120 KB: one CTA (512 TMEM columns) per SM
-  static constexpr int SMEM = BAR_OFF + 256 > 120 * 1024 ? BAR_OFF + 256 : 120 * 1024;
-};
-
-__device__ __forceinline__ void bwd_tile_blocks(const BwdParams& p, int r0, long long* kb0, int* nb) {
-  const long long t_lo = p.pos0 + r0;
-  const long long t_hi = p.pos0 + min(r0 + BM, p.n) - 1;
-  long long k_lo = t_lo - p.W + 1;
-  if (k_lo < 0) k_lo = 0;
-  *kb0 = k_lo / BN;
-  *nb = (int)(t_hi / BN - *kb0 + 1);
-}
-
-template <int NA>
-__global__ void __launch_bounds__(320, 1)
-    attn_dq_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
-                      const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-                      BwdParams p) {
-  using SM = DqSmem<NA>;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const uint32_t sbase = tc::smem_u32(smem);
-  const uint32_t bar0 = sbase + SM::BAR_OFF;
-  const uint32_t q_full = bar0;
-  const uint32_t k_full = bar0 + 8;      // [2]
-  const uint32_t v_full = bar0 + 24;     // [2]
-  const uint32_t kv_empty = bar0 + 40;   // [2]
-  const uint32_t s_full = bar0 + 56;     // [2]
-  const uint32_t s_empty = bar0 + 72;    // [2]
-  const uint32_t ds_full = bar0 + 88;    // [2]
-  const uint32_t ds_empty = bar0 + 104;  // [2]
-  const uint32_t dq_done = bar0 + 120;
-  const uint32_t drain = bar0 + 128;
-  uint32_t* tmem_slot = (uint32_t*)(smem + SM::BAR_OFF + 192);
-  volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 196);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y, part = blockIdx.z;
-  const int r0 = qt * BM;
-  const int kvh = h / (p.H / p.Hkv);
-  long long kb0;
-  int nb_all;
-  bwd_tile_blocks(p, r0, &kb0, &nb_all);
-  const int b_lo = (int)((long long)part * nb_all / p.parts);
-  const int b_hi = (int)((long long)(part + 1) * nb_all / p.parts);
-  const int nb = b_hi - b_lo;
-  kb0 += b_lo;
-  const int ksteps = p.hd / 16;
-  const int nO = (p.hd + 15) & ~15;
-
-  if (threadIdx.x == 0) {
-    tc::mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(k_full + 8 * s, 1);
-      tc::mbar_init(v_full + 8 * s, 1);
-      tc::mbar_init(kv_empty + 8 * s, 1);
-      tc::mbar_init(s_full + 8 * s, 1);
-      tc::mbar_init(s_empty + 8 * s, 256);
-      tc::mbar_init(ds_full + 8 * s, 256);
-      tc::mbar_init(ds_empty + 8 * s, 1);
-    }
-    tc::mbar_init(dq_done, 1);
-    tc::mbar_init(drain, 1);
-    *abort = 0;
-    tc::fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tc::prefetch_tmap(&mapQ);
-    tc::prefetch_tmap(&mapDO);
-    tc::prefetch_tmap(&mapK);
-    tc::prefetch_tmap(&mapV);
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
-    tc::tmem_relinquish();
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256;
-
-  if (warp == 0) {
-    if (lane == 0 && nb > 0) {
-      bool ok = true;
-      int issued = 0;
-      tc::mbar_arrive_expect_tx(q_full, 2 * SM::Q_BYTES);
-      for (int a = 0; a < NA; ++a) {
-        tc::tma_load_2d(sbase + SM::Q_OFF + a * BM * 128, &mapQ, h * p.hd + 64 * a, r0, q_full);
-        tc::tma_load_2d(sbase + SM::DO_OFF + a * BM * 128, &mapDO, h * p.hd + 64 * a, r0, q_full);
-      }
-      for (int i = 0; i < nb && ok; ++i) {
-        const int st = i & 1;
-        if (!tc::mbar_wait(kv_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
-          ok = false;
-          break;
-        }
-        const long long kpos = (kb0 + i) * BN;
-        const int row = kvh * p.R + (int)(kpos % p.R);
-        tc::mbar_arrive_expect_tx(k_full + 8 * st, SM::KV_BYTES);
-        for (int a = 0; a < NA; ++a)
-          tc::tma_load_2d(sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN * 128, &mapK, 64 * a, row,
-                          k_full + 8 * st);
-        tc::mbar_arrive_expect_tx(v_full + 8 * st, SM::KV_BYTES);
-        for (int a = 0; a < NA; ++a)
-          tc::tma_load_2d(sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN * 128, &mapV, 64 * a, row,
-                          v_full + 8 * st);
-        issued = i + 1;
-      }
-      const long long t0 = clock64();
-      while (!tc::mbar_try_wait(q_full, 0) && clock64() - t0 < tc::kWaitClocks) {
-      }
-      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
-        const int st = i & 1;
-        const uint32_t par = (i >> 1) & 1;
-        const long long t1 = clock64();
-        while (!(tc::mbar_try_wait(k_full + 8 * st, par) && tc::mbar_try_wait(v_full + 8 * st, par)) &&
-               clock64() - t1 < tc::kWaitClocks) {
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && nb > 0) {
-      const uint32_t idS = tc::idesc_bf16(BM, BN, 0, 0);
-      const uint32_t idQ = tc::idesc_bf16(BM, nO, 0, 1);
-      bool ok = tc::mbar_wait(q_full, 0, p.err, ERR_A_MMA, abort);
-      bool issued = false;
-      for (int i = 0; i <= nb && ok; ++i) {
-        if (i < nb) {
-          const int st = i & 1;
-          const uint32_t par = (i >> 1) & 1;
-          if (!tc::mbar_wait(k_full + 8 * st, par, p.err, ERR_A_MMA, abort) ||
-              !tc::mbar_wait(v_full + 8 * st, par, p.err, ERR_A_MMA, abort) ||
-              !tc::mbar_wait(s_empty + 8 * st, par ^ 1, p.err, ERR_A_MMA, abort)) {
-            ok = false;
-            break;
-          }
-          tc::tc_fence_after();
-          const uint32_t kb = sbase + SM::K_OFF + st * SM::KV_BYTES;
-          const uint32_t vb = sbase + SM::V_OFF + st * SM::KV_BYTES;
-          for (int j = 0; j < ksteps; ++j) {
-            const int a = j >> 2;
-            const uint32_t ao = a * BM * 128 + 32 * (j & 3);
-            const uint32_t bo = a * BN * 128 + 32 * (j & 3);
-            tc::mma_bf16(tS + st * BN, tc::smem_desc_sw128(sbase + SM::Q_OFF + ao, 16, 1024),
-                         tc::smem_desc_sw128(kb + bo, 16, 1024), idS, j > 0);
-            tc::mma_bf16(tP + st * BN, tc::smem_desc_sw128(sbase + SM::DO_OFF + ao, 16, 1024),
-                         tc::smem_desc_sw128(vb + bo, 16, 1024), idS, j > 0);
-          }
-          issued = true;
-          tc::mma_commit(s_full + 8 * st);
-        }
-        if (i >= 1) {
-          const int k = i - 1;
-          const int st = k & 1;
-          if (!tc::mbar_wait(ds_full + 8 * st, (k >> 1) & 1, p.err, ERR_A_MMA, abort)) {
-            ok = false;
-            break;
-          }
-          tc::tc_fence_after();
-          const uint32_t kb = sbase + SM::K_OFF + st * SM::KV_BYTES;
-#pragma unroll
-          for (int j = 0; j < BN / 16; ++j)
-            tc::mma_bf16(tQ, tc::smem_desc_sw128(sbase + SM::DS_OFF + st * SM::DS_BYTES + 32 * j, 16, 1024),
-                         tc::smem_desc_sw128(kb + 2048 * j, BN * 128, 1024), idQ, (k > 0 || j > 0) ? 1u : 0u);
-          tc::mma_commit(ds_empty + 8 * st);
-          tc::mma_commit(kv_empty + 8 * st);
-        }
-      }
-      if (ok) tc::mma_commit(dq_done);
-      if (!ok && issued) {
-        tc::mma_commit(drain);
-        const long long t0 = clock64();
-        while (!tc::mbar_try_wait(drain, 0) && clock64() - t0 < tc::kWaitClocks) {
-        }
-      }
-    }
-  } else {
-    // eight compute warps: two per TMEM lane quarter, each taking one half
-    // (32 columns) of the block's keys and of dq's head dimension
-    const int quarter = warp & 3;
-    const int hf = (warp - 2) >> 2;
-    const int row = quarter * 32 + lane;
-    const int grow_ = r0 + row;
-    const long long t = p.pos0 + grow_;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const bool rvalid = grow_ < p.n;
-    const float lse2 = rvalid ? p.lse[(int64_t)h * p.ld_lse + grow_] * 1.4426950408889634f : 0.f;
-    const float Dt = rvalid ? p.dsum[(int64_t)h * p.ld_lse + grow_] : 0.f;
-    bool ok = true;
-    for (int i = 0; i < nb; ++i) {
-      const int st = i & 1;
-      const uint32_t par = (i >> 1) & 1;
-      if (!warp_wait(s_full + 8 * st, par, p.err, ERR_A_SOFT, abort)) {
-        ok = false;
-        break;
-      }
-      tc::tc_fence_after();
-      const long long kpos = (kb0 + i) * BN;
-      const long long lo = t - p.W + 1 - kpos, hi = t - kpos;
-      uint32_t pk[16];
-      {
-        float sv[32], dp[32];
-        tc::tmem_ld32(tS + st * BN + 32 * hf + lane_off, sv);
-        tc::tmem_ld32(tP + st * BN + 32 * hf + lane_off, dp);
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int cc = 32 * hf + c;
-          const float p0 = (cc >= lo && cc <= hi) ? exp2f(sv[c] * p.scale_log2 - lse2) : 0.f;
-          const float p1 = (cc + 1 >= lo && cc + 1 <= hi) ? exp2f(sv[c + 1] * p.scale_log2 - lse2) : 0.f;
-          pk[c / 2] = pack_bf16(p0 * (dp[c] - Dt) * p.scale, p1 * (dp[c + 1] - Dt) * p.scale);
-        }
-      }
-      tc::tc_fence_before();
-      tc::mbar_arrive(s_empty + 8 * st);
-      if (!warp_wait(ds_empty + 8 * st, par ^ 1, p.err, ERR_A_SOFT, abort)) {
-        ok = false;
-        break;
-      }
-      {
-        const uint32_t base = sbase + SM::DS_OFF + st * SM::DS_BYTES + row * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          st_shared_v4(base + (((4 * hf + c) ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      }
-      fence_proxy_async_smem();
-      tc::tc_fence_before();
-      tc::mbar_arrive(ds_full + 8 * st);
-    }
-    if (ok && nb > 0 && !warp_wait(dq_done, 0, p.err, ERR_A_SOFT, abort)) ok = false;
-    if (ok) {
-      tc::tc_fence_after();
-      for (int c0 = 32 * hf; c0 < nO; c0 += 64) {
-        float v[32];
-        if (nb > 0) {
-          tc::tmem_ld32(tQ + c0 + lane_off, v);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = 0.f;
-        }
-        if (!rvalid) continue;
-        if (p.parts == 1) {
-          bf16* dst = p.dqkv + (int64_t)grow_ * p.ldg + (int64_t)h * p.hd + c0;
-#pragma unroll
-          for (int k = 0; k < 32; k += 8)
-            if (c0 + k < p.hd) {
-              uint4 u;
-              u.x = pack_bf16(v[k], v[k + 1]);
-              u.y = pack_bf16(v[k + 2], v[k + 3]);
-              u.z = pack_bf16(v[k + 4], v[k + 5]);
-              u.w = pack_bf16(v[k + 6], v[k + 7]);
-              *reinterpret_cast<uint4*>(dst + k) = u;
-            }
-        } else {
-          float* dst = p.ws + ((int64_t)part * p.n + grow_) * ((int64_t)p.H * p.hd) + (int64_t)h * p.hd + c0;
-#pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            if (c0 + k < p.hd) *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-        }
-      }
-    }
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 512);
-  }
-}
 
 // --- dq, two query tiles per CTA, dS kept in TMEM ---------------------------
-// As attn_dq_tc_kernel, but a CTA takes 256 query rows (two 128-row tiles)
-// of one head over 64-key blocks, and dS is written back into TMEM (two bf16
+// A CTA takes 256 query rows (two 128-row tiles) of one head over 64-key
+// blocks, and dS is written back into TMEM (two bf16
 // per 32-bit column) where the dQ product reads it as its A operand:
 //   TMEM per tile t: S [256t, +64) | dP [256t+64, +64) | dQ [256t+128, +128)
 // Each of the 16 compute warps (two per lane quarter and tile) handles 32
@@ -1325,7 +1025,7 @@ __global__ void __launch_bounds__(576, 1)
     }
     for (int t = 0; t < 2; ++t) {
       tc::mbar_init(s_full + 8 * t, 1);
-      tc::mbar_init(ds_full + 8 * t, 256);
+      tc::mbar_init(ds_full + 8 * t, 8);  // one arrival per compute warp of the tile
     }
     tc::mbar_init(dq_done, 1);
     tc::mbar_init(drain, 1);
@@ -1517,7 +1217,7 @@ __global__ void __launch_bounds__(576, 1)
       tmem_st16u(tT + 32 * hf, pk);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc::tc_fence_before();
-      tc::mbar_arrive(ds_full + 8 * t);
+      warp_arrive(ds_full + 8 * t);
     }
     const bool have = cnt > 0;
     if (ok && have && !warp_wait(dq_done, 0, p.err, ERR_A_SOFT, abort)) ok = false;
@@ -1615,8 +1315,8 @@ __global__ void __launch_bounds__(320, 1)
       tc::mbar_init(q_full + 8 * s, 1);
       tc::mbar_init(q_empty + 8 * s, 1);
       tc::mbar_init(s_full + 8 * s, 1);
-      tc::mbar_init(s_empty + 8 * s, 256);
-      tc::mbar_init(pd_full + 8 * s, 256);
+      tc::mbar_init(s_empty + 8 * s, 8);  // one arrival per compute warp
+      tc::mbar_init(pd_full + 8 * s, 8);
       tc::mbar_init(pd_empty + 8 * s, 1);
     }
     tc::mbar_init(acc_done, 1);
@@ -1782,7 +1482,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       tc::tc_fence_before();
-      tc::mbar_arrive(s_empty + 8 * st);
+      warp_arrive(s_empty + 8 * st);
       if (!warp_wait(pd_empty + 8 * st, par ^ 1, p.err, ERR_A_SOFT, abort)) {
         ok = false;
         break;
@@ -1799,7 +1499,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       fence_proxy_async_smem();
       tc::tc_fence_before();
-      tc::mbar_arrive(pd_full + 8 * st);
+      warp_arrive(pd_full + 8 * st);
     }
     if (ok && warp_wait(acc_done, 0, p.err, ERR_A_SOFT, abort)) {
       tc::tc_fence_after();
@@ -1970,7 +1670,10 @@ int map2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint6
 // Key-range parts of a kernel whose CTA takes rows_per_cta query rows of a
 // head over blocks of bn keys: enough CTAs to fill the SMs in whole waves,
 // never more parts than the smallest tile has key blocks, at most max_parts.
-static int split_parts(const AttnArgs& a, int num_sms, int rows_per_cta, int bn, int max_parts) {
+// Each further part costs `overhead` of a CTA's work (its prologue, the
+// partial results and their merge).
+static int split_parts(const AttnArgs& a, int num_sms, int rows_per_cta, int bn, int max_parts,
+                       double overhead) {
   const int ntiles = (a.n + rows_per_cta - 1) / rows_per_cta;
   int nb_min = INT32_MAX;
   for (int t = 0; t < ntiles; ++t) {
@@ -1985,7 +1688,7 @@ static int split_parts(const AttnArgs& a, int num_sms, int rows_per_cta, int bn,
   double best_cost = 1e30;
   for (int P = 1; P <= max_parts && P <= nb_min; ++P) {
     const double waves = std::ceil((double)units * P / num_sms);
-    const double cost = waves / P * (1.0 + 0.02 * (P - 1));
+    const double cost = waves / P * (1.0 + overhead * (P - 1));
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = P;
@@ -2066,7 +1769,9 @@ int launch_fwd2(const AttnArgs& a, int* err, cudaStream_t st, int* kernels) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t plane = (int64_t)a.n * a.H * a.hd, ml = (int64_t)2 * a.n * a.H;
-    int parts = split_parts(a, sms, 2 * BM, BN2, 3);
+    // measured at the 3B shapes: 3 parts beat 1 at 1024 rows (96 tile pairs
+    // for 148 SMs) and lose at 4096 rows, where the pairs fill 2.6 waves
+    int parts = split_parts(a, sms, 2 * BM, BN2, 3, 0.08);
     while (parts > 1 && (int64_t)parts * (plane + ml) > a.ws_elems) --parts;
     if (parts > 1) {
       p.parts = parts;
@@ -2151,7 +1856,7 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
     attn_bwd_prep_tc_kernel<<<(warps + 7) / 8, 256, 0, st>>>((const bf16*)a.dout, (const bf16*)a.out, a.n, a.H,
                                                              a.hd, a.Dsum, a.ld_lse);
   }
-  p.parts = split_parts(a, num_sms, 2 * BM, BN, 4);
+  p.parts = split_parts(a, num_sms, 2 * BM, BN, 4, 0.02);
   const int64_t plane = (int64_t)a.n * a.H * a.hd;
   if (p.parts > 1 && (int64_t)p.parts * plane > a.ws_elems) p.parts = 1;
   attn_dq2_tc_kernel<NA><<<dim3((a.n + 2 * BM - 1) / (2 * BM), a.H, p.parts), 576, DQ::SMEM, st>>>(mq, mdo, mk, mv,
