@@ -443,6 +443,8 @@ __global__ void __launch_bounds__(192, 2)
 // shared memory.  Because MMAs of one thread complete in issue order, the
 // completion of S_t(j) also means P_t(j-1) V has completed: the softmax may
 // then overwrite P_t and rescale O_t without further waiting.
+// Ten warps: warp 0 loads (TMA), warp 1 issues the MMAs, warps 2-5 and 6-9
+// are the softmax warpgroups of tiles 0 and 1, one thread per query row.
 // ---------------------------------------------------------------------------
 constexpr int BN2 = 128;  // keys per block
 
@@ -454,11 +456,7 @@ struct Fwd2Smem {
   static constexpr int K_OFF = 2 * Q_BYTES;
   static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
-  // row-max exchange [tile][parity][half][128] and row-sum exchange
-  // [tile][half][128] between the two warps that share a TMEM lane quarter
-  static constexpr int XMAX_OFF = BAR_OFF + 256;
-  static constexpr int XL_OFF = XMAX_OFF + 2 * 2 * 2 * 128 * 4;
-  static constexpr int END = XL_OFF + 2 * 2 * 128 * 4;
+  static constexpr int END = BAR_OFF + 256;
   // at least 120 KB: one CTA (512 TMEM columns) per SM
   static constexpr int SMEM = END > 120 * 1024 ? END : 120 * 1024;
 };
@@ -554,7 +552,7 @@ __device__ __forceinline__ void tile2_range(const FwdParams& p, int r0, int t, l
 }
 
 template <int NA>
-__global__ void __launch_bounds__(576, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_fwd2_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                         const __grid_constant__ CUtensorMap mapV, FwdParams p) {
   using SM = Fwd2Smem<NA>;
@@ -570,7 +568,6 @@ __global__ void __launch_bounds__(576, 1)
   const uint32_t p_full = bar0 + 72;    // [2] tiles
   const uint32_t o_done = bar0 + 88;    // [2] tiles
   const uint32_t drain = bar0 + 104;
-  const uint32_t xbar = bar0 + 112;     // [2 tiles][4 quarters]: half-warp exchange
   uint32_t* tmem_slot = (uint32_t*)(smem + SM::BAR_OFF + 192);
   volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 196);
 
@@ -598,11 +595,10 @@ __global__ void __launch_bounds__(576, 1)
       tc::mbar_init(k_empty + 8 * s, 1);
       tc::mbar_init(v_empty + 8 * s, 1);
       tc::mbar_init(s_full + 8 * s, 1);
-      tc::mbar_init(p_full + 8 * s, 8);  // one arrival per softmax warp of the tile
+      tc::mbar_init(p_full + 8 * s, 4);  // one arrival per softmax warp of the tile
       tc::mbar_init(o_done + 8 * s, 1);
     }
     tc::mbar_init(drain, 1);
-    for (int x = 0; x < 8; ++x) tc::mbar_init(xbar + 8 * x, 2);  // the two warps of a lane quarter
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -731,15 +727,12 @@ __global__ void __launch_bounds__(576, 1)
       }
     }
   } else {
-    // ---------------- softmax: warps 2-9 tile 0, warps 10-17 tile 1 ------
-    // Two warps share each TMEM lane quarter of a tile; warp half hf takes
-    // keys [64 hf, 64 hf + 64) of every block and output columns
-    // [64 hf, 64 hf + 64).  The block's row maximum is combined through
-    // shared memory (double-buffered by block parity) and an mbarrier of the
-    // 64 threads of the pair, whose waits are bounded like every other wait
-    // here; each half keeps its own partial row sum.
-    const int t = (warp - 2) >> 3;
-    const int hf = ((warp - 2) >> 2) & 1;
+    // ---------------- softmax: warps 2-5 tile 0, warps 6-9 tile 1 --------
+    // One warp per TMEM lane quarter of a tile, one thread per query row
+    // holding all 128 scores of the block in registers: the row maximum
+    // needs no exchange between warps, and a warp overwrites only its own
+    // rows' scores with their packed P (keys 2c, 2c+1 -> column c).
+    const int t = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int grow_ = r0 + BM * t + row;
@@ -747,14 +740,10 @@ __global__ void __launch_bounds__(576, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tS = tmem + 128 * t + lane_off;
     const uint32_t tO = tmem + 256 + 128 * t + lane_off;
-    float* xmax = (float*)(smem + SM::XMAX_OFF) + t * (2 * 2 * 128);
-    float* xl = (float*)(smem + SM::XL_OFF) + t * (2 * 128);
-    const uint32_t xb = xbar + 8 * (4 * t + quarter);
     const float NEG_INF = -INFINITY;
     float m_run = NEG_INF, l_run = 0.f;
     bool ok = true;
     int cnt = 0;
-    int xph = 0;  // completed phases of this pair's exchange barrier
     long long my_lo, my_hi;
     tile2_range(p, r0, t, &my_lo, &my_hi);
     my_lo = max(my_lo, kb_lo);
@@ -765,44 +754,33 @@ __global__ void __launch_bounds__(576, 1)
         break;
       }
       tc::tc_fence_after();
-      float sv[64];
-      tmem_ld32_nw(tS + 64 * hf, *reinterpret_cast<float(*)[32]>(&sv[0]));
-      tmem_ld32_nw(tS + 64 * hf + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+      float sv[128];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld32_nw(tS + 32 * q, *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
       tmem_wait_ld();
       const long long kpos = j * BN2;
-      const long long lo_l = pos - p.W + 1 - kpos - 64 * hf, hi_l = pos - kpos - 64 * hf;
-      const int lo = (int)(lo_l < -1 ? -1 : (lo_l > 64 ? 64 : lo_l));
-      const int hi = (int)(hi_l < -1 ? -1 : (hi_l > 64 ? 64 : hi_l));
+      const long long lo_l = pos - p.W + 1 - kpos, hi_l = pos - kpos;
+      const int lo = (int)(lo_l < -1 ? -1 : (lo_l > 128 ? 128 : lo_l));
+      const int hi = (int)(hi_l < -1 ? -1 : (hi_l > 128 ? 128 : hi_l));
       // maximum of the raw scores (the scale is positive); masked -> -inf
-      if (!(lo <= 0 && hi >= 63)) {
+      if (!(lo <= 0 && hi >= 127)) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) sv[c] = (c >= lo && c <= hi) ? sv[c] : NEG_INF;
+        for (int c = 0; c < 128; ++c) sv[c] = (c >= lo && c <= hi) ? sv[c] : NEG_INF;
       }
       float mb = NEG_INF;
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) mb = max3f(mb, sv[c], sv[c + 1]);
+      for (int c = 0; c < 128; c += 2) mb = max3f(mb, sv[c], sv[c + 1]);
       mb *= p.scale_log2;
-      float* xm = xmax + (cnt & 1) * (2 * 128);
-      xm[hf * 128 + row] = mb;
-      warp_arrive(xb);
-      if (!warp_wait(xb, xph & 1, p.err, ERR_A_SOFT, abort)) {
-        ok = false;
-        break;
-      }
-      ++xph;
-      mb = fmaxf(xm[row], xm[128 + row]);
       const bool grow = mb > m_run + 8.0f;
       const float m_new = grow ? mb : m_run;
       const float alpha = (grow && m_run != NEG_INF) ? exp2f(m_run - m_new) : 1.0f;
       const float m_use = m_new == NEG_INF ? 0.f : m_new;
       // P_t(j-1) V has completed (it was issued before S_t(j)): O_t is
-      // stable and P_t may be overwritten.  Keys [64 hf, 64 hf + 64) go to
-      // packed columns [32 hf, 32 hf + 32); the other half's columns of S
-      // were read before the exchange above.
+      // stable and P_t may be overwritten.
       // p = 2^(s * scale - m): one packed FMA per two scores, one MUFU each
       float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
+      for (int q = 0; q < 4; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
@@ -813,13 +791,13 @@ __global__ void __launch_bounds__(576, 1)
           ls1 += p1;
           pk[c] = pack_bf16(p0, p1);
         }
-        tmem_st16u(tS + 32 * hf + 16 * q, pk);
+        tmem_st16u(tS + 16 * q, pk);
       }
       const float ls = ls0 + ls1;
       l_run = l_run * alpha + ls;
       m_run = m_new;
       if (cnt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        for (int c0 = 64 * hf; c0 < nO && c0 < 64 * hf + 64; c0 += 32) {
+        for (int c0 = 0; c0 < nO; c0 += 32) {
           float v[32];
           tc::tmem_ld32(tO + c0, v);
 #pragma unroll
@@ -831,14 +809,7 @@ __global__ void __launch_bounds__(576, 1)
       tc::tc_fence_before();
       warp_arrive(p_full + 8 * t);
     }
-    // row sum = both halves' partial sums
-    float l_tot = 0.f;
-    if (ok) {
-      xl[hf * 128 + row] = l_run;
-      warp_arrive(xb);
-      ok = warp_wait(xb, xph & 1, p.err, ERR_A_SOFT, abort);
-      l_tot = xl[row] + xl[128 + row];
-    }
+    const float l_tot = l_run;
     if (ok && p.parts > 1) {
       // this part's share: the unnormalised output (zero if the tile saw no
       // key block here) and (max, sum) of the row, merged by the combine
@@ -848,7 +819,7 @@ __global__ void __launch_bounds__(576, 1)
       if (ok) {
         tc::tc_fence_after();
         const int64_t ldw = (int64_t)p.H * p.hd;
-        for (int c0 = 64 * hf; c0 < nO && c0 < 64 * hf + 64; c0 += 32) {
+        for (int c0 = 0; c0 < nO; c0 += 32) {
           float v[32];
           if (have) {
             tc::tmem_ld32(tO + c0, v);
@@ -863,14 +834,14 @@ __global__ void __launch_bounds__(576, 1)
               if (c0 + k < p.hd) *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
           }
         }
-        if (hf == 0 && grow_ < p.n)
+        if (grow_ < p.n)
           *reinterpret_cast<float2*>(p.ws_ml + (((int64_t)zpart * p.H + h) * p.n + grow_) * 2) =
               make_float2(have ? m_run : NEG_INF, have ? l_tot : 0.f);
       }
     } else if (ok && cnt > 0 && warp_wait(o_done + 8 * t, (cnt - 1) & 1, p.err, ERR_A_SOFT, abort)) {
       tc::tc_fence_after();
       const float il = 1.0f / l_tot;
-      for (int c0 = 64 * hf; c0 < nO && c0 < 64 * hf + 64; c0 += 32) {
+      for (int c0 = 0; c0 < nO; c0 += 32) {
         float v[32];
         tc::tmem_ld32(tO + c0, v);
         if (grow_ < p.n) {
@@ -888,7 +859,7 @@ __global__ void __launch_bounds__(576, 1)
           }
         }
       }
-      if (hf == 0 && grow_ < p.n)
+      if (grow_ < p.n)
         p.lse[(int64_t)h * p.ld_lse + grow_] = (m_run + log2f(l_tot)) * 0.69314718055994531f;
     }
   }
@@ -1780,7 +1751,7 @@ int launch_fwd2(const AttnArgs& a, int* err, cudaStream_t st, int* kernels) {
     }
   }
   dim3 grid((a.n + 2 * BM - 1) / (2 * BM), a.H, p.parts);
-  attn_fwd2_tc_kernel<NA><<<grid, 576, SM::SMEM, st>>>(mq, mk, mv, p);
+  attn_fwd2_tc_kernel<NA><<<grid, 320, SM::SMEM, st>>>(mq, mk, mv, p);
   if (kernels) *kernels = p.parts > 1 ? 2 : 1;
   if (p.parts > 1) {
     const int64_t warps = (int64_t)a.n * a.H;
