@@ -898,106 +898,114 @@ struct BwdParams {
   int64_t ldg;
   float* ws;
   int* err;
+  const float2* cs;  // RoPE table [n][hd/2] to rotate dq, dk back with, or null
 };
 
+// The transpose of the forward's RoPE rotation on one adjacent column pair
+// (the pair-interleaved layout of q and k): (x, y) -> (x c + y s, y c - x s).
+__device__ __forceinline__ void rope_back(float& x, float& y, float2 cs) {
+  const float x0 = x;
+  x = x0 * cs.x + y * cs.y;
+  y = y * cs.x - x0 * cs.y;
+}
 
-// --- dq, two query tiles per CTA, dS kept in TMEM ---------------------------
-// A CTA takes 256 query rows (two 128-row tiles) of one head over 64-key
-// blocks, and dS is written back into TMEM (two bf16
-// per 32-bit column) where the dQ product reads it as its A operand:
-//   TMEM per tile t: S [256t, +64) | dP [256t+64, +64) | dQ [256t+128, +128)
-// Each of the 16 compute warps (two per lane quarter and tile) handles 32
-// keys of a block and writes its packed dS over score columns it has read
-// itself (keys 32hf.. -> columns 32hf.., 16 wide), so no warp overwrites
-// scores another warp still has to read; the dQ MMA takes its four K = 16
-// slices from columns {0, 8, 32, 40}.  The MMA warp ping-pongs the tiles.
-// Keys and values move through separate rings of DQ_STAGES blocks: a value
-// block is released once both tiles' dP products of it are issued, a key
-// block once both dQ products are, so the loads run two blocks ahead of the
-// products that need them.
-constexpr int DQ_STAGES = 3;
+
+// --- dq: one 128-row query tile per CTA over 128-key blocks ----------------
+// A CTA takes 128 query rows of one head (all or a part of their key range)
+// over blocks of DQ_BN = 128 keys, so every score product is a
+// 128 x 128 x 16 MMA (64-key blocks made them 128 x 64, which the tensor
+// core runs at two thirds of its rate).  TMEM: S of block i in buffer
+// i & 1 (columns [0, 128) or [384, 512)), dP in [128, 256), dQ in
+// [256, 384).  The compute warps turn S and dP into
+// dS = P (dP - D) / sqrt(hd), written back as bf16 pairs over score columns
+// each warp has read itself (keys 32 ks.. -> columns 32 ks.., 16 wide), and
+// the dQ product reads dS from TMEM as its A operand (K = 16 slices at
+// columns 32 (k >> 1) + 8 (k & 1)).
+// MMA order for block i: S(i + 1) into the other S buffer, then (once dS(i)
+// is ready) dQ(i), then dP(i + 1); so the tensor core computes the next
+// scores while dS(i) is formed.  Products of one thread run in issue order,
+// which keeps every buffer's reader ahead of its next writer.
+// Eighteen warps: warp 0 loads (TMA), warp 1 issues the MMAs, warps 2-17
+// compute dS (four per TMEM lane quarter, 32 of a block's 128 keys each).
+// Keys move through a ring of 3 blocks, values through a ring of 2: a key
+// block is released once its dQ product is done, a value block once its dP
+// product is.
+constexpr int DQ_BN = 128;
+constexpr int DQ_KST = 3, DQ_VST = 2;
 template <int NA>
-struct Dq2Smem {
-  static constexpr int Q_BYTES = NA * BM * 128;   // one 128-row tile
-  static constexpr int KV_BYTES = NA * BN * 128;  // one 64-key block
-  static constexpr int Q_OFF = 0;                 // Q0, Q1
-  static constexpr int DO_OFF = 2 * Q_BYTES;      // dO0, dO1
-  static constexpr int K_OFF = 4 * Q_BYTES;
-  static constexpr int V_OFF = K_OFF + DQ_STAGES * KV_BYTES;
-  static constexpr int BAR_OFF = V_OFF + DQ_STAGES * KV_BYTES;
+struct DqSmem {
+  static constexpr int Q_BYTES = NA * BM * 128;      // one 128-row tile
+  static constexpr int KV_BYTES = NA * DQ_BN * 128;  // one 128-key block
+  static constexpr int Q_OFF = 0;
+  static constexpr int DO_OFF = Q_BYTES;
+  static constexpr int K_OFF = 2 * Q_BYTES;
+  static constexpr int V_OFF = K_OFF + DQ_KST * KV_BYTES;
+  static constexpr int BAR_OFF = V_OFF + DQ_VST * KV_BYTES;
+  // at least 120 KB: one CTA (512 TMEM columns) per SM
   static constexpr int SMEM = BAR_OFF + 256 > 120 * 1024 ? BAR_OFF + 256 : 120 * 1024;
   static_assert(SMEM <= 232448, "shared memory");
-  static_assert(8 + 32 * DQ_STAGES + 48 <= 192, "barrier area");
+  static_assert(8 + 16 * (DQ_KST + DQ_VST) + 32 <= 192, "barrier area");
 };
 
-// key-block range of query tile t of the pair at r0 for the dq kernel
-__device__ __forceinline__ void dq2_range(const BwdParams& p, int r0, int t, long long* lo, long long* hi) {
-  const int rs = r0 + BM * t;
-  if (rs >= p.n) {
-    *lo = 1;
-    *hi = 0;
-    return;
-  }
-  const long long t_lo = p.pos0 + rs;
-  const long long t_hi = p.pos0 + min(rs + BM, p.n) - 1;
+// key-block range [lo, hi] (blocks of DQ_BN) of the tile starting at row r0
+__device__ __forceinline__ void dq_range(const BwdParams& p, int r0, long long* lo, long long* hi) {
+  const long long t_lo = p.pos0 + r0;
+  const long long t_hi = p.pos0 + min(r0 + BM, p.n) - 1;
   long long k_lo = t_lo - p.W + 1;
   if (k_lo < 0) k_lo = 0;
-  *lo = k_lo / BN;
-  *hi = t_hi / BN;
+  *lo = k_lo / DQ_BN;
+  *hi = t_hi / DQ_BN;
 }
 
 template <int NA>
 __global__ void __launch_bounds__(576, 1)
-    attn_dq2_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
-                       const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-                       BwdParams p) {
-  using SM = Dq2Smem<NA>;
+    attn_dq_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
+                      const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                      BwdParams p) {
+  using SM = DqSmem<NA>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = tc::smem_u32(smem);
-  constexpr int NS = DQ_STAGES;
   const uint32_t bar0 = sbase + SM::BAR_OFF;
   const uint32_t q_full = bar0;
-  const uint32_t k_full = bar0 + 8;             // [NS] stages
-  const uint32_t v_full = k_full + 8 * NS;      // [NS]
-  const uint32_t k_empty = v_full + 8 * NS;     // [NS]
-  const uint32_t v_empty = k_empty + 8 * NS;    // [NS]
-  const uint32_t s_full = v_empty + 8 * NS;     // [2] tiles
-  const uint32_t ds_full = s_full + 16;         // [2] tiles
-  const uint32_t dq_done = ds_full + 16;
+  const uint32_t k_full = bar0 + 8;                // [DQ_KST]
+  const uint32_t k_empty = k_full + 8 * DQ_KST;    // [DQ_KST]
+  const uint32_t v_full = k_empty + 8 * DQ_KST;    // [DQ_VST]
+  const uint32_t v_empty = v_full + 8 * DQ_VST;    // [DQ_VST]
+  const uint32_t sdp_full = v_empty + 8 * DQ_VST;  // S(i) and dP(i) done
+  const uint32_t ds_full = sdp_full + 8;           // dS(i) written
+  const uint32_t dq_done = ds_full + 8;
   const uint32_t drain = dq_done + 8;
   uint32_t* tmem_slot = (uint32_t*)(smem + SM::BAR_OFF + 192);
   volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 196);
-  // stage and phase parity of the i-th block of the rings
-  auto stage_of = [](int i) { return i % NS; };
-  auto phase_of = [](int i) { return (uint32_t)((i / NS) & 1); };
+  // ring slot and phase parity of block i in a ring of `st` slots
+  auto slot = [](int i, int st) { return i % st; };
+  auto par = [](int i, int st) { return (uint32_t)((i / st) & 1); };
+  // TMEM column of the S buffer of block i
+  auto s_col = [](int i) { return (uint32_t)((i & 1) ? 384 : 0); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = blockIdx.x * 2 * BM, h = blockIdx.y, part = blockIdx.z;
+  const int r0 = blockIdx.x * BM, h = blockIdx.y, part = blockIdx.z;
   const int kvh = h / (p.H / p.Hkv);
-  long long lo_t[2], hi_t[2];
-  dq2_range(p, r0, 0, &lo_t[0], &hi_t[0]);
-  dq2_range(p, r0, 1, &lo_t[1], &hi_t[1]);
-  const long long u_lo = lo_t[0];
-  const long long u_hi = hi_t[1] >= lo_t[1] ? max(hi_t[0], hi_t[1]) : hi_t[0];
-  const long long nb_all = u_hi - u_lo + 1;
-  const long long jb = u_lo + part * nb_all / p.parts;         // this part's blocks
-  const int nb = (int)(u_lo + (part + 1) * nb_all / p.parts - jb);
-  auto part_of = [&](int t, long long j) { return j >= lo_t[t] && j <= hi_t[t]; };
+  long long t_lo_b, t_hi_b;
+  dq_range(p, r0, &t_lo_b, &t_hi_b);
+  const long long nb_all = t_hi_b - t_lo_b + 1;
+  const long long jb = t_lo_b + part * nb_all / p.parts;  // this part's blocks
+  const int nb = (int)(t_lo_b + (part + 1) * nb_all / p.parts - jb);
   const int ksteps = p.hd / 16;
   const int nO = (p.hd + 15) & ~15;
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < DQ_KST; ++s) {
       tc::mbar_init(k_full + 8 * s, 1);
-      tc::mbar_init(v_full + 8 * s, 1);
       tc::mbar_init(k_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < DQ_VST; ++s) {
+      tc::mbar_init(v_full + 8 * s, 1);
       tc::mbar_init(v_empty + 8 * s, 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      tc::mbar_init(s_full + 8 * t, 1);
-      tc::mbar_init(ds_full + 8 * t, 8);  // one arrival per compute warp of the tile
-    }
+    tc::mbar_init(sdp_full, 1);
+    tc::mbar_init(ds_full, 16);  // one arrival per compute warp
     tc::mbar_init(dq_done, 1);
     tc::mbar_init(drain, 1);
     *abort = 0;
@@ -1022,35 +1030,32 @@ __global__ void __launch_bounds__(576, 1)
     if (lane == 0 && nb > 0) {
       bool ok = true;
       int issued_k = 0, issued_v = 0;
-      tc::mbar_arrive_expect_tx(q_full, 4 * SM::Q_BYTES);
-      for (int t = 0; t < 2; ++t)
-        for (int a = 0; a < NA; ++a) {
-          tc::tma_load_2d(sbase + SM::Q_OFF + t * SM::Q_BYTES + a * BM * 128, &mapQ, h * p.hd + 64 * a,
-                          r0 + BM * t, q_full);
-          tc::tma_load_2d(sbase + SM::DO_OFF + t * SM::Q_BYTES + a * BM * 128, &mapDO, h * p.hd + 64 * a,
-                          r0 + BM * t, q_full);
-        }
+      tc::mbar_arrive_expect_tx(q_full, 2 * SM::Q_BYTES);
+      for (int a = 0; a < NA; ++a) {
+        tc::tma_load_2d(sbase + SM::Q_OFF + a * BM * 128, &mapQ, h * p.hd + 64 * a, r0, q_full);
+        tc::tma_load_2d(sbase + SM::DO_OFF + a * BM * 128, &mapDO, h * p.hd + 64 * a, r0, q_full);
+      }
       for (int i = 0; i < nb && ok; ++i) {
-        const int st = stage_of(i);
-        const long long kpos = (jb + i) * BN;
+        const long long kpos = (jb + i) * DQ_BN;
         const int row = kvh * p.R + (int)(kpos % p.R);
-        if (!tc::mbar_wait(k_empty + 8 * st, phase_of(i) ^ 1, p.err, ERR_A_PROD, abort)) {
+        const int ks = slot(i, DQ_KST), vs = slot(i, DQ_VST);
+        if (!tc::mbar_wait(k_empty + 8 * ks, par(i, DQ_KST) ^ 1, p.err, ERR_A_PROD, abort)) {
           ok = false;
           break;
         }
-        tc::mbar_arrive_expect_tx(k_full + 8 * st, SM::KV_BYTES);
+        tc::mbar_arrive_expect_tx(k_full + 8 * ks, SM::KV_BYTES);
         for (int a = 0; a < NA; ++a)
-          tc::tma_load_2d(sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN * 128, &mapK, 64 * a, row,
-                          k_full + 8 * st);
+          tc::tma_load_2d(sbase + SM::K_OFF + ks * SM::KV_BYTES + a * DQ_BN * 128, &mapK, 64 * a, row,
+                          k_full + 8 * ks);
         issued_k = i + 1;
-        if (!tc::mbar_wait(v_empty + 8 * st, phase_of(i) ^ 1, p.err, ERR_A_PROD, abort)) {
+        if (!tc::mbar_wait(v_empty + 8 * vs, par(i, DQ_VST) ^ 1, p.err, ERR_A_PROD, abort)) {
           ok = false;
           break;
         }
-        tc::mbar_arrive_expect_tx(v_full + 8 * st, SM::KV_BYTES);
+        tc::mbar_arrive_expect_tx(v_full + 8 * vs, SM::KV_BYTES);
         for (int a = 0; a < NA; ++a)
-          tc::tma_load_2d(sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN * 128, &mapV, 64 * a, row,
-                          v_full + 8 * st);
+          tc::tma_load_2d(sbase + SM::V_OFF + vs * SM::KV_BYTES + a * DQ_BN * 128, &mapV, 64 * a, row,
+                          v_full + 8 * vs);
         issued_v = i + 1;
       }
       // the CTA must not exit with copies into its shared memory in flight
@@ -1058,80 +1063,80 @@ __global__ void __launch_bounds__(576, 1)
       const long long t0 = clock64();
       while (!tc::mbar_try_wait(q_full, 0) && clock64() - t0 < tc::kWaitClocks) {
       }
-      for (int i = (issued_k > NS ? issued_k - NS : 0); i < issued_k; ++i) {
+      for (int i = (issued_k > DQ_KST ? issued_k - DQ_KST : 0); i < issued_k; ++i) {
         const long long t1 = clock64();
-        while (!tc::mbar_try_wait(k_full + 8 * stage_of(i), phase_of(i)) && clock64() - t1 < tc::kWaitClocks) {
+        while (!tc::mbar_try_wait(k_full + 8 * slot(i, DQ_KST), par(i, DQ_KST)) &&
+               clock64() - t1 < tc::kWaitClocks) {
         }
       }
-      for (int i = (issued_v > NS ? issued_v - NS : 0); i < issued_v; ++i) {
+      for (int i = (issued_v > DQ_VST ? issued_v - DQ_VST : 0); i < issued_v; ++i) {
         const long long t1 = clock64();
-        while (!tc::mbar_try_wait(v_full + 8 * stage_of(i), phase_of(i)) && clock64() - t1 < tc::kWaitClocks) {
+        while (!tc::mbar_try_wait(v_full + 8 * slot(i, DQ_VST), par(i, DQ_VST)) &&
+               clock64() - t1 < tc::kWaitClocks) {
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && nb > 0) {
-      const uint32_t idS = tc::idesc_bf16(BM, BN, 0, 0);
+      const uint32_t idS = tc::idesc_bf16(BM, DQ_BN, 0, 0);
       const uint32_t idQ = tc::idesc_bf16(BM, nO, 0, 1);
       bool ok = tc::mbar_wait(q_full, 0, p.err, ERR_A_MMA, abort);
       bool issued = false;
-      int cnt[2] = {0, 0};
-      auto issue_sdp = [&](int t, int i) -> bool {
-        const int st = stage_of(i);
-        if (!tc::mbar_wait(k_full + 8 * st, phase_of(i), p.err, ERR_A_MMA, abort) ||
-            !tc::mbar_wait(v_full + 8 * st, phase_of(i), p.err, ERR_A_MMA, abort))
-          return false;
+      // S(i) = Q K(i)^T into its S buffer
+      auto issue_s = [&](int i) -> bool {
+        const int ks = slot(i, DQ_KST);
+        if (!tc::mbar_wait(k_full + 8 * ks, par(i, DQ_KST), p.err, ERR_A_MMA, abort)) return false;
         tc::tc_fence_after();
-        const uint32_t kb = sbase + SM::K_OFF + st * SM::KV_BYTES;
-        const uint32_t vb = sbase + SM::V_OFF + st * SM::KV_BYTES;
+        const uint32_t kb = sbase + SM::K_OFF + ks * SM::KV_BYTES;
         for (int j = 0; j < ksteps; ++j) {
           const int a = j >> 2;
-          const uint32_t ao = a * BM * 128 + 32 * (j & 3);
-          const uint32_t bo = a * BN * 128 + 32 * (j & 3);
-          tc::mma_bf16(tmem + 256 * t, tc::smem_desc_sw128(sbase + SM::Q_OFF + t * SM::Q_BYTES + ao, 16, 1024),
-                       tc::smem_desc_sw128(kb + bo, 16, 1024), idS, j > 0);
-          tc::mma_bf16(tmem + 256 * t + 64,
-                       tc::smem_desc_sw128(sbase + SM::DO_OFF + t * SM::Q_BYTES + ao, 16, 1024),
-                       tc::smem_desc_sw128(vb + bo, 16, 1024), idS, j > 0);
+          tc::mma_bf16(tmem + s_col(i), tc::smem_desc_sw128(sbase + SM::Q_OFF + a * BM * 128 + 32 * (j & 3), 16, 1024),
+                       tc::smem_desc_sw128(kb + a * DQ_BN * 128 + 32 * (j & 3), 16, 1024), idS, j > 0);
         }
-        tc::mma_commit(s_full + 8 * t);
         issued = true;
         return true;
       };
-      // Issue order per block i: dQ(0, i), S/dP(0, i+1), [release K(i)],
-      // dQ(1, i), S/dP(1, i+1), [release V(i+1)].  Every block of the part
-      // is used by at least one tile, so each ring slot is released exactly
-      // once per use.
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-        if (ok && part_of(t, jb)) ok = issue_sdp(t, 0);
-      if (ok) tc::mma_commit(v_empty + 8 * stage_of(0));
-      for (int i = 0; i < nb && ok; ++i) {
-        const long long j = jb + i;
-        const int st = stage_of(i);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!ok) break;
-          if (part_of(t, j)) {
-            if (!tc::mbar_wait(ds_full + 8 * t, cnt[t] & 1, p.err, ERR_A_MMA, abort)) {
-              ok = false;
-              break;
-            }
-            tc::tc_fence_after();
-            const uint32_t kb = sbase + SM::K_OFF + st * SM::KV_BYTES;
-#pragma unroll
-            for (int k = 0; k < BN / 16; ++k)
-              mma_bf16_ts(tmem + 256 * t + 128, tmem + 256 * t + (k < 2 ? 8 * k : 32 + 8 * (k - 2)),
-                          tc::smem_desc_sw128(kb + 2048 * k, BN * 128, 1024), idQ, (cnt[t] > 0 || k > 0) ? 1u : 0u);
-            ++cnt[t];
-          }
-          // both dQ products of block i are issued: its key slot frees
-          // when they complete
-          if (t == 1) tc::mma_commit(k_empty + 8 * st);
-          if (i + 1 < nb && part_of(t, j + 1)) ok = issue_sdp(t, i + 1);
+      // dP(i) = dO V(i)^T; then S(i) and dP(i) are both on their way to the
+      // compute warps, and V(i) is free once dP(i) is done
+      auto issue_dp = [&](int i) -> bool {
+        const int vs = slot(i, DQ_VST);
+        if (!tc::mbar_wait(v_full + 8 * vs, par(i, DQ_VST), p.err, ERR_A_MMA, abort)) return false;
+        tc::tc_fence_after();
+        const uint32_t vb = sbase + SM::V_OFF + vs * SM::KV_BYTES;
+        for (int j = 0; j < ksteps; ++j) {
+          const int a = j >> 2;
+          tc::mma_bf16(tmem + 128, tc::smem_desc_sw128(sbase + SM::DO_OFF + a * BM * 128 + 32 * (j & 3), 16, 1024),
+                       tc::smem_desc_sw128(vb + a * DQ_BN * 128 + 32 * (j & 3), 16, 1024), idS, j > 0);
         }
-        // both dP products of block i + 1 are issued: its value slot frees
-        if (ok && i + 1 < nb) tc::mma_commit(v_empty + 8 * stage_of(i + 1));
+        tc::mma_commit(sdp_full);
+        tc::mma_commit(v_empty + 8 * vs);
+        issued = true;
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok) ok = issue_dp(0);
+      for (int i = 0; i < nb && ok; ++i) {
+        if (i + 1 < nb && !issue_s(i + 1)) {
+          ok = false;
+          break;
+        }
+        if (!tc::mbar_wait(ds_full, (uint32_t)(i & 1), p.err, ERR_A_MMA, abort)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const int ks = slot(i, DQ_KST);
+        const uint32_t kb = sbase + SM::K_OFF + ks * SM::KV_BYTES;
+#pragma unroll
+        for (int k = 0; k < DQ_BN / 16; ++k)
+          mma_bf16_ts(tmem + 256, tmem + s_col(i) + 32 * (k >> 1) + 8 * (k & 1),
+                      tc::smem_desc_sw128(kb + 2048 * k, DQ_BN * 128, 1024), idQ, (i > 0 || k > 0) ? 1u : 0u);
+        // K(i) has served S(i) and dQ(i)
+        tc::mma_commit(k_empty + 8 * ks);
+        if (i + 1 < nb && !issue_dp(i + 1)) {
+          ok = false;
+          break;
+        }
       }
       if (ok) tc::mma_commit(dq_done);
       if (!ok && issued) {
@@ -1142,38 +1147,33 @@ __global__ void __launch_bounds__(576, 1)
       }
     }
   } else {
-    const int t = (warp - 2) >> 3;
-    const int hf = ((warp - 2) >> 2) & 1;
+    const int ks = (warp - 2) >> 2;  // key slice [32 ks, 32 ks + 32) of a block
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int grow_ = r0 + BM * t + row;
+    const int grow_ = r0 + row;
     const long long pos = p.pos0 + grow_;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tT = tmem + 256 * t + lane_off;
     const bool rvalid = grow_ < p.n;
     const float lse2 = rvalid ? p.lse[(int64_t)h * p.ld_lse + grow_] * 1.4426950408889634f : 0.f;
     const float Dt = rvalid ? p.dsum[(int64_t)h * p.ld_lse + grow_] : 0.f;
-    long long my_lo, my_hi;
-    dq2_range(p, r0, t, &my_lo, &my_hi);
-    const long long j_beg = max(my_lo, jb), j_end = min(my_hi, jb + nb - 1);
+    // dS = P (dP - D) / sqrt(hd) = P * (dP * scale - D * scale)
+    const float nDs = -Dt * p.scale;
     bool ok = true;
-    int cnt = 0;
-    for (long long j = j_beg; j <= j_end; ++j, ++cnt) {
-      if (!warp_wait(s_full + 8 * t, cnt & 1, p.err, ERR_A_SOFT, abort)) {
+    for (int i = 0; i < nb; ++i) {
+      if (!warp_wait(sdp_full, (uint32_t)(i & 1), p.err, ERR_A_SOFT, abort)) {
         ok = false;
         break;
       }
       tc::tc_fence_after();
+      const uint32_t ts = tmem + s_col(i) + lane_off + 32 * ks;
       float sv[32], dp[32];
-      tmem_ld32_nw(tT + 32 * hf, sv);
-      tmem_ld32_nw(tT + 64 + 32 * hf, dp);
+      tmem_ld32_nw(ts, sv);
+      tmem_ld32_nw(tmem + 128 + lane_off + 32 * ks, dp);
       tmem_wait_ld();
-      const long long kpos = j * BN + 32 * hf;
+      const long long kpos = (jb + i) * DQ_BN + 32 * ks;
       const long long lo_l = pos - p.W + 1 - kpos, hi_l = pos - kpos;
       const int lo = (int)(lo_l < -1 ? -1 : (lo_l > 32 ? 32 : lo_l));
       const int hi = (int)(hi_l < -1 ? -1 : (hi_l > 32 ? 32 : hi_l));
-      // dS = P (dP - D) / sqrt(hd) = P * (dP * scale - D * scale)
-      const float nDs = -Dt * p.scale;
       uint32_t pk[16];
 #pragma unroll
       for (int c = 0; c < 32; c += 2) {
@@ -1185,25 +1185,31 @@ __global__ void __launch_bounds__(576, 1)
         mul2(p0, p1, y0, y1, d0, d1);
         pk[c / 2] = pack_bf16(d0, d1);
       }
-      tmem_st16u(tT + 32 * hf, pk);
+      tmem_st16u(ts, pk);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc::tc_fence_before();
-      warp_arrive(ds_full + 8 * t);
+      warp_arrive(ds_full);
     }
-    const bool have = cnt > 0;
+    const bool have = nb > 0;
     if (ok && have && !warp_wait(dq_done, 0, p.err, ERR_A_SOFT, abort)) ok = false;
-    if (ok && (have || p.parts > 1)) {
+    const int c0 = 32 * ks;  // this warp's 32 columns of dQ
+    if (ok && (have || p.parts > 1) && c0 < nO) {
       tc::tc_fence_after();
-      for (int c0 = 64 * hf; c0 < nO && c0 < 64 * hf + 64; c0 += 32) {
-        float v[32];
-        if (have) {
-          tc::tmem_ld32(tT + 128 + c0, v);
-        } else {
+      float v[32];
+      if (have) {
+        tc::tmem_ld32(tmem + 256 + lane_off + c0, v);
+      } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = 0.f;
-        }
-        if (!rvalid) continue;
+        for (int k = 0; k < 32; ++k) v[k] = 0.f;
+      }
+      if (rvalid) {
         if (p.parts == 1) {
+          if (p.cs) {
+            const float2* csr = p.cs + (int64_t)grow_ * (p.hd >> 1) + (c0 >> 1);
+#pragma unroll
+            for (int k = 0; k < 32; k += 2)
+              if (c0 + k < p.hd) rope_back(v[k], v[k + 1], csr[k >> 1]);
+          }
           bf16* dst = p.dqkv + (int64_t)grow_ * p.ldg + (int64_t)h * p.hd + c0;
 #pragma unroll
           for (int k = 0; k < 32; k += 8)
@@ -1222,6 +1228,8 @@ __global__ void __launch_bounds__(576, 1)
             if (c0 + k < p.hd) *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
         }
       }
+    } else if (ok && have && c0 >= nO) {
+      tc::tc_fence_after();
     }
   }
   tc::tc_fence_before();
@@ -1561,9 +1569,11 @@ __global__ void attn_bwd_prep_tc_kernel(const bf16* __restrict__ dO, const bf16*
   if (lane == 0) dsum[(int64_t)h * ld + r] = s;
 }
 
-// dq = sum over parts (fixed order) -> bf16 columns [0, H*hd) of dqkv
+// dq = sum over parts (fixed order) -> bf16 columns [0, H*hd) of dqkv,
+// rotated back by the RoPE table cs when given
 __global__ void attn_dq_reduce_kernel(const float* __restrict__ ws, int parts, int n, int cols,
-                                      bf16* __restrict__ dqkv, int64_t ldg) {
+                                      bf16* __restrict__ dqkv, int64_t ldg, const float2* __restrict__ cs,
+                                      int hd) {
   const int64_t total = (int64_t)n * cols / 4;
   const int64_t plane = (int64_t)n * cols;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -1577,14 +1587,20 @@ __global__ void attn_dq_reduce_kernel(const float* __restrict__ ws, int parts, i
       acc.w += v.w;
     }
     const int64_t r = e / cols, c = e % cols;
+    if (cs) {
+      const float2* csr = cs + r * (hd >> 1) + ((c % hd) >> 1);
+      rope_back(acc.x, acc.y, csr[0]);
+      rope_back(acc.z, acc.w, csr[1]);
+    }
     bf16* d = dqkv + r * ldg + c;
     *reinterpret_cast<uint2*>(d) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
   }
 }
 
-// dk, dv of KV head g = sum over its query heads (fixed order) -> bf16
+// dk, dv of KV head g = sum over its query heads (fixed order) -> bf16;
+// dk rotated back by the RoPE table cs when given
 __global__ void attn_dkv_reduce_kernel(const float* __restrict__ ws, int n, int H, int Hkv, int hd,
-                                       bf16* __restrict__ dqkv, int64_t ldg) {
+                                       bf16* __restrict__ dqkv, int64_t ldg, const float2* __restrict__ cs) {
   const int group = H / Hkv;
   const int64_t total = (int64_t)2 * n * Hkv * hd / 4;
   const int64_t plane = (int64_t)H * n * hd;
@@ -1603,6 +1619,11 @@ __global__ void attn_dkv_reduce_kernel(const float* __restrict__ ws, int n, int 
       acc.y += v.y;
       acc.z += v.z;
       acc.w += v.w;
+    }
+    if (cs && which == 0) {
+      const float2* csr = cs + (int64_t)r * (hd >> 1) + (d >> 1);
+      rope_back(acc.x, acc.y, csr[0]);
+      rope_back(acc.z, acc.w, csr[1]);
     }
     bf16* dst = dqkv + (int64_t)r * ldg + (int64_t)(H + which * Hkv + g) * hd + d;
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
@@ -1788,9 +1809,9 @@ int64_t attn_bwd_tc_ws_elems(int n, int H, int hd, int num_sms) {
 
 template <int NA>
 int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
-  using DQ = Dq2Smem<NA>;
+  using DQ = DqSmem<NA>;
   using DKV = DkvSmem<NA>;
-  CUtensorMap mq, mdo, mk, mv, mq64, mdo64;
+  CUtensorMap mq, mdo, mk, mv, mq64, mdo64, mk128, mv128;
   const uint64_t ldq = (uint64_t)a.H * a.hd;
   int rc = map2d(&mq, a.q, ldq, a.n, ldq, BM);
   if (!rc) rc = map2d(&mdo, a.dout, ldq, a.n, ldq, BM);
@@ -1798,10 +1819,14 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
   if (!rc) rc = map2d(&mdo64, a.dout, ldq, a.n, ldq, BN);
   if (!rc) rc = map2d(&mk, a.kring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
   if (!rc) rc = map2d(&mv, a.vring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, BN);
+  // the dq kernel's key/value blocks: DQ_BN rows (R is a multiple of 128,
+  // so a block never wraps around the ring)
+  if (!rc) rc = map2d(&mk128, a.kring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, DQ_BN);
+  if (!rc) rc = map2d(&mv128, a.vring, a.hd, (uint64_t)a.Hkv * a.R, a.hd, DQ_BN);
   if (rc) return rc;
   static std::atomic<uint64_t> attr_dq{0}, attr_dkv{0};
   {
-    cudaError_t e = raise_smem_limit(attr_dq, attn_dq2_tc_kernel<NA>, DQ::SMEM);
+    cudaError_t e = raise_smem_limit(attr_dq, attn_dq_tc_kernel<NA>, DQ::SMEM);
     if (e == cudaSuccess) e = raise_smem_limit(attr_dkv, attn_dkv_tc_kernel<NA>, DKV::SMEM);
     if (e != cudaSuccess) return (int)e;
   }
@@ -1822,28 +1847,29 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
   p.ldg = (int64_t)(a.H + 2 * a.Hkv) * a.hd;
   p.ws = a.ws;
   p.err = err;
+  p.cs = a.rope_cs;
   {
     const int warps = a.n * a.H;
     attn_bwd_prep_tc_kernel<<<(warps + 7) / 8, 256, 0, st>>>((const bf16*)a.dout, (const bf16*)a.out, a.n, a.H,
                                                              a.hd, a.Dsum, a.ld_lse);
   }
-  p.parts = split_parts(a, num_sms, 2 * BM, BN, 4, 0.02);
+  p.parts = split_parts(a, num_sms, BM, DQ_BN, 4, 0.02);
   const int64_t plane = (int64_t)a.n * a.H * a.hd;
-  if (p.parts > 1 && (int64_t)p.parts * plane > a.ws_elems) p.parts = 1;
-  attn_dq2_tc_kernel<NA><<<dim3((a.n + 2 * BM - 1) / (2 * BM), a.H, p.parts), 576, DQ::SMEM, st>>>(mq, mdo, mk, mv,
-                                                                                                  p);
+  while (p.parts > 1 && (int64_t)p.parts * plane > a.ws_elems) --p.parts;
+  attn_dq_tc_kernel<NA><<<dim3((a.n + BM - 1) / BM, a.H, p.parts), 576, DQ::SMEM, st>>>(mq, mdo, mk128, mv128,
+                                                                                        p);
   if (p.parts > 1) {
     const int cols = a.H * a.hd;
     const int64_t quads = plane / 4;
     const int grid = (int)std::min<int64_t>((quads + 255) / 256, (int64_t)num_sms * 8);
-    attn_dq_reduce_kernel<<<grid, 256, 0, st>>>(a.ws, p.parts, a.n, cols, p.dqkv, p.ldg);
+    attn_dq_reduce_kernel<<<grid, 256, 0, st>>>(a.ws, p.parts, a.n, cols, p.dqkv, p.ldg, p.cs, a.hd);
   }
   // dk / dv (after the dq reduction, which may use the same scratch)
   attn_dkv_tc_kernel<NA><<<dim3(a.H, (a.n + BM - 1) / BM), 320, DKV::SMEM, st>>>(mq64, mdo64, mk, mv, p);
   {
     const int64_t quads = (int64_t)2 * a.n * a.Hkv * a.hd / 4;
     const int grid = (int)std::min<int64_t>((quads + 255) / 256, (int64_t)num_sms * 8);
-    attn_dkv_reduce_kernel<<<grid, 256, 0, st>>>(a.ws, a.n, a.H, a.Hkv, a.hd, p.dqkv, p.ldg);
+    attn_dkv_reduce_kernel<<<grid, 256, 0, st>>>(a.ws, a.n, a.H, a.Hkv, a.hd, p.dqkv, p.ldg, p.cs);
   }
   return (int)cudaPeekAtLastError();
 }

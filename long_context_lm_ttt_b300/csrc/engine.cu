@@ -617,15 +617,18 @@ struct Engine : EngineBase {
       attn_fwd_simt<T>(a, st);
     }, [&] { return nk; });
   }
-  void attn_bwd(const AttnArgs& a, cudaStream_t st, int* rc) {
+  // returns true when dq and dk left the kernels already rotated back by
+  // the RoPE table a.rope_cs (tensor-core path)
+  bool attn_bwd(const AttnArgs& a, cudaStream_t st, int* rc) {
     double P, Pl;
     attn_pairs(a.pos0, a.n, &P, &Pl);
     const double hdH = (double)a.H * a.hd;
     const double kv = (double)std::min<int64_t>(a.pos0 + a.n, (int64_t)a.W + a.n - 1) * a.Hkv * a.hd;
     const double bytes = sizeof(T) * (4.0 * a.n * hdH + 2.0 * kv + (double)a.n * qkv_cols) + 8.0 * a.n * a.H;
+    const bool tc = kBF16 && use_tc_attn_bwd && attn_bwd_tc_supported(a);
     prof(P_ATTN_BWD, 6.0 * hdH * P + 4.0 * hdH * Pl, bytes, st, [&] {
       if constexpr (kBF16) {
-        if (use_tc_attn_bwd && attn_bwd_tc_supported(a)) {
+        if (tc) {
           int r = attn_bwd_tc(a, dev_err + 2, st);
           if (r != 0 && *rc == TTT_OK) {
             *rc = TTT_ERR_SHAPE;
@@ -635,7 +638,8 @@ struct Engine : EngineBase {
         }
       }
       attn_bwd_simt<T>(a, st);
-    }, use_tc_attn_bwd && attn_bwd_tc_supported(a) ? 5 : 3);
+    }, tc ? 5 : 3);
+    return tc && a.rope_cs != nullptr;
   }
   // row-wise kernels: bytes moved, no tensor work
   template <typename F>
@@ -867,8 +871,10 @@ struct Engine : EngineBase {
       a.dqkv = dqkv;
       a.ws = attn_ws;
       a.ws_elems = attn_ws_elems;
-      attn_bwd(a, st, rc);
-      row((double)n * (H + Hkv) * hd * 2 * sizeof(T), st, [&] { launch_rope_bwd<T>(dqkv, n, qkv_cols, H + Hkv, hd, cs_cur, st); });
+      a.rope_cs = cs_cur;
+      // the tensor-core backward rotates dq, dk back as it writes them
+      if (!attn_bwd(a, st, rc))
+        row((double)n * (H + Hkv) * hd * 2 * sizeof(T), st, [&] { launch_rope_bwd<T>(dqkv, n, qkv_cols, H + Hkv, hd, cs_cur, st); });
       // dxn = [dq dk dv] Wqkv
       e = epi(EPI_STORE);
       e.out_f32 = 1;

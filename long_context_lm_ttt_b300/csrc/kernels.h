@@ -117,6 +117,10 @@ struct AttnArgs {
   void* dqkv;         // [n, (H+2Hkv)*hd]: dq | dk | dv
   float* ws;          // fp32 scratch of the tensor-core backward
   int64_t ws_elems;   //   (attn_bwd_tc_ws_elems() of the shape)
+  // tensor-core backward: the chunk's RoPE table [n][hd/2] of (cos, sin);
+  // when set, dq and dk leave the kernels already rotated back (the
+  // transpose of the forward rotation), so no separate pass is needed
+  const float2* rope_cs;
 };
 template <typename T> void attn_fwd_simt(const AttnArgs& a, cudaStream_t st);
 // one query position (n == 1, a decode step): key range split into `splits`
