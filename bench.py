@@ -108,7 +108,10 @@ def parse_args():
                     help="tokens per super-chunk of the frozen blocks' bulk pass (0: automatic)")
     ap.add_argument("--mode", choices=["prefill", "decode", "batch"], default="prefill")
     ap.add_argument("--sequences", type=int, default=2,
-                    help="batch: sequences per ttt_prefill_batch call (one context each)")
+                    help="batch: sequences read at once")
+    ap.add_argument("--batch-impl", choices=["grouped", "contexts"], default="grouped",
+                    help="batch: one context holding the sequences (stacked static products, grouped "
+                         "fast-weight GEMMs), or one context per sequence run concurrently (ttt_prefill_batch)")
     ap.add_argument("--context", type=int, default=None,
                     help="decode: tokens prefilled before decoding (default 8 chunks)")
     ap.add_argument("--decode-tokens", type=int, default=None,
@@ -578,9 +581,12 @@ def run_decode(args):
 
 
 def run_batch(args):
-    """--mode batch: tokens/s of ttt_prefill_batch over --sequences
-    contexts (independent sequences, own fast weights), each on its own
-    stream; a step resets every context and prefills all of them."""
+    """--mode batch: tokens/s of B sequences read at once, each with its own
+    fast weights.  grouped: one context with n_seq = B (one ttt_prefill; the
+    products with static weights take every sequence's rows in one launch,
+    the fast MLPs' products are grouped GEMMs).  contexts: B contexts run
+    concurrently by ttt_prefill_batch, one stream each.  A step resets and
+    prefills all B sequences."""
     import torch
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device")
@@ -593,22 +599,40 @@ def run_batch(args):
     s, _ = workload(args)
     T = s.seq_len
     w = inputs.make_weights(s)
-    models = [make_model(TT, s, w, args, T) for _ in range(B)]
+    grouped = args.batch_impl == "grouped"
+    if grouped:
+        models = [TT.TTT(s, w, TT.TTT_BF16, max_tokens=T, bulk_tokens=args.bulk_tokens,
+                         fast_bf16_single=args.fast_bf16_single, n_seq=B)]
+    else:
+        models = [make_model(TT, s, w, args, T) for _ in range(B)]
     del w
     toks = [torch.from_numpy(inputs.make_tokens(s, seed=1 + i)).cuda() for i in range(B)]
+    if grouped:
+        tok_all = torch.stack(toks).contiguous()
+        loss_all = torch.zeros((B, s.n_chunks), dtype=torch.float32, device="cuda")
     losses = [torch.zeros(s.n_chunks, dtype=torch.float32, device="cuda") for _ in range(B)]
     streams = [torch.cuda.Stream() for _ in range(B)]
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
 
     def step():
         for m in models:
             m.reset()
         torch.cuda.synchronize()
+        if grouped:
+            ev0.record()
+            models[0].prefill(tok_all, loss_all)
+            ev1.record()
+            torch.cuda.synchronize()
+            return ev0.elapsed_time(ev1) / 1e3
         t0 = time.perf_counter()
         TT.ttt_prefill_batch([m.ctx for m in models], toks, [T] * B, losses, streams)
         return time.perf_counter() - t0
 
     for _ in range(args.warmup):
         step()
+    if grouped and not torch.isfinite(loss_all).all():
+        raise SystemExit("non-finite chunk losses")
     uuid = str(torch.cuda.get_device_properties(0).uuid)
     clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
     clocks.start()
@@ -616,15 +640,19 @@ def run_batch(args):
     clk = clocks.stop()
     value = B * T * args.steps / sec
     fl = inputs.flops_per_sequence(s)
+    how = ("one context, stacked static products and grouped fast-weight GEMMs" if grouped
+           else "concurrent contexts")
     line = {
-        "metric": f"TTT-E2E prefill tokens/s, {B} sequences per call (concurrent contexts)",
+        "metric": f"TTT-E2E prefill tokens/s, {B} sequences per call ({how})",
         "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(s, args) + f", {B} sequences", "global_batch": B, "seq_len": T},
+        "config": {"workload": workload_name(s, args) + f", {B} sequences", "global_batch": B, "seq_len": T,
+                   "batch_impl": args.batch_impl},
         "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"), "reasons": clk.get("reasons")},
         "model_tflops": fl["total"] * B * args.steps / sec / 1e12,
-        "timing": "host wall clock around each ttt_prefill_batch call (it returns after the work has completed)",
+        "timing": ("CUDA events around each ttt_prefill" if grouped else
+                   "host wall clock around each ttt_prefill_batch call (it returns after the work has completed)"),
     }
     for m in models:
         m.close()

@@ -78,7 +78,13 @@ enum {
  *   re-rounded after every update, at half the tensor work of the fast
  *   MLPs' forward products; an update smaller than half a bf16 step of w
  *   leaves that copy unchanged, so at small lr the forward does not see
- *   the test-time training until updates accumulate past that step).       */
+ *   the test-time training until updates accumulate past that step),
+ *   n_seq (0 or 1: the context holds one sequence; 2 .. 64: it holds n_seq
+ *   independent sequences, each with its own fast weights and key/value
+ *   cache, sharing the static weights.  ttt_prefill then reads all of them
+ *   at once: the products with static weights take every sequence's rows in
+ *   one launch, and the fast MLPs' products run as grouped GEMMs, one
+ *   weight set per sequence.  ttt_decode and ttt_logits need n_seq <= 1.)  */
 typedef struct ttt_config {
   int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, d_ff, vocab;
   int32_t window, chunk, n_ttt_layers, precision;
@@ -87,6 +93,7 @@ typedef struct ttt_config {
   int32_t dual_mlp;
   int32_t bulk_tokens;
   int32_t fast_bf16_single;
+  int32_t n_seq;
 } ttt_config;
 
 /* Initial weights, fp32 values (host or device).  Per-layer fields are
@@ -133,6 +140,9 @@ int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* stream, ttt_ct
  * its bf16 pair, or the single bf16 copy, is re-rounded).  A chunk without targets reports loss 0 and
  * makes no update.
  *   chunk_losses: [ceil(T/b)] fp32, host or device.
+ * With n_seq > 1 the context reads n_seq sequences of the same length T:
+ * tokens is [n_seq][T] and chunk_losses [n_seq][ceil(T/b)], row q for
+ * sequence q; each sequence is trained on exactly as if it were alone.
  * Requires a fresh (or reset) context and 1 <= T <= cfg.max_tokens;
  * otherwise STATE / SHAPE.  Returns after the work has completed on
  * `stream`.  A NaN/Inf chunk loss returns NONFINITE with the first such
@@ -197,7 +207,9 @@ int ttt_decode(ttt_ctx* ctx, const int32_t* tokens, int64_t n_given, int64_t n_s
 int ttt_logits(ttt_ctx* ctx, const int32_t* cont, int32_t n, float* logits, void* stream);
 
 /* Copy the current fp32 value of one fast weight:
- *   block in [0, n_ttt_layers) (0 = layer L-n_ttt_layers),
+ *   block in [0, n_ttt_layers) (0 = layer L-n_ttt_layers); with n_seq > 1,
+ *   block in [0, n_seq * n_ttt_layers): block q * n_ttt_layers + i is
+ *   block i of sequence q,
  *   which 0 = w_gate [d_ff, d], 1 = w_up [d_ff, d], 2 = w_down [d, d_ff],
  *   dst host or device, in the [out, in] layout above. */
 int ttt_get_fast_weights(ttt_ctx* ctx, int32_t block, int32_t which, float* dst, void* stream);

@@ -34,6 +34,21 @@ int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda,
                     const void* B, int64_t ldb, int32_t b_mn, const void* B2, float* C, int64_t ldc,
                     int32_t impl, void* stream);
 
+/* Grouped product, the fast MLPs' products when a context holds several
+ * sequences (ttt_config.n_seq): `groups` products of group_rows rows each,
+ * stacked, each against its own weights:
+ *   C[g R + r, n] = sum_k A[g R + r, k] B_g(n, k)  (+ B2_g(n, k) if B2)
+ *   R = group_rows, B_g = B + g * group_stride (B2_g alike),
+ *   A row-major [groups * R, K] with row pitch lda, B_g(n, k) as B(n, k) of
+ *   ttt_kernel_gemm (b_mn, ldb), C fp32 row-major with pitch ldc.
+ * impl 0: tensor cores, one launch over every group when the tile height
+ * (128, or 256 on CTA pairs) divides R, else one launch per group;
+ * impl 3 / 4: as 0 with 128-row tiles / CTA pairs where R allows;
+ * impl 1: SIMT.  A, B, B2 bf16 (16-byte aligned, pitches multiples of 8). */
+int ttt_kernel_gemm_grouped(int32_t groups, int32_t group_rows, int32_t N, int32_t K, const void* A, int64_t lda,
+                            const void* B, int64_t ldb, int32_t b_mn, int64_t group_stride, const void* B2, float* C,
+                            int64_t ldc, int32_t impl, void* stream);
+
 /* Weight-gradient product with the fused SGD step of the inner loop (the
  * update of one fast weight, one plain gradient step per chunk):
  *   w32[m, n] -= lr * sum_k A(m, k) B(n, k)

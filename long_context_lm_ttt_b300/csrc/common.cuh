@@ -70,6 +70,12 @@ struct Epi {
   void* kring;            // [n_kv][R][hd]
   void* vring;
   const float2* rope_cs;  // [rows][hd/2] (cos, sin) of the rows' positions
+  // rows of several sequences stacked (seg_rows > 0): row m is row
+  // m % seg_rows of sequence m / seg_rows, whose rings start ring_seq
+  // elements after the previous sequence's; positions and the RoPE table
+  // are those of the row within its sequence
+  int seg_rows;
+  int64_t ring_seq;
   // EPI_SWIGLU / EPI_SWIGLU_BWD
   void* stash;            // (g, u) interleaved [rows][2*d_ff]
   int64_t ld_stash;
@@ -108,21 +114,23 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, f
       const int hd = e.hd;
       const int qcols = e.n_q * hd;
       const int kcols = e.n_kv * hd;
+      const int mr = e.seg_rows ? m % e.seg_rows : m;                       // row within its sequence
+      const int64_t rs = e.seg_rows ? (int64_t)(m / e.seg_rows) * e.ring_seq : 0;  // its rings
       if (n < qcols + kcols) {
-        const float2 cs = e.rope_cs[(int64_t)m * (hd >> 1) + ((n % hd) >> 1)];
+        const float2 cs = e.rope_cs[(int64_t)mr * (hd >> 1) + ((n % hd) >> 1)];
         const float a = v0 * cs.x - v1 * cs.y;
         const float b = v1 * cs.x + v0 * cs.y;
         if (n < qcols) {
           store2<T>((T*)e.out + (int64_t)m * e.ldo + n, a, b);
         } else {
           const int c = n - qcols;
-          const int64_t slot = (e.pos0 + m) % e.ring;
-          store2<T>((T*)e.kring + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd), a, b);
+          const int64_t slot = (e.pos0 + mr) % e.ring;
+          store2<T>((T*)e.kring + rs + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd), a, b);
         }
       } else {
         const int c = n - qcols - kcols;
-        const int64_t slot = (e.pos0 + m) % e.ring;
-        store2<T>((T*)e.vring + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd), v0, v1);
+        const int64_t slot = (e.pos0 + mr) % e.ring;
+        store2<T>((T*)e.vring + rs + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd), v0, v1);
       }
     } break;
     case EPI_SWIGLU: {
@@ -227,7 +235,8 @@ __device__ __forceinline__ void epi_src_load(const Epi& e, int m, int col0, uint
     case EPI_QKV: {
       const int hd = e.hd;
       if (col0 >= (e.n_q + e.n_kv) * hd) return;  // values: no rotation
-      p = (const uint8_t*)(e.rope_cs + (int64_t)m * (hd >> 1) + ((col0 % hd) >> 1));
+      const int mr = e.seg_rows ? m % e.seg_rows : m;
+      p = (const uint8_t*)(e.rope_cs + (int64_t)mr * (hd >> 1) + ((col0 % hd) >> 1));
     } break;
     default: return;
   }
@@ -284,8 +293,10 @@ __device__ __forceinline__ void epi_row32(const Epi& e, int m, int col0, const f
       } else {
         const bool is_k = col0 < qcols + kcols;
         const int c = col0 - (is_k ? qcols : qcols + kcols);
-        const int64_t slot = (e.pos0 + m) % e.ring;
-        o = (bf16*)(is_k ? e.kring : e.vring) + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd);
+        const int mr = e.seg_rows ? m % e.seg_rows : m;
+        const int64_t rs = e.seg_rows ? (int64_t)(m / e.seg_rows) * e.ring_seq : 0;
+        const int64_t slot = (e.pos0 + mr) % e.ring;
+        o = (bf16*)(is_k ? e.kring : e.vring) + rs + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd);
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i)

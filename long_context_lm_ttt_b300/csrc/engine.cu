@@ -90,6 +90,10 @@ struct EngineBase {
   ttt_config cfg;
   std::string err;
   int R = 0, R_s = 0, S_bulk = 0, qkv_cols = 0, Vs = 0, num_sms = 148;
+  // sequences the context holds (ttt_config.n_seq): each has its own fast
+  // weights and key/value rings; every activation buffer holds ns blocks
+  // of rows, one per sequence, stacked
+  int ns = 1;
   int64_t pos = 0;
   bool used = false;
   bool use_tc_gemm = false, use_tc_attn = false, use_tc_attn_bwd = false;
@@ -199,6 +203,10 @@ struct Engine : EngineBase {
     float *wgu32_init = nullptr, *wd32_init = nullptr;  // for ttt_reset
     T *kring = nullptr, *vring = nullptr;
     int R = 0;  // ring slots
+    int64_t ring_elems = 0;  // one sequence's ring (keys or values): Hkv * R * hd
+    // fast blocks: one sequence's gate/up and down weights (the stride of
+    // the ns copies every fast-weight array holds)
+    int64_t gu_elems = 0, d_elems = 0;
     // dual_mlp, fast blocks: the static second MLP (after the fast one)
     float* g_mlp2 = nullptr;
     T *wgu2 = nullptr, *wd2 = nullptr;
@@ -330,7 +338,7 @@ struct Engine : EngineBase {
         }
         return a;
       };
-      const int num_m = (b + 127) / 128;
+      const int num_m = (ns * b + 127) / 128;
       const int per = num_sms / gcd(num_sms, num_m);  // n-tiles per whole number of waves
       const int k = std::max(1, 20480 / (per * 256));
       Vs = (int)std::min<int64_t>(V, (int64_t)per * k * 256);
@@ -348,17 +356,21 @@ struct Engine : EngineBase {
     for (int l = 0; l < L; ++l) {
       Layer& y = layers[l];
       const bool fast = l >= L - Lt;
+      const int copies = fast ? ns : 1;  // fast weights: one copy per sequence
+      y.gu_elems = (int64_t)2 * ff * d;
+      y.d_elems = (int64_t)d * ff;
       A_TRY(y.g_attn, d);
       A_TRY(y.g_mlp, d);
       A_TRY(y.wqkv, (size_t)qkv_cols * d);
       A_TRY(y.wo, (size_t)d * Hhd);
-      A_TRY(y.wgu, (size_t)2 * ff * d);
-      A_TRY(y.wd, (size_t)d * ff);
+      A_TRY(y.wgu, (size_t)copies * y.gu_elems);
+      A_TRY(y.wd, (size_t)copies * y.d_elems);
       y.R = fast ? R : R_s;
-      A_TRY(y.kring, (size_t)Hkv * y.R * hd);
-      A_TRY(y.vring, (size_t)Hkv * y.R * hd);
-      CU_TRY(cudaMemsetAsync(y.kring, 0, sizeof(T) * (size_t)Hkv * y.R * hd, st));
-      CU_TRY(cudaMemsetAsync(y.vring, 0, sizeof(T) * (size_t)Hkv * y.R * hd, st));
+      y.ring_elems = (int64_t)Hkv * y.R * hd;
+      A_TRY(y.kring, (size_t)ns * y.ring_elems);
+      A_TRY(y.vring, (size_t)ns * y.ring_elems);
+      CU_TRY(cudaMemsetAsync(y.kring, 0, sizeof(T) * (size_t)ns * y.ring_elems, st));
+      CU_TRY(cudaMemsetAsync(y.vring, 0, sizeof(T) * (size_t)ns * y.ring_elems, st));
       if (!w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo || !w->mlp_norm || !w->w_gate ||
           !w->w_up || !w->w_down) {
         err = "null per-layer weight array";
@@ -376,27 +388,34 @@ struct Engine : EngineBase {
       if ((rc = upload<T>(w->w_down[l], d, ff, 0, y.wd, st))) return rc;
       if (fast) {
         if (kBF16) {
-          A_TRY(y.wgu32, (size_t)2 * ff * d);
-          A_TRY(y.wd32, (size_t)d * ff);
+          A_TRY(y.wgu32, (size_t)ns * y.gu_elems);
+          A_TRY(y.wd32, (size_t)ns * y.d_elems);
           if ((rc = upload<float>(w->w_gate[l], ff, d, 2, y.wgu32, st))) return rc;
           if ((rc = upload<float>(w->w_up[l], ff, d, 3, y.wgu32, st))) return rc;
           if ((rc = upload<float>(w->w_down[l], d, ff, 0, y.wd32, st))) return rc;
           if (!cfg.fast_bf16_single) {
-            A_TRY(y.wgu_lo, (size_t)2 * ff * d);
-            A_TRY(y.wd_lo, (size_t)d * ff);
+            A_TRY(y.wgu_lo, (size_t)ns * y.gu_elems);
+            A_TRY(y.wd_lo, (size_t)ns * y.d_elems);
           }
-          launch_split_bf16(y.wgu32, 2 * (int64_t)ff * d, (bf16*)y.wgu, (bf16*)y.wgu_lo, st);
-          launch_split_bf16(y.wd32, (int64_t)d * ff, (bf16*)y.wd, (bf16*)y.wd_lo, st);
         } else {
           y.wgu32 = (float*)y.wgu;
           y.wd32 = (float*)y.wd;
         }
-        A_TRY(y.wgu32_init, (size_t)2 * ff * d);
-        A_TRY(y.wd32_init, (size_t)d * ff);
-        CU_TRY(cudaMemcpyAsync(y.wgu32_init, y.wgu32, sizeof(float) * 2 * ff * (size_t)d,
-                               cudaMemcpyDeviceToDevice, st));
-        CU_TRY(cudaMemcpyAsync(y.wd32_init, y.wd32, sizeof(float) * (size_t)d * ff,
-                               cudaMemcpyDeviceToDevice, st));
+        A_TRY(y.wgu32_init, (size_t)y.gu_elems);
+        A_TRY(y.wd32_init, (size_t)y.d_elems);
+        CU_TRY(cudaMemcpyAsync(y.wgu32_init, y.wgu32, sizeof(float) * y.gu_elems, cudaMemcpyDeviceToDevice, st));
+        CU_TRY(cudaMemcpyAsync(y.wd32_init, y.wd32, sizeof(float) * y.d_elems, cudaMemcpyDeviceToDevice, st));
+        // every sequence starts from the same initial fast weights
+        for (int q = 1; q < ns; ++q) {
+          CU_TRY(cudaMemcpyAsync(y.wgu32 + q * y.gu_elems, y.wgu32_init, sizeof(float) * y.gu_elems,
+                                 cudaMemcpyDeviceToDevice, st));
+          CU_TRY(cudaMemcpyAsync(y.wd32 + q * y.d_elems, y.wd32_init, sizeof(float) * y.d_elems,
+                                 cudaMemcpyDeviceToDevice, st));
+        }
+        if (kBF16) {
+          launch_split_bf16(y.wgu32, ns * y.gu_elems, (bf16*)y.wgu, (bf16*)y.wgu_lo, st);
+          launch_split_bf16(y.wd32, ns * y.d_elems, (bf16*)y.wd, (bf16*)y.wd_lo, st);
+        }
         if (cfg.dual_mlp) {
           if (!w->mlp2_norm || !w->w_gate2 || !w->w_up2 || !w->w_down2) {
             err = "dual_mlp needs mlp2_norm, w_gate2, w_up2 and w_down2";
@@ -432,14 +451,15 @@ struct Engine : EngineBase {
       s.ld_lse = rows;
       return TTT_OK;
     };
+    const int rows = ns * b;  // chunk rows of all sequences
     if ((rc = alloc_stash(sstash, false, b))) return rc;
     if (L - Lt > 0) {
-      if ((rc = alloc_stash(bstash, false, S_bulk))) return rc;
-      A_TRY(bx[0], (size_t)S_bulk * d);
-      A_TRY(bx[1], (size_t)S_bulk * d);
+      if ((rc = alloc_stash(bstash, false, ns * S_bulk))) return rc;
+      A_TRY(bx[0], (size_t)ns * S_bulk * d);
+      A_TRY(bx[1], (size_t)ns * S_bulk * d);
     }
     for (int k = 0; k < 2; ++k) {
-      A_TRY(x_lo_buf[k], (size_t)S_bulk * d);
+      A_TRY(x_lo_buf[k], (size_t)ns * S_bulk * d);
       A_TRY(cs_bulk_buf[k], (size_t)S_bulk * (hd / 2));
     }
     x_lo = x_lo_buf[0];
@@ -454,65 +474,73 @@ struct Engine : EngineBase {
     }
     fstash.resize(Lt);
     xs.resize(Lt + 1);
-    for (int i = 0; i <= Lt; ++i) A_TRY(xs[i], (size_t)b * d);
+    for (int i = 0; i <= Lt; ++i) A_TRY(xs[i], (size_t)rows * d);
     for (int i = 0; i < Lt; ++i) {
-      if ((rc = alloc_stash(fstash[i], true, b))) return rc;
+      if ((rc = alloc_stash(fstash[i], true, rows))) return rc;
       fstash[i].x = xs[i];
     }
     A_TRY(xlow[0], (size_t)b * d);
     A_TRY(xlow[1], (size_t)b * d);
-    A_TRY(tgt, b);
-    A_TRY(tok_stage, (size_t)std::max<int64_t>(cfg.max_tokens, b));
+    A_TRY(tgt, rows);
+    A_TRY(tok_stage, (size_t)ns * std::max<int64_t>(cfg.max_tokens, b));
     A_TRY(cs, (size_t)b * (hd / 2));
-    A_TRY(hf, (size_t)b * d);
-    A_TRY(rf, b);
-    A_TRY(z_slab, (size_t)b * Vs);
-    A_TRY(p_slab, (size_t)b * Vs);
-    A_TRY(m_run, b);
-    A_TRY(l_run, b);
-    A_TRY(alpha, b);
-    A_TRY(beta, b);
-    A_TRY(ztgt, b);
-    A_TRY(dh_acc, (size_t)b * d);
-    A_TRY(dhf, (size_t)b * d);
-    A_TRY(loss_row, b);
-    A_TRY(dy, (size_t)b * d);
-    A_TRY(dy_t, (size_t)b * d);
-    A_TRY(dgu, (size_t)b * 2 * ff);
-    A_TRY(dhn, (size_t)b * d);
-    A_TRY(dh, (size_t)b * d);
-    A_TRY(dh_t, (size_t)b * d);
-    A_TRY(dO, (size_t)b * Hhd);
-    A_TRY(dqkv, (size_t)b * qkv_cols);
-    A_TRY(dxn, (size_t)b * d);
-    A_TRY(Dsum, (size_t)H * b);
+    A_TRY(hf, (size_t)rows * d);
+    A_TRY(rf, rows);
+    A_TRY(z_slab, (size_t)rows * Vs);
+    A_TRY(p_slab, (size_t)rows * Vs);
+    A_TRY(m_run, rows);
+    A_TRY(l_run, rows);
+    A_TRY(alpha, rows);
+    A_TRY(beta, rows);
+    A_TRY(ztgt, rows);
+    A_TRY(dh_acc, (size_t)rows * d);
+    A_TRY(dhf, (size_t)rows * d);
+    A_TRY(loss_row, rows);
+    A_TRY(dy, (size_t)rows * d);
+    A_TRY(dy_t, (size_t)rows * d);
+    A_TRY(dgu, (size_t)rows * 2 * ff);
+    A_TRY(dhn, (size_t)rows * d);
+    A_TRY(dh, (size_t)rows * d);
+    A_TRY(dh_t, (size_t)rows * d);
+    A_TRY(dO, (size_t)rows * Hhd);
+    A_TRY(dqkv, (size_t)rows * qkv_cols);
+    A_TRY(dxn, (size_t)rows * d);
+    A_TRY(Dsum, (size_t)H * rows);
     if (cfg.dual_mlp && Lt > 0) {
-      A_TRY(hn2, (size_t)b * d);
-      A_TRY(a2, (size_t)b * ff);
-      A_TRY(dy2, (size_t)b * d);
-      A_TRY(dy2_t, (size_t)b * d);
+      A_TRY(hn2, (size_t)rows * d);
+      A_TRY(a2, (size_t)rows * ff);
+      A_TRY(dy2, (size_t)rows * d);
+      A_TRY(dy2_t, (size_t)rows * d);
     }
     if (kBF16 && use_tc_gemm) {
-      gemm_ws_elems = (int64_t)4 * b * std::max<int64_t>(std::max<int64_t>(d, qkv_cols), Hhd);
+      gemm_ws_elems = (int64_t)4 * rows * std::max<int64_t>(std::max<int64_t>(d, qkv_cols), Hhd);
       A_TRY(gemm_ws, (size_t)gemm_ws_elems);
     }
     if (kBF16 && use_tc_attn_bwd) {
       attn_ws_elems = attn_bwd_tc_ws_elems(b, H, hd, num_sms);
       A_TRY(attn_ws, (size_t)attn_ws_elems);
     }
-    A_TRY(losses_stage, (size_t)(cfg.max_tokens + b - 1) / b + 1);
+    A_TRY(losses_stage, (size_t)ns * ((cfg.max_tokens + b - 1) / b + 1));
     A_TRY(dev_err, 4);
     CU_TRY(cudaStreamSynchronize(st));
     return TTT_OK;
   }
 
   // -------------------------------------------------------------------------
+  // groups > 1: a grouped product, rows [q * M / groups, ...) against the
+  // weights B + q * group_stride (one fast-weight set per sequence)
   void gemm(int M, int N, int K, const T* A_, int64_t lda, int a_mn, const T* B_, int64_t ldb,
-            int b_mn, const Epi& e, cudaStream_t st, int* rc, const T* B2 = nullptr) {
+            int b_mn, const Epi& e, cudaStream_t st, int* rc, const T* B2 = nullptr, int groups = 1,
+            int64_t group_stride = 0) {
     // the split-K scratch belongs to the chunk loop; the bulk pass (grid_cap
     // set, other stream) never splits
     GemmArgs<T> g{M, N, K, A_, lda, a_mn, B_, ldb, b_mn, e, B2, grid_cap ? nullptr : gemm_ws,
                   grid_cap ? 0 : gemm_ws_elems, grid_cap};
+    if (groups > 1) {
+      g.groups = groups;
+      g.group_rows = M / groups;
+      g.group_stride = group_stride;
+    }
     int cls = P_GEMM_FWD;
     double out_b = (double)M * N * (e.kind == EPI_STORE && !e.out_f32 ? sizeof(T) : 4);
     switch (e.kind) {
@@ -565,14 +593,17 @@ struct Engine : EngineBase {
     e.kind = kind;
     return e;
   }
-  AttnArgs attn_args(const Stash& S, const Layer& y, int64_t s, int n) {
+  // attention of sequence q (rows [q n, q n + n) of the stash) at positions
+  // s .. s + n - 1, against its own key/value ring
+  AttnArgs attn_args(const Stash& S, const Layer& y, int64_t s, int n, int q = 0) {
+    const int64_t Hhd = (int64_t)cfg.n_heads * cfg.head_dim;
     AttnArgs a;
     memset(&a, 0, sizeof(a));
-    a.q = S.q;
-    a.kring = y.kring;
-    a.vring = y.vring;
-    a.o = S.o;
-    a.lse = S.lse;
+    a.q = S.q + (int64_t)q * n * Hhd;
+    a.kring = y.kring + (int64_t)q * y.ring_elems;
+    a.vring = y.vring + (int64_t)q * y.ring_elems;
+    a.o = S.o + (int64_t)q * n * Hhd;
+    a.lse = S.lse + (int64_t)q * n;
     a.ld_lse = S.ld_lse;
     a.n = n;
     a.H = cfg.n_heads;
@@ -647,15 +678,19 @@ struct Engine : EngineBase {
     prof(P_ROW, 0.0, bytes, st, launch);
   }
 
-  // one decoder block over rows [0, n) at positions s..s+n-1 (RoPE table
-  // cs_), from x_in to x_out, keeping its intermediates in S
+  // one decoder block over the rows of nseq sequences, n rows each, at
+  // positions s..s+n-1 (RoPE table cs_), from x_in to x_out, keeping its
+  // intermediates in S.  Products with static weights take all rows in one
+  // launch; attention runs per sequence; the fast MLP's products are
+  // grouped, one weight set per sequence.
   void block_fwd(int l, Stash& S, const float* x_in, float* x_out, const float2* cs_, int64_t s, int n,
-                 cudaStream_t st, int* rc) {
+                 cudaStream_t st, int* rc, int nseq = 1) {
     const int d = cfg.d_model, H = cfg.n_heads, hd = cfg.head_dim, ff = cfg.d_ff;
     const bool fast = l >= cfg.n_layers - cfg.n_ttt_layers;
     const int64_t Hhd = (int64_t)H * hd;
+    const int rows = nseq * n;
     Layer& y = layers[l];
-    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(x_in, y.g_attn, n, d, cfg.norm_eps, S.xn, S.r1, st); });
+    row((double)rows * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(x_in, y.g_attn, rows, d, cfg.norm_eps, S.xn, S.r1, st); });
     Epi e = epi(EPI_QKV);
     e.out = S.q;
     e.ldo = Hhd;
@@ -667,15 +702,19 @@ struct Engine : EngineBase {
     e.kring = y.kring;
     e.vring = y.vring;
     e.rope_cs = cs_;
-    gemm(n, qkv_cols, d, S.xn, d, 0, y.wqkv, d, 0, e, st, rc);
-    attn_fwd(attn_args(S, y, s, n), st, rc);
+    if (nseq > 1) {
+      e.seg_rows = n;
+      e.ring_seq = y.ring_elems;
+    }
+    gemm(rows, qkv_cols, d, S.xn, d, 0, y.wqkv, d, 0, e, st, rc);
+    for (int q = 0; q < nseq; ++q) attn_fwd(attn_args(S, y, s, n, q), st, rc);
     e = epi(EPI_RESID);
     e.out = S.h;
     e.ldo = d;
     e.resid = x_in;
     e.ldr = d;
-    gemm(n, d, (int)Hhd, S.o, Hhd, 0, y.wo, Hhd, 0, e, st, rc);
-    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(S.h, y.g_mlp, n, d, cfg.norm_eps, S.hn, S.r2, st); });
+    gemm(rows, d, (int)Hhd, S.o, Hhd, 0, y.wo, Hhd, 0, e, st, rc);
+    row((double)rows * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(S.h, y.g_mlp, rows, d, cfg.norm_eps, S.hn, S.r2, st); });
     e = epi(EPI_SWIGLU);
     e.out = S.a;
     e.ldo = ff;
@@ -684,29 +723,30 @@ struct Engine : EngineBase {
     // fast weights in bf16 mode: the pair hi + lo of the master, so updates
     // below one bf16 ulp still reach the forward, or with fast_bf16_single
     // the bf16 copy alone (the low halves are null then)
-    gemm(n, 2 * ff, d, S.hn, d, 0, y.wgu, d, 0, e, st, rc, y.wgu_lo);
+    const int grp = fast ? nseq : 1;
+    gemm(rows, 2 * ff, d, S.hn, d, 0, y.wgu, d, 0, e, st, rc, y.wgu_lo, grp, y.gu_elems);
     const bool dual = fast && cfg.dual_mlp;
     e = epi(EPI_RESID);
     e.out = dual ? S.h2 : x_out;
     e.ldo = d;
     e.resid = S.h;
     e.ldr = d;
-    gemm(n, d, ff, S.a, ff, 0, y.wd, ff, 0, e, st, rc, y.wd_lo);
+    gemm(rows, d, ff, S.a, ff, 0, y.wd, ff, 0, e, st, rc, y.wd_lo, grp, y.d_elems);
     if (dual) {
       // the static second MLP: x_out = h2 + Wd2 (silu(Wg2 n(h2)) * Wu2 n(h2))
-      row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(S.h2, y.g_mlp2, n, d, cfg.norm_eps, hn2, S.r3, st); });
+      row((double)rows * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(S.h2, y.g_mlp2, rows, d, cfg.norm_eps, hn2, S.r3, st); });
       e = epi(EPI_SWIGLU);
       e.out = a2;
       e.ldo = ff;
       e.stash = S.gu2;
       e.ld_stash = 2 * (int64_t)ff;
-      gemm(n, 2 * ff, d, hn2, d, 0, y.wgu2, d, 0, e, st, rc);
+      gemm(rows, 2 * ff, d, hn2, d, 0, y.wgu2, d, 0, e, st, rc);
       e = epi(EPI_RESID);
       e.out = x_out;
       e.ldo = d;
       e.resid = S.h2;
       e.ldr = d;
-      gemm(n, d, ff, a2, ff, 0, y.wd2, ff, 0, e, st, rc);
+      gemm(rows, d, ff, a2, ff, 0, y.wd2, ff, 0, e, st, rc);
     }
   }
 
@@ -716,17 +756,23 @@ struct Engine : EngineBase {
   // (buffers x_lo_buf[buf], cs_bulk_buf[buf]).  Its GEMMs launch one CTA per
   // tile instead of one persistent CTA per SM, so that SMs free up often
   // for the chunk loop running concurrently on the other stream.
-  void static_fwd(const int32_t* tok, int64_t s0, int n, int buf, cudaStream_t st, int* rc) {
+  //
+  // With ns sequences the super-chunk's rows are those of every sequence,
+  // n rows each, stacked; tok holds the sequences' tokens tok_ld apart.
+  void static_fwd(const int32_t* tok, int64_t tok_ld, int64_t s0, int n, int buf, cudaStream_t st, int* rc) {
     const int d = cfg.d_model, hd = cfg.head_dim, lo = cfg.n_layers - cfg.n_ttt_layers;
     float2* cs_ = cs_bulk_buf[buf];
     float* xl = x_lo_buf[buf];
     row((double)n * hd * 4, st, [&] { launch_rope_table(s0, n, hd, cfg.rope_theta, cs_, st); });
     float* x = lo == 0 ? xl : bx[0];
-    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_embed<T>(tok, n, E, d, x, cfg.vocab, dev_err + 1, st); });
+    for (int q = 0; q < ns; ++q)
+      row((double)n * d * (4 + sizeof(T)), st, [&] {
+        launch_embed<T>(tok + q * tok_ld + s0, n, E, d, x + (int64_t)q * n * d, cfg.vocab, dev_err + 1, st);
+      });
     grid_cap = INT_MAX;
     for (int l = 0; l < lo; ++l) {
       float* x_out = l + 1 == lo ? xl : bx[(l + 1) & 1];
-      block_fwd(l, bstash, x, x_out, cs_, s0, n, st, rc);
+      block_fwd(l, bstash, x, x_out, cs_, s0, n, st, rc, ns);
       x = x_out;
     }
     grid_cap = 0;
@@ -735,17 +781,19 @@ struct Engine : EngineBase {
   // fast blocks of positions [s, s+n) from x_in (the output of the static
   // blocks), then the final norm: leaves the normed hidden state in hf and
   // its statistics in rf
-  void fast_fwd(const float* x_in, const float2* cs_, int64_t s, int n, cudaStream_t st, int* rc) {
+  // (nseq sequences: x_in holds their rows stacked, n each)
+  void fast_fwd(const float* x_in, const float2* cs_, int64_t s, int n, cudaStream_t st, int* rc, int nseq = 1) {
     const int L = cfg.n_layers, d = cfg.d_model, Lt = cfg.n_ttt_layers, lo = L - Lt;
+    const int rows = nseq * n;
     cs_cur = cs_;
     if (Lt > 0) fstash[0].x = const_cast<float*>(x_in);
     const float* x = x_in;
     for (int l = lo; l < L; ++l) {
       float* x_out = xs[l + 1 - lo];
-      block_fwd(l, fstash[l - lo], x, x_out, cs_, s, n, st, rc);
+      block_fwd(l, fstash[l - lo], x, x_out, cs_, s, n, st, rc, nseq);
       x = x_out;
     }
-    row((double)n * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(x, g_final, n, d, cfg.norm_eps, hf, rf, st); });
+    row((double)rows * d * (4 + sizeof(T)), st, [&] { launch_rmsnorm_fwd<T>(x, g_final, rows, d, cfg.norm_eps, hf, rf, st); });
   }
 
   // every block for a span of at most b positions (ttt_logits)
@@ -765,10 +813,16 @@ struct Engine : EngineBase {
   // streamed lm_head + cross-entropy: loss of chunk c into losses[c] and the
   // gradient w.r.t. the final normed hidden state into dhf (fp32)
   // need_grad = false (no fast blocks): the loss only, no d hidden
+  // nseq sequences: tok and losses of sequence q start q * tok_ld and
+  // q * loss_ld elements in; the hidden rows are stacked, n per sequence
   void cross_entropy(const int32_t* tok, int64_t n_tok, int64_t s, int n, int n_tgt, float* losses, int c,
-                     cudaStream_t st, int* rc, bool need_grad = true) {
+                     cudaStream_t st, int* rc, bool need_grad = true, int nseq = 1, int64_t tok_ld = 0,
+                     int64_t loss_ld = 0) {
     const int d = cfg.d_model, V = cfg.vocab;
-    row((double)n * 8, st, [&] { launch_targets(tok, n_tok, s, n, tgt, V, dev_err + 1, st); });
+    const int n1 = n;  // rows of one sequence
+    for (int q = 0; q < nseq; ++q)
+      row((double)n1 * 8, st, [&] { launch_targets(tok + q * tok_ld, n_tok, s, n1, tgt + (int64_t)q * n1, V, dev_err + 1, st); });
+    n = nseq * n1;  // every row from here on
     for (int v0 = 0; v0 < V; v0 += Vs) {
       const int nv = std::min(Vs, V - v0);
       const int first = v0 == 0;
@@ -793,18 +847,22 @@ struct Engine : EngineBase {
     row((double)n * d * (8 + sizeof(T)), st, [&] {
       launch_ce_finalize<T>(n, m_run, l_run, ztgt, tgt, inv, need_grad ? dh_acc : nullptr, Wlm, d, dhf, loss_row, st);
     });
-    row((double)n * 4, st, [&] { launch_loss_reduce(loss_row, n, inv, losses, c, dev_err, st); });
+    for (int q = 0; q < nseq; ++q)
+      row((double)n1 * 4, st, [&] { launch_loss_reduce(loss_row + (int64_t)q * n1, n1, inv, losses + q * loss_ld, c, dev_err, st); });
   }
 
   // backward of the chunk loss into the fast MLPs, with the SGD step fused
   // into the weight-gradient GEMMs.  Every read of a fast weight (da, dhn)
   // happens before that weight's update in stream order.
-  void backward(int64_t s, int n, cudaStream_t st, int* rc) {
+  // nseq sequences: rows stacked, n per sequence; the fast MLPs' input
+  // gradients are grouped products and each sequence takes its own SGD step
+  void backward(int64_t s, int n, cudaStream_t st, int* rc, int nseq = 1) {
     const int L = cfg.n_layers, d = cfg.d_model, H = cfg.n_heads, Hkv = cfg.n_kv_heads,
               hd = cfg.head_dim, ff = cfg.d_ff, Lt = cfg.n_ttt_layers;
     const int lo = L - Lt;
     const int64_t Hhd = (int64_t)H * hd;
-    row((double)n * d * (12 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(xs[Lt], g_final, rf, dhf, nullptr, n, d, dy, dy_t, st); });
+    const int rows = nseq * n;
+    row((double)rows * d * (12 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(xs[Lt], g_final, rf, dhf, nullptr, rows, d, dy, dy_t, st); });
     for (int l = L - 1; l >= lo; --l) {
       Stash& S = fstash[l - lo];
       Layer& y = layers[l];
@@ -818,13 +876,13 @@ struct Engine : EngineBase {
         e2.ldo = 2 * (int64_t)ff;
         e2.stash = S.gu2;
         e2.ld_stash = 2 * (int64_t)ff;
-        gemm(n, ff, d, dy_t, d, 0, y.wd2, ff, 1, e2, st, rc);
+        gemm(rows, ff, d, dy_t, d, 0, y.wd2, ff, 1, e2, st, rc);
         e2 = epi(EPI_STORE);
         e2.out_f32 = 1;
         e2.out = dhn;
         e2.ldo = d;
-        gemm(n, d, 2 * ff, dgu, 2 * (int64_t)ff, 0, y.wgu2, d, 1, e2, st, rc);
-        row((double)n * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.h2, y.g_mlp2, S.r3, dhn, dy, n, d, dy2, dy2_t, st); });
+        gemm(rows, d, 2 * ff, dgu, 2 * (int64_t)ff, 0, y.wgu2, d, 1, e2, st, rc);
+        row((double)rows * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.h2, y.g_mlp2, S.r3, dhn, dy, rows, d, dy2, dy2_t, st); });
         gy = dy2;
         gy_t = dy2_t;
       }
@@ -834,54 +892,62 @@ struct Engine : EngineBase {
       e.ldo = 2 * (int64_t)ff;
       e.stash = S.gu;
       e.ld_stash = 2 * (int64_t)ff;
-      gemm(n, ff, d, gy_t, d, 0, y.wd, ff, 1, e, st, rc);
+      gemm(rows, ff, d, gy_t, d, 0, y.wd, ff, 1, e, st, rc, nullptr, nseq, y.d_elems);
       if (l > lo) {
         // dhn = [dg du] [Wg; Wu]
         e = epi(EPI_STORE);
         e.out_f32 = 1;
         e.out = dhn;
         e.ldo = d;
-        gemm(n, d, 2 * ff, dgu, 2 * (int64_t)ff, 0, y.wgu, d, 1, e, st, rc);
+        gemm(rows, d, 2 * ff, dgu, 2 * (int64_t)ff, 0, y.wgu, d, 1, e, st, rc, nullptr, nseq, y.gu_elems);
       }
-      // Wd -= lr dy^T a ;  [Wg;Wu] -= lr [dg du]^T hn
-      e = epi(EPI_SGD);
-      e.w32 = y.wd32;
-      e.w16 = kBF16 ? (void*)y.wd : nullptr;
-      e.w16lo = y.wd_lo;
-      e.ldo = ff;
-      e.lr = cfg.lr;
-      gemm(d, ff, n, gy_t, d, 1, S.a, ff, 1, e, st, rc);
-      e.w32 = y.wgu32;
-      e.w16 = kBF16 ? (void*)y.wgu : nullptr;
-      e.w16lo = y.wgu_lo;
-      e.ldo = d;
-      gemm(2 * ff, d, n, dgu, 2 * (int64_t)ff, 1, S.hn, d, 1, e, st, rc);
+      // per sequence: Wd -= lr dy^T a ;  [Wg;Wu] -= lr [dg du]^T hn
+      for (int q = 0; q < nseq; ++q) {
+        const int64_t r0 = (int64_t)q * n;
+        e = epi(EPI_SGD);
+        e.w32 = y.wd32 + q * y.d_elems;
+        e.w16 = kBF16 ? (void*)(y.wd + q * y.d_elems) : nullptr;
+        e.w16lo = y.wd_lo ? y.wd_lo + q * y.d_elems : nullptr;
+        e.ldo = ff;
+        e.lr = cfg.lr;
+        gemm(d, ff, n, gy_t + r0 * d, d, 1, S.a + r0 * ff, ff, 1, e, st, rc);
+        e.w32 = y.wgu32 + q * y.gu_elems;
+        e.w16 = kBF16 ? (void*)(y.wgu + q * y.gu_elems) : nullptr;
+        e.w16lo = y.wgu_lo ? y.wgu_lo + q * y.gu_elems : nullptr;
+        e.ldo = d;
+        gemm(2 * ff, d, n, dgu + r0 * 2 * ff, 2 * (int64_t)ff, 1, S.hn + r0 * d, d, 1, e, st, rc);
+      }
       if (l == lo) break;
       // through the MLP norm and the residual
-      row((double)n * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.h, y.g_mlp, S.r2, dhn, gy, n, d, dh, dh_t, st); });
+      row((double)rows * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.h, y.g_mlp, S.r2, dhn, gy, rows, d, dh, dh_t, st); });
       // dO = dh Wo
       e = epi(EPI_STORE);
       e.out = dO;
       e.ldo = Hhd;
-      gemm(n, (int)Hhd, d, dh_t, d, 0, y.wo, Hhd, 1, e, st, rc);
-      AttnArgs a = attn_args(S, y, s, n);
-      a.dout = dO;
-      a.out = S.o;
-      a.Dsum = Dsum;
-      a.dqkv = dqkv;
-      a.ws = attn_ws;
-      a.ws_elems = attn_ws_elems;
-      a.rope_cs = cs_cur;
-      // the tensor-core backward rotates dq, dk back as it writes them
-      if (!attn_bwd(a, st, rc))
-        row((double)n * (H + Hkv) * hd * 2 * sizeof(T), st, [&] { launch_rope_bwd<T>(dqkv, n, qkv_cols, H + Hkv, hd, cs_cur, st); });
+      gemm(rows, (int)Hhd, d, dh_t, d, 0, y.wo, Hhd, 1, e, st, rc);
+      for (int q = 0; q < nseq; ++q) {
+        const int64_t r0 = (int64_t)q * n;
+        AttnArgs a = attn_args(S, y, s, n, q);
+        a.dout = dO + r0 * Hhd;
+        a.out = S.o + r0 * Hhd;
+        a.Dsum = Dsum + r0;
+        a.dqkv = dqkv + r0 * qkv_cols;
+        a.ws = attn_ws;
+        a.ws_elems = attn_ws_elems;
+        a.rope_cs = cs_cur;
+        // the tensor-core backward rotates dq, dk back as it writes them
+        if (!attn_bwd(a, st, rc))
+          row((double)n * (H + Hkv) * hd * 2 * sizeof(T), st, [&] {
+            launch_rope_bwd<T>(dqkv + r0 * qkv_cols, n, qkv_cols, H + Hkv, hd, cs_cur, st);
+          });
+      }
       // dxn = [dq dk dv] Wqkv
       e = epi(EPI_STORE);
       e.out_f32 = 1;
       e.out = dxn;
       e.ldo = d;
-      gemm(n, d, qkv_cols, dqkv, qkv_cols, 0, y.wqkv, d, 1, e, st, rc);
-      row((double)n * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.x, y.g_attn, S.r1, dxn, dh, n, d, dy, dy_t, st); });
+      gemm(rows, d, qkv_cols, dqkv, qkv_cols, 0, y.wqkv, d, 1, e, st, rc);
+      row((double)rows * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.x, y.g_attn, S.r1, dxn, dh, rows, d, dy, dy_t, st); });
     }
   }
 
@@ -928,7 +994,7 @@ struct Engine : EngineBase {
     const int nC = (int)((n_tok + b - 1) / b);
     const int32_t* tok_d = tok;
     if (!is_device_ptr(tok)) {
-      CU_TRY(cudaMemcpyAsync(tok_stage, tok, sizeof(int32_t) * n_tok, cudaMemcpyHostToDevice, st));
+      CU_TRY(cudaMemcpyAsync(tok_stage, tok, sizeof(int32_t) * ns * n_tok, cudaMemcpyHostToDevice, st));
       tok_d = tok_stage;
     }
     const bool host_out = !is_device_ptr(losses);
@@ -952,7 +1018,7 @@ struct Engine : EngineBase {
       const int64_t s0 = (int64_t)k * S_bulk;
       const int sn = (int)std::min<int64_t>(S_bulk, n_tok - s0);
       if (k >= 2) cudaStreamWaitEvent(s_bulk, ev_b[k & 1], 0);
-      static_fwd(tok_d + s0, s0, sn, k & 1, s_bulk, &rc);
+      static_fwd(tok_d, n_tok, s0, sn, k & 1, s_bulk, &rc);
       cudaEventRecord(ev_a[k & 1], s_bulk);
     };
     bulk(0);
@@ -967,14 +1033,23 @@ struct Engine : EngineBase {
         const int c = (int)(s / b);
         const int n = (int)std::min<int64_t>(b, n_tok - s);
         const int n_tgt = (int)std::min<int64_t>(n, n_tok - 1 - s);
-        fast_fwd(x_lo + (s - s0) * d, cs_bulk + (s - s0) * (hd / 2), s, n, s_loop, &rc);
+        const float* xin = x_lo + (s - s0) * d;
+        if (ns > 1) {
+          // the chunk's rows of every sequence (sn rows apart in the
+          // super-chunk's output), stacked for the chunk loop
+          CU_TRY(cudaMemcpy2DAsync(xs[0], sizeof(float) * (size_t)n * d, xin, sizeof(float) * (size_t)sn * d,
+                                   sizeof(float) * (size_t)n * d, ns, cudaMemcpyDeviceToDevice, s_loop));
+          xin = xs[0];
+        }
+        fast_fwd(xin, cs_bulk + (s - s0) * (hd / 2), s, n, s_loop, &rc, ns);
         if (n_tgt <= 0) {
-          CU_TRY(cudaMemsetAsync(loss_d + c, 0, sizeof(float), s_loop));
+          for (int q = 0; q < ns; ++q)
+            CU_TRY(cudaMemsetAsync(loss_d + (int64_t)q * nC + c, 0, sizeof(float), s_loop));
           continue;
         }
         // without fast blocks the chunk loop only scores the chunk
-        cross_entropy(tok_d, n_tok, s, n, n_tgt, loss_d, c, s_loop, &rc, cfg.n_ttt_layers > 0);
-        if (cfg.n_ttt_layers > 0) backward(s, n, s_loop, &rc);
+        cross_entropy(tok_d, n_tok, s, n, n_tgt, loss_d, c, s_loop, &rc, cfg.n_ttt_layers > 0, ns, n_tok, nC);
+        if (cfg.n_ttt_layers > 0) backward(s, n, s_loop, &rc, ns);
         CU_TRY(cudaPeekAtLastError());
       }
       CU_TRY(cudaEventRecord(ev_b[k & 1], s_loop));
@@ -989,7 +1064,7 @@ struct Engine : EngineBase {
     }
     pos = n_tok;
     if (host_out)
-      CU_TRY(cudaMemcpyAsync(losses, loss_d, sizeof(float) * nC, cudaMemcpyDeviceToHost, st));
+      CU_TRY(cudaMemcpyAsync(losses, loss_d, sizeof(float) * ns * nC, cudaMemcpyDeviceToHost, st));
     return finish(st, "ttt_prefill");
   }
 
@@ -1004,6 +1079,10 @@ struct Engine : EngineBase {
     if (!tokens || !tokens_out || !losses) {
       err = "null tokens, tokens_out or chunk_losses";
       return TTT_ERR_INVALID;
+    }
+    if (ns > 1) {
+      err = "ttt_decode takes a context of one sequence (n_seq <= 1)";
+      return TTT_ERR_STATE;
     }
     if (n_steps < 1 || n_given < 1 || n_given > n_steps + 1) {
       err = "need 1 <= n_given <= n_steps + 1";
@@ -1095,6 +1174,10 @@ struct Engine : EngineBase {
       err = "null continuation or logits";
       return TTT_ERR_INVALID;
     }
+    if (ns > 1) {
+      err = "ttt_logits takes a context of one sequence (n_seq <= 1)";
+      return TTT_ERR_STATE;
+    }
     const int32_t* c_d = cont;
     if (!is_device_ptr(cont)) {
       CU_TRY(cudaMemcpyAsync(tok_stage, cont, sizeof(int32_t) * n, cudaMemcpyHostToDevice, st));
@@ -1122,15 +1205,18 @@ struct Engine : EngineBase {
 
   int get_fast(int block, int which, float* dst, cudaStream_t st) override {
     const int d = cfg.d_model, ff = cfg.d_ff;
-    if (block < 0 || block >= cfg.n_ttt_layers || which < 0 || which > 2 || !dst) {
+    // with several sequences, block counts over them: sequence q's block i
+    // is q * n_ttt_layers + i
+    if (block < 0 || block >= ns * cfg.n_ttt_layers || which < 0 || which > 2 || !dst) {
       err = "bad block/which/dst";
       return TTT_ERR_INVALID;
     }
-    Layer& y = layers[cfg.n_layers - cfg.n_ttt_layers + block];
+    const int q = block / cfg.n_ttt_layers, i = block % cfg.n_ttt_layers;
+    Layer& y = layers[cfg.n_layers - cfg.n_ttt_layers + i];
     if (which == 2) {
-      CU_TRY(cudaMemcpyAsync(dst, y.wd32, sizeof(float) * (size_t)d * ff, cudaMemcpyDefault, st));
+      CU_TRY(cudaMemcpyAsync(dst, y.wd32 + q * y.d_elems, sizeof(float) * (size_t)d * ff, cudaMemcpyDefault, st));
     } else {
-      CU_TRY(cudaMemcpy2DAsync(dst, sizeof(float) * d, y.wgu32 + (which == 1 ? d : 0),
+      CU_TRY(cudaMemcpy2DAsync(dst, sizeof(float) * d, y.wgu32 + q * y.gu_elems + (which == 1 ? d : 0),
                                sizeof(float) * 2 * d, sizeof(float) * d, ff, cudaMemcpyDefault, st));
     }
     CU_TRY(cudaStreamSynchronize(st));
@@ -1138,20 +1224,22 @@ struct Engine : EngineBase {
   }
 
   int reset(cudaStream_t st) override {
-    const int L = cfg.n_layers, d = cfg.d_model, ff = cfg.d_ff, Hkv = cfg.n_kv_heads, hd = cfg.head_dim;
+    const int L = cfg.n_layers, d = cfg.d_model, ff = cfg.d_ff;
     for (int l = 0; l < L; ++l) {
       Layer& y = layers[l];
-      CU_TRY(cudaMemsetAsync(y.kring, 0, sizeof(T) * (size_t)Hkv * y.R * hd, st));
-      CU_TRY(cudaMemsetAsync(y.vring, 0, sizeof(T) * (size_t)Hkv * y.R * hd, st));
+      CU_TRY(cudaMemsetAsync(y.kring, 0, sizeof(T) * (size_t)ns * y.ring_elems, st));
+      CU_TRY(cudaMemsetAsync(y.vring, 0, sizeof(T) * (size_t)ns * y.ring_elems, st));
       if (l >= L - cfg.n_ttt_layers) {
-        CU_TRY(cudaMemcpyAsync(y.wgu32, y.wgu32_init, sizeof(float) * 2 * ff * (size_t)d,
-                               cudaMemcpyDeviceToDevice, st));
-        CU_TRY(cudaMemcpyAsync(y.wd32, y.wd32_init, sizeof(float) * (size_t)d * ff,
-                               cudaMemcpyDeviceToDevice, st));
+        for (int q = 0; q < ns; ++q) {
+          CU_TRY(cudaMemcpyAsync(y.wgu32 + q * y.gu_elems, y.wgu32_init, sizeof(float) * 2 * ff * (size_t)d,
+                                 cudaMemcpyDeviceToDevice, st));
+          CU_TRY(cudaMemcpyAsync(y.wd32 + q * y.d_elems, y.wd32_init, sizeof(float) * (size_t)d * ff,
+                                 cudaMemcpyDeviceToDevice, st));
+        }
         if (kBF16) {
-          const double nb = 2.0 * ff * d;
-          row(nb * 8, st, [&] { launch_split_bf16(y.wgu32, 2 * (int64_t)ff * d, (bf16*)y.wgu, (bf16*)y.wgu_lo, st); });
-          row(nb * 4, st, [&] { launch_split_bf16(y.wd32, (int64_t)d * ff, (bf16*)y.wd, (bf16*)y.wd_lo, st); });
+          const double nb = 2.0 * ff * d * ns;
+          row(nb * 8, st, [&] { launch_split_bf16(y.wgu32, ns * y.gu_elems, (bf16*)y.wgu, (bf16*)y.wgu_lo, st); });
+          row(nb * 4, st, [&] { launch_split_bf16(y.wd32, ns * y.d_elems, (bf16*)y.wd, (bf16*)y.wd_lo, st); });
         }
       }
     }
@@ -1201,6 +1289,10 @@ static int validate(const ttt_config* c, std::string& msg) {
     msg = "fast_bf16_single must be 0 or 1";
     return TTT_ERR_INVALID;
   }
+  if (c->n_seq < 0 || c->n_seq > 64) {
+    msg = "n_seq must be in [0, 64] (0 or 1: one sequence)";
+    return TTT_ERR_INVALID;
+  }
   if (c->n_heads % c->n_kv_heads) {
     msg = "n_heads must be a multiple of n_kv_heads";
     return TTT_ERR_SHAPE;
@@ -1247,6 +1339,7 @@ extern "C" int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* str
     return TTT_ERR_OOM;
   }
   eng->cfg = *cfg;
+  eng->ns = cfg->n_seq > 1 ? cfg->n_seq : 1;
   eng->prof_clear();
   const int need = cfg->window + cfg->chunk - 1;
   eng->R = ((need + 127) / 128) * 128;

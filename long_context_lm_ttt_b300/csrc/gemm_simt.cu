@@ -1,6 +1,8 @@
 // gemm_simt.cu — plain fp32-FMA tiled GEMM with the shared epilogues.
 // It serves the fp32 check mode (no tensor cores, no tf32) and is the
 // reference the tensor-core GEMM is unit-tested against on the GPU.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -78,6 +80,22 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(int M, int N, int K, con
 template <typename T>
 void gemm_simt(const GemmArgs<T>& g, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0) return;
+  if (g.groups > 1) {
+    // grouped product: one launch per group, on its rows and its B
+    for (int gi = 0; gi < g.groups; ++gi) {
+      GemmArgs<T> s = g;
+      const int64_t r0 = (int64_t)gi * g.group_rows;
+      s.M = (int)std::min<int64_t>(g.group_rows, g.M - r0);
+      if (s.M <= 0) break;
+      s.A = g.a_mn ? g.A + r0 : g.A + r0 * g.lda;
+      s.B = g.B + gi * g.group_stride;
+      s.B2 = g.B2 ? g.B2 + gi * g.group_stride : nullptr;
+      s.e = epi_rows_from<T>(g.e, r0);
+      s.groups = 1;
+      gemm_simt<T>(s, st);
+    }
+    return;
+  }
   dim3 grid((g.N + SBN - 1) / SBN, (g.M + SBM - 1) / SBM);
   gemm_simt_kernel<T><<<grid, 256, 0, st>>>(g.M, g.N, g.K, g.A, g.lda, g.a_mn, g.B, g.ldb, g.b_mn, g.e, g.B2);
 }

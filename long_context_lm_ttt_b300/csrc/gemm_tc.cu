@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(192, 1)
                    const __grid_constant__ CUtensorMap mapB2, const __grid_constant__ CUtensorMap mapS,
                    const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapH,
                    const __grid_constant__ CUtensorMap mapL, int dual, int M, int N, int K, Epi e, int* err,
-                   int splits, float* ws) {
+                   int splits, float* ws, int grp_rows) {
   using C = Cfg<BN, SRC, PAIR>;
   // an MN-major B tile arrives in 64-column boxes
   static_assert(!B_MN || C::BNL % 64 == 0, "MN-major B needs whole 64-column boxes");
@@ -261,7 +261,17 @@ __global__ void __launch_bounds__(192, 1)
             } else {
               tc::tma_load_2d_pair(a_s, &mapA, k0, m0, fbc);
             }
-            if (B_MN) {
+            if (grp_rows) {
+              // grouped: B of the tile's group through the 3-D map
+              const int gi = mt_ * C::TM / grp_rows;
+              if (B_MN) {
+#pragma unroll
+                for (int j = 0; j < C::BNL / 64; ++j)
+                  tc::tma_load_3d_pair(b_s + 8192 * j, mb, nb0 + 64 * j, k0, gi, fbc);
+              } else {
+                tc::tma_load_3d_pair(b_s, mb, k0, nb0, gi, fbc);
+              }
+            } else if (B_MN) {
 #pragma unroll
               for (int j = 0; j < C::BNL / 64; ++j) tc::tma_load_2d_pair(b_s + 8192 * j, mb, nb0 + 64 * j, k0, fbc);
             } else {
@@ -275,7 +285,15 @@ __global__ void __launch_bounds__(192, 1)
             } else {
               tc::tma_load_2d(a_s, &mapA, k0, m0, fb);
             }
-            if (B_MN) {
+            if (grp_rows) {
+              const int gi = mt_ * C::TM / grp_rows;
+              if (B_MN) {
+#pragma unroll
+                for (int j = 0; j < BN / 64; ++j) tc::tma_load_3d(b_s + 8192 * j, mb, n0 + 64 * j, k0, gi, fb);
+              } else {
+                tc::tma_load_3d(b_s, mb, k0, n0, gi, fb);
+              }
+            } else if (B_MN) {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j) tc::tma_load_2d(b_s + 8192 * j, mb, n0 + 64 * j, k0, fb);
             } else {
@@ -715,6 +733,20 @@ int make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, 
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
+// bf16 3-D map: `groups` matrices of [outer, inner] (pitch ld_elems), each
+// group_stride elements after the previous; box {64, box_outer, 1}
+int make_map3(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld_elems, uint64_t groups,
+              uint64_t group_stride, uint32_t box_outer) {
+  cuuint64_t dims[3] = {inner, outer, groups};
+  cuuint64_t strides[2] = {ld_elems * 2, group_stride * 2};
+  cuuint32_t box[3] = {64, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+}
+
 // fp32 [rows, cols] tile map with 128-byte swizzle: box {32 columns, box_rows}
 int make_map_f32(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld_elems,
                  uint32_t box_rows) {
@@ -736,12 +768,17 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
   if (A_MN) rc = make_map(&ma, g.A, g.M, g.K, g.lda, 64, 64);
   else rc = make_map(&ma, g.A, g.K, g.M, g.lda, 64, BM);
   if (rc) return rc;
-  if (B_MN) rc = make_map(&mb, g.B, g.N, g.K, g.ldb, 64, 64);
-  else rc = make_map(&mb, g.B, g.K, g.N, g.ldb, 64, C::BNL);
+  const bool grouped = g.groups > 1;
+  auto map_b = [&](CUtensorMap* m, const bf16* ptr) {
+    if (grouped)
+      return B_MN ? make_map3(m, ptr, g.N, g.K, g.ldb, g.groups, g.group_stride, 64)
+                  : make_map3(m, ptr, g.K, g.N, g.ldb, g.groups, g.group_stride, C::BNL);
+    return B_MN ? make_map(m, ptr, g.N, g.K, g.ldb, 64, 64) : make_map(m, ptr, g.K, g.N, g.ldb, 64, C::BNL);
+  };
+  rc = map_b(&mb, g.B);
   if (rc) return rc;
   if (g.B2) {
-    if (B_MN) rc = make_map(&mb2, g.B2, g.N, g.K, g.ldb, 64, 64);
-    else rc = make_map(&mb2, g.B2, g.K, g.N, g.ldb, 64, C::BNL);
+    rc = map_b(&mb2, g.B2);
     if (rc) return rc;
   } else {
     mb2 = mb;
@@ -795,12 +832,12 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
     const int pairs = std::max(1, std::min(cap / 2, resident.load()));
     cfg.gridDim = dim3(2 * (nunits < pairs ? nunits : pairs));
     const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, ma, mb, mb2, ms, mw, mh, ml, g.B2 ? 1 : 0, g.M, g.N, g.K,
-                                              g.e, err, splits, g.ws);
+                                              g.e, err, splits, g.ws, grouped ? g.group_rows : 0);
     if (le != cudaSuccess) return (int)le;
   } else {
     const int grid = nunits < cap ? nunits : cap;
     kern<<<grid, 192, C::SMEM, st>>>(ma, mb, mb2, ms, mw, mh, ml, g.B2 ? 1 : 0, g.M, g.N, g.K, g.e, err, splits,
-                                     g.ws);
+                                     g.ws, grouped ? g.group_rows : 0);
   }
   if (splits > 1) {
     const int64_t items = (int64_t)g.M * ((g.N + 31) / 32);
@@ -915,6 +952,35 @@ static bool epi_vec_ok(const Epi& e) {
 int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st, int* kernels) {
   GemmArgs<bf16> g = g_in;
   if (kernels) *kernels = 1;
+  if (g.groups > 1) {
+    // one launch for every group when whole tiles fall in one group (the
+    // tile height divides group_rows; pairs need 256); otherwise one
+    // launch per group
+    const bool rows_ok = g.group_rows > 0 && (int64_t)g.groups * g.group_rows == g.M && g.e.kind != EPI_SGD;
+    if (rows_ok && g.group_rows % BM == 0) {
+      if (g.group_rows % (2 * BM) != 0) g.pair = 0;
+    } else {
+      int total = 0;
+      for (int gi = 0; gi < g.groups; ++gi) {
+        GemmArgs<bf16> s = g;
+        const int64_t r0 = (int64_t)gi * g.group_rows;
+        s.M = std::min<int64_t>(g.group_rows, g.M - r0);
+        if (s.M <= 0) break;
+        s.A = g.a_mn ? g.A + r0 : g.A + r0 * g.lda;
+        s.B = g.B + gi * g.group_stride;
+        s.B2 = g.B2 ? g.B2 + gi * g.group_stride : nullptr;
+        s.e = epi_rows_from<bf16>(g.e, r0);
+        s.groups = 1;
+        s.group_rows = 0;
+        int nk = 1;
+        const int rc = gemm_tc(s, num_sms, err, st, &nk);
+        if (rc) return rc;
+        total += nk;
+      }
+      if (kernels) *kernels = total;
+      return 0;
+    }
+  }
   g.e.vec = epi_vec_ok(g.e) ? 1 : 0;
   if (g.M <= 0 || g.N <= 0) return 0;
   // one row, K-major operands, 16-byte aligned rows: stream B once
@@ -934,7 +1000,7 @@ int gemm_tc(const GemmArgs<bf16>& g_in, int num_sms, int* err, cudaStream_t st, 
   // the SGD epilogue (weight-gradient GEMM, both operands MN-major, a bf16
   // copy wanted, with or without its low half) updates the fp32 masters in
   // a TMA-fed shared-memory tile and stores the outputs by TMA
-  if (g.e.kind == EPI_SGD && g.e.vec && g.a_mn && g.b_mn && !g.B2 && (g.N % 32) == 0 && g.e.w16 &&
+  if (g.e.kind == EPI_SGD && g.groups == 1 && g.e.vec && g.a_mn && g.b_mn && !g.B2 && (g.N % 32) == 0 && g.e.w16 &&
       (g.e.ldo % 8) == 0 && a16(g.e.w16) && (!g.e.w16lo || a16(g.e.w16lo))) {
     if (kernels) *kernels = 1;
     const bool pair = g.pair >= 0 ? g.pair == 1 : g.M > BM;

@@ -1,4 +1,5 @@
 // kernel_api.cu — the kernel-level entry points of ttt_kernels.h.
+#include <climits>
 #include <cstring>
 
 #include "../../include/ttt.h"
@@ -64,6 +65,42 @@ extern "C" int ttt_kernel_gemm(int32_t M, int32_t N, int32_t K, const void* A, i
     return TTT_ERR_INVALID;
   }
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
+}
+
+extern "C" int ttt_kernel_gemm_grouped(int32_t groups, int32_t group_rows, int32_t N, int32_t K, const void* A,
+                                       int64_t lda, const void* B, int64_t ldb, int32_t b_mn, int64_t group_stride,
+                                       const void* B2, float* C, int64_t ldc, int32_t impl, void* stream) {
+  if (!A || !B || !C || groups < 1 || group_rows < 1 || N < 0 || K < 1 || (N & 1) || (ldc & 1) ||
+      group_stride < 0)
+    return TTT_ERR_INVALID;
+  if (impl != 0 && impl != 1 && impl != 3 && impl != 4) return TTT_ERR_INVALID;
+  if (int r = ensure_err()) return r;
+  cudaStream_t st = (cudaStream_t)stream;
+  ttt::Epi e;
+  memset(&e, 0, sizeof(e));
+  e.kind = ttt::EPI_STORE;
+  e.out_f32 = 1;
+  e.out = C;
+  e.ldo = ldc;
+  const int64_t M = (int64_t)groups * group_rows;
+  if (M > INT32_MAX) return TTT_ERR_SHAPE;
+  ttt::GemmArgs<ttt::bf16> g{(int)M, N, K, (const ttt::bf16*)A, lda, 0, (const ttt::bf16*)B, ldb, b_mn, e,
+                             (const ttt::bf16*)B2, nullptr, 0};
+  g.groups = groups;
+  g.group_rows = group_rows;
+  g.group_stride = group_stride;
+  if (impl == 1) {
+    ttt::gemm_simt<ttt::bf16>(g, st);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
+  }
+  g.pair = impl == 3 ? 0 : (impl == 4 ? 1 : -1);
+  if (ttt::gemm_tc_init()) return TTT_ERR_CUDA;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int rc = ttt::gemm_tc(g, sms, g_err, st);
+  if (rc == (int)cudaErrorNotSupported || rc == (int)cudaErrorInvalidValue) return TTT_ERR_SHAPE;
+  return rc ? TTT_ERR_CUDA : 0;
 }
 
 extern "C" int ttt_kernel_gemm_sgd(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn,

@@ -46,7 +46,41 @@ struct GemmArgs {
   // tensor-core GEMM tiles: -1 = chosen by the planner, 0 = 128-row tiles on
   // one CTA, 1 = 256-row tiles on a CTA pair (cta_group::2)
   int pair = -1;
+  // grouped product (groups > 1): rows [g * group_rows, (g + 1) * group_rows)
+  // of A and of the output use the B (and B2) of group g, which starts
+  // g * group_stride elements after B (B2); one weight set per sequence
+  int groups = 1;
+  int group_rows = 0;
+  int64_t group_stride = 0;
 };
+
+// The epilogue of rows [r0, ...) of a product seen as a product of its own:
+// every row-indexed pointer of e moved down r0 rows (T: the element type of
+// bf16/fp32 activations).  Covers the epilogues grouped products use.
+template <typename T>
+inline Epi epi_rows_from(const Epi& e, int64_t r0) {
+  Epi o = e;
+  switch (e.kind) {
+    case EPI_STORE:
+      o.out = e.out_f32 ? (void*)((float*)e.out + r0 * e.ldo) : (void*)((T*)e.out + r0 * e.ldo);
+      break;
+    case EPI_RESID:
+      o.out = (float*)e.out + r0 * e.ldo;
+      o.resid = e.resid + r0 * e.ldr;
+      break;
+    case EPI_SWIGLU:
+      o.out = (T*)e.out + r0 * e.ldo;
+      if (e.stash) o.stash = (T*)e.stash + r0 * e.ld_stash;
+      break;
+    case EPI_SWIGLU_BWD:
+      o.out = (T*)e.out + r0 * e.ldo;
+      o.stash = (T*)e.stash + r0 * e.ld_stash;
+      break;
+    default:
+      break;
+  }
+  return o;
+}
 
 // SIMT fp32-accumulate GEMM (check mode; reference for the tensor-core one)
 template <typename T> void gemm_simt(const GemmArgs<T>& g, cudaStream_t st);

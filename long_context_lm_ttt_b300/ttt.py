@@ -42,7 +42,8 @@ class ttt_config(ctypes.Structure):
                 ("vocab", c_int32), ("window", c_int32), ("chunk", c_int32),
                 ("n_ttt_layers", c_int32), ("precision", c_int32), ("lr", c_float),
                 ("rope_theta", c_float), ("norm_eps", c_float), ("max_tokens", c_int64),
-                ("dual_mlp", c_int32), ("bulk_tokens", c_int32), ("fast_bf16_single", c_int32)]
+                ("dual_mlp", c_int32), ("bulk_tokens", c_int32), ("fast_bf16_single", c_int32),
+                ("n_seq", c_int32)]
 
 
 class ttt_weights(ctypes.Structure):
@@ -98,6 +99,9 @@ def load(path: str = LIB_PATH):
     lib.ttt_kernel_gemm_sgd.argtypes = [i32, i32, i32, c_void_p, c_int64, i32, c_void_p, c_int64, i32, c_void_p,
                                         c_void_p, c_void_p, c_int64, c_float, i32, c_void_p]
     lib.ttt_kernel_gemm_sgd.restype = c_int32
+    lib.ttt_kernel_gemm_grouped.argtypes = [i32, i32, i32, i32, c_void_p, c_int64, c_void_p, c_int64, i32, c_int64,
+                                            c_void_p, c_void_p, c_int64, i32, c_void_p]
+    lib.ttt_kernel_gemm_grouped.restype = c_int32
     lib.ttt_kernel_attn_fwd.argtypes = [i32, i32, i32, i32, i32, i32, i32, c_int64, c_void_p, c_void_p,
                                         c_void_p, c_void_p, c_void_p, i32, c_void_p]
     lib.ttt_kernel_attn_fwd.restype = c_int32
@@ -154,14 +158,15 @@ def _check(rc: int, ctx=None):
 
 
 def make_config(shape, precision: int = TTT_BF16, max_tokens: Optional[int] = None,
-                lr: Optional[float] = None, bulk_tokens: int = 0, fast_bf16_single: bool = False) -> ttt_config:
+                lr: Optional[float] = None, bulk_tokens: int = 0, fast_bf16_single: bool = False,
+                n_seq: int = 1) -> ttt_config:
     """ttt_config from any object with the ModelShape field names."""
     return ttt_config(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads, shape.head_dim,
                       shape.d_ff, shape.vocab, shape.window, shape.chunk, shape.n_ttt_layers, precision,
                       shape.lr if lr is None else lr, shape.rope_theta, shape.norm_eps,
                       max_tokens if max_tokens is not None else shape.seq_len,
                       1 if getattr(shape, "dual_mlp", False) else 0, int(bulk_tokens),
-                      1 if fast_bf16_single else 0)
+                      1 if fast_bf16_single else 0, int(n_seq))
 
 
 def make_weights(w: dict):
@@ -279,6 +284,15 @@ def ttt_kernel_gemm_sgd(M, N, K, A, lda, a_mn, B, ldb, b_mn, w32, w16, w16lo, ld
     return rc
 
 
+def ttt_kernel_gemm_grouped(groups, group_rows, N, K, A, lda, B, ldb, b_mn, group_stride, B2, C, ldc, impl,
+                            stream=None) -> int:
+    rc = load().ttt_kernel_gemm_grouped(int(groups), int(group_rows), int(N), int(K), _ptr(A), int(lda), _ptr(B),
+                                        int(ldb), int(b_mn), int(group_stride), _ptr(B2), _ptr(C), int(ldc), int(impl),
+                                        _stream(stream))
+    _check(rc)
+    return rc
+
+
 def ttt_kernel_error() -> int:
     return int(load().ttt_kernel_error())
 
@@ -291,9 +305,10 @@ class TTT:
 
     def __init__(self, shape, weights: dict, precision: int = TTT_BF16,
                  max_tokens: Optional[int] = None, lr: Optional[float] = None, stream=None,
-                 bulk_tokens: int = 0, fast_bf16_single: bool = False):
+                 bulk_tokens: int = 0, fast_bf16_single: bool = False, n_seq: int = 1):
         self.shape = shape
-        self.cfg = make_config(shape, precision, max_tokens, lr, bulk_tokens, fast_bf16_single)
+        self.n_seq = max(1, int(n_seq))
+        self.cfg = make_config(shape, precision, max_tokens, lr, bulk_tokens, fast_bf16_single, n_seq)
         ws, keep = make_weights(weights)
         self.ctx = ttt_create(self.cfg, ws, stream)
         del keep
@@ -303,14 +318,16 @@ class TTT:
 
     def prefill(self, tokens, chunk_losses=None, stream=None):
         """Run the inner loop; returns the chunk losses (numpy for host
-        tokens, else the given / a new float32 CUDA tensor)."""
-        T = len(tokens)
+        tokens, else the given / a new float32 CUDA tensor).  With n_seq > 1,
+        tokens is [n_seq, T] and the losses [n_seq, ceil(T / b)]."""
+        T = tokens.shape[-1] if self.n_seq > 1 else len(tokens)
+        shape = (self.n_seq, self.n_chunks(T)) if self.n_seq > 1 else (self.n_chunks(T),)
         if chunk_losses is None:
             if isinstance(tokens, np.ndarray):
-                chunk_losses = np.zeros(self.n_chunks(T), np.float32)
+                chunk_losses = np.zeros(shape, np.float32)
             else:
                 import torch
-                chunk_losses = torch.zeros(self.n_chunks(T), dtype=torch.float32, device=tokens.device)
+                chunk_losses = torch.zeros(shape, dtype=torch.float32, device=tokens.device)
         ttt_prefill(self.ctx, tokens, T, chunk_losses, stream)
         return chunk_losses
 
@@ -342,12 +359,12 @@ class TTT:
         ttt_logits(self.ctx, cont, n, out, stream)
         return out
 
-    def fast_weights(self, block: int) -> dict:
+    def fast_weights(self, block: int, seq: int = 0) -> dict:
         d, ff = self.cfg.d_model, self.cfg.d_ff
         out = {}
         for which, name, shp in ((0, "w_gate", (ff, d)), (1, "w_up", (ff, d)), (2, "w_down", (d, ff))):
             a = np.zeros(shp, np.float32)
-            ttt_get_fast_weights(self.ctx, block, which, a)
+            ttt_get_fast_weights(self.ctx, seq * self.cfg.n_ttt_layers + block, which, a)
             out[name] = a
         return out
 

@@ -39,14 +39,14 @@ def test_exports_every_declared_call(lib):
 
 
 def test_struct_layout():
-    # 11 int32, 3 float, int64 max_tokens, int32 dual_mlp, bulk_tokens and
-    # fast_bf16_single (+ 4 bytes of tail padding to the int64 alignment), as the
-    # C declaration lays them out
-    assert ctypes.sizeof(T.ttt_config) == 11 * 4 + 3 * 4 + 8 + 3 * 4 + 4
+    # 11 int32, 3 float, int64 max_tokens, int32 dual_mlp, bulk_tokens,
+    # fast_bf16_single and n_seq, as the C declaration lays them out
+    assert ctypes.sizeof(T.ttt_config) == 11 * 4 + 3 * 4 + 8 + 4 * 4
     assert T.ttt_config.max_tokens.offset == 56
     assert T.ttt_config.dual_mlp.offset == 64
     assert T.ttt_config.bulk_tokens.offset == 68
     assert T.ttt_config.fast_bf16_single.offset == 72
+    assert T.ttt_config.n_seq.offset == 76
     assert ctypes.sizeof(T.ttt_weights) == 16 * ctypes.sizeof(ctypes.c_void_p)
 
 
@@ -65,6 +65,8 @@ def _cfg(**kw):
     (dict(dual_mlp=2), T.TTT_ERR_INVALID),
     (dict(bulk_tokens=-1), T.TTT_ERR_INVALID),
     (dict(fast_bf16_single=2), T.TTT_ERR_INVALID),
+    (dict(n_seq=-1), T.TTT_ERR_INVALID),
+    (dict(n_seq=65), T.TTT_ERR_INVALID),
     (dict(n_kv_heads=3), T.TTT_ERR_SHAPE),
     (dict(head_dim=31), T.TTT_ERR_SHAPE),
     (dict(lr=float("nan")), T.TTT_ERR_NONFINITE),

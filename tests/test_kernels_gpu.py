@@ -155,3 +155,37 @@ def test_gemm_sgd_without_low_half(impl):
     assert np.abs(got - ref).max() <= 1e-5 * upd + 2e-9, np.abs(got - ref).max()
     assert torch.equal(hi.cpu(), w32.cpu().to(torch.bfloat16))
 
+
+
+@pytest.mark.parametrize("groups,R,N,K", [(3, 1024, 3072, 512), (2, 128, 640, 256), (3, 96, 384, 128)])
+@pytest.mark.parametrize("b_mn", [0, 1])
+@pytest.mark.parametrize("dual", [False, True])
+@pytest.mark.parametrize("impl", [0, 3, 4, 1])
+def test_gemm_grouped(groups, R, N, K, b_mn, dual, impl):
+    """Grouped product: group g's rows against its own B (and B2).  R =
+    1024 runs every group in one launch on CTA pairs, R = 128 in one launch
+    on single CTAs (a pair tile would straddle two groups), R = 96 one
+    launch per group."""
+    torch, T = _env()
+    if impl == 1 and groups * R * N * K > 2 ** 30:
+        pytest.skip("SIMT reference only on the small shapes")
+    rng = np.random.default_rng(groups * 1000 + R + N + K + 7 * b_mn + 3 * dual + impl)
+    a, a_st = _operand(rng, groups * R, K, 0)
+    bs = [_operand(rng, N, K, b_mn) for _ in range(groups)]
+    b2s = [_operand(rng, N, K, b_mn) for _ in range(groups)] if dual else None
+    stride = N * K
+    cu = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).cuda()
+    B = cu(np.stack([st for _, st in bs]))
+    B2 = cu(np.stack([st for _, st in b2s])) if dual else None
+    C = torch.full((groups * R, N), float("nan"), dtype=torch.float32, device="cuda")
+    ldb = N if b_mn else K
+    T.ttt_kernel_gemm_grouped(groups, R, N, K, cu(a_st), K, B, ldb, b_mn, stride, B2, C, N, impl)
+    torch.cuda.synchronize()
+    assert T.ttt_kernel_error() == 0
+    got = C.cpu().numpy().astype(np.float64)
+    for g in range(groups):
+        ref = a[g * R:(g + 1) * R] @ bs[g][0].T
+        if dual:
+            ref = ref + a[g * R:(g + 1) * R] @ b2s[g][0].T
+        err = np.abs(got[g * R:(g + 1) * R] - ref).max() / np.abs(ref).max()
+        assert err < 1e-5, (g, err)
