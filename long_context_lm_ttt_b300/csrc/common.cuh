@@ -54,7 +54,23 @@ enum EpiKind : int {
   EPI_SGD = 5,        // w32 -= lr * acc; w16 = rn(w32); w16lo = rn(w32 - w16)
   EPI_CE_Z = 6,       // z slab (fp32) + pick the target logit
   EPI_CE_ACC = 7,     // acc_out = acc_out * alpha[m] + acc * beta[m]
+  EPI_ARGMAX = 8,     // out (uint64 per row) = max of argmax_key(acc, n): the greedy pick
 };
+
+// The greedy pick as one 64-bit key, so that an atomic max finds it: the
+// logit's bits made order-preserving as an unsigned word (high half; -0
+// taken as +0) and the complement of its column (low half), so the largest
+// key is the largest logit at its smallest column.  NaN never wins (key 0);
+// argmax_col() turns a key back into the column (0 when nothing won).
+__device__ __forceinline__ unsigned long long argmax_key(float v, int n) {
+  if (v != v) return 0ull;
+  const uint32_t b = v == 0.f ? 0u : __float_as_uint(v);
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (uint32_t)~(uint32_t)n;
+}
+__device__ __forceinline__ int argmax_col(unsigned long long key) {
+  return key == 0ull ? 0 : (int)~(uint32_t)(key & 0xffffffffull);
+}
 
 struct Epi {
   int kind;
@@ -66,6 +82,8 @@ struct Epi {
   // EPI_QKV
   int n_q, n_kv, hd;      // heads of q, heads of k/v, head dim
   int64_t pos0;           // absolute position of row 0
+  const int64_t* pos_dev; // non-null: row 0's position is read here instead
+                          // (decode steps replayed from one captured graph)
   int ring;               // ring slots R
   void* kring;            // [n_kv][R][hd]
   void* vring;
@@ -124,12 +142,12 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, f
           store2<T>((T*)e.out + (int64_t)m * e.ldo + n, a, b);
         } else {
           const int c = n - qcols;
-          const int64_t slot = (e.pos0 + mr) % e.ring;
+          const int64_t slot = ((e.pos_dev ? *e.pos_dev : e.pos0) + mr) % e.ring;
           store2<T>((T*)e.kring + rs + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd), a, b);
         }
       } else {
         const int c = n - qcols - kcols;
-        const int64_t slot = (e.pos0 + mr) % e.ring;
+        const int64_t slot = ((e.pos_dev ? *e.pos_dev : e.pos0) + mr) % e.ring;
         store2<T>((T*)e.vring + rs + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd), v0, v1);
       }
     } break;
@@ -171,6 +189,10 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, f
       const int64_t t = (int64_t)e.tgt[m] - e.col0;
       if (t == n) e.ztgt[m] = v0;
       else if (t == n + 1) e.ztgt[m] = v1;
+    } break;
+    case EPI_ARGMAX: {
+      const unsigned long long k0 = argmax_key(v0, n), k1 = argmax_key(v1, n + 1);
+      atomicMax((unsigned long long*)e.out + m, k0 > k1 ? k0 : k1);
     } break;
     case EPI_CE_ACC: {
       float* o = (float*)e.out + (int64_t)m * e.ldo + n;
@@ -295,7 +317,7 @@ __device__ __forceinline__ void epi_row32(const Epi& e, int m, int col0, const f
         const int c = col0 - (is_k ? qcols : qcols + kcols);
         const int mr = e.seg_rows ? m % e.seg_rows : m;
         const int64_t rs = e.seg_rows ? (int64_t)(m / e.seg_rows) * e.ring_seq : 0;
-        const int64_t slot = (e.pos0 + mr) % e.ring;
+        const int64_t slot = ((e.pos_dev ? *e.pos_dev : e.pos0) + mr) % e.ring;
         o = (bf16*)(is_k ? e.kring : e.vring) + rs + ((int64_t)(c / hd) * e.ring + slot) * hd + (c % hd);
       }
 #pragma unroll

@@ -193,6 +193,9 @@ struct Engine : EngineBase {
       if (e) cudaEventDestroy(e);
     if (sa) cudaStreamDestroy(sa);
     if (sb) cudaStreamDestroy(sb);
+    for (cudaGraphExec_t& g : dec_graph)
+      if (g) cudaGraphExecDestroy(g);
+    if (cap_st) cudaStreamDestroy(cap_st);
   }
 
   struct Layer {
@@ -267,14 +270,22 @@ struct Engine : EngineBase {
   float* losses_stage = nullptr;
   float* logits_stage = nullptr;
   // decode (allocated on first use): the fast blocks' input rows of the
-  // current chunk, its tokens (b + 1: the last is the next input), one row
-  // of logits and the tokens of one call
+  // current chunk, its tokens (b + 1: the last is the next input) and the
+  // tokens of one call
   float* xdec = nullptr;
   int32_t* dtok = nullptr;
-  float* dec_z = nullptr;
   int32_t* dec_out = nullptr;
   float* dec_part = nullptr;  // one-query attention slices (set while decoding)
   float* dec_buf = nullptr;
+  // a decode step's position, row and tokens live in device memory
+  // (dstate) so that one captured graph per step kind (given next token,
+  // greedy) replays every step; dpos is set while such a step is issued
+  DecodeState* dstate = nullptr;
+  unsigned long long* dec_pick = nullptr;  // greedy-pick key (argmax_key)
+  const int64_t* dpos = nullptr;
+  cudaGraphExec_t dec_graph[2] = {nullptr, nullptr};
+  cudaStream_t cap_st = nullptr;
+  bool dec_graph_off = false;  // capture failed once: issue steps directly
   int gemm_cls = -1;          // profile class of the next GEMMs, if set
   int* dev_err = nullptr;  // [0] first non-finite chunk, [1] bad token, [2] kernel check
   float* stage32 = nullptr;
@@ -612,6 +623,7 @@ struct Engine : EngineBase {
     a.W = cfg.window;
     a.R = y.R;
     a.pos0 = s;
+    a.pos_dev = dpos;
     return a;
   }
   void attn_fwd(const AttnArgs& a, cudaStream_t st, int* rc) {
@@ -624,7 +636,10 @@ struct Engine : EngineBase {
     prof(a.n > cfg.chunk ? P_ATTN_FWD_BULK : P_ATTN_FWD, 4.0 * hdH * P, bytes, st, [&] {
       // a decode step: one query, the window split over the whole GPU
       if (dec_part && a.n == 1 && attn_decode_supported(a)) {
-        attn_decode<T>(a, attn_decode_splits(a, num_sms), dec_part, st);
+        if (attn_decode<T>(a, attn_decode_splits(a, num_sms), dec_part, dev_err + 2, st) && *rc == TTT_OK) {
+          *rc = TTT_ERR_CUDA;
+          err = "one-query attention: kernel attribute not set";
+        }
         return;
       }
       if constexpr (kBF16) {
@@ -698,6 +713,7 @@ struct Engine : EngineBase {
     e.n_kv = cfg.n_kv_heads;
     e.hd = hd;
     e.pos0 = s;
+    e.pos_dev = dpos;
     e.ring = y.R;
     e.kring = y.kring;
     e.vring = y.vring;
@@ -799,7 +815,7 @@ struct Engine : EngineBase {
   // every block for a span of at most b positions (ttt_logits)
   void forward_all(const int32_t* tok, int64_t s, int n, cudaStream_t st, int* rc) {
     const int d = cfg.d_model, hd = cfg.head_dim, lo = cfg.n_layers - cfg.n_ttt_layers;
-    row((double)n * hd * 4, st, [&] { launch_rope_table(s, n, hd, cfg.rope_theta, cs, st); });
+    row((double)n * hd * 4, st, [&] { launch_rope_table(s, n, hd, cfg.rope_theta, cs, st, dpos); });
     float* x = xlow[0];
     row((double)n * d * (4 + sizeof(T)), st, [&] { launch_embed<T>(tok, n, E, d, x, cfg.vocab, dev_err + 1, st); });
     for (int l = 0; l < lo; ++l) {
@@ -1068,14 +1084,66 @@ struct Engine : EngineBase {
     return finish(st, "ttt_prefill");
   }
 
+  // One decode step at the position held in dstate: every block over the
+  // step's input token with the current weights (the one-query attention
+  // splitting the window over the GPU), then, for kind 1, the greedy pick;
+  // the tail kernel stores the first fast block's input row, the tokens and
+  // the next input, and advances the state.  Nothing issued here depends on
+  // the host's copy of the position, so the same launches serve every step.
+  void decode_step(int kind, cudaStream_t st, int* rc) {
+    const int b = cfg.chunk, d = cfg.d_model, V = cfg.vocab;
+    const int lo = cfg.n_layers - cfg.n_ttt_layers;
+    dec_part = dec_buf;
+    dpos = &dstate->pos;
+    forward_all(&dstate->tok, pos, 1, st, rc);
+    dpos = nullptr;
+    dec_part = nullptr;
+    if (kind == 1) {
+      // lm_head with the greedy pick fused: each block folds its columns'
+      // keys and takes one atomic max on dec_pick (no logits are stored)
+      Epi e = epi(EPI_ARGMAX);
+      e.out = dec_pick;
+      gemm_cls = P_GEMM_LMHEAD;
+      gemm(1, V, d, hf, d, 0, Wlm, d, 0, e, st, rc);
+      gemm_cls = -1;
+    }
+    row((double)d * 8, st, [&] { launch_decode_tail(dstate, xlow[lo & 1], xdec, d, dtok, dec_pick, b, st); });
+  }
+  // Record the launches of one decode step of the given kind into a graph
+  // (on a stream of the engine's own: capture needs one that is not the
+  // legacy default stream).  The step has run once directly before, so
+  // every lazy set-up (kernel attributes, scratch) is done.  A failed
+  // capture leaves the steps issued directly.
+  void capture_decode_step(int kind) {
+    if (!cap_st && cudaStreamCreateWithFlags(&cap_st, cudaStreamNonBlocking) != cudaSuccess) {
+      cudaGetLastError();
+      dec_graph_off = true;
+      return;
+    }
+    cudaGraph_t g = nullptr;
+    int rc = TTT_OK;
+    if (cudaStreamBeginCapture(cap_st, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+      decode_step(kind, cap_st, &rc);
+      if (cudaStreamEndCapture(cap_st, &g) != cudaSuccess) g = nullptr;
+    }
+    if (!g || rc != TTT_OK || cudaGraphInstantiate(&dec_graph[kind], g, 0) != cudaSuccess) {
+      dec_graph[kind] = nullptr;
+      dec_graph_off = true;
+    }
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+  }
+
   // Decode-time test-time training: one token per step through every block
   // with the current weights, then the greedy next token; when a chunk of b
   // positions is complete, the same test-time step as the prefill's chunk
   // loop (fast blocks recomputed over the chunk, loss, backward, SGD).
+  // The first step of each kind is issued directly and then captured; later
+  // ones replay the graph (one launch from the host instead of one per
+  // kernel).  The chunk's test-time step is issued directly.
   int decode(const int32_t* tokens, int64_t n_given, int64_t n_steps, int32_t* tokens_out, float* losses,
              cudaStream_t st) override {
     const int b = cfg.chunk, d = cfg.d_model, hd = cfg.head_dim, V = cfg.vocab;
-    const int lo = cfg.n_layers - cfg.n_ttt_layers;
     if (!tokens || !tokens_out || !losses) {
       err = "null tokens, tokens_out or chunk_losses";
       return TTT_ERR_INVALID;
@@ -1099,9 +1167,13 @@ struct Engine : EngineBase {
     if (!xdec) {
       A_TRY(xdec, (size_t)b * d);
       A_TRY(dtok, (size_t)b + 1);
-      A_TRY(dec_z, (size_t)V);
       A_TRY(dec_out, (size_t)cfg.max_tokens + 1);
-      A_TRY(dec_buf, (size_t)cfg.n_heads * kMaxDecodeSplits * (hd + 2));
+      const int64_t part_elems = attn_decode_scratch_elems(cfg.n_heads, hd);
+      A_TRY(dec_buf, (size_t)part_elems);
+      // the one-query attention's per-KV-head counters start at zero
+      CU_TRY(cudaMemsetAsync(dec_buf, 0, sizeof(float) * part_elems, st));
+      A_TRY(dec_pick, 1);
+      CU_TRY(mem.alloc((void**)&dstate, sizeof(DecodeState)));
     }
     const int32_t* given = tokens;
     if (!is_device_ptr(tokens)) {
@@ -1114,34 +1186,21 @@ struct Engine : EngineBase {
     int rc = clear_err(st);
     if (rc) return rc;
     used = true;
+    row(0.0, st, [&] { launch_decode_begin(dstate, pos, dec_fill, given, (int)n_given, tok_d, dec_pick, st); });
     int done = 0;  // chunks completed by this call
     for (int64_t i = 0; i < n_steps && rc == TTT_OK; ++i) {
-      const int64_t p = pos;
-      const int r = dec_fill;
-      if (i < n_given) CU_TRY(cudaMemcpyAsync(dtok + r, given + i, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
-      dec_part = dec_buf;
-      forward_all(dtok + r, p, 1, st, &rc);
-      dec_part = nullptr;
-      // input row of the first fast block (the embedding if there is none)
-      CU_TRY(cudaMemcpyAsync(xdec + (int64_t)r * d, xlow[lo & 1], sizeof(float) * d, cudaMemcpyDeviceToDevice, st));
-      if (i + 1 < n_given) {
-        CU_TRY(cudaMemcpyAsync(dtok + r + 1, given + i + 1, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+      const int kind = i + 1 < n_given ? 0 : 1;  // 0: next input given, 1: greedy
+      if (dec_graph[kind] && !prof_on) {
+        CU_TRY(cudaGraphLaunch(dec_graph[kind], st));
       } else {
-        Epi e = epi(EPI_STORE);
-        e.out_f32 = 1;
-        e.out = dec_z;
-        e.ldo = V;
-        gemm_cls = P_GEMM_LMHEAD;
-        gemm(1, V, d, hf, d, 0, Wlm, d, 0, e, st, &rc);
-        gemm_cls = -1;
-        row((double)V * 4, st, [&] { launch_argmax(dec_z, V, dtok + r + 1, st); });
+        decode_step(kind, st, &rc);
+        if (rc == TTT_OK && !prof_on && !dec_graph_off) capture_decode_step(kind);
       }
-      CU_TRY(cudaMemcpyAsync(tok_d + i, dtok + r, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
-      pos = p + 1;
-      dec_fill = r + 1;
+      pos += 1;
+      dec_fill += 1;
       if (dec_fill == b) {
         // chunk [s, s + b) complete; its targets are dtok[1..b]
-        const int64_t s = p + 1 - b;
+        const int64_t s = pos - b;
         row((double)b * hd * 4, st, [&] { launch_rope_table(s, b, hd, cfg.rope_theta, cs, st); });
         fast_fwd(xdec, cs, s, b, st, &rc);
         cross_entropy(dtok, b + 1, 0, b, b, loss_d, done, st, &rc, cfg.n_ttt_layers > 0);

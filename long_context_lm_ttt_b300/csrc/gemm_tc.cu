@@ -680,23 +680,39 @@ __global__ void __launch_bounds__(256) gemv_row_kernel(const bf16* __restrict__ 
     a0 += __shfl_xor_sync(0xffffffffu, a0, o);
     a1 += __shfl_xor_sync(0xffffffffu, a1, o);
   }
-  if (KS == 1) {
-    if (lane == 0 && n < N) epi_pair<bf16>(e, 0, n, a0, a1);
+  bool mine = lane == 0 && n < N;  // this thread holds the pair's sums
+  if (KS > 1) {
+    if (lane == 0) {
+      red[warp][0] = a0;
+      red[warp][1] = a1;
+    }
+    __syncthreads();
+    mine = mine && ks == 0;
+    if (mine) {
+      a0 = a1 = 0.f;
+#pragma unroll
+      for (int t = 0; t < KS; ++t) {
+        a0 += red[warp + t][0];
+        a1 += red[warp + t][1];
+      }
+    }
+  }
+  if (e.kind != EPI_ARGMAX) {
+    if (mine) epi_pair<bf16>(e, 0, n, a0, a1);
     return;
   }
+  // greedy pick: the block's best key, then one atomic per block
+  __shared__ unsigned long long skey[8];
   if (lane == 0) {
-    red[warp][0] = a0;
-    red[warp][1] = a1;
+    const unsigned long long k0 = mine ? argmax_key(a0, n) : 0ull, k1 = mine ? argmax_key(a1, n + 1) : 0ull;
+    skey[warp] = k0 > k1 ? k0 : k1;
   }
   __syncthreads();
-  if (ks == 0 && lane == 0 && n < N) {
-    float s0 = 0.f, s1 = 0.f;
+  if (threadIdx.x == 0) {
+    unsigned long long k = 0ull;
 #pragma unroll
-    for (int t = 0; t < KS; ++t) {
-      s0 += red[warp + t][0];
-      s1 += red[warp + t][1];
-    }
-    epi_pair<bf16>(e, 0, n, s0, s1);
+    for (int w = 0; w < 8; ++w) k = skey[w] > k ? skey[w] : k;
+    if (k) atomicMax((unsigned long long*)e.out, k);
   }
 }
 

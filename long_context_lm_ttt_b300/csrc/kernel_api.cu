@@ -183,16 +183,18 @@ extern "C" int ttt_kernel_attn_fwd(int32_t impl, int32_t n, int32_t H, int32_t H
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return TTT_ERR_CUDA;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const size_t need = (size_t)H * ttt::kMaxDecodeSplits * (hd + 2);
+    const size_t need = (size_t)ttt::attn_decode_scratch_elems(H, hd);
     if (elems_of[dev] < need) {
       if (part_of[dev]) cudaFree(part_of[dev]);
       part_of[dev] = nullptr;
       elems_of[dev] = 0;
       if (cudaMalloc(&part_of[dev], need * sizeof(float)) != cudaSuccess) return TTT_ERR_OOM;
+      // the per-KV-head counters at the start begin at zero
+      if (cudaMemset(part_of[dev], 0, need * sizeof(float)) != cudaSuccess) return TTT_ERR_CUDA;
       elems_of[dev] = need;
     }
     float* part = part_of[dev];
-    ttt::attn_decode<ttt::bf16>(a, ttt::attn_decode_splits(a, sms), part, st);
+    if (ttt::attn_decode<ttt::bf16>(a, ttt::attn_decode_splits(a, sms), part, g_err, st)) return TTT_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
   }
   if (impl == 0 || impl == 2 || impl == 3) {

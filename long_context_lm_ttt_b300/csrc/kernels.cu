@@ -94,10 +94,11 @@ __global__ void rmsnorm_bwd_kernel(const float* __restrict__ x, const float* __r
   }
 }
 
-__global__ void rope_table_kernel(int64_t pos0, int n, int hd, double theta, float2* cs) {
+__global__ void rope_table_kernel(int64_t pos0, const int64_t* pos_dev, int n, int hd, double theta, float2* cs) {
   const int half = hd >> 1;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n * half) return;
+  if (pos_dev) pos0 = *pos_dev;
   const int r = idx / half, i = idx % half;
   const double inv = pow(theta, -(2.0 * (double)i) / (double)hd);
   const double ang = (double)(pos0 + r) * inv;
@@ -250,6 +251,38 @@ __global__ void argmax_kernel(const float* __restrict__ z, int V, int32_t* out) 
       }
     }
     if (l == 0) *out = bi < V ? bi : 0;
+  }
+}
+
+__global__ void decode_begin_kernel(DecodeState* s, int64_t pos, int r, const int32_t* given, int n_given,
+                                    int32_t* out, unsigned long long* pick) {
+  if (threadIdx.x != 0) return;
+  *pick = 0ull;
+  s->pos = pos;
+  s->given = given;
+  s->out = out;
+  s->r = r;
+  s->i = 0;
+  s->n_given = n_given;
+  s->tok = given[0];
+}
+
+__global__ void decode_tail_kernel(DecodeState* s, const float* __restrict__ x, float* __restrict__ xdec, int d,
+                                   int32_t* dtok, unsigned long long* pick, int b) {
+  const int r = s->r;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) xdec[(int64_t)r * d + c] = x[c];
+  __syncthreads();  // every thread has read r before it moves on
+  if (threadIdx.x == 0) {
+    const int i = s->i, tok = s->tok;
+    const int nxt = i + 1 < s->n_given ? s->given[i + 1] : argmax_col(*pick);
+    *pick = 0ull;
+    dtok[r] = tok;
+    dtok[r + 1] = nxt;
+    s->out[i] = tok;
+    s->tok = nxt;
+    s->pos += 1;
+    s->i = i + 1;
+    s->r = r + 1 == b ? 0 : r + 1;
   }
 }
 
@@ -480,9 +513,18 @@ void launch_rmsnorm_bwd(const float* x, const float* g, const float* r, const fl
   }
   rmsnorm_bwd_kernel<T><<<n, RB, 0, st>>>(x, g, r, dy, resid, d, out, out_t);
 }
-void launch_rope_table(int64_t pos0, int n, int hd, float theta, float2* cs, cudaStream_t st) {
+void launch_rope_table(int64_t pos0, int n, int hd, float theta, float2* cs, cudaStream_t st,
+                       const int64_t* pos_dev) {
   const int total = n * (hd / 2);
-  if (total > 0) rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(pos0, n, hd, (double)theta, cs);
+  if (total > 0) rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(pos0, pos_dev, n, hd, (double)theta, cs);
+}
+void launch_decode_begin(DecodeState* s, int64_t pos, int r, const int32_t* given, int n_given, int32_t* out,
+                         unsigned long long* pick, cudaStream_t st) {
+  decode_begin_kernel<<<1, 32, 0, st>>>(s, pos, r, given, n_given, out, pick);
+}
+void launch_decode_tail(DecodeState* s, const float* x, float* xdec, int d, int32_t* dtok, unsigned long long* pick,
+                        int b, cudaStream_t st) {
+  decode_tail_kernel<<<1, 256, 0, st>>>(s, x, xdec, d, dtok, pick, b);
 }
 template <typename T>
 void launch_rope_bwd(T* dqkv, int n, int ld, int n_rot_heads, int hd, const float2* cs, cudaStream_t st) {

@@ -103,7 +103,10 @@ void launch_rmsnorm_fwd(const float* x, const float* g, int n, int d, float eps,
 template <typename T>
 void launch_rmsnorm_bwd(const float* x, const float* g, const float* r, const float* dy,
                         const float* resid, int n, int d, float* out, T* out_t, cudaStream_t st);
-void launch_rope_table(int64_t pos0, int n, int hd, float theta, float2* cs, cudaStream_t st);
+// RoPE table of positions pos0 .. pos0+n-1 (pos0 read from *pos_dev when
+// that is non-null)
+void launch_rope_table(int64_t pos0, int n, int hd, float theta, float2* cs, cudaStream_t st,
+                       const int64_t* pos_dev = nullptr);
 template <typename T>
 void launch_rope_bwd(T* dqkv, int n, int ld, int n_rot_heads, int hd, const float2* cs,
                      cudaStream_t st);
@@ -111,6 +114,31 @@ void launch_targets(const int32_t* tok, int64_t T, int64_t pos0, int n, int32_t*
                     int* err_tok, cudaStream_t st);
 // out[0] = the index of the largest of z[0..V) (smallest index on ties)
 void launch_argmax(const float* z, int V, int32_t* out, cudaStream_t st);
+
+// State of a decode call kept in device memory, so that every step can
+// replay the same captured launches: the step's position and input token,
+// its row within the chunk being filled, its index within the call, and
+// where the given tokens come from and the inputs go to.
+struct DecodeState {
+  int64_t pos;            // absolute position of the step's token
+  const int32_t* given;   // tokens given by the caller (n_given of them)
+  int32_t* out;           // out[i] = input token of step i
+  int32_t r;              // row of the chunk the step fills
+  int32_t i;              // step index within the call
+  int32_t n_given;
+  int32_t tok;            // input token of the step
+};
+// start of a call: pos, r, the given tokens (given[0] is the first input);
+// clears the greedy-pick key
+void launch_decode_begin(DecodeState* s, int64_t pos, int r, const int32_t* given, int n_given, int32_t* out,
+                         unsigned long long* pick, cudaStream_t st);
+// end of a step: xdec[r] = x (d floats, the first fast block's input row),
+// tok row r and the next input (given[i + 1] if there is one, else the
+// column of the greedy-pick key *pick, which is then cleared) into dtok[r],
+// dtok[r + 1], out[i] = the step's input, then the state moves to the next
+// position (r wraps to 0 after row b - 1)
+void launch_decode_tail(DecodeState* s, const float* x, float* xdec, int d, int32_t* dtok, unsigned long long* pick,
+                        int b, cudaStream_t st);
 template <typename T>
 void launch_ce_slab_stats(const float* z, int64_t ldz, int n, int nv, T* p, int64_t ldp,
                           float* m_run, float* l_run, float* alpha, float* beta, int first,
@@ -144,6 +172,8 @@ struct AttnArgs {
   int ld_lse;
   int n, H, Hkv, hd, W, R;
   int64_t pos0;
+  // non-null: pos0 is read from this device word instead (decode kernel only)
+  const int64_t* pos_dev;
   // backward
   const void* dout;   // [n, H*hd]
   const void* out;    // forward output o
@@ -159,12 +189,19 @@ struct AttnArgs {
 template <typename T> void attn_fwd_simt(const AttnArgs& a, cudaStream_t st);
 // one query position (n == 1, a decode step): key range split into `splits`
 // slices (at most kMaxDecodeSplits) folded through fp32 scratch `part` of
-// H * splits * (hd + 2) values; hd a multiple of 32 up to 256, at most 8
-// query heads per KV head
+// attn_decode_scratch_elems() values: kDecCounters counters (one per KV
+// head; zero them once after allocating, the kernels leave them at zero,
+// and their place does not depend on the shape, so one scratch serves
+// every shape), then the slices; hd a multiple of 32 up to 256, at most 8
+// query heads per KV head, at most kDecCounters KV heads.  A bounded wait
+// that gives up writes its code into *err.  Returns non-zero if a kernel
+// attribute could not be set.
 constexpr int kMaxDecodeSplits = 64;
+constexpr int kDecCounters = 256;
 bool attn_decode_supported(const AttnArgs& a);
 int attn_decode_splits(const AttnArgs& a, int num_sms);
-template <typename T> void attn_decode(const AttnArgs& a, int splits, float* part, cudaStream_t st);
+int64_t attn_decode_scratch_elems(int H, int hd);
+template <typename T> int attn_decode(const AttnArgs& a, int splits, float* part, int* err, cudaStream_t st);
 template <typename T> void attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
 // tcgen05 kernels (bf16); attn_tc_supported() tells whether the shape and
 // alignment fit them (64 <= hd <= 128, hd % 16 == 0, R % 128 == 0).  They

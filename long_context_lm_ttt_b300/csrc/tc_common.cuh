@@ -80,6 +80,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
+// 1-D bulk copy of `bytes` contiguous bytes from global to shared memory,
+// completing on `bar` (both addresses 16-byte aligned, bytes a multiple of 16)
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 // TMA store of a shared-memory box (written by ordinary stores: the writing
 // threads fence the generic proxy against the async proxy first)
 __device__ __forceinline__ void fence_proxy_async_smem() {

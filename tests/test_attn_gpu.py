@@ -106,6 +106,8 @@ DECODE_CASES = [
     (4, 4, 32, 64, 300, 128),                  # hd 32, one query head per KV head
     (6, 2, 96, 300, 1024, 640),                # hd 96, GQA 3
     (16, 2, 64, 1000, 999, 1024),              # GQA 8, window covers everything
+    (10, 2, 160, 500, 2000, 512),              # hd 160 (odd dims per lane), ring wraps
+    (8, 2, 256, 4096, 5000, 4608),             # hd 256, GQA 4
 ]
 
 
@@ -122,6 +124,23 @@ def test_attn_fwd_one_query(case):
     err_l = max(abs(lse[h, r] - v) for (r, h), v in rl.items())
     assert err_o < 2e-2, err_o
     assert err_l < 2e-3, err_l
+
+
+def test_attn_fwd_one_query_repeated_calls():
+    """The one-query kernel's last CTA per KV head folds the slices and
+    resets that head's counter: back-to-back calls at other positions stay
+    right, and a repeated call gives the same bits."""
+    torch, T = _env()
+    H, Hkv, hd, W, R = 24, 8, 128, 2048, 4096
+    outs = []
+    for pos0 in (3000, 3001, 100, 3000):
+        q, kr, vr = make_case(1, H, Hkv, hd, W, pos0, R, seed=11)
+        o, lse = run_fwd(T, torch, 4, q, kr, vr, 1, H, Hkv, hd, W, pos0)
+        ro, rl = ref_forward(q, kr, vr, 1, H, Hkv, hd, W, pos0)
+        err_o = max(np.abs(o[r, h * hd:(h + 1) * hd] - v).max() for (r, h), v in ro.items())
+        assert err_o < 2e-2, (pos0, err_o)
+        outs.append((o.copy(), lse.copy()))
+    assert np.array_equal(outs[0][0], outs[3][0]) and np.array_equal(outs[0][1], outs[3][1])
 
 
 @pytest.mark.parametrize("impl", [0, 2, 3])

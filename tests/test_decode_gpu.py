@@ -232,3 +232,33 @@ def test_teacher_forced_decode_dual_mlp(precision):
     cfg = O.OracleConfig.from_mapping(s.as_dict())
     r = O.decode(cfg, w, tok[:N + 1], N)
     _check_losses_weights(losses[:2], fast, r, TOL[precision])
+
+
+@pytest.mark.parametrize("precision", ["fp32", "bf16"])
+def test_decode_graph_replay_is_bitwise_direct_issue(precision):
+    """Decode steps replayed from the captured graphs give bit for bit what
+    the same steps give when every kernel is issued directly (per-launch
+    profiling keeps the engine on direct issue).  Mixes given and greedy
+    steps across two calls and a completed chunk."""
+    s = _shape("tiny-gqa", precision)
+    w, tok = inputs.make_weights(s), inputs.make_tokens(s)
+    N = 2 * s.chunk + 5
+    given = np.ascontiguousarray(tok[:s.chunk // 2], np.int32)
+    runs = []
+    for profiled in (False, True):
+        T, m = _model(s, w, precision, N + 1)
+        try:
+            if profiled:
+                m.profile(True)
+            o1, l1 = m.decode(given, s.chunk + 3)
+            o2, l2 = m.decode(o1[-1:], N - (s.chunk + 3))
+            fast = [m.fast_weights(i) for i in range(s.n_ttt_layers)]
+        finally:
+            m.close()
+        runs.append((o1, l1, o2, l2, fast))
+    (a1, al1, a2, al2, af), (b1, bl1, b2, bl2, bf) = runs
+    assert np.array_equal(a1, b1) and np.array_equal(a2, b2)
+    assert np.array_equal(np.asarray(al1), np.asarray(bl1)) and np.array_equal(np.asarray(al2), np.asarray(bl2))
+    for fa, fb in zip(af, bf):
+        for k in O.FAST:
+            assert np.array_equal(fa[k], fb[k])
