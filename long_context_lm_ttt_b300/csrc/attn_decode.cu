@@ -279,17 +279,20 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 2)
   const int kvh = blockIdx.x, sid = blockIdx.y;  // KV head, key slice
   const int G = H / Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (pos_dev) pos = *pos_dev;
-  const int64_t j_lo = pos - W + 1 > 0 ? pos - W + 1 : 0;
-  const int64_t cnt = pos - j_lo + 1;
-  const int64_t s0 = j_lo + cnt * sid / splits, s1 = j_lo + cnt * (sid + 1) / splits;
-  const int npass = (int)((s1 - s0 + P - 1) / P);
-
   if (threadIdx.x == 0) {
     for (int b = 0; b < kDecBufs; ++b) tc::mbar_init(tc::smem_u32(&bar[b]), 1);
     tc::fence_mbar_init();
     abort_flag = 0;
   }
+  // q, the newest key and value rows and the position come from the
+  // kernels before this one
+  pdl_wait();
+  pdl_trigger();
+  if (pos_dev) pos = *pos_dev;
+  const int64_t j_lo = pos - W + 1 > 0 ? pos - W + 1 : 0;
+  const int64_t cnt = pos - j_lo + 1;
+  const int64_t s0 = j_lo + cnt * sid / splits, s1 = j_lo + cnt * (sid + 1) / splits;
+  const int npass = (int)((s1 - s0 + P - 1) / P);
   __syncthreads();
   // pass ps: keys [s0 + ps P, ...) into buffer ps % kDecBufs (thread 0 only)
   auto issue = [&](int ps) {
@@ -569,10 +572,9 @@ int launch_bulk(const AttnArgs& a, int splits, float* part, int* err, cudaStream
   if (raise_smem_limit(raised, kern, smem) != cudaSuccess) return -1;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.hd);
   int* count = reinterpret_cast<int*>(part);
-  kern<<<dim3(a.Hkv, splits), kBulkWarps * 32, smem, st>>>(
-      (const bf16*)a.q, (const bf16*)a.kring, (const bf16*)a.vring, a.H, a.Hkv, a.W, a.R, a.pos0, a.pos_dev, splits,
-      scale_log2, part + kDecCounters, count, (bf16*)a.o, a.lse, a.ld_lse, err);
-  return 0;
+  return launch_k(kern, dim3(a.Hkv, splits), kBulkWarps * 32, smem, st, (const bf16*)a.q, (const bf16*)a.kring,
+                  (const bf16*)a.vring, a.H, a.Hkv, a.W, a.R, a.pos0, a.pos_dev, splits, scale_log2,
+                  part + kDecCounters, count, (bf16*)a.o, a.lse, a.ld_lse, err) != cudaSuccess;
 }
 template <int EPL>
 int launch_bulk_g(const AttnArgs& a, int splits, float* part, int* err, cudaStream_t st) {

@@ -38,6 +38,16 @@ template <> __device__ __forceinline__ float2 load2<bf16>(const bf16* p) {
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+// Programmatic dependent launch.  A kernel launched with it (launch_k with
+// launches marked by set_pdl) may begin while the previous kernel on its
+// stream still runs.  It calls pdl_wait() before touching anything that
+// kernel or an earlier one writes (the wait returns at once after an
+// ordinary launch), and pdl_trigger() after that wait, which lets the next
+// such kernel begin: so at most two kernels of a chain overlap, and
+// everything two or more kernels back has completed.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // GEMM:  C[m, n] = sum_k A(m, k) * B(n, k)
 //   A(m,k) = a_mn ? A[k*lda + m] : A[m*lda + k]

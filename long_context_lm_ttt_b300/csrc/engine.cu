@@ -104,6 +104,10 @@ struct EngineBase {
                      cudaStream_t st) = 0;
   // decode state: rows of the current chunk already decoded
   int dec_fill = 0;
+  bool dec_graph_off = false;  // capture failed once (or asked): issue steps directly
+  // programmatic dependent launch inside decode steps (off under profiling:
+  // the events between launches would serialise them anyway)
+  bool pdl_ok = true;
   virtual int get_fast(int block, int which, float* dst, cudaStream_t st) = 0;
   virtual int reset(cudaStream_t st) = 0;
 
@@ -285,7 +289,6 @@ struct Engine : EngineBase {
   const int64_t* dpos = nullptr;
   cudaGraphExec_t dec_graph[2] = {nullptr, nullptr};
   cudaStream_t cap_st = nullptr;
-  bool dec_graph_off = false;  // capture failed once: issue steps directly
   int gemm_cls = -1;          // profile class of the next GEMMs, if set
   int* dev_err = nullptr;  // [0] first non-finite chunk, [1] bad token, [2] kernel check
   float* stage32 = nullptr;
@@ -1095,6 +1098,9 @@ struct Engine : EngineBase {
     const int lo = cfg.n_layers - cfg.n_ttt_layers;
     dec_part = dec_buf;
     dpos = &dstate->pos;
+    // consecutive kernels of the step overlap their start-up (and the
+    // one-row products their first weight loads) with the kernel before
+    set_pdl(pdl_ok && !prof_on);
     forward_all(&dstate->tok, pos, 1, st, rc);
     dpos = nullptr;
     dec_part = nullptr;
@@ -1108,6 +1114,7 @@ struct Engine : EngineBase {
       gemm_cls = -1;
     }
     row((double)d * 8, st, [&] { launch_decode_tail(dstate, xlow[lo & 1], xdec, d, dtok, dec_pick, b, st); });
+    set_pdl(false);
   }
   // Record the launches of one decode step of the given kind into a graph
   // (on a stream of the engine's own: capture needs one that is not the
@@ -1424,6 +1431,12 @@ extern "C" int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* str
   // TTT_ATTN_IMPL=simt keeps it on the SIMT kernels (a GPU-side cross-check)
   eng->use_tc_attn = bf && !(a && strcmp(a, "simt") == 0);
   eng->use_tc_attn_bwd = eng->use_tc_attn;
+  // decode steps: TTT_DECODE_LAUNCH=graph keeps the captured graphs without
+  // programmatic dependent launch, =direct issues every kernel from the
+  // host (the same kernels and results; for measuring the launch modes)
+  const char* dl = getenv("TTT_DECODE_LAUNCH");
+  eng->pdl_ok = !(dl && (strcmp(dl, "graph") == 0 || strcmp(dl, "direct") == 0));
+  eng->dec_graph_off = dl && strcmp(dl, "direct") == 0;
   if (eng->use_tc_gemm) {
     int r = ttt::gemm_tc_init();
     if (r) {

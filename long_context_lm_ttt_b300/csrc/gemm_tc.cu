@@ -661,11 +661,46 @@ __global__ void __launch_bounds__(256) gemv_row_kernel(const bf16* __restrict__ 
   const int kchunk = ((K / 8 + KS - 1) / KS) * 8;
   const int k0 = ks * kchunk, k1 = min(K, k0 + kchunk);
   float a0 = 0.f, a1 = 0.f;
+  // the first PRE weight chunks are loaded before waiting on the kernel
+  // that writes x (weights are not written by the kernels this one may
+  // overlap under programmatic launch)
+  constexpr int PRE = 4;
+  constexpr int NB = DUAL ? 4 : 2;
+  uint4 wp[PRE][NB];
+  const bf16* b0 = B + (int64_t)n * ldb;
+  const bf16* b1 = b0 + ldb;
   if (n < N) {
-    const bf16* b0 = B + (int64_t)n * ldb;
-    const bf16* b1 = b0 + ldb;
+#pragma unroll
+    for (int i = 0; i < PRE; ++i) {
+      const int k = k0 + lane * 8 + 256 * i;
+      if (k < k1) {
+        wp[i][0] = __ldg(reinterpret_cast<const uint4*>(b0 + k));
+        wp[i][1] = __ldg(reinterpret_cast<const uint4*>(b1 + k));
+        if (DUAL) {
+          wp[i][NB - 2] = __ldg(reinterpret_cast<const uint4*>(B2 + (int64_t)n * ldb + k));
+          wp[i][NB - 1] = __ldg(reinterpret_cast<const uint4*>(B2 + (int64_t)(n + 1) * ldb + k));
+        }
+      }
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (n < N) {
+#pragma unroll
+    for (int i = 0; i < PRE; ++i) {
+      const int k = k0 + lane * 8 + 256 * i;
+      if (k < k1) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + k);
+        a0 += dot8(xv, wp[i][0]);
+        a1 += dot8(xv, wp[i][1]);
+        if (DUAL) {
+          a0 += dot8(xv, wp[i][NB - 2]);
+          a1 += dot8(xv, wp[i][NB - 1]);
+        }
+      }
+    }
 #pragma unroll 4
-    for (int k = k0 + lane * 8; k < k1; k += 256) {
+    for (int k = k0 + lane * 8 + 256 * PRE; k < k1; k += 256) {
       const uint4 xv = *reinterpret_cast<const uint4*>(x + k);
       a0 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(b0 + k)));
       a1 += dot8(xv, __ldg(reinterpret_cast<const uint4*>(b1 + k)));
@@ -725,10 +760,10 @@ void launch_gemv(const GemmArgs<bf16>& g, int num_sms, cudaStream_t st) {
   const int rp = 8 / ks;
   const int blocks = (g.N / 2 + rp - 1) / rp;
   switch (ks) {
-    case 1: gemv_row_kernel<DUAL, 1><<<blocks, 256, 0, st>>>(g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
-    case 2: gemv_row_kernel<DUAL, 2><<<blocks, 256, 0, st>>>(g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
-    case 4: gemv_row_kernel<DUAL, 4><<<blocks, 256, 0, st>>>(g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
-    default: gemv_row_kernel<DUAL, 8><<<blocks, 256, 0, st>>>(g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
+    case 1: launch_k(gemv_row_kernel<DUAL, 1>, blocks, 256, 0, st, g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
+    case 2: launch_k(gemv_row_kernel<DUAL, 2>, blocks, 256, 0, st, g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
+    case 4: launch_k(gemv_row_kernel<DUAL, 4>, blocks, 256, 0, st, g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
+    default: launch_k(gemv_row_kernel<DUAL, 8>, blocks, 256, 0, st, g.A, g.B, g.B2, g.N, g.K, g.ldb, g.e); break;
   }
 }
 

@@ -49,6 +49,8 @@ __device__ __forceinline__ float block_reduce(float v, Op op, float* sh) {
 template <typename T>
 __global__ void embed_kernel(const int32_t* __restrict__ tok, int d, const T* __restrict__ E,
                              float* __restrict__ x, int V, int* err_tok) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   int64_t id = tok[r];
   if (id < 0 || id >= V) {      // out-of-range id: flag it, read row 0 instead
@@ -95,6 +97,8 @@ __global__ void rmsnorm_bwd_kernel(const float* __restrict__ x, const float* __r
 }
 
 __global__ void rope_table_kernel(int64_t pos0, const int64_t* pos_dev, int n, int hd, double theta, float2* cs) {
+  pdl_wait();
+  pdl_trigger();
   const int half = hd >> 1;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n * half) return;
@@ -269,6 +273,8 @@ __global__ void decode_begin_kernel(DecodeState* s, int64_t pos, int r, const in
 
 __global__ void decode_tail_kernel(DecodeState* s, const float* __restrict__ x, float* __restrict__ xdec, int d,
                                    int32_t* dtok, unsigned long long* pick, int b) {
+  pdl_wait();
+  pdl_trigger();
   const int r = s->r;
   for (int c = threadIdx.x; c < d; c += blockDim.x) xdec[(int64_t)r * d + c] = x[c];
   __syncthreads();  // every thread has read r before it moves on
@@ -338,6 +344,8 @@ template <int VPT>
 __global__ void __launch_bounds__(256) rmsnorm_fwd_vec_kernel(const float* __restrict__ x, const float* __restrict__ g,
                                                               int d, float eps, bf16* __restrict__ out,
                                                               float* __restrict__ rr) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sh[32];
   const int r = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + (int64_t)r * d);
@@ -474,10 +482,14 @@ inline int grid_for(int64_t total, int threads) {
 
 }  // namespace
 
+static thread_local bool t_pdl = false;
+void set_pdl(bool on) { t_pdl = on; }
+bool pdl_enabled() { return t_pdl; }
+
 template <typename T>
 void launch_embed(const int32_t* tok, int n, const T* E, int d, float* x, int V, int* err_tok,
                   cudaStream_t st) {
-  if (n > 0) embed_kernel<T><<<n, RB, 0, st>>>(tok, d, E, x, V, err_tok);
+  if (n > 0) launch_k(embed_kernel<T>, n, RB, 0, st, tok, d, E, x, V, err_tok);
 }
 static inline bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
@@ -488,10 +500,11 @@ void launch_rmsnorm_fwd(const float* x, const float* g, int n, int d, float eps,
   if constexpr (sizeof(T) == 2) {
     if (d % 4 == 0 && d <= 4 * 256 * 4 && al16(x) && al16(g) && ((uintptr_t)out & 7) == 0) {
       const int vpt = (d / 4 + 255) / 256;
-      if (vpt <= 1) rmsnorm_fwd_vec_kernel<1><<<n, 256, 0, st>>>(x, g, d, eps, (bf16*)out, r);
-      else if (vpt <= 2) rmsnorm_fwd_vec_kernel<2><<<n, 256, 0, st>>>(x, g, d, eps, (bf16*)out, r);
-      else if (vpt <= 3) rmsnorm_fwd_vec_kernel<3><<<n, 256, 0, st>>>(x, g, d, eps, (bf16*)out, r);
-      else rmsnorm_fwd_vec_kernel<4><<<n, 256, 0, st>>>(x, g, d, eps, (bf16*)out, r);
+      auto k = vpt <= 1 ? rmsnorm_fwd_vec_kernel<1>
+               : vpt <= 2 ? rmsnorm_fwd_vec_kernel<2>
+               : vpt <= 3 ? rmsnorm_fwd_vec_kernel<3>
+                          : rmsnorm_fwd_vec_kernel<4>;
+      launch_k(k, n, 256, 0, st, x, g, d, eps, (bf16*)out, r);
       return;
     }
   }
@@ -516,7 +529,7 @@ void launch_rmsnorm_bwd(const float* x, const float* g, const float* r, const fl
 void launch_rope_table(int64_t pos0, int n, int hd, float theta, float2* cs, cudaStream_t st,
                        const int64_t* pos_dev) {
   const int total = n * (hd / 2);
-  if (total > 0) rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(pos0, pos_dev, n, hd, (double)theta, cs);
+  if (total > 0) launch_k(rope_table_kernel, (total + 255) / 256, 256, 0, st, pos0, pos_dev, n, hd, (double)theta, cs);
 }
 void launch_decode_begin(DecodeState* s, int64_t pos, int r, const int32_t* given, int n_given, int32_t* out,
                          unsigned long long* pick, cudaStream_t st) {
@@ -524,7 +537,7 @@ void launch_decode_begin(DecodeState* s, int64_t pos, int r, const int32_t* give
 }
 void launch_decode_tail(DecodeState* s, const float* x, float* xdec, int d, int32_t* dtok, unsigned long long* pick,
                         int b, cudaStream_t st) {
-  decode_tail_kernel<<<1, 256, 0, st>>>(s, x, xdec, d, dtok, pick, b);
+  launch_k(decode_tail_kernel, 1, 256, 0, st, s, x, xdec, d, dtok, pick, b);
 }
 template <typename T>
 void launch_rope_bwd(T* dqkv, int n, int ld, int n_rot_heads, int hd, const float2* cs, cudaStream_t st) {

@@ -25,6 +25,28 @@ inline cudaError_t raise_smem_limit(std::atomic<uint64_t>& done, K kern, int byt
   return e;
 }
 
+// While set (per host thread), the launchers of the kernels a decode step
+// issues (one-row products, RMSNorm forward, embedding, RoPE table,
+// one-query attention, step tail) mark their launches for programmatic
+// dependent launch; those kernels call pdl_wait() / pdl_trigger().
+void set_pdl(bool on);
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args... args) {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = grid;
+  c.blockDim = block;
+  c.dynamicSmemBytes = smem;
+  c.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  c.attrs = at;
+  c.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&c, kern, static_cast<KArgs>(args)...);
+}
+
 template <typename T>
 struct GemmArgs {
   int M, N, K;
