@@ -893,7 +893,7 @@ struct BwdParams {
   const float* lse;  // [H][ld_lse]
   const float* dsum; // [H][ld_lse]
   int ld_lse;
-  int parts;
+  int parts;         // dq: key-range parts
   bf16* dqkv;
   int64_t ldg;
   float* ws;
@@ -921,9 +921,12 @@ __device__ __forceinline__ void rope_back(float& x, float& y, float2 cs) {
 // each warp has read itself (keys 32 ks.. -> columns 32 ks.., 16 wide), and
 // the dQ product reads dS from TMEM as its A operand (K = 16 slices at
 // columns 32 (k >> 1) + 8 (k & 1)).
-// MMA order for block i: S(i + 1) into the other S buffer, then (once dS(i)
-// is ready) dQ(i), then dP(i + 1); so the tensor core computes the next
-// scores while dS(i) is formed.  Products of one thread run in issue order,
+// MMA order for block i: S(i + 1) into the other S buffer, dP(i + 1) once
+// the compute warps have loaded dP(i) into registers, then dQ(i) once dS(i)
+// is ready; so the tensor core computes the next block's scores and dP
+// while dS(i) is formed, and dQ(i) while the warps start on block i + 1.
+// dS(i) completions alternate between two barriers by block parity, so a
+// waiter never sees a phase of the block after next.  Products of one thread run in issue order,
 // which keeps every buffer's reader ahead of its next writer.
 // Eighteen warps: warp 0 loads (TMA), warp 1 issues the MMAs, warps 2-17
 // compute dS (four per TMEM lane quarter, 32 of a block's 128 keys each).
@@ -944,7 +947,7 @@ struct DqSmem {
   // at least 120 KB: one CTA (512 TMEM columns) per SM
   static constexpr int SMEM = BAR_OFF + 256 > 120 * 1024 ? BAR_OFF + 256 : 120 * 1024;
   static_assert(SMEM <= 232448, "shared memory");
-  static_assert(8 + 16 * (DQ_KST + DQ_VST) + 32 <= 192, "barrier area");
+  static_assert(8 + 16 * (DQ_KST + DQ_VST) + 48 <= 192, "barrier area");
 };
 
 // key-block range [lo, hi] (blocks of DQ_BN) of the tile starting at row r0
@@ -972,9 +975,10 @@ __global__ void __launch_bounds__(576, 1)
   const uint32_t v_full = k_empty + 8 * DQ_KST;    // [DQ_VST]
   const uint32_t v_empty = v_full + 8 * DQ_VST;    // [DQ_VST]
   const uint32_t sdp_full = v_empty + 8 * DQ_VST;  // S(i) and dP(i) done
-  const uint32_t ds_full = sdp_full + 8;           // dS(i) written
-  const uint32_t dq_done = ds_full + 8;
+  const uint32_t ds_full = sdp_full + 8;           // [2]: dS(i) written (block parity)
+  const uint32_t dq_done = ds_full + 16;
   const uint32_t drain = dq_done + 8;
+  const uint32_t dp_free = drain + 8;              // dP(i) read into registers
   uint32_t* tmem_slot = (uint32_t*)(smem + SM::BAR_OFF + 192);
   volatile int* abort = (volatile int*)(smem + SM::BAR_OFF + 196);
   // ring slot and phase parity of block i in a ring of `st` slots
@@ -1006,8 +1010,10 @@ __global__ void __launch_bounds__(576, 1)
     }
     tc::mbar_init(sdp_full, 1);
     tc::mbar_init(ds_full, 16);  // one arrival per compute warp
+    tc::mbar_init(ds_full + 8, 16);
     tc::mbar_init(dq_done, 1);
     tc::mbar_init(drain, 1);
+    tc::mbar_init(dp_free, 16);
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -1120,7 +1126,20 @@ __global__ void __launch_bounds__(576, 1)
           ok = false;
           break;
         }
-        if (!tc::mbar_wait(ds_full, (uint32_t)(i & 1), p.err, ERR_A_MMA, abort)) {
+        // dP(i + 1) as soon as the compute warps hold dP(i) in registers,
+        // so that it runs while they form dS(i)
+        if (i + 1 < nb) {
+          if (!tc::mbar_wait(dp_free, (uint32_t)(i & 1), p.err, ERR_A_MMA, abort)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          if (!issue_dp(i + 1)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!tc::mbar_wait(ds_full + 8 * (i & 1), (uint32_t)((i >> 1) & 1), p.err, ERR_A_MMA, abort)) {
           ok = false;
           break;
         }
@@ -1133,10 +1152,6 @@ __global__ void __launch_bounds__(576, 1)
                       tc::smem_desc_sw128(kb + 2048 * k, DQ_BN * 128, 1024), idQ, (i > 0 || k > 0) ? 1u : 0u);
         // K(i) has served S(i) and dQ(i)
         tc::mma_commit(k_empty + 8 * ks);
-        if (i + 1 < nb && !issue_dp(i + 1)) {
-          ok = false;
-          break;
-        }
       }
       if (ok) tc::mma_commit(dq_done);
       if (!ok && issued) {
@@ -1170,25 +1185,40 @@ __global__ void __launch_bounds__(576, 1)
       tmem_ld32_nw(ts, sv);
       tmem_ld32_nw(tmem + 128 + lane_off + 32 * ks, dp);
       tmem_wait_ld();
+      // the dP buffer may take dP(i + 1) now
+      tc::tc_fence_before();
+      warp_arrive(dp_free);
       const long long kpos = (jb + i) * DQ_BN + 32 * ks;
       const long long lo_l = pos - p.W + 1 - kpos, hi_l = pos - kpos;
       const int lo = (int)(lo_l < -1 ? -1 : (lo_l > 32 ? 32 : lo_l));
       const int hi = (int)(hi_l < -1 ? -1 : (hi_l > 32 ? 32 : hi_l));
       uint32_t pk[16];
+      if (__all_sync(0xffffffffu, lo <= 0 && hi >= 31)) {
+        // every key of the slice is inside every row's window: no mask
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float x0, x1, y0, y1, d0, d1;
-        fma2(sv[c], sv[c + 1], p.scale_log2, -lse2, x0, x1);
-        const float p0 = (c >= lo && c <= hi) ? ex2_ftz(x0) : 0.f;
-        const float p1 = (c + 1 >= lo && c + 1 <= hi) ? ex2_ftz(x1) : 0.f;
-        fma2(dp[c], dp[c + 1], p.scale, nDs, y0, y1);
-        mul2(p0, p1, y0, y1, d0, d1);
-        pk[c / 2] = pack_bf16(d0, d1);
+        for (int c = 0; c < 32; c += 2) {
+          float x0, x1, y0, y1, d0, d1;
+          fma2(sv[c], sv[c + 1], p.scale_log2, -lse2, x0, x1);
+          fma2(dp[c], dp[c + 1], p.scale, nDs, y0, y1);
+          mul2(ex2_ftz(x0), ex2_ftz(x1), y0, y1, d0, d1);
+          pk[c / 2] = pack_bf16(d0, d1);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float x0, x1, y0, y1, d0, d1;
+          fma2(sv[c], sv[c + 1], p.scale_log2, -lse2, x0, x1);
+          const float p0 = (c >= lo && c <= hi) ? ex2_ftz(x0) : 0.f;
+          const float p1 = (c + 1 >= lo && c + 1 <= hi) ? ex2_ftz(x1) : 0.f;
+          fma2(dp[c], dp[c + 1], p.scale, nDs, y0, y1);
+          mul2(p0, p1, y0, y1, d0, d1);
+          pk[c / 2] = pack_bf16(d0, d1);
+        }
       }
       tmem_st16u(ts, pk);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc::tc_fence_before();
-      warp_arrive(ds_full);
+      warp_arrive(ds_full + 8 * (i & 1));
     }
     const bool have = nb > 0;
     if (ok && have && !warp_wait(dq_done, 0, p.err, ERR_A_SOFT, abort)) ok = false;
@@ -1440,24 +1470,48 @@ __global__ void __launch_bounds__(320, 1)
       const int t0 = (qb0 + i) * BN + 32 * hf;
       uint32_t pp[16], pd[16];
       {
+        // lane c holds the statistics of query t0 + c; the loop below
+        // takes them by shuffle (every lane needs all 32)
+        const int tl = t0 + lane;
+        const float l2_l = tl < p.n ? lse_h[tl] * 1.4426950408889634f : 0.f;
+        const float nDs_l = tl < p.n ? -d_h[tl] * p.scale : 0.f;
         float sv[32], dp[32];
-        tc::tmem_ld32(tS + st * BN + 32 * hf + lane_off, sv);
-        tc::tmem_ld32(tP + st * BN + 32 * hf + lane_off, dp);
+        tmem_ld32_nw(tS + st * BN + 32 * hf + lane_off, sv);
+        tmem_ld32_nw(tP + st * BN + 32 * hf + lane_off, dp);
+        tmem_wait_ld();
+        // every (key, query) pair of the warp's block is valid: no mask
+        const bool all_valid = __all_sync(0xffffffffu, t0 + 31 < p.n && j < p.n && t0 - j >= 0 && t0 + 31 - j < p.W);
+        if (all_valid) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float pv[2], dv[2];
+          for (int c = 0; c < 32; c += 2) {
+            float pv[2], dv[2];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int t = t0 + c + e;
-            const int rel = t - j;
-            const bool valid = t < p.n && j < p.n && rel >= 0 && rel < p.W;
-            const float l2 = valid ? lse_h[t] * 1.4426950408889634f : 0.f;
-            const float Dt = valid ? d_h[t] : 0.f;
-            pv[e] = valid ? ex2_ftz(fmaf(sv[c + e], p.scale_log2, -l2)) : 0.f;
-            dv[e] = pv[e] * fmaf(dp[c + e], p.scale, -Dt * p.scale);
+            for (int e = 0; e < 2; ++e) {
+              const float l2 = __shfl_sync(0xffffffffu, l2_l, c + e);
+              const float nDs = __shfl_sync(0xffffffffu, nDs_l, c + e);
+              pv[e] = ex2_ftz(fmaf(sv[c + e], p.scale_log2, -l2));
+              dv[e] = pv[e] * fmaf(dp[c + e], p.scale, nDs);
+            }
+            pp[c / 2] = pack_bf16(pv[0], pv[1]);
+            pd[c / 2] = pack_bf16(dv[0], dv[1]);
           }
-          pp[c / 2] = pack_bf16(pv[0], pv[1]);
-          pd[c / 2] = pack_bf16(dv[0], dv[1]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int t = t0 + c + e;
+              const int rel = t - j;
+              const bool valid = t < p.n && j < p.n && rel >= 0 && rel < p.W;
+              const float l2 = __shfl_sync(0xffffffffu, l2_l, c + e);
+              const float nDs = __shfl_sync(0xffffffffu, nDs_l, c + e);
+              pv[e] = valid ? ex2_ftz(fmaf(sv[c + e], p.scale_log2, -l2)) : 0.f;
+              dv[e] = valid ? pv[e] * fmaf(dp[c + e], p.scale, nDs) : 0.f;
+            }
+            pp[c / 2] = pack_bf16(pv[0], pv[1]);
+            pd[c / 2] = pack_bf16(dv[0], dv[1]);
+          }
         }
       }
       tc::tc_fence_before();
