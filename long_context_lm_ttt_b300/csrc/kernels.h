@@ -111,6 +111,11 @@ template <typename T> void gemm_simt(const GemmArgs<T>& g, cudaStream_t st);
 // (cudaErrorNotSupported when the shape cannot be described by TMA).
 // *kernels (optional) receives the number of kernels launched (2 with a
 // split-K reduction).
+// one-row product (M = 1) streamed from HBM on SIMT cores (gemv.cu): K-major
+// operands, N even, K a multiple of 8, 16-byte aligned x, B, B2 and row
+// pitch; the epilogue of g.e per column pair, or EPI_ARGMAX
+bool gemv_supported(const GemmArgs<bf16>& g);
+int gemv_row(const GemmArgs<bf16>& g, int num_sms, cudaStream_t st);
 int gemm_tc(const GemmArgs<bf16>& g, int num_sms, int* dev_err, cudaStream_t st, int* kernels = nullptr);
 int gemm_tc_init();
 

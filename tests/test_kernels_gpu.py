@@ -29,6 +29,9 @@ def _operand(rng, rows, cols, mn, bf16=True):
 SHAPES = [(128, 128, 64), (256, 384, 192), (100, 200, 96), (32, 128, 32), (130, 258, 70),
           (1024, 3072, 1024), (512, 512, 4096), (520, 640, 200), (300, 136, 1000),
           (1, 256, 200), (1, 3072, 3072),
+          # one-row products: several K ranges per column pair (a ragged last
+          # one), many pairs per SM, and a single pair
+          (1, 16384, 3072), (1, 3072, 8192), (1, 258, 5000), (1, 2, 64),
           # 192-wide tiles with ragged edges (planner: pairs for a K-major B,
           # single CTAs otherwise)
           (1000, 3000, 200)]
@@ -61,17 +64,20 @@ def test_gemm_bf16(M, N, K, a_mn, b_mn, impl):
     assert T.ttt_kernel_error() == 0
     got = C.cpu().numpy().astype(np.float64)
     err = np.abs(got - ref).max() / np.abs(ref).max()
-    assert err < 1e-5, err          # fp32 accumulation of exact bf16 products
+    # fp32 accumulation of exact bf16 products: the rounding error of a sum
+    # grows with its number of terms (at most linearly, Higham's n u bound),
+    # so the bound grows with K beyond 4096
+    assert err < 1e-5 * max(1.0, K / 4096), err
 
 
 @pytest.mark.parametrize("impl", [0, 1, 3, 4])
 @pytest.mark.parametrize("b_mn", [0, 1])
-@pytest.mark.parametrize("M", [200, 1])
-def test_gemm_dual_b(impl, b_mn, M):
+@pytest.mark.parametrize("M,K", [(200, 320), (1, 320), (1, 5000)])
+def test_gemm_dual_b(impl, b_mn, M, K):
     """C = A B^T + A B2^T (the hi + lo fast-weight pair); M = 1 is the
-    one-row product of a decode step."""
+    one-row product of a decode step (K 5000: several K ranges per pair)."""
     torch, T = _env()
-    N, K = 384, 320
+    N = 384
     rng = np.random.default_rng(3)
     a, a_st = _operand(rng, M, K, 0)
     b, b_st = _operand(rng, N, K, b_mn)
@@ -83,7 +89,8 @@ def test_gemm_dual_b(impl, b_mn, M):
     torch.cuda.synchronize()
     assert T.ttt_kernel_error() == 0
     err = np.abs(C.cpu().numpy() - ref).max() / np.abs(ref).max()
-    assert err < 1e-5, err
+    # 2 K products per output: the fp32 summation bound grows with them
+    assert err < 1e-5 * max(1.0, 2 * K / 4096), err
 
 
 def test_gemm_fp32_simt():
