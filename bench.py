@@ -519,7 +519,10 @@ def run_decode(args):
             o, l = m.decode(tok[ctx:ctx + 1], nd)
             return 1e3 * (time.perf_counter() - t0), o
         ev0.record()
+        # an NVTX range, so that a profiler can take the decode launches alone
+        torch.cuda.nvtx.range_push("decode")
         m.decode(tok_d[ctx:ctx + 1], nd, out_d, loss_d)
+        torch.cuda.nvtx.range_pop()
         ev1.record()
         torch.cuda.synchronize()
         return ev0.elapsed_time(ev1), None
