@@ -81,3 +81,37 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     p = z.data_ptr()
     rc = lib.ttt_kernel_attn_bwd_noalloc(n, H, Hkv, hd, W, R, 0, p, p, p, p, p, n, p, p, p, None)
     assert rc == T.TTT_ERR_SHAPE
+
+
+def test_noalloc_against_fp64_restatement():
+    """The no-alloc backward's dq, dk, dv against the fp64 restatement of
+    the attention backward (the same check as the allocating entry point's
+    in test_attn_gpu.py), on a ragged chunk with head dim 96 whose window
+    wraps the ring."""
+    torch, T, lib = _env()
+    from test_attn_gpu import make_case, ref_backward
+    from long_context_lm_ttt_b300 import inputs
+    n, H, Hkv, hd, W, pos0, R = 256, 6, 2, 96, 300, 1024, 640
+    q, kr, vr = make_case(n, H, Hkv, hd, W, pos0, R, seed=2 * n + hd)
+    rng = np.random.default_rng(n)
+    dout = inputs.round_bf16(rng.standard_normal((n, H * hd)).astype(np.float32))
+    cu = lambda a: torch.from_numpy(a).to(torch.bfloat16).cuda()
+    dq_, dk_, dv_, do_ = cu(q), cu(kr), cu(vr), cu(dout)
+    o = torch.zeros((n, H * hd), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((H, n), dtype=torch.float32, device="cuda")
+    assert lib.ttt_kernel_attn_fwd(0, n, H, Hkv, hd, W, R, pos0, dq_.data_ptr(), dk_.data_ptr(), dv_.data_ptr(),
+                                   o.data_ptr(), lse.data_ptr(), n, None) == 0
+    dsum = torch.zeros((H, n), dtype=torch.float32, device="cuda")
+    g = torch.full((n, (H + 2 * Hkv) * hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    rc = lib.ttt_kernel_attn_bwd_noalloc(n, H, Hkv, hd, W, R, pos0, dq_.data_ptr(), dk_.data_ptr(), dv_.data_ptr(),
+                                         o.data_ptr(), lse.data_ptr(), n, do_.data_ptr(), dsum.data_ptr(),
+                                         g.data_ptr(), None)
+    assert rc == 0, rc
+    torch.cuda.synchronize()
+    assert T.ttt_kernel_error() == 0
+    got = g.float().cpu().numpy().astype(np.float64)
+    rq, rk, rv = ref_backward(q, kr, vr, dout, n, H, Hkv, hd, W, pos0)
+    for name, a, b in (("dq", got[:, :H * hd], rq), ("dk", got[:, H * hd:(H + Hkv) * hd], rk),
+                       ("dv", got[:, (H + Hkv) * hd:], rv)):
+        err = np.abs(a - b).max() / max(np.abs(b).max(), 1e-6)
+        assert err < 2e-2, (name, err)
