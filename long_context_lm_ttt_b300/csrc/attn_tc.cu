@@ -215,6 +215,9 @@ __global__ void __launch_bounds__(192, 2)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything below reads what earlier kernels wrote
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tS = tmem;          // two 64-column score buffers
   const uint32_t tO = tmem + 128;    // output accumulator (nO columns)
 
@@ -615,6 +618,9 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything below reads what earlier kernels wrote
+  pdl_wait();
+  pdl_trigger();
   // columns: S/P of tile 0 | S/P of tile 1 | O of tile 0 | O of tile 1
 
   if (warp == 0) {
@@ -1031,6 +1037,9 @@ __global__ void __launch_bounds__(576, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything below reads what earlier kernels wrote
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0 && nb > 0) {
@@ -1347,6 +1356,9 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything below reads what earlier kernels wrote
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tS = tmem, tP = tmem + 128, tK = tmem + 256, tV = tmem + 384;
 
   if (warp == 0) {
@@ -1570,6 +1582,8 @@ __global__ void __launch_bounds__(320, 1)
 __global__ void attn_fwd_combine_kernel(const float* __restrict__ ws, const float* __restrict__ ws_ml, int parts,
                                         int n, int H, int hd, bf16* __restrict__ o, int64_t ldo,
                                         float* __restrict__ lse, int ld_lse) {
+  pdl_wait();
+  pdl_trigger();
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= n * H) return;
   const int r = w / H, h = w % H;
@@ -1608,6 +1622,8 @@ __global__ void attn_fwd_combine_kernel(const float* __restrict__ ws, const floa
 // D[h][r] = sum_d dO[r, h*hd + d] * O[r, h*hd + d]; one warp per (r, h)
 __global__ void attn_bwd_prep_tc_kernel(const bf16* __restrict__ dO, const bf16* __restrict__ O, int n, int H,
                                         int hd, float* __restrict__ dsum, int ld) {
+  pdl_wait();
+  pdl_trigger();
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= n * H) return;
   const int r = w / H, h = w % H;
@@ -1628,6 +1644,8 @@ __global__ void attn_bwd_prep_tc_kernel(const bf16* __restrict__ dO, const bf16*
 __global__ void attn_dq_reduce_kernel(const float* __restrict__ ws, int parts, int n, int cols,
                                       bf16* __restrict__ dqkv, int64_t ldg, const float2* __restrict__ cs,
                                       int hd) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = (int64_t)n * cols / 4;
   const int64_t plane = (int64_t)n * cols;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -1655,6 +1673,8 @@ __global__ void attn_dq_reduce_kernel(const float* __restrict__ ws, int parts, i
 // dk rotated back by the RoPE table cs when given
 __global__ void attn_dkv_reduce_kernel(const float* __restrict__ ws, int n, int H, int Hkv, int hd,
                                        bf16* __restrict__ dqkv, int64_t ldg, const float2* __restrict__ cs) {
+  pdl_wait();
+  pdl_trigger();
   const int group = H / Hkv;
   const int64_t total = (int64_t)2 * n * Hkv * hd / 4;
   const int64_t plane = (int64_t)H * n * hd;
@@ -1774,7 +1794,7 @@ int launch_fwd(const AttnArgs& a, int* err, cudaStream_t st) {
   p.parts = 1;
   p.ws = p.ws_ml = nullptr;
   dim3 grid((a.n + BM - 1) / BM, a.H);
-  attn_fwd_tc_kernel<NA><<<grid, 192, SM::SMEM, st>>>(mq, mk, mv, p);
+  launch_k(attn_fwd_tc_kernel<NA>, grid, 192, SM::SMEM, st, mq, mk, mv, p);
   return (int)cudaPeekAtLastError();
 }
 
@@ -1826,11 +1846,11 @@ int launch_fwd2(const AttnArgs& a, int* err, cudaStream_t st, int* kernels) {
     }
   }
   dim3 grid((a.n + 2 * BM - 1) / (2 * BM), a.H, p.parts);
-  attn_fwd2_tc_kernel<NA><<<grid, 320, SM::SMEM, st>>>(mq, mk, mv, p);
+  launch_k(attn_fwd2_tc_kernel<NA>, grid, 320, SM::SMEM, st, mq, mk, mv, p);
   if (kernels) *kernels = p.parts > 1 ? 2 : 1;
   if (p.parts > 1) {
     const int64_t warps = (int64_t)a.n * a.H;
-    attn_fwd_combine_kernel<<<(int)((warps + 7) / 8), 256, 0, st>>>(p.ws, p.ws_ml, p.parts, a.n, a.H, a.hd, p.o,
+    launch_k(attn_fwd_combine_kernel, (int)((warps + 7) / 8), 256, 0, st, p.ws, p.ws_ml, p.parts, a.n, a.H, a.hd, p.o,
                                                                       p.ldo, a.lse, a.ld_lse);
   }
   return (int)cudaPeekAtLastError();
@@ -1904,26 +1924,26 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
   p.cs = a.rope_cs;
   {
     const int warps = a.n * a.H;
-    attn_bwd_prep_tc_kernel<<<(warps + 7) / 8, 256, 0, st>>>((const bf16*)a.dout, (const bf16*)a.out, a.n, a.H,
+    launch_k(attn_bwd_prep_tc_kernel, (warps + 7) / 8, 256, 0, st, (const bf16*)a.dout, (const bf16*)a.out, a.n, a.H,
                                                              a.hd, a.Dsum, a.ld_lse);
   }
   p.parts = split_parts(a, num_sms, BM, DQ_BN, 4, 0.02);
   const int64_t plane = (int64_t)a.n * a.H * a.hd;
   while (p.parts > 1 && (int64_t)p.parts * plane > a.ws_elems) --p.parts;
-  attn_dq_tc_kernel<NA><<<dim3((a.n + BM - 1) / BM, a.H, p.parts), 576, DQ::SMEM, st>>>(mq, mdo, mk128, mv128,
+  launch_k(attn_dq_tc_kernel<NA>, dim3((a.n + BM - 1) / BM, a.H, p.parts), 576, DQ::SMEM, st, mq, mdo, mk128, mv128,
                                                                                         p);
   if (p.parts > 1) {
     const int cols = a.H * a.hd;
     const int64_t quads = plane / 4;
     const int grid = (int)std::min<int64_t>((quads + 255) / 256, (int64_t)num_sms * 8);
-    attn_dq_reduce_kernel<<<grid, 256, 0, st>>>(a.ws, p.parts, a.n, cols, p.dqkv, p.ldg, p.cs, a.hd);
+    launch_k(attn_dq_reduce_kernel, grid, 256, 0, st, a.ws, p.parts, a.n, cols, p.dqkv, p.ldg, p.cs, a.hd);
   }
   // dk / dv (after the dq reduction, which may use the same scratch)
-  attn_dkv_tc_kernel<NA><<<dim3(a.H, (a.n + BM - 1) / BM), 320, DKV::SMEM, st>>>(mq64, mdo64, mk, mv, p);
+  launch_k(attn_dkv_tc_kernel<NA>, dim3(a.H, (a.n + BM - 1) / BM), 320, DKV::SMEM, st, mq64, mdo64, mk, mv, p);
   {
     const int64_t quads = (int64_t)2 * a.n * a.Hkv * a.hd / 4;
     const int grid = (int)std::min<int64_t>((quads + 255) / 256, (int64_t)num_sms * 8);
-    attn_dkv_reduce_kernel<<<grid, 256, 0, st>>>(a.ws, a.n, a.H, a.Hkv, a.hd, p.dqkv, p.ldg, p.cs);
+    launch_k(attn_dkv_reduce_kernel, grid, 256, 0, st, a.ws, a.n, a.H, a.Hkv, a.hd, p.dqkv, p.ldg, p.cs);
   }
   return (int)cudaPeekAtLastError();
 }

@@ -85,6 +85,12 @@ struct Status {
     }                                                                                        \
   } while (0)
 
+// programmatic dependent launch for the launches issued while in scope
+struct PdlScope {
+  explicit PdlScope(bool on) { set_pdl(on); }
+  ~PdlScope() { set_pdl(false); }
+};
+
 // ---------------------------------------------------------------------------
 struct EngineBase {
   ttt_config cfg;
@@ -105,6 +111,11 @@ struct EngineBase {
   // decode state: rows of the current chunk already decoded
   int dec_fill = 0;
   bool dec_graph_off = false;  // capture failed once (or asked): issue steps directly
+  // programmatic dependent launch in ttt_prefill's chunk loop: off by
+  // default (measured slower at 3B / 128K: 2.10 s against 2.06 s per
+  // sequence; kernels waiting at their dependency hold the SMs the
+  // overlapped bulk pass fills otherwise)
+  bool pdl_prefill = false;
   // programmatic dependent launch inside decode steps (off under profiling:
   // the events between launches would serialise them anyway)
   bool pdl_ok = true;
@@ -780,6 +791,10 @@ struct Engine : EngineBase {
   // n rows each, stacked; tok holds the sequences' tokens tok_ld apart.
   void static_fwd(const int32_t* tok, int64_t tok_ld, int64_t s0, int n, int buf, cudaStream_t st, int* rc) {
     const int d = cfg.d_model, hd = cfg.head_dim, lo = cfg.n_layers - cfg.n_ttt_layers;
+    // the bulk pass's kernels launch plainly: launched early, they would
+    // hold SMs (waiting on their predecessor) that the chunk loop needs
+    const bool pdl_was = pdl_enabled();
+    set_pdl(false);
     float2* cs_ = cs_bulk_buf[buf];
     float* xl = x_lo_buf[buf];
     row((double)n * hd * 4, st, [&] { launch_rope_table(s0, n, hd, cfg.rope_theta, cs_, st); });
@@ -795,6 +810,7 @@ struct Engine : EngineBase {
       x = x_out;
     }
     grid_cap = 0;
+    set_pdl(pdl_was);
   }
 
   // fast blocks of positions [s, s+n) from x_in (the output of the static
@@ -998,6 +1014,9 @@ struct Engine : EngineBase {
 
   int prefill(const int32_t* tok, int64_t n_tok, float* losses, cudaStream_t st) override {
     const int b = cfg.chunk;
+    // consecutive kernels on each stream overlap their launch and set-up
+    // with the kernel before (each waits on it before touching memory)
+    PdlScope pdl_scope(pdl_prefill && !prof_on);
     if (used) {
       err = "ttt_prefill needs a fresh or reset context";
       return TTT_ERR_STATE;
@@ -1434,6 +1453,10 @@ extern "C" int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* str
   // decode steps: TTT_DECODE_LAUNCH=graph keeps the captured graphs without
   // programmatic dependent launch, =direct issues every kernel from the
   // host (the same kernels and results; for measuring the launch modes)
+  // TTT_PREFILL_LAUNCH=pdl: programmatic dependent launch in the prefill's
+  // chunk loop (for comparison; the default launches plainly)
+  const char* pl = getenv("TTT_PREFILL_LAUNCH");
+  eng->pdl_prefill = pl && strcmp(pl, "pdl") == 0;
   const char* dl = getenv("TTT_DECODE_LAUNCH");
   eng->pdl_ok = !(dl && (strcmp(dl, "graph") == 0 || strcmp(dl, "direct") == 0));
   eng->dec_graph_off = dl && strcmp(dl, "direct") == 0;

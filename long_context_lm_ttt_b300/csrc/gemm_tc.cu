@@ -183,6 +183,9 @@ __global__ void __launch_bounds__(192, 1)
   if (PAIR) tc::cluster_sync();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything below reads what earlier kernels wrote
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -592,6 +595,8 @@ __global__ void __launch_bounds__(192, 1)
 // Sum of the split-K partials (fixed order) through the epilogue; one thread
 // per (row, 32-column chunk), consecutive threads on consecutive chunks.
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, int M, int N, Epi e) {
+  pdl_wait();
+  pdl_trigger();
   const int nch = (N + 31) / 32;
   const int64_t total = (int64_t)M * nch;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -725,11 +730,13 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
     cfg.blockDim = dim3(192);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
     static std::atomic<int> resident{0};  // per instantiation
@@ -744,18 +751,19 @@ int launch(const GemmArgs<bf16>& g, int num_sms, int* err, cudaStream_t st, int 
     }
     const int pairs = std::max(1, std::min(cap / 2, resident.load()));
     cfg.gridDim = dim3(2 * (nunits < pairs ? nunits : pairs));
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, ma, mb, mb2, ms, mw, mh, ml, g.B2 ? 1 : 0, g.M, g.N, g.K,
                                               g.e, err, splits, g.ws, grouped ? g.group_rows : 0);
     if (le != cudaSuccess) return (int)le;
   } else {
     const int grid = nunits < cap ? nunits : cap;
-    kern<<<grid, 192, C::SMEM, st>>>(ma, mb, mb2, ms, mw, mh, ml, g.B2 ? 1 : 0, g.M, g.N, g.K, g.e, err, splits,
+    launch_k(kern, grid, 192, C::SMEM, st, ma, mb, mb2, ms, mw, mh, ml, g.B2 ? 1 : 0, g.M, g.N, g.K, g.e, err, splits,
                                      g.ws, grouped ? g.group_rows : 0);
   }
   if (splits > 1) {
     const int64_t items = (int64_t)g.M * ((g.N + 31) / 32);
     const int rgrid = (int)std::min<int64_t>((items + 127) / 128, (int64_t)num_sms * 16);
-    splitk_reduce_kernel<<<rgrid, 128, 0, st>>>(g.ws, splits, g.M, g.N, g.e);
+    launch_k(splitk_reduce_kernel, rgrid, 128, 0, st, g.ws, splits, g.M, g.N, g.e);
   }
   return (int)cudaPeekAtLastError();
 }

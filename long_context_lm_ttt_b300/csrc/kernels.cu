@@ -63,6 +63,8 @@ __global__ void embed_kernel(const int32_t* __restrict__ tok, int d, const T* __
 template <typename T>
 __global__ void rmsnorm_fwd_kernel(const float* __restrict__ x, const float* __restrict__ g, int d,
                                    float eps, T* __restrict__ out, float* __restrict__ rr) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sh[32];
   const int r = blockIdx.x;
   const float* xr = x + (int64_t)r * d;
@@ -80,6 +82,8 @@ __global__ void rmsnorm_bwd_kernel(const float* __restrict__ x, const float* __r
                                    const float* __restrict__ rr, const float* __restrict__ dy,
                                    const float* __restrict__ resid, int d, float* __restrict__ out,
                                    T* __restrict__ out_t) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sh[32];
   const int r = blockIdx.x;
   const int64_t o = (int64_t)r * d;
@@ -113,6 +117,8 @@ __global__ void rope_table_kernel(int64_t pos0, const int64_t* pos_dev, int n, i
 
 template <typename T>
 __global__ void rope_bwd_kernel(T* dqkv, int n, int ld, int n_rot_heads, int hd, const float2* cs) {
+  pdl_wait();
+  pdl_trigger();
   const int half = hd >> 1;
   const int64_t total = (int64_t)n * n_rot_heads * half;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -129,6 +135,8 @@ __global__ void rope_bwd_kernel(T* dqkv, int n, int ld, int n_rot_heads, int hd,
 
 __global__ void targets_kernel(const int32_t* tok, int64_t T, int64_t pos0, int n, int32_t* tgt, int V,
                                int* err_tok) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= n) return;
   const int64_t t = pos0 + r + 1;
@@ -144,6 +152,8 @@ template <typename T>
 __global__ void ce_slab_stats_kernel(const float* __restrict__ z, int64_t ldz, int nv,
                                      T* __restrict__ p, int64_t ldp, float* m_run, float* l_run,
                                      float* alpha, float* beta, int first) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sh[32];
   const int r = blockIdx.x;
   const float* zr = z + (int64_t)r * ldz;
@@ -181,6 +191,8 @@ __global__ void ce_finalize_kernel(const float* m_run, const float* l_run, const
                                    const int32_t* tgt, float inv_ntgt, const float* __restrict__ dh_acc,
                                    const T* __restrict__ Wlm, int d, float* __restrict__ dhf,
                                    float* loss_row) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   const int64_t o = (int64_t)r * d;
   const int y = tgt[r];
@@ -200,6 +212,8 @@ __global__ void ce_finalize_kernel(const float* m_run, const float* l_run, const
 
 __global__ void loss_reduce_kernel(const float* loss_row, int n, float inv_ntgt, float* out, int chunk,
                                    int* err_chunk) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sh[32];
   float s = 0.f;
   for (int i = threadIdx.x; i < n; i += blockDim.x) s += loss_row[i];
@@ -380,6 +394,8 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_vec_kernel(const float* __res
                                                               const float* __restrict__ rr, const float* __restrict__ dy,
                                                               const float* __restrict__ resid, int d,
                                                               float* __restrict__ out, bf16* __restrict__ out_t) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sh[32];
   const int r = blockIdx.x;
   const int64_t o = (int64_t)r * d;
@@ -431,6 +447,8 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_vec_kernel(const float* __res
 __global__ void __launch_bounds__(1024) ce_slab_stats_vec_kernel(const float* __restrict__ z, int64_t ldz, int nv,
                                                                  bf16* __restrict__ p, int64_t ldp, float* m_run,
                                                                  float* l_run, float* alpha, float* beta, int first) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sh[32];
   const int r = blockIdx.x;
   const float4* zr = reinterpret_cast<const float4*>(z + (int64_t)r * ldz);
@@ -508,7 +526,7 @@ void launch_rmsnorm_fwd(const float* x, const float* g, int n, int d, float eps,
       return;
     }
   }
-  rmsnorm_fwd_kernel<T><<<n, RB, 0, st>>>(x, g, d, eps, out, r);
+  launch_k(rmsnorm_fwd_kernel<T>, n, RB, 0, st, x, g, d, eps, out, r);
 }
 template <typename T>
 void launch_rmsnorm_bwd(const float* x, const float* g, const float* r, const float* dy,
@@ -518,13 +536,13 @@ void launch_rmsnorm_bwd(const float* x, const float* g, const float* r, const fl
     if (d % 4 == 0 && d <= 3 * 256 * 4 && al16(x) && al16(g) && al16(dy) && al16(out) &&
         (!resid || al16(resid)) && ((uintptr_t)out_t & 7) == 0) {
       const int vpt = (d / 4 + 255) / 256;
-      if (vpt <= 1) rmsnorm_bwd_vec_kernel<1><<<n, 256, 0, st>>>(x, g, r, dy, resid, d, out, (bf16*)out_t);
-      else if (vpt <= 2) rmsnorm_bwd_vec_kernel<2><<<n, 256, 0, st>>>(x, g, r, dy, resid, d, out, (bf16*)out_t);
-      else rmsnorm_bwd_vec_kernel<3><<<n, 256, 0, st>>>(x, g, r, dy, resid, d, out, (bf16*)out_t);
+      if (vpt <= 1) launch_k(rmsnorm_bwd_vec_kernel<1>, n, 256, 0, st, x, g, r, dy, resid, d, out, (bf16*)out_t);
+      else if (vpt <= 2) launch_k(rmsnorm_bwd_vec_kernel<2>, n, 256, 0, st, x, g, r, dy, resid, d, out, (bf16*)out_t);
+      else launch_k(rmsnorm_bwd_vec_kernel<3>, n, 256, 0, st, x, g, r, dy, resid, d, out, (bf16*)out_t);
       return;
     }
   }
-  rmsnorm_bwd_kernel<T><<<n, RB, 0, st>>>(x, g, r, dy, resid, d, out, out_t);
+  launch_k(rmsnorm_bwd_kernel<T>, n, RB, 0, st, x, g, r, dy, resid, d, out, out_t);
 }
 void launch_rope_table(int64_t pos0, int n, int hd, float theta, float2* cs, cudaStream_t st,
                        const int64_t* pos_dev) {
@@ -542,11 +560,11 @@ void launch_decode_tail(DecodeState* s, const float* x, float* xdec, int d, int3
 template <typename T>
 void launch_rope_bwd(T* dqkv, int n, int ld, int n_rot_heads, int hd, const float2* cs, cudaStream_t st) {
   const int64_t total = (int64_t)n * n_rot_heads * (hd / 2);
-  if (total > 0) rope_bwd_kernel<T><<<grid_for(total, 256), 256, 0, st>>>(dqkv, n, ld, n_rot_heads, hd, cs);
+  if (total > 0) launch_k(rope_bwd_kernel<T>, grid_for(total, 256), 256, 0, st, dqkv, n, ld, n_rot_heads, hd, cs);
 }
 void launch_targets(const int32_t* tok, int64_t T, int64_t pos0, int n, int32_t* tgt, int V, int* err_tok,
                     cudaStream_t st) {
-  if (n > 0) targets_kernel<<<(n + 255) / 256, 256, 0, st>>>(tok, T, pos0, n, tgt, V, err_tok);
+  if (n > 0) launch_k(targets_kernel, (n + 255) / 256, 256, 0, st, tok, T, pos0, n, tgt, V, err_tok);
 }
 template <typename T>
 void launch_ce_slab_stats(const float* z, int64_t ldz, int n, int nv, T* p, int64_t ldp, float* m_run,
@@ -554,25 +572,25 @@ void launch_ce_slab_stats(const float* z, int64_t ldz, int n, int nv, T* p, int6
   if (n <= 0) return;
   if constexpr (sizeof(T) == 2) {
     if (nv % 4 == 0 && ldz % 4 == 0 && ldp % 4 == 0 && al16(z) && ((uintptr_t)p & 7) == 0) {
-      ce_slab_stats_vec_kernel<<<n, 1024, 0, st>>>(z, ldz, nv, (bf16*)p, ldp, m_run, l_run, alpha, beta, first);
+      launch_k(ce_slab_stats_vec_kernel, n, 1024, 0, st, z, ldz, nv, (bf16*)p, ldp, m_run, l_run, alpha, beta, first);
       return;
     }
   }
-  ce_slab_stats_kernel<T><<<n, RB, 0, st>>>(z, ldz, nv, p, ldp, m_run, l_run, alpha, beta, first);
+  launch_k(ce_slab_stats_kernel<T>, n, RB, 0, st, z, ldz, nv, p, ldp, m_run, l_run, alpha, beta, first);
 }
 template <typename T>
 void launch_ce_finalize(int n, const float* m_run, const float* l_run, const float* ztgt,
                         const int32_t* tgt, float inv_ntgt, const float* dh_acc, const T* Wlm, int d,
                         float* dhf, float* loss_row, cudaStream_t st) {
   if (n > 0)
-    ce_finalize_kernel<T><<<n, RB, 0, st>>>(m_run, l_run, ztgt, tgt, inv_ntgt, dh_acc, Wlm, d, dhf, loss_row);
+    launch_k(ce_finalize_kernel<T>, n, RB, 0, st, m_run, l_run, ztgt, tgt, inv_ntgt, dh_acc, Wlm, d, dhf, loss_row);
 }
 void launch_argmax(const float* z, int V, int32_t* out, cudaStream_t st) {
   argmax_kernel<<<1, 1024, 0, st>>>(z, V, out);
 }
 void launch_loss_reduce(const float* loss_row, int n, float inv_ntgt, float* out, int chunk, int* err_chunk,
                         cudaStream_t st) {
-  loss_reduce_kernel<<<1, RB, 0, st>>>(loss_row, n, inv_ntgt, out, chunk, err_chunk);
+  launch_k(loss_reduce_kernel, 1, RB, 0, st, loss_row, n, inv_ntgt, out, chunk, err_chunk);
 }
 template <typename T>
 void launch_pack(const float* src, int64_t rows, int64_t cols, int mode, int hd, T* dst, cudaStream_t st) {
