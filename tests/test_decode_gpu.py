@@ -262,3 +262,40 @@ def test_decode_graph_replay_is_bitwise_direct_issue(precision):
     for fa, fb in zip(af, bf):
         for k in O.FAST:
             assert np.array_equal(fa[k], fb[k])
+
+
+def test_decode_3b_widths_after_prefill():
+    """Decode at the 3B widths (d 3072, 24 query / 8 KV heads x 128, d_ff
+    8192, V 128256) after a two-chunk prefill, through a completed chunk and
+    into greedy picks: the one-row products at these widths (the lm_head
+    with the fused greedy pick among them), the bulk-copy one-query
+    attention with three query heads per KV head, the graph replay and the
+    chunk's test-time step.  Two blocks, one fast; chunks of 128 and a
+    window of 300 keep the oracle's run short."""
+    s = inputs.shape("3b-4layer", n_layers=2, n_ttt_layers=1, chunk=128, window=300, seq_len=512)
+    w, tok = inputs.make_weights(s), inputs.make_tokens(s)
+    b = s.chunk
+    P, N, n_given = 2 * b, b + 6, b - 10  # greedy from step n_given - 1 on
+    T, m = _model(s, w, "bf16", P + N + 1)
+    try:
+        pl = m.prefill(np.ascontiguousarray(tok[:P], np.int32))
+        out, dl = m.decode(np.ascontiguousarray(tok[P:P + n_given], np.int32), N)
+        fast = [m.fast_weights(i) for i in range(s.n_ttt_layers)]
+    finally:
+        m.close()
+    assert np.array_equal(out[:n_given], tok[P:P + n_given])
+    assert out.min() >= 0 and out.max() < s.vocab
+    cfg = O.OracleConfig.from_mapping(s.as_dict())
+    rp = O.prefill(cfg, w, tok[:P], return_state=True)
+    r = O.decode(cfg, w, out, N, state=rp["state"])  # the GPU's tokens, teacher-forced
+    np.testing.assert_allclose(pl, rp["losses"], rtol=TOL["bf16"])
+    for i in range(n_given - 1, N):
+        z = r["logits"][i]
+        assert z[out[i + 1]] >= z.max() - MARGIN["bf16"] * np.abs(z).max(), (i, out[i + 1], z.argmax())
+    _check_losses_weights(dl[:1], fast, r, TOL["bf16"])
+    # the updates themselves (prefill and decode chunks), not only the
+    # weights they were added to
+    L = s.n_layers
+    for k in O.FAST:
+        w0 = np.asarray(w["layers"][L - 1][k], np.float64)
+        assert rel_fro(fast[0][k] - w0, r["fast"][0][k] - w0) <= TOL["bf16"], k
