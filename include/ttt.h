@@ -193,7 +193,16 @@ int ttt_prefill_batch(ttt_ctx* const* ctxs, int32_t n_ctx, const int32_t* const*
  * of b: a fresh or reset context, or after ttt_prefill of a multiple of b
  * tokens), else STATE; pos + n_steps <= max_tokens, else SHAPE.  A non-finite
  * chunk loss returns NONFINITE with its index within this call.  Returns
- * after the work has completed on `stream`; pos advances by n_steps. */
+ * after the work has completed on `stream`; pos advances by n_steps.
+ * The steps' position and tokens live in device memory, so the first step
+ * of each kind (next input given, or greedy) is issued kernel by kernel and
+ * recorded into a CUDA graph on a stream the context owns; later steps, in
+ * this and later calls, replay that graph on `stream`.  The chunk's
+ * test-time step is always issued kernel by kernel.  Do not call ttt_decode
+ * while a stream capture is active on the calling thread.  Environment
+ * TTT_DECODE_LAUNCH (read at ttt_create): "graph" replays graphs without
+ * programmatic dependent launch between their kernels, "direct" issues every
+ * step kernel by kernel; results are the same in every mode. */
 int ttt_decode(ttt_ctx* ctx, const int32_t* tokens, int64_t n_given, int64_t n_steps, int32_t* tokens_out,
                float* chunk_losses, void* stream);
 
