@@ -128,7 +128,12 @@ typedef struct ttt_ctx ttt_ctx;
  * weights (bf16 by round-to-nearest-even in TTT_BF16 mode), and return the
  * context in *out.  The context is fresh: position 0, initial fast weights.
  * Errors: INVALID (null args, bad enum), SHAPE (unsupported sizes), OOM,
- * CUDA.  On error *out is NULL and nothing is leaked. */
+ * CUDA.  On error *out is NULL and nothing is leaked.
+ * Environment, read here, for cross-checks and measurement only (results
+ * are those of the method in every setting): TTT_GEMM_IMPL=simt and
+ * TTT_ATTN_IMPL=simt keep the products / the attention on SIMT kernels;
+ * TTT_PREFILL_LAUNCH=pdl launches ttt_prefill's chunk loop with
+ * programmatic dependent launch; TTT_DECODE_LAUNCH as under ttt_decode. */
 int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* stream, ttt_ctx** out);
 
 /* The test-time inner loop over tokens[0..T) (int32 ids in [0, V)).
