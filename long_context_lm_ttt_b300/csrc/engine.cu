@@ -116,6 +116,8 @@ struct EngineBase {
   // sequence; kernels waiting at their dependency hold the SMs the
   // overlapped bulk pass fills otherwise)
   bool pdl_prefill = false;
+  // the chunk loop's weight updates on their own stream (ttt_prefill)
+  bool sgd_side_ok = true;
   // programmatic dependent launch inside decode steps (off under profiling:
   // the events between launches would serialise them anyway)
   bool pdl_ok = true;
@@ -204,10 +206,12 @@ struct Engine : EngineBase {
   DeviceArena mem;
   ~Engine() override {
     cudaDeviceSynchronize();
-    for (cudaEvent_t e : {ev_fork, ev_a[0], ev_a[1], ev_b[0], ev_b[1], ev_join_a, ev_join_b})
+    for (cudaEvent_t e : {ev_fork, ev_a[0], ev_a[1], ev_b[0], ev_b[1], ev_join_a, ev_join_b, ev_sgd_fork,
+                          ev_sgd_join[0], ev_sgd_join[1]})
       if (e) cudaEventDestroy(e);
     if (sa) cudaStreamDestroy(sa);
     if (sb) cudaStreamDestroy(sb);
+    if (sc) cudaStreamDestroy(sc);
     for (cudaGraphExec_t& g : dec_graph)
       if (g) cudaGraphExecDestroy(g);
     if (cap_st) cudaStreamDestroy(cap_st);
@@ -261,6 +265,11 @@ struct Engine : EngineBase {
   float* x_lo = nullptr;                        // buffers of the span being processed
   float2* cs_bulk = nullptr;
   cudaStream_t sa = nullptr, sb = nullptr;
+  // the chunk loop's weight updates run on sc, beside the backward of the
+  // layers below (ttt_prefill only; see backward())
+  cudaStream_t sc = nullptr;
+  cudaEvent_t ev_sgd_fork = nullptr, ev_sgd_join[2] = {nullptr, nullptr};
+  bool sgd_side = false;
   cudaEvent_t ev_fork = nullptr, ev_a[2] = {nullptr, nullptr}, ev_b[2] = {nullptr, nullptr},
               ev_join_a = nullptr, ev_join_b = nullptr;
   int grid_cap = 0;  // CTA cap of tensor-core GEMMs (0: one per SM, persistent)
@@ -278,6 +287,10 @@ struct Engine : EngineBase {
   T* p_slab = nullptr;
   float *dy = nullptr, *dhn = nullptr, *dh = nullptr, *dxn = nullptr, *Dsum = nullptr;
   T *dy_t = nullptr, *dgu = nullptr, *dh_t = nullptr, *dO = nullptr, *dqkv = nullptr;
+  // second copies of dy_t and dgu: layers alternate between the two, so a
+  // layer's weight updates (on sc) may still read theirs during the next
+  // layer's backward (allocated for ttt_prefill with 2+ fast blocks)
+  T *dy_t2 = nullptr, *dgu2 = nullptr;
   // dual_mlp: the static MLP's normed input and activation (forward
   // temporaries) and the gradient at its input (backward)
   T *hn2 = nullptr, *a2 = nullptr, *dy2_t = nullptr;
@@ -494,7 +507,9 @@ struct Engine : EngineBase {
       CU_TRY(cudaDeviceGetStreamPriorityRange(&lo_pri, &hi_pri));
       CU_TRY(cudaStreamCreateWithPriority(&sa, cudaStreamNonBlocking, lo_pri));
       CU_TRY(cudaStreamCreateWithPriority(&sb, cudaStreamNonBlocking, hi_pri));
-      for (cudaEvent_t* e : {&ev_fork, &ev_a[0], &ev_a[1], &ev_b[0], &ev_b[1], &ev_join_a, &ev_join_b})
+      CU_TRY(cudaStreamCreateWithPriority(&sc, cudaStreamNonBlocking, (lo_pri + hi_pri) / 2));
+      for (cudaEvent_t* e : {&ev_fork, &ev_a[0], &ev_a[1], &ev_b[0], &ev_b[1], &ev_join_a, &ev_join_b, &ev_sgd_fork,
+                             &ev_sgd_join[0], &ev_sgd_join[1]})
         CU_TRY(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
     }
     fstash.resize(Lt);
@@ -524,6 +539,10 @@ struct Engine : EngineBase {
     A_TRY(dy, (size_t)rows * d);
     A_TRY(dy_t, (size_t)rows * d);
     A_TRY(dgu, (size_t)rows * 2 * ff);
+    if (Lt > 1 && !cfg.dual_mlp) {
+      A_TRY(dy_t2, (size_t)rows * d);
+      A_TRY(dgu2, (size_t)rows * 2 * ff);
+    }
     A_TRY(dhn, (size_t)rows * d);
     A_TRY(dh, (size_t)rows * d);
     A_TRY(dh_t, (size_t)rows * d);
@@ -897,33 +916,45 @@ struct Engine : EngineBase {
     const int lo = L - Lt;
     const int64_t Hhd = (int64_t)H * hd;
     const int rows = nseq * n;
-    row((double)rows * d * (12 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(xs[Lt], g_final, rf, dhf, nullptr, rows, d, dy, dy_t, st); });
+    // With sgd_side, each layer's weight updates run on sc (see below).
+    // deep: dy_t and dgu alternate between two buffers by layer, so the
+    // updates of layer l may run on through layer l - 1's backward, and the
+    // chunk loop waits for them only before layer l - 1's last norm backward
+    // writes their dy_t buffer again; otherwise it waits before layer l's.
+    const bool side = sgd_side && !prof_on;
+    const bool deep = side && dy_t2 && dgu2;
+    T* const dyt[2] = {dy_t, deep ? dy_t2 : dy_t};
+    T* const dgub[2] = {dgu, deep ? dgu2 : dgu};
+    int cur = 0;                         // this layer's dy_t / dgu buffer
+    bool pending[2] = {false, false};    // updates on sc not yet waited for, by buffer
+    row((double)rows * d * (12 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(xs[Lt], g_final, rf, dhf, nullptr, rows, d, dy, dyt[cur], st); });
     for (int l = L - 1; l >= lo; --l) {
       Stash& S = fstash[l - lo];
       Layer& y = layers[l];
+      T* const dgu_l = dgub[cur];
       // gradient at the fast MLP's output: dy, or with dual_mlp the one at
       // the static second MLP's input h2 = dy + n'(h2)^T ([dg2 du2] [Wg2; Wu2])
       float* gy = dy;
-      T* gy_t = dy_t;
+      T* gy_t = dyt[cur];
       if (cfg.dual_mlp) {
         Epi e2 = epi(EPI_SWIGLU_BWD);
-        e2.out = dgu;
+        e2.out = dgu_l;
         e2.ldo = 2 * (int64_t)ff;
         e2.stash = S.gu2;
         e2.ld_stash = 2 * (int64_t)ff;
-        gemm(rows, ff, d, dy_t, d, 0, y.wd2, ff, 1, e2, st, rc);
+        gemm(rows, ff, d, dyt[cur], d, 0, y.wd2, ff, 1, e2, st, rc);
         e2 = epi(EPI_STORE);
         e2.out_f32 = 1;
         e2.out = dhn;
         e2.ldo = d;
-        gemm(rows, d, 2 * ff, dgu, 2 * (int64_t)ff, 0, y.wgu2, d, 1, e2, st, rc);
+        gemm(rows, d, 2 * ff, dgu_l, 2 * (int64_t)ff, 0, y.wgu2, d, 1, e2, st, rc);
         row((double)rows * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.h2, y.g_mlp2, S.r3, dhn, dy, rows, d, dy2, dy2_t, st); });
         gy = dy2;
         gy_t = dy2_t;
       }
       // da = dy Wd  ->  (dg, du) with the stashed (g, u)
       Epi e = epi(EPI_SWIGLU_BWD);
-      e.out = dgu;
+      e.out = dgu_l;
       e.ldo = 2 * (int64_t)ff;
       e.stash = S.gu;
       e.ld_stash = 2 * (int64_t)ff;
@@ -934,9 +965,22 @@ struct Engine : EngineBase {
         e.out_f32 = 1;
         e.out = dhn;
         e.ldo = d;
-        gemm(rows, d, 2 * ff, dgu, 2 * (int64_t)ff, 0, y.wgu, d, 1, e, st, rc, nullptr, nseq, y.gu_elems);
+        gemm(rows, d, 2 * ff, dgu_l, 2 * (int64_t)ff, 0, y.wgu, d, 1, e, st, rc, nullptr, nseq, y.gu_elems);
       }
-      // per sequence: Wd -= lr dy^T a ;  [Wg;Wu] -= lr [dg du]^T hn
+      // per sequence: Wd -= lr dy^T a ;  [Wg;Wu] -= lr [dg du]^T hn.
+      // Nothing after this point reads this layer's fast weights, so with
+      // sgd_side the updates run on sc beside the layer's remaining backward
+      // (norm, o-proj and attention backward, the QKV product), whose
+      // partial waves leave SMs free; they read only dy_t / dy2_t, dgu and
+      // the stash, which nothing rewrites before the wait described above.
+      // One CTA per tile, so that the chunk loop's own CTAs get SMs back
+      // soon.
+      cudaStream_t su = side ? sc : st;
+      if (side) {
+        cudaEventRecord(ev_sgd_fork, st);
+        cudaStreamWaitEvent(sc, ev_sgd_fork, 0);
+        grid_cap = INT_MAX;
+      }
       for (int q = 0; q < nseq; ++q) {
         const int64_t r0 = (int64_t)q * n;
         e = epi(EPI_SGD);
@@ -945,14 +989,23 @@ struct Engine : EngineBase {
         e.w16lo = y.wd_lo ? y.wd_lo + q * y.d_elems : nullptr;
         e.ldo = ff;
         e.lr = cfg.lr;
-        gemm(d, ff, n, gy_t + r0 * d, d, 1, S.a + r0 * ff, ff, 1, e, st, rc);
+        gemm(d, ff, n, gy_t + r0 * d, d, 1, S.a + r0 * ff, ff, 1, e, su, rc);
         e.w32 = y.wgu32 + q * y.gu_elems;
         e.w16 = kBF16 ? (void*)(y.wgu + q * y.gu_elems) : nullptr;
         e.w16lo = y.wgu_lo ? y.wgu_lo + q * y.gu_elems : nullptr;
         e.ldo = d;
-        gemm(2 * ff, d, n, dgu + r0 * 2 * ff, 2 * (int64_t)ff, 1, S.hn + r0 * d, d, 1, e, st, rc);
+        gemm(2 * ff, d, n, dgu_l + r0 * 2 * ff, 2 * (int64_t)ff, 1, S.hn + r0 * d, d, 1, e, su, rc);
       }
-      if (l == lo) break;
+      if (side) {
+        grid_cap = 0;
+        cudaEventRecord(ev_sgd_join[cur], sc);
+        pending[cur] = true;
+      }
+      if (l == lo) {
+        for (int k = 0; k < 2; ++k)
+          if (pending[k]) cudaStreamWaitEvent(st, ev_sgd_join[k], 0);
+        break;
+      }
       // through the MLP norm and the residual
       row((double)rows * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.h, y.g_mlp, S.r2, dhn, gy, rows, d, dh, dh_t, st); });
       // dO = dh Wo
@@ -982,7 +1035,15 @@ struct Engine : EngineBase {
       e.out = dxn;
       e.ldo = d;
       gemm(rows, d, qkv_cols, dqkv, qkv_cols, 0, y.wqkv, d, 1, e, st, rc);
-      row((double)rows * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.x, y.g_attn, S.r1, dxn, dh, rows, d, dy, dy_t, st); });
+      // the next layer's dy_t buffer: its last reader (updates of the layer
+      // above, deep, or of this layer) must be done
+      const int nxt = deep ? 1 - cur : cur;
+      if (pending[nxt]) {
+        cudaStreamWaitEvent(st, ev_sgd_join[nxt], 0);
+        pending[nxt] = false;
+      }
+      row((double)rows * d * (16 + sizeof(T)), st, [&] { launch_rmsnorm_bwd<T>(S.x, y.g_attn, S.r1, dxn, dh, rows, d, dy, dyt[nxt], st); });
+      cur = nxt;
     }
   }
 
@@ -1087,7 +1148,11 @@ struct Engine : EngineBase {
         }
         // without fast blocks the chunk loop only scores the chunk
         cross_entropy(tok_d, n_tok, s, n, n_tgt, loss_d, c, s_loop, &rc, cfg.n_ttt_layers > 0, ns, n_tok, nC);
-        if (cfg.n_ttt_layers > 0) backward(s, n, s_loop, &rc, ns);
+        if (cfg.n_ttt_layers > 0) {
+          sgd_side = sgd_side_ok;
+          backward(s, n, s_loop, &rc, ns);
+          sgd_side = false;
+        }
         CU_TRY(cudaPeekAtLastError());
       }
       CU_TRY(cudaEventRecord(ev_b[k & 1], s_loop));
@@ -1453,6 +1518,10 @@ extern "C" int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* str
   // decode steps: TTT_DECODE_LAUNCH=graph keeps the captured graphs without
   // programmatic dependent launch, =direct issues every kernel from the
   // host (the same kernels and results; for measuring the launch modes)
+  // TTT_PREFILL_UPDATES=inline: the prefill's weight updates on the chunk
+  // loop's stream (for comparison)
+  const char* pu = getenv("TTT_PREFILL_UPDATES");
+  eng->sgd_side_ok = !(pu && strcmp(pu, "inline") == 0);
   // TTT_PREFILL_LAUNCH=pdl: programmatic dependent launch in the prefill's
   // chunk loop (for comparison; the default launches plainly)
   const char* pl = getenv("TTT_PREFILL_LAUNCH");
