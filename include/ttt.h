@@ -133,7 +133,9 @@ typedef struct ttt_ctx ttt_ctx;
  * are those of the method in every setting): TTT_GEMM_IMPL=simt and
  * TTT_ATTN_IMPL=simt keep the products / the attention on SIMT kernels;
  * TTT_PREFILL_LAUNCH=pdl launches ttt_prefill's chunk loop with
- * programmatic dependent launch; TTT_DECODE_LAUNCH as under ttt_decode. */
+ * programmatic dependent launch; TTT_PREFILL_UPDATES=inline keeps its
+ * weight updates on the chunk loop's stream; TTT_DECODE_LAUNCH as under
+ * ttt_decode. */
 int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* stream, ttt_ctx** out);
 
 /* The test-time inner loop over tokens[0..T) (int32 ids in [0, V)).
@@ -153,9 +155,10 @@ int ttt_create(const ttt_config* cfg, const ttt_weights* w, void* stream, ttt_ct
  * `stream`.  A NaN/Inf chunk loss returns NONFINITE with the first such
  * chunk index in ttt_last_error(); the context is then left as is.  After
  * success the context holds the final fast weights and the ring at
- * position T.  Internally the call forks two streams from `stream`: one
- * runs the frozen blocks' bulk pass a super-chunk ahead, the other the
- * chunk loop; both join back into `stream` before the call returns. */
+ * position T.  Internally the call forks streams from `stream`: one runs
+ * the frozen blocks' bulk pass a super-chunk ahead, one the chunk loop, and
+ * one the chunk loop's weight updates beside the backward of the layers
+ * below; all join back into `stream` before the call returns. */
 int ttt_prefill(ttt_ctx* ctx, const int32_t* tokens, int64_t T, float* chunk_losses,
                 void* stream);
 
