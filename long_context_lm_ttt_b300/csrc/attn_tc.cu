@@ -1877,8 +1877,9 @@ int attn_fwd_tc(const AttnArgs& a, int* err, cudaStream_t st, int variant, int* 
 
 int64_t attn_bwd_tc_ws_elems(int n, int H, int hd, int num_sms) {
   (void)num_sms;
-  const int64_t plane = (int64_t)n * H * hd;
-  return std::max<int64_t>(4 * plane, 2 * plane);
+  // up to 4 planes of dq key-range partials, then 2 of dk / dv partials
+  // (dk/dv beside dq); 2 planes are the least the kernels need
+  return (int64_t)6 * n * H * hd;
 }
 
 template <int NA>
@@ -1930,6 +1931,18 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
   p.parts = split_parts(a, num_sms, BM, DQ_BN, 4, 0.02);
   const int64_t plane = (int64_t)a.n * a.H * a.hd;
   while (p.parts > 1 && (int64_t)p.parts * plane > a.ws_elems) --p.parts;
+  // dk / dv beside dq on a.side when the scratch holds its two planes after
+  // dq's parts (the two kernel pairs share only the prep's D and write
+  // disjoint columns of dqkv)
+  const int dq_planes = p.parts > 1 ? p.parts : 0;
+  const bool beside = a.side && a.side_ev[0] && a.side_ev[1] && (int64_t)(dq_planes + 2) * plane <= a.ws_elems;
+  cudaStream_t sk = beside ? a.side : st;
+  BwdParams pk = p;
+  if (beside) {
+    pk.ws = a.ws + (int64_t)dq_planes * plane;
+    cudaEventRecord(a.side_ev[0], st);
+    cudaStreamWaitEvent(a.side, a.side_ev[0], 0);
+  }
   launch_k(attn_dq_tc_kernel<NA>, dim3((a.n + BM - 1) / BM, a.H, p.parts), 576, DQ::SMEM, st, mq, mdo, mk128, mv128,
                                                                                         p);
   if (p.parts > 1) {
@@ -1938,12 +1951,17 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
     const int grid = (int)std::min<int64_t>((quads + 255) / 256, (int64_t)num_sms * 8);
     launch_k(attn_dq_reduce_kernel, grid, 256, 0, st, a.ws, p.parts, a.n, cols, p.dqkv, p.ldg, p.cs, a.hd);
   }
-  // dk / dv (after the dq reduction, which may use the same scratch)
-  launch_k(attn_dkv_tc_kernel<NA>, dim3(a.H, (a.n + BM - 1) / BM), 320, DKV::SMEM, st, mq64, mdo64, mk, mv, p);
+  // dk / dv: beside dq, or after the dq reduction (which may then use the
+  // same scratch)
+  launch_k(attn_dkv_tc_kernel<NA>, dim3(a.H, (a.n + BM - 1) / BM), 320, DKV::SMEM, sk, mq64, mdo64, mk, mv, pk);
   {
     const int64_t quads = (int64_t)2 * a.n * a.Hkv * a.hd / 4;
     const int grid = (int)std::min<int64_t>((quads + 255) / 256, (int64_t)num_sms * 8);
-    launch_k(attn_dkv_reduce_kernel, grid, 256, 0, st, a.ws, a.n, a.H, a.Hkv, a.hd, p.dqkv, p.ldg, p.cs);
+    launch_k(attn_dkv_reduce_kernel, grid, 256, 0, sk, pk.ws, a.n, a.H, a.Hkv, a.hd, p.dqkv, p.ldg, p.cs);
+  }
+  if (beside) {
+    cudaEventRecord(a.side_ev[1], a.side);
+    cudaStreamWaitEvent(st, a.side_ev[1], 0);
   }
   return (int)cudaPeekAtLastError();
 }
@@ -1951,7 +1969,7 @@ int launch_bwd(const AttnArgs& a, int* err, cudaStream_t st, int num_sms) {
 bool attn_bwd_tc_supported(const AttnArgs& a) {
   return attn_tc_supported(a) && a.pos0 % BN == 0 && ((uintptr_t)a.dout & 15) == 0 &&
          ((uintptr_t)a.dqkv & 15) == 0 && a.ws != nullptr &&
-         a.ws_elems >= attn_bwd_tc_ws_elems(a.n, a.H, a.hd, 0) / 2;
+         a.ws_elems >= (int64_t)2 * a.n * a.H * a.hd;
 }
 
 int attn_bwd_tc(const AttnArgs& a, int* err, cudaStream_t st) {

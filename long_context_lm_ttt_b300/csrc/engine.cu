@@ -207,8 +207,9 @@ struct Engine : EngineBase {
   ~Engine() override {
     cudaDeviceSynchronize();
     for (cudaEvent_t e : {ev_fork, ev_a[0], ev_a[1], ev_b[0], ev_b[1], ev_join_a, ev_join_b, ev_sgd_fork,
-                          ev_sgd_join[0], ev_sgd_join[1]})
+                          ev_sgd_join[0], ev_sgd_join[1], ev_dkv[0], ev_dkv[1]})
       if (e) cudaEventDestroy(e);
+    if (sd) cudaStreamDestroy(sd);
     if (sa) cudaStreamDestroy(sa);
     if (sb) cudaStreamDestroy(sb);
     if (sc) cudaStreamDestroy(sc);
@@ -269,6 +270,9 @@ struct Engine : EngineBase {
   // layers below (ttt_prefill only; see backward())
   cudaStream_t sc = nullptr;
   cudaEvent_t ev_sgd_fork = nullptr, ev_sgd_join[2] = {nullptr, nullptr};
+  // and the attention backward's dk/dv kernels on sd, beside its dq kernels
+  cudaStream_t sd = nullptr;
+  cudaEvent_t ev_dkv[2] = {nullptr, nullptr};
   bool sgd_side = false;
   cudaEvent_t ev_fork = nullptr, ev_a[2] = {nullptr, nullptr}, ev_b[2] = {nullptr, nullptr},
               ev_join_a = nullptr, ev_join_b = nullptr;
@@ -508,8 +512,9 @@ struct Engine : EngineBase {
       CU_TRY(cudaStreamCreateWithPriority(&sa, cudaStreamNonBlocking, lo_pri));
       CU_TRY(cudaStreamCreateWithPriority(&sb, cudaStreamNonBlocking, hi_pri));
       CU_TRY(cudaStreamCreateWithPriority(&sc, cudaStreamNonBlocking, (lo_pri + hi_pri) / 2));
+      CU_TRY(cudaStreamCreateWithPriority(&sd, cudaStreamNonBlocking, hi_pri));
       for (cudaEvent_t* e : {&ev_fork, &ev_a[0], &ev_a[1], &ev_b[0], &ev_b[1], &ev_join_a, &ev_join_b, &ev_sgd_fork,
-                             &ev_sgd_join[0], &ev_sgd_join[1]})
+                             &ev_sgd_join[0], &ev_sgd_join[1], &ev_dkv[0], &ev_dkv[1]})
         CU_TRY(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
     }
     fstash.resize(Lt);
@@ -1023,6 +1028,11 @@ struct Engine : EngineBase {
         a.ws = attn_ws;
         a.ws_elems = attn_ws_elems;
         a.rope_cs = cs_cur;
+        if (side) {  // ttt_prefill's chunk loop: dk/dv beside dq
+          a.side = sd;
+          a.side_ev[0] = ev_dkv[0];
+          a.side_ev[1] = ev_dkv[1];
+        }
         // the tensor-core backward rotates dq, dk back as it writes them
         if (!attn_bwd(a, st, rc))
           row((double)n * (H + Hkv) * hd * 2 * sizeof(T), st, [&] {

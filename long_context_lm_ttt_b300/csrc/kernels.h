@@ -212,6 +212,12 @@ struct AttnArgs {
   // when set, dq and dk leave the kernels already rotated back (the
   // transpose of the forward rotation), so no separate pass is needed
   const float2* rope_cs;
+  // tensor-core backward: with side set, the dk/dv kernels run on that
+  // stream beside the dq kernels (side_ev[0] forks it after the shared
+  // prep, side_ev[1] joins it back), when the scratch also holds the dk/dv
+  // partials next to dq's
+  cudaStream_t side;
+  cudaEvent_t side_ev[2];
 };
 template <typename T> void attn_fwd_simt(const AttnArgs& a, cudaStream_t st);
 // one query position (n == 1, a decode step): key range split into `splits`
