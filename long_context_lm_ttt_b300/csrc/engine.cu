@@ -267,7 +267,8 @@ struct Engine : EngineBase {
   float2* cs_bulk = nullptr;
   cudaStream_t sa = nullptr, sb = nullptr;
   // the chunk loop's weight updates run on sc, beside the backward of the
-  // layers below (ttt_prefill only; see backward())
+  // layers below (ttt_prefill only; see backward()), at the chunk loop's
+  // priority: a chunk's backward ends waiting for its last updates
   cudaStream_t sc = nullptr;
   cudaEvent_t ev_sgd_fork = nullptr, ev_sgd_join[2] = {nullptr, nullptr};
   // and the attention backward's dk/dv kernels on sd, beside its dq kernels
@@ -511,7 +512,7 @@ struct Engine : EngineBase {
       CU_TRY(cudaDeviceGetStreamPriorityRange(&lo_pri, &hi_pri));
       CU_TRY(cudaStreamCreateWithPriority(&sa, cudaStreamNonBlocking, lo_pri));
       CU_TRY(cudaStreamCreateWithPriority(&sb, cudaStreamNonBlocking, hi_pri));
-      CU_TRY(cudaStreamCreateWithPriority(&sc, cudaStreamNonBlocking, (lo_pri + hi_pri) / 2));
+      CU_TRY(cudaStreamCreateWithPriority(&sc, cudaStreamNonBlocking, hi_pri));
       CU_TRY(cudaStreamCreateWithPriority(&sd, cudaStreamNonBlocking, hi_pri));
       for (cudaEvent_t* e : {&ev_fork, &ev_a[0], &ev_a[1], &ev_b[0], &ev_b[1], &ev_join_a, &ev_join_b, &ev_sgd_fork,
                              &ev_sgd_join[0], &ev_sgd_join[1], &ev_dkv[0], &ev_dkv[1]})
