@@ -225,53 +225,6 @@ __global__ void loss_reduce_kernel(const float* loss_row, int n, float inv_ntgt,
   }
 }
 
-// greedy next token: the index of the largest logit (the smallest such
-// index on ties; NaN logits never win)
-__global__ void argmax_kernel(const float* __restrict__ z, int V, int32_t* out) {
-  __shared__ float sv[32];
-  __shared__ int si[32];
-  float best = -INFINITY;
-  int bi = V;
-  for (int i = threadIdx.x; i < V; i += blockDim.x) {
-    const float v = z[i];
-    if (v > best) {
-      best = v;
-      bi = i;
-    }
-  }
-  // warp, then block: the larger value wins, the smaller index on equal ones
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (ov > best || (ov == best && oi < bi)) {
-      best = ov;
-      bi = oi;
-    }
-  }
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) {
-    sv[w] = best;
-    si[w] = bi;
-  }
-  __syncthreads();
-  if (w == 0) {
-    const int nw = blockDim.x >> 5;
-    best = l < nw ? sv[l] : -INFINITY;
-    bi = l < nw ? si[l] : V;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > best || (ov == best && oi < bi)) {
-        best = ov;
-        bi = oi;
-      }
-    }
-    if (l == 0) *out = bi < V ? bi : 0;
-  }
-}
-
 __global__ void decode_begin_kernel(DecodeState* s, int64_t pos, int r, const int32_t* given, int n_given,
                                     int32_t* out, unsigned long long* pick) {
   if (threadIdx.x != 0) return;
@@ -327,12 +280,6 @@ __global__ void pack_kernel(const float* __restrict__ src, int64_t rows, int64_t
     const int64_t r = idx / cols, c = idx % cols;
     dst[map_row(r, mode, hd) * cols + c] = from_f<T>(src[idx]);
   }
-}
-
-__global__ void f32_to_bf16_kernel(const float* __restrict__ src, int64_t n, bf16* __restrict__ dst) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x)
-    dst[i] = __float2bfloat16_rn(src[i]);
 }
 
 __global__ void split_bf16_kernel(const float* __restrict__ w, int64_t n, bf16* __restrict__ hi,
@@ -585,9 +532,6 @@ void launch_ce_finalize(int n, const float* m_run, const float* l_run, const flo
   if (n > 0)
     launch_k(ce_finalize_kernel<T>, n, RB, 0, st, m_run, l_run, ztgt, tgt, inv_ntgt, dh_acc, Wlm, d, dhf, loss_row);
 }
-void launch_argmax(const float* z, int V, int32_t* out, cudaStream_t st) {
-  argmax_kernel<<<1, 1024, 0, st>>>(z, V, out);
-}
 void launch_loss_reduce(const float* loss_row, int n, float inv_ntgt, float* out, int chunk, int* err_chunk,
                         cudaStream_t st) {
   launch_k(loss_reduce_kernel, 1, RB, 0, st, loss_row, n, inv_ntgt, out, chunk, err_chunk);
@@ -599,9 +543,6 @@ void launch_pack(const float* src, int64_t rows, int64_t cols, int mode, int hd,
 }
 void launch_split_bf16(const float* w, int64_t n, bf16* hi, bf16* lo, cudaStream_t st) {
   if (n > 0) split_bf16_kernel<<<grid_for(n, 256), 256, 0, st>>>(w, n, hi, lo);
-}
-void launch_f32_to_bf16(const float* src, int64_t n, bf16* dst, cudaStream_t st) {
-  if (n > 0) f32_to_bf16_kernel<<<grid_for(n, 256), 256, 0, st>>>(src, n, dst);
 }
 
 #define INST(T)                                                                                         \

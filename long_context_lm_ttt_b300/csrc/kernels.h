@@ -139,8 +139,6 @@ void launch_rope_bwd(T* dqkv, int n, int ld, int n_rot_heads, int hd, const floa
                      cudaStream_t st);
 void launch_targets(const int32_t* tok, int64_t T, int64_t pos0, int n, int32_t* tgt, int V,
                     int* err_tok, cudaStream_t st);
-// out[0] = the index of the largest of z[0..V) (smallest index on ties)
-void launch_argmax(const float* z, int V, int32_t* out, cudaStream_t st);
 
 // State of a decode call kept in device memory, so that every step can
 // replay the same captured launches: the step's position and input token,
@@ -184,7 +182,6 @@ void launch_loss_reduce(const float* loss_row, int n, float inv_ntgt, float* out
 template <typename T>
 void launch_pack(const float* src, int64_t rows, int64_t cols, int mode, int hd, T* dst,
                  cudaStream_t st);
-void launch_f32_to_bf16(const float* src, int64_t n, bf16* dst, cudaStream_t st);
 // hi = rn(w), lo = rn(w - hi): a bf16 pair whose sum carries ~16 mantissa
 // bits (lo may be null: hi alone)
 void launch_split_bf16(const float* w, int64_t n, bf16* hi, bf16* lo, cudaStream_t st);
