@@ -162,7 +162,28 @@ def test_attn_fwd_3b_shape_sampled(impl):
     assert np.isfinite(o).all()
 
 
-@pytest.mark.parametrize("impl", [2, 3])
+@pytest.mark.parametrize("impl", [0, 3])
+def test_attn_fwd_long_span_sampled(impl):
+    """A 4096-row span of the 3B head layout one super-chunk into the
+    sequence (window 8192), the shape of the frozen blocks' pass: sixteen
+    tile pairs per head, 66 key blocks of 128 per pair, the ring wrapping
+    inside the span; sampled rows."""
+    torch, T = _env()
+    n, H, Hkv, hd, W = 4096, 24, 8, 128, 8192
+    R = 12288
+    pos0 = 16384 + 512
+    q, kr, vr = make_case(n, H, Hkv, hd, W, pos0, R, seed=17)
+    o, lse = run_fwd(T, torch, impl, q, kr, vr, n, H, Hkv, hd, W, pos0)
+    rows = [0, 63, 64, 255, 256, 2047, 3000, 4095]
+    ro, rl = ref_forward(q, kr, vr, n, H, Hkv, hd, W, pos0, rows=rows)
+    err_o = max(np.abs(o[r, h * hd:(h + 1) * hd] - v).max() for (r, h), v in ro.items())
+    err_l = max(abs(lse[h, r] - v) for (r, h), v in rl.items())
+    assert err_o < 2e-2, err_o
+    assert err_l < 2e-3, err_l
+    assert np.isfinite(o).all()
+
+
+@pytest.mark.parametrize("impl", [0, 2, 3])
 def test_attn_fwd_large_scores(impl):
     """Scores spread over a wide range exercise the lazy rescaling of the
     output accumulator (the running max grows by more than 2^8)."""
