@@ -131,6 +131,38 @@ int ttt_kernel_attn_bwd_noalloc(int32_t n, int32_t H, int32_t Hkv, int32_t hd, i
  * through; read the code with ttt_kernel_error(). */
 int ttt_kernel_wait_selftest(int64_t clocks, void* stream);
 
+/* Range checks of the debug build.  libttt_debug.so is this library compiled
+ * with TTT_DEBUG_BOUNDS (python -m long_context_lm_ttt_b300.build
+ * --debug-bounds).  It range-checks, before each access:
+ *   - every tile copy of the tensor-core attention kernels: the inner
+ *     coordinate on a 16-byte boundary and inside the tensor, a key/value
+ *     box inside one head's ring (query and gradient boxes may start past
+ *     the last row, where the copy reads zeros);
+ *   - the one-query attention's key/value slice copies, inside the ring and
+ *     the pass buffer;
+ *   - the decode step's row of the chunk buffers.
+ * A failed check records the first violation per source file and skips the
+ * access.  A skipped copy makes the kernel abort through its bounded waits;
+ * nothing traps.  The context calls (ttt_prefill, ttt_decode, ttt_logits)
+ * then return TTT_ERR_INTERNAL naming the kernel.  libttt.so compiles every
+ * check away.
+ *
+ * ttt_kernel_bounds_checked: 1 if this library carries the checks, else 0.
+ * ttt_kernel_bounds: synchronises the device, then reads and clears the
+ *   records of the current device.  Returns the number of failed checks
+ *   since the last call (0: none; always 0 without the checks) or a negative
+ *   TTT_ERR_* code.  When the count is positive, *kernel, *index and *limit
+ *   (each may be NULL) describe the first failure: the kernel id (1 decode
+ *   tail, 2 one-query attention, 3-6 the tensor-core attention forward,
+ *   two-tile forward, dq and dk/dv kernels, 7 the self-test), and the index
+ *   outside [0, limit).
+ * ttt_kernel_bounds_selftest: launches one thread that evaluates one check
+ *   on (index, limit) and touches no memory.  With the checks, an index
+ *   outside [0, limit) is recorded as kernel 7. */
+int ttt_kernel_bounds_checked(void);
+int ttt_kernel_bounds(int32_t* kernel, int64_t* index, int64_t* limit);
+int ttt_kernel_bounds_selftest(int64_t index, int64_t limit, void* stream);
+
 /* Error word of the tensor-core kernels launched through this header on the
  * current device since the last call, ttt_kernel_attn_bwd_noalloc included
  * (0 = none; otherwise the code of a bounded wait that gave up).  Reading

@@ -1,7 +1,12 @@
 """Build the CUDA library libttt.so in-tree with nvcc for sm_103a.
 
-    python -m long_context_lm_ttt_b300.build          # incremental
-    python -m long_context_lm_ttt_b300.build --clean  # from scratch
+    python -m long_context_lm_ttt_b300.build                 # incremental
+    python -m long_context_lm_ttt_b300.build --clean         # from scratch
+    python -m long_context_lm_ttt_b300.build --debug-bounds  # libttt_debug.so
+
+The debug library is the same sources compiled with TTT_DEBUG_BOUNDS: the
+range checks of csrc/bounds.cuh record a violation and skip the access
+instead of running it.  Setting TTT_LIBRARY=debug makes the binding load it.
 """
 from __future__ import annotations
 
@@ -18,6 +23,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libttt.so")
+BUILD_DEBUG = os.path.join(ROOT, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libttt_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -31,17 +38,18 @@ def _newer(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(clean: bool = False, verbose: bool = False, extra=None) -> str:
-    if clean and os.path.isdir(BUILD):
-        shutil.rmtree(BUILD)
-    os.makedirs(BUILD, exist_ok=True)
+def build(clean: bool = False, verbose: bool = False, extra=None, debug_bounds: bool = False) -> str:
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug_bounds else (BUILD, LIB)
+    if clean and os.path.isdir(build_dir):
+        shutil.rmtree(build_dir)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         glob.glob(os.path.join(ROOT, "include", "*.h"))
-    extra = list(extra or [])
+    extra = list(extra or []) + (["-DTTT_DEBUG_BOUNDS"] if debug_bounds else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         if not clean and not _newer(obj, [src] + headers):
             return obj, None
         cmd = [NVCC] + ARCH + FLAGS + extra + ["-c", src, "-o", obj]
@@ -60,12 +68,12 @@ def build(clean: bool = False, verbose: bool = False, extra=None) -> str:
     if errs:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errs))
     objs = [o for o, _ in results]
-    if _newer(LIB, objs):
-        cmd = [NVCC] + ARCH + ["-shared", "-o", LIB] + objs
+    if _newer(lib, objs):
+        cmd = [NVCC] + ARCH + ["-shared", "-o", lib] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stderr + r.stdout)
-    return LIB
+    return lib
 
 
 def main():
@@ -73,9 +81,11 @@ def main():
     ap.add_argument("--clean", action="store_true")
     ap.add_argument("-v", "--verbose", action="store_true")
     ap.add_argument("--ptxas-info", action="store_true", help="print register/smem usage")
+    ap.add_argument("--debug-bounds", action="store_true", help="build libttt_debug.so with the range checks")
     a = ap.parse_args()
     extra = ["-Xptxas", "-v"] if a.ptxas_info else []
-    print(build(clean=a.clean or a.ptxas_info, verbose=a.verbose or a.ptxas_info, extra=extra))
+    print(build(clean=a.clean or a.ptxas_info, verbose=a.verbose or a.ptxas_info, extra=extra,
+                debug_bounds=a.debug_bounds))
 
 
 if __name__ == "__main__":

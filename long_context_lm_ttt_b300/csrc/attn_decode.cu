@@ -36,11 +36,14 @@
 #include <atomic>
 #include <cmath>
 
+#include "bounds.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
 
 namespace ttt {
+
+TTT_BOUNDS_UNIT(attn_decode)
 
 namespace {
 
@@ -304,6 +307,15 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 2)
     const int slot = (int)(k0 % R);
     const int n1 = n < R - slot ? n : R - slot;
     const int64_t g0 = ((int64_t)kvh * R + slot) * hd;
+    // the debug build checks that both parts lie inside the head's ring and
+    // the pass buffer (the 16-byte rule of the copies holds by construction:
+    // rows of hd * 2 bytes, hd a multiple of 32, 16-byte aligned rings)
+    if (!(TTT_IN(KB_ATTN_DECODE, kvh, Hkv) && TTT_IN(KB_ATTN_DECODE, slot, R) &&
+          TTT_IN(KB_ATTN_DECODE, slot + n1 - 1, R) && TTT_IN(KB_ATTN_DECODE, n - 1, P) &&
+          TTT_IN(KB_ATTN_DECODE, n - n1, slot + 1))) {
+      *(volatile int*)&abort_flag = 1;
+      return;
+    }
     tc::bulk_load_1d(tc::smem_u32(sk + (int64_t)buf * P * hd), kring + g0, n1 * ROW, b);
     tc::bulk_load_1d(tc::smem_u32(sv + (int64_t)buf * P * hd), vring + g0, n1 * ROW, b);
     if (n > n1) {  // the ring wraps inside the pass

@@ -38,9 +38,13 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "bounds.cuh"
 #include "tc_common.cuh"
 
 namespace ttt {
+
+TTT_BOUNDS_UNIT(attn_tc)
+
 namespace {
 
 constexpr int BM = 128;   // query rows per tile
@@ -111,6 +115,26 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
                                           volatile int* abort) {
   const bool ok = tc::mbar_wait(bar, parity, err, code, abort);
   return __all_sync(0xffffffffu, ok);
+}
+
+// A 2-D tile copy of a box of 64 bf16 columns and box_rows rows at column x,
+// row y of a map of inner x outer elements.  The debug build checks that x
+// lies on a 16-byte boundary (an unaligned start raises an illegal-
+// instruction fault) and that the box starts inside the map's columns (its
+// columns may run past the inner extent: head dims below 128 read zeros
+// there).  Query and gradient boxes (ring = 0) may start past the last row:
+// a tile pair whose second tile has no rows loads zeros.  A key/value box
+// (ring > 0) must start inside the map and stay inside one head's ring of
+// `ring` rows.  A failed check skips the copy and raises the kernel's abort
+// flag, so every role leaves its bounded wait.
+__device__ __forceinline__ void tma_load_box(int kid, uint32_t dst, const CUtensorMap* map, int x, int y, int inner,
+                                             int outer, int box_rows, int ring, uint32_t bar, volatile int* abort) {
+  if (TTT_IN(kid, x & 7, 1) && TTT_IN(kid, x, inner) &&
+      (ring <= 0 || (TTT_IN(kid, y, outer) && TTT_IN(kid, y % ring + box_rows - 1, ring)))) {
+    tc::tma_load_2d(dst, map, x, y, bar);
+  } else {
+    *abort = 1;
+  }
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -228,7 +252,8 @@ __global__ void __launch_bounds__(192, 2)
       int issued = 0;
       tc::mbar_arrive_expect_tx(q_full, SM::Q_BYTES);
       for (int a = 0; a < NA; ++a)
-        tc::tma_load_2d(sbase + SM::Q_OFF + a * BM * 128, &mapQ, h * p.hd + 64 * a, r0, q_full);
+        tma_load_box(KB_ATTN_FWD_TC, sbase + SM::Q_OFF + a * BM * 128, &mapQ, h * p.hd + 64 * a, r0,
+                     p.H * p.hd, p.n, BM, 0, q_full, abort);
       for (int i = 0; i < nb && ok; ++i) {
         const int st = i & 1;
         if (!tc::mbar_wait(kv_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
@@ -239,12 +264,12 @@ __global__ void __launch_bounds__(192, 2)
         const int row = kvh * p.R + (int)(kpos % p.R);
         tc::mbar_arrive_expect_tx(k_full + 8 * st, SM::KV_BYTES);
         for (int a = 0; a < NA; ++a)
-          tc::tma_load_2d(sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN * 128, &mapK, 64 * a, row,
-                          k_full + 8 * st);
+          tma_load_box(KB_ATTN_FWD_TC, sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN * 128, &mapK, 64 * a, row,
+                       p.hd, p.Hkv * p.R, BN, p.R, k_full + 8 * st, abort);
         tc::mbar_arrive_expect_tx(v_full + 8 * st, SM::KV_BYTES);
         for (int a = 0; a < NA; ++a)
-          tc::tma_load_2d(sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN * 128, &mapV, 64 * a, row,
-                          v_full + 8 * st);
+          tma_load_box(KB_ATTN_FWD_TC, sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN * 128, &mapV, 64 * a, row,
+                       p.hd, p.Hkv * p.R, BN, p.R, v_full + 8 * st, abort);
         issued = i + 1;
       }
       // let copies in flight land before the CTA can exit
@@ -630,8 +655,8 @@ __global__ void __launch_bounds__(320, 1)
       tc::mbar_arrive_expect_tx(q_full, 2 * SM::Q_BYTES);
       for (int t = 0; t < 2; ++t)
         for (int a = 0; a < NA; ++a)
-          tc::tma_load_2d(sbase + SM::Q_OFF + t * SM::Q_BYTES + a * BM * 128, &mapQ, h * p.hd + 64 * a, r0 + BM * t,
-                          q_full);
+          tma_load_box(KB_ATTN_FWD2_TC, sbase + SM::Q_OFF + t * SM::Q_BYTES + a * BM * 128, &mapQ,
+                       h * p.hd + 64 * a, r0 + BM * t, p.H * p.hd, p.n, BM, 0, q_full, abort);
       for (int i = 0; i < nbl && ok; ++i) {
         const int st = i & 1;
         // K and V of a stage are released separately: K once both tiles'
@@ -645,16 +670,16 @@ __global__ void __launch_bounds__(320, 1)
         const int row = kvh * p.R + (int)(kpos % p.R);
         tc::mbar_arrive_expect_tx(k_full + 8 * st, SM::KV_BYTES);
         for (int a = 0; a < NA; ++a)
-          tc::tma_load_2d(sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN2 * 128, &mapK, 64 * a, row,
-                          k_full + 8 * st);
+          tma_load_box(KB_ATTN_FWD2_TC, sbase + SM::K_OFF + st * SM::KV_BYTES + a * BN2 * 128, &mapK, 64 * a, row,
+                       p.hd, p.Hkv * p.R, BN2, p.R, k_full + 8 * st, abort);
         if (!tc::mbar_wait(v_empty + 8 * st, ((i >> 1) & 1) ^ 1, p.err, ERR_A_PROD, abort)) {
           ok = false;
           break;
         }
         tc::mbar_arrive_expect_tx(v_full + 8 * st, SM::KV_BYTES);
         for (int a = 0; a < NA; ++a)
-          tc::tma_load_2d(sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN2 * 128, &mapV, 64 * a, row,
-                          v_full + 8 * st);
+          tma_load_box(KB_ATTN_FWD2_TC, sbase + SM::V_OFF + st * SM::KV_BYTES + a * BN2 * 128, &mapV, 64 * a, row,
+                       p.hd, p.Hkv * p.R, BN2, p.R, v_full + 8 * st, abort);
         issued = i + 1;
       }
       const long long t0 = clock64();
@@ -1047,8 +1072,10 @@ __global__ void __launch_bounds__(576, 1)
       int issued_k = 0, issued_v = 0;
       tc::mbar_arrive_expect_tx(q_full, 2 * SM::Q_BYTES);
       for (int a = 0; a < NA; ++a) {
-        tc::tma_load_2d(sbase + SM::Q_OFF + a * BM * 128, &mapQ, h * p.hd + 64 * a, r0, q_full);
-        tc::tma_load_2d(sbase + SM::DO_OFF + a * BM * 128, &mapDO, h * p.hd + 64 * a, r0, q_full);
+        tma_load_box(KB_ATTN_DQ_TC, sbase + SM::Q_OFF + a * BM * 128, &mapQ, h * p.hd + 64 * a, r0,
+                     p.H * p.hd, p.n, BM, 0, q_full, abort);
+        tma_load_box(KB_ATTN_DQ_TC, sbase + SM::DO_OFF + a * BM * 128, &mapDO, h * p.hd + 64 * a, r0,
+                     p.H * p.hd, p.n, BM, 0, q_full, abort);
       }
       for (int i = 0; i < nb && ok; ++i) {
         const long long kpos = (jb + i) * DQ_BN;
@@ -1060,8 +1087,8 @@ __global__ void __launch_bounds__(576, 1)
         }
         tc::mbar_arrive_expect_tx(k_full + 8 * ks, SM::KV_BYTES);
         for (int a = 0; a < NA; ++a)
-          tc::tma_load_2d(sbase + SM::K_OFF + ks * SM::KV_BYTES + a * DQ_BN * 128, &mapK, 64 * a, row,
-                          k_full + 8 * ks);
+          tma_load_box(KB_ATTN_DQ_TC, sbase + SM::K_OFF + ks * SM::KV_BYTES + a * DQ_BN * 128, &mapK, 64 * a, row,
+                       p.hd, p.Hkv * p.R, DQ_BN, p.R, k_full + 8 * ks, abort);
         issued_k = i + 1;
         if (!tc::mbar_wait(v_empty + 8 * vs, par(i, DQ_VST) ^ 1, p.err, ERR_A_PROD, abort)) {
           ok = false;
@@ -1069,8 +1096,8 @@ __global__ void __launch_bounds__(576, 1)
         }
         tc::mbar_arrive_expect_tx(v_full + 8 * vs, SM::KV_BYTES);
         for (int a = 0; a < NA; ++a)
-          tc::tma_load_2d(sbase + SM::V_OFF + vs * SM::KV_BYTES + a * DQ_BN * 128, &mapV, 64 * a, row,
-                          v_full + 8 * vs);
+          tma_load_box(KB_ATTN_DQ_TC, sbase + SM::V_OFF + vs * SM::KV_BYTES + a * DQ_BN * 128, &mapV, 64 * a, row,
+                       p.hd, p.Hkv * p.R, DQ_BN, p.R, v_full + 8 * vs, abort);
         issued_v = i + 1;
       }
       // the CTA must not exit with copies into its shared memory in flight
@@ -1371,8 +1398,10 @@ __global__ void __launch_bounds__(320, 1)
       for (int m = 0; m < 2; ++m) {
         const int row = kvh * p.R + (int)((p.pos0 + j0 + 64 * m) % p.R);
         for (int a = 0; a < NA; ++a) {
-          tc::tma_load_2d(sbase + SM::K_OFF + a * BM * 128 + m * 64 * 128, &mapK, 64 * a, row, kv_full);
-          tc::tma_load_2d(sbase + SM::V_OFF + a * BM * 128 + m * 64 * 128, &mapV, 64 * a, row, kv_full);
+          tma_load_box(KB_ATTN_DKV_TC, sbase + SM::K_OFF + a * BM * 128 + m * 64 * 128, &mapK, 64 * a, row,
+                       p.hd, p.Hkv * p.R, 64, p.R, kv_full, abort);
+          tma_load_box(KB_ATTN_DKV_TC, sbase + SM::V_OFF + a * BM * 128 + m * 64 * 128, &mapV, 64 * a, row,
+                       p.hd, p.Hkv * p.R, 64, p.R, kv_full, abort);
         }
       }
       for (int i = 0; i < nb && ok; ++i) {
@@ -1384,10 +1413,10 @@ __global__ void __launch_bounds__(320, 1)
         const int t0 = (qb0 + i) * BN;
         tc::mbar_arrive_expect_tx(q_full + 8 * st, 2 * SM::B_BYTES);
         for (int a = 0; a < NA; ++a) {
-          tc::tma_load_2d(sbase + SM::Q_OFF + st * SM::B_BYTES + a * BN * 128, &mapQ, h * p.hd + 64 * a, t0,
-                          q_full + 8 * st);
-          tc::tma_load_2d(sbase + SM::DO_OFF + st * SM::B_BYTES + a * BN * 128, &mapDO, h * p.hd + 64 * a, t0,
-                          q_full + 8 * st);
+          tma_load_box(KB_ATTN_DKV_TC, sbase + SM::Q_OFF + st * SM::B_BYTES + a * BN * 128, &mapQ,
+                       h * p.hd + 64 * a, t0, p.H * p.hd, p.n, BN, 0, q_full + 8 * st, abort);
+          tma_load_box(KB_ATTN_DKV_TC, sbase + SM::DO_OFF + st * SM::B_BYTES + a * BN * 128, &mapDO,
+                       h * p.hd + 64 * a, t0, p.H * p.hd, p.n, BN, 0, q_full + 8 * st, abort);
         }
         issued = i + 1;
       }

@@ -34,6 +34,7 @@
 #include <vector>
 
 #include "../../include/ttt.h"
+#include "bounds.cuh"
 #include "kernels.h"
 
 namespace ttt {
@@ -1064,6 +1065,18 @@ struct Engine : EngineBase {
     CU_TRY(cudaMemcpyAsync(h_err, dev_err, sizeof(h_err), cudaMemcpyDeviceToHost, st));
     CU_TRY(cudaStreamSynchronize(st));
     if (prof_on) prof_collect();
+    if (kBoundsChecked) {
+      // the debug build's range checks (every stream's work has joined st)
+      CU_TRY(cudaDeviceSynchronize());
+      BoundsRecord br;
+      CU_TRY((cudaError_t)bounds_fetch_all(&br));
+      if (br.count > 0) {
+        err = std::string(what) + ": range check failed in " + bounds_kernel_name(br.kernel) + " (index " +
+              std::to_string(br.index) + " outside [0, " + std::to_string(br.limit) + "), " +
+              std::to_string(br.count) + " failed checks)";
+        return TTT_ERR_INTERNAL;
+      }
+    }
     if (h_err[2] != 0) {
       err = std::string(what) + ": a device-side check failed (code " + std::to_string(h_err[2]) + ")";
       return TTT_ERR_INTERNAL;

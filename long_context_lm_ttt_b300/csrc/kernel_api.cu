@@ -4,6 +4,7 @@
 
 #include "../../include/ttt.h"
 #include "../../include/ttt_kernels.h"
+#include "bounds.cuh"
 #include "kernels.h"
 
 namespace ttt {
@@ -296,6 +297,34 @@ extern "C" int ttt_kernel_wait_selftest(int64_t clocks, void* stream) {
   if (int r = ensure_err()) return r;
   wait_selftest_kernel<<<1, 1, 0, (cudaStream_t)stream>>>((long long)clocks, g_err);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
+}
+
+namespace ttt {
+TTT_BOUNDS_UNIT(kernel_api)
+namespace {
+// evaluates one range check and touches no memory: the debug build records
+// (KB_SELFTEST, index, limit) when index lies outside [0, limit)
+__global__ void bounds_selftest_kernel(long long index, long long limit) {
+  if (!TTT_IN(KB_SELFTEST, index, limit)) return;
+}
+}  // namespace
+}  // namespace ttt
+
+extern "C" int ttt_kernel_bounds_checked(void) { return ttt::kBoundsChecked ? 1 : 0; }
+
+extern "C" int ttt_kernel_bounds_selftest(int64_t index, int64_t limit, void* stream) {
+  ttt::bounds_selftest_kernel<<<1, 1, 0, (cudaStream_t)stream>>>((long long)index, (long long)limit);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TTT_ERR_CUDA;
+}
+
+extern "C" int ttt_kernel_bounds(int32_t* kernel, int64_t* index, int64_t* limit) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return TTT_ERR_CUDA;
+  ttt::BoundsRecord r;
+  if (ttt::bounds_fetch_all(&r)) return TTT_ERR_CUDA;
+  if (kernel) *kernel = r.kernel;
+  if (index) *index = r.index;
+  if (limit) *limit = r.limit;
+  return r.count;
 }
 
 extern "C" int ttt_kernel_error(void) {

@@ -6,10 +6,13 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "bounds.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
 namespace ttt {
+
+TTT_BOUNDS_UNIT(kernels)
 
 namespace {
 
@@ -243,9 +246,13 @@ __global__ void decode_tail_kernel(DecodeState* s, const float* __restrict__ x, 
   pdl_wait();
   pdl_trigger();
   const int r = s->r;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) xdec[(int64_t)r * d + c] = x[c];
+  // the step's row of the chunk buffers (the debug build checks it; every
+  // thread takes the same branch)
+  const bool row_ok = TTT_IN(KB_DECODE_TAIL, r, b);
+  if (row_ok)
+    for (int c = threadIdx.x; c < d; c += blockDim.x) xdec[(int64_t)r * d + c] = x[c];
   __syncthreads();  // every thread has read r before it moves on
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && row_ok) {
     const int i = s->i, tok = s->tok;
     const int nxt = i + 1 < s->n_given ? s->given[i + 1] : argmax_col(*pick);
     *pick = 0ull;

@@ -16,7 +16,9 @@ from typing import Optional, Sequence
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libttt.so")
+# TTT_LIBRARY=debug selects libttt_debug.so, the same library built with the
+# range checks (python -m long_context_lm_ttt_b300.build --debug-bounds)
+LIB_PATH = os.path.join(_HERE, "libttt_debug.so" if os.environ.get("TTT_LIBRARY") == "debug" else "libttt.so")
 
 TTT_OK = 0
 TTT_ERR_INVALID = -1
@@ -113,6 +115,12 @@ def load(path: str = LIB_PATH):
     lib.ttt_kernel_wait_selftest.restype = c_int32
     lib.ttt_kernel_error.argtypes = []
     lib.ttt_kernel_error.restype = c_int32
+    lib.ttt_kernel_bounds_checked.argtypes = []
+    lib.ttt_kernel_bounds_checked.restype = c_int32
+    lib.ttt_kernel_bounds.argtypes = [POINTER(c_int32), POINTER(c_int64), POINTER(c_int64)]
+    lib.ttt_kernel_bounds.restype = c_int32
+    lib.ttt_kernel_bounds_selftest.argtypes = [c_int64, c_int64, c_void_p]
+    lib.ttt_kernel_bounds_selftest.restype = c_int32
     _lib = lib
     return lib
 
@@ -295,6 +303,20 @@ def ttt_kernel_gemm_grouped(groups, group_rows, N, K, A, lda, B, ldb, b_mn, grou
 
 def ttt_kernel_error() -> int:
     return int(load().ttt_kernel_error())
+
+
+def ttt_kernel_bounds_checked() -> bool:
+    return bool(load().ttt_kernel_bounds_checked())
+
+
+def ttt_kernel_bounds():
+    """(count, kernel id, index, limit) of the failed range checks since the
+    last call on the current device; count 0 means none."""
+    k, i, n = c_int32(0), c_int64(0), c_int64(0)
+    rc = int(load().ttt_kernel_bounds(ctypes.byref(k), ctypes.byref(i), ctypes.byref(n)))
+    if rc < 0:
+        raise RuntimeError(f"ttt_kernel_bounds: {ERR_NAMES.get(rc, rc)}")
+    return rc, int(k.value), int(i.value), int(n.value)
 
 
 # ---------------------------------------------------------------------------

@@ -122,3 +122,19 @@ def test_decode_attention_rejects_misaligned_rows(lib, offset):
         Hq = Hkv * 9 if offset == 0 else H
         rc = lib.ttt_kernel_attn_fwd(4, 1, Hq, Hkv, hd, W, R, 5, a[0], a[1], a[2], a[3], base + 0x4000, 1, None)
         assert rc == T.TTT_ERR_SHAPE, (i, offset, rc)
+
+
+def test_debug_library_exports_every_declared_call():
+    """libttt_debug.so, the same sources built with the range checks, exports
+    the same calls and says that it carries the checks (no device work);
+    libttt.so says that it does not."""
+    path = os.path.join(ROOT, "long_context_lm_ttt_b300", "libttt_debug.so")
+    if not os.path.exists(path):
+        from long_context_lm_ttt_b300 import build
+        build.build(debug_bounds=True)
+    dbg = ctypes.CDLL(path)
+    for name in _declared():
+        assert hasattr(dbg, name), name
+    dbg.ttt_kernel_bounds_checked.restype = ctypes.c_int32
+    assert dbg.ttt_kernel_bounds_checked() == 1
+    assert T.load().ttt_kernel_bounds_checked() == 0
