@@ -2,6 +2,7 @@
 points (include/ttt_kernels.h), for profiling one kernel in isolation.
 
     python -m long_context_lm_ttt_b300.microbench gemm --M 1024 --N 16384 --K 3072
+    python -m long_context_lm_ttt_b300.microbench gemm --M 1024 --N 16384 --K 3072 --dual 1   # + A B2^T
     python -m long_context_lm_ttt_b300.microbench gemm-sgd --M 3072 --N 8192 --K 1024
     python -m long_context_lm_ttt_b300.microbench attn-fwd --n 1024 --H 24 --Hkv 8 --hd 128 --W 8192
     python -m long_context_lm_ttt_b300.microbench attn-bwd --n 1024 --H 24 --Hkv 8 --hd 128 --W 8192
@@ -41,17 +42,21 @@ def gemm(args):
     M, N, K = args.M, args.N, args.K
     A = (torch.randn((K, M) if args.a_mn else (M, K), device="cuda", generator=g)).to(torch.bfloat16)
     B = (torch.randn((K, N) if args.b_mn else (N, K), device="cuda", generator=g)).to(torch.bfloat16)
+    # --dual: a second B of the same layout added into the same output (the
+    # forward's fast-weight products read the weights as a bf16 hi/lo pair)
+    B2 = (torch.randn(B.shape, device="cuda", generator=g)).to(torch.bfloat16) if args.dual else None
     C = torch.empty((M, N), device="cuda", dtype=torch.float32)
     lda = M if args.a_mn else K
     ldb = N if args.b_mn else K
 
     def run():
-        T.ttt_kernel_gemm(M, N, K, A, lda, args.a_mn, B, ldb, args.b_mn, None, C, N, args.impl)
+        T.ttt_kernel_gemm(M, N, K, A, lda, args.a_mn, B, ldb, args.b_mn, B2, C, N, args.impl)
 
     ms = _events(run, args.warmup, args.iters)
     assert T.ttt_kernel_error() == 0
-    return {"kernel": "gemm", "M": M, "N": N, "K": K, "a_mn": args.a_mn, "b_mn": args.b_mn, "ms": ms,
-            "tflops": 2.0 * M * N * K / (ms / 1e3) / 1e12}
+    mult = 2.0 if args.dual else 1.0
+    return {"kernel": "gemm", "M": M, "N": N, "K": K, "a_mn": args.a_mn, "b_mn": args.b_mn, "dual": args.dual,
+            "ms": ms, "tflops": mult * 2.0 * M * N * K / (ms / 1e3) / 1e12}
 
 
 def gemm_sgd(args):
@@ -133,6 +138,7 @@ def main():
     g.add_argument("--K", type=int, default=3072)
     g.add_argument("--a-mn", type=int, default=0)
     g.add_argument("--b-mn", type=int, default=0)
+    g.add_argument("--dual", type=int, default=0, help="1: add A B2^T, B2 a second B (counted in TFLOP/s)")
     gs = sub.add_parser("gemm-sgd")
     gs.add_argument("--M", type=int, default=3072)
     gs.add_argument("--N", type=int, default=8192)
