@@ -113,9 +113,10 @@ def test_attention_band_matches_sdpa_with_mask():
 # ---------------------------------------------------------------------------
 # whole forward against a restatement made of torch library routines
 # ---------------------------------------------------------------------------
-def _torch_forward_losses(s, w, tok, fast=None):
+def _torch_forward_logits(s, w, tok, fast=None):
     """Un-chunked SWA forward from library pieces (rms_norm, sdpa with a band
-    mask, silu, cross_entropy; RoPE as complex rotation).  fp64."""
+    mask, silu; RoPE as complex rotation).  fp64 logits [T, V].  ``fast``
+    maps a block index to weights that replace that block's own."""
     T = len(tok)
     H, Hkv, hd = s.n_heads, s.n_kv_heads, s.head_dim
     t = lambda a: torch.as_tensor(np.asarray(a), dtype=torch.float64)
@@ -152,8 +153,12 @@ def _torch_forward_losses(s, w, tok, fast=None):
             hn2 = F.rms_norm(x, (s.d_model,), lwt["mlp2_norm"], eps=s.norm_eps)
             x = x + F.linear(F.silu(F.linear(hn2, lwt["w_gate2"])) * F.linear(hn2, lwt["w_up2"]),
                              lwt["w_down2"])
-    z = F.linear(F.rms_norm(x, (s.d_model,), t(w["final_norm"]), eps=s.norm_eps),
-                 t(w["lm_head"]))
+    return F.linear(F.rms_norm(x, (s.d_model,), t(w["final_norm"]), eps=s.norm_eps), t(w["lm_head"]))
+
+
+def _torch_forward_losses(s, w, tok, fast=None):
+    """Per-position next-token losses of that forward (cross_entropy)."""
+    z = _torch_forward_logits(s, w, tok, fast)
     return F.cross_entropy(z[:-1], torch.as_tensor(tok[1:], dtype=torch.long), reduction="none")
 
 
@@ -163,6 +168,33 @@ def test_forward_matches_torch_library_restatement(name, dual):
     ours = O.full_forward_losses(cfg, w, tok)
     ref = _torch_forward_losses(s, w, tok).numpy()
     np.testing.assert_allclose(ours, ref, rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("lr", [0.0, None])
+def test_logits_after_prefill_match_torch_forward(lr):
+    """logits_after (what ttt_logits returns): the logits of a continuation
+    after reading a context.  With one fast block, the last, the cached keys
+    and values of earlier positions do not depend on the fast weights (each
+    block's MLP follows its attention, and no fast block lies below another
+    block), so the continuation's logits equal one plain forward over context
+    and continuation with the final fast weights (the initial ones at lr = 0).
+    The call leaves the state as it was."""
+    s, cfg, w, tok = _setup("tiny")
+    assert s.n_ttt_layers == 1
+    P, n = 3 * s.chunk + 5, 9  # a ragged context, then n more tokens
+    cont = tok[P:P + n]
+    r = O.prefill(cfg, w, tok[:P], lr=lr, return_state=True)
+    st = r["state"]
+    pos0 = st.pos
+    z = O.logits_after(st, cont)
+    assert st.pos == pos0
+    np.testing.assert_array_equal(O.logits_after(st, cont), z)
+    L = s.n_layers
+    fast = {L - 1: {k: torch.as_tensor(np.asarray(v), dtype=torch.float64) for k, v in r["fast"][-1].items()}}
+    if lr is None:  # the context did move the fast weights
+        assert max(np.abs(r["fast"][-1][k] - w["layers"][L - 1][k]).max() for k in O.FAST) > 0
+    ref = _torch_forward_logits(s, w, np.concatenate([tok[:P], cont]), fast=fast)[P:P + n].numpy()
+    np.testing.assert_allclose(z, ref, rtol=0, atol=1e-10 * np.abs(ref).max())
 
 
 @pytest.mark.parametrize("name,dual", [("tiny", False), ("tiny-ttt2", False), ("tiny-gqa", False),

@@ -98,3 +98,35 @@ def test_skipped_static_mlp_backward_is_caught(monkeypatch):
 
     monkeypatch.setattr(O, "backward_chunk", bad_backward)
     assert P.fd_check("tiny-ttt2", 0, dual_mlp=True) > 1e-3
+
+
+def test_logits_after_at_a_shifted_position_is_caught(monkeypatch):
+    """The continuation rotated as if it started one position early."""
+    def bad_logits_after(st, cont):
+        z, _ = O.forward_span(st, np.asarray(cont), st.pos - 1, write_cache=False)
+        return z
+
+    monkeypatch.setattr(O, "logits_after", bad_logits_after)
+    assert _fails(P.test_logits_after_prefill_match_torch_forward, 0.0)
+    assert _fails(P.test_logits_after_prefill_match_torch_forward, None)
+
+
+def test_logits_after_with_the_initial_weights_is_caught(monkeypatch):
+    """The continuation scored by the fast weights before the context's
+    updates (those of the pin's configuration, tiny)."""
+    from long_context_lm_ttt_b300 import inputs
+    w0 = inputs.make_weights(inputs.shape("tiny"))
+
+    def bad_logits_after(st, cont):
+        L = st.cfg.n_layers
+        saved = {k: st.layers[L - 1][k] for k in O.FAST}
+        try:
+            for k in O.FAST:
+                st.layers[L - 1][k] = np.asarray(w0["layers"][L - 1][k], st.dtype)
+            z, _ = O.forward_span(st, np.asarray(cont), st.pos, write_cache=False)
+        finally:
+            st.layers[L - 1].update(saved)
+        return z
+
+    monkeypatch.setattr(O, "logits_after", bad_logits_after)
+    assert _fails(P.test_logits_after_prefill_match_torch_forward, None)
